@@ -1,0 +1,591 @@
+#!/usr/bin/env python3
+"""Benchmark of the KV-cache flush path on GB300.
+
+One step = one pass of the whole path over one batch of synthetic KV data:
+TurboQuantRVQ encode+pack, KIVI quant+pack of K and V, then unpack+dequant of
+all three.  Metric: HBM GB/s of algorithmic bytes (fp16 in + packed / norms /
+scales out, and the reverse for the dequant kernels) per second, with the
+fraction of the measured GB300 copy bandwidth, plus Gelem/s.
+
+Default workload (N = 1): K and V [4, 32, 32768, 128] fp16 (long-context
+stress), RVQ b = 2 on K, KIVI 2-bit G = 64 with a 128-token residual window on
+K and V.  Inputs are 2 GiB, larger than L2 (129 MB), so no L2 flush is needed
+between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload c5|c3|c2|c1|c4]
+
+--impl reference times the CPU oracle (single-threaded binary64 C) on a
+bounded sample of the same workload per step.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+D = 128
+METRIC = "fused KV quantize+pack HBM GB/s (% of GB300 peak) and Gelem/s, 1 GPU"
+UNIT = "GB/s"
+NOMINAL_HBM_GBS = 8000.0
+
+
+def measured_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# --------------------------------------------------------------------------- workloads
+
+
+class Op:
+    def __init__(self, name, kernel, run, nbytes, nelem, launches=1):
+        self.name, self.kernel, self.run = name, kernel, run
+        self.nbytes, self.nelem, self.launches = nbytes, nelem, launches
+
+
+def rvq_bytes(rows, bits):
+    return rows * (2 * D + 2 * (D * bits // 8) + 4)
+
+
+def kivi_bytes(bh, s_q, bits, G, per_channel):
+    n = bh * s_q * D
+    ng = (s_q + G - 1) // G if per_channel else s_q
+    groups = bh * ng * (D if per_channel else D // G)
+    words = bh * ng * G * bits // 32 * D if per_channel else bh * s_q * D * bits // 32
+    return n * 2 + words * 4 + groups * 4
+
+
+def describe(name):
+    return {
+        "c5": "long-context K,V [4,32,32768,128] fp16 (4x40 outlier channels per head): RVQ b=2 "
+              "encode+pack on K; KIVI 2-bit G=64 residual 128 on K and V; unpack+dequant of all",
+        "c3": "RVQ b=4 encode+pack over 32 layers of keys [1,32,8192,128] fp16 (4x20 outliers), "
+              "then unpack+dequant",
+        "c2": "KIVI 2-bit flush on K,V [1,32,4096,128] G=32 residual 128, then unpack+dequant",
+        "c1": "RVQ b=2 encode+pack of keys [1,8,512,128], then unpack+dequant",
+        "c4": "decode flush: 64 seqs x 8 heads x 128 new tokens into caches of random lengths; "
+              "RVQ b=2 and KIVI 2-bit G=32 (K,V), then unpack+dequant",
+    }[name]
+
+
+def build_workload(name, dev, rank=0):
+    """Device buffers and the op list for one step; also host inputs for e2e."""
+    import torch
+    from kv_cache_quantization_turboquantrvq_gb300 import api, synth
+
+    ops, inputs, results = [], [], []
+    stream = torch.cuda.current_stream()
+
+    def t(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    def rvq_ops(tag, k_dev, bits, dst_off=None, S_dst=None):
+        B, H, S, _ = k_dev.shape
+        S_dst = S if S_dst is None else S_dst
+        cb = [np.ascontiguousarray(a) for a in api.vq_rvq_codebook(D, bits)]
+        W = D * bits // 32
+        p1 = torch.empty((B, H, S_dst, W), dtype=torch.int32, device=dev)
+        p2 = torch.empty_like(p1)
+        nr = torch.empty((B, H, S_dst), dtype=torch.float32, device=dev)
+        out = torch.empty((B, H, S, D), dtype=torch.float16, device=dev)
+        rows = B * H * S
+
+        def enc():
+            api.vq_rvq_encode_pack(k_dev, bits, *cb, packed1=p1, packed2=p2, norms=nr,
+                                   dst_off=dst_off, S_dst=S_dst, stream=stream)
+
+        if dst_off is None:
+            def dec():
+                api.vq_rvq_unpack_dequant(p1, p2, nr, bits, cb[0], cb[2], out=out, stream=stream)
+        else:
+            dec = None
+        ops.append(Op(tag + "rvq_encode", "rvq_encode_kernel", enc, rvq_bytes(rows, bits), rows * D))
+        if dec is not None:
+            ops.append(Op(tag + "rvq_decode", "rvq_decode_kernel", dec, rvq_bytes(rows, bits), rows * D))
+        results.extend([p1, p2, nr])
+
+    def kivi_ops(tag, k_dev, v_dev, bits, G, R, dst_off=None, S_dst=None):
+        B, H, S, _ = k_dev.shape
+        S_q = S - R
+        S_dst = S_q if S_dst is None else S_dst
+        shp = api.kivi_shapes(B, H, S_dst, D, bits, G)
+        outs = {
+            "k_packed": torch.empty(shp["k_packed"], dtype=torch.int32, device=dev),
+            "k_scale": torch.empty(shp["k_scale"], dtype=torch.float16, device=dev),
+            "k_zero": torch.empty(shp["k_scale"], dtype=torch.float16, device=dev),
+            "v_packed": torch.empty(shp["v_packed"], dtype=torch.int32, device=dev),
+            "v_scale": torch.empty(shp["v_scale"], dtype=torch.float16, device=dev),
+            "v_zero": torch.empty(shp["v_scale"], dtype=torch.float16, device=dev),
+        }
+        ko = torch.empty((B, H, S_q, D), dtype=torch.float16, device=dev)
+        vo = torch.empty_like(ko)
+        kb = kivi_bytes(B * H, S_q, bits, G, True)
+        vb = kivi_bytes(B * H, S_q, bits, G, False)
+        ops.append(Op(tag + "kivi_quant_k", "kivi_keys_kernel", lambda: api.vq_kivi_quant_pack(
+            k_dev, None, bits, G, R, outs=outs, dst_off=dst_off, S_dst=S_dst, stream=stream), kb, B * H * S_q * D))
+        ops.append(Op(tag + "kivi_quant_v", "kivi_values_kernel", lambda: api.vq_kivi_quant_pack(
+            None, v_dev, bits, G, R, outs=outs, dst_off=dst_off, S_dst=S_dst, stream=stream), vb, B * H * S_q * D))
+        if dst_off is None:
+            ops.append(Op(tag + "kivi_dequant_k", "kivi_keys_dequant_kernel", lambda: api.vq_kivi_unpack_dequant(
+                outs, B, H, S_q, bits, G, k_out=ko, want_v=False, stream=stream), kb, B * H * S_q * D))
+            ops.append(Op(tag + "kivi_dequant_v", "kivi_values_dequant_kernel", lambda: api.vq_kivi_unpack_dequant(
+                outs, B, H, S_q, bits, G, v_out=vo, want_k=False, stream=stream), vb, B * H * S_q * D))
+        results.extend(outs.values())
+
+    cfgs = synth.CONFIGS
+    if name == "c5":
+        cfg = cfgs["c5_long_32k"]
+        k_np, v_np = synth.keys_for(cfg), synth.values_for(cfg)
+        k, v = t(k_np), t(v_np)
+        inputs = [(k_np, k), (v_np, v)]
+        rvq_ops("", k, cfg["rvq_bits"])
+        kivi_ops("", k, v, cfg["kivi_bits"], cfg["group"], cfg["residual"])
+        # order the step as the path runs: encode everything, then decode everything
+        order = ["rvq_encode", "kivi_quant_k", "kivi_quant_v", "rvq_decode", "kivi_dequant_k", "kivi_dequant_v"]
+        ops.sort(key=lambda o: order.index(o.name))
+    elif name == "c3":
+        cfg = cfgs["c3_rvq_b4_32L_8k"]
+        for layer in range(cfg["layers"]):
+            k_np = synth.keys_for(cfg, layer=layer)
+            k = t(k_np)
+            inputs.append((k_np, k))
+            rvq_ops("L%02d_" % layer, k, cfg["bits"])
+        ops.sort(key=lambda o: (o.kernel != "rvq_encode_kernel", o.name))
+    elif name == "c2":
+        cfg = cfgs["c2_kivi_b2_32x4096"]
+        k_np, v_np = synth.keys_for(cfg), synth.values_for(cfg)
+        k, v = t(k_np), t(v_np)
+        inputs = [(k_np, k), (v_np, v)]
+        kivi_ops("", k, v, cfg["bits"], cfg["group"], cfg["residual"])
+    elif name == "c1":
+        cfg = cfgs["c1_rvq_b2_8x512"]
+        k_np = synth.keys_for(cfg)
+        k = t(k_np)
+        inputs = [(k_np, k)]
+        rvq_ops("", k, cfg["bits"])
+    elif name == "c4":
+        cfg = cfgs["c4_decode_flush_64x8x128"]
+        k_np, v_np = synth.keys_for(cfg), synth.values_for(cfg)
+        k, v = t(k_np), t(v_np)
+        off = t(synth.cache_lengths(cfg["B"], cfg["seed"]))
+        inputs = [(k_np, k), (v_np, v)]
+        rvq_ops("", k, 2, dst_off=off, S_dst=cfg["s_dst"])
+        kivi_ops("", k, v, 2, cfg["group"], 0, dst_off=off, S_dst=cfg["s_dst"])
+    else:
+        raise ValueError(name)
+    return ops, inputs, results
+
+
+# --------------------------------------------------------------------------- clocks
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "50", "-i", str(gpu_index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.06)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        sm, mx, reasons = [], [], set()
+        for line in out.splitlines():
+            p = [x.strip() for x in line.split(",")]
+            if len(p) < 9:
+                continue
+            try:
+                sm.append(float(p[1]))
+                mx.append(float(p[2]))
+            except ValueError:
+                continue
+            for name, val in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                                  "sw_power_cap"), p[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- oracle timing
+
+
+def oracle_sample_rates(name, target_s=2.0):
+    """Time the CPU oracle on bounded samples of each op of the workload.
+    Returns ({op: bytes/s}, description)."""
+    import oracle
+    from kv_cache_quantization_turboquantrvq_gb300 import synth
+
+    rates, desc = {}, []
+    cfgs = synth.CONFIGS
+
+    def timed(fn, nbytes_per_unit, units0, max_units=1 << 22):
+        units = min(units0, max_units)
+        while True:
+            t0 = time.perf_counter()
+            fn(units)
+            dt = time.perf_counter() - t0
+            if dt >= target_s or units >= max_units:
+                return units * nbytes_per_unit / dt, units, dt
+            units = min(max_units, int(units * max(2.0, 1.2 * target_s / max(dt, 1e-4))))
+
+    def rvq_rates(bits, x_rows):
+        c1, b1, c2, b2, _ = oracle.rvq_codebooks(D, bits)
+        o = oracle.rvq_encode(x_rows[:1], bits, c1, b1, c2, b2)
+
+        def enc(n):
+            oracle.rvq_encode(x_rows[:n], bits, c1, b1, c2, b2)
+
+        def dec(n):
+            reps = np.repeat(o["packed1"], n, 0), np.repeat(o["packed2"], n, 0), np.repeat(o["norms"], n)
+            oracle.rvq_decode(*reps, D, bits, c1, c2)
+        r1, n1, _ = timed(enc, rvq_bytes(1, bits), 64, len(x_rows))
+        r2, n2, _ = timed(dec, rvq_bytes(1, bits), 64)
+        return r1, r2, n1, n2
+
+    def kivi_rates(bits, G, x):
+        def kq(n):
+            oracle.kivi_quant(x[:, :, :G * n], bits, G, 0, True)
+
+        def vq_(n):
+            oracle.kivi_quant(x[:, :, :n], bits, G, 0, False)
+        rk, nk, _ = timed(kq, kivi_bytes(1, G, bits, G, True), 1, x.shape[2] // G)
+        rv, nv, _ = timed(vq_, kivi_bytes(1, 1, bits, G, False), 64, x.shape[2])
+        ok = oracle.kivi_quant(x[:, :, :G], bits, G, 0, True)
+        ov = oracle.kivi_quant(x[:, :, :G], bits, G, 0, False)
+
+        def kd(n):
+            oracle.kivi_dequant(np.repeat(ok["packed"], n, 1), np.repeat(ok["scale"], n, 1),
+                                np.repeat(ok["zero"], n, 1), 1, G * n, D, bits, G, True)
+
+        def vd(n):
+            m = max(1, n // G)
+            oracle.kivi_dequant(np.repeat(ov["packed"], m, 1), np.repeat(ov["scale"], m, 1),
+                                np.repeat(ov["zero"], m, 1), 1, G * m, D, bits, G, False)
+        rkd, _, _ = timed(kd, kivi_bytes(1, G, bits, G, True), 1)
+        rvd, _, _ = timed(vd, kivi_bytes(1, 1, bits, G, False), 64)
+        return rk, rv, rkd, rvd, nk, nv
+
+    if name in ("c5", "c1", "c3", "c4"):
+        bits = {"c5": 2, "c1": 2, "c3": 4, "c4": 2}[name]
+        cfg = {"c5": cfgs["c5_long_32k"], "c1": cfgs["c1_rvq_b2_8x512"],
+               "c3": cfgs["c3_rvq_b4_32L_8k"], "c4": cfgs["c4_decode_flush_64x8x128"]}[name]
+        x = synth.kv_tensor(1, 1, 1 << 16, D, cfg["seed"], *cfg.get("k_outliers", (0, 1.0))).reshape(-1, D)
+        r1, r2, n1, n2 = rvq_rates(bits, x)
+        rates["rvq_encode"], rates["rvq_decode"] = r1, r2
+        desc.append("RVQ b=%d encode %d rows, decode %d rows" % (bits, n1, n2))
+    if name in ("c5", "c2", "c4"):
+        cfg = {"c5": cfgs["c5_long_32k"], "c2": cfgs["c2_kivi_b2_32x4096"],
+               "c4": cfgs["c4_decode_flush_64x8x128"]}[name]
+        G = cfg["group"]
+        x = synth.kv_tensor(1, 1, 1 << 16, D, cfg["seed"], 4, 20.0)
+        rk, rv, rkd, rvd, nk, nv = kivi_rates(2, G, x)
+        rates.update(kivi_quant_k=rk, kivi_quant_v=rv, kivi_dequant_k=rkd, kivi_dequant_v=rvd)
+        desc.append("KIVI 2-bit G=%d: %d key groups, %d value rows (and their dequant)" % (G, nk * D, nv))
+    return rates, "; ".join(desc) + " (about %.0f s of CPU per op)" % target_s
+
+
+def step_rate_from_ops(ops, rates):
+    """Whole-step bytes/s if each op ran at its sampled rate."""
+    t = 0.0
+    for o in ops:
+        base = o.name.split("_", 1)[1] if o.name.startswith("L") else o.name
+        t += o.nbytes / rates[base]
+    return sum(o.nbytes for o in ops) / t
+
+
+# --------------------------------------------------------------------------- traffic record
+
+
+def recorded_traffic(kernel):
+    """dram bytes per unit from the committed ncu summary, if the kernel source
+    is unchanged since the counters were taken."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            rec = json.load(f).get(kernel)
+    except Exception:
+        return None
+    if not rec:
+        return None
+    src = os.path.join(ROOT, "kv_cache_quantization_turboquantrvq_gb300", "csrc", rec["source"])
+    try:
+        h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    except Exception:
+        return None
+    if h != rec.get("source_sha256_16"):
+        return None
+    return rec
+
+
+# --------------------------------------------------------------------------- main
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", choices=("c5", "c3", "c2", "c1", "c4"), default="c5")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        return run_reference(args, world)
+
+    import torch
+    import torch.distributed as dist
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    from kv_cache_quantization_turboquantrvq_gb300 import api, build
+    build.build()
+    api.lib()  # fails loudly if the CUDA library is missing
+
+    ops, inputs, results = build_workload(args.workload, dev, rank)
+    stream = torch.cuda.current_stream()
+    K, W = args.steps, max(args.warmup, 3)
+
+    def step(evs=None):
+        for i, o in enumerate(ops):
+            if evs is not None:
+                evs[i].record(stream)
+            o.run()
+        if evs is not None:
+            evs[len(ops)].record(stream)
+
+    for _ in range(W):
+        step()
+    torch.cuda.synchronize()
+    assert api.vq_device_error() == 0
+    if world > 1:
+        dist.barrier()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(ops) + 1)] for _ in range(K)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local_rank)
+    time.sleep(0.1)
+    torch.cuda.synchronize()
+    t_start.record(stream)
+    for k in range(K):
+        step(evs[k])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if world > 1:
+        dist.barrier()
+    elapsed_ms = t_start.elapsed_time(t_end)
+    if world > 1:
+        tt = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(tt.item())
+    step_bytes = sum(o.nbytes for o in ops)
+    step_elems = sum(o.nelem for o in ops)
+    value = world * step_bytes * K / (elapsed_ms * 1e-3) / 1e9
+    gelem = world * step_elems * K / (elapsed_ms * 1e-3) / 1e9
+
+    # per-op average durations (events on the launching stream)
+    per_ms = {}
+    for i, o in enumerate(ops):
+        per_ms[o.name] = statistics.mean(evs[k][i].elapsed_time(evs[k][i + 1]) for k in range(K))
+    by_kernel = {}
+    for o in ops:
+        d = by_kernel.setdefault(o.kernel, {"ms": 0.0, "bytes": 0, "launches": 0})
+        d["ms"] += per_ms[o.name]
+        d["bytes"] += o.nbytes
+        d["launches"] += o.launches
+    peak, peak_src = measured_peak()
+    dom = max(by_kernel, key=lambda n: by_kernel[n]["ms"])
+    dk = by_kernel[dom]
+    avg_launch_ms = dk["ms"] / dk["launches"]
+    ach = dk["bytes"] / dk["launches"] / (avg_launch_ms * 1e-3) / 1e9
+    rec = recorded_traffic(dom)
+    traffic = None
+    if rec is not None:
+        traffic = rec["dram_bytes_per_unit"] * dk["bytes"] / dk["launches"] / rec["alg_bytes_per_unit"]
+
+    # end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        pinned_in = [torch.from_numpy(np.ascontiguousarray(h)).pin_memory() for h, _ in inputs]
+        pinned_out = [torch.empty(r.shape, dtype=r.dtype, pin_memory=True) for r in results]
+        h2d = sum(p.numel() * p.element_size() for p in pinned_in)
+        d2h = sum(p.numel() * p.element_size() for p in pinned_out)
+        Ke = max(3, min(K, 20))
+        for _ in range(2):
+            for p, (_, dv) in zip(pinned_in, inputs):
+                dv.copy_(p, non_blocking=True)
+            step()
+            for p, r in zip(pinned_out, results):
+                p.copy_(r, non_blocking=True)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(Ke):
+            for p, (_, dv) in zip(pinned_in, inputs):
+                dv.copy_(p, non_blocking=True)
+            step()
+            for p, r in zip(pinned_out, results):
+                p.copy_(r, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ems = e0.elapsed_time(e1)
+        if world > 1:
+            tt = torch.tensor([ems], device=dev)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            ems = float(tt.item())
+        e2e = {"value": round(world * step_bytes * Ke / (ems * 1e-3) / 1e9, 2), "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": round(ems / Ke, 4)}
+    assert api.vq_device_error() == 0
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        rates, desc = oracle_sample_rates(args.workload)
+        cpu = {"value": round(step_rate_from_ops(ops, rates) / 1e9, 6), "unit": UNIT, "cores": 1,
+               "kind": "oracle", "sample": desc}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+            "steps": K, "warmup": W, "ms_per_step": round(elapsed_ms / K, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded N(0,1) fp16 with per-head outlier channels)",
+            "config": {"workload": args.workload + ": " + describe(args.workload),
+                       "parallelism": "replicas (independent shards per GPU)" if world > 1 else "single GPU",
+                       "l2": "inputs larger than L2 (129 MB); no flush" if args.workload in ("c5", "c3", "c2")
+                             else "inputs smaller than L2; rotating not applied",
+                       "bytes_per_step": step_bytes, "elements_per_step": step_elems},
+            "pct_of_peak": round(100 * value / world / peak, 2),
+            "pct_of_nominal_8tbs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
+            "gelem_per_s": round(gelem, 3),
+            "per_kernel": {n: {"ms_per_launch": round(d["ms"] / d["launches"], 5),
+                               "GB_s": round(d["bytes"] / d["launches"] / (d["ms"] / d["launches"] * 1e-3) / 1e9, 1),
+                               "frac_of_peak": round(d["bytes"] / d["launches"] / (d["ms"] / d["launches"] * 1e-3) / 1e9 / peak, 4),
+                               "launches_per_step": d["launches"]} for n, d in by_kernel.items()},
+            "roofline": {"kernel": dom, "bound": "hbm", "achieved": round(ach, 1), "peak": peak,
+                         "peak_source": peak_src, "unit": "GB/s", "frac": round(ach / peak, 4),
+                         "traffic": None if traffic is None else int(traffic),
+                         "alg_bytes_per_launch": int(dk["bytes"] / dk["launches"])},
+            "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
+            "gpu_launches": sum(o.launches for o in ops) * K,
+        }
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def run_reference(args, world):
+    """The CPU oracle timed on bounded samples of the workload, one per step."""
+    import oracle
+    oracle.build()
+    # op list without a GPU: sizes only
+    ops = reference_ops(args.workload)
+    W, K = max(args.warmup, 0), args.steps
+    vals, t_total = [], 0.0
+    # about two minutes in all, at most 1 s of CPU per step
+    per_step_target = min(1.0, 120.0 / max(W + K, 1))
+    for i in range(W + K):
+        t0 = time.perf_counter()
+        rates, desc = oracle_sample_rates(args.workload, target_s=per_step_target / 6)
+        dt = time.perf_counter() - t0
+        if i >= W:
+            vals.append(step_rate_from_ops(ops, rates) / 1e9)
+            t_total += dt
+    value = statistics.median(vals)
+    step_bytes = sum(o.nbytes for o in ops)
+    line = {
+        "metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": W, "ms_per_step": round(1e3 * step_bytes / (value * 1e9), 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) fp16 with per-head outlier channels)",
+        "config": {"workload": args.workload + ": " + describe(args.workload),
+                   "bytes_per_step": step_bytes},
+        "impl": "reference",
+        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": desc + "; wall %.1f s over %d steps" % (t_total, K)},
+        "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def reference_ops(name):
+    """Byte/element counts of the workload's ops (no device work)."""
+    from kv_cache_quantization_turboquantrvq_gb300 import synth
+    cfgs = synth.CONFIGS
+    ops = []
+    noop = lambda: None
+    if name == "c5":
+        c = cfgs["c5_long_32k"]
+        rows = c["B"] * c["H"] * c["S"]
+        bh, s_q = c["B"] * c["H"], c["S"] - c["residual"]
+        for n in ("rvq_encode", "rvq_decode"):
+            ops.append(Op(n, n, noop, rvq_bytes(rows, 2), rows * D))
+        for n, pc in (("kivi_quant_k", True), ("kivi_quant_v", False), ("kivi_dequant_k", True),
+                      ("kivi_dequant_v", False)):
+            ops.append(Op(n, n, noop, kivi_bytes(bh, s_q, 2, c["group"], pc), bh * s_q * D))
+    elif name in ("c3", "c1"):
+        c = cfgs["c3_rvq_b4_32L_8k"] if name == "c3" else cfgs["c1_rvq_b2_8x512"]
+        rows = c["B"] * c["H"] * c["S"] * c.get("layers", 1)
+        for n in ("rvq_encode", "rvq_decode"):
+            ops.append(Op(n, n, noop, rvq_bytes(rows, c["bits"]), rows * D))
+    elif name == "c2":
+        c = cfgs["c2_kivi_b2_32x4096"]
+        bh, s_q = c["B"] * c["H"], c["S"] - c["residual"]
+        for n, pc in (("kivi_quant_k", True), ("kivi_quant_v", False), ("kivi_dequant_k", True),
+                      ("kivi_dequant_v", False)):
+            ops.append(Op(n, n, noop, kivi_bytes(bh, s_q, 2, c["group"], pc), bh * s_q * D))
+    elif name == "c4":
+        c = cfgs["c4_decode_flush_64x8x128"]
+        rows = c["B"] * c["H"] * c["S"]
+        ops.append(Op("rvq_encode", "rvq_encode", noop, rvq_bytes(rows, 2), rows * D))
+        for n, pc in (("kivi_quant_k", True), ("kivi_quant_v", False)):
+            ops.append(Op(n, n, noop, kivi_bytes(c["B"] * c["H"], c["S"], 2, c["group"], pc), rows * D))
+    return ops
+
+
+if __name__ == "__main__":
+    sys.exit(main())

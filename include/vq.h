@@ -1,0 +1,180 @@
+/*
+ * vq.h - C ABI of the GB300 (sm_103a) KV-cache flush codecs.
+ *
+ * Two codecs compress fresh fp16 keys/values [B, H, S, D] into bit-packed
+ * resident storage and expand it back:
+ *
+ *   TurboQuantRVQ (VeloxQuant-MLX blog, tag "rvq", sections "The pipeline, as
+ *   it actually runs" and "What 'quantize' means here, precisely"): per key
+ *   row, L2-normalise (norm kept), rotate by the normalised Walsh-Hadamard
+ *   transform y = H u / sqrt(D), quantize y against a Gaussian scalar codebook
+ *   by boundary counting (i1 = #{k : y > b1_k}), take the residual
+ *   r = y - c1[i1], quantize r against a Laplacian-fit codebook
+ *   (i2 = #{k : r > b2_k}), and bit-pack both index streams.
+ *
+ *   KIVI (VeloxQuant-MLX blog, tag "kivi", first post "What we're actually
+ *   optimizing" and second post "What KIVI is"): asymmetric min/max group
+ *   quantization, zero = min, scale = (max - min)/(2^b - 1),
+ *   q = round_half_even((x - zero)/scale); keys per channel over groups of G
+ *   tokens, values per token over groups of G channels; the most recent
+ *   residual_length tokens stay fp16 and are not touched.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - All tensor pointers are DEVICE pointers unless stated otherwise; fp16
+ *    tensors are IEEE binary16 ("void*" in the signatures), row-major and
+ *    contiguous.  Codebook arrays are HOST pointers read during the call.
+ *  - The caller owns and allocates every buffer.  The library allocates no
+ *    memory, keeps no per-call state and never synchronizes the stream.
+ *  - Work is enqueued on `stream` (NULL = the legacy default stream).
+ *  - Arguments are validated on the host before anything is enqueued; a
+ *    non-VQ_OK status means nothing was enqueued, except VQ_ERR_CUDA, which
+ *    reports a failed launch (the CUDA error is left for the caller to read
+ *    with cudaGetLastError()).
+ *  - Conditions that depend on device-resident data (destination offsets)
+ *    are checked on the device; a violation skips the affected rows and sets
+ *    a library-owned device error word, read and cleared by vq_device_error().
+ *  - Inputs must be finite; non-finite inputs give unspecified codes but no
+ *    out-of-bounds access.
+ *  - Packing is LSB first: with E = 32/bits codes per uint32 word, code j of
+ *    a word sits at bit shift j*bits.  On a little-endian machine these words
+ *    have the same bytes as the byte packer of the tag "turboquant" page,
+ *    section "Kernel 1: Bit-Packing".
+ *  - Supported: D == 128, bits in {1, 2, 4}.
+ */
+#ifndef VQ_H
+#define VQ_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream (the same type as cudaStream_t / CUstream). */
+typedef struct CUstream_st *vq_stream_t;
+
+typedef enum {
+    VQ_OK = 0,
+    VQ_ERR_INVALID_ARG = 1,   /* null pointer, bad shape, unsorted codebook ... */
+    VQ_ERR_UNSUPPORTED = 2,   /* valid but not implemented (D != 128, bits 3) */
+    VQ_ERR_MISALIGNED = 3,    /* a tensor pointer is not 16-byte aligned */
+    VQ_ERR_ALIASING = 4,      /* an output overlaps an input or another output */
+    VQ_ERR_CUDA = 5,          /* a CUDA launch failed */
+    VQ_ERR_DEVICE = 6         /* vq_device_error() found a device-side error */
+} vq_status;
+
+/* Device error bits reported by vq_device_error(). */
+#define VQ_DEVERR_WAIT_TIMEOUT 0x1 /* a bounded wait on a copy gave up */
+#define VQ_DEVERR_BAD_OFFSET 0x2   /* a destination offset was out of range */
+
+/* Human-readable name of a status code (static string). */
+const char *vq_status_str(int status);
+
+/* Library version string (static). */
+const char *vq_version(void);
+
+/*
+ * vq_rvq_codebook - the two TurboQuantRVQ codebooks for head dimension D and
+ * `bits` bits per stage, computed on the host in binary64 and rounded to
+ * binary32 (VeloxQuant-MLX blog, tag "rvq", "The pipeline, as it actually
+ * runs": a Gaussian stage-1 codebook and a Laplacian-fit stage-2 codebook).
+ *   c1[2^bits], b1[2^bits - 1]: Lloyd-Max quantizer for N(0, 1/D);
+ *   c2[2^bits], b2[2^bits - 1]: Lloyd-Max quantizer for Laplace(0, beta),
+ *     beta = E|y - c1[i1(y)]| for y ~ N(0, 1/D) (maximum-likelihood Laplace
+ *     scale of the stage-1 residual).
+ * Boundaries are midpoints of adjacent centroids.  All four are HOST arrays
+ * owned by the caller.  Host only; no GPU needed.
+ */
+vq_status vq_rvq_codebook(int D, int bits, float *c1, float *b1, float *c2, float *b2);
+
+/*
+ * vq_rvq_encode_pack - fused TurboQuantRVQ encode + bit-pack of key rows.
+ *   k_f16    [B, H, S, D] fp16, device.
+ *   c1, c2   [2^bits] fp32 centroids, host, ascending.
+ *   b1, b2   [2^bits - 1] fp32 boundaries, host, strictly increasing, each
+ *            strictly between its two neighbouring centroids.
+ *   packed1, packed2  [B, H, S_dst, D*bits/32] uint32, device: the stage-1 and
+ *            stage-2 index streams; code of coordinate d in word d/E at shift
+ *            (d mod E)*bits.
+ *   norms    [B, H, S_dst] fp32, device: ||x||_2 of each row.
+ *   dst_off  NULL (then S_dst must equal S and rows land at token s) or a
+ *            device array [B] of int32 token offsets: row (b, h, s) is written
+ *            at token dst_off[b] + s of the destination, which has capacity
+ *            S_dst tokens; dst_off[b] + S > S_dst or dst_off[b] < 0 skips
+ *            batch b and sets VQ_DEVERR_BAD_OFFSET.
+ * A zero row gets norm 0 and the codes of y = 0.  Codes equal those of exact
+ * arithmetic; rows with a rotated value within a small guard band of a
+ * boundary are recomputed in extended precision on the device.
+ */
+vq_status vq_rvq_encode_pack(const void *k_f16, int B, int H, int S, int D, int bits,
+                             const float *c1, const float *b1, const float *c2, const float *b2,
+                             uint32_t *packed1, uint32_t *packed2, float *norms,
+                             const int32_t *dst_off, int S_dst, vq_stream_t stream);
+
+/*
+ * vq_rvq_unpack_dequant - TurboQuantRVQ unpack + dequant back to keys:
+ *   x_hat = n * H (c1[i1] + c2[i2]) / sqrt(D), rounded to fp16.
+ * (VeloxQuant-MLX blog, tag "turboquant", "Kernel 5: Fused RVQ Decode +
+ * Attend" decodes c1[i1] + c2[i2] in the rotated domain; this call also undoes
+ * the rotation, H / sqrt(D) being its own inverse, and re-applies the norm.)
+ *   packed1, packed2 [B, H, S, D*bits/32] uint32, norms [B, H, S] fp32, device.
+ *   c1, c2 [2^bits] fp32, host.   out_f16 [B, H, S, D] fp16, device.
+ */
+vq_status vq_rvq_unpack_dequant(const uint32_t *packed1, const uint32_t *packed2,
+                                const float *norms, int B, int H, int S, int D, int bits,
+                                const float *c1, const float *c2, void *out_f16,
+                                vq_stream_t stream);
+
+/*
+ * vq_kivi_quant_pack - KIVI flush of K and/or V (either may be NULL, with its
+ * outputs).  Quantizes tokens [0, S_q), S_q = S - residual_length; tokens
+ * [S_q, S) are the fp16 residual window and are not read or written.
+ *   k_f16, v_f16 [B, H, S, D] fp16, device.
+ *   group G: G divides D (values); G*bits is a multiple of 32.
+ * Key layout (per channel, groups of G tokens; NG = ceil(S_dst/G) groups per
+ * (b, h) in the destination):
+ *   k_packed [B, H, NG, G*bits/32, D] uint32: word w of group g, channel d
+ *     holds tokens g*G + w*E + j at shift j*bits (slots past S_q hold 0);
+ *   k_scale, k_zero [B, H, NG, D] fp16.
+ * Value layout (per token, groups of G channels):
+ *   v_packed [B, H, S_dst, D*bits/32] uint32 (LSB-first along D);
+ *   v_scale, v_zero [B, H, S_dst, D/G] fp16.
+ * scale = fp16(fp32((max - min)/(2^bits - 1))), zero = min; a constant group
+ * stores q = 0 and scale = 0.  Codes use exact arithmetic
+ * (t = (x - min)(2^bits - 1)/(max - min), ties to even).
+ * dst_off: NULL (S_dst == S_q, token s -> s) or device int32 [B]: token s of
+ * batch b lands at dst_off[b] + s; dst_off[b] must be a multiple of G and
+ * dst_off[b] + S_q <= S_dst, else batch b is skipped and
+ * VQ_DEVERR_BAD_OFFSET is set.  A ragged last key group (S_q mod G != 0) is
+ * only supported when it ends the destination sequence.
+ */
+vq_status vq_kivi_quant_pack(const void *k_f16, const void *v_f16, int B, int H, int S, int D,
+                             int bits, int group, int residual_length,
+                             uint32_t *k_packed, void *k_scale, void *k_zero,
+                             uint32_t *v_packed, void *v_scale, void *v_zero,
+                             const int32_t *dst_off, int S_dst, vq_stream_t stream);
+
+/*
+ * vq_kivi_unpack_dequant - KIVI unpack + dequant of S_q stored tokens:
+ *   x_hat = fp16(q * scale + zero), evaluated exactly and rounded once.
+ * Layouts as written by vq_kivi_quant_pack with S_dst = S_q (NG = ceil(S_q/G)).
+ * Either side may be NULL.  k_out, v_out [B, H, S_q, D] fp16, device.
+ */
+vq_status vq_kivi_unpack_dequant(const uint32_t *k_packed, const void *k_scale, const void *k_zero,
+                                 const uint32_t *v_packed, const void *v_scale, const void *v_zero,
+                                 int B, int H, int S_q, int D, int bits, int group,
+                                 void *k_out_f16, void *v_out_f16, vq_stream_t stream);
+
+/*
+ * vq_device_error - waits for `stream`, then reads and clears the library's
+ * device error word (VQ_DEVERR_* bits) into *code_out (host pointer).
+ * Returns VQ_ERR_DEVICE if the word was non-zero, VQ_OK otherwise.
+ */
+vq_status vq_device_error(vq_stream_t stream, int *code_out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VQ_H */

@@ -1,0 +1,213 @@
+"""Python binding of the C ABI in include/vq.h (ctypes; argument marshalling only).
+
+Every function here has the name of the C entry point it calls.  Tensors are
+torch CUDA tensors (torch supplies device memory and the current stream);
+codebooks are small host float32 arrays.  All arithmetic runs in the CUDA
+library ``libvqflush.so``; if it is missing this module raises on first use,
+there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libvqflush.so")
+_lib = None
+
+VQ_OK = 0
+VQ_ERR_INVALID_ARG = 1
+VQ_ERR_UNSUPPORTED = 2
+VQ_ERR_MISALIGNED = 3
+VQ_ERR_ALIASING = 4
+VQ_ERR_CUDA = 5
+VQ_ERR_DEVICE = 6
+VQ_DEVERR_WAIT_TIMEOUT = 0x1
+VQ_DEVERR_BAD_OFFSET = 0x2
+
+EXPORTED = ("vq_status_str", "vq_version", "vq_rvq_codebook", "vq_rvq_encode_pack",
+            "vq_rvq_unpack_dequant", "vq_kivi_quant_pack", "vq_kivi_unpack_dequant",
+            "vq_device_error")
+
+
+class VQError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__("%s: %s" % (what, lib().vq_status_str(status).decode()))
+        self.status = status
+
+
+def lib():
+    """Load libvqflush.so (raises OSError when it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise OSError("libvqflush.so is not built (run __graft_entry__.build()): %s" % LIB_PATH)
+    L = ctypes.CDLL(LIB_PATH)
+    P, I = ctypes.c_void_p, ctypes.c_int
+    L.vq_status_str.argtypes = [I]
+    L.vq_status_str.restype = ctypes.c_char_p
+    L.vq_version.argtypes = []
+    L.vq_version.restype = ctypes.c_char_p
+    L.vq_rvq_codebook.argtypes = [I, I, P, P, P, P]
+    L.vq_rvq_encode_pack.argtypes = [P, I, I, I, I, I, P, P, P, P, P, P, P, P, I, P]
+    L.vq_rvq_unpack_dequant.argtypes = [P, P, P, I, I, I, I, I, P, P, P, P]
+    L.vq_kivi_quant_pack.argtypes = [P, P, I, I, I, I, I, I, I, P, P, P, P, P, P, P, I, P]
+    L.vq_kivi_unpack_dequant.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, P, P, P]
+    L.vq_device_error.argtypes = [P, ctypes.POINTER(ctypes.c_int)]
+    for name in EXPORTED[2:]:
+        getattr(L, name).restype = I
+    _lib = L
+    return L
+
+
+def _check(status: int, what: str):
+    if status != VQ_OK:
+        raise VQError(status, what)
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _host(a):
+    a = np.ascontiguousarray(a, dtype=np.float32)
+    return a, a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def vq_status_str(status: int) -> str:
+    return lib().vq_status_str(status).decode()
+
+
+def vq_version() -> str:
+    return lib().vq_version().decode()
+
+
+def vq_rvq_codebook(D: int, bits: int):
+    """(c1, b1, c2, b2) float32 host arrays: Gaussian stage-1 and Laplace-fit stage-2."""
+    L = 1 << bits
+    c1 = np.empty(L, np.float32)
+    b1 = np.empty(L - 1, np.float32)
+    c2 = np.empty(L, np.float32)
+    b2 = np.empty(L - 1, np.float32)
+    _check(lib().vq_rvq_codebook(D, bits, *[a.ctypes.data_as(ctypes.c_void_p) for a in (c1, b1, c2, b2)]),
+           "vq_rvq_codebook")
+    return c1, b1, c2, b2
+
+
+def vq_rvq_encode_pack(k, bits: int, c1, b1, c2, b2, packed1=None, packed2=None, norms=None,
+                       dst_off=None, S_dst=None, stream=None):
+    """Encode fp16 keys k [B, H, S, D] into (packed1, packed2, norms)."""
+    import torch
+    B, H, S, D = k.shape
+    S_dst = S if S_dst is None else S_dst
+    W = D * bits // 32
+    if packed1 is None:
+        packed1 = torch.empty((B, H, S_dst, W), dtype=torch.int32, device=k.device)
+    if packed2 is None:
+        packed2 = torch.empty((B, H, S_dst, W), dtype=torch.int32, device=k.device)
+    if norms is None:
+        norms = torch.empty((B, H, S_dst), dtype=torch.float32, device=k.device)
+    keep = [_host(v) for v in (c1, b1, c2, b2)]
+    _check(lib().vq_rvq_encode_pack(_ptr(k), B, H, S, D, bits, *[p for _, p in keep],
+                                    _ptr(packed1), _ptr(packed2), _ptr(norms), _ptr(dst_off),
+                                    S_dst, _stream(stream)), "vq_rvq_encode_pack")
+    return packed1, packed2, norms
+
+
+def vq_rvq_unpack_dequant(packed1, packed2, norms, bits: int, c1, c2, out=None, stream=None):
+    """Decode (packed1, packed2, norms) [B, H, S, ...] back to fp16 keys [B, H, S, 128]."""
+    import torch
+    B, H, S, _ = packed1.shape
+    D = 128
+    if out is None:
+        out = torch.empty((B, H, S, D), dtype=torch.float16, device=packed1.device)
+    keep = [_host(v) for v in (c1, c2)]
+    _check(lib().vq_rvq_unpack_dequant(_ptr(packed1), _ptr(packed2), _ptr(norms), B, H, S, D, bits,
+                                       keep[0][1], keep[1][1], _ptr(out), _stream(stream)),
+           "vq_rvq_unpack_dequant")
+    return out
+
+
+def kivi_shapes(B, H, S_dst, D, bits, group):
+    """Output shapes of vq_kivi_quant_pack for a destination of S_dst tokens."""
+    NG = (S_dst + group - 1) // group
+    return {
+        "k_packed": (B, H, NG, group * bits // 32, D), "k_scale": (B, H, NG, D),
+        "v_packed": (B, H, S_dst, D * bits // 32), "v_scale": (B, H, S_dst, D // group),
+    }
+
+
+def vq_kivi_quant_pack(k, v, bits: int, group: int, residual_length: int, outs=None,
+                       dst_off=None, S_dst=None, stream=None):
+    """KIVI flush of k and/or v ([B, H, S, D] fp16; either may be None).
+
+    Returns a dict with k_packed, k_scale, k_zero, v_packed, v_scale, v_zero
+    (allocated when `outs` does not provide them)."""
+    import torch
+    ref = k if k is not None else v
+    B, H, S, D = ref.shape
+    S_q = max(S - residual_length, 0)
+    S_dst = S_q if S_dst is None else S_dst
+    shp = kivi_shapes(B, H, S_dst, D, bits, group)
+    outs = dict(outs or {})
+    dev = ref.device
+    if k is not None:
+        outs.setdefault("k_packed", torch.empty(shp["k_packed"], dtype=torch.int32, device=dev))
+        outs.setdefault("k_scale", torch.empty(shp["k_scale"], dtype=torch.float16, device=dev))
+        outs.setdefault("k_zero", torch.empty(shp["k_scale"], dtype=torch.float16, device=dev))
+    if v is not None:
+        outs.setdefault("v_packed", torch.empty(shp["v_packed"], dtype=torch.int32, device=dev))
+        outs.setdefault("v_scale", torch.empty(shp["v_scale"], dtype=torch.float16, device=dev))
+        outs.setdefault("v_zero", torch.empty(shp["v_scale"], dtype=torch.float16, device=dev))
+    g = outs.get
+    _check(lib().vq_kivi_quant_pack(_ptr(k), _ptr(v), B, H, S, D, bits, group, residual_length,
+                                    _ptr(g("k_packed") if k is not None else None),
+                                    _ptr(g("k_scale") if k is not None else None),
+                                    _ptr(g("k_zero") if k is not None else None),
+                                    _ptr(g("v_packed") if v is not None else None),
+                                    _ptr(g("v_scale") if v is not None else None),
+                                    _ptr(g("v_zero") if v is not None else None),
+                                    _ptr(dst_off), S_dst, _stream(stream)), "vq_kivi_quant_pack")
+    return outs
+
+
+def vq_kivi_unpack_dequant(packs: dict, B: int, H: int, S_q: int, bits: int, group: int,
+                           k_out=None, v_out=None, want_k=True, want_v=True, stream=None):
+    """Dequantize the KIVI storage in `packs` (keys and/or values) to fp16 [B, H, S_q, 128]."""
+    import torch
+    D = 128
+    dk = want_k and "k_packed" in packs
+    dv = want_v and "v_packed" in packs
+    ref = packs["k_packed"] if dk else packs["v_packed"]
+    if dk and k_out is None:
+        k_out = torch.empty((B, H, S_q, D), dtype=torch.float16, device=ref.device)
+    if dv and v_out is None:
+        v_out = torch.empty((B, H, S_q, D), dtype=torch.float16, device=ref.device)
+    _check(lib().vq_kivi_unpack_dequant(
+        _ptr(packs["k_packed"]) if dk else None, _ptr(packs["k_scale"]) if dk else None,
+        _ptr(packs["k_zero"]) if dk else None, _ptr(packs["v_packed"]) if dv else None,
+        _ptr(packs["v_scale"]) if dv else None, _ptr(packs["v_zero"]) if dv else None,
+        B, H, S_q, D, bits, group, _ptr(k_out) if dk else None, _ptr(v_out) if dv else None,
+        _stream(stream)), "vq_kivi_unpack_dequant")
+    return k_out, v_out
+
+
+def vq_device_error(stream=None) -> int:
+    """Wait for the stream; read and clear the library's device error bits."""
+    code = ctypes.c_int(0)
+    st = lib().vq_device_error(_stream(stream), ctypes.byref(code))
+    if st not in (VQ_OK, VQ_ERR_DEVICE):
+        raise VQError(st, "vq_device_error")
+    return code.value

@@ -1,0 +1,416 @@
+// api.cpp - the extern "C" entry points of include/vq.h: argument
+// validation, codebook tables, launch dispatch.  Host code only.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <cuda_runtime_api.h>
+
+#include "launch.h"
+#include "vq.h"
+
+namespace vq {
+
+bool rvq_codebook_f64(int D, int bits, double *g, double *l, double *beta_out);
+
+namespace {
+
+constexpr int kD = 128;
+// Guard band (in units of the rotated, unit-norm coordinate y) around every
+// boundary: a row with any y (or stage-2 residual) closer than this to a
+// boundary is recomputed in exact / double-float arithmetic.  The fp32 fast
+// path's error on y is a few 1e-8 (norm, seven butterfly stages, scaling);
+// the band is several times the largest error seen on Gaussian rows with
+// 40x outlier channels.
+constexpr float kGuard = 2.5e-7f;
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+bool overlap(const void *a, size_t na, const void *b, size_t nb)
+{
+    if (!a || !b || na == 0 || nb == 0) return false;
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+}
+
+bool finite_sorted(const float *v, int n)
+{
+    for (int i = 0; i < n; ++i) {
+        if (!std::isfinite(v[i])) return false;
+        if (i > 0 && !(v[i] > v[i - 1])) return false;
+    }
+    return true;
+}
+
+// centroids c[L] ascending, boundaries b[L-1] strictly between neighbours
+bool valid_codebook(const float *c, const float *b, int L)
+{
+    if (!finite_sorted(c, L) || !finite_sorted(b, L - 1)) return false;
+    for (int k = 0; k < L - 1; ++k)
+        if (!(c[k] < b[k] && b[k] < c[k + 1])) return false;
+    return true;
+}
+
+// ---------------------------------------------------------------- grid tables
+// Host copy of the device cell map (two correctly rounded fp32 FMAs and a
+// saturation), so the host knows exactly which fp32 values share a cell.
+int cell_of(float v, float a, float bc)
+{
+    float u = std::fmaf(v, a, bc);
+    if (!(u > 0.0f)) u = 0.0f;  // also NaN -> 0, as the device saturation
+    if (u > 1.0f) u = 1.0f;
+    const float gf = std::fmaf(u, 31.0f, 12582912.0f);
+    uint32_t bits;
+    std::memcpy(&bits, &gf, 4);
+    return (int)(bits & 31u);
+}
+
+int32_t ordered(float f)
+{
+    int32_t i;
+    std::memcpy(&i, &f, 4);
+    return i >= 0 ? i : (int32_t)(0x80000000u - (uint32_t)i);
+}
+
+float from_ordered(int32_t o)
+{
+    const int32_t i = o >= 0 ? o : (int32_t)(0x80000000u - (uint32_t)o);
+    float f;
+    std::memcpy(&f, &i, 4);
+    return f;
+}
+
+// Smallest finite float v with cell_of(v) >= g (the map is monotone in v).
+double cell_lower_edge(int g, float a, float bc)
+{
+    if (g <= 0) return -INFINITY;
+    int32_t lo = ordered(-3.0e38f), hi = ordered(3.0e38f);
+    if (cell_of(from_ordered(hi), a, bc) < g) return INFINITY;
+    while (lo < hi) {
+        const int32_t mid = lo + (hi - lo) / 2;
+        if (cell_of(from_ordered(mid), a, bc) >= g) hi = mid;
+        else lo = mid + 1;
+    }
+    return (double)from_ordered(lo);
+}
+
+bool build_grid(const float *b, int nb, float guard, GridTable &t)
+{
+    const double span = nb > 1 ? (double)b[nb - 1] - (double)b[0] : std::fmax(std::fabs((double)b[0]), 1e-3);
+    for (int trial = 0; trial < 96; ++trial) {
+        const double pad = span * (0.5 / 31.0 + 0.0071 * trial);
+        const double width = (nb > 1 ? span : 0.0) + 2.0 * pad;
+        t.a = (float)(1.0 / width);
+        t.bc = (float)(-((double)b[0] - pad) / width);
+        int cell[16];
+        bool ok = true;
+        for (int k = 0; k < nb && ok; ++k) {
+            cell[k] = cell_of(b[k], t.a, t.bc);
+            if (k > 0 && cell[k] <= cell[k - 1]) ok = false;
+        }
+        for (int k = 0; k < nb && ok; ++k) {
+            const double lo = cell_lower_edge(cell[k], t.a, t.bc);
+            const double hi = cell[k] == 31 ? INFINITY : cell_lower_edge(cell[k] + 1, t.a, t.bc);
+            if (!((double)b[k] - lo >= guard) || !(hi - (double)b[k] > guard)) ok = false;
+        }
+        if (!ok) continue;
+        int k = 0;
+        for (int g = 0; g < 32; ++g) {
+            while (k < nb && cell[k] < g) ++k;
+            const bool has = k < nb && cell[k] == g;
+            t.bnd[g] = has ? b[k] : -INFINITY;
+            t.code[g] = has ? k : k - 1;
+        }
+        return true;
+    }
+    return false;
+}
+
+vq_status cuda_status(cudaError_t e) { return e == cudaSuccess ? VQ_OK : VQ_ERR_CUDA; }
+
+}  // namespace
+
+int sm_count()
+{
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+    if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    if (dev >= 0 && dev < 64) cache[dev] = n;
+    return n;
+}
+
+}  // namespace vq
+
+using namespace vq;
+
+extern "C" {
+
+const char *vq_status_str(int s)
+{
+    switch (s) {
+    case VQ_OK: return "VQ_OK";
+    case VQ_ERR_INVALID_ARG: return "VQ_ERR_INVALID_ARG";
+    case VQ_ERR_UNSUPPORTED: return "VQ_ERR_UNSUPPORTED";
+    case VQ_ERR_MISALIGNED: return "VQ_ERR_MISALIGNED";
+    case VQ_ERR_ALIASING: return "VQ_ERR_ALIASING";
+    case VQ_ERR_CUDA: return "VQ_ERR_CUDA";
+    case VQ_ERR_DEVICE: return "VQ_ERR_DEVICE";
+    default: return "VQ_ERR_UNKNOWN";
+    }
+}
+
+const char *vq_version(void) { return "vqflush 0.1.0 sm_103a"; }
+
+vq_status vq_rvq_codebook(int D, int bits, float *c1, float *b1, float *c2, float *b2)
+{
+    if (!c1 || !b1 || !c2 || !b2) return VQ_ERR_INVALID_ARG;
+    if (D <= 0 || (bits != 1 && bits != 2 && bits != 4)) return VQ_ERR_INVALID_ARG;
+    const int L = 1 << bits;
+    double g[16], l[16], beta;
+    if (!rvq_codebook_f64(D, bits, g, l, &beta)) return VQ_ERR_INVALID_ARG;
+    for (int k = 0; k < L; ++k) {
+        c1[k] = (float)g[k];
+        c2[k] = (float)l[k];
+    }
+    for (int k = 0; k + 1 < L; ++k) {
+        b1[k] = (float)(0.5 * (g[k] + g[k + 1]));
+        b2[k] = (float)(0.5 * (l[k] + l[k + 1]));
+    }
+    return VQ_OK;
+}
+
+vq_status vq_rvq_encode_pack(const void *k_f16, int B, int H, int S, int D, int bits,
+                             const float *c1, const float *b1, const float *c2, const float *b2,
+                             uint32_t *packed1, uint32_t *packed2, float *norms,
+                             const int32_t *dst_off, int S_dst, vq_stream_t stream)
+{
+    if (B < 0 || H < 0 || S < 0) return VQ_ERR_INVALID_ARG;
+    if (bits == 3 || (D != kD && D > 0)) return VQ_ERR_UNSUPPORTED;
+    if (D != kD || (bits != 1 && bits != 2 && bits != 4)) return VQ_ERR_INVALID_ARG;
+    if (!c1 || !b1 || !c2 || !b2) return VQ_ERR_INVALID_ARG;
+    const int L = 1 << bits;
+    if (!valid_codebook(c1, b1, L) || !valid_codebook(c2, b2, L)) return VQ_ERR_INVALID_ARG;
+    if (dst_off == nullptr ? S_dst != S : S_dst < S) return VQ_ERR_INVALID_ARG;
+    const long long N = (long long)B * H * S;
+    const long long Nd = (long long)B * H * S_dst;
+    if (N >= (1LL << 31) || Nd >= (1LL << 31)) return VQ_ERR_UNSUPPORTED;
+    if (N == 0) return VQ_OK;
+    if (!k_f16 || !packed1 || !packed2 || !norms) return VQ_ERR_INVALID_ARG;
+    if (!aligned(k_f16, 16) || !aligned(packed1, 16) || !aligned(packed2, 16) || !aligned(norms, 4) ||
+        (dst_off && !aligned(dst_off, 4)))
+        return VQ_ERR_MISALIGNED;
+    const int W = D * bits / 32;
+    const size_t in_b = (size_t)N * D * 2, pk_b = (size_t)Nd * W * 4, n_b = (size_t)Nd * 4;
+    if (overlap(k_f16, in_b, packed1, pk_b) || overlap(k_f16, in_b, packed2, pk_b) ||
+        overlap(k_f16, in_b, norms, n_b) || overlap(packed1, pk_b, packed2, pk_b) ||
+        overlap(packed1, pk_b, norms, n_b) || overlap(packed2, pk_b, norms, n_b) ||
+        (dst_off && (overlap(dst_off, (size_t)B * 4, packed1, pk_b) ||
+                     overlap(dst_off, (size_t)B * 4, packed2, pk_b) ||
+                     overlap(dst_off, (size_t)B * 4, norms, n_b))))
+        return VQ_ERR_ALIASING;
+
+    RvqEncodeParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.x = k_f16;
+    p.p1 = packed1;
+    p.p2 = packed2;
+    p.norms = norms;
+    p.dst_off = dst_off;
+    p.N = (int)N;
+    p.S = S;
+    p.H = H;
+    p.S_dst = S_dst;
+    p.guard = kGuard;
+    for (int k = 0; k < 16; ++k) {
+        p.c1[k] = k < L ? c1[k] : 0.0f;
+        p.c2[k] = k < L ? c2[k] : 0.0f;
+        p.b1[k] = k < L - 1 ? b1[k] : INFINITY;
+        p.b2[k] = k < L - 1 ? b2[k] : INFINITY;
+    }
+    const bool grid = build_grid(b1, L - 1, kGuard, p.t1) && build_grid(b2, L - 1, kGuard, p.t2);
+    return cuda_status(launch_rvq_encode(p, bits, grid, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+vq_status vq_rvq_unpack_dequant(const uint32_t *packed1, const uint32_t *packed2, const float *norms,
+                                int B, int H, int S, int D, int bits, const float *c1, const float *c2,
+                                void *out_f16, vq_stream_t stream)
+{
+    if (B < 0 || H < 0 || S < 0) return VQ_ERR_INVALID_ARG;
+    if (bits == 3 || (D != kD && D > 0)) return VQ_ERR_UNSUPPORTED;
+    if (D != kD || (bits != 1 && bits != 2 && bits != 4)) return VQ_ERR_INVALID_ARG;
+    if (!c1 || !c2) return VQ_ERR_INVALID_ARG;
+    const int L = 1 << bits;
+    for (int k = 0; k < L; ++k)
+        if (!std::isfinite(c1[k]) || !std::isfinite(c2[k])) return VQ_ERR_INVALID_ARG;
+    const long long N = (long long)B * H * S;
+    if (N >= (1LL << 31)) return VQ_ERR_UNSUPPORTED;
+    if (N == 0) return VQ_OK;
+    if (!packed1 || !packed2 || !norms || !out_f16) return VQ_ERR_INVALID_ARG;
+    if (!aligned(packed1, 16) || !aligned(packed2, 16) || !aligned(norms, 4) || !aligned(out_f16, 16))
+        return VQ_ERR_MISALIGNED;
+    const int W = D * bits / 32;
+    const size_t pk_b = (size_t)N * W * 4, out_b = (size_t)N * D * 2;
+    if (overlap(out_f16, out_b, packed1, pk_b) || overlap(out_f16, out_b, packed2, pk_b) ||
+        overlap(out_f16, out_b, norms, (size_t)N * 4))
+        return VQ_ERR_ALIASING;
+    RvqDecodeParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.p1 = packed1;
+    p.p2 = packed2;
+    p.norms = norms;
+    p.out = out_f16;
+    p.N = (int)N;
+    for (int k = 0; k < 16; ++k) {
+        p.c1[k] = k < L ? c1[k] : 0.0f;
+        p.c2[k] = k < L ? c2[k] : 0.0f;
+    }
+    return cuda_status(launch_rvq_decode(p, bits, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+static vq_status kivi_common_check(int B, int H, int D, int bits, int group)
+{
+    if (B < 0 || H < 0) return VQ_ERR_INVALID_ARG;
+    if (bits == 3 || (D != kD && D > 0)) return VQ_ERR_UNSUPPORTED;
+    if (D != kD || (bits != 1 && bits != 2 && bits != 4)) return VQ_ERR_INVALID_ARG;
+    if (group <= 0 || D % group != 0 || (group * bits) % 32 != 0) return VQ_ERR_INVALID_ARG;
+    if (group != 32 && group != 64 && group != 128) return VQ_ERR_UNSUPPORTED;
+    return VQ_OK;
+}
+
+vq_status vq_kivi_quant_pack(const void *k_f16, const void *v_f16, int B, int H, int S, int D,
+                             int bits, int group, int residual_length,
+                             uint32_t *k_packed, void *k_scale, void *k_zero,
+                             uint32_t *v_packed, void *v_scale, void *v_zero,
+                             const int32_t *dst_off, int S_dst, vq_stream_t stream)
+{
+    vq_status st = kivi_common_check(B, H, D, bits, group);
+    if (st != VQ_OK) return st;
+    if (S < 0 || residual_length < 0) return VQ_ERR_INVALID_ARG;
+    const int S_q = S - residual_length > 0 ? S - residual_length : 0;
+    if (dst_off == nullptr ? S_dst != S_q : S_dst < S_q) return VQ_ERR_INVALID_ARG;
+    if ((long long)B * H * S >= (1LL << 31) || (long long)B * H * S_dst >= (1LL << 31))
+        return VQ_ERR_UNSUPPORTED;
+    if (!k_f16 && !v_f16) return VQ_ERR_INVALID_ARG;
+    if (k_f16 && (!k_packed || !k_scale || !k_zero)) return VQ_ERR_INVALID_ARG;
+    if (v_f16 && (!v_packed || !v_scale || !v_zero)) return VQ_ERR_INVALID_ARG;
+    if ((long long)B * H * S_q == 0) return VQ_OK;
+    const int NG_dst = (S_dst + group - 1) / group;
+    const size_t in_b = (size_t)B * H * S * D * 2;
+    const size_t kpk_b = (size_t)B * H * NG_dst * group * bits / 32 * D * 4;
+    const size_t ksz_b = (size_t)B * H * NG_dst * D * 2;
+    const size_t vpk_b = (size_t)B * H * S_dst * D * bits / 32 * 4;
+    const size_t vsz_b = (size_t)B * H * S_dst * (D / group) * 2;
+    if ((k_f16 && (!aligned(k_f16, 16) || !aligned(k_packed, 16) || !aligned(k_scale, 8) ||
+                   !aligned(k_zero, 8))) ||
+        (v_f16 && (!aligned(v_f16, 16) || !aligned(v_packed, 16) || !aligned(v_scale, 2) ||
+                   !aligned(v_zero, 2))) ||
+        (dst_off && !aligned(dst_off, 4)))
+        return VQ_ERR_MISALIGNED;
+    const void *outs[6] = {k_f16 ? k_packed : nullptr, k_f16 ? k_scale : nullptr, k_f16 ? k_zero : nullptr,
+                           v_f16 ? v_packed : nullptr, v_f16 ? v_scale : nullptr, v_f16 ? v_zero : nullptr};
+    const size_t osz[6] = {kpk_b, ksz_b, ksz_b, vpk_b, vsz_b, vsz_b};
+    for (int i = 0; i < 6; ++i) {
+        if (overlap(outs[i], osz[i], k_f16, in_b) || overlap(outs[i], osz[i], v_f16, in_b) ||
+            (dst_off && overlap(outs[i], osz[i], dst_off, (size_t)B * 4)))
+            return VQ_ERR_ALIASING;
+        for (int j = i + 1; j < 6; ++j)
+            if (overlap(outs[i], osz[i], outs[j], osz[j])) return VQ_ERR_ALIASING;
+    }
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    KiviQuantParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.dst_off = dst_off;
+    p.B = B;
+    p.H = H;
+    p.S = S;
+    p.S_q = S_q;
+    p.S_dst = S_dst;
+    p.group = group;
+    p.NG_dst = NG_dst;
+    if (k_f16) {
+        p.x = k_f16;
+        p.packed = k_packed;
+        p.scale = k_scale;
+        p.zero = k_zero;
+        cudaError_t e = launch_kivi_quant(p, bits, true, s);
+        if (e != cudaSuccess) return VQ_ERR_CUDA;
+    }
+    if (v_f16) {
+        p.x = v_f16;
+        p.packed = v_packed;
+        p.scale = v_scale;
+        p.zero = v_zero;
+        cudaError_t e = launch_kivi_quant(p, bits, false, s);
+        if (e != cudaSuccess) return VQ_ERR_CUDA;
+    }
+    return VQ_OK;
+}
+
+vq_status vq_kivi_unpack_dequant(const uint32_t *k_packed, const void *k_scale, const void *k_zero,
+                                 const uint32_t *v_packed, const void *v_scale, const void *v_zero,
+                                 int B, int H, int S_q, int D, int bits, int group,
+                                 void *k_out_f16, void *v_out_f16, vq_stream_t stream)
+{
+    vq_status st = kivi_common_check(B, H, D, bits, group);
+    if (st != VQ_OK) return st;
+    if (S_q < 0) return VQ_ERR_INVALID_ARG;
+    if ((long long)B * H * S_q >= (1LL << 31)) return VQ_ERR_UNSUPPORTED;
+    const bool dk = k_out_f16 != nullptr, dv = v_out_f16 != nullptr;
+    if (!dk && !dv) return VQ_ERR_INVALID_ARG;
+    if (dk && (!k_packed || !k_scale || !k_zero)) return VQ_ERR_INVALID_ARG;
+    if (dv && (!v_packed || !v_scale || !v_zero)) return VQ_ERR_INVALID_ARG;
+    if ((long long)B * H * S_q == 0) return VQ_OK;
+    if ((dk && (!aligned(k_packed, 16) || !aligned(k_scale, 8) || !aligned(k_zero, 8) ||
+                !aligned(k_out_f16, 8))) ||
+        (dv && (!aligned(v_packed, 4) || !aligned(v_scale, 2) || !aligned(v_zero, 2) ||
+                !aligned(v_out_f16, 16))))
+        return VQ_ERR_MISALIGNED;
+    const int NG = (S_q + group - 1) / group;
+    const size_t out_b = (size_t)B * H * S_q * D * 2;
+    if (dk && (overlap(k_out_f16, out_b, k_packed, (size_t)B * H * NG * group * bits / 32 * D * 4) ||
+               overlap(k_out_f16, out_b, k_scale, (size_t)B * H * NG * D * 2) ||
+               overlap(k_out_f16, out_b, k_zero, (size_t)B * H * NG * D * 2)))
+        return VQ_ERR_ALIASING;
+    if (dv && (overlap(v_out_f16, out_b, v_packed, (size_t)B * H * S_q * D * bits / 32 * 4) ||
+               overlap(v_out_f16, out_b, v_scale, (size_t)B * H * S_q * (D / group) * 2) ||
+               overlap(v_out_f16, out_b, v_zero, (size_t)B * H * S_q * (D / group) * 2)))
+        return VQ_ERR_ALIASING;
+    if (dk && dv && overlap(k_out_f16, out_b, v_out_f16, out_b)) return VQ_ERR_ALIASING;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    KiviDequantParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.BH = B * H;
+    p.S_q = S_q;
+    p.group = group;
+    p.NG = NG;
+    if (dk) {
+        p.packed = k_packed;
+        p.scale = k_scale;
+        p.zero = k_zero;
+        p.out = k_out_f16;
+        if (launch_kivi_dequant(p, bits, true, s) != cudaSuccess) return VQ_ERR_CUDA;
+    }
+    if (dv) {
+        p.packed = v_packed;
+        p.scale = v_scale;
+        p.zero = v_zero;
+        p.out = v_out_f16;
+        if (launch_kivi_dequant(p, bits, false, s) != cudaSuccess) return VQ_ERR_CUDA;
+    }
+    return VQ_OK;
+}
+
+vq_status vq_device_error(vq_stream_t stream, int *code_out)
+{
+    if (!code_out) return VQ_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    unsigned a = 0, b = 0;
+    if (rvq_take_device_error(&a, s) != cudaSuccess) return VQ_ERR_CUDA;
+    if (kivi_take_device_error(&b, s) != cudaSuccess) return VQ_ERR_CUDA;
+    *code_out = (int)(a | b);
+    return (a | b) ? VQ_ERR_DEVICE : VQ_OK;
+}
+
+}  // extern "C"

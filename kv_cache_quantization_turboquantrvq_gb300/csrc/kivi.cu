@@ -1,0 +1,621 @@
+// kivi.cu - KIVI asymmetric min/max group quantize+pack and unpack+dequant
+// for sm_103a.
+//
+// Method (VeloxQuant-MLX blog, tag "kivi", first post "What we're actually
+// optimizing" and second post "What KIVI is"): per group zero = min,
+// scale = (max - min)/(2^b - 1), q = round((x - zero)/scale) with ties to even
+// ("Rounding mode"), recon = q*scale + zero.  Keys: groups of G tokens per
+// channel; values: groups of G channels per token; only tokens [0, S_q) are
+// flushed, the residual window [S_q, S) stays fp16 and is not touched.
+//
+// The pages quantize and immediately dequantize to fp16; here the codes are
+// packed (LSB first, 32/b per uint32) with fp16 scale and zero per group, the
+// storage step the pages name as the next one.
+//
+// Exactness: codes are those of the exact quotient
+//   t = (x - min)(2^b - 1)/(max - min), rounded half to even.
+// The fast path computes t in fp32 (error < 8 ulp of 2^b - 1); an element
+// whose fp32 t is that close to a half-integer is decided again in binary64,
+// where numerator and denominator are exact.  The stored scale is
+// fp16(fp32(range/(2^b - 1))) with both roundings to nearest even.
+//
+// Values (per token): one row per thread, rows staged by per-row bulk copies
+// into a per-warp 3-stage ring (as the RVQ encoder).  Keys (per channel): one
+// [G x 128] tile (contiguous in memory) per warp per step, staged by a single
+// bulk copy; lane l owns channels 4l..4l+3 and walks the G tokens, so no
+// cross-thread reduction is needed (the pages' "one thread, one whole group").
+#include <cuda_fp16.h>
+
+#include "device_common.cuh"
+#include "launch.h"
+
+namespace vq {
+
+VQ_DEFINE_ERROR_WORD(g_kivi_err);
+
+namespace {
+
+constexpr int D = 128;
+constexpr float MAGIC = 12582912.0f;  // 1.5 * 2^23: x + MAGIC rounds x to an integer, ties to even
+
+// ------------------------------------------------------------ group scalars
+
+struct GroupQ {
+    float mn;      // group minimum (exact)
+    float f;       // (2^b - 1) / (max - min) in fp32, 0 for a constant group
+    float range;   // max - min (fp32; exactness checked where it matters)
+    __half scale_h, zero_h;
+};
+
+// RN32 of the exact (mx - mn)/c, given fp16-valued mx > mn.
+__device__ __noinline__ float exact_scale32_slow(float mx, float mn, float c)
+{
+    const double d = (double)mx - (double)mn;  // exact: fp16 values
+    const double q = d / (double)c;
+    float f = (float)q;
+    const float up = __int_as_float(__float_as_int(f) + 1);
+    const float dn = __int_as_float(__float_as_int(f) - 1);
+    const float other = (double)f > q ? dn : up;
+    const double mid = 0.5 * ((double)f + (double)other);
+    if (q == mid) {
+        const double rem = fma(-q, (double)c, d);
+        if (rem > 0.0) return (double)f > (double)other ? f : other;
+        if (rem < 0.0) return (double)f < (double)other ? f : other;
+    }
+    return f;
+}
+
+template <int BITS>
+__device__ __forceinline__ GroupQ group_setup(float mn, float mx)
+{
+    constexpr float C = (float)((1 << BITS) - 1);
+    GroupQ g;
+    g.mn = mn;
+    g.zero_h = __float2half_rn(mn);  // exact: mn is an fp16 value
+    if (mx > mn) {
+        float d, e;
+        two_sum(mx, -mn, d, e);
+        g.range = d;
+        const float s32 = (e == 0.0f) ? __fdiv_rn(d, C) : exact_scale32_slow(mx, mn, C);
+        g.scale_h = __float2half_rn(s32);
+        g.f = __fdiv_rn(C, d);
+    } else {
+        g.range = 0.0f;
+        g.scale_h = __float2half_rn(0.0f);
+        g.f = 0.0f;
+    }
+    return g;
+}
+
+// Exact half-even rounding of t = (x - mn) c / (mx - mn), in binary64 (all
+// operands fp16-valued, so numerator and denominator are exact).
+template <int BITS>
+__device__ __noinline__ uint32_t exact_code_slow(float x, float mn, float mx)
+{
+    const double c = (double)((1 << BITS) - 1);
+    const double num = ((double)x - (double)mn) * c;
+    const double den = (double)mx - (double)mn;
+    const double t = num / den;            // only used to find the candidate k
+    const double k = floor(t);
+    // compare num/den with k + 1/2 exactly: 2 num vs (2k+1) den (both exact)
+    const double lhs = 2.0 * num, rhs = (2.0 * k + 1.0) * den;
+    double q;
+    if (lhs > rhs) q = k + 1.0;
+    else if (lhs < rhs) q = k;
+    else q = (fmod(k, 2.0) == 0.0) ? k : k + 1.0;
+    if (q < 0.0) q = 0.0;
+    if (q > c) q = c;
+    return (uint32_t)q;
+}
+
+// Fast code of one element; falls back to the exact path near a half-integer.
+template <int BITS>
+__device__ __forceinline__ uint32_t code_of(float x, const GroupQ &g, float mx)
+{
+    constexpr float C = (float)((1 << BITS) - 1);
+    constexpr float EPS = 8.0f * C * 5.9604645e-08f;  // 8 ulp(1) * (2^b - 1)
+    const float t = (x - g.mn) * g.f;
+    const float tm = t + MAGIC;
+    const float frac = t - (tm - MAGIC);
+    uint32_t q = (uint32_t)__float_as_int(tm) & ((1u << BITS) - 1u);
+    if (fabsf(frac) > 0.5f - EPS) q = exact_code_slow<BITS>(x, g.mn, mx);
+    return q;
+}
+
+// fp16(q*s + z) rounded once from the exact value: q*s is exact in fp32, the
+// sum is carried as a rounded value plus its exact error, and a non-zero error
+// is folded in as a sticky bit (round-to-odd) before the final fp16 rounding.
+__device__ __forceinline__ __half recon_exact(uint32_t q, float s, float z)
+{
+    const float p = (float)q * s;
+    float sum, err;
+    two_sum(p, z, sum, err);
+    if (err != 0.0f) {
+        uint32_t b = __float_as_uint(sum);
+        if ((err < 0.0f) != (sum < 0.0f)) b -= 1u;  // truncate toward zero
+        b |= 1u;                                     // sticky
+        sum = __uint_as_float(b);
+    }
+    return __float2half_rn(sum);
+}
+
+// ------------------------------------------------------------ values (per token)
+
+constexpr int VAL_WARPS = 8;
+constexpr int VAL_STAGES = 3;
+constexpr int ROW_BYTES = D * 2;
+constexpr int ROW_STRIDE = ROW_BYTES + 16;
+constexpr int VSTAGE_BYTES = 32 * ROW_STRIDE;
+constexpr int VAL_SMEM = VAL_WARPS * VAL_STAGES * VSTAGE_BYTES + VAL_WARPS * VAL_STAGES * 8;
+
+__device__ __forceinline__ bool kivi_off(const KiviQuantParams &p, int b, int &off)
+{
+    off = 0;
+    if (p.dst_off == nullptr) return true;
+    off = __ldg(p.dst_off + b);
+    if (off < 0 || off > p.S_dst - p.S_q || (off % p.group) != 0) {
+        atomicOr(&g_kivi_err, (unsigned)VQ_DEVERR_BAD_OFFSET);
+        return false;
+    }
+    return true;
+}
+
+template <int BITS, int G>
+__global__ void __launch_bounds__(VAL_WARPS * 32, 1)
+    kivi_values_kernel(const __grid_constant__ KiviQuantParams p)
+{
+    constexpr int E = 32 / BITS;
+    constexpr int W = D * BITS / 32;
+    constexpr int NGD = D / G;
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    unsigned char *wbuf = smem + warp * (VAL_STAGES * VSTAGE_BYTES);
+    uint64_t *bars =
+        reinterpret_cast<uint64_t *>(smem + VAL_WARPS * VAL_STAGES * VSTAGE_BYTES) + warp * VAL_STAGES;
+    if (lane == 0) {
+#pragma unroll
+        for (int s = 0; s < VAL_STAGES; ++s) mbar_init(&bars[s], 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+    const uint64_t pol = l2_policy_evict_first();
+    const int N = p.B * p.H * p.S_q;
+    const int nblk = (N + 31) >> 5;
+    const int gw = blockIdx.x * VAL_WARPS + warp;
+    const int tw = gridDim.x * VAL_WARPS;
+    const __half *x = static_cast<const __half *>(p.x);
+
+    auto issue = [&](int blk, int s) {
+        const int r0 = blk << 5;
+        const int nrows = min(32, N - r0);
+        if (lane == 0) mbar_arrive_expect_tx(&bars[s], (uint32_t)(nrows * ROW_BYTES));
+        if (lane < nrows) {
+            const int r = r0 + lane;
+            const int bh = r / p.S_q, s_ = r - bh * p.S_q;
+            bulk_g2s(wbuf + s * VSTAGE_BYTES + lane * ROW_STRIDE,
+                     x + ((size_t)bh * p.S + s_) * D, ROW_BYTES, &bars[s], pol);
+        }
+    };
+#pragma unroll
+    for (int s = 0; s < VAL_STAGES; ++s) {
+        const int blk = gw + s * tw;
+        if (blk < nblk) issue(blk, s);
+    }
+    for (int it = 0;; ++it) {
+        const int blk = gw + it * tw;
+        if (blk >= nblk) break;
+        const int s = it % VAL_STAGES;
+        const bool ok = mbar_wait_bounded(&bars[s], (uint32_t)(it / VAL_STAGES) & 1u);
+        if (!__all_sync(FULL_MASK, ok)) {
+            if (lane == 0) atomicOr(&g_kivi_err, (unsigned)VQ_DEVERR_WAIT_TIMEOUT);
+            for (int k = 1; k < VAL_STAGES; ++k) {
+                const int it2 = it + k;
+                if (gw + it2 * tw < nblk)
+                    (void)mbar_wait_bounded(&bars[it2 % VAL_STAGES], (uint32_t)(it2 / VAL_STAGES) & 1u);
+            }
+            return;
+        }
+        const int row = (blk << 5) + lane;
+        const uint4 *srow = reinterpret_cast<const uint4 *>(wbuf + s * VSTAGE_BYTES + lane * ROW_STRIDE);
+        uint4 raw[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) raw[c] = srow[c];
+        // recycle the stage as soon as the row is in registers
+        __syncwarp();
+        fence_proxy_async_smem();
+        {
+            const int nb = blk + VAL_STAGES * tw;
+            if (nb < nblk) issue(nb, s);
+        }
+        if (row >= N) continue;
+        const __half2 *h = reinterpret_cast<const __half2 *>(raw);  // 64 half2, channel pairs
+        uint32_t words[W];
+#pragma unroll
+        for (int i = 0; i < W; ++i) words[i] = 0u;
+        __half2 sz[NGD];  // (scale, zero) per group
+#pragma unroll
+        for (int j = 0; j < NGD; ++j) {
+            constexpr int P = G / 2;  // half2 per group
+            __half2 lo = h[j * P], hi = h[j * P];
+#pragma unroll
+            for (int i = 1; i < P; ++i) {
+                lo = __hmin2(lo, h[j * P + i]);
+                hi = __hmax2(hi, h[j * P + i]);
+            }
+            const float mn = fminf(__low2float(lo), __high2float(lo));
+            const float mx = fmaxf(__low2float(hi), __high2float(hi));
+            const GroupQ g = group_setup<BITS>(mn, mx);
+            sz[j] = __halves2half2(g.scale_h, g.zero_h);
+#pragma unroll
+            for (int i = 0; i < P; ++i) {
+                const float2 v = __half22float2(h[j * P + i]);
+                const int e = j * G + 2 * i;
+                words[e / E] = __funnelshift_r(words[e / E], code_of<BITS>(v.x, g, mx), BITS);
+                words[(e + 1) / E] = __funnelshift_r(words[(e + 1) / E], code_of<BITS>(v.y, g, mx), BITS);
+            }
+        }
+        const int bh = row / p.S_q, s_ = row - bh * p.S_q;
+        int off;
+        if (!kivi_off(p, bh / p.H, off)) continue;
+        const size_t drow = (size_t)bh * p.S_dst + off + s_;
+        uint32_t *dst = p.packed + drow * W;
+#pragma unroll
+        for (int i = 0; i < W; i += 4) {
+            if constexpr (W >= 4)
+                *reinterpret_cast<uint4 *>(dst + i) = make_uint4(words[i], words[i + 1], words[i + 2], words[i + 3]);
+        }
+        if constexpr (W < 4) {
+#pragma unroll
+            for (int i = 0; i < W; ++i) dst[i] = words[i];
+        }
+        __half *sc = static_cast<__half *>(p.scale) + drow * NGD;
+        __half *zr = static_cast<__half *>(p.zero) + drow * NGD;
+#pragma unroll
+        for (int j = 0; j < NGD; ++j) {
+            sc[j] = __low2half(sz[j]);
+            zr[j] = __high2half(sz[j]);
+        }
+    }
+}
+
+// ------------------------------------------------------------ keys (per channel)
+
+constexpr int KEY_STAGES = 2;
+constexpr int KEY_SMEM_BUDGET = 192 * 1024;
+
+// Warps per CTA for key tiles of G tokens: as many 2-stage rings as fit.
+template <int G>
+__host__ __device__ constexpr int key_warps()
+{
+    return KEY_SMEM_BUDGET / (KEY_STAGES * G * ROW_BYTES) > 12 ? 12
+                                                                 : KEY_SMEM_BUDGET / (KEY_STAGES * G * ROW_BYTES);
+}
+
+template <int G>
+__host__ __device__ constexpr int key_smem()
+{
+    return key_warps<G>() * KEY_STAGES * (G * ROW_BYTES + 8);
+}
+
+template <int BITS, int G>
+__global__ void __launch_bounds__(key_warps<G>() * 32, 1)
+    kivi_keys_kernel(const __grid_constant__ KiviQuantParams p)
+{
+    constexpr int KEY_WARPS = key_warps<G>();
+    constexpr int E = 32 / BITS;
+    constexpr int WG = G * BITS / 32;  // words per channel per group
+    constexpr int TILE = G * ROW_BYTES;
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    unsigned char *wbuf = smem + warp * (KEY_STAGES * TILE);
+    uint64_t *bars =
+        reinterpret_cast<uint64_t *>(smem + KEY_WARPS * KEY_STAGES * TILE) + warp * KEY_STAGES;
+    if (lane == 0) {
+#pragma unroll
+        for (int s = 0; s < KEY_STAGES; ++s) mbar_init(&bars[s], 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+    const uint64_t pol = l2_policy_evict_first();
+    const int NG = (p.S_q + G - 1) / G;
+    const int ntiles = p.B * p.H * NG;
+    const int gw = blockIdx.x * KEY_WARPS + warp;
+    const int tw = gridDim.x * KEY_WARPS;
+    const __half *x = static_cast<const __half *>(p.x);
+
+    auto ntok_of = [&](int tile) {
+        const int g = tile % NG;
+        return min(G, p.S_q - g * G);
+    };
+    auto issue = [&](int tile, int s) {
+        if (lane == 0) {
+            const int bh = tile / NG, g = tile - bh * NG;
+            const uint32_t bytes = (uint32_t)(ntok_of(tile) * ROW_BYTES);
+            mbar_arrive_expect_tx(&bars[s], bytes);
+            bulk_g2s(wbuf + s * TILE, x + ((size_t)bh * p.S + (size_t)g * G) * D, bytes, &bars[s], pol);
+        }
+    };
+#pragma unroll
+    for (int s = 0; s < KEY_STAGES; ++s) {
+        const int t = gw + s * tw;
+        if (t < ntiles) issue(t, s);
+    }
+    for (int it = 0;; ++it) {
+        const int tile = gw + it * tw;
+        if (tile >= ntiles) break;
+        const int s = it % KEY_STAGES;
+        const bool ok = mbar_wait_bounded(&bars[s], (uint32_t)(it / KEY_STAGES) & 1u);
+        if (!__all_sync(FULL_MASK, ok)) {
+            if (lane == 0) atomicOr(&g_kivi_err, (unsigned)VQ_DEVERR_WAIT_TIMEOUT);
+            for (int k = 1; k < KEY_STAGES; ++k) {
+                const int it2 = it + k;
+                if (gw + it2 * tw < ntiles)
+                    (void)mbar_wait_bounded(&bars[it2 % KEY_STAGES], (uint32_t)(it2 / KEY_STAGES) & 1u);
+            }
+            return;
+        }
+        const unsigned char *tb = wbuf + s * TILE;
+        const int ntok = ntok_of(tile);
+        const int bh = tile / NG, g = tile - bh * NG;
+        // pass 1: per-channel min/max over the group's tokens (exact fp16)
+        const uint2 *col = reinterpret_cast<const uint2 *>(tb) + lane;  // channels 4l..4l+3
+        uint2 r0 = col[0];
+        __half2 lo0 = *reinterpret_cast<__half2 *>(&r0.x), lo1 = *reinterpret_cast<__half2 *>(&r0.y);
+        __half2 hi0 = lo0, hi1 = lo1;
+        if (ntok == G) {
+#pragma unroll 8
+            for (int i = 1; i < G; ++i) {
+                uint2 r = col[i * (ROW_BYTES / 8)];
+                const __half2 a = *reinterpret_cast<__half2 *>(&r.x), b = *reinterpret_cast<__half2 *>(&r.y);
+                lo0 = __hmin2(lo0, a); hi0 = __hmax2(hi0, a);
+                lo1 = __hmin2(lo1, b); hi1 = __hmax2(hi1, b);
+            }
+        } else {
+            for (int i = 1; i < ntok; ++i) {
+                uint2 r = col[i * (ROW_BYTES / 8)];
+                const __half2 a = *reinterpret_cast<__half2 *>(&r.x), b = *reinterpret_cast<__half2 *>(&r.y);
+                lo0 = __hmin2(lo0, a); hi0 = __hmax2(hi0, a);
+                lo1 = __hmin2(lo1, b); hi1 = __hmax2(hi1, b);
+            }
+        }
+        const float mxv[4] = {__low2float(hi0), __high2float(hi0), __low2float(hi1), __high2float(hi1)};
+        GroupQ gq[4];
+        gq[0] = group_setup<BITS>(__low2float(lo0), mxv[0]);
+        gq[1] = group_setup<BITS>(__high2float(lo0), mxv[1]);
+        gq[2] = group_setup<BITS>(__low2float(lo1), mxv[2]);
+        gq[3] = group_setup<BITS>(__high2float(lo1), mxv[3]);
+        // pass 2: codes, packed along tokens (token i -> word i/E, shift (i%E)*BITS)
+        uint32_t w[WG][4];
+#pragma unroll
+        for (int k = 0; k < WG; ++k) {
+            w[k][0] = w[k][1] = w[k][2] = w[k][3] = 0u;
+#pragma unroll
+            for (int j = 0; j < E; ++j) {
+                const int i = k * E + j;
+                uint32_t c0 = 0, c1 = 0, c2 = 0, c3 = 0;
+                if (i < ntok) {
+                    uint2 r = col[i * (ROW_BYTES / 8)];
+                    const float2 a = __half22float2(*reinterpret_cast<__half2 *>(&r.x));
+                    const float2 b = __half22float2(*reinterpret_cast<__half2 *>(&r.y));
+                    c0 = code_of<BITS>(a.x, gq[0], mxv[0]);
+                    c1 = code_of<BITS>(a.y, gq[1], mxv[1]);
+                    c2 = code_of<BITS>(b.x, gq[2], mxv[2]);
+                    c3 = code_of<BITS>(b.y, gq[3], mxv[3]);
+                }
+                w[k][0] = __funnelshift_r(w[k][0], c0, BITS);
+                w[k][1] = __funnelshift_r(w[k][1], c1, BITS);
+                w[k][2] = __funnelshift_r(w[k][2], c2, BITS);
+                w[k][3] = __funnelshift_r(w[k][3], c3, BITS);
+            }
+        }
+        // the tile is consumed: recycle the stage
+        __syncwarp();
+        fence_proxy_async_smem();
+        {
+            const int nt = tile + KEY_STAGES * tw;
+            if (nt < ntiles) issue(nt, s);
+        }
+        int off;
+        if (!kivi_off(p, bh / p.H, off)) continue;
+        const size_t gd = (size_t)bh * p.NG_dst + off / G + g;
+#pragma unroll
+        for (int k = 0; k < WG; ++k)
+            *reinterpret_cast<uint4 *>(p.packed + (gd * WG + k) * D + 4 * lane) =
+                make_uint4(w[k][0], w[k][1], w[k][2], w[k][3]);
+        __half2 s01 = __halves2half2(gq[0].scale_h, gq[1].scale_h);
+        __half2 s23 = __halves2half2(gq[2].scale_h, gq[3].scale_h);
+        __half2 z01 = __halves2half2(gq[0].zero_h, gq[1].zero_h);
+        __half2 z23 = __halves2half2(gq[2].zero_h, gq[3].zero_h);
+        *reinterpret_cast<uint2 *>(static_cast<__half *>(p.scale) + gd * D + 4 * lane) =
+            make_uint2(*reinterpret_cast<uint32_t *>(&s01), *reinterpret_cast<uint32_t *>(&s23));
+        *reinterpret_cast<uint2 *>(static_cast<__half *>(p.zero) + gd * D + 4 * lane) =
+            make_uint2(*reinterpret_cast<uint32_t *>(&z01), *reinterpret_cast<uint32_t *>(&z23));
+    }
+}
+
+// ------------------------------------------------------------ dequant
+
+constexpr int DQ_THREADS = 256;
+
+template <int BITS, int G>
+__global__ void __launch_bounds__(DQ_THREADS) kivi_values_dequant_kernel(const __grid_constant__ KiviDequantParams p)
+{
+    constexpr int E = 32 / BITS;
+    constexpr int W = D * BITS / 32;
+    constexpr int NGD = D / G;
+    constexpr uint32_t MASK = (1u << BITS) - 1u;
+    const int N = p.BH * p.S_q;
+    for (int row = blockIdx.x * DQ_THREADS + threadIdx.x; row < N; row += gridDim.x * DQ_THREADS) {
+        uint32_t words[W];
+#pragma unroll
+        for (int i = 0; i < W; ++i) words[i] = __ldg(p.packed + (size_t)row * W + i);
+        const __half *sc = static_cast<const __half *>(p.scale) + (size_t)row * NGD;
+        const __half *zr = static_cast<const __half *>(p.zero) + (size_t)row * NGD;
+        uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__half *>(p.out) + (size_t)row * D);
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+            uint32_t out[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int e = 8 * c + 2 * j;
+                const float s = __half2float(sc[e / G]), z = __half2float(zr[e / G]);
+                const uint32_t q0 = (words[e / E] >> ((e % E) * BITS)) & MASK;
+                const uint32_t q1 = (words[(e + 1) / E] >> (((e + 1) % E) * BITS)) & MASK;
+                const __half2 hv = __halves2half2(recon_exact(q0, s, z), recon_exact(q1, s, z));
+                out[j] = *reinterpret_cast<const uint32_t *>(&hv);
+            }
+            dst[c] = make_uint4(out[0], out[1], out[2], out[3]);
+        }
+    }
+}
+
+template <int BITS, int G>
+__global__ void __launch_bounds__(DQ_THREADS) kivi_keys_dequant_kernel(const __grid_constant__ KiviDequantParams p)
+{
+    constexpr int E = 32 / BITS;
+    constexpr int WG = G * BITS / 32;
+    constexpr uint32_t MASK = (1u << BITS) - 1u;
+    const int lane = threadIdx.x & 31;
+    const int wpb = DQ_THREADS / 32;
+    const int ntiles = p.BH * p.NG;
+    for (int tile = blockIdx.x * wpb + (threadIdx.x >> 5); tile < ntiles; tile += gridDim.x * wpb) {
+        const int bh = tile / p.NG, g = tile - bh * p.NG;
+        const int ntok = min(G, p.S_q - g * G);
+        const uint2 sraw = __ldg(reinterpret_cast<const uint2 *>(static_cast<const __half *>(p.scale) + (size_t)tile * D + 4 * lane));
+        const uint2 zraw = __ldg(reinterpret_cast<const uint2 *>(static_cast<const __half *>(p.zero) + (size_t)tile * D + 4 * lane));
+        const __half *sh = reinterpret_cast<const __half *>(&sraw);
+        const __half *zh = reinterpret_cast<const __half *>(&zraw);
+        float s[4], z[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) { s[j] = __half2float(sh[j]); z[j] = __half2float(zh[j]); }
+        for (int k = 0; k < WG; ++k) {
+            const uint4 wv = __ldg(reinterpret_cast<const uint4 *>(p.packed + ((size_t)tile * WG + k) * D + 4 * lane));
+            const uint32_t wk[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll 4
+            for (int j = 0; j < E; ++j) {
+                const int i = k * E + j;
+                if (i >= ntok) break;
+                __half o[4];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) o[c] = recon_exact((wk[c] >> (j * BITS)) & MASK, s[c], z[c]);
+                const __half2 a = __halves2half2(o[0], o[1]), b = __halves2half2(o[2], o[3]);
+                *reinterpret_cast<uint2 *>(static_cast<__half *>(p.out) + ((size_t)bh * p.S_q + g * G + i) * D + 4 * lane) =
+                    make_uint2(*reinterpret_cast<const uint32_t *>(&a), *reinterpret_cast<const uint32_t *>(&b));
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------ launchers
+
+template <int BITS, int G>
+cudaError_t launch_q(const KiviQuantParams &p, bool per_channel, cudaStream_t stream)
+{
+    const int sms = sm_count();
+    if (per_channel) {
+        auto kern = kivi_keys_kernel<BITS, G>;
+        constexpr int smem = key_smem<G>();
+        constexpr int warps = key_warps<G>();
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        const int ntiles = p.B * p.H * ((p.S_q + G - 1) / G);
+        int grid = (ntiles + warps - 1) / warps;
+        if (grid > sms) grid = sms;
+        if (grid < 1) grid = 1;
+        kern<<<grid, warps * 32, smem, stream>>>(p);
+    } else {
+        auto kern = kivi_values_kernel<BITS, G>;
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, VAL_SMEM);
+        if (e != cudaSuccess) return e;
+        const int nblk = (p.B * p.H * p.S_q + 31) / 32;
+        int grid = (nblk + VAL_WARPS - 1) / VAL_WARPS;
+        if (grid > sms) grid = sms;
+        if (grid < 1) grid = 1;
+        kern<<<grid, VAL_WARPS * 32, VAL_SMEM, stream>>>(p);
+    }
+    return cudaGetLastError();
+}
+
+template <int BITS, int G>
+cudaError_t launch_dq(const KiviDequantParams &p, bool per_channel, cudaStream_t stream)
+{
+    const int cap = sm_count() * 8;
+    if (per_channel) {
+        const int ntiles = p.BH * p.NG;
+        int grid = (ntiles + DQ_THREADS / 32 - 1) / (DQ_THREADS / 32);
+        if (grid > cap) grid = cap;
+        if (grid < 1) grid = 1;
+        kivi_keys_dequant_kernel<BITS, G><<<grid, DQ_THREADS, 0, stream>>>(p);
+    } else {
+        const int N = p.BH * p.S_q;
+        int grid = (N + DQ_THREADS - 1) / DQ_THREADS;
+        if (grid > cap) grid = cap;
+        if (grid < 1) grid = 1;
+        kivi_values_dequant_kernel<BITS, G><<<grid, DQ_THREADS, 0, stream>>>(p);
+    }
+    return cudaGetLastError();
+}
+
+template <int BITS>
+cudaError_t dispatch_q(const KiviQuantParams &p, bool per_channel, cudaStream_t stream)
+{
+    switch (p.group) {
+    case 32: return launch_q<BITS, 32>(p, per_channel, stream);
+    case 64: return launch_q<BITS, 64>(p, per_channel, stream);
+    case 128: return launch_q<BITS, 128>(p, per_channel, stream);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+template <int BITS>
+cudaError_t dispatch_dq(const KiviDequantParams &p, bool per_channel, cudaStream_t stream)
+{
+    switch (p.group) {
+    case 32: return launch_dq<BITS, 32>(p, per_channel, stream);
+    case 64: return launch_dq<BITS, 64>(p, per_channel, stream);
+    case 128: return launch_dq<BITS, 128>(p, per_channel, stream);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_kivi_quant(const KiviQuantParams &p, int bits, bool per_channel, cudaStream_t stream)
+{
+    if (p.B * p.H <= 0 || p.S_q <= 0) return cudaSuccess;
+    switch (bits) {
+    case 1: return dispatch_q<1>(p, per_channel, stream);
+    case 2: return dispatch_q<2>(p, per_channel, stream);
+    case 4: return dispatch_q<4>(p, per_channel, stream);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_kivi_dequant(const KiviDequantParams &p, int bits, bool per_channel, cudaStream_t stream)
+{
+    if (p.BH <= 0 || p.S_q <= 0) return cudaSuccess;
+    switch (bits) {
+    case 1: return dispatch_dq<1>(p, per_channel, stream);
+    case 2: return dispatch_dq<2>(p, per_channel, stream);
+    case 4: return dispatch_dq<4>(p, per_channel, stream);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t kivi_take_device_error(unsigned *bits, cudaStream_t stream)
+{
+    unsigned zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbolAsync(bits, g_kivi_err, sizeof(unsigned), 0,
+                                              cudaMemcpyDeviceToHost, stream);
+    if (e != cudaSuccess) return e;
+    e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return e;
+    if (*bits) e = cudaMemcpyToSymbolAsync(g_kivi_err, &zero, sizeof(unsigned), 0,
+                                           cudaMemcpyHostToDevice, stream);
+    if (e != cudaSuccess) return e;
+    return cudaStreamSynchronize(stream);
+}
+
+}  // namespace vq

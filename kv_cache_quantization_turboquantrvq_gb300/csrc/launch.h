@@ -1,0 +1,73 @@
+// launch.h - internal interface between the C-ABI front end (api.cpp) and the
+// kernel translation units.  Not installed; users include include/vq.h.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime_api.h>
+
+namespace vq {
+
+// Piecewise lookup that turns a scalar quantizer's boundary count into two
+// warp-shuffle table reads.  A value v maps to cell
+//   g(v) = RN(31 * sat(fma(v, a, bc)))  in [0, 31]
+// (computed on the device as two fp32 FMAs; the host builds the tables by
+// evaluating the same fp32 map).  Every boundary lies in its own cell, at least
+// the guard band away from the cell edges, so for v in cell g
+//   #{k : v > b_k} = code[g] + (v > bnd[g]),
+// with bnd[g] = -inf for cells that hold no boundary.
+struct GridTable {
+    float a, bc;
+    float bnd[32];
+    int code[32];
+};
+
+struct RvqEncodeParams {
+    const void *x;       // fp16 [N, 128]
+    uint32_t *p1, *p2;   // [B, H, S_dst, W]
+    float *norms;        // [B, H, S_dst]
+    const int32_t *dst_off;
+    int N, S, H, S_dst;
+    float guard;         // |y - boundary| below this sends the row to the exact path
+    GridTable t1, t2;
+    float c1[16], c2[16], b1[16], b2[16];
+};
+
+struct RvqDecodeParams {
+    const uint32_t *p1, *p2;
+    const float *norms;
+    void *out;           // fp16 [N, 128]
+    int N;
+    float c1[16], c2[16];
+};
+
+struct KiviQuantParams {
+    const void *x;       // fp16 [B, H, S, D]
+    uint32_t *packed;
+    void *scale, *zero;  // fp16
+    const int32_t *dst_off;
+    int B, H, S, S_q, S_dst, group, NG_dst;
+};
+
+struct KiviDequantParams {
+    const uint32_t *packed;
+    const void *scale, *zero;
+    void *out;
+    int BH, S_q, group, NG;
+};
+
+cudaError_t launch_rvq_encode(const RvqEncodeParams &p, int bits, bool use_grid,
+                              cudaStream_t stream);
+cudaError_t launch_rvq_decode(const RvqDecodeParams &p, int bits, cudaStream_t stream);
+cudaError_t launch_kivi_quant(const KiviQuantParams &p, int bits, bool per_channel,
+                              cudaStream_t stream);
+cudaError_t launch_kivi_dequant(const KiviDequantParams &p, int bits, bool per_channel,
+                                cudaStream_t stream);
+
+// Read and clear the device error word of each kernel unit (bitwise OR).
+cudaError_t rvq_take_device_error(unsigned *bits, cudaStream_t stream);
+cudaError_t kivi_take_device_error(unsigned *bits, cudaStream_t stream);
+
+// Number of SMs of the current device (cached per device).
+int sm_count();
+
+}  // namespace vq

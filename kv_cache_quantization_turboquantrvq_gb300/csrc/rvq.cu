@@ -1,0 +1,576 @@
+// rvq.cu - TurboQuantRVQ encode+pack and unpack+dequant kernels for sm_103a.
+//
+// Method (VeloxQuant-MLX blog, tag "rvq", "The pipeline, as it actually runs"
+// and "What 'quantize' means here, precisely"; rotation as in tag
+// "turboquant", "Kernel 3: Fused Hadamard + Quantize"), per key row x of
+// D = 128 fp16 values:
+//   n = ||x||, y = H (x / n) / sqrt(D)           normalise + Walsh-Hadamard
+//   i1 = #{k : y > b1_k},  r = y - c1[i1]          stage 1 + residual
+//   i2 = #{k : r > b2_k}                           stage 2
+//   packed1/packed2: LSB-first b-bit codes in uint32 words, plus the norm.
+// The pages fuse quantize->pack after a separate rotation dispatch; here the
+// norm, rotation, both stages and both packs are one pass over HBM.
+//
+// Encode design (one row per thread):
+//  * each warp owns a private 3-stage ring of 32-row tiles in shared memory,
+//    filled by per-row cp.async.bulk copies (lane i copies row i, 256 B) that
+//    complete on an mbarrier; rows sit at a 272-byte stride so the 32 row
+//    owners read 16-byte chunks without bank conflicts;
+//  * a thread holds its row as 64 float2 (x[k], x[k+64]) and runs six
+//    butterfly stages with the fp32x2 add/fma instructions and the last
+//    (bit 6) stage in scalar fp32 - no shuffles;
+//  * the boundary count of each stage is two table reads by warp shuffle
+//    (GridTable in launch.h) plus one compare;
+//  * every code is kept unless its pre-quantization value lies within a guard
+//    band of a boundary; such rows are redone by the whole warp in exact /
+//    double-float arithmetic (rvq_fixup_row), so the packed words equal those
+//    of exact arithmetic.
+#include <cuda_fp16.h>
+
+#include "device_common.cuh"
+#include "launch.h"
+
+namespace vq {
+
+VQ_DEFINE_ERROR_WORD(g_rvq_err);
+
+namespace {
+
+constexpr int D = 128;
+constexpr int ENC_WARPS = 8;
+constexpr int ENC_STAGES = 3;
+constexpr int ROW_BYTES = D * 2;
+constexpr int ROW_STRIDE = ROW_BYTES + 16;
+constexpr int STAGE_BYTES = 32 * ROW_STRIDE;
+constexpr int ENC_SMEM = ENC_WARPS * ENC_STAGES * STAGE_BYTES + ENC_WARPS * ENC_STAGES * 8;
+
+// sqrt(128) = 8 sqrt(2) as a double-float (nearest fp32 + fp32 remainder).
+constexpr float SQRT_D_HI = 11.313708305358887f;
+constexpr float SQRT_D_LO = 1.936258797741175e-07f;
+constexpr float GRID_MAGIC = 12582912.0f;  // 1.5 * 2^23: fma(u, 31, M) puts RN(31u) in the low bits
+
+__device__ __forceinline__ int grid_cell(float v, float a, float bc)
+{
+    const float u = __saturatef(fmaf(v, a, bc));
+    return __float_as_int(fmaf(u, 31.0f, GRID_MAGIC));  // low 5 bits = cell; shuffles use only those
+}
+
+// Boundary count of v in one stage.  GRID: table lookup (exact count for the
+// fp32 v); otherwise a plain count over the boundaries.  `m` tracks the
+// distance to the nearest boundary that could be decisive.
+template <int BITS, bool GRID>
+__device__ __forceinline__ int stage_code(float v, float tb, int tc, const GridTable &t,
+                                          const float *b, float &m)
+{
+    if constexpr (GRID) {
+        const int g = grid_cell(v, t.a, t.bc);
+        const float bnd = __shfl_sync(FULL_MASK, tb, g);
+        const int cl = __shfl_sync(FULL_MASK, tc, g);
+        const float d = v - bnd;
+        m = fminf(m, fabsf(d));
+        return cl + (d > 0.0f ? 1 : 0);
+    } else {
+        int code = 0;
+#pragma unroll
+        for (int k = 0; k < (1 << BITS) - 1; ++k) {
+            const float d = v - b[k];
+            m = fminf(m, fabsf(d));
+            code += d > 0.0f ? 1 : 0;
+        }
+        return code;
+    }
+}
+
+// Exact boundary count of the double-float value (vh + vl).
+template <int BITS, bool GRID>
+__device__ __forceinline__ int stage_code_df(float vh, float vl, float tb, int tc,
+                                             const GridTable &t, const float *b)
+{
+    if constexpr (GRID) {
+        const int g = grid_cell(vh, t.a, t.bc);
+        const float bnd = __shfl_sync(FULL_MASK, tb, g);
+        const int cl = __shfl_sync(FULL_MASK, tc, g);
+        return cl + ((vh > bnd || (vh == bnd && vl > 0.0f)) ? 1 : 0);
+    } else {
+        int code = 0;
+#pragma unroll
+        for (int k = 0; k < (1 << BITS) - 1; ++k)
+            code += (vh > b[k] || (vh == b[k] && vl > 0.0f)) ? 1 : 0;
+        return code;
+    }
+}
+
+// Destination row of source row `row`; false if its batch offset is invalid.
+__device__ __forceinline__ bool rvq_dst_row(const RvqEncodeParams &p, int row, size_t &drow)
+{
+    const int bh = row / p.S;
+    const int s = row - bh * p.S;
+    int off = 0;
+    if (p.dst_off != nullptr) {
+        off = __ldg(p.dst_off + bh / p.H);
+        if (off < 0 || off > p.S_dst - p.S) {
+            atomicOr(&g_rvq_err, (unsigned)VQ_DEVERR_BAD_OFFSET);
+            return false;
+        }
+    }
+    drow = (size_t)bh * p.S_dst + off + s;
+    return true;
+}
+
+__device__ __forceinline__ void wht_lane_exact(float (&a)[4], int lane)
+{
+    // bits 0-1 of the coordinate index live in the register index
+    float t0 = a[0] + a[1], t1 = a[0] - a[1], t2 = a[2] + a[3], t3 = a[2] - a[3];
+    a[0] = t0 + t2; a[1] = t1 + t3; a[2] = t0 - t2; a[3] = t1 - t3;
+    // bits 2-6 live in the lane index
+#pragma unroll
+    for (int m = 1; m < 32; m <<= 1) {
+        const bool upper = (lane & m) != 0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float o = __shfl_xor_sync(FULL_MASK, a[j], m);
+            a[j] = upper ? (o - a[j]) : (a[j] + o);
+        }
+    }
+}
+
+// Whole-warp recompute of one row in exact / double-float arithmetic.
+// Lane l handles coordinates 4l..4l+3.
+//  * S = H x exactly: x is split into three pieces on power-of-two grids
+//    (q1 = 2^(e-15), q2 = 2^(e-32), the rest, e = exponent of max|x|) whose
+//    Hadamard sums all fit in 24 bits, so each piece's transform is exact in
+//    fp32 and S = S1 + S2 + S3 exactly.
+//  * Q = sum x^2 in double-float (squares of fp16 values are exact in fp32),
+//    n = sqrt(Q) and 1/(n sqrt(D)) in double-float.
+//  * y = S / (n sqrt(D)) in double-float (about 2^-44 relative), and each
+//    boundary count is taken on the double-float value.
+template <int BITS, bool GRID>
+__device__ __noinline__ void rvq_fixup_row(const RvqEncodeParams &p, const unsigned char *srow,
+                                           int row, int lane, float tb1, int tc1, float tb2,
+                                           int tc2, float tcen)
+{
+    constexpr int E = 32 / BITS;
+    constexpr int W = D * BITS / 32;
+    constexpr int LPW = E / 4;  // lanes per packed word
+    const uint2 raw = *reinterpret_cast<const uint2 *>(srow + 8 * lane);
+    const __half2 h01 = *reinterpret_cast<const __half2 *>(&raw.x);
+    const __half2 h23 = *reinterpret_cast<const __half2 *>(&raw.y);
+    float x[4] = {__low2float(h01), __high2float(h01), __low2float(h23), __high2float(h23)};
+
+    // row max |x| and sum of squares (double-float)
+    float amax = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+    float qh = x[0] * x[0], ql = 0.0f;
+#pragma unroll
+    for (int j = 1; j < 4; ++j) {
+        float s, e;
+        two_sum(qh, x[j] * x[j], s, e);
+        qh = s;
+        ql += e;
+    }
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) {
+        amax = fmaxf(amax, __shfl_xor_sync(FULL_MASK, amax, m));
+        const float oh = __shfl_xor_sync(FULL_MASK, qh, m);
+        const float ol = __shfl_xor_sync(FULL_MASK, ql, m);
+        float s, e;
+        two_sum(qh, oh, s, e);
+        e += ql + ol;
+        fast_two_sum(s, e, qh, ql);
+    }
+
+    // n = sqrt(Q), den = n sqrt(D), inv = 1/den, all double-float
+    float nh = 0.0f, nl = 0.0f, ih = 0.0f, il = 0.0f;
+    if (qh > 0.0f) {
+        nh = __fsqrt_rn(qh);
+        nl = __fdiv_rn(fmaf(-nh, nh, qh) + ql, 2.0f * nh);
+        const float ph = nh * SQRT_D_HI;
+        const float pl = fmaf(nh, SQRT_D_HI, -ph) + (nh * SQRT_D_LO + nl * SQRT_D_HI);
+        float dh, dl;
+        fast_two_sum(ph, pl, dh, dl);
+        ih = __fdiv_rn(1.0f, dh);
+        const float t = fmaf(-dh, ih, 1.0f) - dl * ih;
+        il = ih * t;
+    }
+
+    // exact S = H x by three exactly-transformable pieces
+    float s1[4], s2[4], s3[4];
+    if (amax > 0.0f) {
+        const int eM = ((__float_as_int(amax) >> 23) & 0xff) - 127;
+        const float q1 = __int_as_float((eM - 15 + 127) << 23);
+        const float iq1 = __int_as_float((15 - eM + 127) << 23);
+        const float q2 = __int_as_float((eM - 32 + 127) << 23);
+        const float iq2 = __int_as_float((32 - eM + 127) << 23);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float a = rintf(x[j] * iq1) * q1;
+            const float rem = x[j] - a;
+            const float b = rintf(rem * iq2) * q2;
+            s1[j] = a;
+            s2[j] = b;
+            s3[j] = rem - b;
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) s1[j] = s2[j] = s3[j] = 0.0f;
+    }
+    wht_lane_exact(s1, lane);
+    wht_lane_exact(s2, lane);
+    wht_lane_exact(s3, lane);
+
+    uint32_t part1 = 0, part2 = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        float a, e1, b, e2, sh, sl;
+        two_sum(s1[j], s2[j], a, e1);
+        two_sum(a, s3[j], b, e2);
+        fast_two_sum(b, e1 + e2, sh, sl);
+        // y = S * inv
+        const float yh0 = sh * ih;
+        const float yl0 = fmaf(sh, ih, -yh0) + (sh * il + sl * ih);
+        float yh, yl;
+        fast_two_sum(yh0, yl0, yh, yl);
+        const int code1 = stage_code_df<BITS, GRID>(yh, yl, tb1, tc1, p.t1, p.b1);
+        const float c = __shfl_sync(FULL_MASK, tcen, code1);
+        float rh, rl0, rh2, rl;
+        two_sum(yh, -c, rh, rl0);
+        fast_two_sum(rh, rl0 + yl, rh2, rl);
+        const int code2 = stage_code_df<BITS, GRID>(rh2, rl, tb2, tc2, p.t2, p.b2);
+        part1 |= (uint32_t)code1 << (j * BITS);
+        part2 |= (uint32_t)code2 << (j * BITS);
+    }
+    // assemble words: lanes [w*LPW, (w+1)*LPW) hold word w
+    const int sub = lane % LPW;
+    part1 <<= sub * 4 * BITS;
+    part2 <<= sub * 4 * BITS;
+#pragma unroll
+    for (int o = 1; o < LPW; o <<= 1) {
+        part1 |= __shfl_xor_sync(FULL_MASK, part1, o);
+        part2 |= __shfl_xor_sync(FULL_MASK, part2, o);
+    }
+    size_t drow;
+    if (rvq_dst_row(p, row, drow)) {
+        if (sub == 0 && lane / LPW < W) {
+            p.p1[drow * W + lane / LPW] = part1;
+            p.p2[drow * W + lane / LPW] = part2;
+        }
+        if (lane == 0) p.norms[drow] = __fadd_rn(nh, nl);
+    }
+}
+
+template <int BITS, bool GRID>
+__global__ void __launch_bounds__(ENC_WARPS * 32, 1)
+    rvq_encode_kernel(const __grid_constant__ RvqEncodeParams p)
+{
+    constexpr int L = 1 << BITS;
+    constexpr int E = 32 / BITS;
+    constexpr int W = D * BITS / 32;
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    unsigned char *wbuf = smem + warp * (ENC_STAGES * STAGE_BYTES);
+    uint64_t *bars =
+        reinterpret_cast<uint64_t *>(smem + ENC_WARPS * ENC_STAGES * STAGE_BYTES) + warp * ENC_STAGES;
+
+    if (lane == 0) {
+#pragma unroll
+        for (int s = 0; s < ENC_STAGES; ++s) mbar_init(&bars[s], 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+
+    const uint64_t pol = l2_policy_evict_first();
+    const float tb1 = p.t1.bnd[lane];
+    const int tc1 = p.t1.code[lane];
+    const float tb2 = p.t2.bnd[lane];
+    const int tc2 = p.t2.code[lane];
+    const float tcen = p.c1[lane & (L - 1)];
+    const int nblk = (p.N + 31) >> 5;
+    const int gw = blockIdx.x * ENC_WARPS + warp;
+    const int tw = gridDim.x * ENC_WARPS;
+    const __half *x = static_cast<const __half *>(p.x);
+
+    auto issue = [&](int blk, int s) {
+        const int r0 = blk << 5;
+        const int nrows = min(32, p.N - r0);
+        if (lane == 0) mbar_arrive_expect_tx(&bars[s], (uint32_t)(nrows * ROW_BYTES));
+        if (lane < nrows)
+            bulk_g2s(wbuf + s * STAGE_BYTES + lane * ROW_STRIDE, x + (size_t)(r0 + lane) * D,
+                     ROW_BYTES, &bars[s], pol);
+    };
+#pragma unroll
+    for (int s = 0; s < ENC_STAGES; ++s) {
+        const int blk = gw + s * tw;
+        if (blk < nblk) issue(blk, s);
+    }
+
+    for (int it = 0;; ++it) {
+        const int blk = gw + it * tw;
+        if (blk >= nblk) break;
+        const int s = it % ENC_STAGES;
+        const bool ok = mbar_wait_bounded(&bars[s], (uint32_t)(it / ENC_STAGES) & 1u);
+        if (!__all_sync(FULL_MASK, ok)) {
+            // A copy never landed: record it, wait (bounded) for the other
+            // copies this warp has in flight so none writes into a retired
+            // buffer, and stop.
+            if (lane == 0) atomicOr(&g_rvq_err, (unsigned)VQ_DEVERR_WAIT_TIMEOUT);
+            for (int k = 1; k < ENC_STAGES; ++k) {
+                const int it2 = it + k;
+                if (gw + it2 * tw < nblk)
+                    (void)mbar_wait_bounded(&bars[it2 % ENC_STAGES], (uint32_t)(it2 / ENC_STAGES) & 1u);
+            }
+            return;
+        }
+        const unsigned char *sbuf = wbuf + s * STAGE_BYTES;
+        const int row = (blk << 5) + lane;
+        const bool valid = row < p.N;
+
+        // ---- load the row: v[k] = (x[k], x[k + 64])
+        const uint4 *srow = reinterpret_cast<const uint4 *>(sbuf + lane * ROW_STRIDE);
+        float2 v[64];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            const uint4 lo = srow[c];
+            const uint4 hi = srow[c + 8];
+            const __half2 *hl = reinterpret_cast<const __half2 *>(&lo);
+            const __half2 *hh = reinterpret_cast<const __half2 *>(&hi);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float2 a = __half22float2(hl[j]);
+                const float2 b = __half22float2(hh[j]);
+                v[8 * c + 2 * j] = make_float2(a.x, b.x);
+                v[8 * c + 2 * j + 1] = make_float2(a.y, b.y);
+            }
+        }
+
+        // ---- norm (16 partial sums) and 1/(n sqrt(D))
+        float2 acc[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = make_float2(0.0f, 0.0f);
+#pragma unroll
+        for (int k = 0; k < 64; ++k) acc[k & 7] = __ffma2_rn(v[k], v[k], acc[k & 7]);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[i] = __fadd2_rn(acc[i], acc[i + 4]);
+        acc[0] = __fadd2_rn(acc[0], acc[2]);
+        acc[1] = __fadd2_rn(acc[1], acc[3]);
+        acc[0] = __fadd2_rn(acc[0], acc[1]);
+        const float q = acc[0].x + acc[0].y;
+        const float n = __fsqrt_rn(q);
+        const float inv = q > 0.0f ? __frcp_rn(n * SQRT_D_HI) : 0.0f;
+        const float2 inv2 = make_float2(inv, inv);
+#pragma unroll
+        for (int k = 0; k < 64; ++k) v[k] = __fmul2_rn(v[k], inv2);
+
+        // ---- Walsh-Hadamard: index bits 0-5 across the float2 array, bit 6 inside
+        const float2 neg1 = make_float2(-1.0f, -1.0f);
+#pragma unroll
+        for (int h = 1; h < 64; h <<= 1) {
+#pragma unroll
+            for (int k = 0; k < 64; ++k) {
+                if ((k & h) == 0) {
+                    const float2 a = v[k], b = v[k + h];
+                    v[k] = __fadd2_rn(a, b);
+                    v[k + h] = __ffma2_rn(b, neg1, a);
+                }
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < 64; ++k) {
+            const float a = v[k].x, b = v[k].y;
+            v[k] = make_float2(a + b, a - b);
+        }
+
+        // ---- two-stage boundary count and LSB-first packing
+        uint32_t w1[W], w2[W];
+#pragma unroll
+        for (int i = 0; i < W; ++i) w1[i] = w2[i] = 0u;
+        float m = __int_as_float(0x7f800000);
+#pragma unroll
+        for (int e = 0; e < D; ++e) {
+            const float y = e < 64 ? v[e].x : v[e - 64].y;
+            const int code1 = stage_code<BITS, GRID>(y, tb1, tc1, p.t1, p.b1, m);
+            const float r = y - __shfl_sync(FULL_MASK, tcen, code1);
+            const int code2 = stage_code<BITS, GRID>(r, tb2, tc2, p.t2, p.b2, m);
+            w1[e / E] = __funnelshift_r(w1[e / E], (uint32_t)code1, BITS);
+            w2[e / E] = __funnelshift_r(w2[e / E], (uint32_t)code2, BITS);
+        }
+        const bool flag = valid && !(m >= p.guard);
+
+        if (valid && !flag) {
+            size_t drow;
+            if (rvq_dst_row(p, row, drow)) {
+                uint4 *d1 = reinterpret_cast<uint4 *>(p.p1 + drow * W);
+                uint4 *d2 = reinterpret_cast<uint4 *>(p.p2 + drow * W);
+#pragma unroll
+                for (int i = 0; i < W / 4; ++i) {
+                    d1[i] = make_uint4(w1[4 * i], w1[4 * i + 1], w1[4 * i + 2], w1[4 * i + 3]);
+                    d2[i] = make_uint4(w2[4 * i], w2[4 * i + 1], w2[4 * i + 2], w2[4 * i + 3]);
+                }
+                p.norms[drow] = n;
+            }
+        }
+
+        // ---- rows with a value inside the guard band: exact recompute by the warp
+        unsigned fl = __ballot_sync(FULL_MASK, flag);
+        while (fl) {
+            const int r = __ffs(fl) - 1;
+            fl &= fl - 1;
+            rvq_fixup_row<BITS, GRID>(p, sbuf + r * ROW_STRIDE, (blk << 5) + r, lane, tb1, tc1,
+                                      tb2, tc2, tcen);
+        }
+
+        // ---- recycle this stage for the tile ENC_STAGES iterations ahead
+        __syncwarp();
+        fence_proxy_async_smem();
+        const int nb = blk + ENC_STAGES * tw;
+        if (nb < nblk) issue(nb, s);
+    }
+}
+
+// ---------------------------------------------------------------- decode
+//
+// x_hat = n * H (c1[i1] + c2[i2]) / sqrt(D): one row per thread; centroid
+// lookups are warp shuffles from tables replicated every 2^BITS lanes, so the
+// shuffle index can be the packed word shifted right (its low 5 bits).
+constexpr int DEC_THREADS = 128;
+
+template <int BITS>
+__global__ void __launch_bounds__(DEC_THREADS) rvq_decode_kernel(const __grid_constant__ RvqDecodeParams p)
+{
+    constexpr int L = 1 << BITS;
+    constexpr int E = 32 / BITS;
+    constexpr int W = D * BITS / 32;
+    const int lane = threadIdx.x & 31;
+    const float tc1 = p.c1[lane & (L - 1)];
+    const float tc2 = p.c2[lane & (L - 1)];
+    const int nblk = (p.N + 31) >> 5;
+    const int wpb = DEC_THREADS / 32;
+    const float2 neg1 = make_float2(-1.0f, -1.0f);
+    for (int blk = blockIdx.x * wpb + (threadIdx.x >> 5); blk < nblk; blk += gridDim.x * wpb) {
+        const int row = (blk << 5) + lane;
+        const bool valid = row < p.N;
+        uint32_t w1[W], w2[W];
+        float n = 0.0f;
+        if (valid) {
+            const uint4 *s1 = reinterpret_cast<const uint4 *>(p.p1 + (size_t)row * W);
+            const uint4 *s2 = reinterpret_cast<const uint4 *>(p.p2 + (size_t)row * W);
+#pragma unroll
+            for (int i = 0; i < W / 4; ++i) {
+                const uint4 a = __ldg(s1 + i), b = __ldg(s2 + i);
+                w1[4 * i] = a.x; w1[4 * i + 1] = a.y; w1[4 * i + 2] = a.z; w1[4 * i + 3] = a.w;
+                w2[4 * i] = b.x; w2[4 * i + 1] = b.y; w2[4 * i + 2] = b.z; w2[4 * i + 3] = b.w;
+            }
+            n = __ldg(p.norms + row);
+        } else {
+#pragma unroll
+            for (int i = 0; i < W; ++i) w1[i] = w2[i] = 0u;
+        }
+        float2 v[64];
+#pragma unroll
+        for (int e = 0; e < D; ++e) {
+            const int sh = (e % E) * BITS;
+            const float c = __shfl_sync(FULL_MASK, tc1, (int)(w1[e / E] >> sh)) +
+                            __shfl_sync(FULL_MASK, tc2, (int)(w2[e / E] >> sh));
+            if (e < 64) v[e].x = c; else v[e - 64].y = c;
+        }
+#pragma unroll
+        for (int h = 1; h < 64; h <<= 1) {
+#pragma unroll
+            for (int k = 0; k < 64; ++k) {
+                if ((k & h) == 0) {
+                    const float2 a = v[k], b = v[k + h];
+                    v[k] = __fadd2_rn(a, b);
+                    v[k + h] = __ffma2_rn(b, neg1, a);
+                }
+            }
+        }
+        const float sc = __fdiv_rn(n, SQRT_D_HI);
+#pragma unroll
+        for (int k = 0; k < 64; ++k) {
+            const float a = v[k].x, b = v[k].y;
+            v[k] = make_float2((a + b) * sc, (a - b) * sc);
+        }
+        if (valid) {
+            uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__half *>(p.out) + (size_t)row * D);
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                uint32_t lo[4], hi[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const __half2 a = __floats2half2_rn(v[8 * c + 2 * j].x, v[8 * c + 2 * j + 1].x);
+                    const __half2 b = __floats2half2_rn(v[8 * c + 2 * j].y, v[8 * c + 2 * j + 1].y);
+                    lo[j] = *reinterpret_cast<const uint32_t *>(&a);
+                    hi[j] = *reinterpret_cast<const uint32_t *>(&b);
+                }
+                dst[c] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                dst[c + 8] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            }
+        }
+    }
+}
+
+template <int BITS, bool GRID>
+cudaError_t launch_enc(const RvqEncodeParams &p, cudaStream_t stream)
+{
+    auto kern = rvq_encode_kernel<BITS, GRID>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, ENC_SMEM);
+    if (e != cudaSuccess) return e;
+    const int nblk = (p.N + 31) / 32;
+    int grid = (nblk + ENC_WARPS - 1) / ENC_WARPS;
+    const int sms = sm_count();
+    if (grid > sms) grid = sms;
+    if (grid < 1) grid = 1;
+    kern<<<grid, ENC_WARPS * 32, ENC_SMEM, stream>>>(p);
+    return cudaGetLastError();
+}
+
+template <int BITS>
+cudaError_t launch_dec(const RvqDecodeParams &p, cudaStream_t stream)
+{
+    const int nblk = (p.N + 31) / 32;
+    int grid = (nblk + DEC_THREADS / 32 - 1) / (DEC_THREADS / 32);
+    const int cap = sm_count() * 8;
+    if (grid > cap) grid = cap;
+    if (grid < 1) grid = 1;
+    rvq_decode_kernel<BITS><<<grid, DEC_THREADS, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_rvq_encode(const RvqEncodeParams &p, int bits, bool use_grid, cudaStream_t stream)
+{
+    if (p.N <= 0) return cudaSuccess;
+    switch (bits) {
+    case 1: return use_grid ? launch_enc<1, true>(p, stream) : launch_enc<1, false>(p, stream);
+    case 2: return use_grid ? launch_enc<2, true>(p, stream) : launch_enc<2, false>(p, stream);
+    case 4: return use_grid ? launch_enc<4, true>(p, stream) : launch_enc<4, false>(p, stream);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_rvq_decode(const RvqDecodeParams &p, int bits, cudaStream_t stream)
+{
+    if (p.N <= 0) return cudaSuccess;
+    switch (bits) {
+    case 1: return launch_dec<1>(p, stream);
+    case 2: return launch_dec<2>(p, stream);
+    case 4: return launch_dec<4>(p, stream);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t rvq_take_device_error(unsigned *bits, cudaStream_t stream)
+{
+    unsigned zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbolAsync(bits, g_rvq_err, sizeof(unsigned), 0,
+                                              cudaMemcpyDeviceToHost, stream);
+    if (e != cudaSuccess) return e;
+    e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return e;
+    if (*bits) e = cudaMemcpyToSymbolAsync(g_rvq_err, &zero, sizeof(unsigned), 0,
+                                           cudaMemcpyHostToDevice, stream);
+    if (e != cudaSuccess) return e;
+    return cudaStreamSynchronize(stream);
+}
+
+}  // namespace vq
