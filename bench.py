@@ -82,7 +82,7 @@ def describe(name):
     }[name]
 
 
-def build_workload(name, dev, rank=0):
+def build_workload(name, dev, rank=0, layers=None):
     """Device buffers and the op list for one step; also host inputs for e2e."""
     import torch
     from kv_cache_quantization_turboquantrvq_gb300 import api, synth
@@ -159,7 +159,7 @@ def build_workload(name, dev, rank=0):
         ops.sort(key=lambda o: order.index(o.name))
     elif name == "c3":
         cfg = cfgs["c3_rvq_b4_32L_8k"]
-        for layer in range(cfg["layers"]):
+        for layer in range(cfg["layers"] if layers is None else layers):
             k_np = synth.keys_for(cfg, layer=layer)
             k = t(k_np)
             inputs.append((k_np, k))
@@ -360,6 +360,8 @@ def main():
     ap.add_argument("--workload", choices=("c5", "c3", "c2", "c1", "c4"), default="c5")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--layers", type=int, default=None,
+                    help="c3 only: number of layers (default 32; fewer for small profiling runs)")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -384,7 +386,7 @@ def main():
     build.build()
     api.lib()  # fails loudly if the CUDA library is missing
 
-    ops, inputs, results = build_workload(args.workload, dev, rank)
+    ops, inputs, results = build_workload(args.workload, dev, rank, layers=args.layers)
     stream = torch.cuda.current_stream()
     K, W = args.steps, max(args.warmup, 3)
 

@@ -50,81 +50,6 @@ bool valid_codebook(const float *c, const float *b, int L)
     return true;
 }
 
-// ---------------------------------------------------------------- grid tables
-// Host copy of the device cell map (two correctly rounded fp32 FMAs and a
-// saturation), so the host knows exactly which fp32 values share a cell.
-int cell_of(float v, float a, float bc)
-{
-    float u = std::fmaf(v, a, bc);
-    if (!(u > 0.0f)) u = 0.0f;  // also NaN -> 0, as the device saturation
-    if (u > 1.0f) u = 1.0f;
-    const float gf = std::fmaf(u, 31.0f, 12582912.0f);
-    uint32_t bits;
-    std::memcpy(&bits, &gf, 4);
-    return (int)(bits & 31u);
-}
-
-int32_t ordered(float f)
-{
-    int32_t i;
-    std::memcpy(&i, &f, 4);
-    return i >= 0 ? i : (int32_t)(0x80000000u - (uint32_t)i);
-}
-
-float from_ordered(int32_t o)
-{
-    const int32_t i = o >= 0 ? o : (int32_t)(0x80000000u - (uint32_t)o);
-    float f;
-    std::memcpy(&f, &i, 4);
-    return f;
-}
-
-// Smallest finite float v with cell_of(v) >= g (the map is monotone in v).
-double cell_lower_edge(int g, float a, float bc)
-{
-    if (g <= 0) return -INFINITY;
-    int32_t lo = ordered(-3.0e38f), hi = ordered(3.0e38f);
-    if (cell_of(from_ordered(hi), a, bc) < g) return INFINITY;
-    while (lo < hi) {
-        const int32_t mid = lo + (hi - lo) / 2;
-        if (cell_of(from_ordered(mid), a, bc) >= g) hi = mid;
-        else lo = mid + 1;
-    }
-    return (double)from_ordered(lo);
-}
-
-bool build_grid(const float *b, int nb, float guard, GridTable &t)
-{
-    const double span = nb > 1 ? (double)b[nb - 1] - (double)b[0] : std::fmax(std::fabs((double)b[0]), 1e-3);
-    for (int trial = 0; trial < 96; ++trial) {
-        const double pad = span * (0.5 / 31.0 + 0.0071 * trial);
-        const double width = (nb > 1 ? span : 0.0) + 2.0 * pad;
-        t.a = (float)(1.0 / width);
-        t.bc = (float)(-((double)b[0] - pad) / width);
-        int cell[16];
-        bool ok = true;
-        for (int k = 0; k < nb && ok; ++k) {
-            cell[k] = cell_of(b[k], t.a, t.bc);
-            if (k > 0 && cell[k] <= cell[k - 1]) ok = false;
-        }
-        for (int k = 0; k < nb && ok; ++k) {
-            const double lo = cell_lower_edge(cell[k], t.a, t.bc);
-            const double hi = cell[k] == 31 ? INFINITY : cell_lower_edge(cell[k] + 1, t.a, t.bc);
-            if (!((double)b[k] - lo >= guard) || !(hi - (double)b[k] > guard)) ok = false;
-        }
-        if (!ok) continue;
-        int k = 0;
-        for (int g = 0; g < 32; ++g) {
-            while (k < nb && cell[k] < g) ++k;
-            const bool has = k < nb && cell[k] == g;
-            t.bnd[g] = has ? b[k] : -INFINITY;
-            t.code[g] = has ? k : k - 1;
-        }
-        return true;
-    }
-    return false;
-}
-
 vq_status cuda_status(cudaError_t e) { return e == cudaSuccess ? VQ_OK : VQ_ERR_CUDA; }
 
 }  // namespace

@@ -108,18 +108,20 @@ __device__ __noinline__ uint32_t exact_code_slow(float x, float mn, float mx)
     return (uint32_t)q;
 }
 
-// Fast code of one element; falls back to the exact path near a half-integer.
+// Fast code of one element (low BITS bits of the result).  `near` is set when
+// the fp32 t lies within its error bound of a half-integer; the caller then
+// recomputes that group with exact_code_slow.  No branch here, so the fast
+// path of a whole group schedules as straight-line code.
 template <int BITS>
-__device__ __forceinline__ uint32_t code_of(float x, const GroupQ &g, float mx)
+__device__ __forceinline__ uint32_t code_fast(float x, const GroupQ &g, bool &near)
 {
     constexpr float C = (float)((1 << BITS) - 1);
     constexpr float EPS = 8.0f * C * 5.9604645e-08f;  // 8 ulp(1) * (2^b - 1)
     const float t = (x - g.mn) * g.f;
     const float tm = t + MAGIC;
     const float frac = t - (tm - MAGIC);
-    uint32_t q = (uint32_t)__float_as_int(tm) & ((1u << BITS) - 1u);
-    if (fabsf(frac) > 0.5f - EPS) q = exact_code_slow<BITS>(x, g.mn, mx);
-    return q;
+    near |= fabsf(frac) > 0.5f - EPS;
+    return (uint32_t)__float_as_int(tm);
 }
 
 // fp16(q*s + z) rounded once from the exact value: q*s is exact in fp32, the
@@ -137,6 +139,25 @@ __device__ __forceinline__ __half recon_exact(uint32_t q, float s, float z)
         sum = __uint_as_float(b);
     }
     return __float2half_rn(sum);
+}
+
+// True when q*s + z is exact in fp32 for every q in [0, C]: the sum then
+// needs no more than 24 significant bits.  s and z are fp16 values; their
+// quanta are ulp16 (2^-24 for subnormals).
+__device__ __forceinline__ float ulp16_of(float x)
+{
+    int e = ((__float_as_int(x) >> 23) & 0xff) - 127;
+    e = e < -14 ? -14 : e;
+    return __int_as_float((e - 10 + 127) << 23);
+}
+
+template <int BITS>
+__device__ __forceinline__ bool group_sum_exact(float s, float z)
+{
+    constexpr float C = (float)((1 << BITS) - 1);
+    if (s == 0.0f || z == 0.0f) return true;
+    const float q = fminf(ulp16_of(s), ulp16_of(z));
+    return fabsf(z) + C * s < 8388608.0f * q;  // 2^23 quanta: one bit of headroom
 }
 
 // ------------------------------------------------------------ values (per token)
@@ -247,12 +268,22 @@ __global__ void __launch_bounds__(VAL_WARPS * 32, 1)
             const float mx = fmaxf(__low2float(hi), __high2float(hi));
             const GroupQ g = group_setup<BITS>(mn, mx);
             sz[j] = __halves2half2(g.scale_h, g.zero_h);
+            bool near = false;
 #pragma unroll
             for (int i = 0; i < P; ++i) {
                 const float2 v = __half22float2(h[j * P + i]);
                 const int e = j * G + 2 * i;
-                words[e / E] = __funnelshift_r(words[e / E], code_of<BITS>(v.x, g, mx), BITS);
-                words[(e + 1) / E] = __funnelshift_r(words[(e + 1) / E], code_of<BITS>(v.y, g, mx), BITS);
+                words[e / E] = __funnelshift_r(words[e / E], code_fast<BITS>(v.x, g, near), BITS);
+                words[(e + 1) / E] = __funnelshift_r(words[(e + 1) / E], code_fast<BITS>(v.y, g, near), BITS);
+            }
+            if (near) {  // rare: some t of this group is within rounding of a half-integer
+#pragma unroll
+                for (int i = 0; i < P; ++i) {
+                    const float2 v = __half22float2(h[j * P + i]);
+                    const int e = j * G + 2 * i;
+                    words[e / E] = __funnelshift_r(words[e / E], exact_code_slow<BITS>(v.x, mn, mx), BITS);
+                    words[(e + 1) / E] = __funnelshift_r(words[(e + 1) / E], exact_code_slow<BITS>(v.y, mn, mx), BITS);
+                }
             }
         }
         const int bh = row / p.S_q, s_ = row - bh * p.S_q;
@@ -388,6 +419,7 @@ __global__ void __launch_bounds__(key_warps<G>() * 32, 1)
         gq[3] = group_setup<BITS>(__high2float(lo1), mxv[3]);
         // pass 2: codes, packed along tokens (token i -> word i/E, shift (i%E)*BITS)
         uint32_t w[WG][4];
+        bool near[4] = {false, false, false, false};
 #pragma unroll
         for (int k = 0; k < WG; ++k) {
             w[k][0] = w[k][1] = w[k][2] = w[k][3] = 0u;
@@ -399,15 +431,35 @@ __global__ void __launch_bounds__(key_warps<G>() * 32, 1)
                     uint2 r = col[i * (ROW_BYTES / 8)];
                     const float2 a = __half22float2(*reinterpret_cast<__half2 *>(&r.x));
                     const float2 b = __half22float2(*reinterpret_cast<__half2 *>(&r.y));
-                    c0 = code_of<BITS>(a.x, gq[0], mxv[0]);
-                    c1 = code_of<BITS>(a.y, gq[1], mxv[1]);
-                    c2 = code_of<BITS>(b.x, gq[2], mxv[2]);
-                    c3 = code_of<BITS>(b.y, gq[3], mxv[3]);
+                    c0 = code_fast<BITS>(a.x, gq[0], near[0]);
+                    c1 = code_fast<BITS>(a.y, gq[1], near[1]);
+                    c2 = code_fast<BITS>(b.x, gq[2], near[2]);
+                    c3 = code_fast<BITS>(b.y, gq[3], near[3]);
                 }
                 w[k][0] = __funnelshift_r(w[k][0], c0, BITS);
                 w[k][1] = __funnelshift_r(w[k][1], c1, BITS);
                 w[k][2] = __funnelshift_r(w[k][2], c2, BITS);
                 w[k][3] = __funnelshift_r(w[k][3], c3, BITS);
+            }
+        }
+        // rare: a channel with a t within rounding of a half-integer is redone exactly
+        const __half *tokh = reinterpret_cast<const __half *>(tb);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            if (!near[c]) continue;
+            const float mn = gq[c].mn;
+            for (int k = 0; k < WG; ++k) {
+                uint32_t word = 0u;
+                for (int j = 0; j < E; ++j) {
+                    const int i = k * E + j;
+                    const uint32_t q = i < ntok ? exact_code_slow<BITS>(
+                        __half2float(tokh[i * D + 4 * lane + c]), mn, mxv[c]) : 0u;
+                    word |= q << (j * BITS);
+                }
+                if (c == 0) w[k][0] = word;
+                if (c == 1) w[k][1] = word;
+                if (c == 2) w[k][2] = word;
+                if (c == 3) w[k][3] = word;
             }
         }
         // the tile is consumed: recycle the stage
@@ -453,6 +505,14 @@ __global__ void __launch_bounds__(DQ_THREADS) kivi_values_dequant_kernel(const _
         for (int i = 0; i < W; ++i) words[i] = __ldg(p.packed + (size_t)row * W + i);
         const __half *sc = static_cast<const __half *>(p.scale) + (size_t)row * NGD;
         const __half *zr = static_cast<const __half *>(p.zero) + (size_t)row * NGD;
+        float sf[NGD], zf[NGD];
+        bool exact[NGD];
+#pragma unroll
+        for (int j = 0; j < NGD; ++j) {
+            sf[j] = __half2float(sc[j]);
+            zf[j] = __half2float(zr[j]);
+            exact[j] = group_sum_exact<BITS>(sf[j], zf[j]);
+        }
         uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__half *>(p.out) + (size_t)row * D);
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
@@ -460,10 +520,15 @@ __global__ void __launch_bounds__(DQ_THREADS) kivi_values_dequant_kernel(const _
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const int e = 8 * c + 2 * j;
-                const float s = __half2float(sc[e / G]), z = __half2float(zr[e / G]);
+                const float s = sf[e / G], z = zf[e / G];
                 const uint32_t q0 = (words[e / E] >> ((e % E) * BITS)) & MASK;
                 const uint32_t q1 = (words[(e + 1) / E] >> (((e + 1) % E) * BITS)) & MASK;
-                const __half2 hv = __halves2half2(recon_exact(q0, s, z), recon_exact(q1, s, z));
+                __half2 hv;
+                if (exact[e / G]) {
+                    hv = __floats2half2_rn(fmaf((float)q0, s, z), fmaf((float)q1, s, z));
+                } else {
+                    hv = __halves2half2(recon_exact(q0, s, z), recon_exact(q1, s, z));
+                }
                 out[j] = *reinterpret_cast<const uint32_t *>(&hv);
             }
             dst[c] = make_uint4(out[0], out[1], out[2], out[3]);
@@ -488,8 +553,13 @@ __global__ void __launch_bounds__(DQ_THREADS) kivi_keys_dequant_kernel(const __g
         const __half *sh = reinterpret_cast<const __half *>(&sraw);
         const __half *zh = reinterpret_cast<const __half *>(&zraw);
         float s[4], z[4];
+        bool all_exact = true;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) { s[j] = __half2float(sh[j]); z[j] = __half2float(zh[j]); }
+        for (int j = 0; j < 4; ++j) {
+            s[j] = __half2float(sh[j]);
+            z[j] = __half2float(zh[j]);
+            all_exact &= group_sum_exact<BITS>(s[j], z[j]);
+        }
         for (int k = 0; k < WG; ++k) {
             const uint4 wv = __ldg(reinterpret_cast<const uint4 *>(p.packed + ((size_t)tile * WG + k) * D + 4 * lane));
             const uint32_t wk[4] = {wv.x, wv.y, wv.z, wv.w};
@@ -498,8 +568,14 @@ __global__ void __launch_bounds__(DQ_THREADS) kivi_keys_dequant_kernel(const __g
                 const int i = k * E + j;
                 if (i >= ntok) break;
                 __half o[4];
+                if (all_exact) {
 #pragma unroll
-                for (int c = 0; c < 4; ++c) o[c] = recon_exact((wk[c] >> (j * BITS)) & MASK, s[c], z[c]);
+                    for (int c = 0; c < 4; ++c)
+                        o[c] = __float2half_rn(fmaf((float)((wk[c] >> (j * BITS)) & MASK), s[c], z[c]));
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) o[c] = recon_exact((wk[c] >> (j * BITS)) & MASK, s[c], z[c]);
+                }
                 const __half2 a = __halves2half2(o[0], o[1]), b = __halves2half2(o[2], o[3]);
                 *reinterpret_cast<uint2 *>(static_cast<__half *>(p.out) + ((size_t)bh * p.S_q + g * G + i) * D + 4 * lane) =
                     make_uint2(*reinterpret_cast<const uint32_t *>(&a), *reinterpret_cast<const uint32_t *>(&b));

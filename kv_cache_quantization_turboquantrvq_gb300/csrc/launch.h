@@ -67,6 +67,11 @@ cudaError_t launch_kivi_dequant(const KiviDequantParams &p, int bits, bool per_c
 cudaError_t rvq_take_device_error(unsigned *bits, cudaStream_t stream);
 cudaError_t kivi_take_device_error(unsigned *bits, cudaStream_t stream);
 
+// Host side of the cell map (bit-exact copy of the device's) and the table
+// builder; build_grid returns false when no table meets the guard band.
+int grid_cell_host(float v, float a, float bc);
+bool build_grid(const float *b, int nb, float guard, GridTable &t);
+
 // Number of SMs of the current device (cached per device).
 int sm_count();
 

@@ -70,8 +70,10 @@ __device__ __forceinline__ int stage_code(float v, float tb, int tc, const GridT
         m = fminf(m, fabsf(d));
         return cl + (d > 0.0f ? 1 : 0);
     } else {
+        // fallback for codebooks without a grid table: a plain loop over the
+        // boundaries (uniform across the warp), kept rolled to bound code size
         int code = 0;
-#pragma unroll
+#pragma unroll 1
         for (int k = 0; k < (1 << BITS) - 1; ++k) {
             const float d = v - b[k];
             m = fminf(m, fabsf(d));
@@ -93,7 +95,7 @@ __device__ __forceinline__ int stage_code_df(float vh, float vl, float tb, int t
         return cl + ((vh > bnd || (vh == bnd && vl > 0.0f)) ? 1 : 0);
     } else {
         int code = 0;
-#pragma unroll
+#pragma unroll 1
         for (int k = 0; k < (1 << BITS) - 1; ++k)
             code += (vh > b[k] || (vh == b[k] && vl > 0.0f)) ? 1 : 0;
         return code;

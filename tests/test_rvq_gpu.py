@@ -100,6 +100,22 @@ def test_encode_custom_codebook_boundary_at_rotated_value(vq, oracle_mod):
     assert np.array_equal(g1[0], ora["idx1"][0])
 
 
+@pytest.mark.parametrize("bits", [2, 4])
+def test_encode_plain_count_fallback(vq, oracle_mod, bits):
+    """A codebook with two boundaries inside one guard band has no lookup
+    table; the encoder then counts boundaries one by one."""
+    c1, b1, c2, b2 = [a.copy() for a in oracle_mod.rvq_codebooks(D, bits)[:4]]
+    L = 1 << bits
+    mid = L // 2
+    b1[mid] = np.float32(1e-7)   # 1e-7 above the middle boundary b1[mid - 1] = 0
+    c1[mid] = np.float32(5e-8)   # keep the centroid between its two boundaries
+    assert np.all(c1[:-1] < b1) and np.all(b1 < c1[1:])
+    x = _rows((1, 2, 300), 91 + bits)
+    p1, p2, n = _encode(vq, x, bits, (c1, b1, c2, b2))
+    ora = oracle_mod.rvq_encode(x.reshape(-1, D), bits, c1, b1, c2, b2)
+    check_rvq(p1, p2, n, ora, bits)
+
+
 def test_encode_dst_offsets(vq, oracle_mod):
     bits = 2
     cb = oracle_mod.rvq_codebooks(D, bits)[:4]
@@ -157,7 +173,8 @@ def test_decode_parity(vq, oracle_mod, bits):
     got = out.cpu().numpy().reshape(-1, D).astype(np.float64)
     n = ora["norms"].astype(np.float64)[:, None]
     assert np.all(np.abs(got - ref64) <= 1e-3 * n + 1e-30)
-    assert np.mean(got == ref.astype(np.float64)) > 0.99
+    # fp32 arithmetic: most outputs also round to the same fp16 as binary64
+    assert np.mean(got == ref.astype(np.float64)) > 0.95
 
 
 def test_c1_full_parity_and_roundtrip(vq, oracle_mod):
