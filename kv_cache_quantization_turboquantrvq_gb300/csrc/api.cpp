@@ -289,7 +289,7 @@ vq_status vq_kivi_unpack_dequant(const uint32_t *k_packed, const void *k_scale, 
     if ((long long)B * H * S_q == 0) return VQ_OK;
     if ((dk && (!aligned(k_packed, 16) || !aligned(k_scale, 8) || !aligned(k_zero, 8) ||
                 !aligned(k_out_f16, 8))) ||
-        (dv && (!aligned(v_packed, 4) || !aligned(v_scale, 2) || !aligned(v_zero, 2) ||
+        (dv && (!aligned(v_packed, 16) || !aligned(v_scale, 2) || !aligned(v_zero, 2) ||
                 !aligned(v_out_f16, 16))))
         return VQ_ERR_MISALIGNED;
     const int NG = (S_q + group - 1) / group;

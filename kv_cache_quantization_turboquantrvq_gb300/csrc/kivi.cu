@@ -161,13 +161,27 @@ __device__ __forceinline__ bool group_sum_exact(float s, float z)
 }
 
 // ------------------------------------------------------------ values (per token)
+//
+// One row per thread, 32-row blocks per warp.  Rows arrive by per-row bulk
+// copies (rows skip the residual window, so a block need not be contiguous)
+// into a 3-stage ring at a 272-byte stride.  Per group: fp16 min/max, then a
+// rolled loop over the group's output words; words and (scale, zero) are
+// staged in shared memory and written out coalesced.
 
 constexpr int VAL_WARPS = 8;
 constexpr int VAL_STAGES = 3;
 constexpr int ROW_BYTES = D * 2;
 constexpr int ROW_STRIDE = ROW_BYTES + 16;
 constexpr int VSTAGE_BYTES = 32 * ROW_STRIDE;
-constexpr int VAL_SMEM = VAL_WARPS * VAL_STAGES * VSTAGE_BYTES + VAL_WARPS * VAL_STAGES * 8;
+__host__ __device__ constexpr int val_words(int bits) { return D * bits / 32; }
+__host__ __device__ constexpr int val_warp_bytes(int bits, int G)
+{
+    return VAL_STAGES * VSTAGE_BYTES + 32 * (val_words(bits) + 1) * 4 + 32 * (D / G) * 4;
+}
+__host__ __device__ constexpr int val_smem(int bits, int G)
+{
+    return VAL_WARPS * (val_warp_bytes(bits, G) + VAL_STAGES * 8);
+}
 
 __device__ __forceinline__ bool kivi_off(const KiviQuantParams &p, int b, int &off)
 {
@@ -181,6 +195,8 @@ __device__ __forceinline__ bool kivi_off(const KiviQuantParams &p, int b, int &o
     return true;
 }
 
+__device__ __forceinline__ uint32_t h2bits(__half h) { return (uint32_t)__half_as_ushort(h); }
+
 template <int BITS, int G>
 __global__ void __launch_bounds__(VAL_WARPS * 32, 1)
     kivi_values_kernel(const __grid_constant__ KiviQuantParams p)
@@ -188,12 +204,15 @@ __global__ void __launch_bounds__(VAL_WARPS * 32, 1)
     constexpr int E = 32 / BITS;
     constexpr int W = D * BITS / 32;
     constexpr int NGD = D / G;
+    constexpr int WPG = G * BITS / 32;  // words per group
+    constexpr int WB = val_warp_bytes(BITS, G);
     extern __shared__ __align__(128) unsigned char smem[];
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    unsigned char *wbuf = smem + warp * (VAL_STAGES * VSTAGE_BYTES);
-    uint64_t *bars =
-        reinterpret_cast<uint64_t *>(smem + VAL_WARPS * VAL_STAGES * VSTAGE_BYTES) + warp * VAL_STAGES;
+    unsigned char *wbuf = smem + warp * WB;
+    uint32_t *ow = reinterpret_cast<uint32_t *>(wbuf + VAL_STAGES * VSTAGE_BYTES);
+    uint32_t *osz = ow + 32 * (W + 1);  // scale | zero << 16, per row and group
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + VAL_WARPS * WB) + warp * VAL_STAGES;
     if (lane == 0) {
 #pragma unroll
         for (int s = 0; s < VAL_STAGES; ++s) mbar_init(&bars[s], 1);
@@ -238,79 +257,98 @@ __global__ void __launch_bounds__(VAL_WARPS * 32, 1)
             return;
         }
         const int row = (blk << 5) + lane;
-        const uint4 *srow = reinterpret_cast<const uint4 *>(wbuf + s * VSTAGE_BYTES + lane * ROW_STRIDE);
-        uint4 raw[16];
+        const __half *rh = reinterpret_cast<const __half *>(wbuf + s * VSTAGE_BYTES + lane * ROW_STRIDE);
+#pragma unroll 1
+        for (int j = 0; j < NGD; ++j) {
+            const uint4 *gp = reinterpret_cast<const uint4 *>(rh + j * G);
+            uint4 c0 = gp[0];
+            __half2 lo = __hmin2(__hmin2(*reinterpret_cast<__half2 *>(&c0.x), *reinterpret_cast<__half2 *>(&c0.y)),
+                                 __hmin2(*reinterpret_cast<__half2 *>(&c0.z), *reinterpret_cast<__half2 *>(&c0.w)));
+            __half2 hi = __hmax2(__hmax2(*reinterpret_cast<__half2 *>(&c0.x), *reinterpret_cast<__half2 *>(&c0.y)),
+                                 __hmax2(*reinterpret_cast<__half2 *>(&c0.z), *reinterpret_cast<__half2 *>(&c0.w)));
 #pragma unroll
-        for (int c = 0; c < 16; ++c) raw[c] = srow[c];
-        // recycle the stage as soon as the row is in registers
+            for (int i = 1; i < G / 8; ++i) {
+                uint4 c = gp[i];
+                lo = __hmin2(lo, __hmin2(__hmin2(*reinterpret_cast<__half2 *>(&c.x), *reinterpret_cast<__half2 *>(&c.y)),
+                                         __hmin2(*reinterpret_cast<__half2 *>(&c.z), *reinterpret_cast<__half2 *>(&c.w))));
+                hi = __hmax2(hi, __hmax2(__hmax2(*reinterpret_cast<__half2 *>(&c.x), *reinterpret_cast<__half2 *>(&c.y)),
+                                         __hmax2(*reinterpret_cast<__half2 *>(&c.z), *reinterpret_cast<__half2 *>(&c.w))));
+            }
+            const float mn = fminf(__low2float(lo), __high2float(lo));
+            const float mx = fmaxf(__low2float(hi), __high2float(hi));
+            const GroupQ g = group_setup<BITS>(mn, mx);
+            osz[lane * NGD + j] = h2bits(g.scale_h) | (h2bits(g.zero_h) << 16);
+#pragma unroll 1
+            for (int w = 0; w < WPG; ++w) {
+                const uint4 *wp = gp + w * (E / 8);
+                uint32_t word = 0u;
+                bool near = false;
+#pragma unroll
+                for (int i = 0; i < E / 8; ++i) {
+                    uint4 c = wp[i];
+                    const __half2 *hh = reinterpret_cast<const __half2 *>(&c);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const float2 v = __half22float2(hh[k]);
+                        word = __funnelshift_r(word, code_fast<BITS>(v.x, g, near), BITS);
+                        word = __funnelshift_r(word, code_fast<BITS>(v.y, g, near), BITS);
+                    }
+                }
+                if (near) {  // rare: a t within rounding of a half-integer
+                    word = 0u;
+                    for (int e = 0; e < E; ++e)
+                        word |= exact_code_slow<BITS>(__half2float(rh[j * G + w * E + e]), mn, mx) << (e * BITS);
+                }
+                ow[lane * (W + 1) + j * WPG + w] = word;
+            }
+        }
+        // the block is in registers / staging: recycle the stage
         __syncwarp();
         fence_proxy_async_smem();
         {
             const int nb = blk + VAL_STAGES * tw;
             if (nb < nblk) issue(nb, s);
         }
-        if (row >= N) continue;
-        const __half2 *h = reinterpret_cast<const __half2 *>(raw);  // 64 half2, channel pairs
-        uint32_t words[W];
+        // coalesced write-out
+        int dr32 = 0;
+        bool okrow = false;
+        if (row < N) {
+            const int bh = row / p.S_q, s_ = row - bh * p.S_q;
+            int off;
+            okrow = kivi_off(p, bh / p.H, off);
+            dr32 = bh * p.S_dst + off + s_;
+        }
 #pragma unroll
-        for (int i = 0; i < W; ++i) words[i] = 0u;
-        __half2 sz[NGD];  // (scale, zero) per group
+        for (int i = 0; i < W; ++i) {
+            const int idx = i * 32 + lane;
+            const int r = idx / W, w = idx % W;
+            const int dr = __shfl_sync(FULL_MASK, dr32, r);
+            if (__shfl_sync(FULL_MASK, okrow ? 1 : 0, r)) p.packed[(size_t)dr * W + w] = ow[r * (W + 1) + w];
+        }
+        __half *sc = static_cast<__half *>(p.scale);
+        __half *zr = static_cast<__half *>(p.zero);
 #pragma unroll
-        for (int j = 0; j < NGD; ++j) {
-            constexpr int P = G / 2;  // half2 per group
-            __half2 lo = h[j * P], hi = h[j * P];
-#pragma unroll
-            for (int i = 1; i < P; ++i) {
-                lo = __hmin2(lo, h[j * P + i]);
-                hi = __hmax2(hi, h[j * P + i]);
-            }
-            const float mn = fminf(__low2float(lo), __high2float(lo));
-            const float mx = fmaxf(__low2float(hi), __high2float(hi));
-            const GroupQ g = group_setup<BITS>(mn, mx);
-            sz[j] = __halves2half2(g.scale_h, g.zero_h);
-            bool near = false;
-#pragma unroll
-            for (int i = 0; i < P; ++i) {
-                const float2 v = __half22float2(h[j * P + i]);
-                const int e = j * G + 2 * i;
-                words[e / E] = __funnelshift_r(words[e / E], code_fast<BITS>(v.x, g, near), BITS);
-                words[(e + 1) / E] = __funnelshift_r(words[(e + 1) / E], code_fast<BITS>(v.y, g, near), BITS);
-            }
-            if (near) {  // rare: some t of this group is within rounding of a half-integer
-#pragma unroll
-                for (int i = 0; i < P; ++i) {
-                    const float2 v = __half22float2(h[j * P + i]);
-                    const int e = j * G + 2 * i;
-                    words[e / E] = __funnelshift_r(words[e / E], exact_code_slow<BITS>(v.x, mn, mx), BITS);
-                    words[(e + 1) / E] = __funnelshift_r(words[(e + 1) / E], exact_code_slow<BITS>(v.y, mn, mx), BITS);
-                }
+        for (int i = 0; i < NGD; ++i) {
+            const int idx = i * 32 + lane;
+            const int r = idx / NGD, j = idx % NGD;
+            const int dr = __shfl_sync(FULL_MASK, dr32, r);
+            if (__shfl_sync(FULL_MASK, okrow ? 1 : 0, r)) {
+                const uint32_t v = osz[r * NGD + j];
+                sc[(size_t)dr * NGD + j] = __ushort_as_half((unsigned short)(v & 0xffffu));
+                zr[(size_t)dr * NGD + j] = __ushort_as_half((unsigned short)(v >> 16));
             }
         }
-        const int bh = row / p.S_q, s_ = row - bh * p.S_q;
-        int off;
-        if (!kivi_off(p, bh / p.H, off)) continue;
-        const size_t drow = (size_t)bh * p.S_dst + off + s_;
-        uint32_t *dst = p.packed + drow * W;
-#pragma unroll
-        for (int i = 0; i < W; i += 4) {
-            if constexpr (W >= 4)
-                *reinterpret_cast<uint4 *>(dst + i) = make_uint4(words[i], words[i + 1], words[i + 2], words[i + 3]);
-        }
-        if constexpr (W < 4) {
-#pragma unroll
-            for (int i = 0; i < W; ++i) dst[i] = words[i];
-        }
-        __half *sc = static_cast<__half *>(p.scale) + drow * NGD;
-        __half *zr = static_cast<__half *>(p.zero) + drow * NGD;
-#pragma unroll
-        for (int j = 0; j < NGD; ++j) {
-            sc[j] = __low2half(sz[j]);
-            zr[j] = __high2half(sz[j]);
-        }
+        __syncwarp();
     }
 }
 
 // ------------------------------------------------------------ keys (per channel)
+//
+// One [G x 128] tile (contiguous in memory) per warp per step, one bulk copy;
+// lane l owns channels 4l..4l+3.  Pass 1: fp16 min/max down the tokens.
+// Pass 2: a rolled loop over the group's word rows; each step packs E tokens
+// of the lane's four channels into four words and stores them as one 16-byte
+// write (512 contiguous bytes per warp).
 
 constexpr int KEY_STAGES = 2;
 constexpr int KEY_SMEM_BUDGET = 192 * 1024;
@@ -395,21 +433,12 @@ __global__ void __launch_bounds__(key_warps<G>() * 32, 1)
         uint2 r0 = col[0];
         __half2 lo0 = *reinterpret_cast<__half2 *>(&r0.x), lo1 = *reinterpret_cast<__half2 *>(&r0.y);
         __half2 hi0 = lo0, hi1 = lo1;
-        if (ntok == G) {
 #pragma unroll 8
-            for (int i = 1; i < G; ++i) {
-                uint2 r = col[i * (ROW_BYTES / 8)];
-                const __half2 a = *reinterpret_cast<__half2 *>(&r.x), b = *reinterpret_cast<__half2 *>(&r.y);
-                lo0 = __hmin2(lo0, a); hi0 = __hmax2(hi0, a);
-                lo1 = __hmin2(lo1, b); hi1 = __hmax2(hi1, b);
-            }
-        } else {
-            for (int i = 1; i < ntok; ++i) {
-                uint2 r = col[i * (ROW_BYTES / 8)];
-                const __half2 a = *reinterpret_cast<__half2 *>(&r.x), b = *reinterpret_cast<__half2 *>(&r.y);
-                lo0 = __hmin2(lo0, a); hi0 = __hmax2(hi0, a);
-                lo1 = __hmin2(lo1, b); hi1 = __hmax2(hi1, b);
-            }
+        for (int i = 1; i < ntok; ++i) {
+            uint2 r = col[i * (ROW_BYTES / 8)];
+            const __half2 a = *reinterpret_cast<__half2 *>(&r.x), b = *reinterpret_cast<__half2 *>(&r.y);
+            lo0 = __hmin2(lo0, a); hi0 = __hmax2(hi0, a);
+            lo1 = __hmin2(lo1, b); hi1 = __hmax2(hi1, b);
         }
         const float mxv[4] = {__low2float(hi0), __high2float(hi0), __low2float(hi1), __high2float(hi1)};
         GroupQ gq[4];
@@ -417,12 +446,15 @@ __global__ void __launch_bounds__(key_warps<G>() * 32, 1)
         gq[1] = group_setup<BITS>(__high2float(lo0), mxv[1]);
         gq[2] = group_setup<BITS>(__low2float(lo1), mxv[2]);
         gq[3] = group_setup<BITS>(__high2float(lo1), mxv[3]);
-        // pass 2: codes, packed along tokens (token i -> word i/E, shift (i%E)*BITS)
-        uint32_t w[WG][4];
-        bool near[4] = {false, false, false, false};
-#pragma unroll
+        int off;
+        const bool okoff = kivi_off(p, bh / p.H, off);  // uniform across the warp
+        const size_t gd = (size_t)bh * p.NG_dst + off / G + g;
+        // pass 2: word row k holds tokens k*E .. k*E + E - 1 at shifts j*BITS
+        const __half *tokh = reinterpret_cast<const __half *>(tb);
+#pragma unroll 1
         for (int k = 0; k < WG; ++k) {
-            w[k][0] = w[k][1] = w[k][2] = w[k][3] = 0u;
+            uint32_t w0 = 0u, w1 = 0u, w2 = 0u, w3 = 0u;
+            bool n0 = false, n1 = false, n2 = false, n3 = false;
 #pragma unroll
             for (int j = 0; j < E; ++j) {
                 const int i = k * E + j;
@@ -431,36 +463,35 @@ __global__ void __launch_bounds__(key_warps<G>() * 32, 1)
                     uint2 r = col[i * (ROW_BYTES / 8)];
                     const float2 a = __half22float2(*reinterpret_cast<__half2 *>(&r.x));
                     const float2 b = __half22float2(*reinterpret_cast<__half2 *>(&r.y));
-                    c0 = code_fast<BITS>(a.x, gq[0], near[0]);
-                    c1 = code_fast<BITS>(a.y, gq[1], near[1]);
-                    c2 = code_fast<BITS>(b.x, gq[2], near[2]);
-                    c3 = code_fast<BITS>(b.y, gq[3], near[3]);
+                    c0 = code_fast<BITS>(a.x, gq[0], n0);
+                    c1 = code_fast<BITS>(a.y, gq[1], n1);
+                    c2 = code_fast<BITS>(b.x, gq[2], n2);
+                    c3 = code_fast<BITS>(b.y, gq[3], n3);
                 }
-                w[k][0] = __funnelshift_r(w[k][0], c0, BITS);
-                w[k][1] = __funnelshift_r(w[k][1], c1, BITS);
-                w[k][2] = __funnelshift_r(w[k][2], c2, BITS);
-                w[k][3] = __funnelshift_r(w[k][3], c3, BITS);
+                w0 = __funnelshift_r(w0, c0, BITS);
+                w1 = __funnelshift_r(w1, c1, BITS);
+                w2 = __funnelshift_r(w2, c2, BITS);
+                w3 = __funnelshift_r(w3, c3, BITS);
             }
-        }
-        // rare: a channel with a t within rounding of a half-integer is redone exactly
-        const __half *tokh = reinterpret_cast<const __half *>(tb);
+            if (n0 | n1 | n2 | n3) {  // rare: redo the affected channels of this word row exactly
+                const bool nn[4] = {n0, n1, n2, n3};
+                uint32_t rw[4] = {w0, w1, w2, w3};
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            if (!near[c]) continue;
-            const float mn = gq[c].mn;
-            for (int k = 0; k < WG; ++k) {
-                uint32_t word = 0u;
-                for (int j = 0; j < E; ++j) {
-                    const int i = k * E + j;
-                    const uint32_t q = i < ntok ? exact_code_slow<BITS>(
-                        __half2float(tokh[i * D + 4 * lane + c]), mn, mxv[c]) : 0u;
-                    word |= q << (j * BITS);
+                for (int c = 0; c < 4; ++c) {
+                    if (!nn[c]) continue;
+                    uint32_t word = 0u;
+                    for (int j = 0; j < E; ++j) {
+                        const int i = k * E + j;
+                        if (i < ntok)
+                            word |= exact_code_slow<BITS>(__half2float(tokh[i * D + 4 * lane + c]),
+                                                          gq[c].mn, mxv[c]) << (j * BITS);
+                    }
+                    rw[c] = word;
                 }
-                if (c == 0) w[k][0] = word;
-                if (c == 1) w[k][1] = word;
-                if (c == 2) w[k][2] = word;
-                if (c == 3) w[k][3] = word;
+                w0 = rw[0]; w1 = rw[1]; w2 = rw[2]; w3 = rw[3];
             }
+            if (okoff)
+                *reinterpret_cast<uint4 *>(p.packed + (gd * WG + k) * D + 4 * lane) = make_uint4(w0, w1, w2, w3);
         }
         // the tile is consumed: recycle the stage
         __syncwarp();
@@ -469,13 +500,7 @@ __global__ void __launch_bounds__(key_warps<G>() * 32, 1)
             const int nt = tile + KEY_STAGES * tw;
             if (nt < ntiles) issue(nt, s);
         }
-        int off;
-        if (!kivi_off(p, bh / p.H, off)) continue;
-        const size_t gd = (size_t)bh * p.NG_dst + off / G + g;
-#pragma unroll
-        for (int k = 0; k < WG; ++k)
-            *reinterpret_cast<uint4 *>(p.packed + (gd * WG + k) * D + 4 * lane) =
-                make_uint4(w[k][0], w[k][1], w[k][2], w[k][3]);
+        if (!okoff) continue;
         __half2 s01 = __halves2half2(gq[0].scale_h, gq[1].scale_h);
         __half2 s23 = __halves2half2(gq[2].scale_h, gq[3].scale_h);
         __half2 z01 = __halves2half2(gq[0].zero_h, gq[1].zero_h);
@@ -491,48 +516,125 @@ __global__ void __launch_bounds__(key_warps<G>() * 32, 1)
 
 constexpr int DQ_THREADS = 256;
 
+// Values: one row per thread; each row's words arrive by a per-row bulk copy
+// into a 3-stage ring (slots padded for conflict-free 16-byte reads); the fp16
+// row is staged in shared memory and written out coalesced.
+constexpr int VDQ_WARPS = 8;
+constexpr int VDQ_STAGES = 3;
+__host__ __device__ constexpr int vdq_slot(int bits) { return (D * bits / 32) * 4 + 16 > 48 ? (D * bits / 32) * 4 + 16 : 48; }
+__host__ __device__ constexpr int vdq_warp_bytes(int bits) { return VDQ_STAGES * 32 * vdq_slot(bits) + 32 * ROW_STRIDE; }
+__host__ __device__ constexpr int vdq_smem(int bits) { return VDQ_WARPS * (vdq_warp_bytes(bits) + VDQ_STAGES * 8); }
+
 template <int BITS, int G>
-__global__ void __launch_bounds__(DQ_THREADS) kivi_values_dequant_kernel(const __grid_constant__ KiviDequantParams p)
+__global__ void __launch_bounds__(VDQ_WARPS * 32, 1) kivi_values_dequant_kernel(const __grid_constant__ KiviDequantParams p)
 {
     constexpr int E = 32 / BITS;
     constexpr int W = D * BITS / 32;
     constexpr int NGD = D / G;
     constexpr uint32_t MASK = (1u << BITS) - 1u;
-    const int N = p.BH * p.S_q;
-    for (int row = blockIdx.x * DQ_THREADS + threadIdx.x; row < N; row += gridDim.x * DQ_THREADS) {
-        uint32_t words[W];
+    constexpr int SLOT = vdq_slot(BITS);
+    constexpr int WB = vdq_warp_bytes(BITS);
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    unsigned char *wbuf = smem + warp * WB;
+    unsigned char *obuf = wbuf + VDQ_STAGES * 32 * SLOT;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + VDQ_WARPS * WB) + warp * VDQ_STAGES;
+    if (lane == 0) {
 #pragma unroll
-        for (int i = 0; i < W; ++i) words[i] = __ldg(p.packed + (size_t)row * W + i);
-        const __half *sc = static_cast<const __half *>(p.scale) + (size_t)row * NGD;
-        const __half *zr = static_cast<const __half *>(p.zero) + (size_t)row * NGD;
+        for (int s = 0; s < VDQ_STAGES; ++s) mbar_init(&bars[s], 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+    const uint64_t pol = l2_policy_evict_first();
+    const int N = p.BH * p.S_q;
+    const int nblk = (N + 31) >> 5;
+    const int gw = blockIdx.x * VDQ_WARPS + warp;
+    const int tw = gridDim.x * VDQ_WARPS;
+    auto issue = [&](int blk, int s) {
+        const int r0 = blk << 5;
+        const int nrows = min(32, N - r0);
+        if (lane == 0) mbar_arrive_expect_tx(&bars[s], (uint32_t)(nrows * W * 4));
+        if (lane < nrows)
+            bulk_g2s(wbuf + s * 32 * SLOT + lane * SLOT, p.packed + (size_t)(r0 + lane) * W, W * 4, &bars[s], pol);
+    };
+#pragma unroll
+    for (int s = 0; s < VDQ_STAGES; ++s) {
+        const int blk = gw + s * tw;
+        if (blk < nblk) issue(blk, s);
+    }
+    const __half *scp = static_cast<const __half *>(p.scale);
+    const __half *zrp = static_cast<const __half *>(p.zero);
+    for (int it = 0;; ++it) {
+        const int blk = gw + it * tw;
+        if (blk >= nblk) break;
+        const int s = it % VDQ_STAGES;
+        const int row = (blk << 5) + lane;
+        const bool valid = row < N;
         float sf[NGD], zf[NGD];
-        bool exact[NGD];
 #pragma unroll
         for (int j = 0; j < NGD; ++j) {
-            sf[j] = __half2float(sc[j]);
-            zf[j] = __half2float(zr[j]);
-            exact[j] = group_sum_exact<BITS>(sf[j], zf[j]);
+            sf[j] = valid ? __half2float(scp[(size_t)row * NGD + j]) : 0.0f;
+            zf[j] = valid ? __half2float(zrp[(size_t)row * NGD + j]) : 0.0f;
         }
-        uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__half *>(p.out) + (size_t)row * D);
+        const bool ok = mbar_wait_bounded(&bars[s], (uint32_t)(it / VDQ_STAGES) & 1u);
+        if (!__all_sync(FULL_MASK, ok)) {
+            if (lane == 0) atomicOr(&g_kivi_err, (unsigned)VQ_DEVERR_WAIT_TIMEOUT);
+            for (int k = 1; k < VDQ_STAGES; ++k) {
+                const int it2 = it + k;
+                if (gw + it2 * tw < nblk)
+                    (void)mbar_wait_bounded(&bars[it2 % VDQ_STAGES], (uint32_t)(it2 / VDQ_STAGES) & 1u);
+            }
+            return;
+        }
+        uint32_t words[W];
+        {
+            const uint4 *sl = reinterpret_cast<const uint4 *>(wbuf + s * 32 * SLOT + lane * SLOT);
+#pragma unroll
+            for (int i = 0; i < W / 4; ++i) {
+                const uint4 a = sl[i];
+                words[4 * i] = a.x; words[4 * i + 1] = a.y; words[4 * i + 2] = a.z; words[4 * i + 3] = a.w;
+            }
+        }
+        __syncwarp();
+        fence_proxy_async_smem();
+        {
+            const int nb = blk + VDQ_STAGES * tw;
+            if (nb < nblk) issue(nb, s);
+        }
+        bool exact[NGD];
+#pragma unroll
+        for (int j = 0; j < NGD; ++j) exact[j] = group_sum_exact<BITS>(sf[j], zf[j]);
+        uint4 *orow = reinterpret_cast<uint4 *>(obuf + lane * ROW_STRIDE);
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
             uint32_t out[4];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const int e = 8 * c + 2 * j;
-                const float s = sf[e / G], z = zf[e / G];
+                const float sv = sf[e / G], zv = zf[e / G];
                 const uint32_t q0 = (words[e / E] >> ((e % E) * BITS)) & MASK;
                 const uint32_t q1 = (words[(e + 1) / E] >> (((e + 1) % E) * BITS)) & MASK;
                 __half2 hv;
                 if (exact[e / G]) {
-                    hv = __floats2half2_rn(fmaf((float)q0, s, z), fmaf((float)q1, s, z));
+                    hv = __floats2half2_rn(fmaf((float)q0, sv, zv), fmaf((float)q1, sv, zv));
                 } else {
-                    hv = __halves2half2(recon_exact(q0, s, z), recon_exact(q1, s, z));
+                    hv = __halves2half2(recon_exact(q0, sv, zv), recon_exact(q1, sv, zv));
                 }
                 out[j] = *reinterpret_cast<const uint32_t *>(&hv);
             }
-            dst[c] = make_uint4(out[0], out[1], out[2], out[3]);
+            orow[c] = make_uint4(out[0], out[1], out[2], out[3]);
         }
+        __syncwarp();
+        const int nrows = min(32, N - (blk << 5));
+        uint4 *gout = reinterpret_cast<uint4 *>(static_cast<__half *>(p.out) + (size_t)(blk << 5) * D);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int idx = i * 32 + lane;
+            const int r = idx >> 4, c = idx & 15;
+            if (r < nrows) gout[idx] = *reinterpret_cast<const uint4 *>(obuf + r * ROW_STRIDE + c * 16);
+        }
+        __syncwarp();
     }
 }
 
@@ -603,13 +705,14 @@ cudaError_t launch_q(const KiviQuantParams &p, bool per_channel, cudaStream_t st
         kern<<<grid, warps * 32, smem, stream>>>(p);
     } else {
         auto kern = kivi_values_kernel<BITS, G>;
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, VAL_SMEM);
+        constexpr int smem = val_smem(BITS, G);
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
         const int nblk = (p.B * p.H * p.S_q + 31) / 32;
         int grid = (nblk + VAL_WARPS - 1) / VAL_WARPS;
         if (grid > sms) grid = sms;
         if (grid < 1) grid = 1;
-        kern<<<grid, VAL_WARPS * 32, VAL_SMEM, stream>>>(p);
+        kern<<<grid, VAL_WARPS * 32, smem, stream>>>(p);
     }
     return cudaGetLastError();
 }
@@ -625,11 +728,15 @@ cudaError_t launch_dq(const KiviDequantParams &p, bool per_channel, cudaStream_t
         if (grid < 1) grid = 1;
         kivi_keys_dequant_kernel<BITS, G><<<grid, DQ_THREADS, 0, stream>>>(p);
     } else {
-        const int N = p.BH * p.S_q;
-        int grid = (N + DQ_THREADS - 1) / DQ_THREADS;
-        if (grid > cap) grid = cap;
+        auto kern = kivi_values_dequant_kernel<BITS, G>;
+        constexpr int smem = vdq_smem(BITS);
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        const int nblk = (p.BH * p.S_q + 31) / 32;
+        int grid = (nblk + VDQ_WARPS - 1) / VDQ_WARPS;
+        if (grid > sm_count()) grid = sm_count();
         if (grid < 1) grid = 1;
-        kivi_values_dequant_kernel<BITS, G><<<grid, DQ_THREADS, 0, stream>>>(p);
+        kern<<<grid, VDQ_WARPS * 32, smem, stream>>>(p);
     }
     return cudaGetLastError();
 }

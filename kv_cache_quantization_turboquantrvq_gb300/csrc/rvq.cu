@@ -11,16 +11,21 @@
 // The pages fuse quantize->pack after a separate rotation dispatch; here the
 // norm, rotation, both stages and both packs are one pass over HBM.
 //
-// Encode design (one row per thread):
-//  * each warp owns a private 3-stage ring of 32-row tiles in shared memory,
+// Encode design (one row per thread, 32-row blocks per warp):
+//  * each warp owns a private 2-stage ring of 32-row blocks in shared memory,
 //    filled by per-row cp.async.bulk copies (lane i copies row i, 256 B) that
 //    complete on an mbarrier; rows sit at a 272-byte stride so the 32 row
 //    owners read 16-byte chunks without bank conflicts;
 //  * a thread holds its row as 64 float2 (x[k], x[k+64]) and runs six
 //    butterfly stages with the fp32x2 add/fma instructions and the last
 //    (bit 6) stage in scalar fp32 - no shuffles;
+//  * the rotated row goes to a per-thread shared-memory scratch one half at a
+//    time and is quantized by a rolled loop over output words, which keeps the
+//    program small enough for the instruction cache (a fully unrolled
+//    128-coordinate quantizer stalls on instruction fetch);
 //  * the boundary count of each stage is two table reads by warp shuffle
 //    (GridTable in launch.h) plus one compare;
+//  * words are staged in shared memory and written out coalesced;
 //  * every code is kept unless its pre-quantization value lies within a guard
 //    band of a boundary; such rows are redone by the whole warp in exact /
 //    double-float arithmetic (rvq_fixup_row), so the packed words equal those
@@ -37,12 +42,25 @@ VQ_DEFINE_ERROR_WORD(g_rvq_err);
 namespace {
 
 constexpr int D = 128;
-constexpr int ENC_WARPS = 8;
-constexpr int ENC_STAGES = 3;
 constexpr int ROW_BYTES = D * 2;
 constexpr int ROW_STRIDE = ROW_BYTES + 16;
 constexpr int STAGE_BYTES = 32 * ROW_STRIDE;
-constexpr int ENC_SMEM = ENC_WARPS * ENC_STAGES * STAGE_BYTES + ENC_WARPS * ENC_STAGES * 8;
+
+// Encoder shared memory, per warp: ENC_STAGES input blocks, the half-row
+// scratch (16 float4 chunks x 32 lanes), two word-staging arrays with one pad
+// word per row, and the norms of rows redone by the exact path.
+constexpr int ENC_STAGES = 2;
+constexpr int YH_BYTES = 16 * 32 * 16;
+__host__ __device__ constexpr int enc_words(int bits) { return D * bits / 32; }
+__host__ __device__ constexpr int enc_warp_bytes(int bits)
+{
+    return ENC_STAGES * STAGE_BYTES + YH_BYTES + 2 * 32 * (enc_words(bits) + 1) * 4 + 32 * 4;
+}
+__host__ __device__ constexpr int enc_warps(int bits) { return bits == 4 ? 7 : 8; }
+__host__ __device__ constexpr int enc_smem(int bits)
+{
+    return enc_warps(bits) * (enc_warp_bytes(bits) + ENC_STAGES * 8);
+}
 
 // sqrt(128) = 8 sqrt(2) as a double-float (nearest fp32 + fp32 remainder).
 constexpr float SQRT_D_HI = 11.313708305358887f;
@@ -146,10 +164,13 @@ __device__ __forceinline__ void wht_lane_exact(float (&a)[4], int lane)
 //    n = sqrt(Q) and 1/(n sqrt(D)) in double-float.
 //  * y = S / (n sqrt(D)) in double-float (about 2^-44 relative), and each
 //    boundary count is taken on the double-float value.
+// The row's words go to the warp's staging rows (o1, o2, stride W + 1) and
+// its norm to nrm[r].
 template <int BITS, bool GRID>
 __device__ __noinline__ void rvq_fixup_row(const RvqEncodeParams &p, const unsigned char *srow,
-                                           int row, int lane, float tb1, int tc1, float tb2,
-                                           int tc2, float tcen)
+                                           int r, int lane, float tb1, int tc1, float tb2,
+                                           int tc2, float tcen, uint32_t *o1, uint32_t *o2,
+                                           float *nrm)
 {
     constexpr int E = 32 / BITS;
     constexpr int W = D * BITS / 32;
@@ -249,29 +270,31 @@ __device__ __noinline__ void rvq_fixup_row(const RvqEncodeParams &p, const unsig
         part1 |= __shfl_xor_sync(FULL_MASK, part1, o);
         part2 |= __shfl_xor_sync(FULL_MASK, part2, o);
     }
-    size_t drow;
-    if (rvq_dst_row(p, row, drow)) {
-        if (sub == 0 && lane / LPW < W) {
-            p.p1[drow * W + lane / LPW] = part1;
-            p.p2[drow * W + lane / LPW] = part2;
-        }
-        if (lane == 0) p.norms[drow] = __fadd_rn(nh, nl);
+    if (sub == 0 && lane / LPW < W) {
+        o1[r * (W + 1) + lane / LPW] = part1;
+        o2[r * (W + 1) + lane / LPW] = part2;
     }
+    if (lane == 0) nrm[r] = __fadd_rn(nh, nl);
 }
 
 template <int BITS, bool GRID>
-__global__ void __launch_bounds__(ENC_WARPS * 32, 1)
+__global__ void __launch_bounds__(enc_warps(BITS) * 32, 1)
     rvq_encode_kernel(const __grid_constant__ RvqEncodeParams p)
 {
     constexpr int L = 1 << BITS;
     constexpr int E = 32 / BITS;
     constexpr int W = D * BITS / 32;
+    constexpr int WARPS = enc_warps(BITS);
+    constexpr int WB = enc_warp_bytes(BITS);
     extern __shared__ __align__(128) unsigned char smem[];
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    unsigned char *wbuf = smem + warp * (ENC_STAGES * STAGE_BYTES);
-    uint64_t *bars =
-        reinterpret_cast<uint64_t *>(smem + ENC_WARPS * ENC_STAGES * STAGE_BYTES) + warp * ENC_STAGES;
+    unsigned char *wbuf = smem + warp * WB;
+    float4 *yh = reinterpret_cast<float4 *>(wbuf + ENC_STAGES * STAGE_BYTES);
+    uint32_t *o1 = reinterpret_cast<uint32_t *>(wbuf + ENC_STAGES * STAGE_BYTES + YH_BYTES);
+    uint32_t *o2 = o1 + 32 * (W + 1);
+    float *nrm = reinterpret_cast<float *>(o2 + 32 * (W + 1));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + WARPS * WB) + warp * ENC_STAGES;
 
     if (lane == 0) {
 #pragma unroll
@@ -287,8 +310,8 @@ __global__ void __launch_bounds__(ENC_WARPS * 32, 1)
     const int tc2 = p.t2.code[lane];
     const float tcen = p.c1[lane & (L - 1)];
     const int nblk = (p.N + 31) >> 5;
-    const int gw = blockIdx.x * ENC_WARPS + warp;
-    const int tw = gridDim.x * ENC_WARPS;
+    const int gw = blockIdx.x * WARPS + warp;
+    const int tw = gridDim.x * WARPS;
     const __half *x = static_cast<const __half *>(p.x);
 
     auto issue = [&](int blk, int s) {
@@ -381,90 +404,167 @@ __global__ void __launch_bounds__(ENC_WARPS * 32, 1)
             v[k] = make_float2(a + b, a - b);
         }
 
-        // ---- two-stage boundary count and LSB-first packing
-        uint32_t w1[W], w2[W];
-#pragma unroll
-        for (int i = 0; i < W; ++i) w1[i] = w2[i] = 0u;
+        // ---- two-stage boundary count and LSB-first packing, one half-row at
+        // a time through the thread's scratch chunks yh[c * 32 + lane]
         float m = __int_as_float(0x7f800000);
 #pragma unroll
-        for (int e = 0; e < D; ++e) {
-            const float y = e < 64 ? v[e].x : v[e - 64].y;
-            const int code1 = stage_code<BITS, GRID>(y, tb1, tc1, p.t1, p.b1, m);
-            const float r = y - __shfl_sync(FULL_MASK, tcen, code1);
-            const int code2 = stage_code<BITS, GRID>(r, tb2, tc2, p.t2, p.b2, m);
-            w1[e / E] = __funnelshift_r(w1[e / E], (uint32_t)code1, BITS);
-            w2[e / E] = __funnelshift_r(w2[e / E], (uint32_t)code2, BITS);
+        for (int half = 0; half < 2; ++half) {
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+                yh[c * 32 + lane] = half == 0
+                    ? make_float4(v[4 * c].x, v[4 * c + 1].x, v[4 * c + 2].x, v[4 * c + 3].x)
+                    : make_float4(v[4 * c].y, v[4 * c + 1].y, v[4 * c + 2].y, v[4 * c + 3].y);
+            }
+#pragma unroll 1
+            for (int w = 0; w < W / 2; ++w) {
+                uint32_t a1 = 0u, a2 = 0u;
+#pragma unroll
+                for (int cc = 0; cc < E / 4; ++cc) {
+                    const float4 q4 = yh[(w * (E / 4) + cc) * 32 + lane];
+                    const float ys[4] = {q4.x, q4.y, q4.z, q4.w};
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int code1 = stage_code<BITS, GRID>(ys[j], tb1, tc1, p.t1, p.b1, m);
+                        const float rr = ys[j] - __shfl_sync(FULL_MASK, tcen, code1);
+                        const int code2 = stage_code<BITS, GRID>(rr, tb2, tc2, p.t2, p.b2, m);
+                        a1 = __funnelshift_r(a1, (uint32_t)code1, BITS);
+                        a2 = __funnelshift_r(a2, (uint32_t)code2, BITS);
+                    }
+                }
+                o1[lane * (W + 1) + half * (W / 2) + w] = a1;
+                o2[lane * (W + 1) + half * (W / 2) + w] = a2;
+            }
         }
         const bool flag = valid && !(m >= p.guard);
 
-        if (valid && !flag) {
-            size_t drow;
-            if (rvq_dst_row(p, row, drow)) {
-                uint4 *d1 = reinterpret_cast<uint4 *>(p.p1 + drow * W);
-                uint4 *d2 = reinterpret_cast<uint4 *>(p.p2 + drow * W);
-#pragma unroll
-                for (int i = 0; i < W / 4; ++i) {
-                    d1[i] = make_uint4(w1[4 * i], w1[4 * i + 1], w1[4 * i + 2], w1[4 * i + 3]);
-                    d2[i] = make_uint4(w2[4 * i], w2[4 * i + 1], w2[4 * i + 2], w2[4 * i + 3]);
-                }
-                p.norms[drow] = n;
-            }
-        }
-
         // ---- rows with a value inside the guard band: exact recompute by the warp
+        __syncwarp();
         unsigned fl = __ballot_sync(FULL_MASK, flag);
         while (fl) {
             const int r = __ffs(fl) - 1;
             fl &= fl - 1;
-            rvq_fixup_row<BITS, GRID>(p, sbuf + r * ROW_STRIDE, (blk << 5) + r, lane, tb1, tc1,
-                                      tb2, tc2, tcen);
+            rvq_fixup_row<BITS, GRID>(p, sbuf + r * ROW_STRIDE, r, lane, tb1, tc1, tb2, tc2, tcen,
+                                      o1, o2, nrm);
+        }
+        __syncwarp();
+
+        // ---- recycle this stage for the block ENC_STAGES iterations ahead
+        fence_proxy_async_smem();
+        {
+            const int nb = blk + ENC_STAGES * tw;
+            if (nb < nblk) issue(nb, s);
         }
 
-        // ---- recycle this stage for the tile ENC_STAGES iterations ahead
+        // ---- coalesced write-out: word idx = i*32 + lane is word idx % W of row idx / W
+        size_t drow = 0;
+        const bool okrow = valid && rvq_dst_row(p, row, drow);
+        const int drow32 = (int)drow;
+#pragma unroll
+        for (int i = 0; i < W; ++i) {
+            const int idx = i * 32 + lane;
+            const int r = idx / W, w = idx % W;
+            const int dr = __shfl_sync(FULL_MASK, drow32, r);
+            const bool ok = __shfl_sync(FULL_MASK, okrow ? 1 : 0, r) != 0;
+            if (ok) {
+                p.p1[(size_t)dr * W + w] = o1[r * (W + 1) + w];
+                p.p2[(size_t)dr * W + w] = o2[r * (W + 1) + w];
+            }
+        }
+        if (okrow) p.norms[drow] = flag ? nrm[lane] : n;
         __syncwarp();
-        fence_proxy_async_smem();
-        const int nb = blk + ENC_STAGES * tw;
-        if (nb < nblk) issue(nb, s);
     }
 }
 
 // ---------------------------------------------------------------- decode
 //
-// x_hat = n * H (c1[i1] + c2[i2]) / sqrt(D): one row per thread; centroid
-// lookups are warp shuffles from tables replicated every 2^BITS lanes, so the
-// shuffle index can be the packed word shifted right (its low 5 bits).
-constexpr int DEC_THREADS = 128;
+// x_hat = n * H (c1[i1] + c2[i2]) / sqrt(D): one row per thread.  The packed
+// words of each row arrive by two per-row bulk copies into a 3-stage ring
+// (slots padded for conflict-free 16-byte reads); centroid lookups are warp
+// shuffles from tables replicated every 2^BITS lanes, so the packed word
+// shifted right is itself a valid shuffle index; the fp16 row is staged in
+// shared memory and written out coalesced.
+constexpr int DEC_STAGES = 3;
+constexpr int DEC_WARPS = 8;
+__host__ __device__ constexpr int dec_slot(int bits) { return 2 * (D * bits / 32) * 4 + 16; }
+__host__ __device__ constexpr int dec_warp_bytes(int bits) { return DEC_STAGES * 32 * dec_slot(bits) + 32 * ROW_STRIDE; }
+__host__ __device__ constexpr int dec_smem(int bits) { return DEC_WARPS * (dec_warp_bytes(bits) + DEC_STAGES * 8); }
 
 template <int BITS>
-__global__ void __launch_bounds__(DEC_THREADS) rvq_decode_kernel(const __grid_constant__ RvqDecodeParams p)
+__global__ void __launch_bounds__(DEC_WARPS * 32, 1) rvq_decode_kernel(const __grid_constant__ RvqDecodeParams p)
 {
     constexpr int L = 1 << BITS;
     constexpr int E = 32 / BITS;
     constexpr int W = D * BITS / 32;
+    constexpr int SLOT = dec_slot(BITS);
+    constexpr int WB = dec_warp_bytes(BITS);
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    unsigned char *wbuf = smem + warp * WB;
+    unsigned char *obuf = wbuf + DEC_STAGES * 32 * SLOT;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + DEC_WARPS * WB) + warp * DEC_STAGES;
+    if (lane == 0) {
+#pragma unroll
+        for (int s = 0; s < DEC_STAGES; ++s) mbar_init(&bars[s], 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+    const uint64_t pol = l2_policy_evict_first();
     const float tc1 = p.c1[lane & (L - 1)];
     const float tc2 = p.c2[lane & (L - 1)];
     const int nblk = (p.N + 31) >> 5;
-    const int wpb = DEC_THREADS / 32;
+    const int gw = blockIdx.x * DEC_WARPS + warp;
+    const int tw = gridDim.x * DEC_WARPS;
     const float2 neg1 = make_float2(-1.0f, -1.0f);
-    for (int blk = blockIdx.x * wpb + (threadIdx.x >> 5); blk < nblk; blk += gridDim.x * wpb) {
+
+    auto issue = [&](int blk, int s) {
+        const int r0 = blk << 5;
+        const int nrows = min(32, p.N - r0);
+        if (lane == 0) mbar_arrive_expect_tx(&bars[s], (uint32_t)(nrows * 2 * W * 4));
+        if (lane < nrows) {
+            unsigned char *slot = wbuf + s * 32 * SLOT + lane * SLOT;
+            bulk_g2s(slot, p.p1 + (size_t)(r0 + lane) * W, W * 4, &bars[s], pol);
+            bulk_g2s(slot + W * 4, p.p2 + (size_t)(r0 + lane) * W, W * 4, &bars[s], pol);
+        }
+    };
+#pragma unroll
+    for (int s = 0; s < DEC_STAGES; ++s) {
+        const int blk = gw + s * tw;
+        if (blk < nblk) issue(blk, s);
+    }
+    for (int it = 0;; ++it) {
+        const int blk = gw + it * tw;
+        if (blk >= nblk) break;
+        const int s = it % DEC_STAGES;
         const int row = (blk << 5) + lane;
         const bool valid = row < p.N;
+        const float n = valid ? __ldg(p.norms + row) : 0.0f;
+        const bool ok = mbar_wait_bounded(&bars[s], (uint32_t)(it / DEC_STAGES) & 1u);
+        if (!__all_sync(FULL_MASK, ok)) {
+            if (lane == 0) atomicOr(&g_rvq_err, (unsigned)VQ_DEVERR_WAIT_TIMEOUT);
+            for (int k = 1; k < DEC_STAGES; ++k) {
+                const int it2 = it + k;
+                if (gw + it2 * tw < nblk)
+                    (void)mbar_wait_bounded(&bars[it2 % DEC_STAGES], (uint32_t)(it2 / DEC_STAGES) & 1u);
+            }
+            return;
+        }
         uint32_t w1[W], w2[W];
-        float n = 0.0f;
-        if (valid) {
-            const uint4 *s1 = reinterpret_cast<const uint4 *>(p.p1 + (size_t)row * W);
-            const uint4 *s2 = reinterpret_cast<const uint4 *>(p.p2 + (size_t)row * W);
+        {
+            const uint4 *sl = reinterpret_cast<const uint4 *>(wbuf + s * 32 * SLOT + lane * SLOT);
 #pragma unroll
             for (int i = 0; i < W / 4; ++i) {
-                const uint4 a = __ldg(s1 + i), b = __ldg(s2 + i);
+                const uint4 a = sl[i], b = sl[W / 4 + i];
                 w1[4 * i] = a.x; w1[4 * i + 1] = a.y; w1[4 * i + 2] = a.z; w1[4 * i + 3] = a.w;
                 w2[4 * i] = b.x; w2[4 * i + 1] = b.y; w2[4 * i + 2] = b.z; w2[4 * i + 3] = b.w;
             }
-            n = __ldg(p.norms + row);
-        } else {
-#pragma unroll
-            for (int i = 0; i < W; ++i) w1[i] = w2[i] = 0u;
+        }
+        // the words are in registers: recycle the stage
+        __syncwarp();
+        fence_proxy_async_smem();
+        {
+            const int nb = blk + DEC_STAGES * tw;
+            if (nb < nblk) issue(nb, s);
         }
         float2 v[64];
 #pragma unroll
@@ -486,27 +586,32 @@ __global__ void __launch_bounds__(DEC_THREADS) rvq_decode_kernel(const __grid_co
             }
         }
         const float sc = __fdiv_rn(n, SQRT_D_HI);
+        uint4 *orow = reinterpret_cast<uint4 *>(obuf + lane * ROW_STRIDE);
 #pragma unroll
-        for (int k = 0; k < 64; ++k) {
-            const float a = v[k].x, b = v[k].y;
-            v[k] = make_float2((a + b) * sc, (a - b) * sc);
-        }
-        if (valid) {
-            uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__half *>(p.out) + (size_t)row * D);
+        for (int c = 0; c < 8; ++c) {
+            uint32_t lo[4], hi[4];
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                uint32_t lo[4], hi[4];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const __half2 a = __floats2half2_rn(v[8 * c + 2 * j].x, v[8 * c + 2 * j + 1].x);
-                    const __half2 b = __floats2half2_rn(v[8 * c + 2 * j].y, v[8 * c + 2 * j + 1].y);
-                    lo[j] = *reinterpret_cast<const uint32_t *>(&a);
-                    hi[j] = *reinterpret_cast<const uint32_t *>(&b);
-                }
-                dst[c] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-                dst[c + 8] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            for (int j = 0; j < 4; ++j) {
+                const float2 a = v[8 * c + 2 * j], b = v[8 * c + 2 * j + 1];
+                const __half2 l2 = __floats2half2_rn((a.x + a.y) * sc, (b.x + b.y) * sc);
+                const __half2 h2 = __floats2half2_rn((a.x - a.y) * sc, (b.x - b.y) * sc);
+                lo[j] = *reinterpret_cast<const uint32_t *>(&l2);
+                hi[j] = *reinterpret_cast<const uint32_t *>(&h2);
             }
+            orow[c] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            orow[c + 8] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
         }
+        __syncwarp();
+        // coalesced write-out: chunk idx = i*32 + lane is 16-byte chunk idx % 16 of row idx / 16
+        const int nrows = min(32, p.N - (blk << 5));
+        uint4 *gout = reinterpret_cast<uint4 *>(static_cast<__half *>(p.out) + (size_t)(blk << 5) * D);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int idx = i * 32 + lane;
+            const int r = idx >> 4, c = idx & 15;
+            if (r < nrows) gout[idx] = *reinterpret_cast<const uint4 *>(obuf + r * ROW_STRIDE + c * 16);
+        }
+        __syncwarp();
     }
 }
 
@@ -514,26 +619,32 @@ template <int BITS, bool GRID>
 cudaError_t launch_enc(const RvqEncodeParams &p, cudaStream_t stream)
 {
     auto kern = rvq_encode_kernel<BITS, GRID>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, ENC_SMEM);
+    constexpr int smem = enc_smem(BITS);
+    constexpr int warps = enc_warps(BITS);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     const int nblk = (p.N + 31) / 32;
-    int grid = (nblk + ENC_WARPS - 1) / ENC_WARPS;
+    int grid = (nblk + warps - 1) / warps;
     const int sms = sm_count();
     if (grid > sms) grid = sms;
     if (grid < 1) grid = 1;
-    kern<<<grid, ENC_WARPS * 32, ENC_SMEM, stream>>>(p);
+    kern<<<grid, warps * 32, smem, stream>>>(p);
     return cudaGetLastError();
 }
 
 template <int BITS>
 cudaError_t launch_dec(const RvqDecodeParams &p, cudaStream_t stream)
 {
+    auto kern = rvq_decode_kernel<BITS>;
+    constexpr int smem = dec_smem(BITS);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
     const int nblk = (p.N + 31) / 32;
-    int grid = (nblk + DEC_THREADS / 32 - 1) / (DEC_THREADS / 32);
-    const int cap = sm_count() * 8;
-    if (grid > cap) grid = cap;
+    int grid = (nblk + DEC_WARPS - 1) / DEC_WARPS;
+    const int sms = sm_count();
+    if (grid > sms) grid = sms;
     if (grid < 1) grid = 1;
-    rvq_decode_kernel<BITS><<<grid, DEC_THREADS, 0, stream>>>(p);
+    kern<<<grid, DEC_WARPS * 32, smem, stream>>>(p);
     return cudaGetLastError();
 }
 
