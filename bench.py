@@ -82,7 +82,7 @@ def describe(name):
     }[name]
 
 
-def build_workload(name, dev, rank=0, layers=None):
+def build_workload(name, dev, rank=0, layers=None, batch=None):
     """Device buffers and the op list for one step; also host inputs for e2e."""
     import torch
     from kv_cache_quantization_turboquantrvq_gb300 import api, synth
@@ -149,7 +149,7 @@ def build_workload(name, dev, rank=0, layers=None):
     cfgs = synth.CONFIGS
     if name == "c5":
         cfg = cfgs["c5_long_32k"]
-        k_np, v_np = synth.keys_for(cfg), synth.values_for(cfg)
+        k_np, v_np = synth.keys_for(cfg, B=batch), synth.values_for(cfg, B=batch)
         k, v = t(k_np), t(v_np)
         inputs = [(k_np, k), (v_np, v)]
         rvq_ops("", k, cfg["rvq_bits"])
@@ -360,6 +360,8 @@ def main():
     ap.add_argument("--workload", choices=("c5", "c3", "c2", "c1", "c4"), default="c5")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="c5 only: batch size B (default 4; 1 for small profiling runs)")
     ap.add_argument("--layers", type=int, default=None,
                     help="c3 only: number of layers (default 32; fewer for small profiling runs)")
     args = ap.parse_args()
@@ -386,7 +388,7 @@ def main():
     build.build()
     api.lib()  # fails loudly if the CUDA library is missing
 
-    ops, inputs, results = build_workload(args.workload, dev, rank, layers=args.layers)
+    ops, inputs, results = build_workload(args.workload, dev, rank, layers=args.layers, batch=args.batch)
     stream = torch.cuda.current_stream()
     K, W = args.steps, max(args.warmup, 3)
 

@@ -52,6 +52,16 @@ bool valid_codebook(const float *c, const float *b, int L)
 
 vq_status cuda_status(cudaError_t e) { return e == cudaSuccess ? VQ_OK : VQ_ERR_CUDA; }
 
+// Exactly antisymmetric codebook with its middle boundary at 0.
+bool symmetric_codebook(const float *c, const float *b, int L)
+{
+    for (int k = 0; k < L; ++k)
+        if (c[k] != -c[L - 1 - k]) return false;
+    for (int k = 0; k < L - 1; ++k)
+        if (b[k] != -b[L - 2 - k]) return false;
+    return b[L / 2 - 1] == 0.0f;
+}
+
 }  // namespace
 
 int sm_count()
@@ -154,8 +164,12 @@ vq_status vq_rvq_encode_pack(const void *k_f16, int B, int H, int S, int D, int 
         p.b1[k] = k < L - 1 ? b1[k] : INFINITY;
         p.b2[k] = k < L - 1 ? b2[k] : INFINITY;
     }
-    const bool grid = build_grid(b1, L - 1, kGuard, p.t1) && build_grid(b2, L - 1, kGuard, p.t2);
-    return cuda_status(launch_rvq_encode(p, bits, grid, reinterpret_cast<cudaStream_t>(stream)));
+    int mode = RVQ_MODE_PLAIN;
+    if (bits <= 2 && symmetric_codebook(c1, b1, L) && symmetric_codebook(c2, b2, L))
+        mode = RVQ_MODE_SYM;
+    else if (build_grid(b1, L - 1, kGuard, p.t1) && build_grid(b2, L - 1, kGuard, p.t2))
+        mode = RVQ_MODE_GRID;
+    return cuda_status(launch_rvq_encode(p, bits, mode, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 vq_status vq_rvq_unpack_dequant(const uint32_t *packed1, const uint32_t *packed2, const float *norms,

@@ -14,10 +14,14 @@
 //
 // Exactness: codes are those of the exact quotient
 //   t = (x - min)(2^b - 1)/(max - min), rounded half to even.
-// The fast path computes t in fp32 (error < 8 ulp of 2^b - 1); an element
-// whose fp32 t is that close to a half-integer is decided again in binary64,
-// where numerator and denominator are exact.  The stored scale is
-// fp16(fp32(range/(2^b - 1))) with both roundings to nearest even.
+// With A = x - min, R = max - min and C = 2^b - 1, the code is decided against
+// the two half-integers around the fp32 estimate r = rint(A * C/R) by the
+// signs of C*A - (r -+ 1/2)*R, each formed by one FMA.  When R is exact in
+// fp32 with at most 19 significant bits, every exact tie has A and C*A exact in
+// fp32, so those signs (and zeros) are exact; other groups are decided in
+// 64-bit integers.  No per-element branch and no binary64 on the common path.
+// The stored scale is fp16(fp32(range/(2^b - 1))) with both roundings to
+// nearest even.
 //
 // Values (per token): one row per thread, rows staged by per-row bulk copies
 // into a per-warp 3-stage ring (as the RVQ encoder).  Keys (per channel): one
@@ -43,7 +47,8 @@ constexpr float MAGIC = 12582912.0f;  // 1.5 * 2^23: x + MAGIC rounds x to an in
 struct GroupQ {
     float mn;      // group minimum (exact)
     float f;       // (2^b - 1) / (max - min) in fp32, 0 for a constant group
-    float range;   // max - min (fp32; exactness checked where it matters)
+    float rr;      // max - min in fp32
+    bool fast;     // rr exact with <= 19 significant bits: the FMA test is exact
     __half scale_h, zero_h;
 };
 
@@ -75,53 +80,60 @@ __device__ __forceinline__ GroupQ group_setup(float mn, float mx)
     if (mx > mn) {
         float d, e;
         two_sum(mx, -mn, d, e);
-        g.range = d;
+        g.rr = d;
+        g.fast = e == 0.0f && (__float_as_uint(d) & 31u) == 0u;
         const float s32 = (e == 0.0f) ? __fdiv_rn(d, C) : exact_scale32_slow(mx, mn, C);
         g.scale_h = __float2half_rn(s32);
         g.f = __fdiv_rn(C, d);
     } else {
-        g.range = 0.0f;
+        g.rr = 0.0f;
+        g.fast = true;
         g.scale_h = __float2half_rn(0.0f);
         g.f = 0.0f;
     }
     return g;
 }
 
-// Exact half-even rounding of t = (x - mn) c / (mx - mn), in binary64 (all
-// operands fp16-valued, so numerator and denominator are exact).
+// Code of t = (x - mn) C / R, ties to even, in 64-bit integers: fp16 values
+// times 2^24 are integers below 2^40, so 2 C A - (2j + 1) R is exact.
 template <int BITS>
-__device__ __noinline__ uint32_t exact_code_slow(float x, float mn, float mx)
+__device__ __noinline__ uint32_t code_int64(float x, float mn, float mx)
 {
-    const double c = (double)((1 << BITS) - 1);
-    const double num = ((double)x - (double)mn) * c;
-    const double den = (double)mx - (double)mn;
-    const double t = num / den;            // only used to find the candidate k
-    const double k = floor(t);
-    // compare num/den with k + 1/2 exactly: 2 num vs (2k+1) den (both exact)
-    const double lhs = 2.0 * num, rhs = (2.0 * k + 1.0) * den;
-    double q;
-    if (lhs > rhs) q = k + 1.0;
-    else if (lhs < rhs) q = k;
-    else q = (fmod(k, 2.0) == 0.0) ? k : k + 1.0;
-    if (q < 0.0) q = 0.0;
-    if (q > c) q = c;
-    return (uint32_t)q;
+    const long long C = (1 << BITS) - 1;
+    const long long X = __float2ll_rn(x * 16777216.0f);
+    const long long MN = __float2ll_rn(mn * 16777216.0f);
+    const long long R = __float2ll_rn(mx * 16777216.0f) - MN;
+    if (R == 0) return 0u;
+    const long long A = X - MN;
+    uint32_t q = 0;
+    for (int j = 0; j < (int)C; ++j) {
+        const long long Z = 2 * C * A - (2LL * j + 1) * R;
+        q += (Z > 0 || (Z == 0 && (j & 1))) ? 1u : 0u;
+    }
+    return q;
 }
 
-// Fast code of one element (low BITS bits of the result).  `near` is set when
-// the fp32 t lies within its error bound of a half-integer; the caller then
-// recomputes that group with exact_code_slow.  No branch here, so the fast
-// path of a whole group schedules as straight-line code.
+// Exact code of one element of a `fast` group.  r is the nearest integer to
+// the fp32 estimate of t; the threshold r - 1/2 counts when
+// C A - (r - 1/2) R > 0, or = 0 with r even (tie to the even r), and r + 1/2
+// counts when C A - (r + 1/2) R > 0, or = 0 with r odd (tie to the even r + 1).
+// "or = 0" is a comparison against the negative subnormal of smallest
+// magnitude, which only an exact zero exceeds among these values.
 template <int BITS>
-__device__ __forceinline__ uint32_t code_fast(float x, const GroupQ &g, bool &near)
+__device__ __forceinline__ uint32_t code_exact(float x, const GroupQ &g)
 {
     constexpr float C = (float)((1 << BITS) - 1);
-    constexpr float EPS = 8.0f * C * 5.9604645e-08f;  // 8 ulp(1) * (2^b - 1)
-    const float t = (x - g.mn) * g.f;
-    const float tm = t + MAGIC;
-    const float frac = t - (tm - MAGIC);
-    near |= fabsf(frac) > 0.5f - EPS;
-    return (uint32_t)__float_as_int(tm);
+    const float A = x - g.mn;
+    const float tm = A * g.f + MAGIC;           // rint of the estimate, in the low bits
+    const float r = tm - MAGIC;
+    const float ca = A * C;
+    const float zl = fmaf(-(r - 0.5f), g.rr, ca);
+    const float zr = fmaf(-(r + 0.5f), g.rr, ca);
+    const int ri = __float_as_int(tm) - 0x4B400000;
+    const uint32_t odd = (uint32_t)ri & 1u;
+    const float thl = __uint_as_float((1u - odd) * 0x80000001u);  // -0 (no tie credit) or -tiny
+    const float thr = __uint_as_float(odd * 0x80000001u);
+    return (uint32_t)(ri - 1 + (zl > thl ? 1 : 0) + (zr > thr ? 1 : 0));
 }
 
 // fp16(q*s + z) rounded once from the exact value: q*s is exact in fp32, the
@@ -282,22 +294,21 @@ __global__ void __launch_bounds__(VAL_WARPS * 32, 1)
             for (int w = 0; w < WPG; ++w) {
                 const uint4 *wp = gp + w * (E / 8);
                 uint32_t word = 0u;
-                bool near = false;
+                if (g.fast) {
 #pragma unroll
-                for (int i = 0; i < E / 8; ++i) {
-                    uint4 c = wp[i];
-                    const __half2 *hh = reinterpret_cast<const __half2 *>(&c);
+                    for (int i = 0; i < E / 8; ++i) {
+                        uint4 c = wp[i];
+                        const __half2 *hh = reinterpret_cast<const __half2 *>(&c);
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const float2 v = __half22float2(hh[k]);
-                        word = __funnelshift_r(word, code_fast<BITS>(v.x, g, near), BITS);
-                        word = __funnelshift_r(word, code_fast<BITS>(v.y, g, near), BITS);
+                        for (int k = 0; k < 4; ++k) {
+                            const float2 v = __half22float2(hh[k]);
+                            word = __funnelshift_r(word, code_exact<BITS>(v.x, g), BITS);
+                            word = __funnelshift_r(word, code_exact<BITS>(v.y, g), BITS);
+                        }
                     }
-                }
-                if (near) {  // rare: a t within rounding of a half-integer
-                    word = 0u;
+                } else {  // rare: a range that fp32 does not hold exactly
                     for (int e = 0; e < E; ++e)
-                        word |= exact_code_slow<BITS>(__half2float(rh[j * G + w * E + e]), mn, mx) << (e * BITS);
+                        word |= code_int64<BITS>(__half2float(rh[j * G + w * E + e]), mn, mx) << (e * BITS);
                 }
                 ow[lane * (W + 1) + j * WPG + w] = word;
             }
@@ -451,42 +462,41 @@ __global__ void __launch_bounds__(key_warps<G>() * 32, 1)
         const size_t gd = (size_t)bh * p.NG_dst + off / G + g;
         // pass 2: word row k holds tokens k*E .. k*E + E - 1 at shifts j*BITS
         const __half *tokh = reinterpret_cast<const __half *>(tb);
+        const bool allfast = gq[0].fast && gq[1].fast && gq[2].fast && gq[3].fast;
 #pragma unroll 1
         for (int k = 0; k < WG; ++k) {
             uint32_t w0 = 0u, w1 = 0u, w2 = 0u, w3 = 0u;
-            bool n0 = false, n1 = false, n2 = false, n3 = false;
+            if (allfast) {
 #pragma unroll
-            for (int j = 0; j < E; ++j) {
-                const int i = k * E + j;
-                uint32_t c0 = 0, c1 = 0, c2 = 0, c3 = 0;
-                if (i < ntok) {
-                    uint2 r = col[i * (ROW_BYTES / 8)];
-                    const float2 a = __half22float2(*reinterpret_cast<__half2 *>(&r.x));
-                    const float2 b = __half22float2(*reinterpret_cast<__half2 *>(&r.y));
-                    c0 = code_fast<BITS>(a.x, gq[0], n0);
-                    c1 = code_fast<BITS>(a.y, gq[1], n1);
-                    c2 = code_fast<BITS>(b.x, gq[2], n2);
-                    c3 = code_fast<BITS>(b.y, gq[3], n3);
+                for (int j = 0; j < E; ++j) {
+                    const int i = k * E + j;
+                    uint32_t c0 = 0, c1 = 0, c2 = 0, c3 = 0;
+                    if (i < ntok) {
+                        uint2 r = col[i * (ROW_BYTES / 8)];
+                        const float2 a = __half22float2(*reinterpret_cast<__half2 *>(&r.x));
+                        const float2 b = __half22float2(*reinterpret_cast<__half2 *>(&r.y));
+                        c0 = code_exact<BITS>(a.x, gq[0]);
+                        c1 = code_exact<BITS>(a.y, gq[1]);
+                        c2 = code_exact<BITS>(b.x, gq[2]);
+                        c3 = code_exact<BITS>(b.y, gq[3]);
+                    }
+                    w0 = __funnelshift_r(w0, c0, BITS);
+                    w1 = __funnelshift_r(w1, c1, BITS);
+                    w2 = __funnelshift_r(w2, c2, BITS);
+                    w3 = __funnelshift_r(w3, c3, BITS);
                 }
-                w0 = __funnelshift_r(w0, c0, BITS);
-                w1 = __funnelshift_r(w1, c1, BITS);
-                w2 = __funnelshift_r(w2, c2, BITS);
-                w3 = __funnelshift_r(w3, c3, BITS);
-            }
-            if (n0 | n1 | n2 | n3) {  // rare: redo the affected channels of this word row exactly
-                const bool nn[4] = {n0, n1, n2, n3};
-                uint32_t rw[4] = {w0, w1, w2, w3};
+            } else {  // rare: some channel's range is not held exactly by fp32
+                uint32_t rw[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
-                    if (!nn[c]) continue;
-                    uint32_t word = 0u;
                     for (int j = 0; j < E; ++j) {
                         const int i = k * E + j;
-                        if (i < ntok)
-                            word |= exact_code_slow<BITS>(__half2float(tokh[i * D + 4 * lane + c]),
-                                                          gq[c].mn, mxv[c]) << (j * BITS);
+                        if (i >= ntok) break;
+                        const float xv = __half2float(tokh[i * D + 4 * lane + c]);
+                        const uint32_t q = gq[c].fast ? code_exact<BITS>(xv, gq[c])
+                                                      : code_int64<BITS>(xv, gq[c].mn, mxv[c]);
+                        rw[c] |= q << (j * BITS);
                     }
-                    rw[c] = word;
                 }
                 w0 = rw[0]; w1 = rw[1]; w2 = rw[2]; w3 = rw[3];
             }

@@ -55,8 +55,10 @@ struct KiviDequantParams {
     int BH, S_q, group, NG;
 };
 
-cudaError_t launch_rvq_encode(const RvqEncodeParams &p, int bits, bool use_grid,
-                              cudaStream_t stream);
+// Encoder quantizer variants: plain boundary count (any codebook), shuffle
+// tables (GridTable), and the table-free symmetric 1/2-bit quantizer.
+enum RvqMode { RVQ_MODE_PLAIN = 0, RVQ_MODE_GRID = 1, RVQ_MODE_SYM = 2 };
+cudaError_t launch_rvq_encode(const RvqEncodeParams &p, int bits, int mode, cudaStream_t stream);
 cudaError_t launch_rvq_decode(const RvqDecodeParams &p, int bits, cudaStream_t stream);
 cudaError_t launch_kivi_quant(const KiviQuantParams &p, int bits, bool per_channel,
                               cudaStream_t stream);

@@ -19,9 +19,9 @@
 //  * a thread holds its row as 64 float2 (x[k], x[k+64]) and runs six
 //    butterfly stages with the fp32x2 add/fma instructions and the last
 //    (bit 6) stage in scalar fp32 - no shuffles;
-//  * the rotated row goes to a per-thread shared-memory scratch one half at a
-//    time and is quantized by a rolled loop over output words, which keeps the
-//    program small enough for the instruction cache (a fully unrolled
+//  * the rotated row goes to a per-thread shared-memory scratch a quarter at
+//    a time and is quantized by a rolled loop over output words, which keeps
+//    the program small enough for the instruction cache (a fully unrolled
 //    128-coordinate quantizer stalls on instruction fetch);
 //  * the boundary count of each stage is two table reads by warp shuffle
 //    (GridTable in launch.h) plus one compare;
@@ -46,17 +46,17 @@ constexpr int ROW_BYTES = D * 2;
 constexpr int ROW_STRIDE = ROW_BYTES + 16;
 constexpr int STAGE_BYTES = 32 * ROW_STRIDE;
 
-// Encoder shared memory, per warp: ENC_STAGES input blocks, the half-row
-// scratch (16 float4 chunks x 32 lanes), two word-staging arrays with one pad
+// Encoder shared memory, per warp: ENC_STAGES input blocks, the quarter-row
+// scratch (8 float4 chunks x 32 lanes), two word-staging arrays with one pad
 // word per row, and the norms of rows redone by the exact path.
 constexpr int ENC_STAGES = 2;
-constexpr int YH_BYTES = 16 * 32 * 16;
+constexpr int YH_BYTES = 8 * 32 * 16;
 __host__ __device__ constexpr int enc_words(int bits) { return D * bits / 32; }
 __host__ __device__ constexpr int enc_warp_bytes(int bits)
 {
     return ENC_STAGES * STAGE_BYTES + YH_BYTES + 2 * 32 * (enc_words(bits) + 1) * 4 + 32 * 4;
 }
-__host__ __device__ constexpr int enc_warps(int bits) { return bits == 4 ? 7 : 8; }
+__host__ __device__ constexpr int enc_warps(int) { return 8; }
 __host__ __device__ constexpr int enc_smem(int bits)
 {
     return enc_warps(bits) * (enc_warp_bytes(bits) + ENC_STAGES * 8);
@@ -119,6 +119,42 @@ __device__ __forceinline__ int stage_code_df(float vh, float vl, float tb, int t
         return code;
     }
 }
+
+// Symmetric 1- and 2-bit codebooks (c[k] = -c[L-1-k], middle boundary 0) are
+// quantized without tables: |y| is compared with the one positive boundary and
+// the code bits are sign bits.  Codes are built MSB-first by left funnel
+// shifts of sign bits, elements of a word in reverse order, and the word is
+// complemented at the end (the sign bit is the complement of "greater").
+//   b = 2:  i = y > 0 ? 2 + u : 1 - u,  u = |y| > B   (bits: !sgn(y), !(sgn(y) ^ sgn(|y| - B)))
+//   b = 1:  i = y > 0                                   (bit: !sgn(y))
+// The residual of stage 1 is r = sgn(y) (|y| - c) with c the positive centroid.
+__device__ __forceinline__ void sym2_code(float y, float B, float c2, float c3, float E2,
+                                          uint32_t &a1, uint32_t &a2, float &m)
+{
+    const float t1 = fabsf(y) - B;
+    m = fminf(m, fabsf(y));
+    m = fminf(m, fabsf(t1));
+    const float ra = fabsf(y) - (t1 > 0.0f ? c3 : c2);
+    const float t2 = fabsf(ra) - E2;
+    m = fminf(m, fabsf(ra));
+    m = fminf(m, fabsf(t2));
+    const uint32_t yb = __float_as_uint(y), rb = __float_as_uint(ra);
+    a1 = __funnelshift_l(yb, a1, 1);
+    a1 = __funnelshift_l(yb ^ __float_as_uint(t1), a1, 1);
+    a2 = __funnelshift_l(yb ^ rb, a2, 1);
+    a2 = __funnelshift_l(yb ^ rb ^ __float_as_uint(t2), a2, 1);
+}
+
+__device__ __forceinline__ void sym1_code(float y, float c1, uint32_t &a1, uint32_t &a2, float &m)
+{
+    const float r = y - copysignf(c1, y);
+    m = fminf(m, fabsf(y));
+    m = fminf(m, fabsf(r));
+    a1 = __funnelshift_l(__float_as_uint(y), a1, 1);
+    a2 = __funnelshift_l(__float_as_uint(r), a2, 1);
+}
+
+enum { MODE_PLAIN = 0, MODE_GRID = 1, MODE_SYM = 2 };
 
 // Destination row of source row `row`; false if its batch offset is invalid.
 __device__ __forceinline__ bool rvq_dst_row(const RvqEncodeParams &p, int row, size_t &drow)
@@ -277,10 +313,11 @@ __device__ __noinline__ void rvq_fixup_row(const RvqEncodeParams &p, const unsig
     if (lane == 0) nrm[r] = __fadd_rn(nh, nl);
 }
 
-template <int BITS, bool GRID>
+template <int BITS, int MODE>
 __global__ void __launch_bounds__(enc_warps(BITS) * 32, 1)
     rvq_encode_kernel(const __grid_constant__ RvqEncodeParams p)
 {
+    constexpr bool GRID = MODE == MODE_GRID;
     constexpr int L = 1 << BITS;
     constexpr int E = 32 / BITS;
     constexpr int W = D * BITS / 32;
@@ -404,35 +441,64 @@ __global__ void __launch_bounds__(enc_warps(BITS) * 32, 1)
             v[k] = make_float2(a + b, a - b);
         }
 
-        // ---- two-stage boundary count and LSB-first packing, one half-row at
-        // a time through the thread's scratch chunks yh[c * 32 + lane]
+        // ---- two-stage boundary count and LSB-first packing, one quarter-row
+        // (32 coordinates) at a time through the thread's scratch chunks
+        // yh[c * 32 + lane]; quarter q holds coordinates 32q .. 32q + 31
         float m = __int_as_float(0x7f800000);
+#pragma unroll 1
+        for (int qt = 0; qt < 4; ++qt) {
+            if (qt == 0) {
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
+                for (int c = 0; c < 8; ++c)
+                    yh[c * 32 + lane] = make_float4(v[4 * c].x, v[4 * c + 1].x, v[4 * c + 2].x, v[4 * c + 3].x);
+            } else if (qt == 1) {
 #pragma unroll
-            for (int c = 0; c < 16; ++c) {
-                yh[c * 32 + lane] = half == 0
-                    ? make_float4(v[4 * c].x, v[4 * c + 1].x, v[4 * c + 2].x, v[4 * c + 3].x)
-                    : make_float4(v[4 * c].y, v[4 * c + 1].y, v[4 * c + 2].y, v[4 * c + 3].y);
+                for (int c = 0; c < 8; ++c)
+                    yh[c * 32 + lane] = make_float4(v[32 + 4 * c].x, v[33 + 4 * c].x, v[34 + 4 * c].x, v[35 + 4 * c].x);
+            } else if (qt == 2) {
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    yh[c * 32 + lane] = make_float4(v[4 * c].y, v[4 * c + 1].y, v[4 * c + 2].y, v[4 * c + 3].y);
+            } else {
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    yh[c * 32 + lane] = make_float4(v[32 + 4 * c].y, v[33 + 4 * c].y, v[34 + 4 * c].y, v[35 + 4 * c].y);
             }
 #pragma unroll 1
-            for (int w = 0; w < W / 2; ++w) {
+            for (int w = 0; w < W / 4; ++w) {
                 uint32_t a1 = 0u, a2 = 0u;
+                if constexpr (MODE == MODE_SYM) {
 #pragma unroll
-                for (int cc = 0; cc < E / 4; ++cc) {
-                    const float4 q4 = yh[(w * (E / 4) + cc) * 32 + lane];
-                    const float ys[4] = {q4.x, q4.y, q4.z, q4.w};
+                    for (int cc = E / 4 - 1; cc >= 0; --cc) {
+                        const float4 q4 = yh[(w * (E / 4) + cc) * 32 + lane];
+                        const float ys[4] = {q4.x, q4.y, q4.z, q4.w};
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const int code1 = stage_code<BITS, GRID>(ys[j], tb1, tc1, p.t1, p.b1, m);
-                        const float rr = ys[j] - __shfl_sync(FULL_MASK, tcen, code1);
-                        const int code2 = stage_code<BITS, GRID>(rr, tb2, tc2, p.t2, p.b2, m);
-                        a1 = __funnelshift_r(a1, (uint32_t)code1, BITS);
-                        a2 = __funnelshift_r(a2, (uint32_t)code2, BITS);
+                        for (int j = 3; j >= 0; --j) {
+                            if constexpr (BITS == 2)
+                                sym2_code(ys[j], p.b1[2], p.c1[2], p.c1[3], p.b2[2], a1, a2, m);
+                            else
+                                sym1_code(ys[j], p.c1[1], a1, a2, m);
+                        }
+                    }
+                    a1 = ~a1;
+                    a2 = ~a2;
+                } else {
+#pragma unroll
+                    for (int cc = 0; cc < E / 4; ++cc) {
+                        const float4 q4 = yh[(w * (E / 4) + cc) * 32 + lane];
+                        const float ys[4] = {q4.x, q4.y, q4.z, q4.w};
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const int code1 = stage_code<BITS, GRID>(ys[j], tb1, tc1, p.t1, p.b1, m);
+                            const float rr = ys[j] - __shfl_sync(FULL_MASK, tcen, code1);
+                            const int code2 = stage_code<BITS, GRID>(rr, tb2, tc2, p.t2, p.b2, m);
+                            a1 = __funnelshift_r(a1, (uint32_t)code1, BITS);
+                            a2 = __funnelshift_r(a2, (uint32_t)code2, BITS);
+                        }
                     }
                 }
-                o1[lane * (W + 1) + half * (W / 2) + w] = a1;
-                o2[lane * (W + 1) + half * (W / 2) + w] = a2;
+                o1[lane * (W + 1) + qt * (W / 4) + w] = a1;
+                o2[lane * (W + 1) + qt * (W / 4) + w] = a2;
             }
         }
         const bool flag = valid && !(m >= p.guard);
@@ -615,10 +681,10 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) rvq_decode_kernel(const __g
     }
 }
 
-template <int BITS, bool GRID>
+template <int BITS, int MODE>
 cudaError_t launch_enc(const RvqEncodeParams &p, cudaStream_t stream)
 {
-    auto kern = rvq_encode_kernel<BITS, GRID>;
+    auto kern = rvq_encode_kernel<BITS, MODE>;
     constexpr int smem = enc_smem(BITS);
     constexpr int warps = enc_warps(BITS);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -650,13 +716,18 @@ cudaError_t launch_dec(const RvqDecodeParams &p, cudaStream_t stream)
 
 }  // namespace
 
-cudaError_t launch_rvq_encode(const RvqEncodeParams &p, int bits, bool use_grid, cudaStream_t stream)
+cudaError_t launch_rvq_encode(const RvqEncodeParams &p, int bits, int mode, cudaStream_t stream)
 {
     if (p.N <= 0) return cudaSuccess;
-    switch (bits) {
-    case 1: return use_grid ? launch_enc<1, true>(p, stream) : launch_enc<1, false>(p, stream);
-    case 2: return use_grid ? launch_enc<2, true>(p, stream) : launch_enc<2, false>(p, stream);
-    case 4: return use_grid ? launch_enc<4, true>(p, stream) : launch_enc<4, false>(p, stream);
+    switch (bits * 4 + mode) {
+    case 1 * 4 + MODE_PLAIN: return launch_enc<1, MODE_PLAIN>(p, stream);
+    case 1 * 4 + MODE_GRID: return launch_enc<1, MODE_GRID>(p, stream);
+    case 1 * 4 + MODE_SYM: return launch_enc<1, MODE_SYM>(p, stream);
+    case 2 * 4 + MODE_PLAIN: return launch_enc<2, MODE_PLAIN>(p, stream);
+    case 2 * 4 + MODE_GRID: return launch_enc<2, MODE_GRID>(p, stream);
+    case 2 * 4 + MODE_SYM: return launch_enc<2, MODE_SYM>(p, stream);
+    case 4 * 4 + MODE_PLAIN: return launch_enc<4, MODE_PLAIN>(p, stream);
+    case 4 * 4 + MODE_GRID: return launch_enc<4, MODE_GRID>(p, stream);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -100,6 +100,22 @@ def test_encode_custom_codebook_boundary_at_rotated_value(vq, oracle_mod):
     assert np.array_equal(g1[0], ora["idx1"][0])
 
 
+@pytest.mark.parametrize("bits", [1, 2, 4])
+def test_encode_asymmetric_codebook(vq, oracle_mod, bits):
+    """A codebook that is not antisymmetric takes the shuffle-table path."""
+    c1, b1, c2, b2 = [a.copy() for a in oracle_mod.rvq_codebooks(D, bits)[:4]]
+    L = 1 << bits
+    c1[L // 2:] *= np.float32(1.3)
+    b1[L // 2 - 1:] = np.float32(0.5) * (c1[L // 2 - 1:-1] + c1[L // 2:])
+    c2[: L // 2] *= np.float32(0.8)
+    b2[: L // 2] = np.float32(0.5) * (c2[: L // 2] + c2[1: L // 2 + 1])
+    assert np.all(c1[:-1] < b1) and np.all(b1 < c1[1:]) and np.all(c2[:-1] < b2) and np.all(b2 < c2[1:])
+    x = _rows((1, 2, 700), 77 + bits)
+    p1, p2, n = _encode(vq, x, bits, (c1, b1, c2, b2))
+    ora = oracle_mod.rvq_encode(x.reshape(-1, D), bits, c1, b1, c2, b2)
+    check_rvq(p1, p2, n, ora, bits)
+
+
 @pytest.mark.parametrize("bits", [2, 4])
 def test_encode_plain_count_fallback(vq, oracle_mod, bits):
     """A codebook with two boundaries inside one guard band has no lookup
