@@ -92,6 +92,15 @@ __device__ __forceinline__ uint64_t l2_policy_evict_first()
     return pol;
 }
 
+// fp32 sum of an fp16 value and an fp32 value with one rounding (the fp16
+// operand is read directly, without a separate conversion).
+__device__ __forceinline__ float add_f16_f32(__half a, float c)
+{
+    float r;
+    asm("add.rn.f32.f16 %0, %1, %2;" : "=f"(r) : "h"(__half_as_ushort(a)), "f"(c));
+    return r;
+}
+
 // Error-free transformations (Knuth TwoSum, Dekker Fast2Sum) for the
 // extended-precision recompute paths.
 __device__ __forceinline__ void two_sum(float a, float b, float &s, float &e)

@@ -52,6 +52,18 @@ struct GroupQ {
     __half scale_h, zero_h;
 };
 
+// 1.5 * 2^23 - 1: fma(A, f, MAGIC1) holds MAGIC - 1 + rint(A f) exactly.
+constexpr float MAGIC1 = 12582911.0f;
+// Saturated step: sat(z * 2^40 + 1/2) is 0 for z < 0, 1/2 for z == 0 and 1 for
+// z > 0 whenever |z| >= 2^-41; the tie quantities below are multiples of
+// 2^-25 (fp16 data), so nothing smaller than that occurs.
+constexpr float STEP_SCALE = 1099511627776.0f;
+
+__device__ __forceinline__ float step_half(float z)
+{
+    return __saturatef(fmaf(z, STEP_SCALE, 0.5f));
+}
+
 // RN32 of the exact (mx - mn)/c, given fp16-valued mx > mn.
 __device__ __noinline__ float exact_scale32_slow(float mx, float mn, float c)
 {
@@ -113,27 +125,33 @@ __device__ __noinline__ uint32_t code_int64(float x, float mn, float mx)
     return q;
 }
 
-// Exact code of one element of a `fast` group.  r is the nearest integer to
-// the fp32 estimate of t; the threshold r - 1/2 counts when
-// C A - (r - 1/2) R > 0, or = 0 with r even (tie to the even r), and r + 1/2
-// counts when C A - (r + 1/2) R > 0, or = 0 with r odd (tie to the even r + 1).
-// "or = 0" is a comparison against the negative subnormal of smallest
-// magnitude, which only an exact zero exceeds among these values.
+// Exact codes of two elements of a `fast` group, returned in the low bits of
+// qa / qb.  With r = rint(A f) (the fp32 estimate of t rounded), u = C A - r R,
+//   q = r - 1 + step(u + R/2) + step(u - R/2)
+// where step is 0 / 1/2 / 1 for a negative / zero / positive argument: the two
+// terms test t against r - 1/2 and r + 1/2 (exact signs when C A and R are
+// exact, which holds for every exact tie of a fast group), and a tie leaves a
+// half that the final round-to-nearest-even addition resolves to the even
+// neighbour.  Everything runs on the FMA pipe, two elements per instruction
+// where the operation exists for fp32 pairs.
 template <int BITS>
-__device__ __forceinline__ uint32_t code_exact(float x, const GroupQ &g)
+__device__ __forceinline__ void code_pair(__half a, __half b, const GroupQ &g, uint32_t &qa,
+                                          uint32_t &qb)
 {
     constexpr float C = (float)((1 << BITS) - 1);
-    const float A = x - g.mn;
-    const float tm = A * g.f + MAGIC;           // rint of the estimate, in the low bits
-    const float r = tm - MAGIC;
-    const float ca = A * C;
-    const float zl = fmaf(-(r - 0.5f), g.rr, ca);
-    const float zr = fmaf(-(r + 0.5f), g.rr, ca);
-    const int ri = __float_as_int(tm) - 0x4B400000;
-    const uint32_t odd = (uint32_t)ri & 1u;
-    const float thl = __uint_as_float((1u - odd) * 0x80000001u);  // -0 (no tie credit) or -tiny
-    const float thr = __uint_as_float(odd * 0x80000001u);
-    return (uint32_t)(ri - 1 + (zl > thl ? 1 : 0) + (zr > thr ? 1 : 0));
+    const float2 A = make_float2(add_f16_f32(a, -g.mn), add_f16_f32(b, -g.mn));
+    const float2 tm = __ffma2_rn(A, make_float2(g.f, g.f), make_float2(MAGIC1, MAGIC1));
+    const float2 r = __fadd2_rn(tm, make_float2(-MAGIC1, -MAGIC1));
+    const float2 ca = __fmul2_rn(A, make_float2(C, C));
+    const float2 u = __ffma2_rn(r, make_float2(-g.rr, -g.rr), ca);
+    const float h = 0.5f * g.rr;
+    const float2 zl = __fadd2_rn(u, make_float2(h, h));
+    const float2 zr = __fadd2_rn(u, make_float2(-h, -h));
+    const float2 st = __fadd2_rn(make_float2(step_half(zl.x), step_half(zl.y)),
+                                 make_float2(step_half(zr.x), step_half(zr.y)));
+    const float2 qm = __fadd2_rn(tm, st);  // MAGIC + q, ties to even
+    qa = __float_as_uint(qm.x);
+    qb = __float_as_uint(qm.y);
 }
 
 // fp16(q*s + z) rounded once from the exact value: q*s is exact in fp32, the
@@ -301,9 +319,10 @@ __global__ void __launch_bounds__(VAL_WARPS * 32, 1)
                         const __half2 *hh = reinterpret_cast<const __half2 *>(&c);
 #pragma unroll
                         for (int k = 0; k < 4; ++k) {
-                            const float2 v = __half22float2(hh[k]);
-                            word = __funnelshift_r(word, code_exact<BITS>(v.x, g), BITS);
-                            word = __funnelshift_r(word, code_exact<BITS>(v.y, g), BITS);
+                            uint32_t qa, qb;
+                            code_pair<BITS>(__low2half(hh[k]), __high2half(hh[k]), g, qa, qb);
+                            word = __funnelshift_r(word, qa, BITS);
+                            word = __funnelshift_r(word, qb, BITS);
                         }
                     }
                 } else {  // rare: a range that fp32 does not hold exactly
@@ -468,22 +487,24 @@ __global__ void __launch_bounds__(key_warps<G>() * 32, 1)
             uint32_t w0 = 0u, w1 = 0u, w2 = 0u, w3 = 0u;
             if (allfast) {
 #pragma unroll
-                for (int j = 0; j < E; ++j) {
+                for (int j = 0; j < E; j += 2) {
                     const int i = k * E + j;
-                    uint32_t c0 = 0, c1 = 0, c2 = 0, c3 = 0;
+                    uint32_t c0a = 0, c0b = 0, c1a = 0, c1b = 0, c2a = 0, c2b = 0, c3a = 0, c3b = 0;
                     if (i < ntok) {
-                        uint2 r = col[i * (ROW_BYTES / 8)];
-                        const float2 a = __half22float2(*reinterpret_cast<__half2 *>(&r.x));
-                        const float2 b = __half22float2(*reinterpret_cast<__half2 *>(&r.y));
-                        c0 = code_exact<BITS>(a.x, gq[0]);
-                        c1 = code_exact<BITS>(a.y, gq[1]);
-                        c2 = code_exact<BITS>(b.x, gq[2]);
-                        c3 = code_exact<BITS>(b.y, gq[3]);
+                        uint2 ra = col[i * (ROW_BYTES / 8)];
+                        uint2 rb = (i + 1 < ntok) ? col[(i + 1) * (ROW_BYTES / 8)] : ra;
+                        const __half2 a01 = *reinterpret_cast<__half2 *>(&ra.x), a23 = *reinterpret_cast<__half2 *>(&ra.y);
+                        const __half2 b01 = *reinterpret_cast<__half2 *>(&rb.x), b23 = *reinterpret_cast<__half2 *>(&rb.y);
+                        code_pair<BITS>(__low2half(a01), __low2half(b01), gq[0], c0a, c0b);
+                        code_pair<BITS>(__high2half(a01), __high2half(b01), gq[1], c1a, c1b);
+                        code_pair<BITS>(__low2half(a23), __low2half(b23), gq[2], c2a, c2b);
+                        code_pair<BITS>(__high2half(a23), __high2half(b23), gq[3], c3a, c3b);
+                        if (i + 1 >= ntok) c0b = c1b = c2b = c3b = 0u;
                     }
-                    w0 = __funnelshift_r(w0, c0, BITS);
-                    w1 = __funnelshift_r(w1, c1, BITS);
-                    w2 = __funnelshift_r(w2, c2, BITS);
-                    w3 = __funnelshift_r(w3, c3, BITS);
+                    w0 = __funnelshift_r(__funnelshift_r(w0, c0a, BITS), c0b, BITS);
+                    w1 = __funnelshift_r(__funnelshift_r(w1, c1a, BITS), c1b, BITS);
+                    w2 = __funnelshift_r(__funnelshift_r(w2, c2a, BITS), c2b, BITS);
+                    w3 = __funnelshift_r(__funnelshift_r(w3, c3a, BITS), c3b, BITS);
                 }
             } else {  // rare: some channel's range is not held exactly by fp32
                 uint32_t rw[4] = {0u, 0u, 0u, 0u};
@@ -493,8 +514,13 @@ __global__ void __launch_bounds__(key_warps<G>() * 32, 1)
                         const int i = k * E + j;
                         if (i >= ntok) break;
                         const float xv = __half2float(tokh[i * D + 4 * lane + c]);
-                        const uint32_t q = gq[c].fast ? code_exact<BITS>(xv, gq[c])
-                                                      : code_int64<BITS>(xv, gq[c].mn, mxv[c]);
+                        uint32_t q, qdummy;
+                        if (gq[c].fast) {
+                            code_pair<BITS>(__float2half_rn(xv), __float2half_rn(xv), gq[c], q, qdummy);
+                            q &= (1u << BITS) - 1u;
+                        } else {
+                            q = code_int64<BITS>(xv, gq[c].mn, mxv[c]);
+                        }
                         rw[c] |= q << (j * BITS);
                     }
                 }
@@ -535,12 +561,34 @@ __host__ __device__ constexpr int vdq_slot(int bits) { return (D * bits / 32) * 
 __host__ __device__ constexpr int vdq_warp_bytes(int bits) { return VDQ_STAGES * 32 * vdq_slot(bits) + 32 * ROW_STRIDE; }
 __host__ __device__ constexpr int vdq_smem(int bits) { return VDQ_WARPS * (vdq_warp_bytes(bits) + VDQ_STAGES * 8); }
 
+// One group of a row whose q*s + z is not exact in fp32 (rare): every element
+// goes through recon_exact.  wg: the group's words; out: its 16-byte output
+// chunks in the staging row.
+template <int BITS, int G>
+__device__ __noinline__ void vdq_group_exact(const uint32_t *wg, float s, float z, uint4 *out)
+{
+    constexpr int E = 32 / BITS;
+    constexpr uint32_t MASK = (1u << BITS) - 1u;
+    for (int c = 0; c < G / 8; ++c) {
+        uint32_t o[4];
+        for (int j = 0; j < 4; ++j) {
+            const int e = 8 * c + 2 * j;
+            const uint32_t q0 = (wg[e / E] >> ((e % E) * BITS)) & MASK;
+            const uint32_t q1 = (wg[(e + 1) / E] >> (((e + 1) % E) * BITS)) & MASK;
+            const __half2 hv = __halves2half2(recon_exact(q0, s, z), recon_exact(q1, s, z));
+            o[j] = *reinterpret_cast<const uint32_t *>(&hv);
+        }
+        out[c] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+}
+
 template <int BITS, int G>
 __global__ void __launch_bounds__(VDQ_WARPS * 32, 1) kivi_values_dequant_kernel(const __grid_constant__ KiviDequantParams p)
 {
     constexpr int E = 32 / BITS;
     constexpr int W = D * BITS / 32;
     constexpr int NGD = D / G;
+    constexpr int WPG = G * BITS / 32;
     constexpr uint32_t MASK = (1u << BITS) - 1u;
     constexpr int SLOT = vdq_slot(BITS);
     constexpr int WB = vdq_warp_bytes(BITS);
@@ -575,18 +623,28 @@ __global__ void __launch_bounds__(VDQ_WARPS * 32, 1) kivi_values_dequant_kernel(
     }
     const __half *scp = static_cast<const __half *>(p.scale);
     const __half *zrp = static_cast<const __half *>(p.zero);
+    // scale/zero of this lane's row, loaded one block ahead
+    __half sh[NGD], zh[NGD];
+    auto load_sz = [&](int blk) {
+        const int row = (blk << 5) + lane;
+#pragma unroll
+        for (int j = 0; j < NGD; ++j) {
+            sh[j] = (blk < nblk && row < N) ? scp[(size_t)row * NGD + j] : __float2half_rn(0.0f);
+            zh[j] = (blk < nblk && row < N) ? zrp[(size_t)row * NGD + j] : __float2half_rn(0.0f);
+        }
+    };
+    load_sz(gw);
     for (int it = 0;; ++it) {
         const int blk = gw + it * tw;
         if (blk >= nblk) break;
         const int s = it % VDQ_STAGES;
-        const int row = (blk << 5) + lane;
-        const bool valid = row < N;
         float sf[NGD], zf[NGD];
 #pragma unroll
         for (int j = 0; j < NGD; ++j) {
-            sf[j] = valid ? __half2float(scp[(size_t)row * NGD + j]) : 0.0f;
-            zf[j] = valid ? __half2float(zrp[(size_t)row * NGD + j]) : 0.0f;
+            sf[j] = __half2float(sh[j]);
+            zf[j] = __half2float(zh[j]);
         }
+        load_sz(blk + tw);
         const bool ok = mbar_wait_bounded(&bars[s], (uint32_t)(it / VDQ_STAGES) & 1u);
         if (!__all_sync(FULL_MASK, ok)) {
             if (lane == 0) atomicOr(&g_kivi_err, (unsigned)VQ_DEVERR_WAIT_TIMEOUT);
@@ -597,13 +655,38 @@ __global__ void __launch_bounds__(VDQ_WARPS * 32, 1) kivi_values_dequant_kernel(
             }
             return;
         }
-        uint32_t words[W];
-        {
-            const uint4 *sl = reinterpret_cast<const uint4 *>(wbuf + s * 32 * SLOT + lane * SLOT);
+        const uint32_t *wrow = reinterpret_cast<const uint32_t *>(wbuf + s * 32 * SLOT + lane * SLOT);
+        uint4 *orow = reinterpret_cast<uint4 *>(obuf + lane * ROW_STRIDE);
 #pragma unroll
-            for (int i = 0; i < W / 4; ++i) {
-                const uint4 a = sl[i];
-                words[4 * i] = a.x; words[4 * i + 1] = a.y; words[4 * i + 2] = a.z; words[4 * i + 3] = a.w;
+        for (int j = 0; j < NGD; ++j) {
+            if (group_sum_exact<BITS>(sf[j], zf[j])) {
+                uint32_t wg[WPG];
+#pragma unroll
+                for (int i = 0; i < WPG; i += 4) {
+                    if constexpr (WPG >= 4) {
+                        const uint4 a = *reinterpret_cast<const uint4 *>(wrow + j * WPG + i);
+                        wg[i] = a.x; wg[i + 1] = a.y; wg[i + 2] = a.z; wg[i + 3] = a.w;
+                    }
+                }
+                if constexpr (WPG < 4) {
+#pragma unroll
+                    for (int i = 0; i < WPG; ++i) wg[i] = wrow[j * WPG + i];
+                }
+#pragma unroll
+                for (int c = 0; c < G / 8; ++c) {
+                    uint32_t o[4];
+#pragma unroll
+                    for (int jj = 0; jj < 4; ++jj) {
+                        const int e = 8 * c + 2 * jj;
+                        const uint32_t q0 = (wg[e / E] >> ((e % E) * BITS)) & MASK;
+                        const uint32_t q1 = (wg[(e + 1) / E] >> (((e + 1) % E) * BITS)) & MASK;
+                        const __half2 hv = __floats2half2_rn(fmaf((float)q0, sf[j], zf[j]), fmaf((float)q1, sf[j], zf[j]));
+                        o[jj] = *reinterpret_cast<const uint32_t *>(&hv);
+                    }
+                    orow[j * (G / 8) + c] = make_uint4(o[0], o[1], o[2], o[3]);
+                }
+            } else {
+                vdq_group_exact<BITS, G>(wrow + j * WPG, sf[j], zf[j], orow + j * (G / 8));
             }
         }
         __syncwarp();
@@ -612,30 +695,6 @@ __global__ void __launch_bounds__(VDQ_WARPS * 32, 1) kivi_values_dequant_kernel(
             const int nb = blk + VDQ_STAGES * tw;
             if (nb < nblk) issue(nb, s);
         }
-        bool exact[NGD];
-#pragma unroll
-        for (int j = 0; j < NGD; ++j) exact[j] = group_sum_exact<BITS>(sf[j], zf[j]);
-        uint4 *orow = reinterpret_cast<uint4 *>(obuf + lane * ROW_STRIDE);
-#pragma unroll
-        for (int c = 0; c < 16; ++c) {
-            uint32_t out[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int e = 8 * c + 2 * j;
-                const float sv = sf[e / G], zv = zf[e / G];
-                const uint32_t q0 = (words[e / E] >> ((e % E) * BITS)) & MASK;
-                const uint32_t q1 = (words[(e + 1) / E] >> (((e + 1) % E) * BITS)) & MASK;
-                __half2 hv;
-                if (exact[e / G]) {
-                    hv = __floats2half2_rn(fmaf((float)q0, sv, zv), fmaf((float)q1, sv, zv));
-                } else {
-                    hv = __halves2half2(recon_exact(q0, sv, zv), recon_exact(q1, sv, zv));
-                }
-                out[j] = *reinterpret_cast<const uint32_t *>(&hv);
-            }
-            orow[c] = make_uint4(out[0], out[1], out[2], out[3]);
-        }
-        __syncwarp();
         const int nrows = min(32, N - (blk << 5));
         uint4 *gout = reinterpret_cast<uint4 *>(static_cast<__half *>(p.out) + (size_t)(blk << 5) * D);
 #pragma unroll

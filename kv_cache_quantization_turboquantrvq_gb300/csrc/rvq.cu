@@ -128,26 +128,36 @@ __device__ __forceinline__ int stage_code_df(float vh, float vl, float tb, int t
 //   b = 2:  i = y > 0 ? 2 + u : 1 - u,  u = |y| > B   (bits: !sgn(y), !(sgn(y) ^ sgn(|y| - B)))
 //   b = 1:  i = y > 0                                   (bit: !sgn(y))
 // The residual of stage 1 is r = sgn(y) (|y| - c) with c the positive centroid.
-__device__ __forceinline__ void sym2_code(float y, float B, float c2, float c3, float E2,
-                                          uint32_t &a1, uint32_t &a2, float &m)
+// Per-row constants of the symmetric quantizers, in units of S = H x (the
+// unnormalised transform, S = y n sqrt(D)): hb = B/2, c2, dc = c3 - c2 and
+// he = E/2 scaled by den = n sqrt(D).
+struct SymRow {
+    float hb, c2, dc, he, c1;
+};
+
+// The distance from |y| to the nearest of {0, B} is | | |y| - B/2 | - B/2 |,
+// and the same quantity t2 = | |y| - B/2 | - B/2 is positive exactly when
+// |y| > B, so one value gives both the decision and the margin.  The centroid
+// step uses a saturated multiply (1 when t2 > 0, 0 when t2 <= 0), which keeps
+// the selection on the FMA pipe.
+__device__ __forceinline__ void sym2_code(float y, const SymRow &k, uint32_t &a1, uint32_t &a2, float &m)
 {
-    const float t1 = fabsf(y) - B;
-    m = fminf(m, fabsf(y));
-    m = fminf(m, fabsf(t1));
-    const float ra = fabsf(y) - (t1 > 0.0f ? c3 : c2);
-    const float t2 = fabsf(ra) - E2;
-    m = fminf(m, fabsf(ra));
+    const float t2 = fabsf(fabsf(y) - k.hb) - k.hb;
     m = fminf(m, fabsf(t2));
+    const float su = __saturatef(t2 * 1.2676506e30f);  // 2^100
+    const float ra = fmaf(-k.dc, su, fabsf(y) - k.c2);
+    const float t4 = fabsf(fabsf(ra) - k.he) - k.he;
+    m = fminf(m, fabsf(t4));
     const uint32_t yb = __float_as_uint(y), rb = __float_as_uint(ra);
     a1 = __funnelshift_l(yb, a1, 1);
-    a1 = __funnelshift_l(yb ^ __float_as_uint(t1), a1, 1);
+    a1 = __funnelshift_l(yb ^ __float_as_uint(t2), a1, 1);
     a2 = __funnelshift_l(yb ^ rb, a2, 1);
-    a2 = __funnelshift_l(yb ^ rb ^ __float_as_uint(t2), a2, 1);
+    a2 = __funnelshift_l(yb ^ rb ^ __float_as_uint(t4), a2, 1);
 }
 
-__device__ __forceinline__ void sym1_code(float y, float c1, uint32_t &a1, uint32_t &a2, float &m)
+__device__ __forceinline__ void sym1_code(float y, const SymRow &k, uint32_t &a1, uint32_t &a2, float &m)
 {
-    const float r = y - copysignf(c1, y);
+    const float r = y - copysignf(k.c1, y);
     m = fminf(m, fabsf(y));
     m = fminf(m, fabsf(r));
     a1 = __funnelshift_l(__float_as_uint(y), a1, 1);
@@ -386,25 +396,25 @@ __global__ void __launch_bounds__(enc_warps(BITS) * 32, 1)
         const int row = (blk << 5) + lane;
         const bool valid = row < p.N;
 
-        // ---- load the row: v[k] = (x[k], x[k + 64])
+        // ---- load the row and run the first butterfly stage (coordinate bit
+        // 6) on the fp16 values: v[k] = (x[k] + x[k+64], x[k] - x[k+64]),
+        // converting only x[k+64] and adding x[k] as an fp16 operand.
         const uint4 *srow = reinterpret_cast<const uint4 *>(sbuf + lane * ROW_STRIDE);
         float2 v[64];
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
             const uint4 lo = srow[c];
             const uint4 hi = srow[c + 8];
-            const __half2 *hl = reinterpret_cast<const __half2 *>(&lo);
-            const __half2 *hh = reinterpret_cast<const __half2 *>(&hi);
+            const __half *hl = reinterpret_cast<const __half *>(&lo);
+            const __half *hh = reinterpret_cast<const __half *>(&hi);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float2 a = __half22float2(hl[j]);
-                const float2 b = __half22float2(hh[j]);
-                v[8 * c + 2 * j] = make_float2(a.x, b.x);
-                v[8 * c + 2 * j + 1] = make_float2(a.y, b.y);
+            for (int j = 0; j < 8; ++j) {
+                const float b = __half2float(hh[j]);
+                v[8 * c + j] = make_float2(add_f16_f32(hl[j], b), add_f16_f32(hl[j], -b));
             }
         }
 
-        // ---- norm (16 partial sums) and 1/(n sqrt(D))
+        // ---- norm: sum of squares of the stage outputs is twice sum x^2
         float2 acc[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) acc[i] = make_float2(0.0f, 0.0f);
@@ -415,14 +425,18 @@ __global__ void __launch_bounds__(enc_warps(BITS) * 32, 1)
         acc[0] = __fadd2_rn(acc[0], acc[2]);
         acc[1] = __fadd2_rn(acc[1], acc[3]);
         acc[0] = __fadd2_rn(acc[0], acc[1]);
-        const float q = acc[0].x + acc[0].y;
+        const float q = 0.5f * (acc[0].x + acc[0].y);
         const float n = __fsqrt_rn(q);
-        const float inv = q > 0.0f ? __frcp_rn(n * SQRT_D_HI) : 0.0f;
-        const float2 inv2 = make_float2(inv, inv);
+        const float den = n * SQRT_D_HI;
+        if constexpr (MODE != MODE_SYM) {
+            // table and plain modes quantize y = S / den
+            const float inv = q > 0.0f ? __frcp_rn(den) : 0.0f;
+            const float2 inv2 = make_float2(inv, inv);
 #pragma unroll
-        for (int k = 0; k < 64; ++k) v[k] = __fmul2_rn(v[k], inv2);
+            for (int k = 0; k < 64; ++k) v[k] = __fmul2_rn(v[k], inv2);
+        }
 
-        // ---- Walsh-Hadamard: index bits 0-5 across the float2 array, bit 6 inside
+        // ---- remaining butterfly stages: index bits 0-5 across the float2 array
         const float2 neg1 = make_float2(-1.0f, -1.0f);
 #pragma unroll
         for (int h = 1; h < 64; h <<= 1) {
@@ -435,11 +449,14 @@ __global__ void __launch_bounds__(enc_warps(BITS) * 32, 1)
                 }
             }
         }
-#pragma unroll
-        for (int k = 0; k < 64; ++k) {
-            const float a = v[k].x, b = v[k].y;
-            v[k] = make_float2(a + b, a - b);
-        }
+        // symmetric modes quantize S itself against thresholds scaled by den
+        SymRow sk;
+        sk.hb = 0.5f * p.b1[(1 << BITS) - 2] * den;
+        sk.c2 = p.c1[(1 << BITS) - 2] * den;
+        sk.dc = (p.c1[(1 << BITS) - 1] - p.c1[(1 << BITS) - 2]) * den;
+        sk.he = 0.5f * p.b2[(1 << BITS) - 2] * den;
+        sk.c1 = p.c1[(1 << BITS) - 1] * den;
+        const float guard = MODE == MODE_SYM ? p.guard * den : p.guard;
 
         // ---- two-stage boundary count and LSB-first packing, one quarter-row
         // (32 coordinates) at a time through the thread's scratch chunks
@@ -475,9 +492,9 @@ __global__ void __launch_bounds__(enc_warps(BITS) * 32, 1)
 #pragma unroll
                         for (int j = 3; j >= 0; --j) {
                             if constexpr (BITS == 2)
-                                sym2_code(ys[j], p.b1[2], p.c1[2], p.c1[3], p.b2[2], a1, a2, m);
+                                sym2_code(ys[j], sk, a1, a2, m);
                             else
-                                sym1_code(ys[j], p.c1[1], a1, a2, m);
+                                sym1_code(ys[j], sk, a1, a2, m);
                         }
                     }
                     a1 = ~a1;
@@ -501,7 +518,8 @@ __global__ void __launch_bounds__(enc_warps(BITS) * 32, 1)
                 o2[lane * (W + 1) + qt * (W / 4) + w] = a2;
             }
         }
-        const bool flag = valid && !(m >= p.guard);
+        // a zero row has no direction: always take the exact path for it
+        const bool flag = valid && (!(m >= guard) || !(q > 0.0f));
 
         // ---- rows with a value inside the guard band: exact recompute by the warp
         __syncwarp();
@@ -651,16 +669,18 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) rvq_decode_kernel(const __g
                 }
             }
         }
+        // last butterfly stage with the scale n / sqrt(D) applied to its inputs
         const float sc = __fdiv_rn(n, SQRT_D_HI);
+        const float2 sc2 = make_float2(sc, sc);
         uint4 *orow = reinterpret_cast<uint4 *>(obuf + lane * ROW_STRIDE);
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
             uint32_t lo[4], hi[4];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                const float2 a = v[8 * c + 2 * j], b = v[8 * c + 2 * j + 1];
-                const __half2 l2 = __floats2half2_rn((a.x + a.y) * sc, (b.x + b.y) * sc);
-                const __half2 h2 = __floats2half2_rn((a.x - a.y) * sc, (b.x - b.y) * sc);
+                const float2 a = __fmul2_rn(v[8 * c + 2 * j], sc2), b = __fmul2_rn(v[8 * c + 2 * j + 1], sc2);
+                const __half2 l2 = __floats2half2_rn(a.x + a.y, b.x + b.y);
+                const __half2 h2 = __floats2half2_rn(a.x - a.y, b.x - b.y);
                 lo[j] = *reinterpret_cast<const uint32_t *>(&l2);
                 hi[j] = *reinterpret_cast<const uint32_t *>(&h2);
             }
