@@ -313,6 +313,9 @@ __global__ void __launch_bounds__(VAL_WARPS * 32, 1)
                 const uint4 *wp = gp + w * (E / 8);
                 uint32_t word = 0u;
                 if (g.fast) {
+                    // two accumulators (first and second half of the word's
+                    // codes) halve the dependent chain of funnel shifts
+                    uint32_t lo = 0u, hi = 0u;
 #pragma unroll
                     for (int i = 0; i < E / 8; ++i) {
                         uint4 c = wp[i];
@@ -321,10 +324,16 @@ __global__ void __launch_bounds__(VAL_WARPS * 32, 1)
                         for (int k = 0; k < 4; ++k) {
                             uint32_t qa, qb;
                             code_pair<BITS>(__low2half(hh[k]), __high2half(hh[k]), g, qa, qb);
-                            word = __funnelshift_r(word, qa, BITS);
-                            word = __funnelshift_r(word, qb, BITS);
+                            if (i < E / 16 || (E == 8 && k < 2)) {
+                                lo = __funnelshift_r(lo, qa, BITS);
+                                lo = __funnelshift_r(lo, qb, BITS);
+                            } else {
+                                hi = __funnelshift_r(hi, qa, BITS);
+                                hi = __funnelshift_r(hi, qb, BITS);
+                            }
                         }
                     }
+                    word = (hi & 0xffff0000u) | (lo >> 16);
                 } else {  // rare: a range that fp32 does not hold exactly
                     for (int e = 0; e < E; ++e)
                         word |= code_int64<BITS>(__half2float(rh[j * G + w * E + e]), mn, mx) << (e * BITS);

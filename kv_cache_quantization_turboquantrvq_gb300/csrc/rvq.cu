@@ -19,10 +19,11 @@
 //  * a thread holds its row as 64 float2 (x[k], x[k+64]) and runs six
 //    butterfly stages with the fp32x2 add/fma instructions and the last
 //    (bit 6) stage in scalar fp32 - no shuffles;
-//  * the rotated row goes to a per-thread shared-memory scratch a quarter at
-//    a time and is quantized by a rolled loop over output words, which keeps
-//    the program small enough for the instruction cache (a fully unrolled
-//    128-coordinate quantizer stalls on instruction fetch);
+//  * the rotated row goes to a per-thread shared-memory scratch as coordinate
+//    pairs (k, k + 64), a slice at a time, and is quantized by a rolled loop
+//    that builds two output words per step (one from each half of the row);
+//    this keeps the program small enough for the instruction cache (a fully
+//    unrolled 128-coordinate quantizer stalls on instruction fetch);
 //  * the boundary count of each stage is two table reads by warp shuffle
 //    (GridTable in launch.h) plus one compare;
 //  * words are staged in shared memory and written out coalesced;
@@ -46,15 +47,17 @@ constexpr int ROW_BYTES = D * 2;
 constexpr int ROW_STRIDE = ROW_BYTES + 16;
 constexpr int STAGE_BYTES = 32 * ROW_STRIDE;
 
-// Encoder shared memory, per warp: ENC_STAGES input blocks, the quarter-row
-// scratch (8 float4 chunks x 32 lanes), two word-staging arrays with one pad
-// word per row, and the norms of rows redone by the exact path.
+// Encoder shared memory, per warp: ENC_STAGES input blocks, the pair
+// scratch (enc_pairs coordinate pairs (k, k + 64) x 32 lanes, 8 bytes each),
+// two word-staging arrays with one pad word per row, and the norms of rows
+// redone by the exact path.
 constexpr int ENC_STAGES = 2;
-constexpr int YH_BYTES = 8 * 32 * 16;
 __host__ __device__ constexpr int enc_words(int bits) { return D * bits / 32; }
+__host__ __device__ constexpr int enc_pairs(int bits) { return 32 / bits > 16 ? 32 / bits : 16; }
+__host__ __device__ constexpr int enc_scratch_bytes(int bits) { return enc_pairs(bits) * 32 * 8; }
 __host__ __device__ constexpr int enc_warp_bytes(int bits)
 {
-    return ENC_STAGES * STAGE_BYTES + YH_BYTES + 2 * 32 * (enc_words(bits) + 1) * 4 + 32 * 4;
+    return ENC_STAGES * STAGE_BYTES + enc_scratch_bytes(bits) + 2 * 32 * (enc_words(bits) + 1) * 4 + 32 * 4;
 }
 __host__ __device__ constexpr int enc_warps(int) { return 8; }
 __host__ __device__ constexpr int enc_smem(int bits)
@@ -337,8 +340,8 @@ __global__ void __launch_bounds__(enc_warps(BITS) * 32, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     unsigned char *wbuf = smem + warp * WB;
-    float4 *yh = reinterpret_cast<float4 *>(wbuf + ENC_STAGES * STAGE_BYTES);
-    uint32_t *o1 = reinterpret_cast<uint32_t *>(wbuf + ENC_STAGES * STAGE_BYTES + YH_BYTES);
+    float2 *yp = reinterpret_cast<float2 *>(wbuf + ENC_STAGES * STAGE_BYTES);
+    uint32_t *o1 = reinterpret_cast<uint32_t *>(wbuf + ENC_STAGES * STAGE_BYTES + enc_scratch_bytes(BITS));
     uint32_t *o2 = o1 + 32 * (W + 1);
     float *nrm = reinterpret_cast<float *>(o2 + 32 * (W + 1));
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + WARPS * WB) + warp * ENC_STAGES;
@@ -458,66 +461,62 @@ __global__ void __launch_bounds__(enc_warps(BITS) * 32, 1)
         sk.c1 = p.c1[(1 << BITS) - 1] * den;
         const float guard = MODE == MODE_SYM ? p.guard * den : p.guard;
 
-        // ---- two-stage boundary count and LSB-first packing, one quarter-row
-        // (32 coordinates) at a time through the thread's scratch chunks
-        // yh[c * 32 + lane]; quarter q holds coordinates 32q .. 32q + 31
-        float m = __int_as_float(0x7f800000);
+        // ---- two-stage boundary count and LSB-first packing.  Slice `ps` of PP
+        // coordinate pairs (k, k + 64), k in [ps*PP, ps*PP + PP), goes to the
+        // scratch yp[i * 32 + lane]; each step of the word loop reads E pairs
+        // and produces word kx = k/E from the first coordinates and word
+        // kx + W/2 from the second ones.
+        constexpr int PP = enc_pairs(BITS);
+        float mx = __int_as_float(0x7f800000), my = mx;
 #pragma unroll 1
-        for (int qt = 0; qt < 4; ++qt) {
-            if (qt == 0) {
+        for (int ps = 0; ps < 64 / PP; ++ps) {
 #pragma unroll
-                for (int c = 0; c < 8; ++c)
-                    yh[c * 32 + lane] = make_float4(v[4 * c].x, v[4 * c + 1].x, v[4 * c + 2].x, v[4 * c + 3].x);
-            } else if (qt == 1) {
+            for (int q4 = 0; q4 < 64 / PP; ++q4) {
+                if (ps == q4) {
 #pragma unroll
-                for (int c = 0; c < 8; ++c)
-                    yh[c * 32 + lane] = make_float4(v[32 + 4 * c].x, v[33 + 4 * c].x, v[34 + 4 * c].x, v[35 + 4 * c].x);
-            } else if (qt == 2) {
-#pragma unroll
-                for (int c = 0; c < 8; ++c)
-                    yh[c * 32 + lane] = make_float4(v[4 * c].y, v[4 * c + 1].y, v[4 * c + 2].y, v[4 * c + 3].y);
-            } else {
-#pragma unroll
-                for (int c = 0; c < 8; ++c)
-                    yh[c * 32 + lane] = make_float4(v[32 + 4 * c].y, v[33 + 4 * c].y, v[34 + 4 * c].y, v[35 + 4 * c].y);
+                    for (int i = 0; i < PP; ++i) yp[i * 32 + lane] = v[q4 * PP + i];
+                }
             }
 #pragma unroll 1
-            for (int w = 0; w < W / 4; ++w) {
-                uint32_t a1 = 0u, a2 = 0u;
+            for (int w = 0; w < PP / E; ++w) {
+                uint32_t a1x = 0u, a2x = 0u, a1y = 0u, a2y = 0u;
                 if constexpr (MODE == MODE_SYM) {
 #pragma unroll
-                    for (int cc = E / 4 - 1; cc >= 0; --cc) {
-                        const float4 q4 = yh[(w * (E / 4) + cc) * 32 + lane];
-                        const float ys[4] = {q4.x, q4.y, q4.z, q4.w};
-#pragma unroll
-                        for (int j = 3; j >= 0; --j) {
-                            if constexpr (BITS == 2)
-                                sym2_code(ys[j], sk, a1, a2, m);
-                            else
-                                sym1_code(ys[j], sk, a1, a2, m);
+                    for (int i = E - 1; i >= 0; --i) {
+                        const float2 y2 = yp[(w * E + i) * 32 + lane];
+                        if constexpr (BITS == 2) {
+                            sym2_code(y2.x, sk, a1x, a2x, mx);
+                            sym2_code(y2.y, sk, a1y, a2y, my);
+                        } else {
+                            sym1_code(y2.x, sk, a1x, a2x, mx);
+                            sym1_code(y2.y, sk, a1y, a2y, my);
                         }
                     }
-                    a1 = ~a1;
-                    a2 = ~a2;
+                    a1x = ~a1x; a2x = ~a2x; a1y = ~a1y; a2y = ~a2y;
                 } else {
 #pragma unroll
-                    for (int cc = 0; cc < E / 4; ++cc) {
-                        const float4 q4 = yh[(w * (E / 4) + cc) * 32 + lane];
-                        const float ys[4] = {q4.x, q4.y, q4.z, q4.w};
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            const int code1 = stage_code<BITS, GRID>(ys[j], tb1, tc1, p.t1, p.b1, m);
-                            const float rr = ys[j] - __shfl_sync(FULL_MASK, tcen, code1);
-                            const int code2 = stage_code<BITS, GRID>(rr, tb2, tc2, p.t2, p.b2, m);
-                            a1 = __funnelshift_r(a1, (uint32_t)code1, BITS);
-                            a2 = __funnelshift_r(a2, (uint32_t)code2, BITS);
-                        }
+                    for (int i = 0; i < E; ++i) {
+                        const float2 y2 = yp[(w * E + i) * 32 + lane];
+                        const int cx1 = stage_code<BITS, GRID>(y2.x, tb1, tc1, p.t1, p.b1, mx);
+                        const int cy1 = stage_code<BITS, GRID>(y2.y, tb1, tc1, p.t1, p.b1, my);
+                        const float rx = y2.x - __shfl_sync(FULL_MASK, tcen, cx1);
+                        const float ry = y2.y - __shfl_sync(FULL_MASK, tcen, cy1);
+                        const int cx2 = stage_code<BITS, GRID>(rx, tb2, tc2, p.t2, p.b2, mx);
+                        const int cy2 = stage_code<BITS, GRID>(ry, tb2, tc2, p.t2, p.b2, my);
+                        a1x = __funnelshift_r(a1x, (uint32_t)cx1, BITS);
+                        a2x = __funnelshift_r(a2x, (uint32_t)cx2, BITS);
+                        a1y = __funnelshift_r(a1y, (uint32_t)cy1, BITS);
+                        a2y = __funnelshift_r(a2y, (uint32_t)cy2, BITS);
                     }
                 }
-                o1[lane * (W + 1) + qt * (W / 4) + w] = a1;
-                o2[lane * (W + 1) + qt * (W / 4) + w] = a2;
+                const int kx = ps * (PP / E) + w;
+                o1[lane * (W + 1) + kx] = a1x;
+                o2[lane * (W + 1) + kx] = a2x;
+                o1[lane * (W + 1) + W / 2 + kx] = a1y;
+                o2[lane * (W + 1) + W / 2 + kx] = a2y;
             }
         }
+        const float m = fminf(mx, my);
         // a zero row has no direction: always take the exact path for it
         const bool flag = valid && (!(m >= guard) || !(q > 0.0f));
 
