@@ -4,6 +4,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_fp16.h>
 
 #include "vq.h"
@@ -82,6 +83,46 @@ __device__ __forceinline__ void bulk_g2s(void *dst_smem, const void *src_gmem, u
         " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst_smem)),
         "l"(src_gmem), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
         : "memory");
+}
+
+// Tiled tensor copies global -> shared (TMA), completion on `bar`.  The
+// innermost coordinate times the element size must be a multiple of 16 bytes;
+// the box lands in shared memory as the tensor map's layout (and swizzle)
+// dictates, out-of-range elements zero-filled, and always counts its full
+// size in bytes on the barrier.
+__device__ __forceinline__ void tma_load_2d(void *dst_smem, const CUtensorMap *map, int c0, int c1,
+                                            uint64_t *bar, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst_smem)),
+        "l"(map), "r"(c0), "r"(c1), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(void *dst_smem, const CUtensorMap *map, int c0, int c1, int c2,
+                                            uint64_t *bar, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst_smem)),
+        "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
+// Byte offset of 16-byte chunk `c` of 128-byte line `line` in a box written
+// with the 128-byte swizzle (buffer aligned to 1024 bytes).
+__device__ __forceinline__ uint32_t swz128(int line, int c)
+{
+    return (uint32_t)(line * 128 + ((c ^ (line & 7)) << 4));
+}
+
+// Shared memory base rounded up to 1024 bytes (the 128-byte swizzle pattern is
+// taken from address bits 7-9); launches request 1024 extra bytes.
+__device__ __forceinline__ unsigned char *smem_1k(unsigned char *p)
+{
+    const uint32_t a = smem_u32(p);
+    return p + (((a + 1023u) & ~1023u) - a);
 }
 
 // L2 policy for data read exactly once (streamed input).

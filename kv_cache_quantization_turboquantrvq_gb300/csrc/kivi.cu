@@ -190,28 +190,66 @@ __device__ __forceinline__ bool group_sum_exact(float s, float z)
     return fabsf(z) + C * s < 8388608.0f * q;  // 2^23 quanta: one bit of headroom
 }
 
+// ------------------------------------------------------------ fast codes
+//
+// The common path takes q = rint(A f) with A = fl(x - min) and
+// f = fl((2^b - 1)/fl(max - min)).  A f differs from the exact t by three
+// relative roundings, at most 3 * 2^-24 * t < 2^-18.4 for t <= 15, so when
+// |rint(A f) - A f| < 1/2 - 2^-16 the estimate rounds like t.  The test is
+// e = rint(A f) - A f (one FMA, one rounding) and the sign of e^2 - THR with
+// THR = (1/2 - 2^-16)^2; the sign bits of all elements of a word are ANDed,
+// so a clear sign bit sends the word to the exact path (code_pair /
+// code_int64 above).  Random data trips it for about 3e-5 of the elements;
+// exact ties always trip it.
+constexpr float TIE_THR = (float)((0.5 - 1.0 / 65536.0) * (0.5 - 1.0 / 65536.0));
+
+// Codes of two elements (MAGIC-biased: the low bits of qa / qb are the codes)
+// and the running AND of the tie-test sign bits.
+__device__ __forceinline__ void code_pair_fast(__half a, __half b, float mna, float mnb, float2 f,
+                                               float2 nf, uint32_t &qa, uint32_t &qb, uint32_t &ok)
+{
+    const float2 A = make_float2(add_f16_f32(a, -mna), add_f16_f32(b, -mnb));
+    const float2 tm = __ffma2_rn(A, f, make_float2(MAGIC, MAGIC));
+    const float2 r = __fadd2_rn(tm, make_float2(-MAGIC, -MAGIC));
+    const float2 e = __ffma2_rn(A, nf, r);
+    const float2 c = __ffma2_rn(e, e, make_float2(-TIE_THR, -TIE_THR));
+    ok &= __float_as_uint(c.x) & __float_as_uint(c.y);
+    qa = __float_as_uint(tm.x);
+    qb = __float_as_uint(tm.y);
+}
+
+// Exact code of one element (the slow path of a word).
+template <int BITS>
+__device__ __noinline__ uint32_t code_exact(__half h, const GroupQ g, float mx)
+{
+    if (!g.fast) return code_int64<BITS>(__half2float(h), g.mn, mx);
+    uint32_t q, qd;
+    code_pair<BITS>(h, h, g, q, qd);
+    return q & ((1u << BITS) - 1u);
+}
+
 // ------------------------------------------------------------ values (per token)
 //
-// One row per thread, 32-row blocks per warp.  Rows arrive by per-row bulk
-// copies (rows skip the residual window, so a block need not be contiguous)
-// into a 3-stage ring at a 272-byte stride.  Per group: fp16 min/max, then a
-// rolled loop over the group's output words; words and (scale, zero) are
-// staged in shared memory and written out coalesced.
+// Two threads per row: lane l works on row l & 15 of a 16-token block and on
+// channels [64h, 64h + 64), h = l >> 4.  A block never crosses a (b, h) slice
+// (blocks are numbered per slice; rows past S_q are computed and dropped), so
+// it is two TMA tensor boxes of 16 rows x 64 channels, one per channel half,
+// landing with the 128-byte swizzle: row r's 16-byte chunk c sits at chunk
+// c ^ (r & 7) of its 128-byte line, and each quarter-warp of a 16-byte shared
+// load touches eight distinct bank groups.  A per-warp 3-stage ring; a thread
+// moves its 128 bytes to registers at once and the stage is refilled before
+// any arithmetic.  Per group: fp16 min/max (a 128-wide group combines the two
+// halves by one shuffle), then the fast codes word by word; words go straight
+// to global memory (the 16 rows x 2 halves of a block are contiguous there).
 
-constexpr int VAL_WARPS = 8;
-constexpr int VAL_STAGES = 3;
 constexpr int ROW_BYTES = D * 2;
 constexpr int ROW_STRIDE = ROW_BYTES + 16;
-constexpr int VSTAGE_BYTES = 32 * ROW_STRIDE;
-__host__ __device__ constexpr int val_words(int bits) { return D * bits / 32; }
-__host__ __device__ constexpr int val_warp_bytes(int bits, int G)
-{
-    return VAL_STAGES * VSTAGE_BYTES + 32 * (val_words(bits) + 1) * 4 + 32 * (D / G) * 4;
-}
-__host__ __device__ constexpr int val_smem(int bits, int G)
-{
-    return VAL_WARPS * (val_warp_bytes(bits, G) + VAL_STAGES * 8);
-}
+constexpr int VAL_WARPS = 16;
+constexpr int VAL_STAGES = 3;
+constexpr int VROWS = 16;
+constexpr int VSTAGE_BYTES = VROWS * ROW_BYTES;  // two 2 KB swizzled boxes
+__host__ __device__ constexpr int val_smem() { return 1024 + VAL_WARPS * VAL_STAGES * (VSTAGE_BYTES + 8); }
+
 
 __device__ __forceinline__ bool kivi_off(const KiviQuantParams &p, int b, int &off)
 {
@@ -225,24 +263,49 @@ __device__ __forceinline__ bool kivi_off(const KiviQuantParams &p, int b, int &o
     return true;
 }
 
-__device__ __forceinline__ uint32_t h2bits(__half h) { return (uint32_t)__half_as_ushort(h); }
+__device__ __forceinline__ __half2 u2h2(uint32_t u) { return *reinterpret_cast<__half2 *>(&u); }
+
+// The E codes of one values word, exactly (rare path).
+template <int BITS>
+struct WordChunks {
+    uint4 c[32 / BITS / 8];
+};
+
+template <int BITS>
+__device__ __noinline__ uint32_t values_word_exact(const WordChunks<BITS> wc, const GroupQ g, float mx)
+{
+    constexpr int E = 32 / BITS;
+    uint32_t word = 0u;
+    for (int e = 0; e < E; ++e) {
+        const uint4 c = wc.c[e / 8];
+        const uint32_t u = (&c.x)[(e % 8) / 2];
+        const __half h = (e & 1) ? __high2half(u2h2(u)) : __low2half(u2h2(u));
+        word |= code_exact<BITS>(h, g, mx) << (e * BITS);
+    }
+    return word;
+}
 
 template <int BITS, int G>
 __global__ void __launch_bounds__(VAL_WARPS * 32, 1)
     kivi_values_kernel(const __grid_constant__ KiviQuantParams p)
 {
-    constexpr int E = 32 / BITS;
-    constexpr int W = D * BITS / 32;
+    constexpr int E = 32 / BITS;           // codes per word
+    constexpr int W = D * BITS / 32;       // words per row
+    constexpr int WL = W / 2;              // words per thread
+    constexpr int CPW = E / 8;             // 16-byte chunks per word
+    constexpr int GL = G < 64 ? G : 64;    // group members held by one thread
+    constexpr int NGL = 64 / GL;           // groups (or group halves) per thread
+    constexpr int WPGL = WL / NGL;         // words per thread-group
+    constexpr int CPG = GL / 8;            // chunks per thread-group
     constexpr int NGD = D / G;
-    constexpr int WPG = G * BITS / 32;  // words per group
-    constexpr int WB = val_warp_bytes(BITS, G);
-    extern __shared__ __align__(128) unsigned char smem[];
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    unsigned char *smem = smem_1k(smem_raw);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    unsigned char *wbuf = smem + warp * WB;
-    uint32_t *ow = reinterpret_cast<uint32_t *>(wbuf + VAL_STAGES * VSTAGE_BYTES);
-    uint32_t *osz = ow + 32 * (W + 1);  // scale | zero << 16, per row and group
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + VAL_WARPS * WB) + warp * VAL_STAGES;
+    const int rr = lane & 15, hh = lane >> 4;
+    unsigned char *wbuf = smem + warp * (VAL_STAGES * VSTAGE_BYTES);
+    uint64_t *bars =
+        reinterpret_cast<uint64_t *>(smem + VAL_WARPS * VAL_STAGES * VSTAGE_BYTES) + warp * VAL_STAGES;
     if (lane == 0) {
 #pragma unroll
         for (int s = 0; s < VAL_STAGES; ++s) mbar_init(&bars[s], 1);
@@ -250,21 +313,18 @@ __global__ void __launch_bounds__(VAL_WARPS * 32, 1)
     }
     __syncwarp();
     const uint64_t pol = l2_policy_evict_first();
-    const int N = p.B * p.H * p.S_q;
-    const int nblk = (N + 31) >> 5;
+    const int nsb = (p.S_q + VROWS - 1) / VROWS;  // blocks per (b, h) slice
+    const int nblk = p.B * p.H * nsb;
     const int gw = blockIdx.x * VAL_WARPS + warp;
     const int tw = gridDim.x * VAL_WARPS;
-    const __half *x = static_cast<const __half *>(p.x);
 
     auto issue = [&](int blk, int s) {
-        const int r0 = blk << 5;
-        const int nrows = min(32, N - r0);
-        if (lane == 0) mbar_arrive_expect_tx(&bars[s], (uint32_t)(nrows * ROW_BYTES));
-        if (lane < nrows) {
-            const int r = r0 + lane;
-            const int bh = r / p.S_q, s_ = r - bh * p.S_q;
-            bulk_g2s(wbuf + s * VSTAGE_BYTES + lane * ROW_STRIDE,
-                     x + ((size_t)bh * p.S + s_) * D, ROW_BYTES, &bars[s], pol);
+        if (lane == 0) {
+            const int bh = blk / nsb, sb = blk - bh * nsb;
+            mbar_arrive_expect_tx(&bars[s], (uint32_t)VSTAGE_BYTES);
+            unsigned char *dst = wbuf + s * VSTAGE_BYTES;
+            tma_load_3d(dst, &p.tmap, 0, sb * VROWS, bh, &bars[s], pol);
+            tma_load_3d(dst + VSTAGE_BYTES / 2, &p.tmap, 64, sb * VROWS, bh, &bars[s], pol);
         }
     };
 #pragma unroll
@@ -286,124 +346,157 @@ __global__ void __launch_bounds__(VAL_WARPS * 32, 1)
             }
             return;
         }
-        const int row = (blk << 5) + lane;
-        const __half *rh = reinterpret_cast<const __half *>(wbuf + s * VSTAGE_BYTES + lane * ROW_STRIDE);
-#pragma unroll 1
-        for (int j = 0; j < NGD; ++j) {
-            const uint4 *gp = reinterpret_cast<const uint4 *>(rh + j * G);
-            uint4 c0 = gp[0];
-            __half2 lo = __hmin2(__hmin2(*reinterpret_cast<__half2 *>(&c0.x), *reinterpret_cast<__half2 *>(&c0.y)),
-                                 __hmin2(*reinterpret_cast<__half2 *>(&c0.z), *reinterpret_cast<__half2 *>(&c0.w)));
-            __half2 hi = __hmax2(__hmax2(*reinterpret_cast<__half2 *>(&c0.x), *reinterpret_cast<__half2 *>(&c0.y)),
-                                 __hmax2(*reinterpret_cast<__half2 *>(&c0.z), *reinterpret_cast<__half2 *>(&c0.w)));
+        // this thread's 64 values to registers, then refill the stage
+        uint4 c[8];
+        {
+            const unsigned char *src = wbuf + s * VSTAGE_BYTES + hh * (VSTAGE_BYTES / 2);
 #pragma unroll
-            for (int i = 1; i < G / 8; ++i) {
-                uint4 c = gp[i];
-                lo = __hmin2(lo, __hmin2(__hmin2(*reinterpret_cast<__half2 *>(&c.x), *reinterpret_cast<__half2 *>(&c.y)),
-                                         __hmin2(*reinterpret_cast<__half2 *>(&c.z), *reinterpret_cast<__half2 *>(&c.w))));
-                hi = __hmax2(hi, __hmax2(__hmax2(*reinterpret_cast<__half2 *>(&c.x), *reinterpret_cast<__half2 *>(&c.y)),
-                                         __hmax2(*reinterpret_cast<__half2 *>(&c.z), *reinterpret_cast<__half2 *>(&c.w))));
-            }
-            const float mn = fminf(__low2float(lo), __high2float(lo));
-            const float mx = fmaxf(__low2float(hi), __high2float(hi));
-            const GroupQ g = group_setup<BITS>(mn, mx);
-            osz[lane * NGD + j] = h2bits(g.scale_h) | (h2bits(g.zero_h) << 16);
-#pragma unroll 1
-            for (int w = 0; w < WPG; ++w) {
-                const uint4 *wp = gp + w * (E / 8);
-                uint32_t word = 0u;
-                if (g.fast) {
-                    // two accumulators (first and second half of the word's
-                    // codes) halve the dependent chain of funnel shifts
-                    uint32_t lo = 0u, hi = 0u;
-#pragma unroll
-                    for (int i = 0; i < E / 8; ++i) {
-                        uint4 c = wp[i];
-                        const __half2 *hh = reinterpret_cast<const __half2 *>(&c);
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            uint32_t qa, qb;
-                            code_pair<BITS>(__low2half(hh[k]), __high2half(hh[k]), g, qa, qb);
-                            if (i < E / 16 || (E == 8 && k < 2)) {
-                                lo = __funnelshift_r(lo, qa, BITS);
-                                lo = __funnelshift_r(lo, qb, BITS);
-                            } else {
-                                hi = __funnelshift_r(hi, qa, BITS);
-                                hi = __funnelshift_r(hi, qb, BITS);
-                            }
-                        }
-                    }
-                    word = (hi & 0xffff0000u) | (lo >> 16);
-                } else {  // rare: a range that fp32 does not hold exactly
-                    for (int e = 0; e < E; ++e)
-                        word |= code_int64<BITS>(__half2float(rh[j * G + w * E + e]), mn, mx) << (e * BITS);
-                }
-                ow[lane * (W + 1) + j * WPG + w] = word;
-            }
+            for (int i = 0; i < 8; ++i) c[i] = *reinterpret_cast<const uint4 *>(src + swz128(rr, i));
         }
-        // the block is in registers / staging: recycle the stage
         __syncwarp();
         fence_proxy_async_smem();
         {
             const int nb = blk + VAL_STAGES * tw;
             if (nb < nblk) issue(nb, s);
         }
-        // coalesced write-out
-        int dr32 = 0;
+
+        const int bh = blk / nsb;
+        const int s_ = (blk - bh * nsb) * VROWS + rr;
+        size_t dr = 0;
         bool okrow = false;
-        if (row < N) {
-            const int bh = row / p.S_q, s_ = row - bh * p.S_q;
+        if (s_ < p.S_q) {
             int off;
             okrow = kivi_off(p, bh / p.H, off);
-            dr32 = bh * p.S_dst + off + s_;
+            dr = (size_t)bh * p.S_dst + off + s_;
         }
+        uint32_t words[WL];
+        __half scv[NGL], zrv[NGL];
 #pragma unroll
-        for (int i = 0; i < W; ++i) {
-            const int idx = i * 32 + lane;
-            const int r = idx / W, w = idx % W;
-            const int dr = __shfl_sync(FULL_MASK, dr32, r);
-            if (__shfl_sync(FULL_MASK, okrow ? 1 : 0, r)) p.packed[(size_t)dr * W + w] = ow[r * (W + 1) + w];
-        }
-        __half *sc = static_cast<__half *>(p.scale);
-        __half *zr = static_cast<__half *>(p.zero);
+        for (int jl = 0; jl < NGL; ++jl) {
+            __half2 lo = u2h2(c[jl * CPG].x), hi = lo;
 #pragma unroll
-        for (int i = 0; i < NGD; ++i) {
-            const int idx = i * 32 + lane;
-            const int r = idx / NGD, j = idx % NGD;
-            const int dr = __shfl_sync(FULL_MASK, dr32, r);
-            if (__shfl_sync(FULL_MASK, okrow ? 1 : 0, r)) {
-                const uint32_t v = osz[r * NGD + j];
-                sc[(size_t)dr * NGD + j] = __ushort_as_half((unsigned short)(v & 0xffffu));
-                zr[(size_t)dr * NGD + j] = __ushort_as_half((unsigned short)(v >> 16));
+            for (int i = 0; i < CPG; ++i) {
+                const uint4 q = c[jl * CPG + i];
+                const __half2 a = __hmin2(__hmin2(u2h2(q.x), u2h2(q.y)), __hmin2(u2h2(q.z), u2h2(q.w)));
+                const __half2 b = __hmax2(__hmax2(u2h2(q.x), u2h2(q.y)), __hmax2(u2h2(q.z), u2h2(q.w)));
+                lo = __hmin2(lo, a);
+                hi = __hmax2(hi, b);
+            }
+            float mn = fminf(__low2float(lo), __high2float(lo));
+            float mx = fmaxf(__low2float(hi), __high2float(hi));
+            if constexpr (G == 128) {
+                mn = fminf(mn, __shfl_xor_sync(FULL_MASK, mn, 16));
+                mx = fmaxf(mx, __shfl_xor_sync(FULL_MASK, mx, 16));
+            }
+            const GroupQ g = group_setup<BITS>(mn, mx);
+            scv[jl] = g.scale_h;
+            zrv[jl] = g.zero_h;
+            const float2 f2 = make_float2(g.f, g.f), nf2 = make_float2(-g.f, -g.f);
+#pragma unroll
+            for (int w = 0; w < WPGL; ++w) {
+                // two accumulators (first / second half of the word's codes)
+                uint32_t alo = 0u, ahi = 0u, okw = 0xffffffffu;
+#pragma unroll
+                for (int ci = 0; ci < CPW; ++ci) {
+                    const uint4 q = c[jl * CPG + w * CPW + ci];
+                    const uint32_t u4[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        uint32_t qa, qb;
+                        code_pair_fast(__low2half(u2h2(u4[k])), __high2half(u2h2(u4[k])), mn, mn, f2, nf2,
+                                       qa, qb, okw);
+                        if (2 * (4 * ci + k) < E / 2) {
+                            alo = __funnelshift_r(alo, qa, BITS);
+                            alo = __funnelshift_r(alo, qb, BITS);
+                        } else {
+                            ahi = __funnelshift_r(ahi, qa, BITS);
+                            ahi = __funnelshift_r(ahi, qb, BITS);
+                        }
+                    }
+                }
+                uint32_t word = (ahi & 0xffff0000u) | (alo >> 16);
+                if (!(okw >> 31)) {
+                    WordChunks<BITS> wc;
+#pragma unroll
+                    for (int ci = 0; ci < CPW; ++ci) wc.c[ci] = c[jl * CPG + w * CPW + ci];
+                    word = values_word_exact<BITS>(wc, g, mx);
+                }
+                words[jl * WPGL + w] = word;
             }
         }
-        __syncwarp();
+        if (!okrow) continue;
+        uint32_t *dst = p.packed + dr * W + hh * WL;
+        if constexpr (WL == 2) {
+            *reinterpret_cast<uint2 *>(dst) = make_uint2(words[0], words[1]);
+        } else {
+#pragma unroll
+            for (int i = 0; i < WL / 4; ++i)
+                reinterpret_cast<uint4 *>(dst)[i] = make_uint4(words[4 * i], words[4 * i + 1], words[4 * i + 2], words[4 * i + 3]);
+        }
+        __half *sc = static_cast<__half *>(p.scale) + dr * NGD;
+        __half *zr = static_cast<__half *>(p.zero) + dr * NGD;
+        if constexpr (G == 128) {
+            if (hh == 0) {
+                sc[0] = scv[0];
+                zr[0] = zrv[0];
+            }
+        } else if constexpr (NGL == 2) {
+            *reinterpret_cast<__half2 *>(sc + 2 * hh) = __halves2half2(scv[0], scv[1]);
+            *reinterpret_cast<__half2 *>(zr + 2 * hh) = __halves2half2(zrv[0], zrv[1]);
+        } else {
+            sc[hh] = scv[0];
+            zr[hh] = zrv[0];
+        }
     }
 }
 
 // ------------------------------------------------------------ keys (per channel)
 //
-// One [G x 128] tile (contiguous in memory) per warp per step, one bulk copy;
-// lane l owns channels 4l..4l+3.  Pass 1: fp16 min/max down the tokens.
-// Pass 2: a rolled loop over the group's word rows; each step packs E tokens
-// of the lane's four channels into four words and stores them as one 16-byte
-// write (512 contiguous bytes per warp).
+// One [G x 64] half-tile per warp step: channels [64c, 64c + 64) of the G
+// tokens of a group, staged by one TMA tensor box (tokens past S arrive as
+// zeros and are never used; tokens in [S_q, S) are ignored); lane l owns
+// channels 2l and 2l + 1, so each token row of the tile is one conflict-free
+// 32-bit load per lane and no cross-thread reduction is needed (the pages'
+// "one thread, one whole group").  For G <= 64 the lane's 2G values move to
+// registers in the min/max pass and the stage is refilled at once.  Codes of
+// the two channels of a token run as one fp32 pair.  Each word row is stored
+// as 8 bytes per lane (256 contiguous bytes per warp).
 
 constexpr int KEY_STAGES = 2;
-constexpr int KEY_SMEM_BUDGET = 192 * 1024;
+constexpr int KEY_SMEM_BUDGET = 220 * 1024;
+constexpr int KEY_ROW = 128;  // bytes of one token row of a half-tile
 
-// Warps per CTA for key tiles of G tokens: as many 2-stage rings as fit.
 template <int G>
 __host__ __device__ constexpr int key_warps()
 {
-    return KEY_SMEM_BUDGET / (KEY_STAGES * G * ROW_BYTES) > 12 ? 12
-                                                                 : KEY_SMEM_BUDGET / (KEY_STAGES * G * ROW_BYTES);
+    return KEY_SMEM_BUDGET / (KEY_STAGES * G * KEY_ROW) > 16 ? 16
+                                                               : KEY_SMEM_BUDGET / (KEY_STAGES * G * KEY_ROW);
 }
 
 template <int G>
 __host__ __device__ constexpr int key_smem()
 {
-    return key_warps<G>() * KEY_STAGES * (G * ROW_BYTES + 8);
+    return 1024 + key_warps<G>() * KEY_STAGES * (G * KEY_ROW + 8);
+}
+
+// Exact codes of one word of two channels (rare path): tokens w*E .. w*E+E-1.
+template <int BITS>
+struct KeyWord {
+    uint32_t v[32 / BITS];  // half2 (channel 2l, 2l + 1) per token
+};
+
+template <int BITS>
+__device__ __noinline__ uint2 keys_word_exact(const KeyWord<BITS> kw, const GroupQ g0, const GroupQ g1,
+                                              float mx0, float mx1, int nvalid)
+{
+    constexpr int E = 32 / BITS;
+    uint32_t w0 = 0u, w1 = 0u;
+    for (int j = 0; j < E && j < nvalid; ++j) {
+        const __half2 h = u2h2(kw.v[j]);
+        w0 |= code_exact<BITS>(__low2half(h), g0, mx0) << (j * BITS);
+        w1 |= code_exact<BITS>(__high2half(h), g1, mx1) << (j * BITS);
+    }
+    return make_uint2(w0, w1);
 }
 
 template <int BITS, int G>
@@ -413,8 +506,10 @@ __global__ void __launch_bounds__(key_warps<G>() * 32, 1)
     constexpr int KEY_WARPS = key_warps<G>();
     constexpr int E = 32 / BITS;
     constexpr int WG = G * BITS / 32;  // words per channel per group
-    constexpr int TILE = G * ROW_BYTES;
-    extern __shared__ __align__(128) unsigned char smem[];
+    constexpr int TILE = G * KEY_ROW;
+    constexpr bool PRELOAD = G <= 64;
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    unsigned char *smem = smem_1k(smem_raw);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     unsigned char *wbuf = smem + warp * (KEY_STAGES * TILE);
@@ -428,21 +523,20 @@ __global__ void __launch_bounds__(key_warps<G>() * 32, 1)
     __syncwarp();
     const uint64_t pol = l2_policy_evict_first();
     const int NG = (p.S_q + G - 1) / G;
-    const int ntiles = p.B * p.H * NG;
+    const int ntiles = p.B * p.H * NG * 2;
     const int gw = blockIdx.x * KEY_WARPS + warp;
     const int tw = gridDim.x * KEY_WARPS;
-    const __half *x = static_cast<const __half *>(p.x);
 
     auto ntok_of = [&](int tile) {
-        const int g = tile % NG;
+        const int g = (tile >> 1) % NG;
         return min(G, p.S_q - g * G);
     };
     auto issue = [&](int tile, int s) {
         if (lane == 0) {
-            const int bh = tile / NG, g = tile - bh * NG;
-            const uint32_t bytes = (uint32_t)(ntok_of(tile) * ROW_BYTES);
-            mbar_arrive_expect_tx(&bars[s], bytes);
-            bulk_g2s(wbuf + s * TILE, x + ((size_t)bh * p.S + (size_t)g * G) * D, bytes, &bars[s], pol);
+            const int gi = tile >> 1, chh = tile & 1;
+            const int bh = gi / NG, g = gi - bh * NG;
+            mbar_arrive_expect_tx(&bars[s], (uint32_t)TILE);
+            tma_load_3d(wbuf + s * TILE, &p.tmap, 64 * chh, g * G, bh, &bars[s], pol);
         }
     };
 #pragma unroll
@@ -464,96 +558,111 @@ __global__ void __launch_bounds__(key_warps<G>() * 32, 1)
             }
             return;
         }
-        const unsigned char *tb = wbuf + s * TILE;
+        const uint32_t *col = reinterpret_cast<const uint32_t *>(wbuf + s * TILE) + lane;
         const int ntok = ntok_of(tile);
-        const int bh = tile / NG, g = tile - bh * NG;
-        // pass 1: per-channel min/max over the group's tokens (exact fp16)
-        const uint2 *col = reinterpret_cast<const uint2 *>(tb) + lane;  // channels 4l..4l+3
-        uint2 r0 = col[0];
-        __half2 lo0 = *reinterpret_cast<__half2 *>(&r0.x), lo1 = *reinterpret_cast<__half2 *>(&r0.y);
-        __half2 hi0 = lo0, hi1 = lo1;
+        const int gi = tile >> 1, chh = tile & 1;
+        const int bh = gi / NG, g = gi - bh * NG;
+
+        // pass 1: min/max down the tokens (exact fp16); a ragged last group
+        // is padded with its edge token, which leaves min/max unchanged
+        uint32_t v[PRELOAD ? G : 1];
+        __half2 lo, hi;
+        if constexpr (PRELOAD) {
+#pragma unroll
+            for (int i = 0; i < G; ++i) v[i] = col[i * 32];
+            if (ntok < G) {
+                const uint32_t edge = col[(ntok - 1) * 32];
+#pragma unroll
+                for (int i = 0; i < G; ++i)
+                    if (i >= ntok) v[i] = edge;
+            }
+            __syncwarp();
+            fence_proxy_async_smem();
+            {
+                const int nt = tile + KEY_STAGES * tw;
+                if (nt < ntiles) issue(nt, s);
+            }
+            __half2 l2 = u2h2(v[0]), h2 = l2, l3 = u2h2(v[1]), h3 = l3;
+#pragma unroll
+            for (int i = 2; i < G; i += 2) {
+                l2 = __hmin2(l2, u2h2(v[i]));
+                h2 = __hmax2(h2, u2h2(v[i]));
+                l3 = __hmin2(l3, u2h2(v[i + 1]));
+                h3 = __hmax2(h3, u2h2(v[i + 1]));
+            }
+            lo = __hmin2(l2, l3);
+            hi = __hmax2(h2, h3);
+        } else {
+            lo = u2h2(col[0]);
+            hi = lo;
 #pragma unroll 8
-        for (int i = 1; i < ntok; ++i) {
-            uint2 r = col[i * (ROW_BYTES / 8)];
-            const __half2 a = *reinterpret_cast<__half2 *>(&r.x), b = *reinterpret_cast<__half2 *>(&r.y);
-            lo0 = __hmin2(lo0, a); hi0 = __hmax2(hi0, a);
-            lo1 = __hmin2(lo1, b); hi1 = __hmax2(hi1, b);
+            for (int i = 1; i < ntok; ++i) {
+                const __half2 a = u2h2(col[i * 32]);
+                lo = __hmin2(lo, a);
+                hi = __hmax2(hi, a);
+            }
         }
-        const float mxv[4] = {__low2float(hi0), __high2float(hi0), __low2float(hi1), __high2float(hi1)};
-        GroupQ gq[4];
-        gq[0] = group_setup<BITS>(__low2float(lo0), mxv[0]);
-        gq[1] = group_setup<BITS>(__high2float(lo0), mxv[1]);
-        gq[2] = group_setup<BITS>(__low2float(lo1), mxv[2]);
-        gq[3] = group_setup<BITS>(__high2float(lo1), mxv[3]);
+        const float mx0 = __low2float(hi), mx1 = __high2float(hi);
+        const GroupQ g0 = group_setup<BITS>(__low2float(lo), mx0);
+        const GroupQ g1 = group_setup<BITS>(__high2float(lo), mx1);
+        const float2 f2 = make_float2(g0.f, g1.f), nf2 = make_float2(-g0.f, -g1.f);
         int off;
         const bool okoff = kivi_off(p, bh / p.H, off);  // uniform across the warp
         const size_t gd = (size_t)bh * p.NG_dst + off / G + g;
+        uint32_t *dst = p.packed + gd * WG * D + 64 * chh + 2 * lane;
+
         // pass 2: word row k holds tokens k*E .. k*E + E - 1 at shifts j*BITS
-        const __half *tokh = reinterpret_cast<const __half *>(tb);
-        const bool allfast = gq[0].fast && gq[1].fast && gq[2].fast && gq[3].fast;
-#pragma unroll 1
+#pragma unroll
         for (int k = 0; k < WG; ++k) {
-            uint32_t w0 = 0u, w1 = 0u, w2 = 0u, w3 = 0u;
-            if (allfast) {
+            uint32_t a0 = 0u, b0 = 0u, a1 = 0u, b1 = 0u, okw = 0xffffffffu;
+            KeyWord<BITS> kw;
 #pragma unroll
-                for (int j = 0; j < E; j += 2) {
-                    const int i = k * E + j;
-                    uint32_t c0a = 0, c0b = 0, c1a = 0, c1b = 0, c2a = 0, c2b = 0, c3a = 0, c3b = 0;
-                    if (i < ntok) {
-                        uint2 ra = col[i * (ROW_BYTES / 8)];
-                        uint2 rb = (i + 1 < ntok) ? col[(i + 1) * (ROW_BYTES / 8)] : ra;
-                        const __half2 a01 = *reinterpret_cast<__half2 *>(&ra.x), a23 = *reinterpret_cast<__half2 *>(&ra.y);
-                        const __half2 b01 = *reinterpret_cast<__half2 *>(&rb.x), b23 = *reinterpret_cast<__half2 *>(&rb.y);
-                        code_pair<BITS>(__low2half(a01), __low2half(b01), gq[0], c0a, c0b);
-                        code_pair<BITS>(__high2half(a01), __high2half(b01), gq[1], c1a, c1b);
-                        code_pair<BITS>(__low2half(a23), __low2half(b23), gq[2], c2a, c2b);
-                        code_pair<BITS>(__high2half(a23), __high2half(b23), gq[3], c3a, c3b);
-                        if (i + 1 >= ntok) c0b = c1b = c2b = c3b = 0u;
-                    }
-                    w0 = __funnelshift_r(__funnelshift_r(w0, c0a, BITS), c0b, BITS);
-                    w1 = __funnelshift_r(__funnelshift_r(w1, c1a, BITS), c1b, BITS);
-                    w2 = __funnelshift_r(__funnelshift_r(w2, c2a, BITS), c2b, BITS);
-                    w3 = __funnelshift_r(__funnelshift_r(w3, c3a, BITS), c3b, BITS);
+            for (int j = 0; j < E; ++j) {
+                const int i = k * E + j;
+                uint32_t u;
+                if constexpr (PRELOAD) {
+                    u = v[i];
+                } else {
+                    u = col[(i < ntok ? i : ntok - 1) * 32];
                 }
-            } else {  // rare: some channel's range is not held exactly by fp32
-                uint32_t rw[4] = {0u, 0u, 0u, 0u};
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    for (int j = 0; j < E; ++j) {
-                        const int i = k * E + j;
-                        if (i >= ntok) break;
-                        const float xv = __half2float(tokh[i * D + 4 * lane + c]);
-                        uint32_t q, qdummy;
-                        if (gq[c].fast) {
-                            code_pair<BITS>(__float2half_rn(xv), __float2half_rn(xv), gq[c], q, qdummy);
-                            q &= (1u << BITS) - 1u;
-                        } else {
-                            q = code_int64<BITS>(xv, gq[c].mn, mxv[c]);
-                        }
-                        rw[c] |= q << (j * BITS);
-                    }
+                kw.v[j] = u;
+                uint32_t q0, q1;
+                code_pair_fast(__low2half(u2h2(u)), __high2half(u2h2(u)), g0.mn, g1.mn, f2, nf2, q0, q1,
+                               okw);
+                if (j < E / 2) {
+                    a0 = __funnelshift_r(a0, q0, BITS);
+                    a1 = __funnelshift_r(a1, q1, BITS);
+                } else {
+                    b0 = __funnelshift_r(b0, q0, BITS);
+                    b1 = __funnelshift_r(b1, q1, BITS);
                 }
-                w0 = rw[0]; w1 = rw[1]; w2 = rw[2]; w3 = rw[3];
             }
-            if (okoff)
-                *reinterpret_cast<uint4 *>(p.packed + (gd * WG + k) * D + 4 * lane) = make_uint4(w0, w1, w2, w3);
+            uint32_t w0 = (b0 & 0xffff0000u) | (a0 >> 16);
+            uint32_t w1 = (b1 & 0xffff0000u) | (a1 >> 16);
+            const int nvalid = ntok - k * E;  // tokens of this word that exist
+            if (!(okw >> 31)) {
+                const uint2 ww = keys_word_exact<BITS>(kw, g0, g1, mx0, mx1, nvalid);
+                w0 = ww.x;
+                w1 = ww.y;
+            }
+            if (nvalid < E) {  // slots past the last token hold 0
+                const uint32_t m = nvalid <= 0 ? 0u : (0xffffffffu >> (32 - nvalid * BITS));
+                w0 &= m;
+                w1 &= m;
+            }
+            if (okoff) *reinterpret_cast<uint2 *>(dst + (size_t)k * D) = make_uint2(w0, w1);
         }
-        // the tile is consumed: recycle the stage
-        __syncwarp();
-        fence_proxy_async_smem();
-        {
+        if constexpr (!PRELOAD) {
+            __syncwarp();
+            fence_proxy_async_smem();
             const int nt = tile + KEY_STAGES * tw;
             if (nt < ntiles) issue(nt, s);
         }
         if (!okoff) continue;
-        __half2 s01 = __halves2half2(gq[0].scale_h, gq[1].scale_h);
-        __half2 s23 = __halves2half2(gq[2].scale_h, gq[3].scale_h);
-        __half2 z01 = __halves2half2(gq[0].zero_h, gq[1].zero_h);
-        __half2 z23 = __halves2half2(gq[2].zero_h, gq[3].zero_h);
-        *reinterpret_cast<uint2 *>(static_cast<__half *>(p.scale) + gd * D + 4 * lane) =
-            make_uint2(*reinterpret_cast<uint32_t *>(&s01), *reinterpret_cast<uint32_t *>(&s23));
-        *reinterpret_cast<uint2 *>(static_cast<__half *>(p.zero) + gd * D + 4 * lane) =
-            make_uint2(*reinterpret_cast<uint32_t *>(&z01), *reinterpret_cast<uint32_t *>(&z23));
+        *reinterpret_cast<__half2 *>(static_cast<__half *>(p.scale) + gd * D + 64 * chh + 2 * lane) =
+            __halves2half2(g0.scale_h, g1.scale_h);
+        *reinterpret_cast<__half2 *>(static_cast<__half *>(p.zero) + gd * D + 64 * chh + 2 * lane) =
+            __halves2half2(g0.zero_h, g1.zero_h);
     }
 }
 
@@ -561,13 +670,13 @@ __global__ void __launch_bounds__(key_warps<G>() * 32, 1)
 
 constexpr int DQ_THREADS = 256;
 
-// Values: one row per thread; each row's words arrive by a per-row bulk copy
-// into a 3-stage ring (slots padded for conflict-free 16-byte reads); the fp16
-// row is staged in shared memory and written out coalesced.
+// Values: one row per thread; the words of a 32-row block (contiguous in
+// memory) arrive by one bulk copy into a 3-stage ring; the fp16 row is staged
+// in shared memory and written out coalesced.
 constexpr int VDQ_WARPS = 8;
 constexpr int VDQ_STAGES = 3;
-__host__ __device__ constexpr int vdq_slot(int bits) { return (D * bits / 32) * 4 + 16 > 48 ? (D * bits / 32) * 4 + 16 : 48; }
-__host__ __device__ constexpr int vdq_warp_bytes(int bits) { return VDQ_STAGES * 32 * vdq_slot(bits) + 32 * ROW_STRIDE; }
+__host__ __device__ constexpr int vdq_stage(int bits) { return 32 * (D * bits / 32) * 4; }
+__host__ __device__ constexpr int vdq_warp_bytes(int bits) { return VDQ_STAGES * vdq_stage(bits) + 32 * ROW_STRIDE; }
 __host__ __device__ constexpr int vdq_smem(int bits) { return VDQ_WARPS * (vdq_warp_bytes(bits) + VDQ_STAGES * 8); }
 
 // One group of a row whose q*s + z is not exact in fp32 (rare): every element
@@ -599,13 +708,13 @@ __global__ void __launch_bounds__(VDQ_WARPS * 32, 1) kivi_values_dequant_kernel(
     constexpr int NGD = D / G;
     constexpr int WPG = G * BITS / 32;
     constexpr uint32_t MASK = (1u << BITS) - 1u;
-    constexpr int SLOT = vdq_slot(BITS);
+    constexpr int STG = vdq_stage(BITS);
     constexpr int WB = vdq_warp_bytes(BITS);
     extern __shared__ __align__(128) unsigned char smem[];
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     unsigned char *wbuf = smem + warp * WB;
-    unsigned char *obuf = wbuf + VDQ_STAGES * 32 * SLOT;
+    unsigned char *obuf = wbuf + VDQ_STAGES * STG;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + VDQ_WARPS * WB) + warp * VDQ_STAGES;
     if (lane == 0) {
 #pragma unroll
@@ -619,11 +728,12 @@ __global__ void __launch_bounds__(VDQ_WARPS * 32, 1) kivi_values_dequant_kernel(
     const int gw = blockIdx.x * VDQ_WARPS + warp;
     const int tw = gridDim.x * VDQ_WARPS;
     auto issue = [&](int blk, int s) {
-        const int r0 = blk << 5;
-        const int nrows = min(32, N - r0);
-        if (lane == 0) mbar_arrive_expect_tx(&bars[s], (uint32_t)(nrows * W * 4));
-        if (lane < nrows)
-            bulk_g2s(wbuf + s * 32 * SLOT + lane * SLOT, p.packed + (size_t)(r0 + lane) * W, W * 4, &bars[s], pol);
+        if (lane == 0) {
+            const int r0 = blk << 5;
+            const uint32_t bytes = (uint32_t)(min(32, N - r0) * W * 4);
+            mbar_arrive_expect_tx(&bars[s], bytes);
+            bulk_g2s(wbuf + s * STG, p.packed + (size_t)r0 * W, bytes, &bars[s], pol);
+        }
     };
 #pragma unroll
     for (int s = 0; s < VDQ_STAGES; ++s) {
@@ -664,7 +774,7 @@ __global__ void __launch_bounds__(VDQ_WARPS * 32, 1) kivi_values_dequant_kernel(
             }
             return;
         }
-        const uint32_t *wrow = reinterpret_cast<const uint32_t *>(wbuf + s * 32 * SLOT + lane * SLOT);
+        const uint32_t *wrow = reinterpret_cast<const uint32_t *>(wbuf + s * STG + lane * W * 4);
         uint4 *orow = reinterpret_cast<uint4 *>(obuf + lane * ROW_STRIDE);
 #pragma unroll
         for (int j = 0; j < NGD; ++j) {
@@ -767,26 +877,34 @@ __global__ void __launch_bounds__(DQ_THREADS) kivi_keys_dequant_kernel(const __g
 // ------------------------------------------------------------ launchers
 
 template <int BITS, int G>
-cudaError_t launch_q(const KiviQuantParams &p, bool per_channel, cudaStream_t stream)
+cudaError_t launch_q(const KiviQuantParams &p0, bool per_channel, cudaStream_t stream)
 {
     const int sms = sm_count();
+    KiviQuantParams p = p0;
+    {
+        const uint64_t dims[3] = {(uint64_t)D, (uint64_t)p.S, (uint64_t)p.B * p.H};
+        const uint64_t strides[2] = {(uint64_t)D * 2, (uint64_t)p.S * D * 2};
+        const uint32_t box[3] = {64u, per_channel ? (uint32_t)G : (uint32_t)VROWS, 1u};
+        if (!encode_tmap_f16(&p.tmap, p.x, 3, dims, strides, box, !per_channel))
+            return cudaErrorInvalidValue;
+    }
     if (per_channel) {
         auto kern = kivi_keys_kernel<BITS, G>;
         constexpr int smem = key_smem<G>();
         constexpr int warps = key_warps<G>();
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
-        const int ntiles = p.B * p.H * ((p.S_q + G - 1) / G);
+        const int ntiles = p.B * p.H * ((p.S_q + G - 1) / G) * 2;
         int grid = (ntiles + warps - 1) / warps;
         if (grid > sms) grid = sms;
         if (grid < 1) grid = 1;
         kern<<<grid, warps * 32, smem, stream>>>(p);
     } else {
         auto kern = kivi_values_kernel<BITS, G>;
-        constexpr int smem = val_smem(BITS, G);
+        constexpr int smem = val_smem();
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
-        const int nblk = (p.B * p.H * p.S_q + 31) / 32;
+        const int nblk = p.B * p.H * ((p.S_q + VROWS - 1) / VROWS);
         int grid = (nblk + VAL_WARPS - 1) / VAL_WARPS;
         if (grid > sms) grid = sms;
         if (grid < 1) grid = 1;

@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime_api.h>
 
 namespace vq {
@@ -22,6 +23,7 @@ struct GridTable {
 };
 
 struct RvqEncodeParams {
+    CUtensorMap tmap;    // x as [N rows, 128] fp16, 64 x 32 boxes, 128-byte swizzle (set by the launcher)
     const void *x;       // fp16 [N, 128]
     uint32_t *p1, *p2;   // [B, H, S_dst, W]
     float *norms;        // [B, H, S_dst]
@@ -41,6 +43,7 @@ struct RvqDecodeParams {
 };
 
 struct KiviQuantParams {
+    CUtensorMap tmap;    // x as [B*H, S, 128] fp16 (set by the launcher: box and swizzle per kernel)
     const void *x;       // fp16 [B, H, S, D]
     uint32_t *packed;
     void *scale, *zero;  // fp16
@@ -76,5 +79,11 @@ bool build_grid(const float *b, int nb, float guard, GridTable &t);
 
 // Number of SMs of the current device (cached per device).
 int sm_count();
+
+// Tiled tensor map of an fp16 tensor: dims innermost first, strides in bytes
+// of dims 1..rank-1, box in elements; false if the encoder is unavailable or
+// rejects the layout.
+bool encode_tmap_f16(CUtensorMap *map, const void *base, int rank, const uint64_t *dims,
+                     const uint64_t *strides, const uint32_t *box, bool swizzle128);
 
 }  // namespace vq

@@ -13,9 +13,10 @@
 //
 // Encode design (one row per thread, 32-row blocks per warp):
 //  * each warp owns a private 2-stage ring of 32-row blocks in shared memory,
-//    filled by per-row cp.async.bulk copies (lane i copies row i, 256 B) that
-//    complete on an mbarrier; rows sit at a 272-byte stride so the 32 row
-//    owners read 16-byte chunks without bank conflicts;
+//    each block two TMA tensor boxes (32 rows x 64 channels) that complete on
+//    an mbarrier and land with the 128-byte swizzle (chunk c of row r at
+//    chunk c ^ (r & 7)), so the 32 row owners read 16-byte chunks without
+//    bank conflicts;
 //  * a thread holds its row as 64 float2 (x[k], x[k+64]) and runs six
 //    butterfly stages with the fp32x2 add/fma instructions and the last
 //    (bit 6) stage in scalar fp32 - no shuffles;
@@ -45,24 +46,25 @@ namespace {
 constexpr int D = 128;
 constexpr int ROW_BYTES = D * 2;
 constexpr int ROW_STRIDE = ROW_BYTES + 16;
-constexpr int STAGE_BYTES = 32 * ROW_STRIDE;
 
-// Encoder shared memory, per warp: ENC_STAGES input blocks, the pair
+// Encoder shared memory: the input rings of all warps (1024-byte aligned
+// 8 KB blocks), then per warp the pair
 // scratch (enc_pairs coordinate pairs (k, k + 64) x 32 lanes, 8 bytes each),
 // two word-staging arrays with one pad word per row, and the norms of rows
 // redone by the exact path.
 constexpr int ENC_STAGES = 2;
+constexpr int ENC_BLOCK = 32 * ROW_BYTES;  // two swizzled 4 KB boxes
 __host__ __device__ constexpr int enc_words(int bits) { return D * bits / 32; }
 __host__ __device__ constexpr int enc_pairs(int bits) { return 32 / bits > 16 ? 32 / bits : 16; }
 __host__ __device__ constexpr int enc_scratch_bytes(int bits) { return enc_pairs(bits) * 32 * 8; }
 __host__ __device__ constexpr int enc_warp_bytes(int bits)
 {
-    return ENC_STAGES * STAGE_BYTES + enc_scratch_bytes(bits) + 2 * 32 * (enc_words(bits) + 1) * 4 + 32 * 4;
+    return enc_scratch_bytes(bits) + 2 * 32 * (enc_words(bits) + 1) * 4 + 32 * 4;
 }
 __host__ __device__ constexpr int enc_warps(int) { return 8; }
 __host__ __device__ constexpr int enc_smem(int bits)
 {
-    return enc_warps(bits) * (enc_warp_bytes(bits) + ENC_STAGES * 8);
+    return 1024 + enc_warps(bits) * (ENC_STAGES * ENC_BLOCK + enc_warp_bytes(bits) + ENC_STAGES * 8);
 }
 
 // sqrt(128) = 8 sqrt(2) as a double-float (nearest fp32 + fp32 remainder).
@@ -216,7 +218,7 @@ __device__ __forceinline__ void wht_lane_exact(float (&a)[4], int lane)
 // The row's words go to the warp's staging rows (o1, o2, stride W + 1) and
 // its norm to nrm[r].
 template <int BITS, bool GRID>
-__device__ __noinline__ void rvq_fixup_row(const RvqEncodeParams &p, const unsigned char *srow,
+__device__ __noinline__ void rvq_fixup_row(const RvqEncodeParams &p, const unsigned char *sblk,
                                            int r, int lane, float tb1, int tc1, float tb2,
                                            int tc2, float tcen, uint32_t *o1, uint32_t *o2,
                                            float *nrm)
@@ -224,7 +226,9 @@ __device__ __noinline__ void rvq_fixup_row(const RvqEncodeParams &p, const unsig
     constexpr int E = 32 / BITS;
     constexpr int W = D * BITS / 32;
     constexpr int LPW = E / 4;  // lanes per packed word
-    const uint2 raw = *reinterpret_cast<const uint2 *>(srow + 8 * lane);
+    // x[4l .. 4l+3]: box l >> 4, 16-byte chunk (l & 15) >> 1, half (l & 1)
+    const uint2 raw = *reinterpret_cast<const uint2 *>(sblk + (lane >> 4) * (ENC_BLOCK / 2) +
+                                                       swz128(r, (lane & 15) >> 1) + 8 * (lane & 1));
     const __half2 h01 = *reinterpret_cast<const __half2 *>(&raw.x);
     const __half2 h23 = *reinterpret_cast<const __half2 *>(&raw.y);
     float x[4] = {__low2float(h01), __high2float(h01), __low2float(h23), __high2float(h23)};
@@ -336,15 +340,18 @@ __global__ void __launch_bounds__(enc_warps(BITS) * 32, 1)
     constexpr int W = D * BITS / 32;
     constexpr int WARPS = enc_warps(BITS);
     constexpr int WB = enc_warp_bytes(BITS);
-    extern __shared__ __align__(128) unsigned char smem[];
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    unsigned char *smem = smem_1k(smem_raw);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    unsigned char *wbuf = smem + warp * WB;
-    float2 *yp = reinterpret_cast<float2 *>(wbuf + ENC_STAGES * STAGE_BYTES);
-    uint32_t *o1 = reinterpret_cast<uint32_t *>(wbuf + ENC_STAGES * STAGE_BYTES + enc_scratch_bytes(BITS));
+    unsigned char *ring = smem + warp * (ENC_STAGES * ENC_BLOCK);
+    unsigned char *wbuf = smem + WARPS * (ENC_STAGES * ENC_BLOCK) + warp * WB;
+    float2 *yp = reinterpret_cast<float2 *>(wbuf);
+    uint32_t *o1 = reinterpret_cast<uint32_t *>(wbuf + enc_scratch_bytes(BITS));
     uint32_t *o2 = o1 + 32 * (W + 1);
     float *nrm = reinterpret_cast<float *>(o2 + 32 * (W + 1));
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + WARPS * WB) + warp * ENC_STAGES;
+    uint64_t *bars =
+        reinterpret_cast<uint64_t *>(smem + WARPS * (ENC_STAGES * ENC_BLOCK + WB)) + warp * ENC_STAGES;
 
     if (lane == 0) {
 #pragma unroll
@@ -362,15 +369,12 @@ __global__ void __launch_bounds__(enc_warps(BITS) * 32, 1)
     const int nblk = (p.N + 31) >> 5;
     const int gw = blockIdx.x * WARPS + warp;
     const int tw = gridDim.x * WARPS;
-    const __half *x = static_cast<const __half *>(p.x);
-
     auto issue = [&](int blk, int s) {
-        const int r0 = blk << 5;
-        const int nrows = min(32, p.N - r0);
-        if (lane == 0) mbar_arrive_expect_tx(&bars[s], (uint32_t)(nrows * ROW_BYTES));
-        if (lane < nrows)
-            bulk_g2s(wbuf + s * STAGE_BYTES + lane * ROW_STRIDE, x + (size_t)(r0 + lane) * D,
-                     ROW_BYTES, &bars[s], pol);
+        if (lane == 0) {
+            mbar_arrive_expect_tx(&bars[s], (uint32_t)ENC_BLOCK);
+            tma_load_2d(ring + s * ENC_BLOCK, &p.tmap, 0, blk << 5, &bars[s], pol);
+            tma_load_2d(ring + s * ENC_BLOCK + ENC_BLOCK / 2, &p.tmap, 64, blk << 5, &bars[s], pol);
+        }
     };
 #pragma unroll
     for (int s = 0; s < ENC_STAGES; ++s) {
@@ -395,19 +399,18 @@ __global__ void __launch_bounds__(enc_warps(BITS) * 32, 1)
             }
             return;
         }
-        const unsigned char *sbuf = wbuf + s * STAGE_BYTES;
+        const unsigned char *sbuf = ring + s * ENC_BLOCK;
         const int row = (blk << 5) + lane;
         const bool valid = row < p.N;
 
         // ---- load the row and run the first butterfly stage (coordinate bit
         // 6) on the fp16 values: v[k] = (x[k] + x[k+64], x[k] - x[k+64]),
         // converting only x[k+64] and adding x[k] as an fp16 operand.
-        const uint4 *srow = reinterpret_cast<const uint4 *>(sbuf + lane * ROW_STRIDE);
         float2 v[64];
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
-            const uint4 lo = srow[c];
-            const uint4 hi = srow[c + 8];
+            const uint4 lo = *reinterpret_cast<const uint4 *>(sbuf + swz128(lane, c));
+            const uint4 hi = *reinterpret_cast<const uint4 *>(sbuf + ENC_BLOCK / 2 + swz128(lane, c));
             const __half *hl = reinterpret_cast<const __half *>(&lo);
             const __half *hh = reinterpret_cast<const __half *>(&hi);
 #pragma unroll
@@ -526,7 +529,7 @@ __global__ void __launch_bounds__(enc_warps(BITS) * 32, 1)
         while (fl) {
             const int r = __ffs(fl) - 1;
             fl &= fl - 1;
-            rvq_fixup_row<BITS, GRID>(p, sbuf + r * ROW_STRIDE, r, lane, tb1, tc1, tb2, tc2, tcen,
+            rvq_fixup_row<BITS, GRID>(p, sbuf, r, lane, tb1, tc1, tb2, tc2, tcen,
                                       o1, o2, nrm);
         }
         __syncwarp();
@@ -561,15 +564,15 @@ __global__ void __launch_bounds__(enc_warps(BITS) * 32, 1)
 // ---------------------------------------------------------------- decode
 //
 // x_hat = n * H (c1[i1] + c2[i2]) / sqrt(D): one row per thread.  The packed
-// words of each row arrive by two per-row bulk copies into a 3-stage ring
-// (slots padded for conflict-free 16-byte reads); centroid lookups are warp
+// words of a 32-row block (contiguous in both streams) arrive by two bulk
+// copies into a 3-stage ring; centroid lookups are warp
 // shuffles from tables replicated every 2^BITS lanes, so the packed word
 // shifted right is itself a valid shuffle index; the fp16 row is staged in
 // shared memory and written out coalesced.
 constexpr int DEC_STAGES = 3;
 constexpr int DEC_WARPS = 8;
-__host__ __device__ constexpr int dec_slot(int bits) { return 2 * (D * bits / 32) * 4 + 16; }
-__host__ __device__ constexpr int dec_warp_bytes(int bits) { return DEC_STAGES * 32 * dec_slot(bits) + 32 * ROW_STRIDE; }
+__host__ __device__ constexpr int dec_stage(int bits) { return 2 * 32 * (D * bits / 32) * 4; }
+__host__ __device__ constexpr int dec_warp_bytes(int bits) { return DEC_STAGES * dec_stage(bits) + 32 * ROW_STRIDE; }
 __host__ __device__ constexpr int dec_smem(int bits) { return DEC_WARPS * (dec_warp_bytes(bits) + DEC_STAGES * 8); }
 
 template <int BITS>
@@ -578,13 +581,13 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) rvq_decode_kernel(const __g
     constexpr int L = 1 << BITS;
     constexpr int E = 32 / BITS;
     constexpr int W = D * BITS / 32;
-    constexpr int SLOT = dec_slot(BITS);
+    constexpr int STG = dec_stage(BITS);
     constexpr int WB = dec_warp_bytes(BITS);
     extern __shared__ __align__(128) unsigned char smem[];
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     unsigned char *wbuf = smem + warp * WB;
-    unsigned char *obuf = wbuf + DEC_STAGES * 32 * SLOT;
+    unsigned char *obuf = wbuf + DEC_STAGES * STG;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + DEC_WARPS * WB) + warp * DEC_STAGES;
     if (lane == 0) {
 #pragma unroll
@@ -601,13 +604,12 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) rvq_decode_kernel(const __g
     const float2 neg1 = make_float2(-1.0f, -1.0f);
 
     auto issue = [&](int blk, int s) {
-        const int r0 = blk << 5;
-        const int nrows = min(32, p.N - r0);
-        if (lane == 0) mbar_arrive_expect_tx(&bars[s], (uint32_t)(nrows * 2 * W * 4));
-        if (lane < nrows) {
-            unsigned char *slot = wbuf + s * 32 * SLOT + lane * SLOT;
-            bulk_g2s(slot, p.p1 + (size_t)(r0 + lane) * W, W * 4, &bars[s], pol);
-            bulk_g2s(slot + W * 4, p.p2 + (size_t)(r0 + lane) * W, W * 4, &bars[s], pol);
+        if (lane == 0) {
+            const int r0 = blk << 5;
+            const uint32_t bytes = (uint32_t)(min(32, p.N - r0) * W * 4);
+            mbar_arrive_expect_tx(&bars[s], 2 * bytes);
+            bulk_g2s(wbuf + s * STG, p.p1 + (size_t)r0 * W, bytes, &bars[s], pol);
+            bulk_g2s(wbuf + s * STG + STG / 2, p.p2 + (size_t)r0 * W, bytes, &bars[s], pol);
         }
     };
 #pragma unroll
@@ -634,10 +636,11 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) rvq_decode_kernel(const __g
         }
         uint32_t w1[W], w2[W];
         {
-            const uint4 *sl = reinterpret_cast<const uint4 *>(wbuf + s * 32 * SLOT + lane * SLOT);
+            const uint4 *sa = reinterpret_cast<const uint4 *>(wbuf + s * STG + lane * W * 4);
+            const uint4 *sb = reinterpret_cast<const uint4 *>(wbuf + s * STG + STG / 2 + lane * W * 4);
 #pragma unroll
             for (int i = 0; i < W / 4; ++i) {
-                const uint4 a = sl[i], b = sl[W / 4 + i];
+                const uint4 a = sa[i], b = sb[i];
                 w1[4 * i] = a.x; w1[4 * i + 1] = a.y; w1[4 * i + 2] = a.z; w1[4 * i + 3] = a.w;
                 w2[4 * i] = b.x; w2[4 * i + 1] = b.y; w2[4 * i + 2] = b.z; w2[4 * i + 3] = b.w;
             }
@@ -701,8 +704,15 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) rvq_decode_kernel(const __g
 }
 
 template <int BITS, int MODE>
-cudaError_t launch_enc(const RvqEncodeParams &p, cudaStream_t stream)
+cudaError_t launch_enc(const RvqEncodeParams &p0, cudaStream_t stream)
 {
+    RvqEncodeParams p = p0;
+    {
+        const uint64_t dims[2] = {(uint64_t)D, (uint64_t)p.N};
+        const uint64_t strides[1] = {(uint64_t)D * 2};
+        const uint32_t box[2] = {64u, 32u};
+        if (!encode_tmap_f16(&p.tmap, p.x, 2, dims, strides, box, true)) return cudaErrorInvalidValue;
+    }
     auto kern = rvq_encode_kernel<BITS, MODE>;
     constexpr int smem = enc_smem(BITS);
     constexpr int warps = enc_warps(BITS);
