@@ -13,10 +13,10 @@ namespace vq {
 
 constexpr unsigned FULL_MASK = 0xffffffffu;
 
-// Upper bound on polls of one mbarrier phase.  Each try_wait blocks in hardware
-// for a bounded time, so this caps a wait at well under a minute even if a copy
-// never lands; on expiry the kernel records VQ_DEVERR_WAIT_TIMEOUT and returns.
-constexpr uint32_t MBAR_MAX_POLLS = 1u << 22;
+// Upper bound on the wall-clock time of one mbarrier wait (nanoseconds of
+// %globaltimer).  A copy that has not landed by then never will; the kernel
+// records VQ_DEVERR_WAIT_TIMEOUT and returns instead of spinning.
+constexpr uint64_t MBAR_TIMEOUT_NS = 2000000000ull;
 
 // One device error word per translation unit; each .cu exposes a host reader.
 #define VQ_DEFINE_ERROR_WORD(name) static __device__ unsigned int name = 0u
@@ -65,12 +65,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
     return ok != 0;
 }
 
+__device__ __forceinline__ uint64_t globaltimer_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
 // Bounded wait for phase `parity` of `bar`.  Returns false if it gave up.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity)
 {
-    for (uint32_t i = 0; i < MBAR_MAX_POLLS; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
         if (mbar_try_wait(bar, parity)) return true;
-    return false;
+        if (globaltimer_ns() - t0 > MBAR_TIMEOUT_NS) return false;
+    }
 }
 
 // 1-D bulk copy global -> shared, completion signalled on `bar` (tx bytes).

@@ -237,8 +237,8 @@ __device__ __noinline__ uint32_t code_exact(__half h, const GroupQ g, float mx)
 // landing with the 128-byte swizzle: row r's 16-byte chunk c sits at chunk
 // c ^ (r & 7) of its 128-byte line, and each quarter-warp of a 16-byte shared
 // load touches eight distinct bank groups.  A per-warp 3-stage ring; a thread
-// moves its 128 bytes to registers at once and the stage is refilled before
-// any arithmetic.  Per group: fp16 min/max (a 128-wide group combines the two
+// moves its 128 bytes to registers at once; the stage is refilled once the
+// codes are done (the rare exact path reads it).  Per group: fp16 min/max (a 128-wide group combines the two
 // halves by one shuffle), then the fast codes word by word; words go straight
 // to global memory (the 16 rows x 2 halves of a block are contiguous there).
 
@@ -265,21 +265,16 @@ __device__ __forceinline__ bool kivi_off(const KiviQuantParams &p, int b, int &o
 
 __device__ __forceinline__ __half2 u2h2(uint32_t u) { return *reinterpret_cast<__half2 *>(&u); }
 
-// The E codes of one values word, exactly (rare path).
+// The E codes of one values word, exactly (rare path), read from the staged
+// block: base is the lane's 128-byte swizzled line, c0 the word's first chunk.
 template <int BITS>
-struct WordChunks {
-    uint4 c[32 / BITS / 8];
-};
-
-template <int BITS>
-__device__ __noinline__ uint32_t values_word_exact(const WordChunks<BITS> wc, const GroupQ g, float mx)
+__device__ __noinline__ uint32_t values_word_exact(const unsigned char *base, int line, int c0, const GroupQ g,
+                                                   float mx)
 {
     constexpr int E = 32 / BITS;
     uint32_t word = 0u;
     for (int e = 0; e < E; ++e) {
-        const uint4 c = wc.c[e / 8];
-        const uint32_t u = (&c.x)[(e % 8) / 2];
-        const __half h = (e & 1) ? __high2half(u2h2(u)) : __low2half(u2h2(u));
+        const __half h = *reinterpret_cast<const __half *>(base + swz128(line, c0 + e / 8) + 2 * (e % 8));
         word |= code_exact<BITS>(h, g, mx) << (e * BITS);
     }
     return word;
@@ -348,17 +343,9 @@ __global__ void __launch_bounds__(VAL_WARPS * 32, 1)
         }
         // this thread's 64 values to registers, then refill the stage
         uint4 c[8];
-        {
-            const unsigned char *src = wbuf + s * VSTAGE_BYTES + hh * (VSTAGE_BYTES / 2);
+        const unsigned char *src = wbuf + s * VSTAGE_BYTES + hh * (VSTAGE_BYTES / 2);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) c[i] = *reinterpret_cast<const uint4 *>(src + swz128(rr, i));
-        }
-        __syncwarp();
-        fence_proxy_async_smem();
-        {
-            const int nb = blk + VAL_STAGES * tw;
-            if (nb < nblk) issue(nb, s);
-        }
+        for (int i = 0; i < 8; ++i) c[i] = *reinterpret_cast<const uint4 *>(src + swz128(rr, i));
 
         const int bh = blk / nsb;
         const int s_ = (blk - bh * nsb) * VROWS + rr;
@@ -415,14 +402,16 @@ __global__ void __launch_bounds__(VAL_WARPS * 32, 1)
                     }
                 }
                 uint32_t word = (ahi & 0xffff0000u) | (alo >> 16);
-                if (!(okw >> 31)) {
-                    WordChunks<BITS> wc;
-#pragma unroll
-                    for (int ci = 0; ci < CPW; ++ci) wc.c[ci] = c[jl * CPG + w * CPW + ci];
-                    word = values_word_exact<BITS>(wc, g, mx);
-                }
+                if (!(okw >> 31)) word = values_word_exact<BITS>(src, rr, jl * CPG + w * CPW, g, mx);
                 words[jl * WPGL + w] = word;
             }
+        }
+        // the block is consumed: recycle the stage
+        __syncwarp();
+        fence_proxy_async_smem();
+        {
+            const int nb = blk + VAL_STAGES * tw;
+            if (nb < nblk) issue(nb, s);
         }
         if (!okrow) continue;
         uint32_t *dst = p.packed + dr * W + hh * WL;
@@ -458,7 +447,8 @@ __global__ void __launch_bounds__(VAL_WARPS * 32, 1)
 // channels 2l and 2l + 1, so each token row of the tile is one conflict-free
 // 32-bit load per lane and no cross-thread reduction is needed (the pages'
 // "one thread, one whole group").  For G <= 64 the lane's 2G values move to
-// registers in the min/max pass and the stage is refilled at once.  Codes of
+// registers in the min/max pass; the stage is refilled once the codes are
+// done (the rare exact path reads the tile).  Codes of
 // the two channels of a token run as one fp32 pair.  Each word row is stored
 // as 8 bytes per lane (256 contiguous bytes per warp).
 
@@ -479,20 +469,16 @@ __host__ __device__ constexpr int key_smem()
     return 1024 + key_warps<G>() * KEY_STAGES * (G * KEY_ROW + 8);
 }
 
-// Exact codes of one word of two channels (rare path): tokens w*E .. w*E+E-1.
+// Exact codes of one word of two channels (rare path), read from the staged
+// tile: col points at this lane's channel pair of the word's first token.
 template <int BITS>
-struct KeyWord {
-    uint32_t v[32 / BITS];  // half2 (channel 2l, 2l + 1) per token
-};
-
-template <int BITS>
-__device__ __noinline__ uint2 keys_word_exact(const KeyWord<BITS> kw, const GroupQ g0, const GroupQ g1,
+__device__ __noinline__ uint2 keys_word_exact(const uint32_t *col, const GroupQ g0, const GroupQ g1,
                                               float mx0, float mx1, int nvalid)
 {
     constexpr int E = 32 / BITS;
     uint32_t w0 = 0u, w1 = 0u;
     for (int j = 0; j < E && j < nvalid; ++j) {
-        const __half2 h = u2h2(kw.v[j]);
+        const __half2 h = u2h2(col[j * 32]);
         w0 |= code_exact<BITS>(__low2half(h), g0, mx0) << (j * BITS);
         w1 |= code_exact<BITS>(__high2half(h), g1, mx1) << (j * BITS);
     }
@@ -576,12 +562,6 @@ __global__ void __launch_bounds__(key_warps<G>() * 32, 1)
                 for (int i = 0; i < G; ++i)
                     if (i >= ntok) v[i] = edge;
             }
-            __syncwarp();
-            fence_proxy_async_smem();
-            {
-                const int nt = tile + KEY_STAGES * tw;
-                if (nt < ntiles) issue(nt, s);
-            }
             __half2 l2 = u2h2(v[0]), h2 = l2, l3 = u2h2(v[1]), h3 = l3;
 #pragma unroll
             for (int i = 2; i < G; i += 2) {
@@ -615,7 +595,6 @@ __global__ void __launch_bounds__(key_warps<G>() * 32, 1)
 #pragma unroll
         for (int k = 0; k < WG; ++k) {
             uint32_t a0 = 0u, b0 = 0u, a1 = 0u, b1 = 0u, okw = 0xffffffffu;
-            KeyWord<BITS> kw;
 #pragma unroll
             for (int j = 0; j < E; ++j) {
                 const int i = k * E + j;
@@ -625,7 +604,6 @@ __global__ void __launch_bounds__(key_warps<G>() * 32, 1)
                 } else {
                     u = col[(i < ntok ? i : ntok - 1) * 32];
                 }
-                kw.v[j] = u;
                 uint32_t q0, q1;
                 code_pair_fast(__low2half(u2h2(u)), __high2half(u2h2(u)), g0.mn, g1.mn, f2, nf2, q0, q1,
                                okw);
@@ -641,7 +619,7 @@ __global__ void __launch_bounds__(key_warps<G>() * 32, 1)
             uint32_t w1 = (b1 & 0xffff0000u) | (a1 >> 16);
             const int nvalid = ntok - k * E;  // tokens of this word that exist
             if (!(okw >> 31)) {
-                const uint2 ww = keys_word_exact<BITS>(kw, g0, g1, mx0, mx1, nvalid);
+                const uint2 ww = keys_word_exact<BITS>(col + k * E * 32, g0, g1, mx0, mx1, nvalid);
                 w0 = ww.x;
                 w1 = ww.y;
             }
@@ -652,9 +630,10 @@ __global__ void __launch_bounds__(key_warps<G>() * 32, 1)
             }
             if (okoff) *reinterpret_cast<uint2 *>(dst + (size_t)k * D) = make_uint2(w0, w1);
         }
-        if constexpr (!PRELOAD) {
-            __syncwarp();
-            fence_proxy_async_smem();
+        // the tile is consumed: recycle the stage
+        __syncwarp();
+        fence_proxy_async_smem();
+        {
             const int nt = tile + KEY_STAGES * tw;
             if (nt < ntiles) issue(nt, s);
         }

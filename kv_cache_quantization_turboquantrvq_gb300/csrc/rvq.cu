@@ -48,20 +48,27 @@ constexpr int ROW_BYTES = D * 2;
 constexpr int ROW_STRIDE = ROW_BYTES + 16;
 
 // Encoder shared memory: the input rings of all warps (1024-byte aligned
-// 8 KB blocks), then per warp the pair
-// scratch (enc_pairs coordinate pairs (k, k + 64) x 32 lanes, 8 bytes each),
-// two word-staging arrays with one pad word per row, and the norms of rows
-// redone by the exact path.
+// 4 KB blocks of ER = 16 rows), then per warp the pair scratch (enc_pairs
+// coordinate pairs (k, k + 32) of a half row x 32 lanes, 8 bytes each), two
+// word-staging arrays with one pad word per row, and the norms of rows redone
+// by the exact path.  As many warps as fit (at most 16).
+constexpr int ER = 16;
 constexpr int ENC_STAGES = 2;
-constexpr int ENC_BLOCK = 32 * ROW_BYTES;  // two swizzled 4 KB boxes
+constexpr int ENC_BLOCK = ER * ROW_BYTES;  // two swizzled 2 KB boxes
+constexpr int SMEM_MAX = 227 * 1024;
 __host__ __device__ constexpr int enc_words(int bits) { return D * bits / 32; }
 __host__ __device__ constexpr int enc_pairs(int bits) { return 32 / bits > 16 ? 32 / bits : 16; }
 __host__ __device__ constexpr int enc_scratch_bytes(int bits) { return enc_pairs(bits) * 32 * 8; }
 __host__ __device__ constexpr int enc_warp_bytes(int bits)
 {
-    return enc_scratch_bytes(bits) + 2 * 32 * (enc_words(bits) + 1) * 4 + 32 * 4;
+    return enc_scratch_bytes(bits) + 2 * ER * (enc_words(bits) + 1) * 4 + ER * 4;
 }
-__host__ __device__ constexpr int enc_warps(int) { return 8; }
+__host__ __device__ constexpr int enc_warps(int bits)
+{
+    return (SMEM_MAX - 1024) / (ENC_STAGES * ENC_BLOCK + enc_warp_bytes(bits) + ENC_STAGES * 8) > 16
+               ? 16
+               : (SMEM_MAX - 1024) / (ENC_STAGES * ENC_BLOCK + enc_warp_bytes(bits) + ENC_STAGES * 8);
+}
 __host__ __device__ constexpr int enc_smem(int bits)
 {
     return 1024 + enc_warps(bits) * (ENC_STAGES * ENC_BLOCK + enc_warp_bytes(bits) + ENC_STAGES * 8);
@@ -144,20 +151,33 @@ struct SymRow {
 // and the same quantity t2 = | |y| - B/2 | - B/2 is positive exactly when
 // |y| > B, so one value gives both the decision and the margin.  The centroid
 // step uses a saturated multiply (1 when t2 > 0, 0 when t2 <= 0), which keeps
-// the selection on the FMA pipe.
-__device__ __forceinline__ void sym2_code(float y, const SymRow &k, uint32_t &a1, uint32_t &a2, float &m)
+// the selection on the FMA pipe.  The code bits are sign bits of y, y t2, y ra
+// and y ra t4: the sign of an IEEE product is the XOR of its operands' signs
+// (zeros and flushed results included), so the XORs run as fp32-pair
+// multiplies on the FMA pipe.  Two coordinates (a pair) per call.
+__device__ __forceinline__ void sym2_code2(float2 y, const SymRow &k, uint32_t &a1x, uint32_t &a2x,
+                                           uint32_t &a1y, uint32_t &a2y, float &mx, float &my)
 {
-    const float t2 = fabsf(fabsf(y) - k.hb) - k.hb;
-    m = fminf(m, fabsf(t2));
-    const float su = __saturatef(t2 * 1.2676506e30f);  // 2^100
-    const float ra = fmaf(-k.dc, su, fabsf(y) - k.c2);
-    const float t4 = fabsf(fabsf(ra) - k.he) - k.he;
-    m = fminf(m, fabsf(t4));
-    const uint32_t yb = __float_as_uint(y), rb = __float_as_uint(ra);
-    a1 = __funnelshift_l(yb, a1, 1);
-    a1 = __funnelshift_l(yb ^ __float_as_uint(t2), a1, 1);
-    a2 = __funnelshift_l(yb ^ rb, a2, 1);
-    a2 = __funnelshift_l(yb ^ rb ^ __float_as_uint(t4), a2, 1);
+    const float2 t2a = make_float2(fabsf(y.x) - k.hb, fabsf(y.y) - k.hb);
+    const float2 t2 = make_float2(fabsf(t2a.x) - k.hb, fabsf(t2a.y) - k.hb);
+    const float2 su = make_float2(__saturatef(t2.x * 1.2676506e30f), __saturatef(t2.y * 1.2676506e30f));  // 2^100
+    // |y| - c2 = (|y| - B/2) + (B/2 - c2)
+    const float2 ya = __fadd2_rn(t2a, make_float2(k.hb - k.c2, k.hb - k.c2));
+    const float2 ra = __ffma2_rn(make_float2(-k.dc, -k.dc), su, ya);
+    const float2 t4 = make_float2(fabsf(fabsf(ra.x) - k.he) - k.he, fabsf(fabsf(ra.y) - k.he) - k.he);
+    mx = fminf(mx, fminf(fabsf(t2.x), fabsf(t4.x)));
+    my = fminf(my, fminf(fabsf(t2.y), fabsf(t4.y)));
+    const float2 p1 = __fmul2_rn(y, t2);
+    const float2 p2 = __fmul2_rn(y, ra);
+    const float2 p3 = __fmul2_rn(p2, t4);
+    a1x = __funnelshift_l(__float_as_uint(y.x), a1x, 1);
+    a1x = __funnelshift_l(__float_as_uint(p1.x), a1x, 1);
+    a2x = __funnelshift_l(__float_as_uint(p2.x), a2x, 1);
+    a2x = __funnelshift_l(__float_as_uint(p3.x), a2x, 1);
+    a1y = __funnelshift_l(__float_as_uint(y.y), a1y, 1);
+    a1y = __funnelshift_l(__float_as_uint(p1.y), a1y, 1);
+    a2y = __funnelshift_l(__float_as_uint(p2.y), a2y, 1);
+    a2y = __funnelshift_l(__float_as_uint(p3.y), a2y, 1);
 }
 
 __device__ __forceinline__ void sym1_code(float y, const SymRow &k, uint32_t &a1, uint32_t &a2, float &m)
@@ -338,18 +358,20 @@ __global__ void __launch_bounds__(enc_warps(BITS) * 32, 1)
     constexpr int L = 1 << BITS;
     constexpr int E = 32 / BITS;
     constexpr int W = D * BITS / 32;
+    constexpr int WL = W / 2;  // words of a half row
     constexpr int WARPS = enc_warps(BITS);
     constexpr int WB = enc_warp_bytes(BITS);
     extern __shared__ __align__(128) unsigned char smem_raw[];
     unsigned char *smem = smem_1k(smem_raw);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const int rr = lane & 15, hh = lane >> 4;
     unsigned char *ring = smem + warp * (ENC_STAGES * ENC_BLOCK);
     unsigned char *wbuf = smem + WARPS * (ENC_STAGES * ENC_BLOCK) + warp * WB;
     float2 *yp = reinterpret_cast<float2 *>(wbuf);
     uint32_t *o1 = reinterpret_cast<uint32_t *>(wbuf + enc_scratch_bytes(BITS));
-    uint32_t *o2 = o1 + 32 * (W + 1);
-    float *nrm = reinterpret_cast<float *>(o2 + 32 * (W + 1));
+    uint32_t *o2 = o1 + ER * (W + 1);
+    float *nrm = reinterpret_cast<float *>(o2 + ER * (W + 1));
     uint64_t *bars =
         reinterpret_cast<uint64_t *>(smem + WARPS * (ENC_STAGES * ENC_BLOCK + WB)) + warp * ENC_STAGES;
 
@@ -366,14 +388,17 @@ __global__ void __launch_bounds__(enc_warps(BITS) * 32, 1)
     const float tb2 = p.t2.bnd[lane];
     const int tc2 = p.t2.code[lane];
     const float tcen = p.c1[lane & (L - 1)];
-    const int nblk = (p.N + 31) >> 5;
+    const int nblk = (p.N + ER - 1) / ER;
     const int gw = blockIdx.x * WARPS + warp;
     const int tw = gridDim.x * WARPS;
+    // the second thread of a row takes x[k] - x[k + 64]: flip the fp16 signs
+    const uint32_t negm = hh ? 0x80008000u : 0u;
+
     auto issue = [&](int blk, int s) {
         if (lane == 0) {
             mbar_arrive_expect_tx(&bars[s], (uint32_t)ENC_BLOCK);
-            tma_load_2d(ring + s * ENC_BLOCK, &p.tmap, 0, blk << 5, &bars[s], pol);
-            tma_load_2d(ring + s * ENC_BLOCK + ENC_BLOCK / 2, &p.tmap, 64, blk << 5, &bars[s], pol);
+            tma_load_2d(ring + s * ENC_BLOCK, &p.tmap, 0, blk * ER, &bars[s], pol);
+            tma_load_2d(ring + s * ENC_BLOCK + ENC_BLOCK / 2, &p.tmap, 64, blk * ER, &bars[s], pol);
         }
     };
 #pragma unroll
@@ -400,38 +425,43 @@ __global__ void __launch_bounds__(enc_warps(BITS) * 32, 1)
             return;
         }
         const unsigned char *sbuf = ring + s * ENC_BLOCK;
-        const int row = (blk << 5) + lane;
+        const int row = blk * ER + rr;
         const bool valid = row < p.N;
 
-        // ---- load the row and run the first butterfly stage (coordinate bit
-        // 6) on the fp16 values: v[k] = (x[k] + x[k+64], x[k] - x[k+64]),
-        // converting only x[k+64] and adding x[k] as an fp16 operand.
-        float2 v[64];
+        // ---- first butterfly stage (coordinate bit 6) on the fp16 values:
+        // u[k] = x[k] + (-1)^h x[k + 64], k in [0, 64), held as pairs
+        // (u[k], u[k + 32]); only the second operand is converted, the first
+        // is added as an fp16 operand.
+        float2 v[32];
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-            const uint4 lo = *reinterpret_cast<const uint4 *>(sbuf + swz128(lane, c));
-            const uint4 hi = *reinterpret_cast<const uint4 *>(sbuf + ENC_BLOCK / 2 + swz128(lane, c));
-            const __half *hl = reinterpret_cast<const __half *>(&lo);
-            const __half *hh = reinterpret_cast<const __half *>(&hi);
+        for (int c = 0; c < 4; ++c) {
+            const uint4 la = *reinterpret_cast<const uint4 *>(sbuf + swz128(rr, c));
+            const uint4 lb = *reinterpret_cast<const uint4 *>(sbuf + swz128(rr, c + 4));
+            uint4 ha = *reinterpret_cast<const uint4 *>(sbuf + ENC_BLOCK / 2 + swz128(rr, c));
+            uint4 hb = *reinterpret_cast<const uint4 *>(sbuf + ENC_BLOCK / 2 + swz128(rr, c + 4));
+            ha.x ^= negm; ha.y ^= negm; ha.z ^= negm; ha.w ^= negm;
+            hb.x ^= negm; hb.y ^= negm; hb.z ^= negm; hb.w ^= negm;
+            const __half *pla = reinterpret_cast<const __half *>(&la);
+            const __half *plb = reinterpret_cast<const __half *>(&lb);
+            const __half *pha = reinterpret_cast<const __half *>(&ha);
+            const __half *phb = reinterpret_cast<const __half *>(&hb);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const float b = __half2float(hh[j]);
-                v[8 * c + j] = make_float2(add_f16_f32(hl[j], b), add_f16_f32(hl[j], -b));
-            }
+            for (int j = 0; j < 8; ++j)
+                v[8 * c + j] = make_float2(add_f16_f32(pla[j], __half2float(pha[j])),
+                                           add_f16_f32(plb[j], __half2float(phb[j])));
         }
 
-        // ---- norm: sum of squares of the stage outputs is twice sum x^2
-        float2 acc[8];
+        // ---- norm: the two halves' sums of squares add up to twice sum x^2
+        float2 acc[4];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] = make_float2(0.0f, 0.0f);
+        for (int i = 0; i < 4; ++i) acc[i] = make_float2(0.0f, 0.0f);
 #pragma unroll
-        for (int k = 0; k < 64; ++k) acc[k & 7] = __ffma2_rn(v[k], v[k], acc[k & 7]);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) acc[i] = __fadd2_rn(acc[i], acc[i + 4]);
+        for (int k = 0; k < 32; ++k) acc[k & 3] = __ffma2_rn(v[k], v[k], acc[k & 3]);
         acc[0] = __fadd2_rn(acc[0], acc[2]);
         acc[1] = __fadd2_rn(acc[1], acc[3]);
         acc[0] = __fadd2_rn(acc[0], acc[1]);
-        const float q = 0.5f * (acc[0].x + acc[0].y);
+        const float qs = acc[0].x + acc[0].y;
+        const float q = 0.5f * (qs + __shfl_xor_sync(FULL_MASK, qs, 16));
         const float n = __fsqrt_rn(q);
         const float den = n * SQRT_D_HI;
         if constexpr (MODE != MODE_SYM) {
@@ -439,15 +469,15 @@ __global__ void __launch_bounds__(enc_warps(BITS) * 32, 1)
             const float inv = q > 0.0f ? __frcp_rn(den) : 0.0f;
             const float2 inv2 = make_float2(inv, inv);
 #pragma unroll
-            for (int k = 0; k < 64; ++k) v[k] = __fmul2_rn(v[k], inv2);
+            for (int k = 0; k < 32; ++k) v[k] = __fmul2_rn(v[k], inv2);
         }
 
-        // ---- remaining butterfly stages: index bits 0-5 across the float2 array
+        // ---- H64 of the half: coordinate bits 0-4 across the array, bit 5 in the pair
         const float2 neg1 = make_float2(-1.0f, -1.0f);
 #pragma unroll
-        for (int h = 1; h < 64; h <<= 1) {
+        for (int h = 1; h < 32; h <<= 1) {
 #pragma unroll
-            for (int k = 0; k < 64; ++k) {
+            for (int k = 0; k < 32; ++k) {
                 if ((k & h) == 0) {
                     const float2 a = v[k], b = v[k + h];
                     v[k] = __fadd2_rn(a, b);
@@ -455,6 +485,9 @@ __global__ void __launch_bounds__(enc_warps(BITS) * 32, 1)
                 }
             }
         }
+#pragma unroll
+        for (int k = 0; k < 32; ++k) v[k] = make_float2(v[k].x + v[k].y, v[k].x - v[k].y);
+
         // symmetric modes quantize S itself against thresholds scaled by den
         SymRow sk;
         sk.hb = 0.5f * p.b1[(1 << BITS) - 2] * den;
@@ -465,16 +498,18 @@ __global__ void __launch_bounds__(enc_warps(BITS) * 32, 1)
         const float guard = MODE == MODE_SYM ? p.guard * den : p.guard;
 
         // ---- two-stage boundary count and LSB-first packing.  Slice `ps` of PP
-        // coordinate pairs (k, k + 64), k in [ps*PP, ps*PP + PP), goes to the
+        // coordinate pairs (k, k + 32), k in [ps*PP, ps*PP + PP), goes to the
         // scratch yp[i * 32 + lane]; each step of the word loop reads E pairs
-        // and produces word kx = k/E from the first coordinates and word
-        // kx + W/2 from the second ones.
-        constexpr int PP = enc_pairs(BITS);
+        // and produces word kx = k/E of the half from the first coordinates
+        // and word kx + WL/2 from the second ones.
+        constexpr int PP = enc_pairs(BITS) < 32 ? enc_pairs(BITS) : 32;
         float mx = __int_as_float(0x7f800000), my = mx;
+        uint32_t *w1row = o1 + rr * (W + 1) + hh * WL;
+        uint32_t *w2row = o2 + rr * (W + 1) + hh * WL;
 #pragma unroll 1
-        for (int ps = 0; ps < 64 / PP; ++ps) {
+        for (int ps = 0; ps < 32 / PP; ++ps) {
 #pragma unroll
-            for (int q4 = 0; q4 < 64 / PP; ++q4) {
+            for (int q4 = 0; q4 < 32 / PP; ++q4) {
                 if (ps == q4) {
 #pragma unroll
                     for (int i = 0; i < PP; ++i) yp[i * 32 + lane] = v[q4 * PP + i];
@@ -488,8 +523,7 @@ __global__ void __launch_bounds__(enc_warps(BITS) * 32, 1)
                     for (int i = E - 1; i >= 0; --i) {
                         const float2 y2 = yp[(w * E + i) * 32 + lane];
                         if constexpr (BITS == 2) {
-                            sym2_code(y2.x, sk, a1x, a2x, mx);
-                            sym2_code(y2.y, sk, a1y, a2y, my);
+                            sym2_code2(y2, sk, a1x, a2x, a1y, a2y, mx, my);
                         } else {
                             sym1_code(y2.x, sk, a1x, a2x, mx);
                             sym1_code(y2.y, sk, a1y, a2y, my);
@@ -513,24 +547,26 @@ __global__ void __launch_bounds__(enc_warps(BITS) * 32, 1)
                     }
                 }
                 const int kx = ps * (PP / E) + w;
-                o1[lane * (W + 1) + kx] = a1x;
-                o2[lane * (W + 1) + kx] = a2x;
-                o1[lane * (W + 1) + W / 2 + kx] = a1y;
-                o2[lane * (W + 1) + W / 2 + kx] = a2y;
+                w1row[kx] = a1x;
+                w2row[kx] = a2x;
+                w1row[WL / 2 + kx] = a1y;
+                w2row[WL / 2 + kx] = a2y;
             }
         }
         const float m = fminf(mx, my);
         // a zero row has no direction: always take the exact path for it
-        const bool flag = valid && (!(m >= guard) || !(q > 0.0f));
+        const bool hflag = valid && (!(m >= guard) || !(q > 0.0f));
+        // (the shuffle runs on every lane: no short-circuit around it)
+        const int pflag = __shfl_xor_sync(FULL_MASK, hflag ? 1 : 0, 16);
+        const bool flag = hflag || pflag != 0;
 
         // ---- rows with a value inside the guard band: exact recompute by the warp
         __syncwarp();
-        unsigned fl = __ballot_sync(FULL_MASK, flag);
+        unsigned fl = __ballot_sync(FULL_MASK, flag) & 0xffffu;
         while (fl) {
             const int r = __ffs(fl) - 1;
             fl &= fl - 1;
-            rvq_fixup_row<BITS, GRID>(p, sbuf, r, lane, tb1, tc1, tb2, tc2, tcen,
-                                      o1, o2, nrm);
+            rvq_fixup_row<BITS, GRID>(p, sbuf, r, lane, tb1, tc1, tb2, tc2, tcen, o1, o2, nrm);
         }
         __syncwarp();
 
@@ -546,46 +582,88 @@ __global__ void __launch_bounds__(enc_warps(BITS) * 32, 1)
         const bool okrow = valid && rvq_dst_row(p, row, drow);
         const int drow32 = (int)drow;
 #pragma unroll
-        for (int i = 0; i < W; ++i) {
+        for (int i = 0; i < ER * W / 32; ++i) {
             const int idx = i * 32 + lane;
             const int r = idx / W, w = idx % W;
             const int dr = __shfl_sync(FULL_MASK, drow32, r);
-            const bool ok = __shfl_sync(FULL_MASK, okrow ? 1 : 0, r) != 0;
-            if (ok) {
+            const bool okr = __shfl_sync(FULL_MASK, okrow ? 1 : 0, r) != 0;
+            if (okr) {
                 p.p1[(size_t)dr * W + w] = o1[r * (W + 1) + w];
                 p.p2[(size_t)dr * W + w] = o2[r * (W + 1) + w];
             }
         }
-        if (okrow) p.norms[drow] = flag ? nrm[lane] : n;
+        if (okrow && hh == 0) p.norms[drow] = flag ? nrm[rr] : n;
         __syncwarp();
     }
 }
 
 // ---------------------------------------------------------------- decode
 //
-// x_hat = n * H (c1[i1] + c2[i2]) / sqrt(D): one row per thread.  The packed
-// words of a 32-row block (contiguous in both streams) arrive by two bulk
-// copies into a 3-stage ring; centroid lookups are warp
-// shuffles from tables replicated every 2^BITS lanes, so the packed word
-// shifted right is itself a valid shuffle index; the fp16 row is staged in
-// shared memory and written out coalesced.
+// x_hat = n * H (c1[i1] + c2[i2]) / sqrt(D), two threads per row: lane l
+// works on row l & 15 of a 16-row block and on the coordinates
+// [64h, 64h + 64), h = l >> 4.  With H = [[H64, H64], [H64, -H64]], thread h
+// transforms its own half, A_h = H64 u_h, scales it, swaps it with its
+// partner (lane l ^ 16) and keeps A_0 + A_1 (h = 0) or A_0 - A_1 (h = 1): the
+// coordinates it outputs.  The packed words of a 16-row block (contiguous in
+// both streams) arrive by two bulk copies into a 3-stage ring.  For b <= 2
+// the two codes of a coordinate index one merged table c1[i1] + c2[i2] (16 or
+// 4 fp32 entries held one per lane and replicated across the warp, read by
+// shuffle): the words of both streams are first interleaved so that a plain
+// shift leaves the merged index in the low bits.  For b = 4 each stage has its
+// own 16-entry table.  The fp16 half rows are staged in shared memory and
+// written out coalesced.
 constexpr int DEC_STAGES = 3;
-constexpr int DEC_WARPS = 8;
-__host__ __device__ constexpr int dec_stage(int bits) { return 2 * 32 * (D * bits / 32) * 4; }
-__host__ __device__ constexpr int dec_warp_bytes(int bits) { return DEC_STAGES * dec_stage(bits) + 32 * ROW_STRIDE; }
+constexpr int DEC_WARPS = 16;
+constexpr int DROWS = 16;
+__host__ __device__ constexpr int dec_stage(int bits) { return 2 * DROWS * (D * bits / 32) * 4; }
+__host__ __device__ constexpr int dec_warp_bytes(int bits) { return DEC_STAGES * dec_stage(bits) + DROWS * ROW_STRIDE; }
 __host__ __device__ constexpr int dec_smem(int bits) { return DEC_WARPS * (dec_warp_bytes(bits) + DEC_STAGES * 8); }
+
+// Decoded values c1[i1] + c2[i2] of the 64 coordinates of one half row, as 32
+// pairs (u[2k], u[2k + 1]).  w1 / w2: the half row's words of each stream.
+template <int BITS>
+__device__ __forceinline__ void dec_lookup(const uint32_t (&w1)[BITS * 2], const uint32_t (&w2)[BITS * 2],
+                                           float tab, float tc1, float tc2, float2 (&v)[32])
+{
+    constexpr int E = 32 / BITS;
+    float u[64];
+    if constexpr (BITS == 4) {
+#pragma unroll
+        for (int e = 0; e < 64; ++e) {
+            const int sh = (e % E) * 4;
+            u[e] = __shfl_sync(FULL_MASK, tc1, (int)(w1[e / E] >> sh)) +
+                   __shfl_sync(FULL_MASK, tc2, (int)(w2[e / E] >> sh));
+        }
+    } else {
+        // merged index i1 | i2 << BITS: even coordinates from me, odd from mo
+        constexpr uint32_t CM = BITS == 2 ? 0x33333333u : 0x55555555u;
+#pragma unroll
+        for (int j = 0; j < 2 * BITS; ++j) {
+            const uint32_t me = (w1[j] & CM) | ((w2[j] << BITS) & ~CM);
+            const uint32_t mo = ((w1[j] >> BITS) & CM) | (w2[j] & ~CM);
+#pragma unroll
+            for (int m = 0; m < E / 2; ++m) {
+                u[j * E + 2 * m] = __shfl_sync(FULL_MASK, tab, (int)(me >> (2 * BITS * m)));
+                u[j * E + 2 * m + 1] = __shfl_sync(FULL_MASK, tab, (int)(mo >> (2 * BITS * m)));
+            }
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < 32; ++k) v[k] = make_float2(u[2 * k], u[2 * k + 1]);
+}
 
 template <int BITS>
 __global__ void __launch_bounds__(DEC_WARPS * 32, 1) rvq_decode_kernel(const __grid_constant__ RvqDecodeParams p)
 {
     constexpr int L = 1 << BITS;
-    constexpr int E = 32 / BITS;
     constexpr int W = D * BITS / 32;
+    constexpr int WH = W / 2;  // words per half row
     constexpr int STG = dec_stage(BITS);
     constexpr int WB = dec_warp_bytes(BITS);
     extern __shared__ __align__(128) unsigned char smem[];
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const int rr = lane & 15, hh = lane >> 4;
     unsigned char *wbuf = smem + warp * WB;
     unsigned char *obuf = wbuf + DEC_STAGES * STG;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + DEC_WARPS * WB) + warp * DEC_STAGES;
@@ -596,17 +674,21 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) rvq_decode_kernel(const __g
     }
     __syncwarp();
     const uint64_t pol = l2_policy_evict_first();
+    // tables: per-stage (replicated every 2^BITS lanes) and merged (index
+    // i1 | i2 << BITS, replicated every 2^(2 BITS) lanes; b <= 2 only)
     const float tc1 = p.c1[lane & (L - 1)];
     const float tc2 = p.c2[lane & (L - 1)];
-    const int nblk = (p.N + 31) >> 5;
+    const float tab = BITS == 4 ? 0.0f : p.c1[lane & (L - 1)] + p.c2[(lane >> BITS) & (L - 1)];
+    const int nblk = (p.N + DROWS - 1) / DROWS;
     const int gw = blockIdx.x * DEC_WARPS + warp;
     const int tw = gridDim.x * DEC_WARPS;
     const float2 neg1 = make_float2(-1.0f, -1.0f);
+    const float2 sgn = hh ? neg1 : make_float2(1.0f, 1.0f);
 
     auto issue = [&](int blk, int s) {
         if (lane == 0) {
-            const int r0 = blk << 5;
-            const uint32_t bytes = (uint32_t)(min(32, p.N - r0) * W * 4);
+            const int r0 = blk * DROWS;
+            const uint32_t bytes = (uint32_t)(min(DROWS, p.N - r0) * W * 4);
             mbar_arrive_expect_tx(&bars[s], 2 * bytes);
             bulk_g2s(wbuf + s * STG, p.p1 + (size_t)r0 * W, bytes, &bars[s], pol);
             bulk_g2s(wbuf + s * STG + STG / 2, p.p2 + (size_t)r0 * W, bytes, &bars[s], pol);
@@ -621,7 +703,7 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) rvq_decode_kernel(const __g
         const int blk = gw + it * tw;
         if (blk >= nblk) break;
         const int s = it % DEC_STAGES;
-        const int row = (blk << 5) + lane;
+        const int row = blk * DROWS + rr;
         const bool valid = row < p.N;
         const float n = valid ? __ldg(p.norms + row) : 0.0f;
         const bool ok = mbar_wait_bounded(&bars[s], (uint32_t)(it / DEC_STAGES) & 1u);
@@ -634,15 +716,16 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) rvq_decode_kernel(const __g
             }
             return;
         }
-        uint32_t w1[W], w2[W];
+        uint32_t w1[WH], w2[WH];
         {
-            const uint4 *sa = reinterpret_cast<const uint4 *>(wbuf + s * STG + lane * W * 4);
-            const uint4 *sb = reinterpret_cast<const uint4 *>(wbuf + s * STG + STG / 2 + lane * W * 4);
+            const uint32_t *sa = reinterpret_cast<const uint32_t *>(wbuf + s * STG) + rr * W + hh * WH;
+            const uint32_t *sb = reinterpret_cast<const uint32_t *>(wbuf + s * STG + STG / 2) + rr * W + hh * WH;
 #pragma unroll
-            for (int i = 0; i < W / 4; ++i) {
-                const uint4 a = sa[i], b = sb[i];
-                w1[4 * i] = a.x; w1[4 * i + 1] = a.y; w1[4 * i + 2] = a.z; w1[4 * i + 3] = a.w;
-                w2[4 * i] = b.x; w2[4 * i + 1] = b.y; w2[4 * i + 2] = b.z; w2[4 * i + 3] = b.w;
+            for (int i = 0; i < WH; i += 2) {
+                const uint2 a = *reinterpret_cast<const uint2 *>(sa + i);
+                const uint2 b = *reinterpret_cast<const uint2 *>(sb + i);
+                w1[i] = a.x; w1[i + 1] = a.y;
+                w2[i] = b.x; w2[i + 1] = b.y;
             }
         }
         // the words are in registers: recycle the stage
@@ -652,18 +735,13 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) rvq_decode_kernel(const __g
             const int nb = blk + DEC_STAGES * tw;
             if (nb < nblk) issue(nb, s);
         }
-        float2 v[64];
+        float2 v[32];
+        dec_lookup<BITS>(w1, w2, tab, tc1, tc2, v);
+        // H64 on the half: coordinate bits 1-5 across the array, bit 0 in the pair
 #pragma unroll
-        for (int e = 0; e < D; ++e) {
-            const int sh = (e % E) * BITS;
-            const float c = __shfl_sync(FULL_MASK, tc1, (int)(w1[e / E] >> sh)) +
-                            __shfl_sync(FULL_MASK, tc2, (int)(w2[e / E] >> sh));
-            if (e < 64) v[e].x = c; else v[e - 64].y = c;
-        }
+        for (int h = 1; h < 32; h <<= 1) {
 #pragma unroll
-        for (int h = 1; h < 64; h <<= 1) {
-#pragma unroll
-            for (int k = 0; k < 64; ++k) {
+            for (int k = 0; k < 32; ++k) {
                 if ((k & h) == 0) {
                     const float2 a = v[k], b = v[k + h];
                     v[k] = __fadd2_rn(a, b);
@@ -671,30 +749,29 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) rvq_decode_kernel(const __g
                 }
             }
         }
-        // last butterfly stage with the scale n / sqrt(D) applied to its inputs
+        // scale by n / sqrt(D), swap halves with the partner, last stage
         const float sc = __fdiv_rn(n, SQRT_D_HI);
         const float2 sc2 = make_float2(sc, sc);
-        uint4 *orow = reinterpret_cast<uint4 *>(obuf + lane * ROW_STRIDE);
+        uint32_t o[32];
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-            uint32_t lo[4], hi[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float2 a = __fmul2_rn(v[8 * c + 2 * j], sc2), b = __fmul2_rn(v[8 * c + 2 * j + 1], sc2);
-                const __half2 l2 = __floats2half2_rn(a.x + a.y, b.x + b.y);
-                const __half2 h2 = __floats2half2_rn(a.x - a.y, b.x - b.y);
-                lo[j] = *reinterpret_cast<const uint32_t *>(&l2);
-                hi[j] = *reinterpret_cast<const uint32_t *>(&h2);
-            }
-            orow[c] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-            orow[c + 8] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        for (int k = 0; k < 32; ++k) {
+            const float2 a = __fmul2_rn(make_float2(v[k].x + v[k].y, v[k].x - v[k].y), sc2);
+            const float2 b = make_float2(__shfl_xor_sync(FULL_MASK, a.x, 16), __shfl_xor_sync(FULL_MASK, a.y, 16));
+            // h = 0: a + b; h = 1: b - a (own half is the second operand)
+            const float2 x2 = __ffma2_rn(a, sgn, b);
+            const __half2 hx = __floats2half2_rn(x2.x, x2.y);
+            o[k] = *reinterpret_cast<const uint32_t *>(&hx);
         }
+        // o[k] holds coordinates 2k, 2k + 1 of the half
+        uint4 *orow = reinterpret_cast<uint4 *>(obuf + rr * ROW_STRIDE + hh * 128);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) orow[c] = make_uint4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
         __syncwarp();
         // coalesced write-out: chunk idx = i*32 + lane is 16-byte chunk idx % 16 of row idx / 16
-        const int nrows = min(32, p.N - (blk << 5));
-        uint4 *gout = reinterpret_cast<uint4 *>(static_cast<__half *>(p.out) + (size_t)(blk << 5) * D);
+        const int nrows = min(DROWS, p.N - blk * DROWS);
+        uint4 *gout = reinterpret_cast<uint4 *>(static_cast<__half *>(p.out) + (size_t)blk * DROWS * D);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
+        for (int i = 0; i < 8; ++i) {
             const int idx = i * 32 + lane;
             const int r = idx >> 4, c = idx & 15;
             if (r < nrows) gout[idx] = *reinterpret_cast<const uint4 *>(obuf + r * ROW_STRIDE + c * 16);
@@ -710,7 +787,7 @@ cudaError_t launch_enc(const RvqEncodeParams &p0, cudaStream_t stream)
     {
         const uint64_t dims[2] = {(uint64_t)D, (uint64_t)p.N};
         const uint64_t strides[1] = {(uint64_t)D * 2};
-        const uint32_t box[2] = {64u, 32u};
+        const uint32_t box[2] = {64u, (uint32_t)ER};
         if (!encode_tmap_f16(&p.tmap, p.x, 2, dims, strides, box, true)) return cudaErrorInvalidValue;
     }
     auto kern = rvq_encode_kernel<BITS, MODE>;
@@ -718,7 +795,7 @@ cudaError_t launch_enc(const RvqEncodeParams &p0, cudaStream_t stream)
     constexpr int warps = enc_warps(BITS);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    const int nblk = (p.N + 31) / 32;
+    const int nblk = (p.N + ER - 1) / ER;
     int grid = (nblk + warps - 1) / warps;
     const int sms = sm_count();
     if (grid > sms) grid = sms;
@@ -734,7 +811,7 @@ cudaError_t launch_dec(const RvqDecodeParams &p, cudaStream_t stream)
     constexpr int smem = dec_smem(BITS);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    const int nblk = (p.N + 31) / 32;
+    const int nblk = (p.N + DROWS - 1) / DROWS;
     int grid = (nblk + DEC_WARPS - 1) / DEC_WARPS;
     const int sms = sm_count();
     if (grid > sms) grid = sms;
