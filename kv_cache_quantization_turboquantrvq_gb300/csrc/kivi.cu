@@ -447,26 +447,47 @@ __global__ void __launch_bounds__(VAL_WARPS * 32, 1)
 // channels 2l and 2l + 1, so each token row of the tile is one conflict-free
 // 32-bit load per lane and no cross-thread reduction is needed (the pages'
 // "one thread, one whole group").  For G <= 64 the lane's 2G values move to
-// registers in the min/max pass; the stage is refilled once the codes are
-// done (the rare exact path reads the tile).  Codes of
+// registers in the min/max pass and the stage is refilled at once (the rare
+// exact path gets its word through a small scratch).  Codes of
 // the two channels of a token run as one fp32 pair.  Each word row is stored
 // as 8 bytes per lane (256 contiguous bytes per warp).
 
-constexpr int KEY_STAGES = 2;
 constexpr int KEY_SMEM_BUDGET = 220 * 1024;
 constexpr int KEY_ROW = 128;  // bytes of one token row of a half-tile
 
+// For G <= 64 the lane's tile column lives in registers after the min/max pass
+// and the stage is refilled at once, so one stage per warp keeps a copy in
+// flight during the codes; G = 128 reads the tile twice and double-buffers.
 template <int G>
-__host__ __device__ constexpr int key_warps()
+__host__ __device__ constexpr int key_stages()
 {
-    return KEY_SMEM_BUDGET / (KEY_STAGES * G * KEY_ROW) > 16 ? 16
-                                                               : KEY_SMEM_BUDGET / (KEY_STAGES * G * KEY_ROW);
+    return G <= 64 ? 1 : 2;
 }
 
-template <int G>
+// Exact-path scratch per warp (G <= 64): one word's values, 32 lanes.
+template <int BITS>
+__host__ __device__ constexpr int key_scratch()
+{
+    return (32 / BITS) * 32 * 4;
+}
+
+template <int BITS, int G>
+__host__ __device__ constexpr int key_warp_bytes()
+{
+    return key_stages<G>() * (G * KEY_ROW) + (G <= 64 ? key_scratch<BITS>() : 0);
+}
+
+template <int BITS, int G>
+__host__ __device__ constexpr int key_warps()
+{
+    return KEY_SMEM_BUDGET / (key_warp_bytes<BITS, G>() + 16) > 16 ? 16
+                                                                      : KEY_SMEM_BUDGET / (key_warp_bytes<BITS, G>() + 16);
+}
+
+template <int BITS, int G>
 __host__ __device__ constexpr int key_smem()
 {
-    return 1024 + key_warps<G>() * KEY_STAGES * (G * KEY_ROW + 8);
+    return 1024 + key_warps<BITS, G>() * (key_warp_bytes<BITS, G>() + 16);
 }
 
 // Exact codes of one word of two channels (rare path), read from the staged
@@ -486,21 +507,23 @@ __device__ __noinline__ uint2 keys_word_exact(const uint32_t *col, const GroupQ 
 }
 
 template <int BITS, int G>
-__global__ void __launch_bounds__(key_warps<G>() * 32, 1)
+__global__ void __launch_bounds__(key_warps<BITS, G>() * 32, 1)
     kivi_keys_kernel(const __grid_constant__ KiviQuantParams p)
 {
-    constexpr int KEY_WARPS = key_warps<G>();
+    constexpr int KEY_WARPS = key_warps<BITS, G>();
+    constexpr int KEY_STAGES = key_stages<G>();
     constexpr int E = 32 / BITS;
     constexpr int WG = G * BITS / 32;  // words per channel per group
     constexpr int TILE = G * KEY_ROW;
     constexpr bool PRELOAD = G <= 64;
+    constexpr int WBYTES = key_warp_bytes<BITS, G>();
     extern __shared__ __align__(128) unsigned char smem_raw[];
     unsigned char *smem = smem_1k(smem_raw);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    unsigned char *wbuf = smem + warp * (KEY_STAGES * TILE);
-    uint64_t *bars =
-        reinterpret_cast<uint64_t *>(smem + KEY_WARPS * KEY_STAGES * TILE) + warp * KEY_STAGES;
+    unsigned char *wbuf = smem + warp * WBYTES;
+    uint32_t *xs = reinterpret_cast<uint32_t *>(wbuf + KEY_STAGES * TILE);  // exact-path scratch
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + KEY_WARPS * WBYTES) + warp * KEY_STAGES;
     if (lane == 0) {
 #pragma unroll
         for (int s = 0; s < KEY_STAGES; ++s) mbar_init(&bars[s], 1);
@@ -562,6 +585,13 @@ __global__ void __launch_bounds__(key_warps<G>() * 32, 1)
                 for (int i = 0; i < G; ++i)
                     if (i >= ntok) v[i] = edge;
             }
+            // the column is in registers: refill the stage now
+            __syncwarp();
+            fence_proxy_async_smem();
+            {
+                const int nt = tile + KEY_STAGES * tw;
+                if (nt < ntiles) issue(nt, s);
+            }
             __half2 l2 = u2h2(v[0]), h2 = l2, l3 = u2h2(v[1]), h3 = l3;
 #pragma unroll
             for (int i = 2; i < G; i += 2) {
@@ -619,7 +649,16 @@ __global__ void __launch_bounds__(key_warps<G>() * 32, 1)
             uint32_t w1 = (b1 & 0xffff0000u) | (a1 >> 16);
             const int nvalid = ntok - k * E;  // tokens of this word that exist
             if (!(okw >> 31)) {
-                const uint2 ww = keys_word_exact<BITS>(col + k * E * 32, g0, g1, mx0, mx1, nvalid);
+                const uint32_t *wc;
+                if constexpr (PRELOAD) {
+                    // the stage is already refilling: pass the word through scratch
+#pragma unroll
+                    for (int j = 0; j < E; ++j) xs[j * 32 + lane] = v[k * E + j];
+                    wc = xs + lane;
+                } else {
+                    wc = col + k * E * 32;
+                }
+                const uint2 ww = keys_word_exact<BITS>(wc, g0, g1, mx0, mx1, nvalid);
                 w0 = ww.x;
                 w1 = ww.y;
             }
@@ -630,10 +669,10 @@ __global__ void __launch_bounds__(key_warps<G>() * 32, 1)
             }
             if (okoff) *reinterpret_cast<uint2 *>(dst + (size_t)k * D) = make_uint2(w0, w1);
         }
-        // the tile is consumed: recycle the stage
-        __syncwarp();
-        fence_proxy_async_smem();
-        {
+        if constexpr (!PRELOAD) {
+            // the tile is consumed: recycle the stage
+            __syncwarp();
+            fence_proxy_async_smem();
             const int nt = tile + KEY_STAGES * tw;
             if (nt < ntiles) issue(nt, s);
         }
@@ -869,8 +908,8 @@ cudaError_t launch_q(const KiviQuantParams &p0, bool per_channel, cudaStream_t s
     }
     if (per_channel) {
         auto kern = kivi_keys_kernel<BITS, G>;
-        constexpr int smem = key_smem<G>();
-        constexpr int warps = key_warps<G>();
+        constexpr int smem = key_smem<BITS, G>();
+        constexpr int warps = key_warps<BITS, G>();
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
         const int ntiles = p.B * p.H * ((p.S_q + G - 1) / G) * 2;

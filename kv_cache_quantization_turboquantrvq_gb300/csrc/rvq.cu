@@ -391,8 +391,6 @@ __global__ void __launch_bounds__(enc_warps(BITS) * 32, 1)
     const int nblk = (p.N + ER - 1) / ER;
     const int gw = blockIdx.x * WARPS + warp;
     const int tw = gridDim.x * WARPS;
-    // the second thread of a row takes x[k] - x[k + 64]: flip the fp16 signs
-    const uint32_t negm = hh ? 0x80008000u : 0u;
 
     auto issue = [&](int blk, int s) {
         if (lane == 0) {
@@ -428,30 +426,28 @@ __global__ void __launch_bounds__(enc_warps(BITS) * 32, 1)
         const int row = blk * ER + rr;
         const bool valid = row < p.N;
 
-        // ---- first butterfly stage (coordinate bit 6) on the fp16 values:
-        // u[k] = x[k] + (-1)^h x[k + 64], k in [0, 64), held as pairs
-        // (u[k], u[k + 32]); only the second operand is converted, the first
-        // is added as an fp16 operand.
+        // ---- this thread's input half x_h = x[64h .. 64h + 63] as pairs
+        // (x_h[k], x_h[k + 32]); the bit-5 butterfly runs on the fp16 values
+        // (only the second operand is converted, the first is added as an
+        // fp16 operand), then bits 0-4 across the array: Z_h = H64 x_h.
         float2 v[32];
+        {
+            const unsigned char *src = sbuf + hh * (ENC_BLOCK / 2);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            const uint4 la = *reinterpret_cast<const uint4 *>(sbuf + swz128(rr, c));
-            const uint4 lb = *reinterpret_cast<const uint4 *>(sbuf + swz128(rr, c + 4));
-            uint4 ha = *reinterpret_cast<const uint4 *>(sbuf + ENC_BLOCK / 2 + swz128(rr, c));
-            uint4 hb = *reinterpret_cast<const uint4 *>(sbuf + ENC_BLOCK / 2 + swz128(rr, c + 4));
-            ha.x ^= negm; ha.y ^= negm; ha.z ^= negm; ha.w ^= negm;
-            hb.x ^= negm; hb.y ^= negm; hb.z ^= negm; hb.w ^= negm;
-            const __half *pla = reinterpret_cast<const __half *>(&la);
-            const __half *plb = reinterpret_cast<const __half *>(&lb);
-            const __half *pha = reinterpret_cast<const __half *>(&ha);
-            const __half *phb = reinterpret_cast<const __half *>(&hb);
+            for (int c = 0; c < 4; ++c) {
+                const uint4 la = *reinterpret_cast<const uint4 *>(src + swz128(rr, c));
+                const uint4 lb = *reinterpret_cast<const uint4 *>(src + swz128(rr, c + 4));
+                const __half *pa = reinterpret_cast<const __half *>(&la);
+                const __half *pb = reinterpret_cast<const __half *>(&lb);
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-                v[8 * c + j] = make_float2(add_f16_f32(pla[j], __half2float(pha[j])),
-                                           add_f16_f32(plb[j], __half2float(phb[j])));
+                for (int j = 0; j < 8; ++j) {
+                    const float b = __half2float(pb[j]);
+                    v[8 * c + j] = make_float2(add_f16_f32(pa[j], b), add_f16_f32(pa[j], -b));
+                }
+            }
         }
 
-        // ---- norm: the two halves' sums of squares add up to twice sum x^2
+        // ---- norm: the sums of squares after that stage add up to twice sum x^2
         float2 acc[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) acc[i] = make_float2(0.0f, 0.0f);
@@ -471,8 +467,6 @@ __global__ void __launch_bounds__(enc_warps(BITS) * 32, 1)
 #pragma unroll
             for (int k = 0; k < 32; ++k) v[k] = __fmul2_rn(v[k], inv2);
         }
-
-        // ---- H64 of the half: coordinate bits 0-4 across the array, bit 5 in the pair
         const float2 neg1 = make_float2(-1.0f, -1.0f);
 #pragma unroll
         for (int h = 1; h < 32; h <<= 1) {
@@ -485,8 +479,17 @@ __global__ void __launch_bounds__(enc_warps(BITS) * 32, 1)
                 }
             }
         }
+        // ---- bit 6 across the two threads: y_0 = Z_0 + Z_1, y_1 = Z_0 - Z_1;
+        // afterwards v[k] = (y_h[k], y_h[k + 32]) of this thread's output half
+        {
+            const float2 sgn = hh ? neg1 : make_float2(1.0f, 1.0f);
 #pragma unroll
-        for (int k = 0; k < 32; ++k) v[k] = make_float2(v[k].x + v[k].y, v[k].x - v[k].y);
+            for (int k = 0; k < 32; ++k) {
+                const float2 o = make_float2(__shfl_xor_sync(FULL_MASK, v[k].x, 16),
+                                             __shfl_xor_sync(FULL_MASK, v[k].y, 16));
+                v[k] = __ffma2_rn(v[k], sgn, o);
+            }
+        }
 
         // symmetric modes quantize S itself against thresholds scaled by den
         SymRow sk;
