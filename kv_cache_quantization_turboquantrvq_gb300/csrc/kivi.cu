@@ -135,23 +135,29 @@ __device__ __noinline__ uint32_t code_int64(float x, float mn, float mx)
 // neighbour.  Everything runs on the FMA pipe, two elements per instruction
 // where the operation exists for fp32 pairs.
 template <int BITS>
-__device__ __forceinline__ void code_pair(__half a, __half b, const GroupQ &g, uint32_t &qa,
-                                          uint32_t &qb)
+__device__ __forceinline__ void code_pair2(__half a, __half b, float2 mn, float2 f, float2 rr, uint32_t &qa,
+                                           uint32_t &qb)
 {
     constexpr float C = (float)((1 << BITS) - 1);
-    const float2 A = make_float2(add_f16_f32(a, -g.mn), add_f16_f32(b, -g.mn));
-    const float2 tm = __ffma2_rn(A, make_float2(g.f, g.f), make_float2(MAGIC1, MAGIC1));
+    const float2 A = make_float2(add_f16_f32(a, -mn.x), add_f16_f32(b, -mn.y));
+    const float2 tm = __ffma2_rn(A, f, make_float2(MAGIC1, MAGIC1));
     const float2 r = __fadd2_rn(tm, make_float2(-MAGIC1, -MAGIC1));
     const float2 ca = __fmul2_rn(A, make_float2(C, C));
-    const float2 u = __ffma2_rn(r, make_float2(-g.rr, -g.rr), ca);
-    const float h = 0.5f * g.rr;
-    const float2 zl = __fadd2_rn(u, make_float2(h, h));
-    const float2 zr = __fadd2_rn(u, make_float2(-h, -h));
+    const float2 u = __ffma2_rn(r, make_float2(-rr.x, -rr.y), ca);
+    const float2 h = make_float2(0.5f * rr.x, 0.5f * rr.y);
+    const float2 zl = __fadd2_rn(u, h);
+    const float2 zr = __fadd2_rn(u, make_float2(-h.x, -h.y));
     const float2 st = __fadd2_rn(make_float2(step_half(zl.x), step_half(zl.y)),
                                  make_float2(step_half(zr.x), step_half(zr.y)));
     const float2 qm = __fadd2_rn(tm, st);  // MAGIC + q, ties to even
     qa = __float_as_uint(qm.x);
     qb = __float_as_uint(qm.y);
+}
+
+template <int BITS>
+__device__ __forceinline__ void code_pair(__half a, __half b, const GroupQ &g, uint32_t &qa, uint32_t &qb)
+{
+    code_pair2<BITS>(a, b, make_float2(g.mn, g.mn), make_float2(g.f, g.f), make_float2(g.rr, g.rr), qa, qb);
 }
 
 // fp16(q*s + z) rounded once from the exact value: q*s is exact in fp32, the
@@ -447,8 +453,11 @@ __global__ void __launch_bounds__(VAL_WARPS * 32, 1)
 // channels 2l and 2l + 1, so each token row of the tile is one conflict-free
 // 32-bit load per lane and no cross-thread reduction is needed (the pages'
 // "one thread, one whole group").  For G <= 64 the lane's 2G values move to
-// registers in the min/max pass and the stage is refilled at once (the rare
-// exact path gets its word through a small scratch).  Codes of
+// registers in the min/max pass and the stage is refilled at once.  A word
+// that holds a near-tie is redone inline by the exact FMA test (code_pair2);
+// the rare group whose range fp32 does not hold is finished after the loop
+// from global memory (no call inside the unrolled loop: a call site there
+// costs the whole loop).  Codes of
 // the two channels of a token run as one fp32 pair.  Each word row is stored
 // as 8 bytes per lane (256 contiguous bytes per warp).
 
@@ -464,17 +473,10 @@ __host__ __device__ constexpr int key_stages()
     return G <= 64 ? 1 : 2;
 }
 
-// Exact-path scratch per warp (G <= 64): one word's values, 32 lanes.
-template <int BITS>
-__host__ __device__ constexpr int key_scratch()
-{
-    return (32 / BITS) * 32 * 4;
-}
-
 template <int BITS, int G>
 __host__ __device__ constexpr int key_warp_bytes()
 {
-    return key_stages<G>() * (G * KEY_ROW) + (G <= 64 ? key_scratch<BITS>() : 0);
+    return key_stages<G>() * (G * KEY_ROW);
 }
 
 template <int BITS, int G>
@@ -490,20 +492,25 @@ __host__ __device__ constexpr int key_smem()
     return 1024 + key_warps<BITS, G>() * (key_warp_bytes<BITS, G>() + 16);
 }
 
-// Exact codes of one word of two channels (rare path), read from the staged
-// tile: col points at this lane's channel pair of the word's first token.
-template <int BITS>
-__device__ __noinline__ uint2 keys_word_exact(const uint32_t *col, const GroupQ g0, const GroupQ g1,
-                                              float mx0, float mx1, int nvalid)
+// Words of a tile column whose group range is not held exactly by fp32 and
+// that hold a near-tie (rarely both): all codes of the flagged words again,
+// exactly, from global memory.  xcol: channel 2l of the group's first token;
+// dst: word row 0 of this lane's channel pair.
+template <int BITS, int G>
+__device__ __noinline__ void keys_words_slow(const __half *xcol, uint32_t *dst, uint32_t mask, int ntok,
+                                             const GroupQ g0, const GroupQ g1, float mx0, float mx1)
 {
     constexpr int E = 32 / BITS;
-    uint32_t w0 = 0u, w1 = 0u;
-    for (int j = 0; j < E && j < nvalid; ++j) {
-        const __half2 h = u2h2(col[j * 32]);
-        w0 |= code_exact<BITS>(__low2half(h), g0, mx0) << (j * BITS);
-        w1 |= code_exact<BITS>(__high2half(h), g1, mx1) << (j * BITS);
+    for (int k = 0; k < G * BITS / 32; ++k) {
+        if (!((mask >> k) & 1u)) continue;
+        uint32_t w0 = 0u, w1 = 0u;
+        for (int j = 0; j < E && k * E + j < ntok; ++j) {
+            const __half2 h = *reinterpret_cast<const __half2 *>(xcol + (size_t)(k * E + j) * D);
+            w0 |= code_exact<BITS>(__low2half(h), g0, mx0) << (j * BITS);
+            w1 |= code_exact<BITS>(__high2half(h), g1, mx1) << (j * BITS);
+        }
+        *reinterpret_cast<uint2 *>(dst + (size_t)k * D) = make_uint2(w0, w1);
     }
-    return make_uint2(w0, w1);
 }
 
 template <int BITS, int G>
@@ -522,7 +529,6 @@ __global__ void __launch_bounds__(key_warps<BITS, G>() * 32, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     unsigned char *wbuf = smem + warp * WBYTES;
-    uint32_t *xs = reinterpret_cast<uint32_t *>(wbuf + KEY_STAGES * TILE);  // exact-path scratch
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + KEY_WARPS * WBYTES) + warp * KEY_STAGES;
     if (lane == 0) {
 #pragma unroll
@@ -622,6 +628,9 @@ __global__ void __launch_bounds__(key_warps<BITS, G>() * 32, 1)
         uint32_t *dst = p.packed + gd * WG * D + 64 * chh + 2 * lane;
 
         // pass 2: word row k holds tokens k*E .. k*E + E - 1 at shifts j*BITS
+        const bool allfast = g0.fast && g1.fast;
+        const float2 mn2 = make_float2(g0.mn, g1.mn), rr2 = make_float2(g0.rr, g1.rr);
+        uint32_t slowmask = 0u;
 #pragma unroll
         for (int k = 0; k < WG; ++k) {
             uint32_t a0 = 0u, b0 = 0u, a1 = 0u, b1 = 0u, okw = 0xffffffffu;
@@ -645,23 +654,36 @@ __global__ void __launch_bounds__(key_warps<BITS, G>() * 32, 1)
                     b1 = __funnelshift_r(b1, q1, BITS);
                 }
             }
+            if (!(okw >> 31)) {
+                if (allfast) {
+                    // a near-tie in the word: exact codes for all of it
+                    a0 = b0 = a1 = b1 = 0u;
+#pragma unroll
+                    for (int j = 0; j < E; ++j) {
+                        const int i = k * E + j;
+                        uint32_t u;
+                        if constexpr (PRELOAD) {
+                            u = v[i];
+                        } else {
+                            u = col[(i < ntok ? i : ntok - 1) * 32];
+                        }
+                        uint32_t q0, q1;
+                        code_pair2<BITS>(__low2half(u2h2(u)), __high2half(u2h2(u)), mn2, f2, rr2, q0, q1);
+                        if (j < E / 2) {
+                            a0 = __funnelshift_r(a0, q0, BITS);
+                            a1 = __funnelshift_r(a1, q1, BITS);
+                        } else {
+                            b0 = __funnelshift_r(b0, q0, BITS);
+                            b1 = __funnelshift_r(b1, q1, BITS);
+                        }
+                    }
+                } else {
+                    slowmask |= 1u << k;
+                }
+            }
             uint32_t w0 = (b0 & 0xffff0000u) | (a0 >> 16);
             uint32_t w1 = (b1 & 0xffff0000u) | (a1 >> 16);
             const int nvalid = ntok - k * E;  // tokens of this word that exist
-            if (!(okw >> 31)) {
-                const uint32_t *wc;
-                if constexpr (PRELOAD) {
-                    // the stage is already refilling: pass the word through scratch
-#pragma unroll
-                    for (int j = 0; j < E; ++j) xs[j * 32 + lane] = v[k * E + j];
-                    wc = xs + lane;
-                } else {
-                    wc = col + k * E * 32;
-                }
-                const uint2 ww = keys_word_exact<BITS>(wc, g0, g1, mx0, mx1, nvalid);
-                w0 = ww.x;
-                w1 = ww.y;
-            }
             if (nvalid < E) {  // slots past the last token hold 0
                 const uint32_t m = nvalid <= 0 ? 0u : (0xffffffffu >> (32 - nvalid * BITS));
                 w0 &= m;
@@ -669,6 +691,10 @@ __global__ void __launch_bounds__(key_warps<BITS, G>() * 32, 1)
             }
             if (okoff) *reinterpret_cast<uint2 *>(dst + (size_t)k * D) = make_uint2(w0, w1);
         }
+        if (slowmask != 0u && okoff)
+            keys_words_slow<BITS, G>(static_cast<const __half *>(p.x) + ((size_t)bh * p.S + (size_t)g * G) * D +
+                                         64 * chh + 2 * lane,
+                                     dst, slowmask, ntok, g0, g1, mx0, mx1);
         if constexpr (!PRELOAD) {
             // the tile is consumed: recycle the stage
             __syncwarp();
