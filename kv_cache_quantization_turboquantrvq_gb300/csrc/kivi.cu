@@ -262,7 +262,7 @@ __device__ __forceinline__ bool kivi_off(const KiviQuantParams &p, int b, int &o
     off = 0;
     if (p.dst_off == nullptr) return true;
     off = __ldg(p.dst_off + b);
-    if (off < 0 || off > p.S_dst - p.S_q || (off % p.group) != 0) {
+    if (off < 0 || off > p.S_dst - p.S_q || (off & (p.group - 1)) != 0) {
         atomicOr(&g_kivi_err, (unsigned)VQ_DEVERR_BAD_OFFSET);
         return false;
     }
@@ -321,7 +321,7 @@ __global__ void __launch_bounds__(VAL_WARPS * 32, 1)
 
     auto issue = [&](int blk, int s) {
         if (lane == 0) {
-            const int bh = blk / nsb, sb = blk - bh * nsb;
+            const int bh = fdiv(p.divBlk, blk), sb = blk - bh * nsb;
             mbar_arrive_expect_tx(&bars[s], (uint32_t)VSTAGE_BYTES);
             unsigned char *dst = wbuf + s * VSTAGE_BYTES;
             tma_load_3d(dst, &p.tmap, 0, sb * VROWS, bh, &bars[s], pol);
@@ -353,13 +353,13 @@ __global__ void __launch_bounds__(VAL_WARPS * 32, 1)
 #pragma unroll
         for (int i = 0; i < 8; ++i) c[i] = *reinterpret_cast<const uint4 *>(src + swz128(rr, i));
 
-        const int bh = blk / nsb;
+        const int bh = fdiv(p.divBlk, blk);
         const int s_ = (blk - bh * nsb) * VROWS + rr;
         size_t dr = 0;
         bool okrow = false;
         if (s_ < p.S_q) {
             int off;
-            okrow = kivi_off(p, bh / p.H, off);
+            okrow = kivi_off(p, fdiv(p.divH, bh), off);
             dr = (size_t)bh * p.S_dst + off + s_;
         }
         uint32_t words[WL];
@@ -543,13 +543,14 @@ __global__ void __launch_bounds__(key_warps<BITS, G>() * 32, 1)
     const int tw = gridDim.x * KEY_WARPS;
 
     auto ntok_of = [&](int tile) {
-        const int g = (tile >> 1) % NG;
+        const int gi = tile >> 1;
+        const int g = gi - fdiv(p.divBlk, gi) * NG;
         return min(G, p.S_q - g * G);
     };
     auto issue = [&](int tile, int s) {
         if (lane == 0) {
             const int gi = tile >> 1, chh = tile & 1;
-            const int bh = gi / NG, g = gi - bh * NG;
+            const int bh = fdiv(p.divBlk, gi), g = gi - bh * NG;
             mbar_arrive_expect_tx(&bars[s], (uint32_t)TILE);
             tma_load_3d(wbuf + s * TILE, &p.tmap, 64 * chh, g * G, bh, &bars[s], pol);
         }
@@ -576,7 +577,7 @@ __global__ void __launch_bounds__(key_warps<BITS, G>() * 32, 1)
         const uint32_t *col = reinterpret_cast<const uint32_t *>(wbuf + s * TILE) + lane;
         const int ntok = ntok_of(tile);
         const int gi = tile >> 1, chh = tile & 1;
-        const int bh = gi / NG, g = gi - bh * NG;
+        const int bh = fdiv(p.divBlk, gi), g = gi - bh * NG;
 
         // pass 1: min/max down the tokens (exact fp16); a ragged last group
         // is padded with its edge token, which leaves min/max unchanged
@@ -623,7 +624,7 @@ __global__ void __launch_bounds__(key_warps<BITS, G>() * 32, 1)
         const GroupQ g1 = group_setup<BITS>(__high2float(lo), mx1);
         const float2 f2 = make_float2(g0.f, g1.f), nf2 = make_float2(-g0.f, -g1.f);
         int off;
-        const bool okoff = kivi_off(p, bh / p.H, off);  // uniform across the warp
+        const bool okoff = kivi_off(p, fdiv(p.divH, bh), off);  // uniform across the warp
         const size_t gd = (size_t)bh * p.NG_dst + off / G + g;
         uint32_t *dst = p.packed + gd * WG * D + 64 * chh + 2 * lane;
 
@@ -925,6 +926,8 @@ cudaError_t launch_q(const KiviQuantParams &p0, bool per_channel, cudaStream_t s
 {
     const int sms = sm_count();
     KiviQuantParams p = p0;
+    p.divH = make_fastdiv((uint32_t)p.H);
+    p.divBlk = make_fastdiv((uint32_t)(per_channel ? (p.S_q + G - 1) / G : (p.S_q + VROWS - 1) / VROWS));
     {
         const uint64_t dims[3] = {(uint64_t)D, (uint64_t)p.S, (uint64_t)p.B * p.H};
         const uint64_t strides[2] = {(uint64_t)D * 2, (uint64_t)p.S * D * 2};

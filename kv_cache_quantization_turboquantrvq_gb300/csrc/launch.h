@@ -22,6 +22,34 @@ struct GridTable {
     int code[32];
 };
 
+// Division by a divisor d fixed for a launch, for numerators 0 <= n < 2^31:
+// q = umulhi(n, m) >> s with l = ceil(log2 d), m = ceil(2^(31 + l) / d),
+// s = l - 1 (Granlund and Montgomery, "Division by invariant integers using
+// multiplication", 1994, Theorem 4.2 with N = 31); d = 1 is flagged and
+// passes n through.
+struct FastDiv {
+    uint32_t m = 1u, s = 0u, one = 1u;
+};
+
+inline FastDiv make_fastdiv(uint32_t d)
+{
+    FastDiv f;
+    if (d <= 1u) return f;
+    uint32_t l = 0;
+    while ((1ull << l) < d) ++l;
+    f.m = (uint32_t)(((1ull << (31 + l)) + d - 1) / d);
+    f.s = l - 1;
+    f.one = 0u;
+    return f;
+}
+
+#ifdef __CUDACC__
+__device__ __forceinline__ int fdiv(const FastDiv &f, int n)
+{
+    return f.one ? n : (int)(__umulhi((uint32_t)n, f.m) >> f.s);
+}
+#endif
+
 struct RvqEncodeParams {
     CUtensorMap tmap;    // x as [N rows, 128] fp16, 64 x 32 boxes, 128-byte swizzle (set by the launcher)
     const void *x;       // fp16 [N, 128]
@@ -29,6 +57,7 @@ struct RvqEncodeParams {
     float *norms;        // [B, H, S_dst]
     const int32_t *dst_off;
     int N, S, H, S_dst;
+    FastDiv divS, divH;  // by S and by H (set by the launcher)
     float guard;         // |y - boundary| below this sends the row to the exact path
     GridTable t1, t2;
     float c1[16], c2[16], b1[16], b2[16];
@@ -49,6 +78,7 @@ struct KiviQuantParams {
     void *scale, *zero;  // fp16
     const int32_t *dst_off;
     int B, H, S, S_q, S_dst, group, NG_dst;
+    FastDiv divH, divBlk;  // by H, and by blocks (values) or groups (keys) per (b, h) slice (set by the launcher)
 };
 
 struct KiviDequantParams {

@@ -194,11 +194,11 @@ enum { MODE_PLAIN = 0, MODE_GRID = 1, MODE_SYM = 2 };
 // Destination row of source row `row`; false if its batch offset is invalid.
 __device__ __forceinline__ bool rvq_dst_row(const RvqEncodeParams &p, int row, size_t &drow)
 {
-    const int bh = row / p.S;
+    const int bh = fdiv(p.divS, row);
     const int s = row - bh * p.S;
     int off = 0;
     if (p.dst_off != nullptr) {
-        off = __ldg(p.dst_off + bh / p.H);
+        off = __ldg(p.dst_off + fdiv(p.divH, bh));
         if (off < 0 || off > p.S_dst - p.S) {
             atomicOr(&g_rvq_err, (unsigned)VQ_DEVERR_BAD_OFFSET);
             return false;
@@ -787,6 +787,8 @@ template <int BITS, int MODE>
 cudaError_t launch_enc(const RvqEncodeParams &p0, cudaStream_t stream)
 {
     RvqEncodeParams p = p0;
+    p.divS = make_fastdiv((uint32_t)p.S);
+    p.divH = make_fastdiv((uint32_t)p.H);
     {
         const uint64_t dims[2] = {(uint64_t)D, (uint64_t)p.N};
         const uint64_t strides[1] = {(uint64_t)D * 2};
