@@ -11,23 +11,23 @@
 // The pages fuse quantize->pack after a separate rotation dispatch; here the
 // norm, rotation, both stages and both packs are one pass over HBM.
 //
-// Encode design (one row per thread, 32-row blocks per warp):
-//  * each warp owns a private 2-stage ring of 32-row blocks in shared memory,
-//    each block two TMA tensor boxes (32 rows x 64 channels) that complete on
-//    an mbarrier and land with the 128-byte swizzle (chunk c of row r at
-//    chunk c ^ (r & 7)), so the 32 row owners read 16-byte chunks without
+// Encode design (two threads per row, 16-row blocks per warp, 16 warps/SM):
+//  * each warp owns a private 2-stage ring of 16-row blocks in shared memory,
+//    each block two TMA tensor boxes (16 rows x 64 channels, one per input
+//    half) that complete on an mbarrier and land with the 128-byte swizzle
+//    (chunk c of row r at chunk c ^ (r & 7)), so 16-byte row reads are free of
 //    bank conflicts;
-//  * a thread holds its row as 64 float2 (x[k], x[k+64]) and runs six
-//    butterfly stages with the fp32x2 add/fma instructions and the last
-//    (bit 6) stage in scalar fp32 - no shuffles;
-//  * the rotated row goes to a per-thread shared-memory scratch as coordinate
-//    pairs (k, k + 64), a slice at a time, and is quantized by a rolled loop
-//    that builds two output words per step (one from each half of the row);
-//    this keeps the program small enough for the instruction cache (a fully
-//    unrolled 128-coordinate quantizer stalls on instruction fetch);
-//  * the boundary count of each stage is two table reads by warp shuffle
-//    (GridTable in launch.h) plus one compare;
-//  * words are staged in shared memory and written out coalesced;
+//  * lane l takes row l & 15 and input half h = l >> 4: with
+//    H = [[H64, H64], [H64, -H64]] it computes Z_h = H64 x_h on its own 64
+//    values (the first butterfly fused with the fp16 -> fp32 conversion,
+//    then five fp32x2 stages), swaps Z_h with its partner (lane l ^ 16) by
+//    shuffles and keeps Z_0 + Z_1 or Z_0 - Z_1: its 64 output coordinates;
+//    the norm comes from the partners' sums of squares (Parseval);
+//  * the quantizer is unrolled over those 64 coordinates, in registers: the
+//    symmetric 1/2-bit codebooks take sign-bit arithmetic (no tables), other
+//    codebooks the shuffle-table count (GridTable in launch.h) or a plain
+//    count; each thread stores its half of the row's words (the 16 rows x 2
+//    halves of a block are contiguous in global memory);
 //  * every code is kept unless its pre-quantization value lies within a guard
 //    band of a boundary; such rows are redone by the whole warp in exact /
 //    double-float arithmetic (rvq_fixup_row), so the packed words equal those
@@ -48,30 +48,18 @@ constexpr int ROW_BYTES = D * 2;
 constexpr int ROW_STRIDE = ROW_BYTES + 16;
 
 // Encoder shared memory: the input rings of all warps (1024-byte aligned
-// 4 KB blocks of ER = 16 rows), then per warp the pair scratch (enc_pairs
-// coordinate pairs (k, k + 32) of a half row x 32 lanes, 8 bytes each), two
-// word-staging arrays with one pad word per row, and the norms of rows redone
-// by the exact path.  As many warps as fit (at most 16).
+// 4 KB blocks of ER = 16 rows).  Everything else lives in registers: the
+// quantizer is unrolled over a thread's half row (64 coordinates), which is
+// small enough for the instruction cache, and the words go straight to global
+// memory.
 constexpr int ER = 16;
 constexpr int ENC_STAGES = 2;
 constexpr int ENC_BLOCK = ER * ROW_BYTES;  // two swizzled 2 KB boxes
 constexpr int SMEM_MAX = 227 * 1024;
-__host__ __device__ constexpr int enc_words(int bits) { return D * bits / 32; }
-__host__ __device__ constexpr int enc_pairs(int bits) { return 32 / bits > 16 ? 32 / bits : 16; }
-__host__ __device__ constexpr int enc_scratch_bytes(int bits) { return enc_pairs(bits) * 32 * 8; }
-__host__ __device__ constexpr int enc_warp_bytes(int bits)
-{
-    return enc_scratch_bytes(bits) + 2 * ER * (enc_words(bits) + 1) * 4 + ER * 4;
-}
-__host__ __device__ constexpr int enc_warps(int bits)
-{
-    return (SMEM_MAX - 1024) / (ENC_STAGES * ENC_BLOCK + enc_warp_bytes(bits) + ENC_STAGES * 8) > 16
-               ? 16
-               : (SMEM_MAX - 1024) / (ENC_STAGES * ENC_BLOCK + enc_warp_bytes(bits) + ENC_STAGES * 8);
-}
+__host__ __device__ constexpr int enc_warps(int) { return 16; }
 __host__ __device__ constexpr int enc_smem(int bits)
 {
-    return 1024 + enc_warps(bits) * (ENC_STAGES * ENC_BLOCK + enc_warp_bytes(bits) + ENC_STAGES * 8);
+    return 1024 + enc_warps(bits) * ENC_STAGES * (ENC_BLOCK + 8);
 }
 
 // sqrt(128) = 8 sqrt(2) as a double-float (nearest fp32 + fp32 remainder).
@@ -235,13 +223,12 @@ __device__ __forceinline__ void wht_lane_exact(float (&a)[4], int lane)
 //    n = sqrt(Q) and 1/(n sqrt(D)) in double-float.
 //  * y = S / (n sqrt(D)) in double-float (about 2^-44 relative), and each
 //    boundary count is taken on the double-float value.
-// The row's words go to the warp's staging rows (o1, o2, stride W + 1) and
-// its norm to nrm[r].
+// The row's raw values are read from the staged block (row r of it, global
+// row `row`); its words and norm go straight to global memory.
 template <int BITS, bool GRID>
 __device__ __noinline__ void rvq_fixup_row(const RvqEncodeParams &p, const unsigned char *sblk,
-                                           int r, int lane, float tb1, int tc1, float tb2,
-                                           int tc2, float tcen, uint32_t *o1, uint32_t *o2,
-                                           float *nrm)
+                                           int r, int row, int lane, float tb1, int tc1, float tb2,
+                                           int tc2, float tcen)
 {
     constexpr int E = 32 / BITS;
     constexpr int W = D * BITS / 32;
@@ -343,11 +330,13 @@ __device__ __noinline__ void rvq_fixup_row(const RvqEncodeParams &p, const unsig
         part1 |= __shfl_xor_sync(FULL_MASK, part1, o);
         part2 |= __shfl_xor_sync(FULL_MASK, part2, o);
     }
+    size_t drow = 0;
+    if (!rvq_dst_row(p, row, drow)) return;
     if (sub == 0 && lane / LPW < W) {
-        o1[r * (W + 1) + lane / LPW] = part1;
-        o2[r * (W + 1) + lane / LPW] = part2;
+        p.p1[drow * W + lane / LPW] = part1;
+        p.p2[drow * W + lane / LPW] = part2;
     }
-    if (lane == 0) nrm[r] = __fadd_rn(nh, nl);
+    if (lane == 0) p.norms[drow] = __fadd_rn(nh, nl);
 }
 
 template <int BITS, int MODE>
@@ -360,20 +349,13 @@ __global__ void __launch_bounds__(enc_warps(BITS) * 32, 1)
     constexpr int W = D * BITS / 32;
     constexpr int WL = W / 2;  // words of a half row
     constexpr int WARPS = enc_warps(BITS);
-    constexpr int WB = enc_warp_bytes(BITS);
     extern __shared__ __align__(128) unsigned char smem_raw[];
     unsigned char *smem = smem_1k(smem_raw);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int rr = lane & 15, hh = lane >> 4;
     unsigned char *ring = smem + warp * (ENC_STAGES * ENC_BLOCK);
-    unsigned char *wbuf = smem + WARPS * (ENC_STAGES * ENC_BLOCK) + warp * WB;
-    float2 *yp = reinterpret_cast<float2 *>(wbuf);
-    uint32_t *o1 = reinterpret_cast<uint32_t *>(wbuf + enc_scratch_bytes(BITS));
-    uint32_t *o2 = o1 + ER * (W + 1);
-    float *nrm = reinterpret_cast<float *>(o2 + ER * (W + 1));
-    uint64_t *bars =
-        reinterpret_cast<uint64_t *>(smem + WARPS * (ENC_STAGES * ENC_BLOCK + WB)) + warp * ENC_STAGES;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + WARPS * ENC_STAGES * ENC_BLOCK) + warp * ENC_STAGES;
 
     if (lane == 0) {
 #pragma unroll
@@ -500,61 +482,46 @@ __global__ void __launch_bounds__(enc_warps(BITS) * 32, 1)
         sk.c1 = p.c1[(1 << BITS) - 1] * den;
         const float guard = MODE == MODE_SYM ? p.guard * den : p.guard;
 
-        // ---- two-stage boundary count and LSB-first packing.  Slice `ps` of PP
-        // coordinate pairs (k, k + 32), k in [ps*PP, ps*PP + PP), goes to the
-        // scratch yp[i * 32 + lane]; each step of the word loop reads E pairs
-        // and produces word kx = k/E of the half from the first coordinates
-        // and word kx + WL/2 from the second ones.
-        constexpr int PP = enc_pairs(BITS) < 32 ? enc_pairs(BITS) : 32;
+        // ---- two-stage boundary count and LSB-first packing, unrolled over the
+        // half row: word kx of the half from the first coordinates of pairs
+        // [kx*E, kx*E + E), word kx + WL/2 from the second ones.
         float mx = __int_as_float(0x7f800000), my = mx;
-        uint32_t *w1row = o1 + rr * (W + 1) + hh * WL;
-        uint32_t *w2row = o2 + rr * (W + 1) + hh * WL;
-#pragma unroll 1
-        for (int ps = 0; ps < 32 / PP; ++ps) {
+        uint32_t wa1[WL], wa2[WL];
 #pragma unroll
-            for (int q4 = 0; q4 < 32 / PP; ++q4) {
-                if (ps == q4) {
+        for (int kx = 0; kx < WL / 2; ++kx) {
+            uint32_t a1x = 0u, a2x = 0u, a1y = 0u, a2y = 0u;
+            if constexpr (MODE == MODE_SYM) {
 #pragma unroll
-                    for (int i = 0; i < PP; ++i) yp[i * 32 + lane] = v[q4 * PP + i];
-                }
-            }
-#pragma unroll 1
-            for (int w = 0; w < PP / E; ++w) {
-                uint32_t a1x = 0u, a2x = 0u, a1y = 0u, a2y = 0u;
-                if constexpr (MODE == MODE_SYM) {
-#pragma unroll
-                    for (int i = E - 1; i >= 0; --i) {
-                        const float2 y2 = yp[(w * E + i) * 32 + lane];
-                        if constexpr (BITS == 2) {
-                            sym2_code2(y2, sk, a1x, a2x, a1y, a2y, mx, my);
-                        } else {
-                            sym1_code(y2.x, sk, a1x, a2x, mx);
-                            sym1_code(y2.y, sk, a1y, a2y, my);
-                        }
-                    }
-                    a1x = ~a1x; a2x = ~a2x; a1y = ~a1y; a2y = ~a2y;
-                } else {
-#pragma unroll
-                    for (int i = 0; i < E; ++i) {
-                        const float2 y2 = yp[(w * E + i) * 32 + lane];
-                        const int cx1 = stage_code<BITS, GRID>(y2.x, tb1, tc1, p.t1, p.b1, mx);
-                        const int cy1 = stage_code<BITS, GRID>(y2.y, tb1, tc1, p.t1, p.b1, my);
-                        const float rx = y2.x - __shfl_sync(FULL_MASK, tcen, cx1);
-                        const float ry = y2.y - __shfl_sync(FULL_MASK, tcen, cy1);
-                        const int cx2 = stage_code<BITS, GRID>(rx, tb2, tc2, p.t2, p.b2, mx);
-                        const int cy2 = stage_code<BITS, GRID>(ry, tb2, tc2, p.t2, p.b2, my);
-                        a1x = __funnelshift_r(a1x, (uint32_t)cx1, BITS);
-                        a2x = __funnelshift_r(a2x, (uint32_t)cx2, BITS);
-                        a1y = __funnelshift_r(a1y, (uint32_t)cy1, BITS);
-                        a2y = __funnelshift_r(a2y, (uint32_t)cy2, BITS);
+                for (int i = E - 1; i >= 0; --i) {
+                    const float2 y2 = v[kx * E + i];
+                    if constexpr (BITS == 2) {
+                        sym2_code2(y2, sk, a1x, a2x, a1y, a2y, mx, my);
+                    } else {
+                        sym1_code(y2.x, sk, a1x, a2x, mx);
+                        sym1_code(y2.y, sk, a1y, a2y, my);
                     }
                 }
-                const int kx = ps * (PP / E) + w;
-                w1row[kx] = a1x;
-                w2row[kx] = a2x;
-                w1row[WL / 2 + kx] = a1y;
-                w2row[WL / 2 + kx] = a2y;
+                a1x = ~a1x; a2x = ~a2x; a1y = ~a1y; a2y = ~a2y;
+            } else {
+#pragma unroll
+                for (int i = 0; i < E; ++i) {
+                    const float2 y2 = v[kx * E + i];
+                    const int cx1 = stage_code<BITS, GRID>(y2.x, tb1, tc1, p.t1, p.b1, mx);
+                    const int cy1 = stage_code<BITS, GRID>(y2.y, tb1, tc1, p.t1, p.b1, my);
+                    const float rx = y2.x - __shfl_sync(FULL_MASK, tcen, cx1);
+                    const float ry = y2.y - __shfl_sync(FULL_MASK, tcen, cy1);
+                    const int cx2 = stage_code<BITS, GRID>(rx, tb2, tc2, p.t2, p.b2, mx);
+                    const int cy2 = stage_code<BITS, GRID>(ry, tb2, tc2, p.t2, p.b2, my);
+                    a1x = __funnelshift_r(a1x, (uint32_t)cx1, BITS);
+                    a2x = __funnelshift_r(a2x, (uint32_t)cx2, BITS);
+                    a1y = __funnelshift_r(a1y, (uint32_t)cy1, BITS);
+                    a2y = __funnelshift_r(a2y, (uint32_t)cy2, BITS);
+                }
             }
+            wa1[kx] = a1x;
+            wa2[kx] = a2x;
+            wa1[WL / 2 + kx] = a1y;
+            wa2[WL / 2 + kx] = a2y;
         }
         const float m = fminf(mx, my);
         // a zero row has no direction: always take the exact path for it
@@ -563,13 +530,33 @@ __global__ void __launch_bounds__(enc_warps(BITS) * 32, 1)
         const int pflag = __shfl_xor_sync(FULL_MASK, hflag ? 1 : 0, 16);
         const bool flag = hflag || pflag != 0;
 
+        // ---- the fast words of this half, straight to global memory (the 16
+        // rows x 2 halves of a block are contiguous there); rows with a value
+        // inside the guard band are written by the exact recompute instead
+        size_t drow = 0;
+        const bool okrow = valid && !flag && rvq_dst_row(p, row, drow);
+        if (okrow) {
+            uint32_t *d1 = p.p1 + drow * W + hh * WL;
+            uint32_t *d2 = p.p2 + drow * W + hh * WL;
+            if constexpr (WL == 2) {
+                *reinterpret_cast<uint2 *>(d1) = make_uint2(wa1[0], wa1[1]);
+                *reinterpret_cast<uint2 *>(d2) = make_uint2(wa2[0], wa2[1]);
+            } else {
+#pragma unroll
+                for (int i = 0; i < WL / 4; ++i) {
+                    reinterpret_cast<uint4 *>(d1)[i] = make_uint4(wa1[4 * i], wa1[4 * i + 1], wa1[4 * i + 2], wa1[4 * i + 3]);
+                    reinterpret_cast<uint4 *>(d2)[i] = make_uint4(wa2[4 * i], wa2[4 * i + 1], wa2[4 * i + 2], wa2[4 * i + 3]);
+                }
+            }
+            if (hh == 0) p.norms[drow] = n;
+        }
+
         // ---- rows with a value inside the guard band: exact recompute by the warp
-        __syncwarp();
         unsigned fl = __ballot_sync(FULL_MASK, flag) & 0xffffu;
         while (fl) {
             const int r = __ffs(fl) - 1;
             fl &= fl - 1;
-            rvq_fixup_row<BITS, GRID>(p, sbuf, r, lane, tb1, tc1, tb2, tc2, tcen, o1, o2, nrm);
+            rvq_fixup_row<BITS, GRID>(p, sbuf, r, blk * ER + r, lane, tb1, tc1, tb2, tc2, tcen);
         }
         __syncwarp();
 
@@ -580,23 +567,6 @@ __global__ void __launch_bounds__(enc_warps(BITS) * 32, 1)
             if (nb < nblk) issue(nb, s);
         }
 
-        // ---- coalesced write-out: word idx = i*32 + lane is word idx % W of row idx / W
-        size_t drow = 0;
-        const bool okrow = valid && rvq_dst_row(p, row, drow);
-        const int drow32 = (int)drow;
-#pragma unroll
-        for (int i = 0; i < ER * W / 32; ++i) {
-            const int idx = i * 32 + lane;
-            const int r = idx / W, w = idx % W;
-            const int dr = __shfl_sync(FULL_MASK, drow32, r);
-            const bool okr = __shfl_sync(FULL_MASK, okrow ? 1 : 0, r) != 0;
-            if (okr) {
-                p.p1[(size_t)dr * W + w] = o1[r * (W + 1) + w];
-                p.p2[(size_t)dr * W + w] = o2[r * (W + 1) + w];
-            }
-        }
-        if (okrow && hh == 0) p.norms[drow] = flag ? nrm[rr] : n;
-        __syncwarp();
     }
 }
 
