@@ -48,19 +48,28 @@ constexpr int ROW_BYTES = D * 2;
 constexpr int ROW_STRIDE = ROW_BYTES + 16;
 
 // Encoder shared memory: the input rings of all warps (1024-byte aligned
-// 4 KB blocks of ER = 16 rows).  Everything else lives in registers: the
-// quantizer is unrolled over a thread's half row (64 coordinates), which is
-// small enough for the instruction cache, and the words go straight to global
-// memory.
+// 4 KB blocks of ER = 16 rows), then, for the table-driven quantizers only,
+// per warp a slice scratch (enc_pairs coordinate pairs x 32 lanes) and a
+// per-lane word staging row (stride WL + 1 words per stream).  The symmetric
+// 1/2-bit quantizer is unrolled over a thread's 64 coordinates in registers
+// (small enough for the instruction cache); the 16-level table quantizer is
+// not, so it runs a rolled loop over slices of the half row.
 constexpr int ER = 16;
 constexpr int ENC_STAGES = 2;
 constexpr int ENC_BLOCK = ER * ROW_BYTES;  // two swizzled 2 KB boxes
 constexpr int SMEM_MAX = 227 * 1024;
-__host__ __device__ constexpr int enc_warps(int) { return 16; }
-__host__ __device__ constexpr int enc_smem(int bits)
+enum { MODE_PLAIN = 0, MODE_GRID = 1, MODE_SYM = 2 };
+__host__ __device__ constexpr int enc_pairs(int bits) { return 32 / bits > 8 ? 32 / bits : 8; }
+__host__ __device__ constexpr int enc_warp_bytes(int bits, int mode)
 {
-    return 1024 + enc_warps(bits) * ENC_STAGES * (ENC_BLOCK + 8);
+    return ENC_STAGES * (ENC_BLOCK + 8) +
+           (mode == MODE_SYM ? 0 : enc_pairs(bits) * 32 * 8 + 2 * 32 * (D * bits / 64 + 1) * 4);
 }
+__host__ __device__ constexpr int enc_warps(int bits, int mode)
+{
+    return (SMEM_MAX - 1024) / enc_warp_bytes(bits, mode) > 16 ? 16 : (SMEM_MAX - 1024) / enc_warp_bytes(bits, mode);
+}
+__host__ __device__ constexpr int enc_smem(int bits, int mode) { return 1024 + enc_warps(bits, mode) * enc_warp_bytes(bits, mode); }
 
 // sqrt(128) = 8 sqrt(2) as a double-float (nearest fp32 + fp32 remainder).
 constexpr float SQRT_D_HI = 11.313708305358887f;
@@ -176,8 +185,6 @@ __device__ __forceinline__ void sym1_code(float y, const SymRow &k, uint32_t &a1
     a1 = __funnelshift_l(__float_as_uint(y), a1, 1);
     a2 = __funnelshift_l(__float_as_uint(r), a2, 1);
 }
-
-enum { MODE_PLAIN = 0, MODE_GRID = 1, MODE_SYM = 2 };
 
 // Destination row of source row `row`; false if its batch offset is invalid.
 __device__ __forceinline__ bool rvq_dst_row(const RvqEncodeParams &p, int row, size_t &drow)
@@ -340,7 +347,7 @@ __device__ __noinline__ void rvq_fixup_row(const RvqEncodeParams &p, const unsig
 }
 
 template <int BITS, int MODE>
-__global__ void __launch_bounds__(enc_warps(BITS) * 32, 1)
+__global__ void __launch_bounds__(enc_warps(BITS, MODE) * 32, 1)
     rvq_encode_kernel(const __grid_constant__ RvqEncodeParams p)
 {
     constexpr bool GRID = MODE == MODE_GRID;
@@ -348,14 +355,20 @@ __global__ void __launch_bounds__(enc_warps(BITS) * 32, 1)
     constexpr int E = 32 / BITS;
     constexpr int W = D * BITS / 32;
     constexpr int WL = W / 2;  // words of a half row
-    constexpr int WARPS = enc_warps(BITS);
+    constexpr int WARPS = enc_warps(BITS, MODE);
+    constexpr bool ROLLED = MODE != MODE_SYM;
+    constexpr int PP = enc_pairs(BITS);
     extern __shared__ __align__(128) unsigned char smem_raw[];
     unsigned char *smem = smem_1k(smem_raw);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int rr = lane & 15, hh = lane >> 4;
     unsigned char *ring = smem + warp * (ENC_STAGES * ENC_BLOCK);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + WARPS * ENC_STAGES * ENC_BLOCK) + warp * ENC_STAGES;
+    unsigned char *wextra = smem + WARPS * ENC_STAGES * ENC_BLOCK + warp * (enc_warp_bytes(BITS, MODE) - ENC_STAGES * (ENC_BLOCK + 8));
+    float2 *yp = reinterpret_cast<float2 *>(wextra);                                   // ROLLED only
+    uint32_t *ws = reinterpret_cast<uint32_t *>(wextra + PP * 32 * 8) + lane * 2 * (WL + 1);  // ROLLED only
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + WARPS * (enc_warp_bytes(BITS, MODE) - ENC_STAGES * 8)) +
+                     warp * ENC_STAGES;
 
     if (lane == 0) {
 #pragma unroll
@@ -482,15 +495,16 @@ __global__ void __launch_bounds__(enc_warps(BITS) * 32, 1)
         sk.c1 = p.c1[(1 << BITS) - 1] * den;
         const float guard = MODE == MODE_SYM ? p.guard * den : p.guard;
 
-        // ---- two-stage boundary count and LSB-first packing, unrolled over the
-        // half row: word kx of the half from the first coordinates of pairs
-        // [kx*E, kx*E + E), word kx + WL/2 from the second ones.
+        // ---- two-stage boundary count and LSB-first packing: word kx of the
+        // half from the first coordinates of pairs [kx*E, kx*E + E), word
+        // kx + WL/2 from the second ones.
         float mx = __int_as_float(0x7f800000), my = mx;
         uint32_t wa1[WL], wa2[WL];
+        if constexpr (!ROLLED) {
+            // symmetric 1/2-bit books: unrolled, in registers
 #pragma unroll
-        for (int kx = 0; kx < WL / 2; ++kx) {
-            uint32_t a1x = 0u, a2x = 0u, a1y = 0u, a2y = 0u;
-            if constexpr (MODE == MODE_SYM) {
+            for (int kx = 0; kx < WL / 2; ++kx) {
+                uint32_t a1x = 0u, a2x = 0u, a1y = 0u, a2y = 0u;
 #pragma unroll
                 for (int i = E - 1; i >= 0; --i) {
                     const float2 y2 = v[kx * E + i];
@@ -501,27 +515,52 @@ __global__ void __launch_bounds__(enc_warps(BITS) * 32, 1)
                         sym1_code(y2.y, sk, a1y, a2y, my);
                     }
                 }
-                a1x = ~a1x; a2x = ~a2x; a1y = ~a1y; a2y = ~a2y;
-            } else {
+                wa1[kx] = ~a1x;
+                wa2[kx] = ~a2x;
+                wa1[WL / 2 + kx] = ~a1y;
+                wa2[WL / 2 + kx] = ~a2y;
+            }
+        } else {
+            // table / plain count: slices of PP pairs through the scratch
+            // yp[i * 32 + lane], a rolled word loop, words staged per lane
+#pragma unroll 1
+            for (int ps = 0; ps < 32 / PP; ++ps) {
 #pragma unroll
-                for (int i = 0; i < E; ++i) {
-                    const float2 y2 = v[kx * E + i];
-                    const int cx1 = stage_code<BITS, GRID>(y2.x, tb1, tc1, p.t1, p.b1, mx);
-                    const int cy1 = stage_code<BITS, GRID>(y2.y, tb1, tc1, p.t1, p.b1, my);
-                    const float rx = y2.x - __shfl_sync(FULL_MASK, tcen, cx1);
-                    const float ry = y2.y - __shfl_sync(FULL_MASK, tcen, cy1);
-                    const int cx2 = stage_code<BITS, GRID>(rx, tb2, tc2, p.t2, p.b2, mx);
-                    const int cy2 = stage_code<BITS, GRID>(ry, tb2, tc2, p.t2, p.b2, my);
-                    a1x = __funnelshift_r(a1x, (uint32_t)cx1, BITS);
-                    a2x = __funnelshift_r(a2x, (uint32_t)cx2, BITS);
-                    a1y = __funnelshift_r(a1y, (uint32_t)cy1, BITS);
-                    a2y = __funnelshift_r(a2y, (uint32_t)cy2, BITS);
+                for (int q4 = 0; q4 < 32 / PP; ++q4) {
+                    if (ps == q4) {
+#pragma unroll
+                        for (int i = 0; i < PP; ++i) yp[i * 32 + lane] = v[q4 * PP + i];
+                    }
+                }
+#pragma unroll 1
+                for (int w = 0; w < PP / E; ++w) {
+                    uint32_t a1x = 0u, a2x = 0u, a1y = 0u, a2y = 0u;
+#pragma unroll
+                    for (int i = 0; i < E; ++i) {
+                        const float2 y2 = yp[(w * E + i) * 32 + lane];
+                        const int cx1 = stage_code<BITS, GRID>(y2.x, tb1, tc1, p.t1, p.b1, mx);
+                        const int cy1 = stage_code<BITS, GRID>(y2.y, tb1, tc1, p.t1, p.b1, my);
+                        const float rx = y2.x - __shfl_sync(FULL_MASK, tcen, cx1);
+                        const float ry = y2.y - __shfl_sync(FULL_MASK, tcen, cy1);
+                        const int cx2 = stage_code<BITS, GRID>(rx, tb2, tc2, p.t2, p.b2, mx);
+                        const int cy2 = stage_code<BITS, GRID>(ry, tb2, tc2, p.t2, p.b2, my);
+                        a1x = __funnelshift_r(a1x, (uint32_t)cx1, BITS);
+                        a2x = __funnelshift_r(a2x, (uint32_t)cx2, BITS);
+                        a1y = __funnelshift_r(a1y, (uint32_t)cy1, BITS);
+                        a2y = __funnelshift_r(a2y, (uint32_t)cy2, BITS);
+                    }
+                    const int kx = ps * (PP / E) + w;
+                    ws[kx] = a1x;
+                    ws[WL / 2 + kx] = a1y;
+                    ws[WL + 1 + kx] = a2x;
+                    ws[WL + 1 + WL / 2 + kx] = a2y;
                 }
             }
-            wa1[kx] = a1x;
-            wa2[kx] = a2x;
-            wa1[WL / 2 + kx] = a1y;
-            wa2[WL / 2 + kx] = a2y;
+#pragma unroll
+            for (int i = 0; i < WL; ++i) {
+                wa1[i] = ws[i];
+                wa2[i] = ws[WL + 1 + i];
+            }
         }
         const float m = fminf(mx, my);
         // a zero row has no direction: always take the exact path for it
@@ -766,8 +805,8 @@ cudaError_t launch_enc(const RvqEncodeParams &p0, cudaStream_t stream)
         if (!encode_tmap_f16(&p.tmap, p.x, 2, dims, strides, box, true)) return cudaErrorInvalidValue;
     }
     auto kern = rvq_encode_kernel<BITS, MODE>;
-    constexpr int smem = enc_smem(BITS);
-    constexpr int warps = enc_warps(BITS);
+    constexpr int smem = enc_smem(BITS, MODE);
+    constexpr int warps = enc_warps(BITS, MODE);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     const int nblk = (p.N + ER - 1) / ER;
