@@ -629,25 +629,38 @@ constexpr int DEC_WARPS = 16;
 constexpr int DROWS = 16;
 __host__ __device__ constexpr int dec_stage(int bits) { return 2 * DROWS * (D * bits / 32) * 4; }
 __host__ __device__ constexpr int dec_warp_bytes(int bits) { return DEC_STAGES * dec_stage(bits) + DROWS * ROW_STRIDE; }
-__host__ __device__ constexpr int dec_smem(int bits) { return DEC_WARPS * (dec_warp_bytes(bits) + DEC_STAGES * 8); }
+__host__ __device__ constexpr int dec_table_bytes(int bits) { return bits == 4 ? 256 * 32 * 4 : 0; }
+__host__ __device__ constexpr int dec_smem(int bits)
+{
+    return dec_table_bytes(bits) + DEC_WARPS * (dec_warp_bytes(bits) + DEC_STAGES * 8);
+}
 
 // Decoded values c1[i1] + c2[i2] of the 64 coordinates of one half row, as 32
 // pairs (u[2k], u[2k + 1]).  w1 / w2: the half row's words of each stream.
+// The two codes of a coordinate index one merged table: for b <= 2 a 16- or
+// 4-entry table held one entry per lane (replicated across the warp) and read
+// by shuffle; for b = 4 a 256-entry table in shared memory, replicated per
+// lane (entry e of lane l at e * 32 + l, so every read is conflict-free).  The
+// words of both streams are first interleaved so that a shift (b <= 2) or a
+// byte extraction (b = 4) leaves the merged index i1 | i2 << b.
 template <int BITS>
 __device__ __forceinline__ void dec_lookup(const uint32_t (&w1)[BITS * 2], const uint32_t (&w2)[BITS * 2],
-                                           float tab, float tc1, float tc2, float2 (&v)[32])
+                                           float tab, const float *stab, float2 (&v)[32])
 {
     constexpr int E = 32 / BITS;
     float u[64];
     if constexpr (BITS == 4) {
 #pragma unroll
-        for (int e = 0; e < 64; ++e) {
-            const int sh = (e % E) * 4;
-            u[e] = __shfl_sync(FULL_MASK, tc1, (int)(w1[e / E] >> sh)) +
-                   __shfl_sync(FULL_MASK, tc2, (int)(w2[e / E] >> sh));
+        for (int j = 0; j < 2 * BITS; ++j) {
+            const uint32_t me = (w1[j] & 0x0F0F0F0Fu) | ((w2[j] << 4) & 0xF0F0F0F0u);
+            const uint32_t mo = ((w1[j] >> 4) & 0x0F0F0F0Fu) | (w2[j] & 0xF0F0F0F0u);
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                u[j * E + 2 * m] = stab[__byte_perm(me, 0u, 0x4440u + m) * 32];
+                u[j * E + 2 * m + 1] = stab[__byte_perm(mo, 0u, 0x4440u + m) * 32];
+            }
         }
     } else {
-        // merged index i1 | i2 << BITS: even coordinates from me, odd from mo
         constexpr uint32_t CM = BITS == 2 ? 0x33333333u : 0x55555555u;
 #pragma unroll
         for (int j = 0; j < 2 * BITS; ++j) {
@@ -676,20 +689,26 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) rvq_decode_kernel(const __g
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int rr = lane & 15, hh = lane >> 4;
-    unsigned char *wbuf = smem + warp * WB;
+    float *stab = reinterpret_cast<float *>(smem);  // b = 4: merged table, replicated per lane
+    unsigned char *wbuf = smem + dec_table_bytes(BITS) + warp * WB;
     unsigned char *obuf = wbuf + DEC_STAGES * STG;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + DEC_WARPS * WB) + warp * DEC_STAGES;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + dec_table_bytes(BITS) + DEC_WARPS * WB) + warp * DEC_STAGES;
     if (lane == 0) {
 #pragma unroll
         for (int s = 0; s < DEC_STAGES; ++s) mbar_init(&bars[s], 1);
         fence_mbar_init();
     }
+    if constexpr (BITS == 4) {
+        for (int i = threadIdx.x; i < 256 * 32; i += blockDim.x) {
+            const int e = i >> 5;
+            stab[i] = p.c1[e & 15] + p.c2[e >> 4];
+        }
+        __syncthreads();
+    }
     __syncwarp();
     const uint64_t pol = l2_policy_evict_first();
     // tables: per-stage (replicated every 2^BITS lanes) and merged (index
     // i1 | i2 << BITS, replicated every 2^(2 BITS) lanes; b <= 2 only)
-    const float tc1 = p.c1[lane & (L - 1)];
-    const float tc2 = p.c2[lane & (L - 1)];
     const float tab = BITS == 4 ? 0.0f : p.c1[lane & (L - 1)] + p.c2[(lane >> BITS) & (L - 1)];
     const int nblk = (p.N + DROWS - 1) / DROWS;
     const int gw = blockIdx.x * DEC_WARPS + warp;
@@ -748,7 +767,7 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) rvq_decode_kernel(const __g
             if (nb < nblk) issue(nb, s);
         }
         float2 v[32];
-        dec_lookup<BITS>(w1, w2, tab, tc1, tc2, v);
+        dec_lookup<BITS>(w1, w2, tab, stab + lane, v);
         // H64 on the half: coordinate bits 1-5 across the array, bit 0 in the pair
 #pragma unroll
         for (int h = 1; h < 32; h <<= 1) {
