@@ -93,18 +93,20 @@ __device__ __forceinline__ int stage_code(float v, float tb, int tc, const GridT
         const int g = grid_cell(v, t.a, t.bc);
         const float bnd = __shfl_sync(FULL_MASK, tb, g);
         const int cl = __shfl_sync(FULL_MASK, tc, g);
-        const float d = v - bnd;
+        // v > bnd exactly when bnd - v is negative (an exact tie gives +0):
+        // the increment is that sign bit
+        const float d = bnd - v;
         m = fminf(m, fabsf(d));
-        return cl + (d > 0.0f ? 1 : 0);
+        return cl + (int)(__float_as_uint(d) >> 31);
     } else {
         // fallback for codebooks without a grid table: a plain loop over the
         // boundaries (uniform across the warp), kept rolled to bound code size
         int code = 0;
 #pragma unroll 1
         for (int k = 0; k < (1 << BITS) - 1; ++k) {
-            const float d = v - b[k];
+            const float d = b[k] - v;
             m = fminf(m, fabsf(d));
-            code += d > 0.0f ? 1 : 0;
+            code += (int)(__float_as_uint(d) >> 31);
         }
         return code;
     }
