@@ -715,49 +715,37 @@ __global__ void __launch_bounds__(key_warps<BITS, G>() * 32, 1)
 
 constexpr int DQ_THREADS = 256;
 
-// Values: one row per thread; the words of a 32-row block (contiguous in
-// memory) arrive by one bulk copy into a 3-stage ring; the fp16 row is staged
-// in shared memory and written out coalesced.
-constexpr int VDQ_WARPS = 8;
+// Values: two threads per row: lane l works on row l & 15 of a 16-row block
+// and on channels [64h, 64h + 64), h = l >> 4.  The words of a block
+// (contiguous in memory) arrive by one bulk copy into a per-warp 3-stage
+// ring; scale/zero of the lane's groups are read one block ahead; per group
+// the exactness test picks one FMA per element or the rare round-to-odd path
+// (a small rolled loop over the staged words); the fp16 half rows are staged
+// in shared memory and written out coalesced (the 16 rows of a block are
+// contiguous).
+constexpr int VDQ_WARPS = 16;
 constexpr int VDQ_STAGES = 3;
-__host__ __device__ constexpr int vdq_stage(int bits) { return 32 * (D * bits / 32) * 4; }
-__host__ __device__ constexpr int vdq_warp_bytes(int bits) { return VDQ_STAGES * vdq_stage(bits) + 32 * ROW_STRIDE; }
+constexpr int VDR = 16;  // rows per block
+__host__ __device__ constexpr int vdq_stage(int bits) { return VDR * (D * bits / 32) * 4; }
+__host__ __device__ constexpr int vdq_warp_bytes(int bits) { return VDQ_STAGES * vdq_stage(bits) + VDR * ROW_STRIDE; }
 __host__ __device__ constexpr int vdq_smem(int bits) { return VDQ_WARPS * (vdq_warp_bytes(bits) + VDQ_STAGES * 8); }
-
-// One group of a row whose q*s + z is not exact in fp32 (rare): every element
-// goes through recon_exact.  wg: the group's words; out: its 16-byte output
-// chunks in the staging row.
-template <int BITS, int G>
-__device__ __noinline__ void vdq_group_exact(const uint32_t *wg, float s, float z, uint4 *out)
-{
-    constexpr int E = 32 / BITS;
-    constexpr uint32_t MASK = (1u << BITS) - 1u;
-    for (int c = 0; c < G / 8; ++c) {
-        uint32_t o[4];
-        for (int j = 0; j < 4; ++j) {
-            const int e = 8 * c + 2 * j;
-            const uint32_t q0 = (wg[e / E] >> ((e % E) * BITS)) & MASK;
-            const uint32_t q1 = (wg[(e + 1) / E] >> (((e + 1) % E) * BITS)) & MASK;
-            const __half2 hv = __halves2half2(recon_exact(q0, s, z), recon_exact(q1, s, z));
-            o[j] = *reinterpret_cast<const uint32_t *>(&hv);
-        }
-        out[c] = make_uint4(o[0], o[1], o[2], o[3]);
-    }
-}
 
 template <int BITS, int G>
 __global__ void __launch_bounds__(VDQ_WARPS * 32, 1) kivi_values_dequant_kernel(const __grid_constant__ KiviDequantParams p)
 {
     constexpr int E = 32 / BITS;
     constexpr int W = D * BITS / 32;
+    constexpr int WL = W / 2;              // words of a half row
     constexpr int NGD = D / G;
-    constexpr int WPG = G * BITS / 32;
+    constexpr int GL = G < 64 ? G : 64;    // group members held by one thread
+    constexpr int NGL = 64 / GL;           // groups (or group halves) per thread
     constexpr uint32_t MASK = (1u << BITS) - 1u;
     constexpr int STG = vdq_stage(BITS);
     constexpr int WB = vdq_warp_bytes(BITS);
     extern __shared__ __align__(128) unsigned char smem[];
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const int rr = lane & 15, hh = lane >> 4;
     unsigned char *wbuf = smem + warp * WB;
     unsigned char *obuf = wbuf + VDQ_STAGES * STG;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + VDQ_WARPS * WB) + warp * VDQ_STAGES;
@@ -769,13 +757,13 @@ __global__ void __launch_bounds__(VDQ_WARPS * 32, 1) kivi_values_dequant_kernel(
     __syncwarp();
     const uint64_t pol = l2_policy_evict_first();
     const int N = p.BH * p.S_q;
-    const int nblk = (N + 31) >> 5;
+    const int nblk = (N + VDR - 1) / VDR;
     const int gw = blockIdx.x * VDQ_WARPS + warp;
     const int tw = gridDim.x * VDQ_WARPS;
     auto issue = [&](int blk, int s) {
         if (lane == 0) {
-            const int r0 = blk << 5;
-            const uint32_t bytes = (uint32_t)(min(32, N - r0) * W * 4);
+            const int r0 = blk * VDR;
+            const uint32_t bytes = (uint32_t)(min(VDR, N - r0) * W * 4);
             mbar_arrive_expect_tx(&bars[s], bytes);
             bulk_g2s(wbuf + s * STG, p.packed + (size_t)r0 * W, bytes, &bars[s], pol);
         }
@@ -787,14 +775,16 @@ __global__ void __launch_bounds__(VDQ_WARPS * 32, 1) kivi_values_dequant_kernel(
     }
     const __half *scp = static_cast<const __half *>(p.scale);
     const __half *zrp = static_cast<const __half *>(p.zero);
-    // scale/zero of this lane's row, loaded one block ahead
-    __half sh[NGD], zh[NGD];
+    // scale/zero of this lane's groups, loaded one block ahead
+    const int j0 = G == 128 ? 0 : hh * NGL;
+    __half sh[NGL], zh[NGL];
     auto load_sz = [&](int blk) {
-        const int row = (blk << 5) + lane;
+        const int row = blk * VDR + rr;
+        const bool ok = blk < nblk && row < N;
 #pragma unroll
-        for (int j = 0; j < NGD; ++j) {
-            sh[j] = (blk < nblk && row < N) ? scp[(size_t)row * NGD + j] : __float2half_rn(0.0f);
-            zh[j] = (blk < nblk && row < N) ? zrp[(size_t)row * NGD + j] : __float2half_rn(0.0f);
+        for (int j = 0; j < NGL; ++j) {
+            sh[j] = ok ? scp[(size_t)row * NGD + j0 + j] : __float2half_rn(0.0f);
+            zh[j] = ok ? zrp[(size_t)row * NGD + j0 + j] : __float2half_rn(0.0f);
         }
     };
     load_sz(gw);
@@ -802,9 +792,9 @@ __global__ void __launch_bounds__(VDQ_WARPS * 32, 1) kivi_values_dequant_kernel(
         const int blk = gw + it * tw;
         if (blk >= nblk) break;
         const int s = it % VDQ_STAGES;
-        float sf[NGD], zf[NGD];
+        float sf[NGL], zf[NGL];
 #pragma unroll
-        for (int j = 0; j < NGD; ++j) {
+        for (int j = 0; j < NGL; ++j) {
             sf[j] = __half2float(sh[j]);
             zf[j] = __half2float(zh[j]);
         }
@@ -819,38 +809,47 @@ __global__ void __launch_bounds__(VDQ_WARPS * 32, 1) kivi_values_dequant_kernel(
             }
             return;
         }
-        const uint32_t *wrow = reinterpret_cast<const uint32_t *>(wbuf + s * STG + lane * W * 4);
-        uint4 *orow = reinterpret_cast<uint4 *>(obuf + lane * ROW_STRIDE);
+        const uint32_t *wrow = reinterpret_cast<const uint32_t *>(wbuf + s * STG) + rr * W + hh * WL;
+        uint32_t wd[WL];
+        if constexpr (WL == 2) {
+            const uint2 a = *reinterpret_cast<const uint2 *>(wrow);
+            wd[0] = a.x; wd[1] = a.y;
+        } else {
 #pragma unroll
-        for (int j = 0; j < NGD; ++j) {
-            if (group_sum_exact<BITS>(sf[j], zf[j])) {
-                uint32_t wg[WPG];
+            for (int i = 0; i < WL; i += 4) {
+                const uint4 a = *reinterpret_cast<const uint4 *>(wrow + i);
+                wd[i] = a.x; wd[i + 1] = a.y; wd[i + 2] = a.z; wd[i + 3] = a.w;
+            }
+        }
+        uint4 *orow = reinterpret_cast<uint4 *>(obuf + rr * ROW_STRIDE + hh * 128);
 #pragma unroll
-                for (int i = 0; i < WPG; i += 4) {
-                    if constexpr (WPG >= 4) {
-                        const uint4 a = *reinterpret_cast<const uint4 *>(wrow + j * WPG + i);
-                        wg[i] = a.x; wg[i + 1] = a.y; wg[i + 2] = a.z; wg[i + 3] = a.w;
-                    }
-                }
-                if constexpr (WPG < 4) {
+        for (int jl = 0; jl < NGL; ++jl) {
+            if (group_sum_exact<BITS>(sf[jl], zf[jl])) {
+                const float2 s2 = make_float2(sf[jl], sf[jl]), z2 = make_float2(zf[jl], zf[jl]);
 #pragma unroll
-                    for (int i = 0; i < WPG; ++i) wg[i] = wrow[j * WPG + i];
-                }
-#pragma unroll
-                for (int c = 0; c < G / 8; ++c) {
+                for (int c = 0; c < GL / 8; ++c) {
                     uint32_t o[4];
 #pragma unroll
                     for (int jj = 0; jj < 4; ++jj) {
-                        const int e = 8 * c + 2 * jj;
-                        const uint32_t q0 = (wg[e / E] >> ((e % E) * BITS)) & MASK;
-                        const uint32_t q1 = (wg[(e + 1) / E] >> (((e + 1) % E) * BITS)) & MASK;
-                        const __half2 hv = __floats2half2_rn(fmaf((float)q0, sf[j], zf[j]), fmaf((float)q1, sf[j], zf[j]));
+                        const int e = jl * GL + 8 * c + 2 * jj;  // element within the half row
+                        const uint32_t q0 = (wd[e / E] >> ((e % E) * BITS)) & MASK;
+                        const uint32_t q1 = (wd[(e + 1) / E] >> (((e + 1) % E) * BITS)) & MASK;
+                        const float2 r2 = __ffma2_rn(make_float2((float)q0, (float)q1), s2, z2);
+                        const __half2 hv = __floats2half2_rn(r2.x, r2.y);
                         o[jj] = *reinterpret_cast<const uint32_t *>(&hv);
                     }
-                    orow[j * (G / 8) + c] = make_uint4(o[0], o[1], o[2], o[3]);
+                    orow[jl * (GL / 8) + c] = make_uint4(o[0], o[1], o[2], o[3]);
                 }
             } else {
-                vdq_group_exact<BITS, G>(wrow + j * WPG, sf[j], zf[j], orow + j * (G / 8));
+                // q*s + z not exact in fp32 for this group (rare): round once
+                // from the exact value, element by element
+#pragma unroll 1
+                for (int e = jl * GL; e < jl * GL + GL; e += 2) {
+                    const uint32_t q0 = (wrow[e / E] >> ((e % E) * BITS)) & MASK;
+                    const uint32_t q1 = (wrow[(e + 1) / E] >> (((e + 1) % E) * BITS)) & MASK;
+                    const __half2 hv = __halves2half2(recon_exact(q0, sf[jl], zf[jl]), recon_exact(q1, sf[jl], zf[jl]));
+                    reinterpret_cast<uint32_t *>(orow)[e / 2] = *reinterpret_cast<const uint32_t *>(&hv);
+                }
             }
         }
         __syncwarp();
@@ -859,10 +858,10 @@ __global__ void __launch_bounds__(VDQ_WARPS * 32, 1) kivi_values_dequant_kernel(
             const int nb = blk + VDQ_STAGES * tw;
             if (nb < nblk) issue(nb, s);
         }
-        const int nrows = min(32, N - (blk << 5));
-        uint4 *gout = reinterpret_cast<uint4 *>(static_cast<__half *>(p.out) + (size_t)(blk << 5) * D);
+        const int nrows = min(VDR, N - blk * VDR);
+        uint4 *gout = reinterpret_cast<uint4 *>(static_cast<__half *>(p.out) + (size_t)blk * VDR * D);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
+        for (int i = 0; i < VDR / 2; ++i) {
             const int idx = i * 32 + lane;
             const int r = idx >> 4, c = idx & 15;
             if (r < nrows) gout[idx] = *reinterpret_cast<const uint4 *>(obuf + r * ROW_STRIDE + c * 16);
@@ -975,7 +974,7 @@ cudaError_t launch_dq(const KiviDequantParams &p, bool per_channel, cudaStream_t
         constexpr int smem = vdq_smem(BITS);
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
-        const int nblk = (p.BH * p.S_q + 31) / 32;
+        const int nblk = (p.BH * p.S_q + VDR - 1) / VDR;
         int grid = (nblk + VDQ_WARPS - 1) / VDQ_WARPS;
         if (grid > sm_count()) grid = sm_count();
         if (grid < 1) grid = 1;
