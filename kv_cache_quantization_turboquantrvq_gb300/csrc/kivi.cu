@@ -931,7 +931,9 @@ cudaError_t launch_q(const KiviQuantParams &p0, bool per_channel, cudaStream_t s
         const uint64_t dims[3] = {(uint64_t)D, (uint64_t)p.S, (uint64_t)p.B * p.H};
         const uint64_t strides[2] = {(uint64_t)D * 2, (uint64_t)p.S * D * 2};
         const uint32_t box[3] = {64u, per_channel ? (uint32_t)G : (uint32_t)VROWS, 1u};
-        if (!encode_tmap_f16(&p.tmap, p.x, 3, dims, strides, box, !per_channel))
+        // keys: a warp loads one 128-byte half of each token row (the other
+        // half belongs to another warp's tile): no 256-byte promotion
+        if (!encode_tmap_f16(&p.tmap, p.x, 3, dims, strides, box, !per_channel, !per_channel))
             return cudaErrorInvalidValue;
     }
     if (per_channel) {

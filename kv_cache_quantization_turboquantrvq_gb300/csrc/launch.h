@@ -111,9 +111,10 @@ bool build_grid(const float *b, int nb, float guard, GridTable &t);
 int sm_count();
 
 // Tiled tensor map of an fp16 tensor: dims innermost first, strides in bytes
-// of dims 1..rank-1, box in elements; false if the encoder is unavailable or
-// rejects the layout.
+// of dims 1..rank-1, box in elements; L2 promotion of 256 bytes when both
+// 128-byte halves of a row are loaded together, else 128; false if the
+// encoder is unavailable or rejects the layout.
 bool encode_tmap_f16(CUtensorMap *map, const void *base, int rank, const uint64_t *dims,
-                     const uint64_t *strides, const uint32_t *box, bool swizzle128);
+                     const uint64_t *strides, const uint32_t *box, bool swizzle128, bool promote256);
 
 }  // namespace vq

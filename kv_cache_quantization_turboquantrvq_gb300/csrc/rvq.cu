@@ -823,7 +823,7 @@ cudaError_t launch_enc(const RvqEncodeParams &p0, cudaStream_t stream)
         const uint64_t dims[2] = {(uint64_t)D, (uint64_t)p.N};
         const uint64_t strides[1] = {(uint64_t)D * 2};
         const uint32_t box[2] = {64u, (uint32_t)ER};
-        if (!encode_tmap_f16(&p.tmap, p.x, 2, dims, strides, box, true)) return cudaErrorInvalidValue;
+        if (!encode_tmap_f16(&p.tmap, p.x, 2, dims, strides, box, true, true)) return cudaErrorInvalidValue;
     }
     auto kern = rvq_encode_kernel<BITS, MODE>;
     constexpr int smem = enc_smem(BITS, MODE);

@@ -35,7 +35,7 @@ EncodeTiled encoder()
 }  // namespace
 
 bool encode_tmap_f16(CUtensorMap *map, const void *base, int rank, const uint64_t *dims,
-                     const uint64_t *strides, const uint32_t *box, bool swizzle128)
+                     const uint64_t *strides, const uint32_t *box, bool swizzle128, bool promote256)
 {
     EncodeTiled fn = encoder();
     if (fn == nullptr || rank < 1 || rank > 5) return false;
@@ -50,7 +50,8 @@ bool encode_tmap_f16(CUtensorMap *map, const void *base, int rank, const uint64_
     const CUresult r =
         fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, (cuuint32_t)rank, const_cast<void *>(base), gd, gs, bx, es,
            CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
-           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+           promote256 ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B : CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
