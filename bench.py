@@ -82,8 +82,12 @@ def describe(name):
     }[name]
 
 
-def build_workload(name, dev, rank=0, layers=None, batch=None):
-    """Device buffers and the op list for one step; also host inputs for e2e."""
+def build_workload(name, dev, rank=0, layers=None, batch=None, chunked=False, chunk_stream=None):
+    """Device buffers and the op list for one step; also host inputs for e2e.
+
+    With chunked=True, also returns the same step split into chunks that own
+    their inputs (views of the full device inputs), ops and results, for the
+    pipelined end-to-end measurement (C5: per batch, C3: per layer)."""
     import torch
     from kv_cache_quantization_turboquantrvq_gb300 import api, synth
 
@@ -93,7 +97,7 @@ def build_workload(name, dev, rank=0, layers=None, batch=None):
     def t(a):
         return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
 
-    def rvq_ops(tag, k_dev, bits, dst_off=None, S_dst=None):
+    def rvq_ops(tag, k_dev, bits, dst_off=None, S_dst=None, ops=ops, results=results, stream=stream):
         B, H, S, _ = k_dev.shape
         S_dst = S if S_dst is None else S_dst
         cb = [np.ascontiguousarray(a) for a in api.vq_rvq_codebook(D, bits)]
@@ -118,7 +122,8 @@ def build_workload(name, dev, rank=0, layers=None, batch=None):
             ops.append(Op(tag + "rvq_decode", "rvq_decode_kernel", dec, rvq_bytes(rows, bits), rows * D))
         results.extend([p1, p2, nr])
 
-    def kivi_ops(tag, k_dev, v_dev, bits, G, R, dst_off=None, S_dst=None):
+    def kivi_ops(tag, k_dev, v_dev, bits, G, R, dst_off=None, S_dst=None, ops=ops, results=results,
+                 stream=stream):
         B, H, S, _ = k_dev.shape
         S_q = S - R
         S_dst = S_q if S_dst is None else S_dst
@@ -146,6 +151,13 @@ def build_workload(name, dev, rank=0, layers=None, batch=None):
                 outs, B, H, S_q, bits, G, v_out=vo, want_k=False, stream=stream), vb, B * H * S_q * D))
         results.extend(outs.values())
 
+    chunks = []
+
+    def new_chunk(chunk_inputs):
+        c = {"inputs": chunk_inputs, "ops": [], "results": []}
+        chunks.append(c)
+        return c
+
     cfgs = synth.CONFIGS
     if name == "c5":
         cfg = cfgs["c5_long_32k"]
@@ -157,6 +169,13 @@ def build_workload(name, dev, rank=0, layers=None, batch=None):
         # order the step as the path runs: encode everything, then decode everything
         order = ["rvq_encode", "kivi_quant_k", "kivi_quant_v", "rvq_decode", "kivi_dequant_k", "kivi_dequant_v"]
         ops.sort(key=lambda o: order.index(o.name))
+        if chunked:
+            for b in range(k.shape[0]):
+                c = new_chunk([(k_np[b:b + 1], k[b:b + 1]), (v_np[b:b + 1], v[b:b + 1])])
+                rvq_ops("", k[b:b + 1], cfg["rvq_bits"], ops=c["ops"], results=c["results"], stream=chunk_stream)
+                kivi_ops("", k[b:b + 1], v[b:b + 1], cfg["kivi_bits"], cfg["group"], cfg["residual"],
+                         ops=c["ops"], results=c["results"], stream=chunk_stream)
+                c["ops"].sort(key=lambda o: order.index(o.name))
     elif name == "c3":
         cfg = cfgs["c3_rvq_b4_32L_8k"]
         for layer in range(cfg["layers"] if layers is None else layers):
@@ -164,6 +183,9 @@ def build_workload(name, dev, rank=0, layers=None, batch=None):
             k = t(k_np)
             inputs.append((k_np, k))
             rvq_ops("L%02d_" % layer, k, cfg["bits"])
+            if chunked:
+                c = new_chunk([(k_np, k)])
+                rvq_ops("L%02d_" % layer, k, cfg["bits"], ops=c["ops"], results=c["results"], stream=chunk_stream)
         ops.sort(key=lambda o: (o.kernel != "rvq_encode_kernel", o.name))
     elif name == "c2":
         cfg = cfgs["c2_kivi_b2_32x4096"]
@@ -187,6 +209,14 @@ def build_workload(name, dev, rank=0, layers=None, batch=None):
         kivi_ops("", k, v, 2, cfg["group"], 0, dst_off=off, S_dst=cfg["s_dst"])
     else:
         raise ValueError(name)
+    if chunked and not chunks:
+        # no split for this workload: one chunk, the step's own ops on the chunk stream
+        c = new_chunk(inputs)
+        c["ops"] = ops
+        c["results"] = results
+        c["own_stream"] = False
+    if chunked:
+        return ops, inputs, results, chunks
     return ops, inputs, results
 
 
@@ -388,7 +418,11 @@ def main():
     build.build()
     api.lib()  # fails loudly if the CUDA library is missing
 
-    ops, inputs, results = build_workload(args.workload, dev, rank, layers=args.layers, batch=args.batch)
+    s_run = torch.cuda.Stream()  # e2e kernel stream
+    built = build_workload(args.workload, dev, rank, layers=args.layers, batch=args.batch,
+                           chunked=not args.no_e2e, chunk_stream=s_run)
+    ops, inputs, results = built[:3]
+    chunks = built[3] if len(built) > 3 else []
     stream = torch.cuda.current_stream()
     K, W = args.steps, max(args.warmup, 3)
 
@@ -449,30 +483,53 @@ def main():
     if rec is not None:
         traffic = rec["dram_bytes_per_unit"] * dk["bytes"] / dk["launches"] / rec["alg_bytes_per_unit"]
 
-    # end to end through the public API with host buffers
+    # end to end through the public API with host buffers: the step's chunks
+    # (C5: one per batch, C3: one per layer) are pipelined over three streams,
+    # host->device copy of chunk c+1 and device->host copy of chunk c-1
+    # overlapping the kernels of chunk c
     e2e = None
     if not args.no_e2e:
-        pinned_in = [torch.from_numpy(np.ascontiguousarray(h)).pin_memory() for h, _ in inputs]
-        pinned_out = [torch.empty(r.shape, dtype=r.dtype, pin_memory=True) for r in results]
-        h2d = sum(p.numel() * p.element_size() for p in pinned_in)
-        d2h = sum(p.numel() * p.element_size() for p in pinned_out)
+        s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+        for c in chunks:
+            c["pin_in"] = [torch.from_numpy(np.ascontiguousarray(h)).pin_memory() for h, _ in c["inputs"]]
+            c["pin_out"] = [torch.empty(r.shape, dtype=r.dtype, pin_memory=True) for r in c["results"]]
+            c["ev_in"], c["ev_run"] = torch.cuda.Event(), torch.cuda.Event()
+        h2d = sum(p.numel() * p.element_size() for c in chunks for p in c["pin_in"])
+        d2h = sum(p.numel() * p.element_size() for c in chunks for p in c["pin_out"])
+        assert sum(o.nbytes for c in chunks for o in c["ops"]) == step_bytes
+
+        def e2e_step():
+            for c in chunks:
+                s_in.wait_event(c["ev_run"])  # the inputs' previous readers are done
+                with torch.cuda.stream(s_in):
+                    for p, (_, dv) in zip(c["pin_in"], c["inputs"]):
+                        dv.copy_(p, non_blocking=True)
+                c["ev_in"].record(s_in)
+                s_run.wait_event(c["ev_in"])
+                if c.get("own_stream", True):
+                    for o in c["ops"]:
+                        o.run()
+                else:  # the step's own ops run on the current stream: order it after the copies
+                    stream.wait_event(c["ev_in"])
+                    for o in c["ops"]:
+                        o.run()
+                    s_run.wait_stream(stream)
+                c["ev_run"].record(s_run)
+                s_out.wait_event(c["ev_run"])
+                with torch.cuda.stream(s_out):
+                    for p, r in zip(c["pin_out"], c["results"]):
+                        p.copy_(r, non_blocking=True)
+
         Ke = max(3, min(K, 20))
         for _ in range(2):
-            for p, (_, dv) in zip(pinned_in, inputs):
-                dv.copy_(p, non_blocking=True)
-            step()
-            for p, r in zip(pinned_out, results):
-                p.copy_(r, non_blocking=True)
+            e2e_step()
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
+        e0.record(s_in)
         for _ in range(Ke):
-            for p, (_, dv) in zip(pinned_in, inputs):
-                dv.copy_(p, non_blocking=True)
-            step()
-            for p, r in zip(pinned_out, results):
-                p.copy_(r, non_blocking=True)
-        e1.record(stream)
+            e2e_step()
+        s_out.wait_event(chunks[-1]["ev_run"])
+        e1.record(s_out)
         torch.cuda.synchronize()
         ems = e0.elapsed_time(e1)
         if world > 1:
@@ -481,7 +538,8 @@ def main():
             ems = float(tt.item())
         e2e = {"value": round(world * step_bytes * Ke / (ems * 1e-3) / 1e9, 2), "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "ms_per_step": round(ems / Ke, 4)}
+               "ms_per_step": round(ems / Ke, 4), "chunks_per_step": len(chunks),
+               "overlap": "host copies of neighbouring chunks overlap the kernels (3 streams)"}
     assert api.vq_device_error() == 0
 
     cpu = None
