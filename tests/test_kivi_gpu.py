@@ -59,7 +59,10 @@ def _gen(shape, seed, scale=1.0, outl=0):
     return (synth.kv_tensor(B, H, S, D, seed, outl, 20.0).astype(np.float32) * scale).astype(np.float16)
 
 
-@pytest.mark.parametrize("bits,G", [(1, 32), (2, 32), (4, 32), (2, 64), (4, 64), (2, 128)])
+ALL_BG = [(b, g) for b in (1, 2, 4) for g in (32, 64, 128)]
+
+
+@pytest.mark.parametrize("bits,G", ALL_BG)
 @pytest.mark.parametrize("S,R", [(96, 0), (133, 10), (70, 3)])
 def test_quant_parity_small(vq, oracle_mod, bits, G, S, R):
     k = _gen((2, 3, S), 11 + bits + G, outl=4)
@@ -152,7 +155,7 @@ def test_bad_offset_sets_device_error(vq):
     assert vq.vq_device_error() == 0
 
 
-@pytest.mark.parametrize("bits,G", [(1, 32), (2, 32), (4, 32), (2, 64), (4, 64)])
+@pytest.mark.parametrize("bits,G", ALL_BG)
 def test_dequant_parity_bit_exact(vq, oracle_mod, bits, G):
     """GPU dequant of the oracle's packed storage vs the oracle's dequant."""
     S, R = 3 * G + 5, 0
