@@ -65,11 +65,22 @@ __host__ __device__ constexpr int enc_warp_bytes(int bits, int mode)
     return ENC_STAGES * (ENC_BLOCK + 8) +
            (mode == MODE_SYM ? 0 : enc_pairs(bits) * 32 * 8 + 2 * 32 * (D * bits / 64 + 1) * 4);
 }
+// The table-driven quantizer reads its cell tables from shared memory,
+// replicated per lane (entry g of lane l at g * 32 + l: conflict-free): stage 1
+// {boundary, code below it, centroid below, centroid step} (16 bytes), stage 2
+// {boundary, code below it} (8 bytes).
+constexpr int ENC_TAB_BYTES = 32 * 32 * 16 + 32 * 32 * 8;
+__host__ __device__ constexpr int enc_tab_bytes(int mode) { return mode == MODE_GRID ? ENC_TAB_BYTES : 0; }
 __host__ __device__ constexpr int enc_warps(int bits, int mode)
 {
-    return (SMEM_MAX - 1024) / enc_warp_bytes(bits, mode) > 16 ? 16 : (SMEM_MAX - 1024) / enc_warp_bytes(bits, mode);
+    return (SMEM_MAX - 1024 - enc_tab_bytes(mode)) / enc_warp_bytes(bits, mode) > 16
+               ? 16
+               : (SMEM_MAX - 1024 - enc_tab_bytes(mode)) / enc_warp_bytes(bits, mode);
 }
-__host__ __device__ constexpr int enc_smem(int bits, int mode) { return 1024 + enc_warps(bits, mode) * enc_warp_bytes(bits, mode); }
+__host__ __device__ constexpr int enc_smem(int bits, int mode)
+{
+    return 1024 + enc_tab_bytes(mode) + enc_warps(bits, mode) * enc_warp_bytes(bits, mode);
+}
 
 // sqrt(128) = 8 sqrt(2) as a double-float (nearest fp32 + fp32 remainder).
 constexpr float SQRT_D_HI = 11.313708305358887f;
@@ -129,6 +140,33 @@ __device__ __forceinline__ int stage_code_df(float vh, float vl, float tb, int t
             code += (vh > b[k] || (vh == b[k] && vl > 0.0f)) ? 1 : 0;
         return code;
     }
+}
+
+// Both stages of one coordinate from the shared-memory cell tables: the
+// stage-1 entry carries the boundary of the cell, the code below it and the
+// centroids on both sides, so the residual needs no further lookup; two
+// table reads per coordinate instead of five shuffles.  v > bnd exactly when
+// bnd - v is negative (an exact tie gives +0), and the centroid step is taken
+// with the saturated multiple of the same difference.
+__device__ __forceinline__ void grid2_code(float v, const GridTable &ta, const GridTable &tb,
+                                           const unsigned char *t1l, const unsigned char *t2l, int &c1,
+                                           int &c2, float &m)
+{
+    const float u1 = __saturatef(fmaf(v, ta.a, ta.bc));
+    // cell in [0, 31]: u1 is saturated (NaN saturates to 0)
+    const uint32_t g1 = __float_as_uint(fmaf(u1, 31.0f, GRID_MAGIC)) - 0x4B400000u;
+    const float4 e1 = *reinterpret_cast<const float4 *>(t1l + g1 * 512u);
+    const float d1 = e1.x - v;
+    m = fminf(m, fabsf(d1));
+    c1 = __float_as_int(e1.y) + (int)(__float_as_uint(d1) >> 31);
+    const float s1 = __saturatef(d1 * -1.2676506e30f);  // 1 when v > bnd
+    const float r = fmaf(-s1, e1.w, v - e1.z);
+    const float u2 = __saturatef(fmaf(r, tb.a, tb.bc));
+    const uint32_t g2 = __float_as_uint(fmaf(u2, 31.0f, GRID_MAGIC)) - 0x4B400000u;
+    const float2 e2 = *reinterpret_cast<const float2 *>(t2l + g2 * 256u);
+    const float d2 = e2.x - r;
+    m = fminf(m, fabsf(d2));
+    c2 = __float_as_int(e2.y) + (int)(__float_as_uint(d2) >> 31);
 }
 
 // Symmetric 1- and 2-bit codebooks (c[k] = -c[L-1-k], middle boundary 0) are
@@ -361,7 +399,8 @@ __global__ void __launch_bounds__(enc_warps(BITS, MODE) * 32, 1)
     constexpr bool ROLLED = MODE != MODE_SYM;
     constexpr int PP = enc_pairs(BITS);
     extern __shared__ __align__(128) unsigned char smem_raw[];
-    unsigned char *smem = smem_1k(smem_raw);
+    unsigned char *stab = smem_1k(smem_raw);       // cell tables (GRID mode)
+    unsigned char *smem = stab + enc_tab_bytes(MODE);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int rr = lane & 15, hh = lane >> 4;
@@ -385,6 +424,25 @@ __global__ void __launch_bounds__(enc_warps(BITS, MODE) * 32, 1)
     const float tb2 = p.t2.bnd[lane];
     const int tc2 = p.t2.code[lane];
     const float tcen = p.c1[lane & (L - 1)];
+    if constexpr (GRID) {
+        // cell tables, replicated per lane; an empty cell (boundary -inf)
+        // always takes code + 1, so its centroid step is 0
+        float4 *t1s = reinterpret_cast<float4 *>(stab);
+        float2 *t2s = reinterpret_cast<float2 *>(stab + 32 * 32 * 16);
+        for (int i = threadIdx.x; i < 32 * 32; i += blockDim.x) {
+            const int g = i >> 5;
+            const int c = p.t1.code[g];
+            const bool empty = !(p.t1.bnd[g] > -3.0e38f);
+            const float chi = p.c1[c + 1];
+            const float clo = p.c1[empty ? c + 1 : c];
+            t1s[i] = make_float4(p.t1.bnd[g], __int_as_float(c), clo, chi - clo);
+            t2s[i] = make_float2(p.t2.bnd[g], __int_as_float(p.t2.code[g]));
+        }
+        __syncthreads();
+    }
+    // this lane's table columns: entry g at g * 512 (stage 1) / g * 256 (stage 2)
+    const unsigned char *t1l = stab + lane * 16;
+    const unsigned char *t2l = stab + 32 * 32 * 16 + lane * 8;
     const int nblk = (p.N + ER - 1) / ER;
     const int gw = blockIdx.x * WARPS + warp;
     const int tw = gridDim.x * WARPS;
@@ -540,12 +598,18 @@ __global__ void __launch_bounds__(enc_warps(BITS, MODE) * 32, 1)
 #pragma unroll
                     for (int i = 0; i < E; ++i) {
                         const float2 y2 = yp[(w * E + i) * 32 + lane];
-                        const int cx1 = stage_code<BITS, GRID>(y2.x, tb1, tc1, p.t1, p.b1, mx);
-                        const int cy1 = stage_code<BITS, GRID>(y2.y, tb1, tc1, p.t1, p.b1, my);
-                        const float rx = y2.x - __shfl_sync(FULL_MASK, tcen, cx1);
-                        const float ry = y2.y - __shfl_sync(FULL_MASK, tcen, cy1);
-                        const int cx2 = stage_code<BITS, GRID>(rx, tb2, tc2, p.t2, p.b2, mx);
-                        const int cy2 = stage_code<BITS, GRID>(ry, tb2, tc2, p.t2, p.b2, my);
+                        int cx1, cy1, cx2, cy2;
+                        if constexpr (GRID) {
+                            grid2_code(y2.x, p.t1, p.t2, t1l, t2l, cx1, cx2, mx);
+                            grid2_code(y2.y, p.t1, p.t2, t1l, t2l, cy1, cy2, my);
+                        } else {
+                            cx1 = stage_code<BITS, GRID>(y2.x, tb1, tc1, p.t1, p.b1, mx);
+                            cy1 = stage_code<BITS, GRID>(y2.y, tb1, tc1, p.t1, p.b1, my);
+                            const float rx = y2.x - __shfl_sync(FULL_MASK, tcen, cx1);
+                            const float ry = y2.y - __shfl_sync(FULL_MASK, tcen, cy1);
+                            cx2 = stage_code<BITS, GRID>(rx, tb2, tc2, p.t2, p.b2, mx);
+                            cy2 = stage_code<BITS, GRID>(ry, tb2, tc2, p.t2, p.b2, my);
+                        }
                         a1x = __funnelshift_r(a1x, (uint32_t)cx1, BITS);
                         a2x = __funnelshift_r(a2x, (uint32_t)cx2, BITS);
                         a1y = __funnelshift_r(a1y, (uint32_t)cy1, BITS);
