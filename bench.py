@@ -464,15 +464,17 @@ def main():
     gelem = world * step_elems * K / (elapsed_ms * 1e-3) / 1e9
 
     # per-op average durations (events on the launching stream)
-    per_ms = {}
+    per_ms, per_step = {}, {}
     for i, o in enumerate(ops):
-        per_ms[o.name] = statistics.mean(evs[k][i].elapsed_time(evs[k][i + 1]) for k in range(K))
+        per_step[o.name] = [evs[k][i].elapsed_time(evs[k][i + 1]) for k in range(K)]
+        per_ms[o.name] = statistics.mean(per_step[o.name])
     by_kernel = {}
     for o in ops:
-        d = by_kernel.setdefault(o.kernel, {"ms": 0.0, "bytes": 0, "launches": 0})
+        d = by_kernel.setdefault(o.kernel, {"ms": 0.0, "bytes": 0, "launches": 0, "steps": [0.0] * K})
         d["ms"] += per_ms[o.name]
         d["bytes"] += o.nbytes
         d["launches"] += o.launches
+        d["steps"] = [a + b for a, b in zip(d["steps"], per_step[o.name])]
     peak, peak_src = measured_peak()
     dom = max(by_kernel, key=lambda n: by_kernel[n]["ms"])
     dk = by_kernel[dom]
@@ -563,6 +565,9 @@ def main():
             "pct_of_nominal_8tbs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
             "gelem_per_s": round(gelem, 3),
             "per_kernel": {n: {"ms_per_launch": round(d["ms"] / d["launches"], 5),
+                               "ms_per_launch_median": round(statistics.median(d["steps"]) / d["launches"], 5),
+                               "ms_per_launch_min": round(min(d["steps"]) / d["launches"], 5),
+                               "ms_per_launch_max": round(max(d["steps"]) / d["launches"], 5),
                                "GB_s": round(d["bytes"] / d["launches"] / (d["ms"] / d["launches"] * 1e-3) / 1e9, 1),
                                "frac_of_peak": round(d["bytes"] / d["launches"] / (d["ms"] / d["launches"] * 1e-3) / 1e9 / peak, 4),
                                "launches_per_step": d["launches"]} for n, d in by_kernel.items()},
