@@ -61,6 +61,7 @@ def _load():
     lib.oracle_unpack_lsb_first.argtypes = [P, L, I, P]
     lib.oracle_rvq_encode.argtypes = [P, L, I, I, P, P, P, P] + [P] * 9
     lib.oracle_rvq_decode.argtypes = [P, P, P, L, I, I, P, P, P, P]
+    lib.oracle_rvq_attend.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, P, P, D, P, P]
     lib.oracle_kivi_quant.argtypes = [P, L, I, I, I, I, I, I, P, P, P, P, P]
     lib.oracle_kivi_dequant.argtypes = [P, P, P, L, I, I, I, I, I, P]
     _lib = lib
@@ -201,6 +202,29 @@ def rvq_decode(packed1, packed2, norms, D: int, bits: int, c1, c2, want_f64: boo
     f64 = np.empty((N, D), np.float64) if want_f64 else None
     _load().oracle_rvq_decode(_p(p1), _p(p2), _p(n), N, D, bits, _p(_c(c1, np.float32)),
                               _p(_c(c2, np.float32)), _p(out.view(np.uint16)), _p(f64))
+    return (out, f64) if want_f64 else out
+
+
+def rvq_attend(q, packed1, packed2, norms, v, bits: int, c1, c2, scale: float, lens=None,
+               want_f64: bool = False):
+    """Decode-time attention over an RVQ key cache (see oracle.c).
+    q [B, Hq, D] fp16; packed1/2 [B, Hkv, S_cap, W] uint32; norms [B, Hkv, S_cap] fp32;
+    v [B, Hkv, S_cap, D] fp16; lens [B] int32 or None.  Returns fp16 [B, Hq, D]
+    (and binary64 if asked)."""
+    qa = _c(q, np.float16)
+    B, Hq, D = qa.shape
+    p1 = _c(packed1, np.uint32)
+    p2 = _c(packed2, np.uint32)
+    _, Hkv, S_cap, _ = p1.shape
+    nr = _c(norms, np.float32)
+    va = _c(v, np.float16)
+    ln = None if lens is None else _c(lens, np.int32)
+    out = np.empty((B, Hq, D), np.float16)
+    f64 = np.empty((B, Hq, D), np.float64) if want_f64 else None
+    _load().oracle_rvq_attend(_p(qa.view(np.uint16)), _p(p1), _p(p2), _p(nr), _p(va.view(np.uint16)),
+                              None if ln is None else _p(ln), B, Hq, Hkv, S_cap, D, bits,
+                              _p(_c(c1, np.float32)), _p(_c(c2, np.float32)), float(scale),
+                              _p(out.view(np.uint16)), _p(f64))
     return (out, f64) if want_f64 else out
 
 

@@ -390,6 +390,80 @@ void oracle_rvq_decode(const uint32_t *packed1, const uint32_t *packed2, const f
     free(H); free(yh); free(q1); free(q2);
 }
 
+/*
+ * Decode-time attention over a TurboQuantRVQ key cache.  [TQ] "Kernel 5:
+ * Fused RVQ Decode + Attend": keys decoded on the fly from the two code
+ * streams, online softmax, values accumulated, never materialising the keys.
+ * Readings (the pages give the loop, not the interface): one query token per
+ * (batch, query head); query head hq reads kv head hq / (Hq / Hkv)
+ * (grouped-query attention); a key is the flush codec's decoded row
+ *   k_s = n_s * H (c1[i1] + c2[i2]) / sqrt(D)        (original domain)
+ * values are fp16; only the first lens[b] tokens of a cache take part
+ * (lens NULL: all S_cap); the weights are the exact softmax of
+ * scale * (q . k_s); an empty cache gives zeros.  Binary64 throughout, the
+ * output rounded once to binary16.
+ *
+ * q [B, Hq, D] fp16; packed1/2 [B, Hkv, S_cap, D*b/32]; norms [B, Hkv, S_cap];
+ * v [B, Hkv, S_cap, D] fp16; out [B, Hq, D].
+ */
+void oracle_rvq_attend(const uint16_t *q_f16, const uint32_t *packed1, const uint32_t *packed2,
+                       const float *norms, const uint16_t *v_f16, const int32_t *lens, int B,
+                       int Hq, int Hkv, int S_cap, int D, int bits, const float *c1,
+                       const float *c2, double scale, uint16_t *out_f16, double *out_f64)
+{
+    int W = D * bits / 32, G = Hq / Hkv;
+    double *H = (double *)malloc(sizeof(double) * D * D);
+    double *K = (double *)malloc(sizeof(double) * (size_t)S_cap * D);
+    double *yh = (double *)malloc(sizeof(double) * D);
+    double *sc = (double *)malloc(sizeof(double) * (S_cap > 0 ? S_cap : 1));
+    double *acc = (double *)malloc(sizeof(double) * D);
+    uint8_t *q1 = (uint8_t *)malloc(D), *q2 = (uint8_t *)malloc(D);
+    oracle_hadamard_matrix(D, H);
+    double inv_sqrt_d = 1.0 / sqrt((double)D);
+    for (int b = 0; b < B; ++b) {
+        int len = lens ? lens[b] : S_cap;
+        if (len > S_cap) len = S_cap;
+        if (len < 0) len = 0;
+        for (int h = 0; h < Hkv; ++h) {
+            long base = ((long)b * Hkv + h) * S_cap;
+            for (int s = 0; s < len; ++s) {
+                oracle_unpack_lsb_first(packed1 + (base + s) * W, D, bits, q1);
+                oracle_unpack_lsb_first(packed2 + (base + s) * W, D, bits, q2);
+                for (int i = 0; i < D; ++i) yh[i] = (double)c1[q1[i]] + (double)c2[q2[i]];
+                double n = (double)norms[base + s];
+                for (int j = 0; j < D; ++j) {
+                    double a = 0.0;
+                    for (int i = 0; i < D; ++i) a += H[(long)j * D + i] * yh[i];
+                    K[(long)s * D + j] = n * a * inv_sqrt_d;
+                }
+            }
+            for (int g = 0; g < G; ++g) {
+                long qo = ((long)b * Hq + (long)h * G + g) * D;
+                double m = -INFINITY;
+                for (int s = 0; s < len; ++s) {
+                    double dot = 0.0;
+                    for (int d = 0; d < D; ++d) dot += oracle_f16_to_f64(q_f16[qo + d]) * K[(long)s * D + d];
+                    sc[s] = scale * dot;
+                    if (sc[s] > m) m = sc[s];
+                }
+                double l = 0.0;
+                for (int d = 0; d < D; ++d) acc[d] = 0.0;
+                for (int s = 0; s < len; ++s) {
+                    double w = exp(sc[s] - m);
+                    l += w;
+                    for (int d = 0; d < D; ++d) acc[d] += w * oracle_f16_to_f64(v_f16[(base + s) * D + d]);
+                }
+                for (int d = 0; d < D; ++d) {
+                    double o = len > 0 ? acc[d] / l : 0.0;
+                    if (out_f64) out_f64[qo + d] = o;
+                    if (out_f16) out_f16[qo + d] = oracle_f64_to_f16_rn(o);
+                }
+            }
+        }
+    }
+    free(H); free(K); free(yh); free(sc); free(acc); free(q1); free(q2);
+}
+
 /* ------------------------------------------------------------------------ */
 /* KIVI asymmetric min/max group quantization.                               */
 /* [KIVI] first post, "What we're actually optimizing" and second post,      */
