@@ -13,7 +13,7 @@ K and V.  Inputs are 2 GiB, larger than L2 (129 MB), so no L2 flush is needed
 between steps.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload c5|c3|c2|c1|c4]
+                  [--workload c5|c3|c2|c1|c4|attn]
 
 --impl reference times the CPU oracle (single-threaded binary64 C) on a
 bounded sample of the same workload per step.
@@ -52,9 +52,13 @@ def measured_peak():
 
 
 class Op:
-    def __init__(self, name, kernel, run, nbytes, nelem, launches=1):
+    """One timed call.  `launches` counts the launches of `kernel` (per-launch
+    figures divide by it); `gpu_launches` counts every kernel the call starts."""
+
+    def __init__(self, name, kernel, run, nbytes, nelem, launches=1, gpu_launches=None):
         self.name, self.kernel, self.run = name, kernel, run
         self.nbytes, self.nelem, self.launches = nbytes, nelem, launches
+        self.gpu_launches = launches if gpu_launches is None else gpu_launches
 
 
 def rvq_bytes(rows, bits):
@@ -69,8 +73,17 @@ def kivi_bytes(bh, s_q, bits, G, per_channel):
     return n * 2 + words * 4 + groups * 4
 
 
+def attend_bytes(lens, Hkv, Hq, bits):
+    """Algorithmic bytes of one decode-attention call: every valid key's two
+    code streams, norm and fp16 value row, plus the queries in and outputs out."""
+    keys = int(np.sum(np.asarray(lens, np.int64))) * Hkv
+    return keys * (2 * (D * bits // 8) + 4 + 2 * D) + len(lens) * Hq * D * 2 * 2
+
+
 def describe(name):
     return {
+        "attn": "decode attention over RVQ b=2 key caches (fp16 values): 64 seqs x 8 kv heads x "
+                "32 query heads, capacity 16384, lengths uniform in [1k,16k]",
         "c5": "long-context K,V [4,32,32768,128] fp16 (4x40 outlier channels per head): RVQ b=2 "
               "encode+pack on K; KIVI 2-bit G=64 residual 128 on K and V; unpack+dequant of all",
         "c3": "RVQ b=4 encode+pack over 32 layers of keys [1,32,8192,128] fp16 (4x20 outliers), "
@@ -207,6 +220,42 @@ def build_workload(name, dev, rank=0, layers=None, batch=None, chunked=False, ch
         inputs = [(k_np, k), (v_np, v)]
         rvq_ops("", k, 2, dst_off=off, S_dst=cfg["s_dst"])
         kivi_ops("", k, v, 2, cfg["group"], 0, dst_off=off, S_dst=cfg["s_dst"])
+    elif name == "attn":
+        # the cache (codes, norms, values) is resident state; a step's input is
+        # the batch of queries and its result the attention output
+        cfg = cfgs["attn_decode_64x8x32_16k"]
+        B, Hkv, Hq, S, bits = cfg["B"], cfg["Hkv"], cfg["Hq"], cfg["S_cap"], cfg["bits"]
+        B = B if batch is None else batch
+        lens_np = synth.cache_lengths(B, cfg["seed"])
+        rng = np.random.default_rng(cfg["seed"])
+        W = D * bits // 32
+        g = torch.Generator(device=dev)
+        g.manual_seed(cfg["seed"])
+        p1 = torch.randint(-2 ** 31, 2 ** 31 - 1, (B, Hkv, S, W), dtype=torch.int32, device=dev, generator=g)
+        p2 = torch.randint(-2 ** 31, 2 ** 31 - 1, (B, Hkv, S, W), dtype=torch.int32, device=dev, generator=g)
+        nr = torch.empty((B, Hkv, S), dtype=torch.float32, device=dev).uniform_(4.0, 24.0, generator=g)
+        vv = torch.randn((B, Hkv, S, D), dtype=torch.float16, device=dev, generator=g)
+        q_np = rng.standard_normal((B, Hq, D)).astype(np.float16)
+        q, lens = t(q_np), t(lens_np)
+        c1, _, c2, _ = [np.ascontiguousarray(a) for a in api.vq_rvq_codebook(D, bits)]
+        out = torch.empty((B, Hq, D), dtype=torch.float16, device=dev)
+        ws = torch.empty((max(api.vq_rvq_attend_workspace(B, Hq, Hkv, S), 16) + 3) // 4,
+                         dtype=torch.float32, device=dev)
+        nsplit = 2 if ws.numel() > 4 else 1
+
+        def att(stream=stream):
+            api.vq_rvq_attend(q, p1, p2, nr, vv, bits, c1, c2, 1.0 / np.sqrt(D), lens=lens, out=out,
+                              workspace=ws, stream=stream)
+        ops.append(Op("rvq_attend", "rvq_attend_kernel", att, attend_bytes(lens_np, Hkv, Hq, bits),
+                      int(lens_np.sum()) * Hkv * D, gpu_launches=nsplit))
+        inputs = [(q_np, q)]
+        results.append(out)
+        if chunked:
+            c = new_chunk(inputs)
+            c["ops"] = [Op("rvq_attend", "rvq_attend_kernel", lambda: att(chunk_stream),
+                           attend_bytes(lens_np, Hkv, Hq, bits), int(lens_np.sum()) * Hkv * D,
+                           gpu_launches=nsplit)]
+            c["results"] = [out]
     else:
         raise ValueError(name)
     if chunked and not chunks:
@@ -343,6 +392,25 @@ def oracle_sample_rates(name, target_s=2.0):
         rk, rv, rkd, rvd, nk, nv = kivi_rates(2, G, x)
         rates.update(kivi_quant_k=rk, kivi_quant_v=rv, kivi_dequant_k=rkd, kivi_dequant_v=rvd)
         desc.append("KIVI 2-bit G=%d: %d key groups, %d value rows (and their dequant)" % (G, nk * D, nv))
+    if name == "attn":
+        cfg = cfgs["attn_decode_64x8x32_16k"]
+        bits, gq = cfg["bits"], cfg["Hq"] // cfg["Hkv"]
+        c1, _, c2, _, _ = oracle.rvq_codebooks(D, bits)
+        smax = 1 << 17
+        rng = np.random.default_rng(cfg["seed"])
+        W = D * bits // 32
+        p1 = rng.integers(0, 2 ** 32, (1, 1, smax, W), dtype=np.uint32)
+        p2 = rng.integers(0, 2 ** 32, (1, 1, smax, W), dtype=np.uint32)
+        nr = rng.uniform(4.0, 24.0, (1, 1, smax)).astype(np.float32)
+        v = rng.standard_normal((1, 1, smax, D)).astype(np.float16)
+        q = rng.standard_normal((1, gq, D)).astype(np.float16)
+
+        def att(n):
+            oracle.rvq_attend(q, p1[:, :, :n], p2[:, :, :n], nr[:, :, :n], v[:, :, :n], bits, c1, c2,
+                              1.0 / np.sqrt(D))
+        r, n, _ = timed(att, attend_bytes([1], 1, 0, bits), 256, smax)
+        rates["rvq_attend"] = r
+        desc.append("RVQ b=%d attention of %d query heads over one kv head of %d keys" % (bits, gq, n))
     return rates, "; ".join(desc) + " (about %.0f s of CPU per op)" % target_s
 
 
@@ -387,11 +455,11 @@ def main():
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--workload", choices=("c5", "c3", "c2", "c1", "c4"), default="c5")
+    ap.add_argument("--workload", choices=("c5", "c3", "c2", "c1", "c4", "attn"), default="c5")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--batch", type=int, default=None,
-                    help="c5 only: batch size B (default 4; 1 for small profiling runs)")
+                    help="c5 and attn only: batch size B (default 4 and 64; fewer for small profiling runs)")
     ap.add_argument("--layers", type=int, default=None,
                     help="c3 only: number of layers (default 32; fewer for small profiling runs)")
     args = ap.parse_args()
@@ -558,7 +626,7 @@ def main():
             "data": "synthetic (seeded N(0,1) fp16 with per-head outlier channels)",
             "config": {"workload": args.workload + ": " + describe(args.workload),
                        "parallelism": "replicas (independent shards per GPU)" if world > 1 else "single GPU",
-                       "l2": "inputs larger than L2 (129 MB); no flush" if args.workload in ("c5", "c3", "c2")
+                       "l2": "inputs larger than L2 (129 MB); no flush" if args.workload in ("c5", "c3", "c2", "attn")
                              else "inputs smaller than L2; rotating not applied",
                        "bytes_per_step": step_bytes, "elements_per_step": step_elems},
             "pct_of_peak": round(100 * value / world / peak, 2),
@@ -576,7 +644,7 @@ def main():
                          "traffic": None if traffic is None else int(traffic),
                          "alg_bytes_per_launch": int(dk["bytes"] / dk["launches"])},
             "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
-            "gpu_launches": sum(o.launches for o in ops) * K,
+            "gpu_launches": sum(o.gpu_launches for o in ops) * K,
         }
         print(json.dumps(line))
     if world > 1:
@@ -651,6 +719,11 @@ def reference_ops(name):
         ops.append(Op("rvq_encode", "rvq_encode", noop, rvq_bytes(rows, 2), rows * D))
         for n, pc in (("kivi_quant_k", True), ("kivi_quant_v", False)):
             ops.append(Op(n, n, noop, kivi_bytes(c["B"] * c["H"], c["S"], 2, c["group"], pc), rows * D))
+    elif name == "attn":
+        c = cfgs["attn_decode_64x8x32_16k"]
+        lens = synth.cache_lengths(c["B"], c["seed"])
+        ops.append(Op("rvq_attend", "rvq_attend", noop, attend_bytes(lens, c["Hkv"], c["Hq"], c["bits"]),
+                      int(lens.sum()) * c["Hkv"] * D))
     return ops
 
 

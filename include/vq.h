@@ -127,6 +127,35 @@ vq_status vq_rvq_unpack_dequant(const uint32_t *packed1, const uint32_t *packed2
                                 vq_stream_t stream);
 
 /*
+ * vq_rvq_attend - decode-time attention over a TurboQuantRVQ key cache
+ * (VeloxQuant-MLX blog, tag "turboquant", "Kernel 5: Fused RVQ Decode +
+ * Attend — Online Softmax Without Materializing K").  For every batch b and
+ * query head hq, with kv head h = hq / (Hq / Hkv):
+ *   out[b][hq] = sum_s softmax_s(scale * q[b][hq] . k_s) v[b][h][s]
+ * over the first lens[b] tokens (all S_cap when lens is NULL; an empty cache
+ * gives zeros), where k_s = n_s H (c1[i1] + c2[i2]) / sqrt(D) is the key that
+ * vq_rvq_encode_pack encoded.  Keys are scored in the rotated domain straight
+ * from their codes and never materialised.  fp32 arithmetic, fp16 output.
+ *   q [B, Hq, D] fp16, device.
+ *   packed1, packed2 [B, Hkv, S_cap, D*bits/32] uint32, norms [B, Hkv, S_cap]
+ *     fp32, v [B, Hkv, S_cap, D] fp16, device (an RVQ cache and its values).
+ *   lens [B] int32, device, or NULL.   c1, c2 [2^bits] fp32, host.
+ *   scale: softmax scale (commonly 1/sqrt(D)).   out [B, Hq, D] fp16, device.
+ *   workspace: device memory of at least the size vq_rvq_attend_workspace
+ *     reports for these shapes on the current device (NULL when that is 0),
+ *     owned by the caller and not shared by calls in flight at the same time;
+ *     a smaller workspace is accepted and only reduces the parallelism over
+ *     the cache length.
+ * D = 128, bits in {1, 2, 4}, Hq = GQ * Hkv with GQ in {1, 2, 4, 8}.
+ */
+vq_status vq_rvq_attend_workspace(int B, int Hq, int Hkv, int S_cap, size_t *bytes);
+vq_status vq_rvq_attend(const void *q_f16, const uint32_t *packed1, const uint32_t *packed2,
+                        const float *norms, const void *v_f16, const int32_t *lens, int B, int Hq,
+                        int Hkv, int S_cap, int D, int bits, const float *c1, const float *c2,
+                        float scale, void *out_f16, void *workspace, size_t workspace_bytes,
+                        vq_stream_t stream);
+
+/*
  * vq_kivi_quant_pack - KIVI flush of K and/or V (either may be NULL, with its
  * outputs).  Quantizes tokens [0, S_q), S_q = S - residual_length; tokens
  * [S_q, S) are the fp16 residual window and are not read or written.

@@ -29,7 +29,7 @@ VQ_DEVERR_BAD_OFFSET = 0x2
 
 EXPORTED = ("vq_status_str", "vq_version", "vq_rvq_codebook", "vq_rvq_encode_pack",
             "vq_rvq_unpack_dequant", "vq_kivi_quant_pack", "vq_kivi_unpack_dequant",
-            "vq_device_error")
+            "vq_device_error", "vq_rvq_attend_workspace", "vq_rvq_attend")
 
 
 class VQError(RuntimeError):
@@ -57,6 +57,9 @@ def lib():
     L.vq_kivi_quant_pack.argtypes = [P, P, I, I, I, I, I, I, I, P, P, P, P, P, P, P, I, P]
     L.vq_kivi_unpack_dequant.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, P, P, P]
     L.vq_device_error.argtypes = [P, ctypes.POINTER(ctypes.c_int)]
+    L.vq_rvq_attend_workspace.argtypes = [I, I, I, I, ctypes.POINTER(ctypes.c_size_t)]
+    L.vq_rvq_attend.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, P, P, ctypes.c_float, P, P,
+                                ctypes.c_size_t, P]
     for name in EXPORTED[2:]:
         getattr(L, name).restype = I
     _lib = L
@@ -147,6 +150,35 @@ def kivi_shapes(B, H, S_dst, D, bits, group):
         "k_packed": (B, H, NG, group * bits // 32, D), "k_scale": (B, H, NG, D),
         "v_packed": (B, H, S_dst, D * bits // 32), "v_scale": (B, H, S_dst, D // group),
     }
+
+
+def vq_rvq_attend_workspace(B: int, Hq: int, Hkv: int, S_cap: int) -> int:
+    """Workspace bytes vq_rvq_attend wants for these shapes on the current device."""
+    n = ctypes.c_size_t(0)
+    _check(lib().vq_rvq_attend_workspace(B, Hq, Hkv, S_cap, ctypes.byref(n)), "vq_rvq_attend_workspace")
+    return int(n.value)
+
+
+def vq_rvq_attend(q, packed1, packed2, norms, v, bits: int, c1, c2, scale: float, lens=None, out=None,
+                  workspace=None, stream=None):
+    """Decode-time attention of q [B, Hq, 128] over an RVQ key cache
+    (packed1, packed2, norms [B, Hkv, S_cap, ...]) and fp16 values v
+    [B, Hkv, S_cap, 128]; lens [B] int32 (device) or None.  Returns fp16
+    [B, Hq, 128].  The workspace is allocated when not given."""
+    import torch
+    B, Hq, D = q.shape
+    _, Hkv, S_cap, _ = packed1.shape
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=torch.float16, device=q.device)
+    if workspace is None:
+        nbytes = vq_rvq_attend_workspace(B, Hq, Hkv, S_cap)
+        workspace = torch.empty((max(nbytes, 16) + 3) // 4, dtype=torch.float32, device=q.device)
+    wbytes = workspace.numel() * workspace.element_size()
+    keep = [_host(t) for t in (c1, c2)]
+    _check(lib().vq_rvq_attend(_ptr(q), _ptr(packed1), _ptr(packed2), _ptr(norms), _ptr(v), _ptr(lens),
+                               B, Hq, Hkv, S_cap, D, bits, keep[0][1], keep[1][1], float(scale), _ptr(out),
+                               _ptr(workspace), wbytes, _stream(stream)), "vq_rvq_attend")
+    return out
 
 
 def vq_kivi_quant_pack(k, v, bits: int, group: int, residual_length: int, outs=None,

@@ -208,6 +208,92 @@ vq_status vq_rvq_unpack_dequant(const uint32_t *packed1, const uint32_t *packed2
     return cuda_status(launch_rvq_decode(p, bits, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+static size_t attend_ws_bytes(int B, int Hq, int nsplit)
+{
+    return nsplit > 1 ? (size_t)B * Hq * nsplit * AT_PART * sizeof(float) : 0;
+}
+
+static vq_status attend_shape_check(int B, int Hq, int Hkv, int S_cap)
+{
+    if (B < 0 || Hq < 0 || Hkv <= 0 || S_cap < 0) return VQ_ERR_INVALID_ARG;
+    if (Hq % Hkv != 0) return VQ_ERR_INVALID_ARG;
+    const int gq = Hq / Hkv;
+    if (Hq > 0 && gq != 1 && gq != 2 && gq != 4 && gq != 8) return VQ_ERR_UNSUPPORTED;
+    if ((long long)B * Hkv * S_cap >= (1LL << 31)) return VQ_ERR_UNSUPPORTED;
+    return VQ_OK;
+}
+
+vq_status vq_rvq_attend_workspace(int B, int Hq, int Hkv, int S_cap, size_t *bytes)
+{
+    if (!bytes) return VQ_ERR_INVALID_ARG;
+    const vq_status st = attend_shape_check(B, Hq, Hkv, S_cap);
+    if (st != VQ_OK) return st;
+    *bytes = attend_ws_bytes(B, Hq, rvq_attend_splits(B, Hkv, S_cap));
+    return VQ_OK;
+}
+
+vq_status vq_rvq_attend(const void *q_f16, const uint32_t *packed1, const uint32_t *packed2,
+                        const float *norms, const void *v_f16, const int32_t *lens, int B, int Hq,
+                        int Hkv, int S_cap, int D, int bits, const float *c1, const float *c2,
+                        float scale, void *out_f16, void *workspace, size_t workspace_bytes,
+                        vq_stream_t stream)
+{
+    vq_status st = attend_shape_check(B, Hq, Hkv, S_cap);
+    if (st != VQ_OK) return st;
+    if (bits == 3 || (D != kD && D > 0)) return VQ_ERR_UNSUPPORTED;
+    if (D != kD || (bits != 1 && bits != 2 && bits != 4)) return VQ_ERR_INVALID_ARG;
+    if (!c1 || !c2 || !std::isfinite(scale)) return VQ_ERR_INVALID_ARG;
+    const int L = 1 << bits;
+    for (int k = 0; k < L; ++k)
+        if (!std::isfinite(c1[k]) || !std::isfinite(c2[k])) return VQ_ERR_INVALID_ARG;
+    if ((long long)B * Hq == 0) return VQ_OK;
+    if (!q_f16 || !out_f16) return VQ_ERR_INVALID_ARG;
+    const bool cache = S_cap > 0;
+    if (cache && (!packed1 || !packed2 || !norms || !v_f16)) return VQ_ERR_INVALID_ARG;
+    if (!aligned(q_f16, 16) || !aligned(out_f16, 16) || (lens && !aligned(lens, 4)) ||
+        (cache && (!aligned(packed1, 16) || !aligned(packed2, 16) || !aligned(norms, 4) || !aligned(v_f16, 16))) ||
+        (workspace && !aligned(workspace, 16)))
+        return VQ_ERR_MISALIGNED;
+    const int W = D * bits / 32;
+    const size_t rows = (size_t)B * Hkv * S_cap;
+    const size_t out_b = (size_t)B * Hq * D * 2;
+    if (overlap(out_f16, out_b, q_f16, out_b) || (cache && (overlap(out_f16, out_b, packed1, rows * W * 4) ||
+                                                            overlap(out_f16, out_b, packed2, rows * W * 4) ||
+                                                            overlap(out_f16, out_b, norms, rows * 4) ||
+                                                            overlap(out_f16, out_b, v_f16, rows * D * 2))) ||
+        (lens && overlap(out_f16, out_b, lens, (size_t)B * 4)) ||
+        (workspace && overlap(out_f16, out_b, workspace, workspace_bytes)))
+        return VQ_ERR_ALIASING;
+    int nsplit = rvq_attend_splits(B, Hkv, S_cap);
+    const size_t per_split = (size_t)B * Hq * AT_PART * sizeof(float);
+    if (!workspace) workspace_bytes = 0;
+    if (nsplit > 1 && workspace_bytes < attend_ws_bytes(B, Hq, nsplit)) {
+        const size_t fit = workspace_bytes / per_split;
+        nsplit = fit > 1 ? (int)fit : 1;
+    }
+    RvqAttendParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.q = q_f16;
+    p.p1 = packed1;
+    p.p2 = packed2;
+    p.norms = norms;
+    p.v = v_f16;
+    p.lens = lens;
+    p.out = out_f16;
+    p.ws = static_cast<float *>(workspace);
+    p.B = B;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.S_cap = S_cap;
+    p.nsplit = nsplit;
+    p.qscale = (float)((double)scale * 1.4426950408889634 / std::sqrt((double)D));
+    for (int k = 0; k < 16; ++k) {
+        p.c1[k] = k < L ? c1[k] : 0.0f;
+        p.c2[k] = k < L ? c2[k] : 0.0f;
+    }
+    return cuda_status(launch_rvq_attend(p, bits, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 static vq_status kivi_common_check(int B, int H, int D, int bits, int group)
 {
     if (B < 0 || H < 0) return VQ_ERR_INVALID_ARG;

@@ -88,6 +88,23 @@ struct KiviDequantParams {
     int BH, S_q, group, NG;
 };
 
+// Decode-time attention over an RVQ key cache (attend.cu).
+constexpr int AT_PART = 2 + 128;  // floats of one split's partial: max, sum, output
+struct RvqAttendParams {
+    const void *q;                 // fp16 [B, Hq, 128]
+    const uint32_t *p1, *p2;       // [B, Hkv, S_cap, W]
+    const float *norms;            // [B, Hkv, S_cap]
+    const void *v;                 // fp16 [B, Hkv, S_cap, 128]
+    const int32_t *lens;           // [B] or null
+    void *out;                     // fp16 [B, Hq, 128]
+    float *ws;                     // [B, Hq, nsplit, AT_PART] when nsplit > 1
+    int B, Hq, Hkv, S_cap, nsplit;
+    float qscale;                  // softmax scale * log2(e) / sqrt(128)
+    float c1[16], c2[16];
+};
+int rvq_attend_splits(int B, int Hkv, int S_cap);
+cudaError_t launch_rvq_attend(const RvqAttendParams &p, int bits, cudaStream_t stream);
+
 // Encoder quantizer variants: plain boundary count (any codebook), shuffle
 // tables (GridTable), and the table-free symmetric 1/2-bit quantizer.
 enum RvqMode { RVQ_MODE_PLAIN = 0, RVQ_MODE_GRID = 1, RVQ_MODE_SYM = 2 };

@@ -87,6 +87,10 @@ CONFIGS = {
     # unpack+dequant of both.
     "c5_long_32k": dict(kind="long", B=4, H=32, S=32768, rvq_bits=2, kivi_bits=2, group=64,
                         residual=128, seed=105, k_outliers=(4, 40.0), v_outliers=(4, 40.0)),
+    # Decode-time attention over the flushed cache: 64 sequences, 8 kv heads
+    # and 32 query heads (GQA 4), RVQ b=2 keys and fp16 values in caches of
+    # capacity 16384 holding random lengths in [1k, 16k].
+    "attn_decode_64x8x32_16k": dict(kind="attend", B=64, Hkv=8, Hq=32, S_cap=16384, bits=2, seed=110),
 }
 
 
