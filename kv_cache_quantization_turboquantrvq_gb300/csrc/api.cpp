@@ -228,7 +228,9 @@ vq_status vq_rvq_attend_workspace(int B, int Hq, int Hkv, int S_cap, size_t *byt
     if (!bytes) return VQ_ERR_INVALID_ARG;
     const vq_status st = attend_shape_check(B, Hq, Hkv, S_cap);
     if (st != VQ_OK) return st;
-    *bytes = attend_ws_bytes(B, Hq, rvq_attend_splits(B, Hkv, S_cap));
+    int nsplit = 1, chunk = 0;
+    rvq_attend_plan(B, Hkv, S_cap, &nsplit, &chunk);
+    *bytes = attend_ws_bytes(B, Hq, nsplit);
     return VQ_OK;
 }
 
@@ -264,12 +266,13 @@ vq_status vq_rvq_attend(const void *q_f16, const uint32_t *packed1, const uint32
         (lens && overlap(out_f16, out_b, lens, (size_t)B * 4)) ||
         (workspace && overlap(out_f16, out_b, workspace, workspace_bytes)))
         return VQ_ERR_ALIASING;
-    int nsplit = rvq_attend_splits(B, Hkv, S_cap);
+    int nsplit = 1, chunk = 0;
+    rvq_attend_plan(B, Hkv, S_cap, &nsplit, &chunk);
     const size_t per_split = (size_t)B * Hq * AT_PART * sizeof(float);
     if (!workspace) workspace_bytes = 0;
     if (nsplit > 1 && workspace_bytes < attend_ws_bytes(B, Hq, nsplit)) {
         const size_t fit = workspace_bytes / per_split;
-        nsplit = fit > 1 ? (int)fit : 1;
+        rvq_attend_plan_fit(S_cap, fit > (size_t)nsplit ? nsplit : (int)fit, &nsplit, &chunk);
     }
     RvqAttendParams p;
     std::memset(&p, 0, sizeof(p));
@@ -286,6 +289,7 @@ vq_status vq_rvq_attend(const void *q_f16, const uint32_t *packed1, const uint32
     p.Hkv = Hkv;
     p.S_cap = S_cap;
     p.nsplit = nsplit;
+    p.chunk = chunk;
     p.qscale = (float)((double)scale * 1.4426950408889634 / std::sqrt((double)D));
     for (int k = 0; k < 16; ++k) {
         p.c1[k] = k < L ? c1[k] : 0.0f;
@@ -431,11 +435,12 @@ vq_status vq_device_error(vq_stream_t stream, int *code_out)
 {
     if (!code_out) return VQ_ERR_INVALID_ARG;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    unsigned a = 0, b = 0;
+    unsigned a = 0, b = 0, c = 0;
     if (rvq_take_device_error(&a, s) != cudaSuccess) return VQ_ERR_CUDA;
     if (kivi_take_device_error(&b, s) != cudaSuccess) return VQ_ERR_CUDA;
-    *code_out = (int)(a | b);
-    return (a | b) ? VQ_ERR_DEVICE : VQ_OK;
+    if (attend_take_device_error(&c, s) != cudaSuccess) return VQ_ERR_CUDA;
+    *code_out = (int)(a | b | c);
+    return (a | b | c) ? VQ_ERR_DEVICE : VQ_OK;
 }
 
 }  // extern "C"

@@ -98,11 +98,15 @@ struct RvqAttendParams {
     const int32_t *lens;           // [B] or null
     void *out;                     // fp16 [B, Hq, 128]
     float *ws;                     // [B, Hq, nsplit, AT_PART] when nsplit > 1
-    int B, Hq, Hkv, S_cap, nsplit;
+    int B, Hq, Hkv, S_cap;
+    int nsplit, chunk;             // chunks per (sequence, kv head) and keys per chunk
     float qscale;                  // softmax scale * log2(e) / sqrt(128)
     float c1[16], c2[16];
 };
-int rvq_attend_splits(int B, int Hkv, int S_cap);
+// Chunking of the keys: the default plan, and the finest one that fits
+// `max_splits` partials per (sequence, query head) in a workspace.
+void rvq_attend_plan(int B, int Hkv, int S_cap, int *nsplit, int *chunk);
+void rvq_attend_plan_fit(int S_cap, int max_splits, int *nsplit, int *chunk);
 cudaError_t launch_rvq_attend(const RvqAttendParams &p, int bits, cudaStream_t stream);
 
 // Encoder quantizer variants: plain boundary count (any codebook), shuffle
@@ -118,6 +122,7 @@ cudaError_t launch_kivi_dequant(const KiviDequantParams &p, int bits, bool per_c
 // Read and clear the device error word of each kernel unit (bitwise OR).
 cudaError_t rvq_take_device_error(unsigned *bits, cudaStream_t stream);
 cudaError_t kivi_take_device_error(unsigned *bits, cudaStream_t stream);
+cudaError_t attend_take_device_error(unsigned *bits, cudaStream_t stream);
 
 // Host side of the cell map (bit-exact copy of the device's) and the table
 // builder; build_grid returns false when no table meets the guard band.
