@@ -156,6 +156,36 @@ vq_status vq_rvq_attend(const void *q_f16, const uint32_t *packed1, const uint32
                         vq_stream_t stream);
 
 /*
+ * vq_rvq_attend_noalloc - vq_rvq_attend without a caller workspace.  The
+ * pages have no counterpart to this call: it is a convenience of this
+ * library for callers that cannot hand over device memory (for example, a
+ * captured graph whose allocations are fixed).  The per-chunk partial
+ * results go to a scratch array that the library itself holds in device
+ * memory, one per device, VQ_ATTEND_SCRATCH_BYTES long; its address is looked
+ * up once per device on first use.  Same arguments, computation and results
+ * as vq_rvq_attend with a workspace of the size vq_rvq_attend_workspace
+ * reports (the same chunking, so the output is bit-identical).
+ *   Size limit: when that chunking needs more than VQ_ATTEND_SCRATCH_BYTES of
+ *     partials (B * Hq * chunks * 520 bytes), the call returns
+ *     VQ_ERR_UNSUPPORTED before any launch; use vq_rvq_attend then.
+ *   Zero state: nothing in the scratch has to start at zero and the library
+ *     never clears it.  Every partial that the combine step reads was written
+ *     earlier in the same call by the chunk that owns it; chunks without keys
+ *     are neither written nor read, so values left by earlier calls are
+ *     never used.
+ *   Overlapping calls race: every call on a device shares the one scratch.
+ *     Two calls whose kernels can run at the same time (different streams
+ *     without an ordering between them, or host threads issuing to different
+ *     streams) overwrite each other's partials and give wrong outputs with no
+ *     error.  Issue such calls on one stream, or order them with events.
+ */
+#define VQ_ATTEND_SCRATCH_BYTES (16u * 1024u * 1024u)
+vq_status vq_rvq_attend_noalloc(const void *q_f16, const uint32_t *packed1, const uint32_t *packed2,
+                                const float *norms, const void *v_f16, const int32_t *lens, int B,
+                                int Hq, int Hkv, int S_cap, int D, int bits, const float *c1,
+                                const float *c2, float scale, void *out_f16, vq_stream_t stream);
+
+/*
  * vq_kivi_quant_pack - KIVI flush of K and/or V (either may be NULL, with its
  * outputs).  Quantizes tokens [0, S_q), S_q = S - residual_length; tokens
  * [S_q, S) are the fp16 residual window and are not read or written.

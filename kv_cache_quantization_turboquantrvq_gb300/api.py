@@ -29,7 +29,8 @@ VQ_DEVERR_BAD_OFFSET = 0x2
 
 EXPORTED = ("vq_status_str", "vq_version", "vq_rvq_codebook", "vq_rvq_encode_pack",
             "vq_rvq_unpack_dequant", "vq_kivi_quant_pack", "vq_kivi_unpack_dequant",
-            "vq_device_error", "vq_rvq_attend_workspace", "vq_rvq_attend")
+            "vq_device_error", "vq_rvq_attend_workspace", "vq_rvq_attend", "vq_rvq_attend_noalloc")
+VQ_ATTEND_SCRATCH_BYTES = 16 * 1024 * 1024
 
 
 class VQError(RuntimeError):
@@ -60,6 +61,7 @@ def lib():
     L.vq_rvq_attend_workspace.argtypes = [I, I, I, I, ctypes.POINTER(ctypes.c_size_t)]
     L.vq_rvq_attend.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, P, P, ctypes.c_float, P, P,
                                 ctypes.c_size_t, P]
+    L.vq_rvq_attend_noalloc.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, P, P, ctypes.c_float, P, P]
     for name in EXPORTED[2:]:
         getattr(L, name).restype = I
     _lib = L
@@ -178,6 +180,22 @@ def vq_rvq_attend(q, packed1, packed2, norms, v, bits: int, c1, c2, scale: float
     _check(lib().vq_rvq_attend(_ptr(q), _ptr(packed1), _ptr(packed2), _ptr(norms), _ptr(v), _ptr(lens),
                                B, Hq, Hkv, S_cap, D, bits, keep[0][1], keep[1][1], float(scale), _ptr(out),
                                _ptr(workspace), wbytes, _stream(stream)), "vq_rvq_attend")
+    return out
+
+
+def vq_rvq_attend_noalloc(q, packed1, packed2, norms, v, bits: int, c1, c2, scale: float, lens=None,
+                          out=None, stream=None):
+    """vq_rvq_attend with the library's static device scratch instead of a
+    workspace (calls must not overlap in time on one device)."""
+    import torch
+    B, Hq, D = q.shape
+    _, Hkv, S_cap, _ = packed1.shape
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=torch.float16, device=q.device)
+    keep = [_host(t) for t in (c1, c2)]
+    _check(lib().vq_rvq_attend_noalloc(_ptr(q), _ptr(packed1), _ptr(packed2), _ptr(norms), _ptr(v), _ptr(lens),
+                                       B, Hq, Hkv, S_cap, D, bits, keep[0][1], keep[1][1], float(scale),
+                                       _ptr(out), _stream(stream)), "vq_rvq_attend_noalloc")
     return out
 
 

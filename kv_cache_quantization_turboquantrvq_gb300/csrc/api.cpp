@@ -234,11 +234,13 @@ vq_status vq_rvq_attend_workspace(int B, int Hq, int Hkv, int S_cap, size_t *byt
     return VQ_OK;
 }
 
-vq_status vq_rvq_attend(const void *q_f16, const uint32_t *packed1, const uint32_t *packed2,
-                        const float *norms, const void *v_f16, const int32_t *lens, int B, int Hq,
-                        int Hkv, int S_cap, int D, int bits, const float *c1, const float *c2,
-                        float scale, void *out_f16, void *workspace, size_t workspace_bytes,
-                        vq_stream_t stream)
+// Shared body of vq_rvq_attend (caller workspace) and vq_rvq_attend_noalloc
+// (the library's static scratch, which must hold the default plan's partials).
+static vq_status rvq_attend_impl(const void *q_f16, const uint32_t *packed1, const uint32_t *packed2,
+                                 const float *norms, const void *v_f16, const int32_t *lens, int B,
+                                 int Hq, int Hkv, int S_cap, int D, int bits, const float *c1,
+                                 const float *c2, float scale, void *out_f16, void *workspace,
+                                 size_t workspace_bytes, bool static_scratch, vq_stream_t stream)
 {
     vq_status st = attend_shape_check(B, Hq, Hkv, S_cap);
     if (st != VQ_OK) return st;
@@ -268,6 +270,11 @@ vq_status vq_rvq_attend(const void *q_f16, const uint32_t *packed1, const uint32
         return VQ_ERR_ALIASING;
     int nsplit = 1, chunk = 0;
     rvq_attend_plan(B, Hkv, S_cap, &nsplit, &chunk);
+    if (static_scratch) {
+        // the same plan as with a full workspace, or a size-limit error
+        if (attend_static_scratch(&workspace, &workspace_bytes) != cudaSuccess) return VQ_ERR_CUDA;
+        if (attend_ws_bytes(B, Hq, nsplit) > workspace_bytes) return VQ_ERR_UNSUPPORTED;
+    }
     const size_t per_split = (size_t)B * Hq * AT_PART * sizeof(float);
     if (!workspace) workspace_bytes = 0;
     if (nsplit > 1 && workspace_bytes < attend_ws_bytes(B, Hq, nsplit)) {
@@ -296,6 +303,25 @@ vq_status vq_rvq_attend(const void *q_f16, const uint32_t *packed1, const uint32
         p.c2[k] = k < L ? c2[k] : 0.0f;
     }
     return cuda_status(launch_rvq_attend(p, bits, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+vq_status vq_rvq_attend(const void *q_f16, const uint32_t *packed1, const uint32_t *packed2,
+                        const float *norms, const void *v_f16, const int32_t *lens, int B, int Hq,
+                        int Hkv, int S_cap, int D, int bits, const float *c1, const float *c2,
+                        float scale, void *out_f16, void *workspace, size_t workspace_bytes,
+                        vq_stream_t stream)
+{
+    return rvq_attend_impl(q_f16, packed1, packed2, norms, v_f16, lens, B, Hq, Hkv, S_cap, D, bits, c1, c2,
+                           scale, out_f16, workspace, workspace_bytes, false, stream);
+}
+
+vq_status vq_rvq_attend_noalloc(const void *q_f16, const uint32_t *packed1, const uint32_t *packed2,
+                                const float *norms, const void *v_f16, const int32_t *lens, int B,
+                                int Hq, int Hkv, int S_cap, int D, int bits, const float *c1,
+                                const float *c2, float scale, void *out_f16, vq_stream_t stream)
+{
+    return rvq_attend_impl(q_f16, packed1, packed2, norms, v_f16, lens, B, Hq, Hkv, S_cap, D, bits, c1, c2,
+                           scale, out_f16, nullptr, 0, true, stream);
 }
 
 static vq_status kivi_common_check(int B, int H, int D, int bits, int group)

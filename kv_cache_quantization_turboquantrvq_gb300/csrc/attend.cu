@@ -30,6 +30,8 @@
 // carries scale * log2(e)).
 #include <cuda_fp16.h>
 
+#include <mutex>
+
 #include "device_common.cuh"
 #include "launch.h"
 
@@ -38,6 +40,10 @@ namespace vq {
 namespace {
 
 VQ_DEFINE_ERROR_WORD(g_at_err);
+
+// Scratch for the split partials of vq_rvq_attend_noalloc (no caller
+// workspace); one array per device, in the module's static device memory.
+static __device__ __align__(256) float g_at_scratch[VQ_ATTEND_SCRATCH_BYTES / sizeof(float)];
 
 constexpr int D = 128;
 constexpr int AT_WARPS = 8;
@@ -481,6 +487,25 @@ cudaError_t launch_rvq_attend(const RvqAttendParams &p, int bits, cudaStream_t s
     case 4: return dispatch_at<4>(p, stream);
     default: return cudaErrorInvalidValue;
     }
+}
+
+cudaError_t attend_static_scratch(void **ptr, size_t *bytes)
+{
+    // the symbol's device address, looked up once per device
+    static std::mutex mu;
+    static void *addr[64] = {nullptr};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (addr[dev] == nullptr) {
+        e = cudaGetSymbolAddress(&addr[dev], g_at_scratch);
+        if (e != cudaSuccess) return e;
+    }
+    *ptr = addr[dev];
+    *bytes = sizeof(g_at_scratch);
+    return cudaSuccess;
 }
 
 cudaError_t attend_take_device_error(unsigned *bits, cudaStream_t stream)

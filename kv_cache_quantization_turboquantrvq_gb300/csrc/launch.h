@@ -108,6 +108,9 @@ struct RvqAttendParams {
 void rvq_attend_plan(int B, int Hkv, int S_cap, int *nsplit, int *chunk);
 void rvq_attend_plan_fit(int S_cap, int max_splits, int *nsplit, int *chunk);
 cudaError_t launch_rvq_attend(const RvqAttendParams &p, int bits, cudaStream_t stream);
+// Device address and size of the library's static attention scratch on the
+// current device.
+cudaError_t attend_static_scratch(void **ptr, size_t *bytes);
 
 // Encoder quantizer variants: plain boundary count (any codebook), shuffle
 // tables (GridTable), and the table-free symmetric 1/2-bit quantizer.
