@@ -168,7 +168,9 @@ vq_status vq_rvq_encode_pack(const void *k_f16, int B, int H, int S, int D, int 
     if (bits <= 2 && symmetric_codebook(c1, b1, L) && symmetric_codebook(c2, b2, L))
         mode = RVQ_MODE_SYM;
     else if (build_grid(b1, L - 1, kGuard, p.t1) && build_grid(b2, L - 1, kGuard, p.t2))
-        mode = RVQ_MODE_GRID;
+        // the shuffle tables also serve the exact recompute of the pair mode
+        mode = bits == 4 && build_pair_table(c1, b1, c2, b2, bits, kGuard, p.pt) ? RVQ_MODE_PAIR
+                                                                                 : RVQ_MODE_GRID;
     return cuda_status(launch_rvq_encode(p, bits, mode, reinterpret_cast<cudaStream_t>(stream)));
 }
 

@@ -22,6 +22,20 @@ struct GridTable {
     int code[32];
 };
 
+// Both 4-bit stage codes of a coordinate from one lookup.  The pair (i1, i2)
+// is a step function of y whose steps are the stage-1 boundaries and, inside
+// stage-1 cell k, the stage-2 boundaries shifted by c1[k] (i2 counts
+// y - c1[k] > b2_j, i.e. y > c1[k] + b2_j).  The device maps y to one of
+// PT_CELLS cells, g(v) = RN((PT_CELLS - 1) sat(fma(v, a, bc))); a table is
+// accepted when every boundary has a cell of its own and lies at least the
+// guard band away from that cell's edges.  Entry g: the boundary in the cell
+// (-inf if none) and the pairs below / above it, i1 | i2 << 4, in bytes 0 / 1.
+constexpr int PT_CELLS = 1024;
+struct PairTable {
+    float a, bc;
+    uint2 ent[PT_CELLS];  // x: boundary (fp32 bits), y: pairs
+};
+
 // Division by a divisor d fixed for a launch, for numerators 0 <= n < 2^31:
 // q = umulhi(n, m) >> s with l = ceil(log2 d), m = ceil(2^(31 + l) / d),
 // s = l - 1 (Granlund and Montgomery, "Division by invariant integers using
@@ -61,6 +75,7 @@ struct RvqEncodeParams {
     float guard;         // |y - boundary| below this sends the row to the exact path
     GridTable t1, t2;
     float c1[16], c2[16], b1[16], b2[16];
+    PairTable pt;  // RVQ_MODE_PAIR only
 };
 
 struct RvqDecodeParams {
@@ -114,7 +129,7 @@ cudaError_t attend_static_scratch(void **ptr, size_t *bytes);
 
 // Encoder quantizer variants: plain boundary count (any codebook), shuffle
 // tables (GridTable), and the table-free symmetric 1/2-bit quantizer.
-enum RvqMode { RVQ_MODE_PLAIN = 0, RVQ_MODE_GRID = 1, RVQ_MODE_SYM = 2 };
+enum RvqMode { RVQ_MODE_PLAIN = 0, RVQ_MODE_GRID = 1, RVQ_MODE_SYM = 2, RVQ_MODE_PAIR = 3 };
 cudaError_t launch_rvq_encode(const RvqEncodeParams &p, int bits, int mode, cudaStream_t stream);
 cudaError_t launch_rvq_decode(const RvqDecodeParams &p, int bits, cudaStream_t stream);
 cudaError_t launch_kivi_quant(const KiviQuantParams &p, int bits, bool per_channel,
@@ -131,6 +146,9 @@ cudaError_t attend_take_device_error(unsigned *bits, cudaStream_t stream);
 // builder; build_grid returns false when no table meets the guard band.
 int grid_cell_host(float v, float a, float bc);
 bool build_grid(const float *b, int nb, float guard, GridTable &t);
+int pair_cell_host(float v, float a, float bc);
+bool build_pair_table(const float *c1, const float *b1, const float *c2, const float *b2, int bits,
+                      float guard, PairTable &t);
 
 // Number of SMs of the current device (cached per device).
 int sm_count();

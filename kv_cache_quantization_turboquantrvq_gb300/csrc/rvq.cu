@@ -58,19 +58,22 @@ constexpr int ER = 16;
 constexpr int ENC_STAGES = 2;
 constexpr int ENC_BLOCK = ER * ROW_BYTES;  // two swizzled 2 KB boxes
 constexpr int SMEM_MAX = 227 * 1024;
-enum { MODE_PLAIN = 0, MODE_GRID = 1, MODE_SYM = 2 };
+enum { MODE_PLAIN = 0, MODE_GRID = 1, MODE_SYM = 2, MODE_PAIR = 3 };
 __host__ __device__ constexpr int enc_pairs(int bits) { return 32 / bits > 8 ? 32 / bits : 8; }
 __host__ __device__ constexpr int enc_warp_bytes(int bits, int mode)
 {
     return ENC_STAGES * (ENC_BLOCK + 8) +
-           (mode == MODE_SYM ? 0 : enc_pairs(bits) * 32 * 8 + 2 * 32 * (D * bits / 64 + 1) * 4);
+           (mode == MODE_SYM || mode == MODE_PAIR ? 0 : enc_pairs(bits) * 32 * 8 + 2 * 32 * (D * bits / 64 + 1) * 4);
 }
 // The table-driven quantizer reads its cell tables from shared memory,
 // replicated per lane (entry g of lane l at g * 32 + l: conflict-free): stage 1
 // {boundary, code below it, centroid below, centroid step} (16 bytes), stage 2
 // {boundary, code below it} (8 bytes).
 constexpr int ENC_TAB_BYTES = 32 * 32 * 16 + 32 * 32 * 8;
-__host__ __device__ constexpr int enc_tab_bytes(int mode) { return mode == MODE_GRID ? ENC_TAB_BYTES : 0; }
+__host__ __device__ constexpr int enc_tab_bytes(int mode)
+{
+    return mode == MODE_GRID ? ENC_TAB_BYTES : (mode == MODE_PAIR ? PT_CELLS * 8 : 0);
+}
 __host__ __device__ constexpr int enc_warps(int bits, int mode)
 {
     return (SMEM_MAX - 1024 - enc_tab_bytes(mode)) / enc_warp_bytes(bits, mode) > 16
@@ -167,6 +170,21 @@ __device__ __forceinline__ void grid2_code(float v, const GridTable &ta, const G
     const float d2 = e2.x - r;
     m = fminf(m, fabsf(d2));
     c2 = __float_as_int(e2.y) + (int)(__float_as_uint(d2) >> 31);
+}
+
+// Both 4-bit codes of one coordinate from the pair table (PairTable in
+// launch.h): one cell lookup, one comparison with the cell's boundary (v > bnd
+// exactly when bnd - v is negative; an exact tie gives +0), and the byte of
+// the chosen pair, i1 | i2 << 4, in the low byte of the result.
+__device__ __forceinline__ uint32_t pair_code(float v, float a, float bc, const uint2 *tab, float &m)
+{
+    const float u = __saturatef(fmaf(v, a, bc));
+    // cell in [0, PT_CELLS - 1]: u is saturated (NaN saturates to 0)
+    const uint32_t g = __float_as_uint(fmaf(u, (float)(PT_CELLS - 1), GRID_MAGIC)) - 0x4B400000u;
+    const uint2 e = tab[g];
+    const float d = __uint_as_float(e.x) - v;
+    m = fminf(m, fabsf(d));
+    return __byte_perm(e.y, 0u, __float_as_uint(d) >> 31);
 }
 
 // Symmetric 1- and 2-bit codebooks (c[k] = -c[L-1-k], middle boundary 0) are
@@ -396,10 +414,10 @@ __global__ void __launch_bounds__(enc_warps(BITS, MODE) * 32, 1)
     constexpr int W = D * BITS / 32;
     constexpr int WL = W / 2;  // words of a half row
     constexpr int WARPS = enc_warps(BITS, MODE);
-    constexpr bool ROLLED = MODE != MODE_SYM;
+    constexpr bool ROLLED = MODE == MODE_GRID || MODE == MODE_PLAIN;
     constexpr int PP = enc_pairs(BITS);
     extern __shared__ __align__(128) unsigned char smem_raw[];
-    unsigned char *stab = smem_1k(smem_raw);       // cell tables (GRID mode)
+    unsigned char *stab = smem_1k(smem_raw);       // cell tables (GRID), pair table (PAIR)
     unsigned char *smem = stab + enc_tab_bytes(MODE);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -438,6 +456,11 @@ __global__ void __launch_bounds__(enc_warps(BITS, MODE) * 32, 1)
             t1s[i] = make_float4(p.t1.bnd[g], __int_as_float(c), clo, chi - clo);
             t2s[i] = make_float2(p.t2.bnd[g], __int_as_float(p.t2.code[g]));
         }
+        __syncthreads();
+    }
+    if constexpr (MODE == MODE_PAIR) {
+        uint2 *pt = reinterpret_cast<uint2 *>(stab);
+        for (int i = threadIdx.x; i < PT_CELLS; i += blockDim.x) pt[i] = p.pt.ent[i];
         __syncthreads();
     }
     // this lane's table columns: entry g at g * 512 (stage 1) / g * 256 (stage 2)
@@ -560,7 +583,35 @@ __global__ void __launch_bounds__(enc_warps(BITS, MODE) * 32, 1)
         // kx + WL/2 from the second ones.
         float mx = __int_as_float(0x7f800000), my = mx;
         uint32_t wa1[WL], wa2[WL];
-        if constexpr (!ROLLED) {
+        if constexpr (MODE == MODE_PAIR) {
+            // 4-bit pair table, unrolled: the pairs of a word's 8 coordinates
+            // collect as bytes (even coordinates in b0, odd in b1, first at
+            // byte 0), then the low nibbles make the stage-1 word and the
+            // high nibbles the stage-2 word
+            const uint2 *ptab = reinterpret_cast<const uint2 *>(stab);
+            const float pa = p.pt.a, pbc = p.pt.bc;
+#pragma unroll
+            for (int kx = 0; kx < WL / 2; ++kx) {
+                uint32_t b0x = 0u, b1x = 0u, b0y = 0u, b1y = 0u;
+#pragma unroll
+                for (int i = 0; i < E; ++i) {
+                    const float2 y2 = v[kx * E + i];
+                    const uint32_t px = pair_code(y2.x, pa, pbc, ptab, mx);
+                    const uint32_t py = pair_code(y2.y, pa, pbc, ptab, my);
+                    if (i & 1) {
+                        b1x = __funnelshift_r(b1x, px, 8);
+                        b1y = __funnelshift_r(b1y, py, 8);
+                    } else {
+                        b0x = __funnelshift_r(b0x, px, 8);
+                        b0y = __funnelshift_r(b0y, py, 8);
+                    }
+                }
+                wa1[kx] = (b0x & 0x0F0F0F0Fu) | ((b1x & 0x0F0F0F0Fu) << 4);
+                wa2[kx] = ((b0x >> 4) & 0x0F0F0F0Fu) | (b1x & 0xF0F0F0F0u);
+                wa1[WL / 2 + kx] = (b0y & 0x0F0F0F0Fu) | ((b1y & 0x0F0F0F0Fu) << 4);
+                wa2[WL / 2 + kx] = ((b0y >> 4) & 0x0F0F0F0Fu) | (b1y & 0xF0F0F0F0u);
+            }
+        } else if constexpr (!ROLLED) {
             // symmetric 1/2-bit books: unrolled, in registers
 #pragma unroll
             for (int kx = 0; kx < WL / 2; ++kx) {
@@ -661,7 +712,7 @@ __global__ void __launch_bounds__(enc_warps(BITS, MODE) * 32, 1)
         while (fl) {
             const int r = __ffs(fl) - 1;
             fl &= fl - 1;
-            rvq_fixup_row<BITS, GRID>(p, sbuf, r, blk * ER + r, lane, tb1, tc1, tb2, tc2, tcen);
+            rvq_fixup_row<BITS, GRID || MODE == MODE_PAIR>(p, sbuf, r, blk * ER + r, lane, tb1, tc1, tb2, tc2, tcen);
         }
         __syncwarp();
 
@@ -933,6 +984,7 @@ cudaError_t launch_rvq_encode(const RvqEncodeParams &p, int bits, int mode, cuda
     case 2 * 4 + MODE_SYM: return launch_enc<2, MODE_SYM>(p, stream);
     case 4 * 4 + MODE_PLAIN: return launch_enc<4, MODE_PLAIN>(p, stream);
     case 4 * 4 + MODE_GRID: return launch_enc<4, MODE_GRID>(p, stream);
+    case 4 * 4 + MODE_PAIR: return launch_enc<4, MODE_PAIR>(p, stream);
     default: return cudaErrorInvalidValue;
     }
 }

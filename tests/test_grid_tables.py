@@ -60,3 +60,42 @@ def test_no_table_when_boundaries_too_close(harness):
     b = np.array([-1.0, 0.0, 1e-7, 1.0], np.float32)  # two boundaries inside one guard band
     rc, out = _run(harness, b)
     assert out == "NOTABLE"
+
+
+def _pair_args(c1, b1, c2, b2):
+    return ["pair", GUARD] + ["%.9g" % float(x) for a in (c1, b1, c2, b2) for x in np.asarray(a, np.float32)]
+
+
+def test_pair_table_for_library_4bit_codebook(harness):
+    """The one-lookup two-stage table of the 4-bit encoder: every looked-up
+    pair outside the guard band equals the exact pair, and no step of the pair
+    function is within the guard band of a value in another cell."""
+    from kv_cache_quantization_turboquantrvq_gb300 import api, build
+    build.build()
+    c1, b1, c2, b2 = api.vq_rvq_codebook(128, 4)
+    r = subprocess.run([harness] + _pair_args(c1, b1, c2, b2), capture_output=True, text=True)
+    assert r.returncode == 0, r.stdout
+    assert r.stdout.startswith("OK") and "steps 163" in r.stdout
+
+
+def test_pair_table_for_scaled_and_perturbed_codebooks(harness):
+    """Other 16-level books (the library's at other dimensions, and randomly
+    perturbed ones): a table is either built and exact, or refused."""
+    from kv_cache_quantization_turboquantrvq_gb300 import api, build
+    build.build()
+    rng = np.random.default_rng(5)
+    built = 0
+    books = [api.vq_rvq_codebook(d, 4) for d in (64, 256)]
+    c1, b1, c2, b2 = api.vq_rvq_codebook(128, 4)
+    for _ in range(6):
+        j1 = np.sort(c1 * rng.uniform(0.97, 1.03, 16)).astype(np.float32)
+        j2 = np.sort(c2 * rng.uniform(0.95, 1.05, 16)).astype(np.float32)
+        books.append((j1, (0.5 * (j1[1:] + j1[:-1])).astype(np.float32), j2,
+                      (0.5 * (j2[1:] + j2[:-1])).astype(np.float32)))
+    for book in books:
+        r = subprocess.run([harness] + _pair_args(*book), capture_output=True, text=True)
+        if r.stdout.strip() == "NOTABLE":
+            continue  # the encoder then uses the two-table quantizer
+        assert r.returncode == 0, r.stdout
+        built += 1
+    assert built >= 6
