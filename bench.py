@@ -456,6 +456,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", choices=("c5", "c3", "c2", "c1", "c4", "attn"), default="c5")
+    ap.add_argument("--graph", action="store_true",
+                    help="also capture the step in a CUDA graph and time its replays "
+                         "(launch-bound workloads: c4, c1); `value` is then the graph's")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--batch", type=int, default=None,
@@ -486,6 +489,9 @@ def main():
     build.build()
     api.lib()  # fails loudly if the CUDA library is missing
 
+    if args.graph:
+        # a graph is captured on a side stream: run the whole bench there
+        torch.cuda.set_stream(torch.cuda.Stream())
     s_run = torch.cuda.Stream()  # e2e kernel stream
     built = build_workload(args.workload, dev, rank, layers=args.layers, batch=args.batch,
                            chunked=not args.no_e2e, chunk_stream=s_run)
@@ -529,6 +535,35 @@ def main():
     step_bytes = sum(o.nbytes for o in ops)
     step_elems = sum(o.nelem for o in ops)
     value = world * step_bytes * K / (elapsed_ms * 1e-3) / 1e9
+
+    # the same step as one CUDA graph (no host work or launch gaps between kernels)
+    graph = None
+    if args.graph:
+        g = torch.cuda.CUDAGraph()
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=stream):
+            step()
+        for _ in range(W):
+            g.replay()
+        torch.cuda.synchronize()
+        assert api.vq_device_error() == 0
+        if world > 1:
+            dist.barrier()
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        g0.record(stream)
+        for _ in range(K):
+            g.replay()
+        g1.record(stream)
+        torch.cuda.synchronize()
+        gms = g0.elapsed_time(g1)
+        if world > 1:
+            tt = torch.tensor([gms], device=dev)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            gms = float(tt.item())
+        graph = {"ms_per_step": round(gms / K, 5),
+                 "eager_value": round(value, 2), "eager_ms_per_step": round(elapsed_ms / K, 5)}
+        elapsed_ms = gms
+        value = world * step_bytes * K / (elapsed_ms * 1e-3) / 1e9
     gelem = world * step_elems * K / (elapsed_ms * 1e-3) / 1e9
 
     # per-op average durations (events on the launching stream)
@@ -643,7 +678,7 @@ def main():
                          "peak_source": peak_src, "unit": "GB/s", "frac": round(ach / peak, 4),
                          "traffic": None if traffic is None else int(traffic),
                          "alg_bytes_per_launch": int(dk["bytes"] / dk["launches"])},
-            "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
+            "cpu_baseline": cpu, "e2e": e2e, "clocks": clk, "graph": graph,
             "gpu_launches": sum(o.gpu_launches for o in ops) * K,
         }
         print(json.dumps(line))
