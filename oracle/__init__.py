@@ -59,9 +59,9 @@ def _load():
     lib.oracle_rvq_codebooks.restype = I
     lib.oracle_pack_lsb_first.argtypes = [P, L, I, P]
     lib.oracle_unpack_lsb_first.argtypes = [P, L, I, P]
-    lib.oracle_rvq_encode.argtypes = [P, L, I, I, P, P, P, P] + [P] * 9
-    lib.oracle_rvq_decode.argtypes = [P, P, P, L, I, I, P, P, P, P]
-    lib.oracle_rvq_attend.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, P, P, D, P, P]
+    lib.oracle_rvq_encode.argtypes = [P, L, I, I, P, P, P, P] + [P] * 10
+    lib.oracle_rvq_decode.argtypes = [P, P, P, L, I, I, P, P, P, P, P]
+    lib.oracle_rvq_attend.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, P, P, D, P, P, P]
     lib.oracle_kivi_quant.argtypes = [P, L, I, I, I, I, I, I, P, P, P, P, P]
     lib.oracle_kivi_dequant.argtypes = [P, P, P, L, I, I, I, I, I, P]
     _lib = lib
@@ -163,8 +163,18 @@ def unpack_lsb_first(words: np.ndarray, n: int, bits: int) -> np.ndarray:
 # ---------------------------------------------------------------- RVQ
 
 
-def rvq_encode(x_f16: np.ndarray, bits: int, c1, b1, c2, b2, want_values: bool = False):
-    """TurboQuantRVQ encode of rows x [..., D] (fp16).
+def _signs(signs, D):
+    """Sign words of the randomised-sign rotation (bit j: coordinate j negated), or None."""
+    if signs is None:
+        return None
+    s = _c(signs, np.uint32).ravel()
+    assert s.size == D // 32
+    return s
+
+
+def rvq_encode(x_f16: np.ndarray, bits: int, c1, b1, c2, b2, want_values: bool = False, signs=None):
+    """TurboQuantRVQ encode of rows x [..., D] (fp16); `signs` (D/32 uint32
+    words) selects the randomised-sign rotation H diag(s).
 
     Returns a dict with packed1, packed2 [N, D*bits/32] uint32, norms [N] fp32,
     idx1, idx2, tie1, tie2 [N, D] uint8 and, when want_values, y and r [N, D]
@@ -186,13 +196,13 @@ def rvq_encode(x_f16: np.ndarray, bits: int, c1, b1, c2, b2, want_values: bool =
     _load().oracle_rvq_encode(_p(x.view(np.uint16)), N, D, bits, *[_p(v) for v in cb],
                               _p(out["idx1"]), _p(out["idx2"]), _p(out["packed1"]),
                               _p(out["packed2"]), _p(out["norms"]), _p(out["tie1"]),
-                              _p(out["tie2"]), _p(y), _p(r))
+                              _p(out["tie2"]), _p(y), _p(r), _p(_signs(signs, D)))
     if want_values:
         out["y"], out["r"] = y, r
     return out
 
 
-def rvq_decode(packed1, packed2, norms, D: int, bits: int, c1, c2, want_f64: bool = False):
+def rvq_decode(packed1, packed2, norms, D: int, bits: int, c1, c2, want_f64: bool = False, signs=None):
     """TurboQuantRVQ unpack + dequant; returns fp16 [N, D] (and binary64 if asked)."""
     p1 = _c(packed1, np.uint32)
     p2 = _c(packed2, np.uint32)
@@ -201,12 +211,13 @@ def rvq_decode(packed1, packed2, norms, D: int, bits: int, c1, c2, want_f64: boo
     out = np.empty((N, D), np.float16)
     f64 = np.empty((N, D), np.float64) if want_f64 else None
     _load().oracle_rvq_decode(_p(p1), _p(p2), _p(n), N, D, bits, _p(_c(c1, np.float32)),
-                              _p(_c(c2, np.float32)), _p(out.view(np.uint16)), _p(f64))
+                              _p(_c(c2, np.float32)), _p(out.view(np.uint16)), _p(f64),
+                              _p(_signs(signs, D)))
     return (out, f64) if want_f64 else out
 
 
 def rvq_attend(q, packed1, packed2, norms, v, bits: int, c1, c2, scale: float, lens=None,
-               want_f64: bool = False):
+               want_f64: bool = False, signs=None):
     """Decode-time attention over an RVQ key cache (see oracle.c).
     q [B, Hq, D] fp16; packed1/2 [B, Hkv, S_cap, W] uint32; norms [B, Hkv, S_cap] fp32;
     v [B, Hkv, S_cap, D] fp16; lens [B] int32 or None.  Returns fp16 [B, Hq, D]
@@ -224,7 +235,7 @@ def rvq_attend(q, packed1, packed2, norms, v, bits: int, c1, c2, scale: float, l
     _load().oracle_rvq_attend(_p(qa.view(np.uint16)), _p(p1), _p(p2), _p(nr), _p(va.view(np.uint16)),
                               None if ln is None else _p(ln), B, Hq, Hkv, S_cap, D, bits,
                               _p(_c(c1, np.float32)), _p(_c(c2, np.float32)), float(scale),
-                              _p(out.view(np.uint16)), _p(f64))
+                              _p(out.view(np.uint16)), _p(f64), _p(_signs(signs, D)))
     return (out, f64) if want_f64 else out
 
 

@@ -108,6 +108,25 @@ void oracle_hadamard_matrix(int D, double *H)
             H[(long)i * D + j] = (popcount_u32((unsigned)(i & j)) & 1) ? -1.0 : 1.0;
 }
 
+/*
+ * The rotation of the randomised-sign variant.  [TQ] "Kernel 3: Fused
+ * Hadamard + Quantize" states TurboQuantMSE's rotation as diag * H * x /
+ * sqrt(D); its kernel listing multiplies each loaded x by diag before the
+ * butterfly, i.e. computes H diag(s) x / sqrt(D).  Reading: the listing's
+ * order, R = H diag(s) (column j of H scaled by s_j), with s_j = -1 when bit
+ * j of signs[j / 32] is set.  signs NULL gives R = H.  R / sqrt(D) is
+ * orthogonal; its inverse is R^T / sqrt(D) = diag(s) H / sqrt(D).
+ */
+static void rotation_matrix(int D, const uint32_t *signs, double *R)
+{
+    oracle_hadamard_matrix(D, R);
+    if (!signs) return;
+    for (int j = 0; j < D; ++j) {
+        if ((signs[j / 32] >> (j % 32)) & 1u)
+            for (int i = 0; i < D; ++i) R[(long)i * D + j] = -R[(long)i * D + j];
+    }
+}
+
 /* ------------------------------------------------------------------------ */
 /* Codebooks.                                                                */
 /* [RVQ] "The pipeline, as it actually runs": stage 1 quantizes against a     */
@@ -291,7 +310,8 @@ void oracle_unpack_lsb_first(const uint32_t *words, long n, int bits, uint8_t *c
 /* [RVQ] "The pipeline, as it actually runs" and "What 'quantize' means      */
 /* here, precisely": for each key row x (D values):                          */
 /*   n = ||x||_2 (kept as the row norm), u = x / n                           */
-/*   y = H u / sqrt(D)                        (rotate)                       */
+/*   y = R u / sqrt(D)                        (rotate; R = H, or H diag(s)    */
+/*                                             for the randomised signs)     */
 /*   i1 = #{k : y > b1_k}                     (stage-1 boundary count)       */
 /*   r = y - c1[i1]                           (dequantize1, residual)        */
 /*   i2 = #{k : r > b2_k}                     (stage-2 boundary count)       */
@@ -307,7 +327,8 @@ void oracle_unpack_lsb_first(const uint32_t *words, long n, int bits, uint8_t *c
 void oracle_rvq_encode(const uint16_t *x_f16, long N, int D, int bits,
                        const float *c1, const float *b1, const float *c2, const float *b2,
                        uint8_t *idx1, uint8_t *idx2, uint32_t *packed1, uint32_t *packed2,
-                       float *norms, uint8_t *tie1, uint8_t *tie2, double *y_out, double *r_out)
+                       float *norms, uint8_t *tie1, uint8_t *tie2, double *y_out, double *r_out,
+                       const uint32_t *signs)
 {
     int L = 1 << bits;
     int W = D * bits / 32;
@@ -315,7 +336,7 @@ void oracle_rvq_encode(const uint16_t *x_f16, long N, int D, int bits,
     double *x = (double *)malloc(sizeof(double) * D);
     double *u = (double *)malloc(sizeof(double) * D);
     uint8_t *q1 = (uint8_t *)malloc(D), *q2 = (uint8_t *)malloc(D);
-    oracle_hadamard_matrix(D, H);
+    rotation_matrix(D, signs, H);
     double inv_sqrt_d = 1.0 / sqrt((double)D);
     for (long row = 0; row < N; ++row) {
         const uint16_t *xr = x_f16 + row * D;
@@ -362,17 +383,19 @@ void oracle_rvq_encode(const uint16_t *x_f16, long N, int D, int bits,
  * decodes a key in the rotated domain as c1[i1] + c2[i2].  Reading: the flush
  * codec returns the original domain, so the rotation is undone (H / sqrt(D) is
  * symmetric and its own inverse) and the stored norm re-applied:
- *   x_hat = n * H (c1[i1] + c2[i2]) / sqrt(D), rounded to binary16.
+ *   x_hat = n * H (c1[i1] + c2[i2]) / sqrt(D), rounded to binary16,
+ * and with the randomised signs the transpose of the encoder's rotation,
+ *   x_hat = n * R^T (c1[i1] + c2[i2]) / sqrt(D),  R = H diag(s).
  */
 void oracle_rvq_decode(const uint32_t *packed1, const uint32_t *packed2, const float *norms,
                        long N, int D, int bits, const float *c1, const float *c2,
-                       uint16_t *out_f16, double *out_f64)
+                       uint16_t *out_f16, double *out_f64, const uint32_t *signs)
 {
     int W = D * bits / 32;
     double *H = (double *)malloc(sizeof(double) * D * D);
     double *yh = (double *)malloc(sizeof(double) * D);
     uint8_t *q1 = (uint8_t *)malloc(D), *q2 = (uint8_t *)malloc(D);
-    oracle_hadamard_matrix(D, H);
+    rotation_matrix(D, signs, H);
     double inv_sqrt_d = 1.0 / sqrt((double)D);
     for (long row = 0; row < N; ++row) {
         oracle_unpack_lsb_first(packed1 + row * W, D, bits, q1);
@@ -381,7 +404,7 @@ void oracle_rvq_decode(const uint32_t *packed1, const uint32_t *packed2, const f
         double n = (double)norms[row];
         for (int j = 0; j < D; ++j) {
             double acc = 0.0;
-            for (int i = 0; i < D; ++i) acc += H[(long)j * D + i] * yh[i];
+            for (int i = 0; i < D; ++i) acc += H[(long)i * D + j] * yh[i];  /* R^T */
             double v = n * acc * inv_sqrt_d;
             if (out_f64) out_f64[row * D + j] = v;
             if (out_f16) out_f16[row * D + j] = oracle_f64_to_f16_rn(v);
@@ -397,7 +420,8 @@ void oracle_rvq_decode(const uint32_t *packed1, const uint32_t *packed2, const f
  * Readings (the pages give the loop, not the interface): one query token per
  * (batch, query head); query head hq reads kv head hq / (Hq / Hkv)
  * (grouped-query attention); a key is the flush codec's decoded row
- *   k_s = n_s * H (c1[i1] + c2[i2]) / sqrt(D)        (original domain)
+ *   k_s = n_s * R^T (c1[i1] + c2[i2]) / sqrt(D)      (original domain;
+ *                                                     R = H or H diag(s))
  * values are fp16; only the first lens[b] tokens of a cache take part
  * (lens NULL: all S_cap); the weights are the exact softmax of
  * scale * (q . k_s); an empty cache gives zeros.  Binary64 throughout, the
@@ -409,7 +433,8 @@ void oracle_rvq_decode(const uint32_t *packed1, const uint32_t *packed2, const f
 void oracle_rvq_attend(const uint16_t *q_f16, const uint32_t *packed1, const uint32_t *packed2,
                        const float *norms, const uint16_t *v_f16, const int32_t *lens, int B,
                        int Hq, int Hkv, int S_cap, int D, int bits, const float *c1,
-                       const float *c2, double scale, uint16_t *out_f16, double *out_f64)
+                       const float *c2, double scale, uint16_t *out_f16, double *out_f64,
+                       const uint32_t *signs)
 {
     int W = D * bits / 32, G = Hq / Hkv;
     double *H = (double *)malloc(sizeof(double) * D * D);
@@ -418,7 +443,7 @@ void oracle_rvq_attend(const uint16_t *q_f16, const uint32_t *packed1, const uin
     double *sc = (double *)malloc(sizeof(double) * (S_cap > 0 ? S_cap : 1));
     double *acc = (double *)malloc(sizeof(double) * D);
     uint8_t *q1 = (uint8_t *)malloc(D), *q2 = (uint8_t *)malloc(D);
-    oracle_hadamard_matrix(D, H);
+    rotation_matrix(D, signs, H);
     double inv_sqrt_d = 1.0 / sqrt((double)D);
     for (int b = 0; b < B; ++b) {
         int len = lens ? lens[b] : S_cap;
@@ -433,7 +458,7 @@ void oracle_rvq_attend(const uint16_t *q_f16, const uint32_t *packed1, const uin
                 double n = (double)norms[base + s];
                 for (int j = 0; j < D; ++j) {
                     double a = 0.0;
-                    for (int i = 0; i < D; ++i) a += H[(long)j * D + i] * yh[i];
+                    for (int i = 0; i < D; ++i) a += H[(long)i * D + j] * yh[i];  /* R^T */
                     K[(long)s * D + j] = n * a * inv_sqrt_d;
                 }
             }
