@@ -186,6 +186,34 @@ vq_status vq_rvq_attend_noalloc(const void *q_f16, const uint32_t *packed1, cons
                                 const float *c2, float scale, void *out_f16, vq_stream_t stream);
 
 /*
+ * Randomised-sign rotation (turboquant page, "Kernel 3: Fused Hadamard +
+ * Quantize": TurboQuantMSE's randomized Hadamard preconditioner).  The
+ * page's formula reads diag * H * x / sqrt(D) while its kernel flips the
+ * signs of x on load and then runs the butterfly; these calls follow the
+ * kernel: the rotation is H diag(s) / sqrt(D), with s_j = -1 when bit j of
+ * signs[j / 32] is set.  Decode and attention use its transpose
+ * diag(s) H / sqrt(D) (keys k = n diag(s) H (c1[i1] + c2[i2]) / sqrt(D); the
+ * query is rotated by H diag(s) / sqrt(D)).  signs: host, D/32 uint32 words,
+ * chosen by the caller (e.g. from a seed), the same for encode, decode and
+ * attention of one cache.  All-zero signs give the plain calls' results bit
+ * for bit.  Arguments, layouts and errors otherwise as the plain calls;
+ * signs == NULL is VQ_ERR_INVALID_ARG.
+ */
+vq_status vq_rvq_encode_pack_rs(const void *k_f16, int B, int H, int S, int D, int bits,
+                                const float *c1, const float *b1, const float *c2, const float *b2,
+                                uint32_t *packed1, uint32_t *packed2, float *norms,
+                                const int32_t *dst_off, int S_dst, const uint32_t *signs,
+                                vq_stream_t stream);
+vq_status vq_rvq_unpack_dequant_rs(const uint32_t *packed1, const uint32_t *packed2, const float *norms,
+                                   int B, int H, int S, int D, int bits, const float *c1, const float *c2,
+                                   const uint32_t *signs, void *out_f16, vq_stream_t stream);
+vq_status vq_rvq_attend_rs(const void *q_f16, const uint32_t *packed1, const uint32_t *packed2,
+                           const float *norms, const void *v_f16, const int32_t *lens, int B, int Hq,
+                           int Hkv, int S_cap, int D, int bits, const float *c1, const float *c2,
+                           const uint32_t *signs, float scale, void *out_f16, void *workspace,
+                           size_t workspace_bytes, vq_stream_t stream);
+
+/*
  * vq_kivi_quant_pack - KIVI flush of K and/or V (either may be NULL, with its
  * outputs).  Quantizes tokens [0, S_q), S_q = S - residual_length; tokens
  * [S_q, S) are the fp16 residual window and are not read or written.

@@ -29,7 +29,8 @@ VQ_DEVERR_BAD_OFFSET = 0x2
 
 EXPORTED = ("vq_status_str", "vq_version", "vq_rvq_codebook", "vq_rvq_encode_pack",
             "vq_rvq_unpack_dequant", "vq_kivi_quant_pack", "vq_kivi_unpack_dequant",
-            "vq_device_error", "vq_rvq_attend_workspace", "vq_rvq_attend", "vq_rvq_attend_noalloc")
+            "vq_device_error", "vq_rvq_attend_workspace", "vq_rvq_attend", "vq_rvq_attend_noalloc",
+            "vq_rvq_encode_pack_rs", "vq_rvq_unpack_dequant_rs", "vq_rvq_attend_rs")
 VQ_ATTEND_SCRATCH_BYTES = 16 * 1024 * 1024
 
 
@@ -62,6 +63,10 @@ def lib():
     L.vq_rvq_attend.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, P, P, ctypes.c_float, P, P,
                                 ctypes.c_size_t, P]
     L.vq_rvq_attend_noalloc.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, P, P, ctypes.c_float, P, P]
+    L.vq_rvq_encode_pack_rs.argtypes = [P, I, I, I, I, I, P, P, P, P, P, P, P, P, I, P, P]
+    L.vq_rvq_unpack_dequant_rs.argtypes = [P, P, P, I, I, I, I, I, P, P, P, P, P]
+    L.vq_rvq_attend_rs.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, P, P, P, ctypes.c_float, P, P,
+                                   ctypes.c_size_t, P]
     for name in EXPORTED[2:]:
         getattr(L, name).restype = I
     _lib = L
@@ -111,9 +116,17 @@ def vq_rvq_codebook(D: int, bits: int):
     return c1, b1, c2, b2
 
 
+def _sign_words(signs):
+    s = np.ascontiguousarray(np.asarray(signs, dtype=np.uint32).ravel())
+    if s.size != 4:
+        raise ValueError("signs: 4 uint32 words (one bit per coordinate of D = 128)")
+    return s
+
+
 def vq_rvq_encode_pack(k, bits: int, c1, b1, c2, b2, packed1=None, packed2=None, norms=None,
-                       dst_off=None, S_dst=None, stream=None):
-    """Encode fp16 keys k [B, H, S, D] into (packed1, packed2, norms)."""
+                       dst_off=None, S_dst=None, stream=None, signs=None):
+    """Encode fp16 keys k [B, H, S, D] into (packed1, packed2, norms); with
+    `signs` (4 uint32 words) the randomised-sign rotation H diag(s)."""
     import torch
     B, H, S, D = k.shape
     S_dst = S if S_dst is None else S_dst
@@ -125,13 +138,20 @@ def vq_rvq_encode_pack(k, bits: int, c1, b1, c2, b2, packed1=None, packed2=None,
     if norms is None:
         norms = torch.empty((B, H, S_dst), dtype=torch.float32, device=k.device)
     keep = [_host(v) for v in (c1, b1, c2, b2)]
-    _check(lib().vq_rvq_encode_pack(_ptr(k), B, H, S, D, bits, *[p for _, p in keep],
-                                    _ptr(packed1), _ptr(packed2), _ptr(norms), _ptr(dst_off),
-                                    S_dst, _stream(stream)), "vq_rvq_encode_pack")
+    if signs is None:
+        _check(lib().vq_rvq_encode_pack(_ptr(k), B, H, S, D, bits, *[p for _, p in keep],
+                                        _ptr(packed1), _ptr(packed2), _ptr(norms), _ptr(dst_off),
+                                        S_dst, _stream(stream)), "vq_rvq_encode_pack")
+    else:
+        sw = _sign_words(signs)
+        _check(lib().vq_rvq_encode_pack_rs(_ptr(k), B, H, S, D, bits, *[p for _, p in keep],
+                                           _ptr(packed1), _ptr(packed2), _ptr(norms), _ptr(dst_off),
+                                           S_dst, sw.ctypes.data_as(ctypes.c_void_p), _stream(stream)),
+               "vq_rvq_encode_pack_rs")
     return packed1, packed2, norms
 
 
-def vq_rvq_unpack_dequant(packed1, packed2, norms, bits: int, c1, c2, out=None, stream=None):
+def vq_rvq_unpack_dequant(packed1, packed2, norms, bits: int, c1, c2, out=None, stream=None, signs=None):
     """Decode (packed1, packed2, norms) [B, H, S, ...] back to fp16 keys [B, H, S, 128]."""
     import torch
     B, H, S, _ = packed1.shape
@@ -139,9 +159,15 @@ def vq_rvq_unpack_dequant(packed1, packed2, norms, bits: int, c1, c2, out=None, 
     if out is None:
         out = torch.empty((B, H, S, D), dtype=torch.float16, device=packed1.device)
     keep = [_host(v) for v in (c1, c2)]
-    _check(lib().vq_rvq_unpack_dequant(_ptr(packed1), _ptr(packed2), _ptr(norms), B, H, S, D, bits,
-                                       keep[0][1], keep[1][1], _ptr(out), _stream(stream)),
-           "vq_rvq_unpack_dequant")
+    if signs is None:
+        _check(lib().vq_rvq_unpack_dequant(_ptr(packed1), _ptr(packed2), _ptr(norms), B, H, S, D, bits,
+                                           keep[0][1], keep[1][1], _ptr(out), _stream(stream)),
+               "vq_rvq_unpack_dequant")
+    else:
+        sw = _sign_words(signs)
+        _check(lib().vq_rvq_unpack_dequant_rs(_ptr(packed1), _ptr(packed2), _ptr(norms), B, H, S, D, bits,
+                                              keep[0][1], keep[1][1], sw.ctypes.data_as(ctypes.c_void_p),
+                                              _ptr(out), _stream(stream)), "vq_rvq_unpack_dequant_rs")
     return out
 
 
@@ -162,7 +188,7 @@ def vq_rvq_attend_workspace(B: int, Hq: int, Hkv: int, S_cap: int) -> int:
 
 
 def vq_rvq_attend(q, packed1, packed2, norms, v, bits: int, c1, c2, scale: float, lens=None, out=None,
-                  workspace=None, stream=None):
+                  workspace=None, stream=None, signs=None):
     """Decode-time attention of q [B, Hq, 128] over an RVQ key cache
     (packed1, packed2, norms [B, Hkv, S_cap, ...]) and fp16 values v
     [B, Hkv, S_cap, 128]; lens [B] int32 (device) or None.  Returns fp16
@@ -177,9 +203,16 @@ def vq_rvq_attend(q, packed1, packed2, norms, v, bits: int, c1, c2, scale: float
         workspace = torch.empty((max(nbytes, 16) + 3) // 4, dtype=torch.float32, device=q.device)
     wbytes = workspace.numel() * workspace.element_size()
     keep = [_host(t) for t in (c1, c2)]
-    _check(lib().vq_rvq_attend(_ptr(q), _ptr(packed1), _ptr(packed2), _ptr(norms), _ptr(v), _ptr(lens),
-                               B, Hq, Hkv, S_cap, D, bits, keep[0][1], keep[1][1], float(scale), _ptr(out),
-                               _ptr(workspace), wbytes, _stream(stream)), "vq_rvq_attend")
+    if signs is None:
+        _check(lib().vq_rvq_attend(_ptr(q), _ptr(packed1), _ptr(packed2), _ptr(norms), _ptr(v), _ptr(lens),
+                                   B, Hq, Hkv, S_cap, D, bits, keep[0][1], keep[1][1], float(scale),
+                                   _ptr(out), _ptr(workspace), wbytes, _stream(stream)), "vq_rvq_attend")
+    else:
+        sw = _sign_words(signs)
+        _check(lib().vq_rvq_attend_rs(_ptr(q), _ptr(packed1), _ptr(packed2), _ptr(norms), _ptr(v), _ptr(lens),
+                                      B, Hq, Hkv, S_cap, D, bits, keep[0][1], keep[1][1],
+                                      sw.ctypes.data_as(ctypes.c_void_p), float(scale), _ptr(out),
+                                      _ptr(workspace), wbytes, _stream(stream)), "vq_rvq_attend_rs")
     return out
 
 

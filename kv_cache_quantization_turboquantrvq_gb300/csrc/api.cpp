@@ -62,6 +62,18 @@ bool symmetric_codebook(const float *c, const float *b, int L)
     return b[L / 2 - 1] == 0.0f;
 }
 
+// The randomised-sign rotation's sign words (bit j: coordinate j negated), or
+// none; the kernels apply them only when has_sgn is set.
+template <class P>
+void set_signs(P &p, const uint32_t *signs)
+{
+    p.has_sgn = 0;
+    for (int i = 0; i < 4; ++i) {
+        p.sgn[i] = signs ? signs[i] : 0u;
+        if (p.sgn[i]) p.has_sgn = 1;
+    }
+}
+
 }  // namespace
 
 int sm_count()
@@ -116,10 +128,11 @@ vq_status vq_rvq_codebook(int D, int bits, float *c1, float *b1, float *c2, floa
     return VQ_OK;
 }
 
-vq_status vq_rvq_encode_pack(const void *k_f16, int B, int H, int S, int D, int bits,
-                             const float *c1, const float *b1, const float *c2, const float *b2,
-                             uint32_t *packed1, uint32_t *packed2, float *norms,
-                             const int32_t *dst_off, int S_dst, vq_stream_t stream)
+static vq_status rvq_encode_impl(const void *k_f16, int B, int H, int S, int D, int bits,
+                                 const float *c1, const float *b1, const float *c2, const float *b2,
+                                 uint32_t *packed1, uint32_t *packed2, float *norms,
+                                 const int32_t *dst_off, int S_dst, const uint32_t *signs,
+                                 vq_stream_t stream)
 {
     if (B < 0 || H < 0 || S < 0) return VQ_ERR_INVALID_ARG;
     if (bits == 3 || (D != kD && D > 0)) return VQ_ERR_UNSUPPORTED;
@@ -171,12 +184,33 @@ vq_status vq_rvq_encode_pack(const void *k_f16, int B, int H, int S, int D, int 
         // the shuffle tables also serve the exact recompute of the pair mode
         mode = bits == 4 && build_pair_table(c1, b1, c2, b2, bits, kGuard, p.pt) ? RVQ_MODE_PAIR
                                                                                  : RVQ_MODE_GRID;
+    set_signs(p, signs);
     return cuda_status(launch_rvq_encode(p, bits, mode, reinterpret_cast<cudaStream_t>(stream)));
 }
 
-vq_status vq_rvq_unpack_dequant(const uint32_t *packed1, const uint32_t *packed2, const float *norms,
-                                int B, int H, int S, int D, int bits, const float *c1, const float *c2,
-                                void *out_f16, vq_stream_t stream)
+vq_status vq_rvq_encode_pack(const void *k_f16, int B, int H, int S, int D, int bits,
+                             const float *c1, const float *b1, const float *c2, const float *b2,
+                             uint32_t *packed1, uint32_t *packed2, float *norms,
+                             const int32_t *dst_off, int S_dst, vq_stream_t stream)
+{
+    return rvq_encode_impl(k_f16, B, H, S, D, bits, c1, b1, c2, b2, packed1, packed2, norms, dst_off, S_dst,
+                           nullptr, stream);
+}
+
+vq_status vq_rvq_encode_pack_rs(const void *k_f16, int B, int H, int S, int D, int bits,
+                                const float *c1, const float *b1, const float *c2, const float *b2,
+                                uint32_t *packed1, uint32_t *packed2, float *norms,
+                                const int32_t *dst_off, int S_dst, const uint32_t *signs,
+                                vq_stream_t stream)
+{
+    if (!signs) return VQ_ERR_INVALID_ARG;
+    return rvq_encode_impl(k_f16, B, H, S, D, bits, c1, b1, c2, b2, packed1, packed2, norms, dst_off, S_dst,
+                           signs, stream);
+}
+
+static vq_status rvq_decode_impl(const uint32_t *packed1, const uint32_t *packed2, const float *norms,
+                                 int B, int H, int S, int D, int bits, const float *c1, const float *c2,
+                                 void *out_f16, const uint32_t *signs, vq_stream_t stream)
 {
     if (B < 0 || H < 0 || S < 0) return VQ_ERR_INVALID_ARG;
     if (bits == 3 || (D != kD && D > 0)) return VQ_ERR_UNSUPPORTED;
@@ -207,7 +241,23 @@ vq_status vq_rvq_unpack_dequant(const uint32_t *packed1, const uint32_t *packed2
         p.c1[k] = k < L ? c1[k] : 0.0f;
         p.c2[k] = k < L ? c2[k] : 0.0f;
     }
+    set_signs(p, signs);
     return cuda_status(launch_rvq_decode(p, bits, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+vq_status vq_rvq_unpack_dequant(const uint32_t *packed1, const uint32_t *packed2, const float *norms,
+                                int B, int H, int S, int D, int bits, const float *c1, const float *c2,
+                                void *out_f16, vq_stream_t stream)
+{
+    return rvq_decode_impl(packed1, packed2, norms, B, H, S, D, bits, c1, c2, out_f16, nullptr, stream);
+}
+
+vq_status vq_rvq_unpack_dequant_rs(const uint32_t *packed1, const uint32_t *packed2, const float *norms,
+                                   int B, int H, int S, int D, int bits, const float *c1, const float *c2,
+                                   const uint32_t *signs, void *out_f16, vq_stream_t stream)
+{
+    if (!signs) return VQ_ERR_INVALID_ARG;
+    return rvq_decode_impl(packed1, packed2, norms, B, H, S, D, bits, c1, c2, out_f16, signs, stream);
 }
 
 static size_t attend_ws_bytes(int B, int Hq, int nsplit)
@@ -242,7 +292,8 @@ static vq_status rvq_attend_impl(const void *q_f16, const uint32_t *packed1, con
                                  const float *norms, const void *v_f16, const int32_t *lens, int B,
                                  int Hq, int Hkv, int S_cap, int D, int bits, const float *c1,
                                  const float *c2, float scale, void *out_f16, void *workspace,
-                                 size_t workspace_bytes, bool static_scratch, vq_stream_t stream)
+                                 size_t workspace_bytes, bool static_scratch, const uint32_t *signs,
+                                 vq_stream_t stream)
 {
     vq_status st = attend_shape_check(B, Hq, Hkv, S_cap);
     if (st != VQ_OK) return st;
@@ -304,6 +355,7 @@ static vq_status rvq_attend_impl(const void *q_f16, const uint32_t *packed1, con
         p.c1[k] = k < L ? c1[k] : 0.0f;
         p.c2[k] = k < L ? c2[k] : 0.0f;
     }
+    set_signs(p, signs);
     return cuda_status(launch_rvq_attend(p, bits, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -314,7 +366,18 @@ vq_status vq_rvq_attend(const void *q_f16, const uint32_t *packed1, const uint32
                         vq_stream_t stream)
 {
     return rvq_attend_impl(q_f16, packed1, packed2, norms, v_f16, lens, B, Hq, Hkv, S_cap, D, bits, c1, c2,
-                           scale, out_f16, workspace, workspace_bytes, false, stream);
+                           scale, out_f16, workspace, workspace_bytes, false, nullptr, stream);
+}
+
+vq_status vq_rvq_attend_rs(const void *q_f16, const uint32_t *packed1, const uint32_t *packed2,
+                           const float *norms, const void *v_f16, const int32_t *lens, int B, int Hq,
+                           int Hkv, int S_cap, int D, int bits, const float *c1, const float *c2,
+                           const uint32_t *signs, float scale, void *out_f16, void *workspace,
+                           size_t workspace_bytes, vq_stream_t stream)
+{
+    if (!signs) return VQ_ERR_INVALID_ARG;
+    return rvq_attend_impl(q_f16, packed1, packed2, norms, v_f16, lens, B, Hq, Hkv, S_cap, D, bits, c1, c2,
+                           scale, out_f16, workspace, workspace_bytes, false, signs, stream);
 }
 
 vq_status vq_rvq_attend_noalloc(const void *q_f16, const uint32_t *packed1, const uint32_t *packed2,
@@ -323,7 +386,7 @@ vq_status vq_rvq_attend_noalloc(const void *q_f16, const uint32_t *packed1, cons
                                 const float *c2, float scale, void *out_f16, vq_stream_t stream)
 {
     return rvq_attend_impl(q_f16, packed1, packed2, norms, v_f16, lens, B, Hq, Hkv, S_cap, D, bits, c1, c2,
-                           scale, out_f16, nullptr, 0, true, stream);
+                           scale, out_f16, nullptr, 0, true, nullptr, stream);
 }
 
 static vq_status kivi_common_check(int B, int H, int D, int bits, int group)

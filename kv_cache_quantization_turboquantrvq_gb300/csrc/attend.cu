@@ -207,7 +207,12 @@ __global__ void __launch_bounds__(AT_WARPS * 32, 1) rvq_attend_kernel(const __gr
     // rotated, pre-scaled query of the GQ heads: warp g transforms head g
     if (warp < GQ) {
         const __half *qh = static_cast<const __half *>(p.q) + ((size_t)b * p.Hq + (size_t)h * GQ + warp) * D;
-        const uint2 raw = *reinterpret_cast<const uint2 *>(qh + 4 * lane);
+        uint2 raw = *reinterpret_cast<const uint2 *>(qh + 4 * lane);
+        if (p.has_sgn) {
+            // randomised signs: the query is rotated by H diag(s) like the keys
+            raw.x ^= half2_sign_mask(sign_pair(p.sgn, 4 * lane));
+            raw.y ^= half2_sign_mask(sign_pair(p.sgn, 4 * lane + 2));
+        }
         const __half2 h01 = *reinterpret_cast<const __half2 *>(&raw.x);
         const __half2 h23 = *reinterpret_cast<const __half2 *>(&raw.y);
         float a[4] = {__low2float(h01), __high2float(h01), __low2float(h23), __high2float(h23)};

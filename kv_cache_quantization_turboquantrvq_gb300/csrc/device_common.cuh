@@ -21,6 +21,19 @@ constexpr uint64_t MBAR_TIMEOUT_NS = 2000000000ull;
 // One device error word per translation unit; each .cu exposes a host reader.
 #define VQ_DEFINE_ERROR_WORD(name) static __device__ unsigned int name = 0u
 
+// Sign-flip mask of one fp16 pair: bit 0 of `two` flips the low half (bit 15),
+// bit 1 the high half (bit 31).  Used for the randomised-sign rotation.
+__host__ __device__ __forceinline__ uint32_t half2_sign_mask(uint32_t two)
+{
+    return ((two & 1u) << 15) | ((two & 2u) << 30);
+}
+
+// The two sign bits of coordinates c, c + 1 (c even) from sign words s[4].
+__host__ __device__ __forceinline__ uint32_t sign_pair(const uint32_t *s, int c)
+{
+    return (s[c >> 5] >> (c & 31)) & 3u;
+}
+
 __device__ __forceinline__ uint32_t smem_u32(const void *p)
 {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));

@@ -75,6 +75,8 @@ struct RvqEncodeParams {
     float guard;         // |y - boundary| below this sends the row to the exact path
     GridTable t1, t2;
     float c1[16], c2[16], b1[16], b2[16];
+    uint32_t sgn[4];  // randomised-sign rotation H diag(s): bit j negates coordinate j
+    int has_sgn;
     PairTable pt;  // RVQ_MODE_PAIR only
 };
 
@@ -84,6 +86,8 @@ struct RvqDecodeParams {
     void *out;           // fp16 [N, 128]
     int N;
     float c1[16], c2[16];
+    uint32_t sgn[4];     // inverse of the randomised-sign rotation: diag(s) H
+    int has_sgn;
 };
 
 struct KiviQuantParams {
@@ -117,6 +121,8 @@ struct RvqAttendParams {
     int nsplit, chunk;             // chunks per (sequence, kv head) and keys per chunk
     float qscale;                  // softmax scale * log2(e) / sqrt(128)
     float c1[16], c2[16];
+    uint32_t sgn[4];               // randomised-sign rotation of the cache (the query is
+    int has_sgn;                   // rotated by H diag(s) too)
 };
 // Chunking of the keys: the default plan, and the finest one that fits
 // `max_splits` partials per (sequence, query head) in a workspace.

@@ -74,15 +74,18 @@ __host__ __device__ constexpr int enc_tab_bytes(int mode)
 {
     return mode == MODE_GRID ? ENC_TAB_BYTES : (mode == MODE_PAIR ? PT_CELLS * 8 : 0);
 }
+// sign masks of the randomised rotation (2 halves x 8 chunks x 16 B), padded so
+// that the TMA rings after them stay 1024-byte aligned (128-byte swizzle)
+constexpr int ENC_SGN_BYTES = 1024;
 __host__ __device__ constexpr int enc_warps(int bits, int mode)
 {
-    return (SMEM_MAX - 1024 - enc_tab_bytes(mode)) / enc_warp_bytes(bits, mode) > 16
+    return (SMEM_MAX - 1024 - enc_tab_bytes(mode) - ENC_SGN_BYTES) / enc_warp_bytes(bits, mode) > 16
                ? 16
-               : (SMEM_MAX - 1024 - enc_tab_bytes(mode)) / enc_warp_bytes(bits, mode);
+               : (SMEM_MAX - 1024 - enc_tab_bytes(mode) - ENC_SGN_BYTES) / enc_warp_bytes(bits, mode);
 }
 __host__ __device__ constexpr int enc_smem(int bits, int mode)
 {
-    return 1024 + enc_tab_bytes(mode) + enc_warps(bits, mode) * enc_warp_bytes(bits, mode);
+    return 1024 + enc_tab_bytes(mode) + ENC_SGN_BYTES + enc_warps(bits, mode) * enc_warp_bytes(bits, mode);
 }
 
 // sqrt(128) = 8 sqrt(2) as a double-float (nearest fp32 + fp32 remainder).
@@ -299,8 +302,12 @@ __device__ __noinline__ void rvq_fixup_row(const RvqEncodeParams &p, const unsig
     constexpr int W = D * BITS / 32;
     constexpr int LPW = E / 4;  // lanes per packed word
     // x[4l .. 4l+3]: box l >> 4, 16-byte chunk (l & 15) >> 1, half (l & 1)
-    const uint2 raw = *reinterpret_cast<const uint2 *>(sblk + (lane >> 4) * (ENC_BLOCK / 2) +
-                                                       swz128(r, (lane & 15) >> 1) + 8 * (lane & 1));
+    uint2 raw = *reinterpret_cast<const uint2 *>(sblk + (lane >> 4) * (ENC_BLOCK / 2) +
+                                                 swz128(r, (lane & 15) >> 1) + 8 * (lane & 1));
+    if (p.has_sgn) {
+        raw.x ^= half2_sign_mask(sign_pair(p.sgn, 4 * lane));
+        raw.y ^= half2_sign_mask(sign_pair(p.sgn, 4 * lane + 2));
+    }
     const __half2 h01 = *reinterpret_cast<const __half2 *>(&raw.x);
     const __half2 h23 = *reinterpret_cast<const __half2 *>(&raw.y);
     float x[4] = {__low2float(h01), __high2float(h01), __low2float(h23), __high2float(h23)};
@@ -418,7 +425,8 @@ __global__ void __launch_bounds__(enc_warps(BITS, MODE) * 32, 1)
     constexpr int PP = enc_pairs(BITS);
     extern __shared__ __align__(128) unsigned char smem_raw[];
     unsigned char *stab = smem_1k(smem_raw);       // cell tables (GRID), pair table (PAIR)
-    unsigned char *smem = stab + enc_tab_bytes(MODE);
+    uint4 *ssg = reinterpret_cast<uint4 *>(stab + enc_tab_bytes(MODE));  // sign masks
+    unsigned char *smem = stab + enc_tab_bytes(MODE) + ENC_SGN_BYTES;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int rr = lane & 15, hh = lane >> 4;
@@ -461,8 +469,14 @@ __global__ void __launch_bounds__(enc_warps(BITS, MODE) * 32, 1)
     if constexpr (MODE == MODE_PAIR) {
         uint2 *pt = reinterpret_cast<uint2 *>(stab);
         for (int i = threadIdx.x; i < PT_CELLS; i += blockDim.x) pt[i] = p.pt.ent[i];
-        __syncthreads();
     }
+    if (threadIdx.x < 16) {
+        // chunk t & 7 (8 coordinates) of half t >> 3: coordinates 64 (t >> 3) + 8 (t & 7) ..
+        const int c0 = 64 * (threadIdx.x >> 3) + 8 * (threadIdx.x & 7);
+        ssg[threadIdx.x] = make_uint4(half2_sign_mask(sign_pair(p.sgn, c0)), half2_sign_mask(sign_pair(p.sgn, c0 + 2)),
+                                      half2_sign_mask(sign_pair(p.sgn, c0 + 4)), half2_sign_mask(sign_pair(p.sgn, c0 + 6)));
+    }
+    __syncthreads();
     // this lane's table columns: entry g at g * 512 (stage 1) / g * 256 (stage 2)
     const unsigned char *t1l = stab + lane * 16;
     const unsigned char *t2l = stab + 32 * 32 * 16 + lane * 8;
@@ -513,8 +527,14 @@ __global__ void __launch_bounds__(enc_warps(BITS, MODE) * 32, 1)
             const unsigned char *src = sbuf + hh * (ENC_BLOCK / 2);
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
-                const uint4 la = *reinterpret_cast<const uint4 *>(src + swz128(rr, c));
-                const uint4 lb = *reinterpret_cast<const uint4 *>(src + swz128(rr, c + 4));
+                uint4 la = *reinterpret_cast<const uint4 *>(src + swz128(rr, c));
+                uint4 lb = *reinterpret_cast<const uint4 *>(src + swz128(rr, c + 4));
+                if (p.has_sgn) {
+                    // randomised signs: x -> diag(s) x on the fp16 bits
+                    const uint4 ma = ssg[hh * 8 + c], mb = ssg[hh * 8 + c + 4];
+                    la = make_uint4(la.x ^ ma.x, la.y ^ ma.y, la.z ^ ma.z, la.w ^ ma.w);
+                    lb = make_uint4(lb.x ^ mb.x, lb.y ^ mb.y, lb.z ^ mb.z, lb.w ^ mb.w);
+                }
                 const __half *pa = reinterpret_cast<const __half *>(&la);
                 const __half *pb = reinterpret_cast<const __half *>(&lb);
 #pragma unroll
@@ -749,7 +769,8 @@ __host__ __device__ constexpr int dec_warp_bytes(int bits) { return DEC_STAGES *
 __host__ __device__ constexpr int dec_table_bytes(int bits) { return bits == 4 ? 256 * 32 * 4 : 0; }
 __host__ __device__ constexpr int dec_smem(int bits)
 {
-    return dec_table_bytes(bits) + DEC_WARPS * (dec_warp_bytes(bits) + DEC_STAGES * 8);
+    // + 256 B: sign masks of the randomised rotation (64 pair words)
+    return dec_table_bytes(bits) + DEC_WARPS * (dec_warp_bytes(bits) + DEC_STAGES * 8) + 256;
 }
 
 // Decoded values c1[i1] + c2[i2] of the 64 coordinates of one half row, as 32
@@ -810,6 +831,8 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) rvq_decode_kernel(const __g
     unsigned char *wbuf = smem + dec_table_bytes(BITS) + warp * WB;
     unsigned char *obuf = wbuf + DEC_STAGES * STG;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + dec_table_bytes(BITS) + DEC_WARPS * WB) + warp * DEC_STAGES;
+    // sign masks: word hh * 32 + k flips output coordinates 64 hh + 2k, 64 hh + 2k + 1
+    uint32_t *sgm = reinterpret_cast<uint32_t *>(smem + dec_table_bytes(BITS) + DEC_WARPS * (WB + DEC_STAGES * 8));
     if (lane == 0) {
 #pragma unroll
         for (int s = 0; s < DEC_STAGES; ++s) mbar_init(&bars[s], 1);
@@ -820,8 +843,9 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) rvq_decode_kernel(const __g
             const int e = i >> 5;
             stab[i] = p.c1[e & 15] + p.c2[e >> 4];
         }
-        __syncthreads();
     }
+    if (threadIdx.x < 64) sgm[threadIdx.x] = half2_sign_mask(sign_pair(p.sgn, 2 * threadIdx.x));
+    __syncthreads();
     __syncwarp();
     const uint64_t pol = l2_policy_evict_first();
     // tables: per-stage (replicated every 2^BITS lanes) and merged (index
@@ -910,7 +934,19 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) rvq_decode_kernel(const __g
             const __half2 hx = __floats2half2_rn(x2.x, x2.y);
             o[k] = *reinterpret_cast<const uint32_t *>(&hx);
         }
-        // o[k] holds coordinates 2k, 2k + 1 of the half
+        // o[k] holds coordinates 2k, 2k + 1 of the half; randomised signs:
+        // x_hat -> diag(s) x_hat on the fp16 bits
+        if (p.has_sgn) {
+            const uint4 *m4 = reinterpret_cast<const uint4 *>(sgm + hh * 32);
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const uint4 m = m4[c];
+                o[4 * c] ^= m.x;
+                o[4 * c + 1] ^= m.y;
+                o[4 * c + 2] ^= m.z;
+                o[4 * c + 3] ^= m.w;
+            }
+        }
         uint4 *orow = reinterpret_cast<uint4 *>(obuf + rr * ROW_STRIDE + hh * 128);
 #pragma unroll
         for (int c = 0; c < 8; ++c) orow[c] = make_uint4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
