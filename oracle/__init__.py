@@ -64,6 +64,7 @@ def _load():
     lib.oracle_rvq_attend.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, P, P, D, P, P, P]
     lib.oracle_kivi_quant.argtypes = [P, L, I, I, I, I, I, I, P, P, P, P, P]
     lib.oracle_kivi_dequant.argtypes = [P, P, P, L, I, I, I, I, I, P]
+    lib.oracle_kivi_attend.argtypes = [P] * 11 + [I] * 8 + [D, P, P]
     _lib = lib
     return lib
 
@@ -286,3 +287,32 @@ def kivi_dequant(packed, scale_f16, zero_f16, BH: int, S_q: int, D: int, bits: i
                                 D, bits, group, 1 if per_channel else 0,
                                 _p(out.view(np.uint16)))
     return out
+
+
+def kivi_attend(q, k_packed, k_scale, k_zero, v_packed, v_scale, v_zero, bits: int, group: int,
+                scale: float, k_res=None, v_res=None, lens=None, res_lens=None, want_f64: bool = False):
+    """Decode-time attention over a KIVI cache with the dequantization inside
+    the attention (see oracle.c).  q [B, Hq, D] fp16; k_packed
+    [B, Hkv, NG, G*b/32, D] uint32, k_scale/k_zero [B, Hkv, NG, D] fp16;
+    v_packed [B, Hkv, S_cap, D*b/32], v_scale/v_zero [B, Hkv, S_cap, D/G];
+    k_res, v_res [B, Hkv, R, D] fp16 or None; lens, res_lens [B] int32 or None.
+    Returns fp16 [B, Hq, D] (and binary64 if asked)."""
+    qa = _c(q, np.float16)
+    B, Hq, D = qa.shape
+    vp = _c(v_packed, np.uint32)
+    _, Hkv, S_cap, _ = vp.shape
+    kp = _c(k_packed, np.uint32)
+    ks, kz = _c(k_scale, np.float16), _c(k_zero, np.float16)
+    vs, vz = _c(v_scale, np.float16), _c(v_zero, np.float16)
+    R = 0 if k_res is None else k_res.shape[2]
+    kr = None if k_res is None else _c(k_res, np.float16)
+    vr = None if v_res is None else _c(v_res, np.float16)
+    ln = None if lens is None else _c(lens, np.int32)
+    rl = None if res_lens is None else _c(res_lens, np.int32)
+    out = np.empty((B, Hq, D), np.float16)
+    f64 = np.empty((B, Hq, D), np.float64) if want_f64 else None
+    h16 = lambda a: None if a is None else _p(a.view(np.uint16))
+    _load().oracle_kivi_attend(h16(qa), _p(kp), h16(ks), h16(kz), _p(vp), h16(vs), h16(vz), h16(kr), h16(vr),
+                               _p(ln), _p(rl), B, Hq, Hkv, S_cap, R, D, bits, group, float(scale),
+                               _p(out.view(np.uint16)), _p(f64))
+    return (out, f64) if want_f64 else out

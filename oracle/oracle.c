@@ -671,3 +671,93 @@ void oracle_kivi_dequant(const uint32_t *packed, const uint16_t *scale_h, const 
             }
     }
 }
+
+/*
+ * Decode-time attention over a KIVI cache with dequantization inside the
+ * attention ([KIVI] first post, closing section: "Dequant-in-SDPA - teach
+ * attention to read packed codes directly, so expansion happens in registers
+ * and never in RAM"; the reconstruction is the quantizer's g_hat = q * scale
+ * + zero, [KIVI] second post, "What KIVI is").  Readings: keys and values are
+ * reconstructed exactly (binary64, no fp16 rounding of the expansion); the
+ * cache of sequence b is its first lens[b] quantized tokens (lens NULL: all
+ * S_cap) followed by the first res_lens[b] tokens of the fp16 residual window
+ * (res_lens NULL: all R), the window holding the most recent tokens ([KIVI]
+ * second post: "KIVI holds the last R tokens in fp16"); one query token per
+ * (batch, query head), query head hq reads kv head hq / (Hq / Hkv); exact
+ * softmax of scale * (q . k); an empty cache gives zeros.
+ *
+ * Layouts: the flush's (oracle_kivi_quant) with S_cap tokens per (b, h):
+ *   k_packed [B*Hkv, NG, G*b/32, D] (NG = S_cap / G), k_scale/k_zero [B*Hkv, NG, D];
+ *   v_packed [B*Hkv, S_cap, D*b/32], v_scale/v_zero [B*Hkv, S_cap, D/G];
+ *   k_res, v_res [B*Hkv, R, D] fp16; q [B, Hq, D]; out [B, Hq, D].
+ */
+void oracle_kivi_attend(const uint16_t *q_f16, const uint32_t *k_packed, const uint16_t *k_scale,
+                        const uint16_t *k_zero, const uint32_t *v_packed, const uint16_t *v_scale,
+                        const uint16_t *v_zero, const uint16_t *k_res, const uint16_t *v_res,
+                        const int32_t *lens, const int32_t *res_lens, int B, int Hq, int Hkv,
+                        int S_cap, int R, int D, int bits, int G, double scale, uint16_t *out_f16,
+                        double *out_f64)
+{
+    int per_word = 32 / bits, NG = S_cap / G, wpg = G * bits / 32, wpr = D * bits / 32;
+    uint32_t mask = (1u << bits) - 1u;
+    int GQ = Hq / Hkv, T = S_cap + R;
+    double *K = (double *)malloc(sizeof(double) * (size_t)(T > 0 ? T : 1) * D);
+    double *V = (double *)malloc(sizeof(double) * (size_t)(T > 0 ? T : 1) * D);
+    double *sc = (double *)malloc(sizeof(double) * (T > 0 ? T : 1));
+    double *acc = (double *)malloc(sizeof(double) * D);
+    for (int b = 0; b < B; ++b) {
+        int L = lens ? lens[b] : S_cap;
+        if (L > S_cap) L = S_cap;
+        if (L < 0) L = 0;
+        int Lr = res_lens ? res_lens[b] : R;
+        if (Lr > R) Lr = R;
+        if (Lr < 0) Lr = 0;
+        for (int h = 0; h < Hkv; ++h) {
+            long bh = (long)b * Hkv + h;
+            for (int s = 0; s < L; ++s) {
+                int g = s / G, i = s % G;
+                long gi = bh * NG + g;
+                long row = bh * S_cap + s;
+                for (int d = 0; d < D; ++d) {
+                    uint32_t kw = k_packed[(gi * wpg + i / per_word) * D + d];
+                    uint32_t kq = (kw >> ((i % per_word) * bits)) & mask;
+                    K[(long)s * D + d] = (double)kq * oracle_f16_to_f64(k_scale[gi * D + d]) +
+                                         oracle_f16_to_f64(k_zero[gi * D + d]);
+                    uint32_t vw = v_packed[row * wpr + d / per_word];
+                    uint32_t vq = (vw >> ((d % per_word) * bits)) & mask;
+                    V[(long)s * D + d] = (double)vq * oracle_f16_to_f64(v_scale[row * (D / G) + d / G]) +
+                                         oracle_f16_to_f64(v_zero[row * (D / G) + d / G]);
+                }
+            }
+            for (int r = 0; r < Lr; ++r)
+                for (int d = 0; d < D; ++d) {
+                    K[(long)(L + r) * D + d] = oracle_f16_to_f64(k_res[(bh * R + r) * D + d]);
+                    V[(long)(L + r) * D + d] = oracle_f16_to_f64(v_res[(bh * R + r) * D + d]);
+                }
+            int n = L + Lr;
+            for (int gq = 0; gq < GQ; ++gq) {
+                long qo = ((long)b * Hq + (long)h * GQ + gq) * D;
+                double m = -INFINITY;
+                for (int s = 0; s < n; ++s) {
+                    double dot = 0.0;
+                    for (int d = 0; d < D; ++d) dot += oracle_f16_to_f64(q_f16[qo + d]) * K[(long)s * D + d];
+                    sc[s] = scale * dot;
+                    if (sc[s] > m) m = sc[s];
+                }
+                double l = 0.0;
+                for (int d = 0; d < D; ++d) acc[d] = 0.0;
+                for (int s = 0; s < n; ++s) {
+                    double w = exp(sc[s] - m);
+                    l += w;
+                    for (int d = 0; d < D; ++d) acc[d] += w * V[(long)s * D + d];
+                }
+                for (int d = 0; d < D; ++d) {
+                    double o = n > 0 ? acc[d] / l : 0.0;
+                    if (out_f64) out_f64[qo + d] = o;
+                    if (out_f16) out_f16[qo + d] = oracle_f64_to_f16_rn(o);
+                }
+            }
+        }
+    }
+    free(K); free(V); free(sc); free(acc);
+}
