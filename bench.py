@@ -13,7 +13,7 @@ K and V.  Inputs are 2 GiB, larger than L2 (129 MB), so no L2 flush is needed
 between steps.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload c5|c3|c2|c1|c4|attn]
+                  [--workload c5|c3|c2|c1|c4|attn|kattn]
 
 --impl reference times the CPU oracle (single-threaded binary64 C) on a
 bounded sample of the same workload per step.
@@ -80,8 +80,21 @@ def attend_bytes(lens, Hkv, Hq, bits):
     return keys * (2 * (D * bits // 8) + 4 + 2 * D) + len(lens) * Hq * D * 2 * 2
 
 
+def kattend_bytes(lens, res_lens, Hkv, Hq, bits, G):
+    """Algorithmic bytes of one KIVI attention call: every valid quantized
+    token's key and value codes, its share of the key group's scale/zero and
+    its value groups' scales/zeros, every residual token's fp16 key and value
+    rows, plus the queries in and outputs out."""
+    per_tok = 2 * (D * bits // 8) + 4 * D // G + 4 * (D // G)
+    q = int(np.sum(np.asarray(lens, np.int64))) * Hkv * per_tok
+    r = int(np.sum(np.asarray(res_lens, np.int64))) * Hkv * 4 * D
+    return q + r + len(lens) * Hq * D * 2 * 2
+
+
 def describe(name):
     return {
+        "kattn": "decode attention over KIVI 2-bit G=32 caches with the dequantization inside: 64 seqs x 8 kv "
+                 "heads x 32 query heads, capacity 16384 (lengths uniform in [1k,16k]) + 128-token fp16 window",
         "attn": "decode attention over RVQ b=2 key caches (fp16 values): 64 seqs x 8 kv heads x "
                 "32 query heads, capacity 16384, lengths uniform in [1k,16k]",
         "c5": "long-context K,V [4,32,32768,128] fp16 (4x40 outlier channels per head): RVQ b=2 "
@@ -256,6 +269,48 @@ def build_workload(name, dev, rank=0, layers=None, batch=None, chunked=False, ch
                            attend_bytes(lens_np, Hkv, Hq, bits), int(lens_np.sum()) * Hkv * D,
                            gpu_launches=nsplit)]
             c["results"] = [out]
+    elif name == "kattn":
+        # resident KIVI cache (random codes, positive scales, N(0,1) zeros) and
+        # fp16 window; a step's input is the batch of queries
+        cfg = cfgs["kattn_decode_64x8x32_16k"]
+        B, Hkv, Hq, S, R, bits, G = (cfg["B"], cfg["Hkv"], cfg["Hq"], cfg["S_cap"], cfg["R"], cfg["bits"],
+                                     cfg["group"])
+        B = B if batch is None else batch
+        lens_np = (synth.cache_lengths(B, cfg["seed"]) // 32 * 32).astype(np.int32)
+        rng = np.random.default_rng(cfg["seed"])
+        res_np = rng.integers(0, R + 1, B).astype(np.int32)
+        g = torch.Generator(device=dev)
+        g.manual_seed(cfg["seed"])
+        NG = S // G
+        ri = lambda shape: torch.randint(-2 ** 31, 2 ** 31 - 1, shape, dtype=torch.int32, device=dev, generator=g)
+        cache = {
+            "k_packed": ri((B, Hkv, NG, G * bits // 32, D)),
+            "k_scale": torch.empty((B, Hkv, NG, D), dtype=torch.float16, device=dev).uniform_(0.05, 0.5, generator=g),
+            "k_zero": torch.randn((B, Hkv, NG, D), dtype=torch.float16, device=dev, generator=g),
+            "v_packed": ri((B, Hkv, S, D * bits // 32)),
+            "v_scale": torch.empty((B, Hkv, S, D // G), dtype=torch.float16, device=dev).uniform_(0.05, 0.5, generator=g),
+            "v_zero": torch.randn((B, Hkv, S, D // G), dtype=torch.float16, device=dev, generator=g),
+        }
+        kr = torch.randn((B, Hkv, R, D), dtype=torch.float16, device=dev, generator=g)
+        vr = torch.randn((B, Hkv, R, D), dtype=torch.float16, device=dev, generator=g)
+        q_np = rng.standard_normal((B, Hq, D)).astype(np.float16)
+        q, lens, res = t(q_np), t(lens_np), t(res_np)
+        out = torch.empty((B, Hq, D), dtype=torch.float16, device=dev)
+        ws = torch.empty((max(api.vq_kivi_attend_workspace(B, Hq, Hkv, S, R), 16) + 3) // 4,
+                         dtype=torch.float32, device=dev)
+        nb = kattend_bytes(lens_np, res_np, Hkv, Hq, bits, G)
+        ne = int(lens_np.sum() + res_np.sum()) * Hkv * D
+
+        def katt(stream=stream):
+            api.vq_kivi_attend(q, cache, bits, G, 1.0 / np.sqrt(D), k_res=kr, v_res=vr, lens=lens, res_lens=res,
+                               out=out, workspace=ws, stream=stream)
+        ops.append(Op("kivi_attend", "kivi_attend_kernel", katt, nb, ne, gpu_launches=3))
+        inputs = [(q_np, q)]
+        results.append(out)
+        if chunked:
+            c = new_chunk(inputs)
+            c["ops"] = [Op("kivi_attend", "kivi_attend_kernel", lambda: katt(chunk_stream), nb, ne, gpu_launches=3)]
+            c["results"] = [out]
     else:
         raise ValueError(name)
     if chunked and not chunks:
@@ -411,6 +466,29 @@ def oracle_sample_rates(name, target_s=2.0):
         r, n, _ = timed(att, attend_bytes([1], 1, 0, bits), 256, smax)
         rates["rvq_attend"] = r
         desc.append("RVQ b=%d attention of %d query heads over one kv head of %d keys" % (bits, gq, n))
+    if name == "kattn":
+        cfg = cfgs["kattn_decode_64x8x32_16k"]
+        bits, G, gq, R = cfg["bits"], cfg["group"], cfg["Hq"] // cfg["Hkv"], cfg["R"]
+        smax = 1 << 15
+        rng = np.random.default_rng(cfg["seed"])
+        kk = rng.standard_normal((1, 1, smax + R, D)).astype(np.float16)
+        vv = rng.standard_normal((1, 1, smax + R, D)).astype(np.float16)
+        kq = oracle.kivi_quant(kk, bits, G, R, True)
+        vq_ = oracle.kivi_quant(vv, bits, G, R, False)
+        qq = rng.standard_normal((1, gq, D)).astype(np.float16)
+        NG = smax // G
+
+        def katt(n):
+            ng = max(1, n // G)
+            oracle.kivi_attend(qq, kq["packed"].reshape(1, 1, NG, -1, D)[:, :, :ng],
+                               kq["scale"].reshape(1, 1, NG, D)[:, :, :ng], kq["zero"].reshape(1, 1, NG, D)[:, :, :ng],
+                               vq_["packed"].reshape(1, 1, smax, -1)[:, :, :ng * G],
+                               vq_["scale"].reshape(1, 1, smax, -1)[:, :, :ng * G],
+                               vq_["zero"].reshape(1, 1, smax, -1)[:, :, :ng * G], bits, G, 1.0 / np.sqrt(D))
+        per_tok = kattend_bytes([1], [0], 1, 0, bits, G)
+        r, n, _ = timed(katt, per_tok, 256, smax)
+        rates["kivi_attend"] = r
+        desc.append("KIVI %d-bit G=%d attention of %d query heads over one kv head of %d tokens" % (bits, G, gq, n))
     return rates, "; ".join(desc) + " (about %.0f s of CPU per op)" % target_s
 
 
@@ -455,7 +533,7 @@ def main():
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--workload", choices=("c5", "c3", "c2", "c1", "c4", "attn"), default="c5")
+    ap.add_argument("--workload", choices=("c5", "c3", "c2", "c1", "c4", "attn", "kattn"), default="c5")
     ap.add_argument("--graph", action="store_true",
                     help="also capture the step in a CUDA graph and time its replays "
                          "(launch-bound workloads: c4, c1); `value` is then the graph's")
@@ -661,7 +739,7 @@ def main():
             "data": "synthetic (seeded N(0,1) fp16 with per-head outlier channels)",
             "config": {"workload": args.workload + ": " + describe(args.workload),
                        "parallelism": "replicas (independent shards per GPU)" if world > 1 else "single GPU",
-                       "l2": "inputs larger than L2 (129 MB); no flush" if args.workload in ("c5", "c3", "c2", "attn")
+                       "l2": "inputs larger than L2 (129 MB); no flush" if args.workload in ("c5", "c3", "c2", "attn", "kattn")
                              else "inputs smaller than L2; rotating not applied",
                        "bytes_per_step": step_bytes, "elements_per_step": step_elems},
             "pct_of_peak": round(100 * value / world / peak, 2),
@@ -754,6 +832,13 @@ def reference_ops(name):
         ops.append(Op("rvq_encode", "rvq_encode", noop, rvq_bytes(rows, 2), rows * D))
         for n, pc in (("kivi_quant_k", True), ("kivi_quant_v", False)):
             ops.append(Op(n, n, noop, kivi_bytes(c["B"] * c["H"], c["S"], 2, c["group"], pc), rows * D))
+    elif name == "kattn":
+        c = cfgs["kattn_decode_64x8x32_16k"]
+        lens = (synth.cache_lengths(c["B"], c["seed"]) // 32 * 32).astype(np.int32)
+        res = np.random.default_rng(c["seed"]).integers(0, c["R"] + 1, c["B"]).astype(np.int32)
+        ops.append(Op("kivi_attend", "kivi_attend", noop,
+                      kattend_bytes(lens, res, c["Hkv"], c["Hq"], c["bits"], c["group"]),
+                      int(lens.sum() + res.sum()) * c["Hkv"] * D))
     elif name == "attn":
         c = cfgs["attn_decode_64x8x32_16k"]
         lens = synth.cache_lengths(c["B"], c["seed"])

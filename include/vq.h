@@ -214,6 +214,38 @@ vq_status vq_rvq_attend_rs(const void *q_f16, const uint32_t *packed1, const uin
                            size_t workspace_bytes, vq_stream_t stream);
 
 /*
+ * vq_kivi_attend - decode-time attention over a KIVI cache, reading the packed
+ * codes directly (kivi page, first post, closing section: "Dequant-in-SDPA";
+ * the reconstruction is the quantizer's g_hat = q * scale + zero, second
+ * post, "What KIVI is").  Keys and values are reconstructed in registers in
+ * fp32 (q * scale is exact, one rounding for + zero) and never written out.
+ * For every batch b and query head hq, with kv head h = hq / (Hq / Hkv):
+ *   out[b][hq] = sum_t softmax_t(scale * q . k_t) v_t
+ * over the first lens[b] quantized tokens (all S_cap when lens is NULL)
+ * followed by the first res_lens[b] tokens of the fp16 residual window (all R
+ * when res_lens is NULL); an empty cache gives zeros.
+ *   q [B, Hq, D] fp16.  Quantized cache, in the layouts vq_kivi_quant_pack
+ *   writes with S_dst = S_cap (NG = S_cap / group key groups):
+ *     k_packed [B, Hkv, NG, group*bits/32, D] uint32, k_scale, k_zero
+ *     [B, Hkv, NG, D] fp16; v_packed [B, Hkv, S_cap, D*bits/32] uint32,
+ *     v_scale, v_zero [B, Hkv, S_cap, D/group] fp16.
+ *   k_res, v_res [B, Hkv, R, D] fp16 (NULL when R == 0).  All device, 16-byte
+ *   aligned.  lens, res_lens [B] int32, device, or NULL.
+ *   workspace: as vq_rvq_attend (size from vq_kivi_attend_workspace); with a
+ *   residual window at least 2 * B * Hq * 520 bytes are required
+ *   (VQ_ERR_INVALID_ARG otherwise).
+ * D = 128, bits in {1, 2, 4}, group in {32, 64, 128} with S_cap a multiple of
+ * group (VQ_ERR_UNSUPPORTED otherwise), Hq = GQ * Hkv with GQ in {1, 2, 4, 8}.
+ */
+vq_status vq_kivi_attend_workspace(int B, int Hq, int Hkv, int S_cap, int R, size_t *bytes);
+vq_status vq_kivi_attend(const void *q_f16, const uint32_t *k_packed, const void *k_scale,
+                         const void *k_zero, const uint32_t *v_packed, const void *v_scale,
+                         const void *v_zero, const void *k_res, const void *v_res,
+                         const int32_t *lens, const int32_t *res_lens, int B, int Hq, int Hkv,
+                         int S_cap, int R, int D, int bits, int group, float scale, void *out_f16,
+                         void *workspace, size_t workspace_bytes, vq_stream_t stream);
+
+/*
  * vq_kivi_quant_pack - KIVI flush of K and/or V (either may be NULL, with its
  * outputs).  Quantizes tokens [0, S_q), S_q = S - residual_length; tokens
  * [S_q, S) are the fp16 residual window and are not read or written.

@@ -30,7 +30,8 @@ VQ_DEVERR_BAD_OFFSET = 0x2
 EXPORTED = ("vq_status_str", "vq_version", "vq_rvq_codebook", "vq_rvq_encode_pack",
             "vq_rvq_unpack_dequant", "vq_kivi_quant_pack", "vq_kivi_unpack_dequant",
             "vq_device_error", "vq_rvq_attend_workspace", "vq_rvq_attend", "vq_rvq_attend_noalloc",
-            "vq_rvq_encode_pack_rs", "vq_rvq_unpack_dequant_rs", "vq_rvq_attend_rs")
+            "vq_rvq_encode_pack_rs", "vq_rvq_unpack_dequant_rs", "vq_rvq_attend_rs",
+            "vq_kivi_attend_workspace", "vq_kivi_attend")
 VQ_ATTEND_SCRATCH_BYTES = 16 * 1024 * 1024
 
 
@@ -67,6 +68,8 @@ def lib():
     L.vq_rvq_unpack_dequant_rs.argtypes = [P, P, P, I, I, I, I, I, P, P, P, P, P]
     L.vq_rvq_attend_rs.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, P, P, P, ctypes.c_float, P, P,
                                    ctypes.c_size_t, P]
+    L.vq_kivi_attend_workspace.argtypes = [I, I, I, I, I, ctypes.POINTER(ctypes.c_size_t)]
+    L.vq_kivi_attend.argtypes = [P] * 11 + [I] * 8 + [ctypes.c_float, P, P, ctypes.c_size_t, P]
     for name in EXPORTED[2:]:
         getattr(L, name).restype = I
     _lib = L
@@ -229,6 +232,38 @@ def vq_rvq_attend_noalloc(q, packed1, packed2, norms, v, bits: int, c1, c2, scal
     _check(lib().vq_rvq_attend_noalloc(_ptr(q), _ptr(packed1), _ptr(packed2), _ptr(norms), _ptr(v), _ptr(lens),
                                        B, Hq, Hkv, S_cap, D, bits, keep[0][1], keep[1][1], float(scale),
                                        _ptr(out), _stream(stream)), "vq_rvq_attend_noalloc")
+    return out
+
+
+def vq_kivi_attend_workspace(B: int, Hq: int, Hkv: int, S_cap: int, R: int) -> int:
+    """Workspace bytes vq_kivi_attend wants for these shapes on the current device."""
+    n = ctypes.c_size_t(0)
+    _check(lib().vq_kivi_attend_workspace(B, Hq, Hkv, S_cap, R, ctypes.byref(n)), "vq_kivi_attend_workspace")
+    return int(n.value)
+
+
+def vq_kivi_attend(q, cache: dict, bits: int, group: int, scale: float, k_res=None, v_res=None, lens=None,
+                   res_lens=None, out=None, workspace=None, stream=None):
+    """Decode-time attention of q [B, Hq, 128] over a KIVI cache (`cache`: the
+    dict vq_kivi_quant_pack returns, written with S_dst = S_cap) plus the fp16
+    residual window k_res, v_res [B, Hkv, R, 128].  Returns fp16 [B, Hq, 128]."""
+    import torch
+    B, Hq, D = q.shape
+    vp = cache["v_packed"]
+    Hkv, S_cap = vp.shape[1], vp.shape[2]
+    R = 0 if k_res is None else k_res.shape[2]
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=torch.float16, device=q.device)
+    if workspace is None:
+        nbytes = vq_kivi_attend_workspace(B, Hq, Hkv, S_cap, R)
+        workspace = torch.empty((max(nbytes, 16) + 3) // 4, dtype=torch.float32, device=q.device)
+    wbytes = workspace.numel() * workspace.element_size()
+    c = cache
+    _check(lib().vq_kivi_attend(_ptr(q), _ptr(c["k_packed"]), _ptr(c["k_scale"]), _ptr(c["k_zero"]),
+                                _ptr(c["v_packed"]), _ptr(c["v_scale"]), _ptr(c["v_zero"]), _ptr(k_res),
+                                _ptr(v_res), _ptr(lens), _ptr(res_lens), B, Hq, Hkv, S_cap, R, D, bits, group,
+                                float(scale), _ptr(out), _ptr(workspace), wbytes, _stream(stream)),
+           "vq_kivi_attend")
     return out
 
 

@@ -389,6 +389,107 @@ vq_status vq_rvq_attend_noalloc(const void *q_f16, const uint32_t *packed1, cons
                            scale, out_f16, nullptr, 0, true, nullptr, stream);
 }
 
+static vq_status kivi_attend_check(int B, int Hq, int Hkv, int S_cap, int R, int D, int bits, int group)
+{
+    vq_status st = attend_shape_check(B, Hq, Hkv, S_cap);
+    if (st != VQ_OK) return st;
+    if (R < 0) return VQ_ERR_INVALID_ARG;
+    if (bits == 3 || (D != kD && D > 0)) return VQ_ERR_UNSUPPORTED;
+    if (D != kD || (bits != 1 && bits != 2 && bits != 4)) return VQ_ERR_INVALID_ARG;
+    if (group != 32 && group != 64 && group != 128) return VQ_ERR_UNSUPPORTED;
+    if (S_cap % group != 0) return VQ_ERR_UNSUPPORTED;  // whole key groups
+    if ((long long)B * Hkv * R >= (1LL << 31)) return VQ_ERR_UNSUPPORTED;
+    return VQ_OK;
+}
+
+vq_status vq_kivi_attend_workspace(int B, int Hq, int Hkv, int S_cap, int R, size_t *bytes)
+{
+    if (!bytes) return VQ_ERR_INVALID_ARG;
+    const vq_status st = attend_shape_check(B, Hq, Hkv, S_cap);
+    if (st != VQ_OK) return st;
+    if (R < 0) return VQ_ERR_INVALID_ARG;
+    int nsplit = 1, chunk = 0;
+    rvq_attend_plan(B, Hkv, S_cap, &nsplit, &chunk);
+    const int nparts = nsplit + (R > 0 ? 1 : 0);
+    *bytes = nparts > 1 ? (size_t)B * Hq * nparts * AT_PART * sizeof(float) : 0;
+    return VQ_OK;
+}
+
+vq_status vq_kivi_attend(const void *q_f16, const uint32_t *k_packed, const void *k_scale, const void *k_zero,
+                         const uint32_t *v_packed, const void *v_scale, const void *v_zero, const void *k_res,
+                         const void *v_res, const int32_t *lens, const int32_t *res_lens, int B, int Hq, int Hkv,
+                         int S_cap, int R, int D, int bits, int group, float scale, void *out_f16,
+                         void *workspace, size_t workspace_bytes, vq_stream_t stream)
+{
+    vq_status st = kivi_attend_check(B, Hq, Hkv, S_cap, R, D, bits, group);
+    if (st != VQ_OK) return st;
+    if (!std::isfinite(scale)) return VQ_ERR_INVALID_ARG;
+    if ((long long)B * Hq == 0) return VQ_OK;
+    if (!q_f16 || !out_f16) return VQ_ERR_INVALID_ARG;
+    const bool cache = S_cap > 0, win = R > 0;
+    if (cache && (!k_packed || !k_scale || !k_zero || !v_packed || !v_scale || !v_zero)) return VQ_ERR_INVALID_ARG;
+    if (win && (!k_res || !v_res)) return VQ_ERR_INVALID_ARG;
+    if (!aligned(q_f16, 16) || !aligned(out_f16, 16) || (lens && !aligned(lens, 4)) ||
+        (res_lens && !aligned(res_lens, 4)) || (workspace && !aligned(workspace, 16)) ||
+        (cache && (!aligned(k_packed, 16) || !aligned(k_scale, 16) || !aligned(k_zero, 16) ||
+                   !aligned(v_packed, 16) || !aligned(v_scale, 16) || !aligned(v_zero, 16))) ||
+        (win && (!aligned(k_res, 16) || !aligned(v_res, 16))))
+        return VQ_ERR_MISALIGNED;
+    const int W = D * bits / 32, NG = S_cap / (group > 0 ? group : 1);
+    const size_t BH = (size_t)B * Hkv;
+    const size_t out_b = (size_t)B * Hq * D * 2;
+    const size_t kp_b = BH * NG * (group * bits / 32) * D * 4, ks_b = BH * NG * D * 2;
+    const size_t vp_b = BH * S_cap * W * 4, vs_b = BH * S_cap * (D / group) * 2, r_b = BH * R * D * 2;
+    if (overlap(out_f16, out_b, q_f16, out_b) ||
+        (cache && (overlap(out_f16, out_b, k_packed, kp_b) || overlap(out_f16, out_b, k_scale, ks_b) ||
+                   overlap(out_f16, out_b, k_zero, ks_b) || overlap(out_f16, out_b, v_packed, vp_b) ||
+                   overlap(out_f16, out_b, v_scale, vs_b) || overlap(out_f16, out_b, v_zero, vs_b))) ||
+        (win && (overlap(out_f16, out_b, k_res, r_b) || overlap(out_f16, out_b, v_res, r_b))) ||
+        (lens && overlap(out_f16, out_b, lens, (size_t)B * 4)) ||
+        (res_lens && overlap(out_f16, out_b, res_lens, (size_t)B * 4)) ||
+        (workspace && overlap(out_f16, out_b, workspace, workspace_bytes)))
+        return VQ_ERR_ALIASING;
+    int nsplit = 1, chunk = 0;
+    rvq_attend_plan(B, Hkv, S_cap, &nsplit, &chunk);
+    const size_t per_part = (size_t)B * Hq * AT_PART * sizeof(float);
+    if (!workspace) workspace_bytes = 0;
+    const int extra = win ? 1 : 0;
+    if (nsplit + extra > 1 && workspace_bytes < per_part * (size_t)(nsplit + extra)) {
+        // fewer chunks fit; the residual window always needs a part of its own
+        const size_t fit = workspace_bytes / per_part;
+        if (win && fit < 2) return VQ_ERR_INVALID_ARG;
+        rvq_attend_plan_fit(S_cap, (int)((fit > (size_t)(nsplit + extra) ? nsplit + extra : fit) - extra),
+                            &nsplit, &chunk);
+    }
+    if (chunk <= 0) chunk = 32;
+    KiviAttendParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.q = q_f16;
+    p.kp = k_packed;
+    p.ks = k_scale;
+    p.kz = k_zero;
+    p.vp = v_packed;
+    p.vs = v_scale;
+    p.vz = v_zero;
+    p.kr = k_res;
+    p.vr = v_res;
+    p.lens = lens;
+    p.res_lens = res_lens;
+    p.out = out_f16;
+    p.ws = static_cast<float *>(workspace);
+    p.B = B;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.S_cap = S_cap;
+    p.R = R;
+    p.G = group;
+    p.NG = NG;
+    p.nsplit = nsplit;
+    p.chunk = chunk;
+    p.qscale = (float)((double)scale * 1.4426950408889634);
+    return cuda_status(launch_kivi_attend(p, bits, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 static vq_status kivi_common_check(int B, int H, int D, int bits, int group)
 {
     if (B < 0 || H < 0) return VQ_ERR_INVALID_ARG;
@@ -526,12 +627,13 @@ vq_status vq_device_error(vq_stream_t stream, int *code_out)
 {
     if (!code_out) return VQ_ERR_INVALID_ARG;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    unsigned a = 0, b = 0, c = 0;
+    unsigned a = 0, b = 0, c = 0, d = 0;
     if (rvq_take_device_error(&a, s) != cudaSuccess) return VQ_ERR_CUDA;
     if (kivi_take_device_error(&b, s) != cudaSuccess) return VQ_ERR_CUDA;
     if (attend_take_device_error(&c, s) != cudaSuccess) return VQ_ERR_CUDA;
-    *code_out = (int)(a | b | c);
-    return (a | b | c) ? VQ_ERR_DEVICE : VQ_OK;
+    if (kivi_attend_take_device_error(&d, s) != cudaSuccess) return VQ_ERR_CUDA;
+    *code_out = (int)(a | b | c | d);
+    return (a | b | c | d) ? VQ_ERR_DEVICE : VQ_OK;
 }
 
 }  // extern "C"

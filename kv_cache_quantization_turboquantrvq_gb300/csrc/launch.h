@@ -129,6 +129,24 @@ struct RvqAttendParams {
 void rvq_attend_plan(int B, int Hkv, int S_cap, int *nsplit, int *chunk);
 void rvq_attend_plan_fit(int S_cap, int max_splits, int *nsplit, int *chunk);
 cudaError_t launch_rvq_attend(const RvqAttendParams &p, int bits, cudaStream_t stream);
+// Decode-time attention over a KIVI cache (dequantization inside).
+struct KiviAttendParams {
+    const void *q;                     // fp16 [B, Hq, 128]
+    const uint32_t *kp;                // [B, Hkv, NG, G*b/32, 128]
+    const void *ks, *kz;               // fp16 [B, Hkv, NG, 128]
+    const uint32_t *vp;                // [B, Hkv, S_cap, 128*b/32]
+    const void *vs, *vz;               // fp16 [B, Hkv, S_cap, 128/G]
+    const void *kr, *vr;               // fp16 [B, Hkv, R, 128] residual window (R > 0)
+    const int32_t *lens, *res_lens;    // [B] or null
+    void *out;                         // fp16 [B, Hq, 128]
+    float *ws;                         // [B, Hq, nsplit + (R > 0), AT_PART] partials
+    int B, Hq, Hkv, S_cap, R, G, NG;
+    int nsplit, chunk;                 // chunks of the quantized tokens (part nsplit: the window)
+    float qscale;                      // softmax scale * log2(e)
+};
+cudaError_t launch_kivi_attend(const KiviAttendParams &p, int bits, cudaStream_t stream);
+cudaError_t kivi_attend_take_device_error(unsigned *bits, cudaStream_t stream);
+
 // Device address and size of the library's static attention scratch on the
 // current device.
 cudaError_t attend_static_scratch(void **ptr, size_t *bytes);

@@ -411,7 +411,9 @@ __device__ __noinline__ void rvq_fixup_row(const RvqEncodeParams &p, const unsig
     if (lane == 0) p.norms[drow] = __fadd_rn(nh, nl);
 }
 
-template <int BITS, int MODE>
+// SGN: the randomised-sign rotation (a separate instantiation, so that the
+// plain rotation carries no per-row test).
+template <int BITS, int MODE, bool SGN>
 __global__ void __launch_bounds__(enc_warps(BITS, MODE) * 32, 1)
     rvq_encode_kernel(const __grid_constant__ RvqEncodeParams p)
 {
@@ -529,7 +531,7 @@ __global__ void __launch_bounds__(enc_warps(BITS, MODE) * 32, 1)
             for (int c = 0; c < 4; ++c) {
                 uint4 la = *reinterpret_cast<const uint4 *>(src + swz128(rr, c));
                 uint4 lb = *reinterpret_cast<const uint4 *>(src + swz128(rr, c + 4));
-                if (p.has_sgn) {
+                if constexpr (SGN) {
                     // randomised signs: x -> diag(s) x on the fp16 bits
                     const uint4 ma = ssg[hh * 8 + c], mb = ssg[hh * 8 + c + 4];
                     la = make_uint4(la.x ^ ma.x, la.y ^ ma.y, la.z ^ ma.z, la.w ^ ma.w);
@@ -815,7 +817,7 @@ __device__ __forceinline__ void dec_lookup(const uint32_t (&w1)[BITS * 2], const
     for (int k = 0; k < 32; ++k) v[k] = make_float2(u[2 * k], u[2 * k + 1]);
 }
 
-template <int BITS>
+template <int BITS, bool SGN>
 __global__ void __launch_bounds__(DEC_WARPS * 32, 1) rvq_decode_kernel(const __grid_constant__ RvqDecodeParams p)
 {
     constexpr int L = 1 << BITS;
@@ -936,7 +938,7 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) rvq_decode_kernel(const __g
         }
         // o[k] holds coordinates 2k, 2k + 1 of the half; randomised signs:
         // x_hat -> diag(s) x_hat on the fp16 bits
-        if (p.has_sgn) {
+        if constexpr (SGN) {
             const uint4 *m4 = reinterpret_cast<const uint4 *>(sgm + hh * 32);
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
@@ -976,7 +978,7 @@ cudaError_t launch_enc(const RvqEncodeParams &p0, cudaStream_t stream)
         const uint32_t box[2] = {64u, (uint32_t)ER};
         if (!encode_tmap_f16(&p.tmap, p.x, 2, dims, strides, box, true, true)) return cudaErrorInvalidValue;
     }
-    auto kern = rvq_encode_kernel<BITS, MODE>;
+    auto kern = p.has_sgn ? rvq_encode_kernel<BITS, MODE, true> : rvq_encode_kernel<BITS, MODE, false>;
     constexpr int smem = enc_smem(BITS, MODE);
     constexpr int warps = enc_warps(BITS, MODE);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -993,7 +995,7 @@ cudaError_t launch_enc(const RvqEncodeParams &p0, cudaStream_t stream)
 template <int BITS>
 cudaError_t launch_dec(const RvqDecodeParams &p, cudaStream_t stream)
 {
-    auto kern = rvq_decode_kernel<BITS>;
+    auto kern = p.has_sgn ? rvq_decode_kernel<BITS, true> : rvq_decode_kernel<BITS, false>;
     constexpr int smem = dec_smem(BITS);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;

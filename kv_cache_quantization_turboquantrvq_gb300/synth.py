@@ -91,6 +91,11 @@ CONFIGS = {
     # and 32 query heads (GQA 4), RVQ b=2 keys and fp16 values in caches of
     # capacity 16384 holding random lengths in [1k, 16k].
     "attn_decode_64x8x32_16k": dict(kind="attend", B=64, Hkv=8, Hq=32, S_cap=16384, bits=2, seed=110),
+    # The same decode batch over a KIVI 2-bit (G = 32) cache with dequantization
+    # inside the attention, plus a 128-token fp16 residual window holding
+    # random fill levels in [0, 128].
+    "kattn_decode_64x8x32_16k": dict(kind="kattend", B=64, Hkv=8, Hq=32, S_cap=16384, R=128, bits=2,
+                                     group=32, seed=111),
 }
 
 
