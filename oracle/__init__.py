@@ -184,7 +184,7 @@ def rvq_encode(x_f16: np.ndarray, bits: int, c1, b1, c2, b2, want_values: bool =
     x = _c(x_f16, np.float16)
     D = x.shape[-1]
     N = x.size // D
-    W = D * bits // 32
+    W = -(-D // (32 // bits))  # words per row: floor(32/b) codes each
     out = {
         "packed1": np.empty((N, W), np.uint32), "packed2": np.empty((N, W), np.uint32),
         "norms": np.empty(N, np.float32),

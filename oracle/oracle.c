@@ -283,8 +283,8 @@ int oracle_rvq_codebooks(int D, int bits, float *c1, float *b1, float *c2, float
 /* ------------------------------------------------------------------------ */
 /* Bit packing.                                                              */
 /* [RVQ] "The kernel" and [TQ] "Kernel 1: Bit-Packing": b-bit codes, LSB     */
-/* first: element i of a run goes to word i / (32/b) at shift               */
-/* (i mod 32/b) * b.                                                         */
+/* first: element i of a run goes to word i / E at shift (i mod E) * b with  */
+/* E = floor(32/b) codes per word (b = 3: 10 codes, the top 2 bits zero).    */
 /* ------------------------------------------------------------------------ */
 
 void oracle_pack_lsb_first(const uint8_t *codes, long n, int bits, uint32_t *words)
@@ -331,7 +331,7 @@ void oracle_rvq_encode(const uint16_t *x_f16, long N, int D, int bits,
                        const uint32_t *signs)
 {
     int L = 1 << bits;
-    int W = D * bits / 32;
+    int W = (D + 32 / bits - 1) / (32 / bits);  /* words per row: E = floor(32/b) codes each */
     double *H = (double *)malloc(sizeof(double) * D * D);
     double *x = (double *)malloc(sizeof(double) * D);
     double *u = (double *)malloc(sizeof(double) * D);
@@ -391,7 +391,7 @@ void oracle_rvq_decode(const uint32_t *packed1, const uint32_t *packed2, const f
                        long N, int D, int bits, const float *c1, const float *c2,
                        uint16_t *out_f16, double *out_f64, const uint32_t *signs)
 {
-    int W = D * bits / 32;
+    int W = (D + 32 / bits - 1) / (32 / bits);
     double *H = (double *)malloc(sizeof(double) * D * D);
     double *yh = (double *)malloc(sizeof(double) * D);
     uint8_t *q1 = (uint8_t *)malloc(D), *q2 = (uint8_t *)malloc(D);
@@ -436,7 +436,7 @@ void oracle_rvq_attend(const uint16_t *q_f16, const uint32_t *packed1, const uin
                        const float *c2, double scale, uint16_t *out_f16, double *out_f64,
                        const uint32_t *signs)
 {
-    int W = D * bits / 32, G = Hq / Hkv;
+    int W = (D + 32 / bits - 1) / (32 / bits), G = Hq / Hkv;
     double *H = (double *)malloc(sizeof(double) * D * D);
     double *K = (double *)malloc(sizeof(double) * (size_t)S_cap * D);
     double *yh = (double *)malloc(sizeof(double) * D);

@@ -181,7 +181,7 @@ def test_stage2_beta_is_mean_abs_residual(oracle_mod, bits):
     assert abs(mc - beta) < 5e-4 * sigma * 10
 
 
-@pytest.mark.parametrize("bits", [1, 2, 4])
+@pytest.mark.parametrize("bits", [1, 2, 3, 4])
 def test_rvq_codebooks_structure(oracle_mod, bits):
     c1, b1, c2, b2, beta = oracle_mod.rvq_codebooks(128, bits)
     L = 1 << bits
@@ -275,11 +275,12 @@ def test_rvq_encode_strict_greater_at_exact_boundary(oracle_mod):
     assert np.all(out["tie1"] == 1) and np.all(out["tie2"] == 1)
 
 
-@pytest.mark.parametrize("bits", [1, 2, 4])
-def test_rvq_encode_invariants(oracle_mod, bits):
-    c1, b1, c2, b2, _ = oracle_mod.rvq_codebooks(128, bits)
-    rng = np.random.default_rng(100 + bits)
-    x = (rng.standard_normal((64, 128)) * 0.7).astype(np.float16)
+@pytest.mark.parametrize("D,bits", [(128, 1), (128, 2), (128, 3), (128, 4), (8, 3), (16, 1), (32, 4),
+                                    (64, 2), (64, 3), (256, 3), (256, 4)])
+def test_rvq_encode_invariants(oracle_mod, D, bits):
+    c1, b1, c2, b2, _ = oracle_mod.rvq_codebooks(D, bits)
+    rng = np.random.default_rng(100 + bits + D)
+    x = (rng.standard_normal((64, D)) * 0.7).astype(np.float16)
     o = oracle_mod.rvq_encode(x, bits, c1, b1, c2, b2, want_values=True)
     # norm and rotation preserve length
     n = np.sqrt((x.astype(np.float64) ** 2).sum(1))
@@ -297,11 +298,14 @@ def test_rvq_encode_invariants(oracle_mod, bits):
     clean = (o["tie2"] == 0) & (o3["tie2"] == 0)
     assert np.array_equal(o3["idx1"][clean], (L - o["idx1"])[clean])
     assert np.array_equal(o3["idx2"][clean], (L - o["idx2"])[clean])
-    # packed words are the LSB-first packing of the index streams
-    assert np.array_equal(o["packed1"].ravel(), oracle_mod.pack_lsb_first(o["idx1"], bits))
-    assert np.array_equal(o["packed2"].ravel(), oracle_mod.pack_lsb_first(o["idx2"], bits))
+    # packed words are the LSB-first packing of each row's index streams
+    for k in ("1", "2"):
+        rows = np.stack([oracle_mod.pack_lsb_first(r, bits) for r in o["idx" + k]])
+        assert np.array_equal(o["packed" + k], rows)
+    # words per row: ceil(D / floor(32/b)) (b = 3: ten codes per word)
+    assert o["packed1"].shape == (64, -(-D // (32 // bits)))
     # zero row: u = 0, so y = 0 and every code counts the negative boundaries
-    z = oracle_mod.rvq_encode(np.zeros((1, 128), np.float16), bits, c1, b1, c2, b2)
+    z = oracle_mod.rvq_encode(np.zeros((1, D), np.float16), bits, c1, b1, c2, b2)
     assert z["norms"][0] == 0
     assert np.all(z["idx1"] == (0.0 > b1).sum())
 
@@ -469,3 +473,27 @@ def test_kivi_layouts_and_dequant(oracle_mod, bits):
                 scv, zev = o["scale"][bh, s, d // G], o["zero"][bh, s, d // G]
             v = Fraction(int(codes[bh, s, d])) * Fraction(float(scv)) + Fraction(float(zev))
             assert dq[bh, s, d] == np.float16(float(v))
+
+
+@pytest.mark.parametrize("D", [8, 16, 32, 64, 256])
+def test_rotation_closed_forms_at_other_widths(oracle_mod, D):
+    """x = e_j gives y_i = (-1)^popcount(i & j) / sqrt(D) (column j of the
+    Sylvester matrix), at every width the pages test."""
+    c1, b1, c2, b2, _ = oracle_mod.rvq_codebooks(D, 2)
+    for j in (0, D - 1, D // 3):
+        x = np.zeros((1, D), np.float16)
+        x[0, j] = -2.0
+        y = oracle_mod.rvq_encode(x, 2, c1, b1, c2, b2, want_values=True)["y"][0]
+        ref = np.array([-(-1.0) ** bin(i & j).count("1") for i in range(D)]) / np.sqrt(D)
+        np.testing.assert_allclose(y, ref, rtol=0, atol=1e-15)
+
+
+def test_three_bit_words_leave_the_top_bits_clear(oracle_mod):
+    rng = np.random.default_rng(3)
+    codes = rng.integers(0, 8, 10 * 37).astype(np.uint8)
+    words = oracle_mod.pack_lsb_first(codes, 3)
+    assert len(words) == 37 and np.all(words >> 30 == 0)
+    assert np.array_equal(oracle_mod.unpack_lsb_first(words, len(codes), 3), codes)
+    # a row of D = 128 codes takes 13 words, the last holding 8 codes
+    w = oracle_mod.pack_lsb_first(np.full(128, 7, np.uint8), 3)
+    assert len(w) == 13 and w[-1] == (1 << 24) - 1
