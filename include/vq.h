@@ -36,11 +36,15 @@
  *    a library-owned device error word, read and cleared by vq_device_error().
  *  - Inputs must be finite; non-finite inputs give unspecified codes but no
  *    out-of-bounds access.
- *  - Packing is LSB first: with E = 32/bits codes per uint32 word, code j of
- *    a word sits at bit shift j*bits.  On a little-endian machine these words
- *    have the same bytes as the byte packer of the tag "turboquant" page,
- *    section "Kernel 1: Bit-Packing".
- *  - Supported: D == 128, bits in {1, 2, 4}.
+ *  - Packing is LSB first: with E = floor(32/bits) codes per uint32 word,
+ *    code j of a word sits at bit shift j*bits.  For bits in {1, 2, 4} these
+ *    words have, on a little-endian machine, the same bytes as the byte packer
+ *    of the tag "turboquant" page, section "Kernel 1: Bit-Packing".
+ *  - Supported: RVQ encode and decode at D in {8, 16, 32, 64, 128, 256} and
+ *    bits in {1, 2, 3, 4} (the widths and bit counts the tag "rvq" page tests,
+ *    "Bit-exactness, checked the boring way"); D = 128 with bits in {1, 2, 4}
+ *    runs the dedicated kernels, the rest a general one.  KIVI, attention and
+ *    the randomised-sign calls: D == 128, bits in {1, 2, 4}.
  */
 #ifndef VQ_H
 #define VQ_H
@@ -94,9 +98,10 @@ vq_status vq_rvq_codebook(int D, int bits, float *c1, float *b1, float *c2, floa
  *   c1, c2   [2^bits] fp32 centroids, host, ascending.
  *   b1, b2   [2^bits - 1] fp32 boundaries, host, strictly increasing, each
  *            strictly between its two neighbouring centroids.
- *   packed1, packed2  [B, H, S_dst, D*bits/32] uint32, device: the stage-1 and
- *            stage-2 index streams; code of coordinate d in word d/E at shift
- *            (d mod E)*bits.
+ *   packed1, packed2  [B, H, S_dst, W] uint32, device: the stage-1 and
+ *            stage-2 index streams; E = floor(32/bits) codes per word (10 for
+ *            bits = 3, whose top two bits stay zero), W = ceil(D/E) words per
+ *            row; code of coordinate d in word d/E at shift (d mod E)*bits.
  *   norms    [B, H, S_dst] fp32, device: ||x||_2 of each row.
  *   dst_off  NULL (then S_dst must equal S and rows land at token s) or a
  *            device array [B] of int32 token offsets: row (b, h, s) is written
@@ -118,7 +123,7 @@ vq_status vq_rvq_encode_pack(const void *k_f16, int B, int H, int S, int D, int 
  * (VeloxQuant-MLX blog, tag "turboquant", "Kernel 5: Fused RVQ Decode +
  * Attend" decodes c1[i1] + c2[i2] in the rotated domain; this call also undoes
  * the rotation, H / sqrt(D) being its own inverse, and re-applies the norm.)
- *   packed1, packed2 [B, H, S, D*bits/32] uint32, norms [B, H, S] fp32, device.
+ *   packed1, packed2 [B, H, S, W] uint32 (W as above), norms [B, H, S] fp32, device.
  *   c1, c2 [2^bits] fp32, host.   out_f16 [B, H, S, D] fp16, device.
  */
 vq_status vq_rvq_unpack_dequant(const uint32_t *packed1, const uint32_t *packed2,

@@ -107,6 +107,11 @@ def vq_version() -> str:
     return lib().vq_version().decode()
 
 
+def rvq_words(D: int, bits: int) -> int:
+    """Packed words per row and stream: floor(32/b) codes per word."""
+    return -(-D // (32 // bits))
+
+
 def vq_rvq_codebook(D: int, bits: int):
     """(c1, b1, c2, b2) float32 host arrays: Gaussian stage-1 and Laplace-fit stage-2."""
     L = 1 << bits
@@ -133,7 +138,7 @@ def vq_rvq_encode_pack(k, bits: int, c1, b1, c2, b2, packed1=None, packed2=None,
     import torch
     B, H, S, D = k.shape
     S_dst = S if S_dst is None else S_dst
-    W = D * bits // 32
+    W = rvq_words(D, bits)
     if packed1 is None:
         packed1 = torch.empty((B, H, S_dst, W), dtype=torch.int32, device=k.device)
     if packed2 is None:
@@ -154,11 +159,11 @@ def vq_rvq_encode_pack(k, bits: int, c1, b1, c2, b2, packed1=None, packed2=None,
     return packed1, packed2, norms
 
 
-def vq_rvq_unpack_dequant(packed1, packed2, norms, bits: int, c1, c2, out=None, stream=None, signs=None):
-    """Decode (packed1, packed2, norms) [B, H, S, ...] back to fp16 keys [B, H, S, 128]."""
+def vq_rvq_unpack_dequant(packed1, packed2, norms, bits: int, c1, c2, out=None, stream=None, signs=None,
+                          D: int = 128):
+    """Decode (packed1, packed2, norms) [B, H, S, W] back to fp16 keys [B, H, S, D]."""
     import torch
     B, H, S, _ = packed1.shape
-    D = 128
     if out is None:
         out = torch.empty((B, H, S, D), dtype=torch.float16, device=packed1.device)
     keep = [_host(v) for v in (c1, c2)]

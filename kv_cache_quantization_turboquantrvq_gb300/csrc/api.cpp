@@ -22,6 +22,18 @@ constexpr int kD = 128;
 // the band is several times the largest error seen on Gaussian rows with
 // 40x outlier channels.
 constexpr float kGuard = 2.5e-7f;
+// the generic (any width) path's guard band: its fp32 rotation runs up to 8
+// butterfly stages at D = 256, and a flagged step costs only a binary64 pass
+constexpr float kGuardGeneric = 1e-6f;
+
+// RVQ widths and bit counts (the rvq page tests D = 8 .. 256 and b = 1 .. 4);
+// D = 128 with b in {1, 2, 4} has the dedicated kernels.
+bool rvq_shape_supported(int D, int bits)
+{
+    return (D == 8 || D == 16 || D == 32 || D == 64 || D == 128 || D == 256) && bits >= 1 && bits <= 4;
+}
+bool rvq_fast_shape(int D, int bits) { return D == 128 && bits != 3; }
+int rvq_words(int D, int bits) { return (D + 32 / bits - 1) / (32 / bits); }
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
@@ -113,7 +125,7 @@ const char *vq_version(void) { return "vqflush 0.1.0 sm_103a"; }
 vq_status vq_rvq_codebook(int D, int bits, float *c1, float *b1, float *c2, float *b2)
 {
     if (!c1 || !b1 || !c2 || !b2) return VQ_ERR_INVALID_ARG;
-    if (D <= 0 || (bits != 1 && bits != 2 && bits != 4)) return VQ_ERR_INVALID_ARG;
+    if (D <= 0 || bits < 1 || bits > 4) return VQ_ERR_INVALID_ARG;
     const int L = 1 << bits;
     double g[16], l[16], beta;
     if (!rvq_codebook_f64(D, bits, g, l, &beta)) return VQ_ERR_INVALID_ARG;
@@ -135,8 +147,9 @@ static vq_status rvq_encode_impl(const void *k_f16, int B, int H, int S, int D, 
                                  vq_stream_t stream)
 {
     if (B < 0 || H < 0 || S < 0) return VQ_ERR_INVALID_ARG;
-    if (bits == 3 || (D != kD && D > 0)) return VQ_ERR_UNSUPPORTED;
-    if (D != kD || (bits != 1 && bits != 2 && bits != 4)) return VQ_ERR_INVALID_ARG;
+    if (bits < 1 || bits > 4) return VQ_ERR_INVALID_ARG;
+    if (!rvq_shape_supported(D, bits)) return VQ_ERR_UNSUPPORTED;
+    if (signs && !rvq_fast_shape(D, bits)) return VQ_ERR_UNSUPPORTED;
     if (!c1 || !b1 || !c2 || !b2) return VQ_ERR_INVALID_ARG;
     const int L = 1 << bits;
     if (!valid_codebook(c1, b1, L) || !valid_codebook(c2, b2, L)) return VQ_ERR_INVALID_ARG;
@@ -149,7 +162,7 @@ static vq_status rvq_encode_impl(const void *k_f16, int B, int H, int S, int D, 
     if (!aligned(k_f16, 16) || !aligned(packed1, 16) || !aligned(packed2, 16) || !aligned(norms, 4) ||
         (dst_off && !aligned(dst_off, 4)))
         return VQ_ERR_MISALIGNED;
-    const int W = D * bits / 32;
+    const int W = rvq_words(D, bits);
     const size_t in_b = (size_t)N * D * 2, pk_b = (size_t)Nd * W * 4, n_b = (size_t)Nd * 4;
     if (overlap(k_f16, in_b, packed1, pk_b) || overlap(k_f16, in_b, packed2, pk_b) ||
         overlap(k_f16, in_b, norms, n_b) || overlap(packed1, pk_b, packed2, pk_b) ||
@@ -159,6 +172,28 @@ static vq_status rvq_encode_impl(const void *k_f16, int B, int H, int S, int D, 
                      overlap(dst_off, (size_t)B * 4, norms, n_b))))
         return VQ_ERR_ALIASING;
 
+    if (!rvq_fast_shape(D, bits)) {
+        RvqGenericParams g;
+        std::memset(&g, 0, sizeof(g));
+        g.x = k_f16;
+        g.p1 = packed1;
+        g.p2 = packed2;
+        g.norms = norms;
+        g.dst_off = dst_off;
+        g.N = (int)N;
+        g.S = S;
+        g.H = H;
+        g.S_dst = S_dst;
+        g.D = D;
+        g.guard = kGuardGeneric;
+        for (int k = 0; k < 16; ++k) {
+            g.c1[k] = k < L ? c1[k] : 0.0f;
+            g.c2[k] = k < L ? c2[k] : 0.0f;
+            g.b1[k] = k < L - 1 ? b1[k] : INFINITY;
+            g.b2[k] = k < L - 1 ? b2[k] : INFINITY;
+        }
+        return cuda_status(launch_rvq_generic(g, bits, true, reinterpret_cast<cudaStream_t>(stream)));
+    }
     RvqEncodeParams p;
     std::memset(&p, 0, sizeof(p));
     p.x = k_f16;
@@ -213,8 +248,9 @@ static vq_status rvq_decode_impl(const uint32_t *packed1, const uint32_t *packed
                                  void *out_f16, const uint32_t *signs, vq_stream_t stream)
 {
     if (B < 0 || H < 0 || S < 0) return VQ_ERR_INVALID_ARG;
-    if (bits == 3 || (D != kD && D > 0)) return VQ_ERR_UNSUPPORTED;
-    if (D != kD || (bits != 1 && bits != 2 && bits != 4)) return VQ_ERR_INVALID_ARG;
+    if (bits < 1 || bits > 4) return VQ_ERR_INVALID_ARG;
+    if (!rvq_shape_supported(D, bits)) return VQ_ERR_UNSUPPORTED;
+    if (signs && !rvq_fast_shape(D, bits)) return VQ_ERR_UNSUPPORTED;
     if (!c1 || !c2) return VQ_ERR_INVALID_ARG;
     const int L = 1 << bits;
     for (int k = 0; k < L; ++k)
@@ -225,11 +261,26 @@ static vq_status rvq_decode_impl(const uint32_t *packed1, const uint32_t *packed
     if (!packed1 || !packed2 || !norms || !out_f16) return VQ_ERR_INVALID_ARG;
     if (!aligned(packed1, 16) || !aligned(packed2, 16) || !aligned(norms, 4) || !aligned(out_f16, 16))
         return VQ_ERR_MISALIGNED;
-    const int W = D * bits / 32;
+    const int W = rvq_words(D, bits);
     const size_t pk_b = (size_t)N * W * 4, out_b = (size_t)N * D * 2;
     if (overlap(out_f16, out_b, packed1, pk_b) || overlap(out_f16, out_b, packed2, pk_b) ||
         overlap(out_f16, out_b, norms, (size_t)N * 4))
         return VQ_ERR_ALIASING;
+    if (!rvq_fast_shape(D, bits)) {
+        RvqGenericParams g;
+        std::memset(&g, 0, sizeof(g));
+        g.p1 = const_cast<uint32_t *>(packed1);
+        g.p2 = const_cast<uint32_t *>(packed2);
+        g.norms = const_cast<float *>(norms);
+        g.out = out_f16;
+        g.N = (int)N;
+        g.D = D;
+        for (int k = 0; k < 16; ++k) {
+            g.c1[k] = k < L ? c1[k] : 0.0f;
+            g.c2[k] = k < L ? c2[k] : 0.0f;
+        }
+        return cuda_status(launch_rvq_generic(g, bits, false, reinterpret_cast<cudaStream_t>(stream)));
+    }
     RvqDecodeParams p;
     std::memset(&p, 0, sizeof(p));
     p.p1 = packed1;
@@ -632,8 +683,10 @@ vq_status vq_device_error(vq_stream_t stream, int *code_out)
     if (kivi_take_device_error(&b, s) != cudaSuccess) return VQ_ERR_CUDA;
     if (attend_take_device_error(&c, s) != cudaSuccess) return VQ_ERR_CUDA;
     if (kivi_attend_take_device_error(&d, s) != cudaSuccess) return VQ_ERR_CUDA;
-    *code_out = (int)(a | b | c | d);
-    return (a | b | c | d) ? VQ_ERR_DEVICE : VQ_OK;
+    unsigned e = 0;
+    if (gen_take_device_error(&e, s) != cudaSuccess) return VQ_ERR_CUDA;
+    *code_out = (int)(a | b | c | d | e);
+    return (a | b | c | d | e) ? VQ_ERR_DEVICE : VQ_OK;
 }
 
 }  // extern "C"

@@ -147,6 +147,21 @@ struct KiviAttendParams {
 cudaError_t launch_kivi_attend(const KiviAttendParams &p, int bits, cudaStream_t stream);
 cudaError_t kivi_attend_take_device_error(unsigned *bits, cudaStream_t stream);
 
+// TurboQuantRVQ at the other widths and bit counts (D in {8, ..., 256}, b in
+// {1, 2, 3, 4}): words per row W = ceil(D / floor(32 / b)).
+struct RvqGenericParams {
+    const void *x;                 // encode: fp16 [N, D]
+    uint32_t *p1, *p2;             // encode: [B, H, S_dst, W]; decode: [N, W]
+    float *norms;                  // encode: [B, H, S_dst]; decode: [N]
+    void *out;                     // decode: fp16 [N, D]
+    const int32_t *dst_off;        // encode only, or null
+    int N, S, H, S_dst, D;
+    float guard;                   // |value - boundary| below this: binary64 recompute
+    float c1[16], c2[16], b1[16], b2[16];
+};
+cudaError_t launch_rvq_generic(const RvqGenericParams &p, int bits, bool encode, cudaStream_t stream);
+cudaError_t gen_take_device_error(unsigned *bits, cudaStream_t stream);
+
 // Device address and size of the library's static attention scratch on the
 // current device.
 cudaError_t attend_static_scratch(void **ptr, size_t *bytes);

@@ -42,9 +42,11 @@ def check_codes(got, ref, tie, what, allow_rate=TIE_RATE, strict=True):
     return int(n), int(got.size), int(tie.sum())
 
 
-def check_rvq(gpu_p1, gpu_p2, gpu_norms, ora, bits, strict=True):
-    g1 = unpack_rows(np.asarray(gpu_p1).reshape(-1, 4 * bits), bits)
-    g2 = unpack_rows(np.asarray(gpu_p2).reshape(-1, 4 * bits), bits)
+def check_rvq(gpu_p1, gpu_p2, gpu_norms, ora, bits, strict=True, D=128):
+    E = 32 // bits
+    W = -(-D // E)
+    g1 = unpack_rows(np.asarray(gpu_p1).reshape(-1, W), bits, D)
+    g2 = unpack_rows(np.asarray(gpu_p2).reshape(-1, W), bits, D)
     s1 = check_codes(g1, ora["idx1"], ora["tie1"], "stage-1 codes", strict=strict)
     s2 = check_codes(g2, ora["idx2"], ora["tie2"], "stage-2 codes", strict=strict)
     gn = np.asarray(gpu_norms, dtype=np.float32).reshape(-1).astype(np.float64)
@@ -52,10 +54,9 @@ def check_rvq(gpu_p1, gpu_p2, gpu_norms, ora, bits, strict=True):
     rel = np.abs(gn - rn) / np.maximum(rn, 1e-30)
     assert np.all((rel <= NORM_RTOL) | (rn == gn)), "norm rel err %g" % rel.max()
     # words equal wherever no code in them is tie-flagged
-    W = 4 * bits
-    E = 32 // bits
-    t1 = ora["tie1"].reshape(-1, W, E).any(-1)
-    t2 = ora["tie2"].reshape(-1, W, E).any(-1)
+    pad = W * E - D
+    t1 = np.pad(ora["tie1"].reshape(-1, D), ((0, 0), (0, pad))).reshape(-1, W, E).any(-1)
+    t2 = np.pad(ora["tie2"].reshape(-1, D), ((0, 0), (0, pad))).reshape(-1, W, E).any(-1)
     w1 = np.asarray(gpu_p1).view(np.uint32).reshape(-1, W)
     w2 = np.asarray(gpu_p2).view(np.uint32).reshape(-1, W)
     assert np.array_equal(w1[~t1], ora["packed1"][~t1])

@@ -71,8 +71,8 @@ def _enc(L, k=A, B=1, H=2, S=8, D=128, bits=2, cb=None, p1=A + (1 << 24), p2=A +
 
 def test_rvq_encode_validation(L):
     from kv_cache_quantization_turboquantrvq_gb300 import api
-    assert _enc(L, D=64) == api.VQ_ERR_UNSUPPORTED
-    assert _enc(L, bits=3) == api.VQ_ERR_UNSUPPORTED
+    assert _enc(L, D=96) == api.VQ_ERR_UNSUPPORTED   # not a power of two
+    assert _enc(L, D=512) == api.VQ_ERR_UNSUPPORTED  # wider than the pages test
     assert _enc(L, bits=5) == api.VQ_ERR_INVALID_ARG
     assert _enc(L, B=-1) == api.VQ_ERR_INVALID_ARG
     assert _enc(L, k=0) == api.VQ_ERR_INVALID_ARG
@@ -105,7 +105,8 @@ def test_rvq_decode_validation(L):
     def dec(p1=A, p2=A + (1 << 24), n=A + (2 << 24), out=A + (3 << 24), D=128, bits=2, S=8):
         return L.vq_rvq_unpack_dequant(P(p1), P(p2), P(n), 1, 2, S, D, bits, P(c1.ctypes.data),
                                        P(c2.ctypes.data), P(out), None)
-    assert dec(D=256) == api.VQ_ERR_UNSUPPORTED
+    assert dec(D=512) == api.VQ_ERR_UNSUPPORTED
+    assert dec(D=48) == api.VQ_ERR_UNSUPPORTED
     assert dec(out=0) == api.VQ_ERR_INVALID_ARG
     assert dec(out=A + (3 << 24) + 8) == api.VQ_ERR_MISALIGNED
     assert dec(out=A + 64) == api.VQ_ERR_ALIASING
