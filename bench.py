@@ -108,6 +108,25 @@ def describe(name):
     }[name]
 
 
+def max_over_ranks(x: float, world: int, dev) -> float:
+    """The largest of the ranks' values of x (a time): an all-reduce MAX on a
+    one-element tensor on `dev` (the rank's GPU under NCCL, the CPU under gloo)."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def shard_configs(rank: int) -> dict:
+    """The named configurations with rank-dependent seeds: under torchrun every
+    rank processes its own shard (same shapes, independent data)."""
+    from kv_cache_quantization_turboquantrvq_gb300 import synth
+    return {k: dict(v, seed=v["seed"] + 100003 * rank) for k, v in synth.CONFIGS.items()}
+
+
 def build_workload(name, dev, rank=0, layers=None, batch=None, chunked=False, chunk_stream=None):
     """Device buffers and the op list for one step; also host inputs for e2e.
 
@@ -184,7 +203,7 @@ def build_workload(name, dev, rank=0, layers=None, batch=None, chunked=False, ch
         chunks.append(c)
         return c
 
-    cfgs = synth.CONFIGS
+    cfgs = shard_configs(rank)
     if name == "c5":
         cfg = cfgs["c5_long_32k"]
         k_np, v_np = synth.keys_for(cfg, B=batch), synth.values_for(cfg, B=batch)
@@ -605,11 +624,7 @@ def main():
     clk = clocks.stop()
     if world > 1:
         dist.barrier()
-    elapsed_ms = t_start.elapsed_time(t_end)
-    if world > 1:
-        tt = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(tt.item())
+    elapsed_ms = max_over_ranks(t_start.elapsed_time(t_end), world, dev)
     step_bytes = sum(o.nbytes for o in ops)
     step_elems = sum(o.nelem for o in ops)
     value = world * step_bytes * K / (elapsed_ms * 1e-3) / 1e9
@@ -633,11 +648,7 @@ def main():
             g.replay()
         g1.record(stream)
         torch.cuda.synchronize()
-        gms = g0.elapsed_time(g1)
-        if world > 1:
-            tt = torch.tensor([gms], device=dev)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            gms = float(tt.item())
+        gms = max_over_ranks(g0.elapsed_time(g1), world, dev)
         graph = {"ms_per_step": round(gms / K, 5),
                  "eager_value": round(value, 2), "eager_ms_per_step": round(elapsed_ms / K, 5)}
         elapsed_ms = gms
@@ -714,11 +725,7 @@ def main():
         s_out.wait_event(chunks[-1]["ev_run"])
         e1.record(s_out)
         torch.cuda.synchronize()
-        ems = e0.elapsed_time(e1)
-        if world > 1:
-            tt = torch.tensor([ems], device=dev)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            ems = float(tt.item())
+        ems = max_over_ranks(e0.elapsed_time(e1), world, dev)
         e2e = {"value": round(world * step_bytes * Ke / (ems * 1e-3) / 1e9, 2), "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": round(ems / Ke, 4), "chunks_per_step": len(chunks),
