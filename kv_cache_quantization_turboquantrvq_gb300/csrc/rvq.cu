@@ -199,32 +199,36 @@ __device__ __forceinline__ uint32_t pair_code(float v, float a, float bc, const 
 //   b = 1:  i = y > 0                                   (bit: !sgn(y))
 // The residual of stage 1 is r = sgn(y) (|y| - c) with c the positive centroid.
 // Per-row constants of the symmetric quantizers, in units of S = H x (the
-// unnormalised transform, S = y n sqrt(D)): hb = B/2, c2, dc = c3 - c2 and
-// he = E/2 scaled by den = n sqrt(D).
+// unnormalised transform, S = y n sqrt(D)): the positive boundaries B and E
+// of the two stages, B - c2, dc = c3 - c2 and (b = 1) c1, each scaled by
+// den = n sqrt(D).
 struct SymRow {
-    float hb, c2, dc, he, c1;
+    float bb, be, bc2, dc, c1;
 };
 
-// The distance from |y| to the nearest of {0, B} is | | |y| - B/2 | - B/2 |,
-// and the same quantity t2 = | |y| - B/2 | - B/2 is positive exactly when
-// |y| > B, so one value gives both the decision and the margin.  The centroid
-// step uses a saturated multiply (1 when t2 > 0, 0 when t2 <= 0), which keeps
-// the selection on the FMA pipe.  The code bits are sign bits of y, y t2, y ra
-// and y ra t4: the sign of an IEEE product is the XOR of its operands' signs
-// (zeros and flushed results included), so the XORs run as fp32-pair
-// multiplies on the FMA pipe.  Two coordinates (a pair) per call.
+// t2 = |y| - B is positive exactly when |y| > B; the margin of stage 1 is the
+// distance to the nearer of its boundaries 0 and B, min(|y|, |t2|), taken with
+// the running minimum in one three-input min.  The centroid step uses a
+// saturated multiply (1 when t2 > 0, 0 when t2 <= 0), which keeps the
+// selection on the FMA pipe; ra = |y| - c(i) and t4 = |ra| - E likewise for
+// stage 2.  The code bits are sign bits of y, y t2, y ra and y ra t4: the sign
+// of an IEEE product is the XOR of its operands' signs (zeros and flushed
+// results included), so the XORs run as fp32-pair multiplies on the FMA pipe.
+// A value exactly on a boundary has margin 0 and goes to the exact path.  Two
+// coordinates (a pair) per call.
 __device__ __forceinline__ void sym2_code2(float2 y, const SymRow &k, uint32_t &a1x, uint32_t &a2x,
                                            uint32_t &a1y, uint32_t &a2y, float &mx, float &my)
 {
-    const float2 t2a = make_float2(fabsf(y.x) - k.hb, fabsf(y.y) - k.hb);
-    const float2 t2 = make_float2(fabsf(t2a.x) - k.hb, fabsf(t2a.y) - k.hb);
+    const float2 t2 = make_float2(fabsf(y.x) - k.bb, fabsf(y.y) - k.bb);
     const float2 su = make_float2(__saturatef(t2.x * 1.2676506e30f), __saturatef(t2.y * 1.2676506e30f));  // 2^100
-    // |y| - c2 = (|y| - B/2) + (B/2 - c2)
-    const float2 ya = __fadd2_rn(t2a, make_float2(k.hb - k.c2, k.hb - k.c2));
+    // |y| - c2 = (|y| - B) + (B - c2)
+    const float2 ya = __fadd2_rn(t2, make_float2(k.bc2, k.bc2));
     const float2 ra = __ffma2_rn(make_float2(-k.dc, -k.dc), su, ya);
-    const float2 t4 = make_float2(fabsf(fabsf(ra.x) - k.he) - k.he, fabsf(fabsf(ra.y) - k.he) - k.he);
-    mx = fminf(mx, fminf(fabsf(t2.x), fabsf(t4.x)));
-    my = fminf(my, fminf(fabsf(t2.y), fabsf(t4.y)));
+    const float2 t4 = make_float2(fabsf(ra.x) - k.be, fabsf(ra.y) - k.be);
+    mx = fminf(fminf(mx, fabsf(y.x)), fabsf(t2.x));
+    my = fminf(fminf(my, fabsf(y.y)), fabsf(t2.y));
+    mx = fminf(fminf(mx, fabsf(ra.x)), fabsf(t4.x));
+    my = fminf(fminf(my, fabsf(ra.y)), fabsf(t4.y));
     const float2 p1 = __fmul2_rn(y, t2);
     const float2 p2 = __fmul2_rn(y, ra);
     const float2 p3 = __fmul2_rn(p2, t4);
@@ -593,10 +597,10 @@ __global__ void __launch_bounds__(enc_warps(BITS, MODE) * 32, 1)
 
         // symmetric modes quantize S itself against thresholds scaled by den
         SymRow sk;
-        sk.hb = 0.5f * p.b1[(1 << BITS) - 2] * den;
-        sk.c2 = p.c1[(1 << BITS) - 2] * den;
+        sk.bb = p.b1[(1 << BITS) - 2] * den;
+        sk.be = p.b2[(1 << BITS) - 2] * den;
+        sk.bc2 = (p.b1[(1 << BITS) - 2] - p.c1[(1 << BITS) - 2]) * den;
         sk.dc = (p.c1[(1 << BITS) - 1] - p.c1[(1 << BITS) - 2]) * den;
-        sk.he = 0.5f * p.b2[(1 << BITS) - 2] * den;
         sk.c1 = p.c1[(1 << BITS) - 1] * den;
         const float guard = MODE == MODE_SYM ? p.guard * den : p.guard;
 
