@@ -81,6 +81,8 @@ struct RvqEncodeParams {
 };
 
 struct RvqDecodeParams {
+    CUtensorMap tm1, tm2;  // b >= 2: the packed words as [N rows, W] uint32, 16-row boxes,
+                           // 32- or 64-byte swizzle (set by the launcher)
     const uint32_t *p1, *p2;
     const float *norms;
     void *out;           // fp16 [N, 128]
@@ -198,5 +200,9 @@ int sm_count();
 // encoder is unavailable or rejects the layout.
 bool encode_tmap_f16(CUtensorMap *map, const void *base, int rank, const uint64_t *dims,
                      const uint64_t *strides, const uint32_t *box, bool swizzle128, bool promote256);
+// Tensor map over packed words [rows, words] uint32 with boxes of
+// {words, box_rows}; swizzle_bytes 0, 32 or 64 (the row length in bytes).
+bool encode_tmap_words(CUtensorMap *map, const void *base, uint64_t rows, uint32_t words, uint32_t box_rows,
+                       int swizzle_bytes);
 
 }  // namespace vq

@@ -775,8 +775,10 @@ __host__ __device__ constexpr int dec_warp_bytes(int bits) { return DEC_STAGES *
 __host__ __device__ constexpr int dec_table_bytes(int bits) { return bits == 4 ? 256 * 32 * 4 : 0; }
 __host__ __device__ constexpr int dec_smem(int bits)
 {
-    // + 256 B: sign masks of the randomised rotation (64 pair words)
-    return dec_table_bytes(bits) + DEC_WARPS * (dec_warp_bytes(bits) + DEC_STAGES * 8) + 256;
+    // 1024-byte alignment of the (swizzled) stages, the b = 4 table, every
+    // warp's stages, every warp's output staging, the mbarriers and the sign
+    // masks of the randomised rotation (64 pair words)
+    return 1024 + dec_table_bytes(bits) + DEC_WARPS * dec_warp_bytes(bits) + DEC_WARPS * DEC_STAGES * 8 + 256;
 }
 
 // Decoded values c1[i1] + c2[i2] of the 64 coordinates of one half row, as 32
@@ -828,17 +830,20 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) rvq_decode_kernel(const __g
     constexpr int W = D * BITS / 32;
     constexpr int WH = W / 2;  // words per half row
     constexpr int STG = dec_stage(BITS);
-    constexpr int WB = dec_warp_bytes(BITS);
-    extern __shared__ __align__(128) unsigned char smem[];
+    extern __shared__ __align__(128) unsigned char smem_raw[];
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int rr = lane & 15, hh = lane >> 4;
+    unsigned char *smem = smem_1k(smem_raw);
     float *stab = reinterpret_cast<float *>(smem);  // b = 4: merged table, replicated per lane
-    unsigned char *wbuf = smem + dec_table_bytes(BITS) + warp * WB;
-    unsigned char *obuf = wbuf + DEC_STAGES * STG;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + dec_table_bytes(BITS) + DEC_WARPS * WB) + warp * DEC_STAGES;
+    unsigned char *stages = smem + dec_table_bytes(BITS);  // every warp's stages, 1024-byte aligned
+    unsigned char *wbuf = stages + warp * DEC_STAGES * STG;
+    unsigned char *obufs = stages + DEC_WARPS * DEC_STAGES * STG;
+    unsigned char *obuf = obufs + warp * DROWS * ROW_STRIDE;
+    uint64_t *bars_all = reinterpret_cast<uint64_t *>(obufs + DEC_WARPS * DROWS * ROW_STRIDE);
+    uint64_t *bars = bars_all + warp * DEC_STAGES;
     // sign masks: word hh * 32 + k flips output coordinates 64 hh + 2k, 64 hh + 2k + 1
-    uint32_t *sgm = reinterpret_cast<uint32_t *>(smem + dec_table_bytes(BITS) + DEC_WARPS * (WB + DEC_STAGES * 8));
+    uint32_t *sgm = reinterpret_cast<uint32_t *>(bars_all + DEC_WARPS * DEC_STAGES);
     if (lane == 0) {
 #pragma unroll
         for (int s = 0; s < DEC_STAGES; ++s) mbar_init(&bars[s], 1);
@@ -866,10 +871,18 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) rvq_decode_kernel(const __g
     auto issue = [&](int blk, int s) {
         if (lane == 0) {
             const int r0 = blk * DROWS;
-            const uint32_t bytes = (uint32_t)(min(DROWS, p.N - r0) * W * 4);
-            mbar_arrive_expect_tx(&bars[s], 2 * bytes);
-            bulk_g2s(wbuf + s * STG, p.p1 + (size_t)r0 * W, bytes, &bars[s], pol);
-            bulk_g2s(wbuf + s * STG + STG / 2, p.p2 + (size_t)r0 * W, bytes, &bars[s], pol);
+            if constexpr (BITS >= 2) {
+                // 16-row boxes of both streams with the 32- (b = 2) or 64-byte
+                // (b = 4) swizzle; rows past N arrive as zeros
+                mbar_arrive_expect_tx(&bars[s], (uint32_t)(2 * DROWS * W * 4));
+                tma_load_2d(wbuf + s * STG, &p.tm1, 0, r0, &bars[s], pol);
+                tma_load_2d(wbuf + s * STG + STG / 2, &p.tm2, 0, r0, &bars[s], pol);
+            } else {
+                const uint32_t bytes = (uint32_t)(min(DROWS, p.N - r0) * W * 4);
+                mbar_arrive_expect_tx(&bars[s], 2 * bytes);
+                bulk_g2s(wbuf + s * STG, p.p1 + (size_t)r0 * W, bytes, &bars[s], pol);
+                bulk_g2s(wbuf + s * STG + STG / 2, p.p2 + (size_t)r0 * W, bytes, &bars[s], pol);
+            }
         }
     };
 #pragma unroll
@@ -895,7 +908,22 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) rvq_decode_kernel(const __g
             return;
         }
         uint32_t w1[WH], w2[WH];
-        {
+        if constexpr (BITS >= 2) {
+            // 16-byte chunk k of row rr sits at chunk k ^ ((rr >> 1) & 3) (64-byte
+            // rows, 64-byte swizzle) or k ^ ((rr >> 2) & 1) (32-byte rows, 32-byte
+            // swizzle): the lanes of a quarter warp read distinct banks
+            const unsigned char *ra = wbuf + s * STG + rr * (W * 4);
+            const unsigned char *rb = ra + STG / 2;
+#pragma unroll
+            for (int k2 = 0; k2 < WH / 4; ++k2) {
+                const int k = hh * (WH / 4) + k2;
+                const int pk = BITS == 4 ? (k ^ ((rr >> 1) & 3)) : (k ^ ((rr >> 2) & 1));
+                const uint4 a = *reinterpret_cast<const uint4 *>(ra + (pk << 4));
+                const uint4 b = *reinterpret_cast<const uint4 *>(rb + (pk << 4));
+                w1[4 * k2] = a.x; w1[4 * k2 + 1] = a.y; w1[4 * k2 + 2] = a.z; w1[4 * k2 + 3] = a.w;
+                w2[4 * k2] = b.x; w2[4 * k2 + 1] = b.y; w2[4 * k2 + 2] = b.z; w2[4 * k2 + 3] = b.w;
+            }
+        } else {
             const uint32_t *sa = reinterpret_cast<const uint32_t *>(wbuf + s * STG) + rr * W + hh * WH;
             const uint32_t *sb = reinterpret_cast<const uint32_t *>(wbuf + s * STG + STG / 2) + rr * W + hh * WH;
 #pragma unroll
@@ -997,8 +1025,15 @@ cudaError_t launch_enc(const RvqEncodeParams &p0, cudaStream_t stream)
 }
 
 template <int BITS>
-cudaError_t launch_dec(const RvqDecodeParams &p, cudaStream_t stream)
+cudaError_t launch_dec(const RvqDecodeParams &p0, cudaStream_t stream)
 {
+    RvqDecodeParams p = p0;
+    if constexpr (BITS >= 2) {
+        constexpr uint32_t W = D * BITS / 32;
+        if (!encode_tmap_words(&p.tm1, p.p1, (uint64_t)p.N, W, DROWS, (int)(W * 4)) ||
+            !encode_tmap_words(&p.tm2, p.p2, (uint64_t)p.N, W, DROWS, (int)(W * 4)))
+            return cudaErrorInvalidValue;
+    }
     auto kern = p.has_sgn ? rvq_decode_kernel<BITS, true> : rvq_decode_kernel<BITS, false>;
     constexpr int smem = dec_smem(BITS);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);

@@ -55,4 +55,22 @@ bool encode_tmap_f16(CUtensorMap *map, const void *base, int rank, const uint64_
     return r == CUDA_SUCCESS;
 }
 
+bool encode_tmap_words(CUtensorMap *map, const void *base, uint64_t rows, uint32_t words, uint32_t box_rows,
+                       int swizzle_bytes)
+{
+    EncodeTiled fn = encoder();
+    if (fn == nullptr) return false;
+    const cuuint64_t gd[2] = {words, rows};
+    const cuuint64_t gs[1] = {(cuuint64_t)words * 4};
+    const cuuint32_t bx[2] = {words, box_rows};
+    const cuuint32_t es[2] = {1, 1};
+    const CUtensorMapSwizzle sw = swizzle_bytes == 64   ? CU_TENSOR_MAP_SWIZZLE_64B
+                                  : swizzle_bytes == 32 ? CU_TENSOR_MAP_SWIZZLE_32B
+                                                        : CU_TENSOR_MAP_SWIZZLE_NONE;
+    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void *>(base), gd, gs, bx, es,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 }  // namespace vq
