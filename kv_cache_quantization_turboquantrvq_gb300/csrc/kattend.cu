@@ -92,11 +92,12 @@ __device__ __forceinline__ void ka_load_query(const KiviAttendParams &p, int b, 
 }
 
 // Merge the warps' (m, l, o) through shared memory and write the output (one
-// part) or this part's partial.  o is per lane coordinates 4 lane .. + 3.
+// part) or this part's partial.  o holds the lane's coordinates cbase .. + 3
+// (the 32 lanes of a warp cover all 128).
 template <int GQ>
 __device__ __forceinline__ void ka_merge_write(const KiviAttendParams &p, unsigned char *scratch, int b, int h,
                                                int part, int nparts, const float (&m)[GQ], const float (&l)[GQ],
-                                               const float (&o)[GQ][4])
+                                               const float (&o)[GQ][4], int cbase)
 {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nw = blockDim.x >> 5;
@@ -109,7 +110,7 @@ __device__ __forceinline__ void ka_merge_write(const KiviAttendParams &p, unsign
             ms[warp * GQ + g] = m[g];
             ls[warp * GQ + g] = l[g];
         }
-        *reinterpret_cast<float4 *>(os + (warp * GQ + g) * D + 4 * lane) = make_float4(o[g][0], o[g][1], o[g][2], o[g][3]);
+        *reinterpret_cast<float4 *>(os + (warp * GQ + g) * D + cbase) = make_float4(o[g][0], o[g][1], o[g][2], o[g][3]);
     }
     __syncthreads();
     for (int i = threadIdx.x; i < GQ * D; i += blockDim.x) {
@@ -200,21 +201,27 @@ __global__ void __launch_bounds__(KA_WARPS * 32, 1) kivi_attend_kernel(const __g
     __syncthreads();
 
     const int tg = lane >> 3, cg = lane & 7;
-    // key bits of this lane's 8 tokens: word kw0, from bit ksh
+    // key bits of this lane's 8 tokens: word kw0, from bit ksh; token j's code
+    // sits at bit j * BITS of x = word >> ksh (b = 4: tokens 4..7 at bit
+    // 4 (j - 4) of x >> 16, so that every masked code stays below 2^20)
     constexpr int KBITS8 = 8 * BITS;
     const int kw0 = (tg * KBITS8) / 32, ksh = (tg * KBITS8) % 32;
-    // value bits of this lane's 4 coordinates: word vwi, from bit vsh; group vj
-    const int vwi = (4 * lane * BITS) / 32, vsh = (4 * lane * BITS) % 32, vj = (4 * lane) / G;
+    // values: lane (vh, cl) takes coordinates 8 cl .. 8 cl + 7 (one value
+    // group) of the tokens of parity vh; their codes at bit c * BITS of
+    // word vwi >> vsh (b = 4: coordinates 4..7 of the high half)
+    const int vh = lane >> 4, cl = lane & 15;
+    const int vwi = (8 * cl * BITS) / 32, vsh = (8 * cl * BITS) % 32, vj = (8 * cl) / G;
     float *my_w = wb + warp * KT * GQ;
 
-    float m[GQ], l[GQ], o[GQ][4], zb[GQ];
+    float m[GQ], l[GQ], zb[GQ];
+    float2 o2[GQ][4];  // coordinate pairs (2i, 2i + 1) of the lane's 8, scaled by 2^(code shift)
 #pragma unroll
     for (int g = 0; g < GQ; ++g) {
         m[g] = NEG_INF;
         l[g] = 0.0f;
         zb[g] = 0.0f;  // sum of w z (the value zeros' share), per head
 #pragma unroll
-        for (int c = 0; c < 4; ++c) o[g][c] = 0.0f;
+        for (int i = 0; i < 4; ++i) o2[g][i] = f2(0.0f, 0.0f);
     }
 
     for (int it = 0;; ++it) {
@@ -239,7 +246,8 @@ __global__ void __launch_bounds__(KA_WARPS * 32, 1) kivi_attend_kernel(const __g
         const __half *kze = reinterpret_cast<const __half *>(sb + KW + 256);
 
         // ---- scores: partial dot products over this lane's 16 channels for
-        // its 8 tokens (token pairs in the two halves of a float2)
+        // its 8 tokens (token pairs in the two halves of a float2), each code
+        // scaled by 2^(its bit offset) until the end of the channel loop
         float2 acc[4][GQ];
         float bias[GQ];
 #pragma unroll
@@ -261,34 +269,51 @@ __global__ void __launch_bounds__(KA_WARPS * 32, 1) kivi_attend_kernel(const __g
             const float2 z23 = __half22float2(*reinterpret_cast<const __half2 *>(&zv.y));
             const float sc[4] = {s01.x, s01.y, s23.x, s23.y};
             const float ze[4] = {z01.x, z01.y, z23.x, z23.y};
+            float qd[GQ][4];
+#pragma unroll
+            for (int g = 0; g < GQ; ++g) {
+                const float4 q4 = *reinterpret_cast<const float4 *>(qf + g * D + d0);
+                qd[g][0] = q4.x; qd[g][1] = q4.y; qd[g][2] = q4.z; qd[g][3] = q4.w;
+            }
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 const uint32_t x = ww[c] >> ksh;
+                const uint32_t xh = BITS == 4 ? x >> 16 : x;
                 float2 cf[4];
 #pragma unroll
-                for (int jp = 0; jp < 4; ++jp)
-                    cf[jp] = __fadd2_rn(f2(magic_code(x >> (2 * jp * BITS), MASK), magic_code(x >> ((2 * jp + 1) * BITS), MASK)),
+                for (int jp = 0; jp < 4; ++jp) {
+                    const int j0 = 2 * jp, j1 = 2 * jp + 1;
+                    const uint32_t s0b = (uint32_t)((BITS == 4 && j0 >= 4 ? j0 - 4 : j0) * BITS);
+                    const uint32_t s1b = (uint32_t)((BITS == 4 && j1 >= 4 ? j1 - 4 : j1) * BITS);
+                    const uint32_t src0 = (BITS == 4 && j0 >= 4) ? xh : x;
+                    const uint32_t src1 = (BITS == 4 && j1 >= 4) ? xh : x;
+                    cf[jp] = __fadd2_rn(f2(magic_code(src0, MASK << s0b), magic_code(src1, MASK << s1b)),
                                         f2(-TWO23, -TWO23));
+                }
 #pragma unroll
                 for (int g = 0; g < GQ; ++g) {
-                    const float qd = qf[g * D + d0 + c];
-                    const float qk = qd * sc[c];
-                    bias[g] = fmaf(qd, ze[c], bias[g]);
+                    const float qk = qd[g][c] * sc[c];
+                    bias[g] = fmaf(qd[g][c], ze[c], bias[g]);
 #pragma unroll
                     for (int jp = 0; jp < 4; ++jp) acc[jp][g] = __ffma2_rn(f2(qk, qk), cf[jp], acc[jp][g]);
                 }
             }
         }
-        // ---- reduce over the 8 lanes of the token group: exchange on the
-        // token bits so that lane cg ends with token cg (all heads)
+        // undo the code scales (exact powers of two) and add the zero term
         float v8[8][GQ];
 #pragma unroll
-        for (int g = 0; g < GQ; ++g)
+        for (int jp = 0; jp < 4; ++jp) {
+            const int j0 = 2 * jp, j1 = 2 * jp + 1;
+            const float u0 = __int_as_float((127 - (BITS == 4 && j0 >= 4 ? j0 - 4 : j0) * BITS) << 23);
+            const float u1 = __int_as_float((127 - (BITS == 4 && j1 >= 4 ? j1 - 4 : j1) * BITS) << 23);
 #pragma unroll
-            for (int jp = 0; jp < 4; ++jp) {
-                v8[2 * jp][g] = acc[jp][g].x + bias[g];
-                v8[2 * jp + 1][g] = acc[jp][g].y + bias[g];
+            for (int g = 0; g < GQ; ++g) {
+                v8[j0][g] = fmaf(acc[jp][g].x, u0, bias[g]);
+                v8[j1][g] = fmaf(acc[jp][g].y, u1, bias[g]);
             }
+        }
+        // ---- reduce over the 8 lanes of the token group: exchange on the
+        // token bits so that lane cg ends with token cg (all heads)
         {
             const bool hi4 = (cg & 4) != 0;
 #pragma unroll
@@ -329,7 +354,7 @@ __global__ void __launch_bounds__(KA_WARPS * 32, 1) kivi_attend_kernel(const __g
                 l[g] *= f;
                 zb[g] *= f;
 #pragma unroll
-                for (int c = 0; c < 4; ++c) o[g][c] *= f;
+                for (int i = 0; i < 4; ++i) o2[g][i] = __fmul2_rn(o2[g][i], f2(f, f));
                 m[g] = mt;
             }
             wv[g] = exp2f(sc - m[g]);
@@ -339,52 +364,54 @@ __global__ void __launch_bounds__(KA_WARPS * 32, 1) kivi_attend_kernel(const __g
         for (int g = 0; g < GQ; ++g) my_w[lane * GQ + g] = wv[g];
         __syncwarp();
 
-        // ---- values: coordinates 4 lane .. 4 lane + 3, two tokens per paired FMA
+        // ---- values: lane (vh, cl), coordinates 8 cl .. 8 cl + 7 of the
+        // tokens k = vh, vh + 2, ...; coordinate pairs per paired FMA
         {
             const uint32_t *vwords = reinterpret_cast<const uint32_t *>(sb + KW + 512);
             const __half *vsc = reinterpret_cast<const __half *>(sb + KW + 512 + VW);
             const __half *vze = reinterpret_cast<const __half *>(sb + KW + 512 + VW + VS);
-            float2 o2[GQ][4], z2[GQ];
-#pragma unroll
-            for (int g = 0; g < GQ; ++g) {
-                z2[g] = f2(0.0f, 0.0f);
-#pragma unroll
-                for (int c = 0; c < 4; ++c) o2[g][c] = f2(0.0f, 0.0f);
-            }
-            auto pair = [&](int k, bool second) {
-                // tokens k and k + 1 (the second only when `second`)
-                const uint32_t x0 = vwords[k * W + vwi] >> vsh;
-                const uint32_t x1 = second ? vwords[(k + 1) * W + vwi] >> vsh : 0u;
-                const float s0v = __half2float(vsc[k * (D / G) + vj]);
-                const float s1v = second ? __half2float(vsc[(k + 1) * (D / G) + vj]) : 0.0f;
-                const float z0v = __half2float(vze[k * (D / G) + vj]);
-                const float z1v = second ? __half2float(vze[(k + 1) * (D / G) + vj]) : 0.0f;
+            auto token = [&](int k) {
+                const uint32_t x = vwords[k * W + vwi] >> vsh;
+                const uint32_t xh = BITS == 4 ? x >> 16 : x;
+                const float sk = __half2float(vsc[k * (D / G) + vj]);
+                const float zk = __half2float(vze[k * (D / G) + vj]);
                 float2 cf[4];
 #pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    cf[c] = __fadd2_rn(f2(magic_code(x0 >> (c * BITS), MASK), magic_code(x1 >> (c * BITS), MASK)),
+                for (int i = 0; i < 4; ++i) {
+                    const int c0 = 2 * i, c1 = 2 * i + 1;
+                    const uint32_t s0b = (uint32_t)((BITS == 4 && c0 >= 4 ? c0 - 4 : c0) * BITS);
+                    const uint32_t s1b = (uint32_t)((BITS == 4 && c1 >= 4 ? c1 - 4 : c1) * BITS);
+                    const uint32_t src0 = (BITS == 4 && c0 >= 4) ? xh : x;
+                    const uint32_t src1 = (BITS == 4 && c1 >= 4) ? xh : x;
+                    cf[i] = __fadd2_rn(f2(magic_code(src0, MASK << s0b), magic_code(src1, MASK << s1b)),
                                        f2(-TWO23, -TWO23));
+                }
+                float wk[GQ];
+                if constexpr (GQ == 1) {
+                    wk[0] = my_w[k];
+                } else if constexpr (GQ == 2) {
+                    const float2 w2 = *reinterpret_cast<const float2 *>(my_w + k * 2);
+                    wk[0] = w2.x; wk[1] = w2.y;
+                } else {
+#pragma unroll
+                    for (int g = 0; g < GQ; g += 4) {
+                        const float4 w4 = *reinterpret_cast<const float4 *>(my_w + k * GQ + g);
+                        wk[g] = w4.x; wk[g + 1] = w4.y; wk[g + 2] = w4.z; wk[g + 3] = w4.w;
+                    }
+                }
 #pragma unroll
                 for (int g = 0; g < GQ; ++g) {
-                    const float w0 = my_w[k * GQ + g];
-                    const float w1 = second ? my_w[(k + 1) * GQ + g] : 0.0f;
-                    const float2 a = __fmul2_rn(f2(w0, w1), f2(s0v, s1v));
-                    z2[g] = __ffma2_rn(f2(w0, w1), f2(z0v, z1v), z2[g]);
+                    const float a = wk[g] * sk;
+                    zb[g] = fmaf(wk[g], zk, zb[g]);
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) o2[g][c] = __ffma2_rn(a, cf[c], o2[g][c]);
+                    for (int i = 0; i < 4; ++i) o2[g][i] = __ffma2_rn(f2(a, a), cf[i], o2[g][i]);
                 }
             };
             if (n == KT) {
 #pragma unroll 4
-                for (int k = 0; k < KT; k += 2) pair(k, true);
+                for (int k = vh; k < KT; k += 2) token(k);
             } else {
-                for (int k = 0; k < n; k += 2) pair(k, k + 1 < n);
-            }
-#pragma unroll
-            for (int g = 0; g < GQ; ++g) {
-                zb[g] += z2[g].x + z2[g].y;
-#pragma unroll
-                for (int c = 0; c < 4; ++c) o[g][c] += o2[g][c].x + o2[g][c].y;
+                for (int k = vh; k < n; k += 2) token(k);
             }
         }
 
@@ -393,18 +420,32 @@ __global__ void __launch_bounds__(KA_WARPS * 32, 1) kivi_attend_kernel(const __g
         if (t + KA_STAGES * KA_WARPS < ntiles) issue(t + KA_STAGES * KA_WARPS, st);
     }
 
-    // l: each lane summed its own tokens' weights; zb: each lane summed the
-    // weighted zeros of its coordinates' value group, which every one of its
-    // 4 coordinates receives
+    // l: each lane summed its own tokens' weights; the value halves (vh = 0, 1)
+    // hold the even and odd tokens of the same 8 coordinates: add them, undo
+    // the code scales, and fold in the zeros' share (one value group per lane)
+    float o[GQ][4];
 #pragma unroll
     for (int g = 0; g < GQ; ++g) {
 #pragma unroll
         for (int off = 16; off >= 1; off >>= 1) l[g] += __shfl_xor_sync(FULL_MASK, l[g], off);
+        zb[g] += __shfl_xor_sync(FULL_MASK, zb[g], 16);
+        float full[8];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) o[g][c] += zb[g];
+        for (int i = 0; i < 4; ++i) {
+            const float ox = o2[g][i].x + __shfl_xor_sync(FULL_MASK, o2[g][i].x, 16);
+            const float oy = o2[g][i].y + __shfl_xor_sync(FULL_MASK, o2[g][i].y, 16);
+            const int c0 = 2 * i, c1 = 2 * i + 1;
+            const float u0 = __int_as_float((127 - (BITS == 4 && c0 >= 4 ? c0 - 4 : c0) * BITS) << 23);
+            const float u1 = __int_as_float((127 - (BITS == 4 && c1 >= 4 ? c1 - 4 : c1) * BITS) << 23);
+            full[c0] = fmaf(ox, u0, zb[g]);
+            full[c1] = fmaf(oy, u1, zb[g]);
+        }
+        // this lane publishes coordinates 8 cl + 4 vh .. + 3
+#pragma unroll
+        for (int c = 0; c < 4; ++c) o[g][c] = vh ? full[4 + c] : full[c];
     }
     __syncthreads();
-    ka_merge_write<GQ>(p, stages, b, h, split, nparts, m, l, o);
+    ka_merge_write<GQ>(p, stages, b, h, split, nparts, m, l, o, 8 * cl + 4 * vh);
 }
 
 // The fp16 residual window of one (sequence, kv head): warp w takes tokens
@@ -465,7 +506,7 @@ __global__ void __launch_bounds__(KA_WARPS * 32) kivi_attend_residual_kernel(con
         }
     }
     // l is already the warp's total (every lane holds the same sums)
-    ka_merge_write<GQ>(p, scratch, b, h, p.nsplit, nparts, m, l, o);
+    ka_merge_write<GQ>(p, scratch, b, h, p.nsplit, nparts, m, l, o, 4 * lane);
 }
 
 // Combine the parts of one (sequence, query head): the quantized chunks that
