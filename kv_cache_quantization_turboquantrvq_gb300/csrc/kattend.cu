@@ -11,18 +11,22 @@
 //
 // Keys.  With the group's scale s and zero z of channel d,
 //   q . k_t = sum_d (q_d s_d) code_{t,d} + sum_d q_d z_d,
-// so a 32-token tile (inside one key group: G is a multiple of 32) costs one
-// product q_d s_d per channel and one fused multiply-add per code.  Key words
-// are channel-major (one word holds consecutive tokens of a channel), so lane
-// (tg, cg) = (lane >> 3, lane & 7) takes tokens 8 tg .. 8 tg + 7 and channels
-// 16 cg .. 16 cg + 15: its partial dot products are reduced over the 8 lanes
-// of its token group by an exchange that leaves token `lane` on lane `lane`
-// (one key per lane for the online softmax).  Codes become floats by the
-// 2^23 magic-number trick (OR into the mantissa of 2^23, subtract 2^23), two
-// tokens at a time, so the arithmetic runs as paired FMAs.
-// Values.  sum_t w_t (code_{t,d} s_t + z_t) = sum_t (w_t s_t) code_{t,d} +
-// sum_t w_t z_t: lanes own 4 coordinates (inside one value group), two tokens
-// per paired FMA.
+// a dense product of the tile's codes [32 tokens x 128 channels] with the
+// columns (q s) of the GQ query heads.  Values, with the token's scale s_t and
+// zero z_t of the coordinate's group,
+//   sum_t w_t v_{t,d} = sum_t code_{t,d} (w_t s_t) + sum_t w_t z_t,
+// a dense product of the codes [128 coordinates x 32 tokens] with the columns
+// (w s).  Both run on the tensor cores as 16 x 8 x 16 tiles (mma.sync, fp16
+// operands, fp32 accumulation): the codes are exact in fp16 (byte-permuted
+// into place, masked into the mantissa of 1024 and 1024 subtracted, each row
+// still scaled by a power of two that the epilogue removes), and every float
+// column is carried as two fp16 columns, u rounded to fp16 and the rounded
+// rest, so a head's products keep about 22 bits.  The 8 columns of a tile are
+// 4 heads x (hi, lo).  The tensor-core rate is not the limit (the columns are
+// few): the gain is that one instruction does 2048 multiply-adds, leaving
+// the byte shuffling of the codes as the main cost.  The query
+// is scaled by a power of two so that |q| <= 1 and every q s fits in fp16.
+// The zero terms are plain sums (one per head and group).
 // Grid, staging and merging as the RVQ attention: fixed-size chunks of the
 // quantized tokens per CTA, one more CTA per (sequence, kv head) for the
 // residual window, per-warp double-buffered bulk copies (key words, the
@@ -44,7 +48,6 @@ constexpr int KA_WARPS = 8;
 constexpr int KT = 32;  // tokens per warp tile
 constexpr int KA_STAGES = 2;
 constexpr float NEG_INF = -__builtin_huge_valf();
-constexpr float TWO23 = 8388608.0f;
 
 __host__ __device__ constexpr int ka_stage(int bits, int G)
 {
@@ -60,58 +63,54 @@ __host__ __device__ constexpr int ka_region(int bits, int G, int GQ)
                ? KA_WARPS * KA_STAGES * ka_stage(bits, G)
                : KA_WARPS * GQ * (D + 2) * 4;
 }
+constexpr int QS = D + 16;  // query row stride (floats): rows of 4 heads fall on 2 bank halves
 __host__ __device__ constexpr int ka_smem(int bits, int G, int GQ)
 {
-    // query [g][d], weights [warp][token][g], stages / merge, mbarriers
-    return D * GQ * 4 + KA_WARPS * KT * GQ * 4 + ka_region(bits, G, GQ) + KA_WARPS * KA_STAGES * 8;
+    // query [g][QS], weights [warp][g][slot], stages / merge, mbarriers
+    return QS * GQ * 4 + KA_WARPS * KT * GQ * 4 + ka_region(bits, G, GQ) + KA_WARPS * KA_STAGES * 8;
 }
 
-__device__ __forceinline__ int ord_of(float x)
+// Load the GQ query rows of kv head h, times scale * log2 e, into qf (row
+// stride STRIDE).  With `bounded`, the rows are also multiplied by 2^-e, the
+// smallest power of two that brings every |entry| to at most 1 (e >= 0), and
+// 2^e is returned: the products q_d s_d of the key scores then stay inside
+// the fp16 range whatever the key scales (|s| <= 65504), and the scores are
+// multiplied back by 2^e, exactly.
+template <int GQ, int STRIDE>
+__device__ __forceinline__ float ka_load_query(const KiviAttendParams &p, int b, int h, float *qf, bool bounded)
 {
-    const int i = __float_as_int(x);
-    return i >= 0 ? i : i ^ 0x7fffffff;
-}
-__device__ __forceinline__ float float_of_ord(int i) { return __int_as_float(i >= 0 ? i : i ^ 0x7fffffff); }
-__device__ __forceinline__ float2 f2(float a, float b) { return make_float2(a, b); }
-
-// 2^23 + (x & m) as a float: the code in the low mantissa bits of 2^23.
-__device__ __forceinline__ float magic_code(uint32_t x, uint32_t m)
-{
-    return __uint_as_float((x & m) | 0x4B000000u);
-}
-
-// Load and scale the GQ query rows of kv head h (fp32, times scale * log2 e).
-template <int GQ>
-__device__ __forceinline__ void ka_load_query(const KiviAttendParams &p, int b, int h, float *qf)
-{
+    const __half *q = static_cast<const __half *>(p.q) + ((size_t)b * p.Hq + (size_t)h * GQ) * D;
+    const float qs = p.qscale;
+    float pe = 1.0f, ps = 1.0f;
+    if (bounded) {
+        const int lane = threadIdx.x & 31;
+        float mx = 0.0f;
+        for (int i = lane; i < GQ * D; i += 32) mx = fmaxf(mx, fabsf(__half2float(q[i])));
+        mx = __uint_as_float(__reduce_max_sync(FULL_MASK, __float_as_uint(mx))) * fabsf(qs);
+        if (mx > 1.0f && mx <= 3.0e38f) {
+            const int ex = (int)((__float_as_uint(mx) >> 23) & 0xffu) - 126;  // mx < 2^ex
+            pe = __uint_as_float((uint32_t)(127 + ex) << 23);
+            ps = __uint_as_float((uint32_t)(127 - ex) << 23);
+        }
+    }
     for (int i = threadIdx.x; i < GQ * D; i += blockDim.x) {
         const int g = i / D, d = i - g * D;
-        const __half v = static_cast<const __half *>(p.q)[((size_t)b * p.Hq + (size_t)h * GQ + g) * D + d];
-        qf[g * D + d] = __half2float(v) * p.qscale;
+        qf[g * STRIDE + d] = __half2float(q[i]) * qs * ps;
     }
+    return pe;
 }
 
-// Merge the warps' (m, l, o) through shared memory and write the output (one
-// part) or this part's partial.  o holds the lane's coordinates cbase .. + 3
-// (the 32 lanes of a warp cover all 128).
+// Merge the warps' (m, l, o) staged in shared memory (ms[warp][g],
+// ls[warp][g], os[warp][g][d]) and write the output (one part) or this part's
+// partial.
 template <int GQ>
-__device__ __forceinline__ void ka_merge_write(const KiviAttendParams &p, unsigned char *scratch, int b, int h,
-                                               int part, int nparts, const float (&m)[GQ], const float (&l)[GQ],
-                                               const float (&o)[GQ][4], int cbase)
+__device__ __forceinline__ void ka_merge_finish(const KiviAttendParams &p, unsigned char *scratch, int b, int h,
+                                                int part, int nparts)
 {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nw = blockDim.x >> 5;
-    float *ms = reinterpret_cast<float *>(scratch);
-    float *ls = ms + nw * GQ;
-    float *os = ls + nw * GQ;
-#pragma unroll
-    for (int g = 0; g < GQ; ++g) {
-        if (lane == 0) {
-            ms[warp * GQ + g] = m[g];
-            ls[warp * GQ + g] = l[g];
-        }
-        *reinterpret_cast<float4 *>(os + (warp * GQ + g) * D + cbase) = make_float4(o[g][0], o[g][1], o[g][2], o[g][3]);
-    }
+    const float *ms = reinterpret_cast<const float *>(scratch);
+    const float *ls = ms + nw * GQ;
+    const float *os = ls + nw * GQ;
     __syncthreads();
     for (int i = threadIdx.x; i < GQ * D; i += blockDim.x) {
         const int g = i / D, d = i - g * D;
@@ -138,19 +137,78 @@ __device__ __forceinline__ void ka_merge_write(const KiviAttendParams &p, unsign
     }
 }
 
+__device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
+__device__ __forceinline__ __half2 bits_h2(uint32_t u) { return *reinterpret_cast<__half2 *>(&u); }
+
+// One operand register of two fp16 codes: the code in byte `sel` picks of x
+// (low half) and of y (high half), at bit `shift` of that byte (mask m has the
+// code bits of both halves).  OR-ing the masked bits into the mantissa of
+// 1024 and subtracting 1024 leaves code * 2^shift in each half, exactly.
+__device__ __forceinline__ uint32_t code_pair(uint32_t x, uint32_t y, uint32_t sel, uint32_t m)
+{
+    const uint32_t t = (__byte_perm(x, y, sel) & m) | 0x64006400u;
+    return h2_bits(__hsub2(bits_h2(t), bits_h2(0x64006400u)));
+}
+
+// The fp16 pair (hi(u0), hi(u1)), or on `lo` lanes (u0 - hi(u0), u1 - hi(u1))
+// rounded to fp16: the two columns of one head together carry u to about 22
+// bits.
+__device__ __forceinline__ uint32_t split_pack(float u0, float u1, bool lo)
+{
+    const __half2 hi = __floats2half2_rn(u0, u1);
+    const float2 hf = __half22float2(hi);
+    const __half2 lw = __floats2half2_rn(u0 - hf.x, u1 - hf.y);
+    return h2_bits(lo ? lw : hi);
+}
+
+// d += a * b for one 16 x 8 x 16 tile, fp16 operands, fp32 accumulation.
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                          uint32_t b0, uint32_t b1)
+{
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t quad_at(const uint4 &v, int i)
+{
+    return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
+}
+
+// Up to 4 fp16 scales (or zeros) of one token's value groups, as floats.
+template <int NV>
+__device__ __forceinline__ void load_groups(const __half *src, float (&f)[NV])
+{
+    if constexpr (NV == 4) {
+        const uint2 u = *reinterpret_cast<const uint2 *>(src);
+        const float2 a = __half22float2(bits_h2(u.x)), c = __half22float2(bits_h2(u.y));
+        f[0] = a.x; f[1] = a.y; f[2] = c.x; f[3] = c.y;
+    } else if constexpr (NV == 2) {
+        const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(src));
+        f[0] = a.x; f[1] = a.y;
+    } else {
+        f[0] = __half2float(src[0]);
+    }
+}
+
 // One chunk of the quantized tokens of one (sequence, kv head).
 template <int BITS, int G, int GQ>
-__global__ void __launch_bounds__(KA_WARPS * 32, 1) kivi_attend_kernel(const __grid_constant__ KiviAttendParams p)
+__global__ void __launch_bounds__(KA_WARPS * 32, GQ <= 4 ? 2 : 1)
+    kivi_attend_kernel(const __grid_constant__ KiviAttendParams p)
 {
     constexpr int STG = ka_stage(BITS, G);
     constexpr int KW = BITS * 512;            // key words of a tile (bytes)
     constexpr int VW = KT * 16 * BITS;        // value words of a tile (bytes)
     constexpr int VS = KT * (D / G) * 2;      // value scales (or zeros) of a tile (bytes)
     constexpr int W = D * BITS / 32;          // value words per token
+    constexpr int NV = D / G;                 // value groups per token
+    constexpr int NT = (2 * GQ + 7) / 8;      // n-tiles of 8 (head, hi / lo) columns
+    constexpr int MPQ = 8 / BITS;             // value m-tiles per 4 words of a token
     constexpr uint32_t MASK = (1u << BITS) - 1u;
     extern __shared__ __align__(128) unsigned char smem[];
     float *qf = reinterpret_cast<float *>(smem);
-    float *wb = qf + GQ * D;
+    float *wb = qf + GQ * QS;
     unsigned char *stages = reinterpret_cast<unsigned char *>(wb + KA_WARPS * KT * GQ);
     uint64_t *bars = reinterpret_cast<uint64_t *>(stages + ka_region(BITS, G, GQ));
 
@@ -197,31 +255,43 @@ __global__ void __launch_bounds__(KA_WARPS * 32, 1) kivi_attend_kernel(const __g
         const int t = warp + s * KA_WARPS;
         if (t < ntiles) issue(t, s);
     }
-    ka_load_query<GQ>(p, b, h, qf);
+    const float pe = ka_load_query<GQ, QS>(p, b, h, qf, true);
     __syncthreads();
 
-    const int tg = lane >> 3, cg = lane & 7;
-    // key bits of this lane's 8 tokens: word kw0, from bit ksh; token j's code
-    // sits at bit j * BITS of x = word >> ksh (b = 4: tokens 4..7 at bit
-    // 4 (j - 4) of x >> 16, so that every masked code stays below 2^20)
-    constexpr int KBITS8 = 8 * BITS;
-    const int kw0 = (tg * KBITS8) / 32, ksh = (tg * KBITS8) % 32;
-    // values: lane (vh, cl) takes coordinates 8 cl .. 8 cl + 7 (one value
-    // group) of the tokens of parity vh; their codes at bit c * BITS of
-    // word vwi >> vsh (b = 4: coordinates 4..7 of the high half)
-    const int vh = lane >> 4, cl = lane & 15;
-    const int vwi = (8 * cl * BITS) / 32, vsh = (8 * cl * BITS) % 32, vj = (8 * cl) / G;
-    float *my_w = wb + warp * KT * GQ;
+    // Fragment roles (m16n8k16): lane = 4 g8 + t4.  Operand rows are tokens
+    // (keys) or coordinates (values) 16 mt + g8 and + 8; the lane's k entries
+    // 2 t4, 2 t4 + 1, 2 t4 + 8, 2 t4 + 9 are channels 16 kt + 4 t4 + 0..3
+    // (keys) or tokens 16 kt + t4 + 0, 4, 8, 12 (values); its B column g8 is
+    // head 4 nt + g8 / 2, hi part for even g8, lo part for odd; its
+    // accumulator columns 2 t4, 2 t4 + 1 are head 4 nt + t4, hi and lo.
+    const int g8 = lane >> 2, t4 = lane & 3;
+    const bool lo = (g8 & 1) != 0;
+    // a row's code sits at bit ((row BITS) mod 32) of its word: byte
+    // ((row BITS) mod 32) / 8, shift (g8 BITS) mod 8 for every row of the lane
+    const int sh = (g8 * BITS) & 7;
+    const uint32_t msk = (MASK << sh) * 0x10001u;
+    const float usc = __uint_as_float((uint32_t)(127 - sh) << 23);  // 2^-shift
+    uint32_t sel0[2], sel1[2];  // by the parity of mt (only b = 1 depends on it)
+#pragma unroll
+    for (int par = 0; par < 2; ++par) {
+        const int by0 = (((16 * par + g8) * BITS) & 31) >> 3;
+        const int by1 = (((16 * par + g8 + 8) * BITS) & 31) >> 3;
+        sel0[par] = (uint32_t)(by0 * 0x1111 + 0x4400);
+        sel1[par] = (uint32_t)(by1 * 0x1111 + 0x4400);
+    }
+    float *my_w = wb + warp * KT * GQ;  // weights [head][slot]
 
-    float m[GQ], l[GQ], zb[GQ];
-    float2 o2[GQ][4];  // coordinate pairs (2i, 2i + 1) of the lane's 8, scaled by 2^(code shift)
+    float m[NT], l[NT], zb[NT][NV], acc_v[NT][8][4];
 #pragma unroll
-    for (int g = 0; g < GQ; ++g) {
-        m[g] = NEG_INF;
-        l[g] = 0.0f;
-        zb[g] = 0.0f;  // sum of w z (the value zeros' share), per head
+    for (int nt = 0; nt < NT; ++nt) {
+        m[nt] = NEG_INF;
+        l[nt] = 0.0f;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) o2[g][i] = f2(0.0f, 0.0f);
+        for (int gr = 0; gr < NV; ++gr) zb[nt][gr] = 0.0f;
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) acc_v[nt][mt][j] = 0.0f;
     }
 
     for (int it = 0;; ++it) {
@@ -241,177 +311,179 @@ __global__ void __launch_bounds__(KA_WARPS * 32, 1) kivi_attend_kernel(const __g
             break;
         }
         const unsigned char *sb = my_st + st * STG;
-        const uint32_t *kwords = reinterpret_cast<const uint32_t *>(sb) + kw0 * D;
+        const uint32_t *kwords = reinterpret_cast<const uint32_t *>(sb);
         const __half *ksc = reinterpret_cast<const __half *>(sb + KW);
         const __half *kze = reinterpret_cast<const __half *>(sb + KW + 256);
+        const uint32_t *vwords = reinterpret_cast<const uint32_t *>(sb + KW + 512);
+        const __half *vsc = reinterpret_cast<const __half *>(sb + KW + 512 + VW);
+        const __half *vze = reinterpret_cast<const __half *>(sb + KW + 512 + VW + VS);
+        const bool full = n == KT;
 
-        // ---- scores: partial dot products over this lane's 16 channels for
-        // its 8 tokens (token pairs in the two halves of a float2), each code
-        // scaled by 2^(its bit offset) until the end of the channel loop
-        float2 acc[4][GQ];
-        float bias[GQ];
+        // ---- scores: S[token][(head, part)] = sum_c code[token][c] (q s)[c][(head, part)]
+        float acc_k[NT][2][4];
 #pragma unroll
-        for (int g = 0; g < GQ; ++g) {
-            bias[g] = 0.0f;
+        for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-            for (int jp = 0; jp < 4; ++jp) acc[jp][g] = f2(0.0f, 0.0f);
-        }
+            for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4) {
-            const int d0 = cg * 16 + c4 * 4;
-            const uint4 wv = *reinterpret_cast<const uint4 *>(kwords + d0);
-            const uint2 sv = *reinterpret_cast<const uint2 *>(ksc + d0);
-            const uint2 zv = *reinterpret_cast<const uint2 *>(kze + d0);
-            const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
-            const float2 s01 = __half22float2(*reinterpret_cast<const __half2 *>(&sv.x));
-            const float2 s23 = __half22float2(*reinterpret_cast<const __half2 *>(&sv.y));
-            const float2 z01 = __half22float2(*reinterpret_cast<const __half2 *>(&zv.x));
-            const float2 z23 = __half22float2(*reinterpret_cast<const __half2 *>(&zv.y));
-            const float sc[4] = {s01.x, s01.y, s23.x, s23.y};
-            const float ze[4] = {z01.x, z01.y, z23.x, z23.y};
-            float qd[GQ][4];
+                for (int j = 0; j < 4; ++j) acc_k[nt][mt][j] = 0.0f;
 #pragma unroll
-            for (int g = 0; g < GQ; ++g) {
-                const float4 q4 = *reinterpret_cast<const float4 *>(qf + g * D + d0);
-                qd[g][0] = q4.x; qd[g][1] = q4.y; qd[g][2] = q4.z; qd[g][3] = q4.w;
+        for (int kt = 0; kt < 8; ++kt) {
+            const int c0 = 16 * kt + 4 * t4;
+            const uint2 sv = *reinterpret_cast<const uint2 *>(ksc + c0);
+            const float2 s01 = __half22float2(bits_h2(sv.x)), s23 = __half22float2(bits_h2(sv.y));
+            uint32_t bk[NT][2];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                const int hb = 4 * nt + (g8 >> 1);
+                float4 qv = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                if (hb < GQ) qv = *reinterpret_cast<const float4 *>(qf + hb * QS + c0);
+                bk[nt][0] = split_pack(qv.x * s01.x, qv.y * s01.y, lo);
+                bk[nt][1] = split_pack(qv.z * s23.x, qv.w * s23.y, lo);
             }
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const uint32_t x = ww[c] >> ksh;
-                const uint32_t xh = BITS == 4 ? x >> 16 : x;
-                float2 cf[4];
+            for (int mt = 0; mt < 2; ++mt) {
+                const int r0 = mt * BITS / 2, r1 = (2 * mt + 1) * BITS / 4;  // word rows of tokens g8, g8 + 8
+                const uint4 w0 = *reinterpret_cast<const uint4 *>(kwords + r0 * D + c0);
+                const uint4 w1 = r1 != r0 ? *reinterpret_cast<const uint4 *>(kwords + r1 * D + c0) : w0;
+                const uint32_t a0 = code_pair(w0.x, w0.y, sel0[mt], msk);
+                const uint32_t a1 = code_pair(w1.x, w1.y, sel1[mt], msk);
+                const uint32_t a2 = code_pair(w0.z, w0.w, sel0[mt], msk);
+                const uint32_t a3 = code_pair(w1.z, w1.w, sel1[mt], msk);
 #pragma unroll
-                for (int jp = 0; jp < 4; ++jp) {
-                    const int j0 = 2 * jp, j1 = 2 * jp + 1;
-                    const uint32_t s0b = (uint32_t)((BITS == 4 && j0 >= 4 ? j0 - 4 : j0) * BITS);
-                    const uint32_t s1b = (uint32_t)((BITS == 4 && j1 >= 4 ? j1 - 4 : j1) * BITS);
-                    const uint32_t src0 = (BITS == 4 && j0 >= 4) ? xh : x;
-                    const uint32_t src1 = (BITS == 4 && j1 >= 4) ? xh : x;
-                    cf[jp] = __fadd2_rn(f2(magic_code(src0, MASK << s0b), magic_code(src1, MASK << s1b)),
-                                        f2(-TWO23, -TWO23));
-                }
-#pragma unroll
-                for (int g = 0; g < GQ; ++g) {
-                    const float qk = qd[g][c] * sc[c];
-                    bias[g] = fmaf(qd[g][c], ze[c], bias[g]);
-#pragma unroll
-                    for (int jp = 0; jp < 4; ++jp) acc[jp][g] = __ffma2_rn(f2(qk, qk), cf[jp], acc[jp][g]);
-                }
+                for (int nt = 0; nt < NT; ++nt) mma_16816(acc_k[nt][mt], a0, a1, a2, a3, bk[nt][0], bk[nt][1]);
             }
         }
-        // undo the code scales (exact powers of two) and add the zero term
-        float v8[8][GQ];
+        // zero term sum_c q_c z_c of head 4 nt + (lane >> 3), channels
+        // 4 (lane & 7) + 32 x, reduced over the 8 lanes of the head
+        float bias[NT];
 #pragma unroll
-        for (int jp = 0; jp < 4; ++jp) {
-            const int j0 = 2 * jp, j1 = 2 * jp + 1;
-            const float u0 = __int_as_float((127 - (BITS == 4 && j0 >= 4 ? j0 - 4 : j0) * BITS) << 23);
-            const float u1 = __int_as_float((127 - (BITS == 4 && j1 >= 4 ? j1 - 4 : j1) * BITS) << 23);
+        for (int nt = 0; nt < NT; ++nt) {
+            const int hz = 4 * nt + (lane >> 3), cz = 4 * (lane & 7);
+            float bz = 0.0f;
+            if (hz < GQ) {
 #pragma unroll
-            for (int g = 0; g < GQ; ++g) {
-                v8[j0][g] = fmaf(acc[jp][g].x, u0, bias[g]);
-                v8[j1][g] = fmaf(acc[jp][g].y, u1, bias[g]);
-            }
-        }
-        // ---- reduce over the 8 lanes of the token group: exchange on the
-        // token bits so that lane cg ends with token cg (all heads)
-        {
-            const bool hi4 = (cg & 4) != 0;
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-#pragma unroll
-                for (int g = 0; g < GQ; ++g) {
-                    const float keep = hi4 ? v8[4 + i][g] : v8[i][g];
-                    const float send = hi4 ? v8[i][g] : v8[4 + i][g];
-                    v8[i][g] = keep + __shfl_xor_sync(FULL_MASK, send, 4);
+                for (int x = 0; x < 4; ++x) {
+                    const float4 q4 = *reinterpret_cast<const float4 *>(qf + hz * QS + cz + 32 * x);
+                    const uint2 zu = *reinterpret_cast<const uint2 *>(kze + cz + 32 * x);
+                    const float2 z01 = __half22float2(bits_h2(zu.x)), z23 = __half22float2(bits_h2(zu.y));
+                    bz = fmaf(q4.x, z01.x, bz);
+                    bz = fmaf(q4.y, z01.y, bz);
+                    bz = fmaf(q4.z, z23.x, bz);
+                    bz = fmaf(q4.w, z23.y, bz);
                 }
-            const bool hi2 = (cg & 2) != 0;
-#pragma unroll
-            for (int i = 0; i < 2; ++i)
-#pragma unroll
-                for (int g = 0; g < GQ; ++g) {
-                    const float keep = hi2 ? v8[2 + i][g] : v8[i][g];
-                    const float send = hi2 ? v8[i][g] : v8[2 + i][g];
-                    v8[i][g] = keep + __shfl_xor_sync(FULL_MASK, send, 2);
-                }
-            const bool hi1 = (cg & 1) != 0;
-#pragma unroll
-            for (int g = 0; g < GQ; ++g) {
-                const float keep = hi1 ? v8[1][g] : v8[0][g];
-                const float send = hi1 ? v8[0][g] : v8[1][g];
-                v8[0][g] = keep + __shfl_xor_sync(FULL_MASK, send, 1);
             }
+            bz += __shfl_xor_sync(FULL_MASK, bz, 1);
+            bz += __shfl_xor_sync(FULL_MASK, bz, 2);
+            bz += __shfl_xor_sync(FULL_MASK, bz, 4);
+            bias[nt] = __shfl_sync(FULL_MASK, bz, 8 * t4);  // head 4 nt + t4
         }
 
-        // ---- online softmax over the tile (token `lane` on this lane)
-        const bool valid = lane < n;
-        float wv[GQ];
+        // ---- online softmax: this lane holds tokens 16 mt + g8 + 8 rh of head 4 nt + t4
+        float w[NT][4];
 #pragma unroll
-        for (int g = 0; g < GQ; ++g) {
-            const float sc = valid ? v8[0][g] : NEG_INF;
-            const float mt = float_of_ord(__reduce_max_sync(FULL_MASK, ord_of(sc)));
-            if (mt > m[g]) {  // warp-uniform
-                const float f = exp2f(m[g] - mt);
-                l[g] *= f;
-                zb[g] *= f;
+        for (int nt = 0; nt < NT; ++nt) {
+            float sc[4];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) o2[g][i] = __fmul2_rn(o2[g][i], f2(f, f));
-                m[g] = mt;
+            for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+                for (int rh = 0; rh < 2; ++rh) {
+                    const float a = acc_k[nt][mt][2 * rh] + acc_k[nt][mt][2 * rh + 1];
+                    const float s = fmaf(a, usc, bias[nt]) * pe;
+                    sc[2 * mt + rh] = (16 * mt + g8 + 8 * rh < n) ? s : NEG_INF;
+                }
+            float mx = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
+            mx = fmaxf(mx, __shfl_xor_sync(FULL_MASK, mx, 4));
+            mx = fmaxf(mx, __shfl_xor_sync(FULL_MASK, mx, 8));
+            mx = fmaxf(mx, __shfl_xor_sync(FULL_MASK, mx, 16));
+            if (mx > m[nt]) {
+                const float f = exp2f(m[nt] - mx);
+                l[nt] *= f;
+#pragma unroll
+                for (int gr = 0; gr < NV; ++gr) zb[nt][gr] *= f;
+#pragma unroll
+                for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) acc_v[nt][mt][j] *= f;
+                m[nt] = mx;
             }
-            wv[g] = exp2f(sc - m[g]);
-            l[g] += wv[g];
-        }
 #pragma unroll
-        for (int g = 0; g < GQ; ++g) my_w[lane * GQ + g] = wv[g];
+            for (int i = 0; i < 4; ++i) {
+                w[nt][i] = exp2f(sc[i] - m[nt]);
+                l[nt] += w[nt][i];
+            }
+            const int hh = 4 * nt + t4;
+            if (hh < GQ) {
+#pragma unroll
+                for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+                    for (int rh = 0; rh < 2; ++rh)
+                        my_w[hh * KT + 16 * mt + 4 * (g8 & 3) + (g8 >> 2) + 2 * rh] = w[nt][2 * mt + rh];
+            }
+        }
+        // the value zeros' share sum_t w_t z_t, per head and value group
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+            for (int rh = 0; rh < 2; ++rh) {
+                const int tok = 16 * mt + g8 + 8 * rh;
+                float z[NV];
+                load_groups<NV>(vze + tok * NV, z);
+                if (!full && tok >= n) {
+#pragma unroll
+                    for (int gr = 0; gr < NV; ++gr) z[gr] = 0.0f;
+                }
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                    for (int gr = 0; gr < NV; ++gr) zb[nt][gr] = fmaf(w[nt][2 * mt + rh], z[gr], zb[nt][gr]);
+            }
         __syncwarp();
 
-        // ---- values: lane (vh, cl), coordinates 8 cl .. 8 cl + 7 of the
-        // tokens k = vh, vh + 2, ...; coordinate pairs per paired FMA
-        {
-            const uint32_t *vwords = reinterpret_cast<const uint32_t *>(sb + KW + 512);
-            const __half *vsc = reinterpret_cast<const __half *>(sb + KW + 512 + VW);
-            const __half *vze = reinterpret_cast<const __half *>(sb + KW + 512 + VW + VS);
-            auto token = [&](int k) {
-                const uint32_t x = vwords[k * W + vwi] >> vsh;
-                const uint32_t xh = BITS == 4 ? x >> 16 : x;
-                const float sk = __half2float(vsc[k * (D / G) + vj]);
-                const float zk = __half2float(vze[k * (D / G) + vj]);
-                float2 cf[4];
+        // ---- values: O[coord][(head, part)] += sum_t code[t][coord] (w s)[t][(head, part)]
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int c0 = 2 * i, c1 = 2 * i + 1;
-                    const uint32_t s0b = (uint32_t)((BITS == 4 && c0 >= 4 ? c0 - 4 : c0) * BITS);
-                    const uint32_t s1b = (uint32_t)((BITS == 4 && c1 >= 4 ? c1 - 4 : c1) * BITS);
-                    const uint32_t src0 = (BITS == 4 && c0 >= 4) ? xh : x;
-                    const uint32_t src1 = (BITS == 4 && c1 >= 4) ? xh : x;
-                    cf[i] = __fadd2_rn(f2(magic_code(src0, MASK << s0b), magic_code(src1, MASK << s1b)),
-                                       f2(-TWO23, -TWO23));
+        for (int kt = 0; kt < 2; ++kt) {
+            float sv[4][NV];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int tok = 16 * kt + t4 + 4 * i;
+                load_groups<NV>(vsc + tok * NV, sv[i]);
+                if (!full && tok >= n) {
+#pragma unroll
+                    for (int gr = 0; gr < NV; ++gr) sv[i][gr] = 0.0f;
                 }
-                float wk[GQ];
-                if constexpr (GQ == 1) {
-                    wk[0] = my_w[k];
-                } else if constexpr (GQ == 2) {
-                    const float2 w2 = *reinterpret_cast<const float2 *>(my_w + k * 2);
-                    wk[0] = w2.x; wk[1] = w2.y;
-                } else {
+            }
+            uint32_t bv[NT][NV][2];
 #pragma unroll
-                    for (int g = 0; g < GQ; g += 4) {
-                        const float4 w4 = *reinterpret_cast<const float4 *>(my_w + k * GQ + g);
-                        wk[g] = w4.x; wk[g + 1] = w4.y; wk[g + 2] = w4.z; wk[g + 3] = w4.w;
-                    }
+            for (int nt = 0; nt < NT; ++nt) {
+                const int hb = 4 * nt + (g8 >> 1);
+                float4 wv = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                if (hb < GQ) wv = *reinterpret_cast<const float4 *>(my_w + hb * KT + 16 * kt + 4 * t4);
+#pragma unroll
+                for (int gr = 0; gr < NV; ++gr) {
+                    bv[nt][gr][0] = split_pack(wv.x * sv[0][gr], wv.y * sv[1][gr], lo);
+                    bv[nt][gr][1] = split_pack(wv.z * sv[2][gr], wv.w * sv[3][gr], lo);
                 }
+            }
 #pragma unroll
-                for (int g = 0; g < GQ; ++g) {
-                    const float a = wk[g] * sk;
-                    zb[g] = fmaf(wk[g], zk, zb[g]);
+            for (int qd = 0; qd < W / 4; ++qd) {
+                uint4 vq[4];
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) o2[g][i] = __ffma2_rn(f2(a, a), cf[i], o2[g][i]);
+                for (int i = 0; i < 4; ++i)
+                    vq[i] = *reinterpret_cast<const uint4 *>(vwords + (16 * kt + t4 + 4 * i) * W + 4 * qd);
+#pragma unroll
+                for (int mm = 0; mm < MPQ; ++mm) {
+                    const int mt = qd * MPQ + mm;
+                    const int o0 = mt * BITS / 2 - 4 * qd, o1 = (2 * mt + 1) * BITS / 4 - 4 * qd;  // words of coords g8, g8 + 8
+                    const uint32_t a0 = code_pair(quad_at(vq[0], o0), quad_at(vq[1], o0), sel0[mt & 1], msk);
+                    const uint32_t a1 = code_pair(quad_at(vq[0], o1), quad_at(vq[1], o1), sel1[mt & 1], msk);
+                    const uint32_t a2 = code_pair(quad_at(vq[2], o0), quad_at(vq[3], o0), sel0[mt & 1], msk);
+                    const uint32_t a3 = code_pair(quad_at(vq[2], o1), quad_at(vq[3], o1), sel1[mt & 1], msk);
+                    const int gr = 16 * mt / G;
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt)
+                        mma_16816(acc_v[nt][mt], a0, a1, a2, a3, bv[nt][gr][0], bv[nt][gr][1]);
                 }
-            };
-            if (n == KT) {
-#pragma unroll 4
-                for (int k = vh; k < KT; k += 2) token(k);
-            } else {
-                for (int k = vh; k < n; k += 2) token(k);
             }
         }
 
@@ -420,32 +492,38 @@ __global__ void __launch_bounds__(KA_WARPS * 32, 1) kivi_attend_kernel(const __g
         if (t + KA_STAGES * KA_WARPS < ntiles) issue(t + KA_STAGES * KA_WARPS, st);
     }
 
-    // l: each lane summed its own tokens' weights; the value halves (vh = 0, 1)
-    // hold the even and odd tokens of the same 8 coordinates: add them, undo
-    // the code scales, and fold in the zeros' share (one value group per lane)
-    float o[GQ][4];
+    // totals over the 8 row lanes of each head, then the head's outputs:
+    // coordinates 16 mt + g8 (+ 8) = (hi + lo) 2^-shift + the zeros' share
 #pragma unroll
-    for (int g = 0; g < GQ; ++g) {
+    for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-        for (int off = 16; off >= 1; off >>= 1) l[g] += __shfl_xor_sync(FULL_MASK, l[g], off);
-        zb[g] += __shfl_xor_sync(FULL_MASK, zb[g], 16);
-        float full[8];
+        for (int off = 4; off <= 16; off <<= 1) {
+            l[nt] += __shfl_xor_sync(FULL_MASK, l[nt], off);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float ox = o2[g][i].x + __shfl_xor_sync(FULL_MASK, o2[g][i].x, 16);
-            const float oy = o2[g][i].y + __shfl_xor_sync(FULL_MASK, o2[g][i].y, 16);
-            const int c0 = 2 * i, c1 = 2 * i + 1;
-            const float u0 = __int_as_float((127 - (BITS == 4 && c0 >= 4 ? c0 - 4 : c0) * BITS) << 23);
-            const float u1 = __int_as_float((127 - (BITS == 4 && c1 >= 4 ? c1 - 4 : c1) * BITS) << 23);
-            full[c0] = fmaf(ox, u0, zb[g]);
-            full[c1] = fmaf(oy, u1, zb[g]);
+            for (int gr = 0; gr < NV; ++gr) zb[nt][gr] += __shfl_xor_sync(FULL_MASK, zb[nt][gr], off);
         }
-        // this lane publishes coordinates 8 cl + 4 vh .. + 3
+    __syncthreads();  // every warp is done with its stages: they hold the merge now
+    float *ms = reinterpret_cast<float *>(stages);
+    float *ls = ms + KA_WARPS * GQ;
+    float *os = ls + KA_WARPS * GQ;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) o[g][c] = vh ? full[4 + c] : full[c];
+    for (int nt = 0; nt < NT; ++nt) {
+        const int hh = 4 * nt + t4;
+        if (hh < GQ) {
+            if (g8 == 0) {
+                ms[warp * GQ + hh] = m[nt];
+                ls[warp * GQ + hh] = l[nt];
+            }
+            float *o = os + (warp * GQ + hh) * D;
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt) {
+                const float z = zb[nt][16 * mt / G];
+                o[16 * mt + g8] = fmaf(acc_v[nt][mt][0] + acc_v[nt][mt][1], usc, z);
+                o[16 * mt + g8 + 8] = fmaf(acc_v[nt][mt][2] + acc_v[nt][mt][3], usc, z);
+            }
+        }
     }
-    __syncthreads();
-    ka_merge_write<GQ>(p, stages, b, h, split, nparts, m, l, o, 8 * cl + 4 * vh);
+    ka_merge_finish<GQ>(p, stages, b, h, split, nparts);
 }
 
 // The fp16 residual window of one (sequence, kv head): warp w takes tokens
@@ -463,7 +541,7 @@ __global__ void __launch_bounds__(KA_WARPS * 32) kivi_attend_residual_kernel(con
     rl = rl < 0 ? 0 : (rl > p.R ? p.R : rl);
     const int nparts = p.nsplit + 1;
     if (rl == 0) return;  // the combine skips an empty window
-    ka_load_query<GQ>(p, b, h, qf);
+    (void)ka_load_query<GQ, D>(p, b, h, qf, false);
     __syncthreads();
     float qv[GQ][4];
 #pragma unroll
@@ -506,7 +584,18 @@ __global__ void __launch_bounds__(KA_WARPS * 32) kivi_attend_residual_kernel(con
         }
     }
     // l is already the warp's total (every lane holds the same sums)
-    ka_merge_write<GQ>(p, scratch, b, h, p.nsplit, nparts, m, l, o, 4 * lane);
+    float *ms = reinterpret_cast<float *>(scratch);
+    float *ls = ms + KA_WARPS * GQ;
+    float *os = ls + KA_WARPS * GQ;
+#pragma unroll
+    for (int g = 0; g < GQ; ++g) {
+        if (lane == 0) {
+            ms[warp * GQ + g] = m[g];
+            ls[warp * GQ + g] = l[g];
+        }
+        *reinterpret_cast<float4 *>(os + (warp * GQ + g) * D + 4 * lane) = make_float4(o[g][0], o[g][1], o[g][2], o[g][3]);
+    }
+    ka_merge_finish<GQ>(p, scratch, b, h, p.nsplit, nparts);
 }
 
 // Combine the parts of one (sequence, query head): the quantized chunks that
