@@ -46,7 +46,6 @@ VQ_DEFINE_ERROR_WORD(g_ka_err);
 constexpr int D = 128;
 constexpr int KA_WARPS = 8;
 constexpr int KT = 32;  // tokens per warp tile
-constexpr int KA_STAGES = 2;
 constexpr float NEG_INF = -__builtin_huge_valf();
 
 __host__ __device__ constexpr int ka_stage(int bits, int G)
@@ -55,27 +54,33 @@ __host__ __device__ constexpr int ka_stage(int bits, int G)
     // (32 rows of 4 bits words), value scales + zeros (2 x 32 x 128/G halves)
     return bits * 512 + 512 + KT * 16 * bits + 2 * KT * (D / G) * 2;
 }
+// Tiles in flight per warp: three where that still leaves room for two CTAs
+// per SM, else two.
+__host__ __device__ constexpr int ka_nst(int bits, int G)
+{
+    return 3 * KA_WARPS * ka_stage(bits, G) <= 100 * 1024 ? 3 : 2;
+}
 // The stage area also serves the final merge of the warps (m, l and the
 // unnormalised outputs of every warp), so it is at least that large.
 __host__ __device__ constexpr int ka_region(int bits, int G, int GQ)
 {
-    return KA_WARPS * KA_STAGES * ka_stage(bits, G) > KA_WARPS * GQ * (D + 2) * 4
-               ? KA_WARPS * KA_STAGES * ka_stage(bits, G)
+    return KA_WARPS * ka_nst(bits, G) * ka_stage(bits, G) > KA_WARPS * GQ * (D + 2) * 4
+               ? KA_WARPS * ka_nst(bits, G) * ka_stage(bits, G)
                : KA_WARPS * GQ * (D + 2) * 4;
 }
 constexpr int QS = D + 16;  // query row stride (floats): rows of 4 heads fall on 2 bank halves
 __host__ __device__ constexpr int ka_smem(int bits, int G, int GQ)
 {
     // query [g][QS], weights [warp][g][slot], stages / merge, mbarriers
-    return QS * GQ * 4 + KA_WARPS * KT * GQ * 4 + ka_region(bits, G, GQ) + KA_WARPS * KA_STAGES * 8;
+    return QS * GQ * 4 + KA_WARPS * KT * GQ * 4 + ka_region(bits, G, GQ) + KA_WARPS * ka_nst(bits, G) * 8;
 }
 
 // Load the GQ query rows of kv head h, times scale * log2 e, into qf (row
-// stride STRIDE).  With `bounded`, the rows are also multiplied by 2^-e, the
-// smallest power of two that brings every |entry| to at most 1 (e >= 0), and
-// 2^e is returned: the products q_d s_d of the key scores then stay inside
-// the fp16 range whatever the key scales (|s| <= 65504), and the scores are
-// multiplied back by 2^e, exactly.
+// stride STRIDE).  With `bounded`, the rows are also multiplied by the power
+// of two 2^-e that brings max |entry| into [1/2, 1), and 2^e is returned: the
+// products q_d s_d of the key scores then stay inside the fp16 range whatever
+// the key scales (|s| <= 65504), as far from its subnormals as that allows,
+// and the scores are multiplied back by 2^e, exactly.
 template <int GQ, int STRIDE>
 __device__ __forceinline__ float ka_load_query(const KiviAttendParams &p, int b, int h, float *qf, bool bounded)
 {
@@ -87,8 +92,8 @@ __device__ __forceinline__ float ka_load_query(const KiviAttendParams &p, int b,
         float mx = 0.0f;
         for (int i = lane; i < GQ * D; i += 32) mx = fmaxf(mx, fabsf(__half2float(q[i])));
         mx = __uint_as_float(__reduce_max_sync(FULL_MASK, __float_as_uint(mx))) * fabsf(qs);
-        if (mx > 1.0f && mx <= 3.0e38f) {
-            const int ex = (int)((__float_as_uint(mx) >> 23) & 0xffu) - 126;  // mx < 2^ex
+        if (mx >= 1.0e-30f && mx <= 1.0e30f) {
+            const int ex = (int)((__float_as_uint(mx) >> 23) & 0xffu) - 126;  // 2^(ex-1) <= mx < 2^ex
             pe = __uint_as_float((uint32_t)(127 + ex) << 23);
             ps = __uint_as_float((uint32_t)(127 - ex) << 23);
         }
@@ -140,25 +145,24 @@ __device__ __forceinline__ void ka_merge_finish(const KiviAttendParams &p, unsig
 __device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
 __device__ __forceinline__ __half2 bits_h2(uint32_t u) { return *reinterpret_cast<__half2 *>(&u); }
 
-// One operand register of two fp16 codes: the code in byte `sel` picks of x
-// (low half) and of y (high half), at bit `shift` of that byte (mask m has the
-// code bits of both halves).  OR-ing the masked bits into the mantissa of
-// 1024 and subtracting 1024 leaves code * 2^shift in each half, exactly.
-__device__ __forceinline__ uint32_t code_pair(uint32_t x, uint32_t y, uint32_t sel, uint32_t m)
+// The fp16 pair of this lane's part of u: hi lanes (mh = ~0x1fff, ml = 0)
+// take u with its mantissa cut to fp16's 10 bits (exact in fp16), lo lanes
+// (mh = ~0, ml = ~0x1fff) the rest u - hi, rounded to fp16: the two columns
+// of one head together carry u to about 21 bits.
+__device__ __forceinline__ uint32_t split_pack(float2 u, uint32_t mh, uint32_t ml)
 {
-    const uint32_t t = (__byte_perm(x, y, sel) & m) | 0x64006400u;
-    return h2_bits(__hsub2(bits_h2(t), bits_h2(0x64006400u)));
+    const uint32_t ux = __float_as_uint(u.x), uy = __float_as_uint(u.y);
+    const float2 a = make_float2(__uint_as_float(ux & mh), __uint_as_float(uy & mh));
+    const float2 c = make_float2(__uint_as_float((ux & ml) ^ 0x80000000u), __uint_as_float((uy & ml) ^ 0x80000000u));
+    return h2_bits(__float22half2_rn(__fadd2_rn(a, c)));
 }
 
-// The fp16 pair (hi(u0), hi(u1)), or on `lo` lanes (u0 - hi(u0), u1 - hi(u1))
-// rounded to fp16: the two columns of one head together carry u to about 22
-// bits.
-__device__ __forceinline__ uint32_t split_pack(float u0, float u1, bool lo)
+// code * 2^shift in each half of x's masked bits: OR-ing them into the
+// mantissa of 1024 and subtracting 1024 is exact.  (Codes left as fp16
+// subnormals, with no subtraction, lose precision in the tile products.)
+__device__ __forceinline__ uint32_t code_h2(uint32_t x, uint32_t m)
 {
-    const __half2 hi = __floats2half2_rn(u0, u1);
-    const float2 hf = __half22float2(hi);
-    const __half2 lw = __floats2half2_rn(u0 - hf.x, u1 - hf.y);
-    return h2_bits(lo ? lw : hi);
+    return h2_bits(__hsub2(bits_h2((x & m) | 0x64006400u), bits_h2(0x64006400u)));
 }
 
 // d += a * b for one 16 x 8 x 16 tile, fp16 operands, fp32 accumulation.
@@ -192,12 +196,30 @@ __device__ __forceinline__ void load_groups(const __half *src, float (&f)[NV])
     }
 }
 
+// The NV fp16 scales (or zeros) of one token, packed: halves 0, 1 in .x and
+// 2, 3 in .y.
+template <int NV>
+__device__ __forceinline__ uint2 load_groups_raw(const __half *src)
+{
+    if constexpr (NV == 4) return *reinterpret_cast<const uint2 *>(src);
+    else if constexpr (NV == 2) return make_uint2(*reinterpret_cast<const uint32_t *>(src), 0u);
+    else return make_uint2((uint32_t)__half_as_ushort(src[0]), 0u);
+}
+// Group gr's scales of two tokens, as floats.
+__device__ __forceinline__ float2 group_pair(uint2 a, uint2 b, int gr)
+{
+    const uint32_t wa = gr < 2 ? a.x : a.y, wb = gr < 2 ? b.x : b.y;
+    const uint32_t sel = (gr & 1) ? 0x7632u : 0x5410u;  // the high or the low halves of both
+    return __half22float2(bits_h2(__byte_perm(wa, wb, sel)));
+}
+
 // One chunk of the quantized tokens of one (sequence, kv head).
 template <int BITS, int G, int GQ>
 __global__ void __launch_bounds__(KA_WARPS * 32, GQ <= 4 ? 2 : 1)
     kivi_attend_kernel(const __grid_constant__ KiviAttendParams p)
 {
     constexpr int STG = ka_stage(BITS, G);
+    constexpr int KA_STAGES = ka_nst(BITS, G);
     constexpr int KW = BITS * 512;            // key words of a tile (bytes)
     constexpr int VW = KT * 16 * BITS;        // value words of a tile (bytes)
     constexpr int VS = KT * (D / G) * 2;      // value scales (or zeros) of a tile (bytes)
@@ -205,6 +227,7 @@ __global__ void __launch_bounds__(KA_WARPS * 32, GQ <= 4 ? 2 : 1)
     constexpr int NV = D / G;                 // value groups per token
     constexpr int NT = (2 * GQ + 7) / 8;      // n-tiles of 8 (head, hi / lo) columns
     constexpr int MPQ = 8 / BITS;             // value m-tiles per 4 words of a token
+    constexpr bool VPAIR = BITS < 4;          // value rows paired inside one byte (else split)
     constexpr uint32_t MASK = (1u << BITS) - 1u;
     extern __shared__ __align__(128) unsigned char smem[];
     float *qf = reinterpret_cast<float *>(smem);
@@ -258,27 +281,33 @@ __global__ void __launch_bounds__(KA_WARPS * 32, GQ <= 4 ? 2 : 1)
     const float pe = ka_load_query<GQ, QS>(p, b, h, qf, true);
     __syncthreads();
 
-    // Fragment roles (m16n8k16): lane = 4 g8 + t4.  Operand rows are tokens
-    // (keys) or coordinates (values) 16 mt + g8 and + 8; the lane's k entries
+    // Fragment roles (m16n8k16), lane = 4 g8 + t4.  The lane's k entries
     // 2 t4, 2 t4 + 1, 2 t4 + 8, 2 t4 + 9 are channels 16 kt + 4 t4 + 0..3
-    // (keys) or tokens 16 kt + t4 + 0, 4, 8, 12 (values); its B column g8 is
+    // (keys) or tokens 16 kt + t4 + 0, 4, 8, 12 (values).  Its B column g8 is
     // head 4 nt + g8 / 2, hi part for even g8, lo part for odd; its
     // accumulator columns 2 t4, 2 t4 + 1 are head 4 nt + t4, hi and lo.
+    // Its operand rows g8 and g8 + 8 are entries 2 g8 and 2 g8 + 1 of the
+    // m-tile's 16 (paired: both codes in one byte, one byte permute serves
+    // both registers), or entries g8 and g8 + 8 (split: b = 4 values, whose
+    // 16 coordinates span two words).  Codes enter as code * 2^shift; the
+    // epilogue multiplies each row by 2^-shift.
     const int g8 = lane >> 2, t4 = lane & 3;
     const bool lo = (g8 & 1) != 0;
-    // a row's code sits at bit ((row BITS) mod 32) of its word: byte
-    // ((row BITS) mod 32) / 8, shift (g8 BITS) mod 8 for every row of the lane
-    const int sh = (g8 * BITS) & 7;
-    const uint32_t msk = (MASK << sh) * 0x10001u;
-    const float usc = __uint_as_float((uint32_t)(127 - sh) << 23);  // 2^-shift
-    uint32_t sel0[2], sel1[2];  // by the parity of mt (only b = 1 depends on it)
+    const uint32_t mh = lo ? 0xFFFFFFFFu : 0xFFFFE000u, ml = lo ? 0xFFFFE000u : 0u;
+    const int psh0 = (2 * g8 * BITS) & 7, psh1 = psh0 + BITS;
+    const uint32_t pm0 = (MASK << psh0) * 0x10001u, pm1 = (MASK << psh1) * 0x10001u;
+    uint32_t psel[2];  // by the parity of mt (only b = 1 depends on it)
 #pragma unroll
-    for (int par = 0; par < 2; ++par) {
-        const int by0 = (((16 * par + g8) * BITS) & 31) >> 3;
-        const int by1 = (((16 * par + g8 + 8) * BITS) & 31) >> 3;
-        sel0[par] = (uint32_t)(by0 * 0x1111 + 0x4400);
-        sel1[par] = (uint32_t)(by1 * 0x1111 + 0x4400);
-    }
+    for (int par = 0; par < 2; ++par)
+        psel[par] = (uint32_t)(((((16 * par + 2 * g8) * BITS) & 31) >> 3) * 0x1111 + 0x4400);
+    const int kro = (2 * g8 * BITS) >> 5;  // key word row of entry 2 g8 past the m-tile's first
+    const int ssh = (g8 * BITS) & 7;
+    const uint32_t sm = (MASK << ssh) * 0x10001u;
+    const uint32_t ssel = (uint32_t)((((g8 * BITS) & 31) >> 3) * 0x1111 + 0x4400);
+    const float uk0 = __uint_as_float((uint32_t)(127 - psh0) << 23) * pe;
+    const float uk1 = __uint_as_float((uint32_t)(127 - psh1) << 23) * pe;
+    const float uv0 = __uint_as_float((uint32_t)(127 - (VPAIR ? psh0 : ssh)) << 23);
+    const float uv1 = __uint_as_float((uint32_t)(127 - (VPAIR ? psh1 : ssh)) << 23);
     float *my_w = wb + warp * KT * GQ;  // weights [head][slot]
 
     float m[NT], l[NT], zb[NT][NV], acc_v[NT][8][4];
@@ -337,19 +366,17 @@ __global__ void __launch_bounds__(KA_WARPS * 32, GQ <= 4 ? 2 : 1)
             for (int nt = 0; nt < NT; ++nt) {
                 const int hb = 4 * nt + (g8 >> 1);
                 float4 qv = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-                if (hb < GQ) qv = *reinterpret_cast<const float4 *>(qf + hb * QS + c0);
-                bk[nt][0] = split_pack(qv.x * s01.x, qv.y * s01.y, lo);
-                bk[nt][1] = split_pack(qv.z * s23.x, qv.w * s23.y, lo);
+                if (GQ % 4 == 0 || hb < GQ) qv = *reinterpret_cast<const float4 *>(qf + hb * QS + c0);
+                bk[nt][0] = split_pack(__fmul2_rn(make_float2(qv.x, qv.y), s01), mh, ml);
+                bk[nt][1] = split_pack(__fmul2_rn(make_float2(qv.z, qv.w), s23), mh, ml);
             }
 #pragma unroll
             for (int mt = 0; mt < 2; ++mt) {
-                const int r0 = mt * BITS / 2, r1 = (2 * mt + 1) * BITS / 4;  // word rows of tokens g8, g8 + 8
-                const uint4 w0 = *reinterpret_cast<const uint4 *>(kwords + r0 * D + c0);
-                const uint4 w1 = r1 != r0 ? *reinterpret_cast<const uint4 *>(kwords + r1 * D + c0) : w0;
-                const uint32_t a0 = code_pair(w0.x, w0.y, sel0[mt], msk);
-                const uint32_t a1 = code_pair(w1.x, w1.y, sel1[mt], msk);
-                const uint32_t a2 = code_pair(w0.z, w0.w, sel0[mt], msk);
-                const uint32_t a3 = code_pair(w1.z, w1.w, sel1[mt], msk);
+                const uint4 w4 = *reinterpret_cast<const uint4 *>(kwords + (mt * BITS / 2 + kro) * D + c0);
+                const uint32_t x01 = __byte_perm(w4.x, w4.y, psel[mt]);
+                const uint32_t x23 = __byte_perm(w4.z, w4.w, psel[mt]);
+                const uint32_t a0 = code_h2(x01, pm0), a1 = code_h2(x01, pm1);
+                const uint32_t a2 = code_h2(x23, pm0), a3 = code_h2(x23, pm1);
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) mma_16816(acc_k[nt][mt], a0, a1, a2, a3, bk[nt][0], bk[nt][1]);
             }
@@ -361,7 +388,7 @@ __global__ void __launch_bounds__(KA_WARPS * 32, GQ <= 4 ? 2 : 1)
         for (int nt = 0; nt < NT; ++nt) {
             const int hz = 4 * nt + (lane >> 3), cz = 4 * (lane & 7);
             float bz = 0.0f;
-            if (hz < GQ) {
+            if (GQ % 4 == 0 || hz < GQ) {
 #pragma unroll
                 for (int x = 0; x < 4; ++x) {
                     const float4 q4 = *reinterpret_cast<const float4 *>(qf + hz * QS + cz + 32 * x);
@@ -376,10 +403,31 @@ __global__ void __launch_bounds__(KA_WARPS * 32, GQ <= 4 ? 2 : 1)
             bz += __shfl_xor_sync(FULL_MASK, bz, 1);
             bz += __shfl_xor_sync(FULL_MASK, bz, 2);
             bz += __shfl_xor_sync(FULL_MASK, bz, 4);
-            bias[nt] = __shfl_sync(FULL_MASK, bz, 8 * t4);  // head 4 nt + t4
+            bias[nt] = __shfl_sync(FULL_MASK, bz, 8 * t4) * pe;  // head 4 nt + t4
+        }
+        // exponent offset of the weights: with every value scale of the tile
+        // below 2^(E + 1), weights up to 2^(14 - E) keep w s below 2^15 and
+        // out of the fp16 subnormals (the offset enters the running max, so
+        // it cancels in the normalisation)
+        float fsig;
+        {
+            uint32_t mb = 0;
+            if (4 * lane < KT * NV) {
+                const uint2 su = *reinterpret_cast<const uint2 *>(vsc + 4 * lane);
+                uint32_t hw[2] = {su.x & 0x7fff7fffu, su.y & 0x7fff7fffu};
+                if (!full) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        if ((4 * lane + j) / NV >= n) hw[j >> 1] &= (j & 1) ? 0x0000ffffu : 0xffff0000u;
+                }
+                const uint32_t mm = __vmaxu2(hw[0], hw[1]);
+                mb = max(mm & 0xffffu, mm >> 16);
+            }
+            mb = __reduce_max_sync(FULL_MASK, mb);
+            fsig = (float)min(14 - ((int)(mb >> 10) - 15), 30);
         }
 
-        // ---- online softmax: this lane holds tokens 16 mt + g8 + 8 rh of head 4 nt + t4
+        // ---- online softmax: this lane holds tokens 16 mt + 2 g8 + rh of head 4 nt + t4
         float w[NT][4];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
@@ -389,15 +437,16 @@ __global__ void __launch_bounds__(KA_WARPS * 32, GQ <= 4 ? 2 : 1)
 #pragma unroll
                 for (int rh = 0; rh < 2; ++rh) {
                     const float a = acc_k[nt][mt][2 * rh] + acc_k[nt][mt][2 * rh + 1];
-                    const float s = fmaf(a, usc, bias[nt]) * pe;
-                    sc[2 * mt + rh] = (16 * mt + g8 + 8 * rh < n) ? s : NEG_INF;
+                    const float s = fmaf(a, rh ? uk1 : uk0, bias[nt]);
+                    sc[2 * mt + rh] = (16 * mt + 2 * g8 + rh < n) ? s : NEG_INF;
                 }
             float mx = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
             mx = fmaxf(mx, __shfl_xor_sync(FULL_MASK, mx, 4));
             mx = fmaxf(mx, __shfl_xor_sync(FULL_MASK, mx, 8));
             mx = fmaxf(mx, __shfl_xor_sync(FULL_MASK, mx, 16));
-            if (mx > m[nt]) {
-                const float f = exp2f(m[nt] - mx);
+            const float cand = mx - fsig;
+            if (cand > m[nt]) {
+                const float f = exp2f(m[nt] - cand);
                 l[nt] *= f;
 #pragma unroll
                 for (int gr = 0; gr < NV; ++gr) zb[nt][gr] *= f;
@@ -405,7 +454,7 @@ __global__ void __launch_bounds__(KA_WARPS * 32, GQ <= 4 ? 2 : 1)
                 for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
                     for (int j = 0; j < 4; ++j) acc_v[nt][mt][j] *= f;
-                m[nt] = mx;
+                m[nt] = cand;
             }
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
@@ -413,12 +462,15 @@ __global__ void __launch_bounds__(KA_WARPS * 32, GQ <= 4 ? 2 : 1)
                 l[nt] += w[nt][i];
             }
             const int hh = 4 * nt + t4;
-            if (hh < GQ) {
+            if (GQ % 4 == 0 || hh < GQ) {
+                // token 16 mt + r goes to slot 16 mt + 4 (r mod 4) + r / 4
 #pragma unroll
                 for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-                    for (int rh = 0; rh < 2; ++rh)
-                        my_w[hh * KT + 16 * mt + 4 * (g8 & 3) + (g8 >> 2) + 2 * rh] = w[nt][2 * mt + rh];
+                    for (int rh = 0; rh < 2; ++rh) {
+                        const int r = 2 * g8 + rh;
+                        my_w[hh * KT + 16 * mt + 4 * (r & 3) + (r >> 2)] = w[nt][2 * mt + rh];
+                    }
             }
         }
         // the value zeros' share sum_t w_t z_t, per head and value group
@@ -426,7 +478,7 @@ __global__ void __launch_bounds__(KA_WARPS * 32, GQ <= 4 ? 2 : 1)
         for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
             for (int rh = 0; rh < 2; ++rh) {
-                const int tok = 16 * mt + g8 + 8 * rh;
+                const int tok = 16 * mt + 2 * g8 + rh;
                 float z[NV];
                 load_groups<NV>(vze + tok * NV, z);
                 if (!full && tok >= n) {
@@ -443,28 +495,21 @@ __global__ void __launch_bounds__(KA_WARPS * 32, GQ <= 4 ? 2 : 1)
         // ---- values: O[coord][(head, part)] += sum_t code[t][coord] (w s)[t][(head, part)]
 #pragma unroll
         for (int kt = 0; kt < 2; ++kt) {
-            float sv[4][NV];
+            uint2 sr[4];  // the NV fp16 scales of tokens 16 kt + t4 + 4 i
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const int tok = 16 * kt + t4 + 4 * i;
-                load_groups<NV>(vsc + tok * NV, sv[i]);
-                if (!full && tok >= n) {
-#pragma unroll
-                    for (int gr = 0; gr < NV; ++gr) sv[i][gr] = 0.0f;
-                }
+                sr[i] = load_groups_raw<NV>(vsc + tok * NV);
+                if (!full && tok >= n) sr[i] = make_uint2(0u, 0u);
             }
-            uint32_t bv[NT][NV][2];
+            float4 wv[NT];
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
                 const int hb = 4 * nt + (g8 >> 1);
-                float4 wv = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-                if (hb < GQ) wv = *reinterpret_cast<const float4 *>(my_w + hb * KT + 16 * kt + 4 * t4);
-#pragma unroll
-                for (int gr = 0; gr < NV; ++gr) {
-                    bv[nt][gr][0] = split_pack(wv.x * sv[0][gr], wv.y * sv[1][gr], lo);
-                    bv[nt][gr][1] = split_pack(wv.z * sv[2][gr], wv.w * sv[3][gr], lo);
-                }
+                wv[nt] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                if (GQ % 4 == 0 || hb < GQ) wv[nt] = *reinterpret_cast<const float4 *>(my_w + hb * KT + 16 * kt + 4 * t4);
             }
+            uint32_t bv[NT][2];
 #pragma unroll
             for (int qd = 0; qd < W / 4; ++qd) {
                 uint4 vq[4];
@@ -474,15 +519,30 @@ __global__ void __launch_bounds__(KA_WARPS * 32, GQ <= 4 ? 2 : 1)
 #pragma unroll
                 for (int mm = 0; mm < MPQ; ++mm) {
                     const int mt = qd * MPQ + mm;
-                    const int o0 = mt * BITS / 2 - 4 * qd, o1 = (2 * mt + 1) * BITS / 4 - 4 * qd;  // words of coords g8, g8 + 8
-                    const uint32_t a0 = code_pair(quad_at(vq[0], o0), quad_at(vq[1], o0), sel0[mt & 1], msk);
-                    const uint32_t a1 = code_pair(quad_at(vq[0], o1), quad_at(vq[1], o1), sel1[mt & 1], msk);
-                    const uint32_t a2 = code_pair(quad_at(vq[2], o0), quad_at(vq[3], o0), sel0[mt & 1], msk);
-                    const uint32_t a3 = code_pair(quad_at(vq[2], o1), quad_at(vq[3], o1), sel1[mt & 1], msk);
-                    const int gr = 16 * mt / G;
+                    if ((16 * mt) % G == 0) {  // first m-tile of value group gr: its (w s) columns
+                        const int gr = 16 * mt / G;
+                        const float2 s01 = group_pair(sr[0], sr[1], gr), s23 = group_pair(sr[2], sr[3], gr);
 #pragma unroll
-                    for (int nt = 0; nt < NT; ++nt)
-                        mma_16816(acc_v[nt][mt], a0, a1, a2, a3, bv[nt][gr][0], bv[nt][gr][1]);
+                        for (int nt = 0; nt < NT; ++nt) {
+                            bv[nt][0] = split_pack(__fmul2_rn(make_float2(wv[nt].x, wv[nt].y), s01), mh, ml);
+                            bv[nt][1] = split_pack(__fmul2_rn(make_float2(wv[nt].z, wv[nt].w), s23), mh, ml);
+                        }
+                    }
+                    uint32_t a0, a1, a2, a3;
+                    if constexpr (VPAIR) {
+                        const int o = mt * BITS / 2 - 4 * qd;  // word of coordinates 16 mt + 2 g8, + 1
+                        const uint32_t x01 = __byte_perm(quad_at(vq[0], o), quad_at(vq[1], o), psel[mt & 1]);
+                        const uint32_t x23 = __byte_perm(quad_at(vq[2], o), quad_at(vq[3], o), psel[mt & 1]);
+                        a0 = code_h2(x01, pm0); a1 = code_h2(x01, pm1); a2 = code_h2(x23, pm0); a3 = code_h2(x23, pm1);
+                    } else {
+                        const int o0 = 2 * mt - 4 * qd, o1 = o0 + 1;  // words of coordinates 16 mt + g8, + 8
+                        a0 = code_h2(__byte_perm(quad_at(vq[0], o0), quad_at(vq[1], o0), ssel), sm);
+                        a1 = code_h2(__byte_perm(quad_at(vq[0], o1), quad_at(vq[1], o1), ssel), sm);
+                        a2 = code_h2(__byte_perm(quad_at(vq[2], o0), quad_at(vq[3], o0), ssel), sm);
+                        a3 = code_h2(__byte_perm(quad_at(vq[2], o1), quad_at(vq[3], o1), ssel), sm);
+                    }
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) mma_16816(acc_v[nt][mt], a0, a1, a2, a3, bv[nt][0], bv[nt][1]);
                 }
             }
         }
@@ -493,7 +553,7 @@ __global__ void __launch_bounds__(KA_WARPS * 32, GQ <= 4 ? 2 : 1)
     }
 
     // totals over the 8 row lanes of each head, then the head's outputs:
-    // coordinates 16 mt + g8 (+ 8) = (hi + lo) 2^-shift + the zeros' share
+    // (hi + lo) 2^-shift + the zeros' share
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -509,7 +569,7 @@ __global__ void __launch_bounds__(KA_WARPS * 32, GQ <= 4 ? 2 : 1)
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
         const int hh = 4 * nt + t4;
-        if (hh < GQ) {
+        if (GQ % 4 == 0 || hh < GQ) {
             if (g8 == 0) {
                 ms[warp * GQ + hh] = m[nt];
                 ls[warp * GQ + hh] = l[nt];
@@ -518,8 +578,10 @@ __global__ void __launch_bounds__(KA_WARPS * 32, GQ <= 4 ? 2 : 1)
 #pragma unroll
             for (int mt = 0; mt < 8; ++mt) {
                 const float z = zb[nt][16 * mt / G];
-                o[16 * mt + g8] = fmaf(acc_v[nt][mt][0] + acc_v[nt][mt][1], usc, z);
-                o[16 * mt + g8 + 8] = fmaf(acc_v[nt][mt][2] + acc_v[nt][mt][3], usc, z);
+                const int d0 = VPAIR ? 16 * mt + 2 * g8 : 16 * mt + g8;
+                const int d1 = VPAIR ? d0 + 1 : d0 + 8;
+                o[d0] = fmaf(acc_v[nt][mt][0] + acc_v[nt][mt][1], uv0, z);
+                o[d1] = fmaf(acc_v[nt][mt][2] + acc_v[nt][mt][3], uv1, z);
             }
         }
     }
