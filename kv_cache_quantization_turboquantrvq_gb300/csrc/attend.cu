@@ -13,18 +13,21 @@
 // a fixed number of keys; one CTA of 8 warps takes one chunk, so the grid is
 // balanced whatever the mix of cache lengths.  The GQ = Hq / Hkv query heads
 // of a kv head are served together, so each key and value row is read once.
-// Each warp streams its own tiles of 32 keys: the bulk-copy engine
-// (cp.async.bulk) lands the tile's value rows and both code streams - three
-// contiguous ranges - in one of two shared-memory stages per warp while the
-// warp works on the other.  Per tile:
+// Each warp streams its own tiles of 32 keys: TMA lands the tile's value rows
+// (two 64-coordinate boxes, 128-byte swizzled) and the bulk-copy engine both
+// code streams in one of two shared-memory stages per warp while the warp
+// works on the other.  Per tile:
 //   scores   one key per lane: the lane decodes its key's 128 coordinates
 //            through a shuffle table (c1 + c2 merged for b <= 2) and forms
 //            the GQ dot products with the rotated query, which every lane
 //            reads from shared memory as a broadcast (paired-FMA arithmetic);
 //   softmax  the tile maximum per head is one warp redux; running maximum,
 //            rescale and the per-lane partial sums follow the online softmax;
-//   values   lanes own 4 coordinates each; the weights are broadcast from
-//            shared memory and the value rows read from the stage.
+//   values   a dense product on the tensor cores: O[coord][(head, hi/lo)] +=
+//            sum_k V[k][coord] w[k][(head, hi/lo)] in 16 x 8 x 16 tiles, the
+//            fp16 values read transposed from the swizzled boxes (ldmatrix),
+//            each weight carried as two fp16 columns (its leading 11 bits and
+//            the rounded rest) and accumulated in fp32.
 // Warps, then CTAs (the chunks, through the caller's workspace and a combine
 // kernel), are merged at the end.  Softmax arithmetic is in base 2 (the query
 // carries scale * log2(e)).
@@ -54,17 +57,21 @@ constexpr float NEG_INF = -__builtin_huge_valf();
 template <int BITS>
 struct AtTile {
     static constexpr int W = D * BITS / 32;       // code words per key and stream
-    static constexpr int VAL = TK * D * 2;        // value rows of a tile (bytes)
+    static constexpr int VAL = TK * D * 2;        // value rows of a tile: two 64-coordinate boxes
     static constexpr int COD = TK * W * 4;        // one code stream of a tile
     static constexpr int STAGE = VAL + 2 * COD;
 };
 
+constexpr int WS = TK + 8;    // weights row stride (floats) per head: 4 heads on distinct banks
+constexpr float SIG = 14.0f;  // exponent offset of the weights (w <= 2^14, never fp16-subnormal)
+
 template <int BITS, int GQ>
 constexpr int at_smem()
 {
-    return D * GQ * 4                                  // rotated query [c][g]
-           + AT_WARPS * TK * GQ * 4                     // weights [warp][key][g]
-           + AT_WARPS * AT_STAGES * AtTile<BITS>::STAGE // stages
+    return 1024                                         // alignment slack (128-byte swizzle)
+           + AT_WARPS * AT_STAGES * AtTile<BITS>::STAGE // stages (multiples of 1024 bytes)
+           + D * GQ * 4                                 // rotated query [c][g]
+           + AT_WARPS * GQ * WS * 4                     // weights [warp][g][key]
            + AT_WARPS * AT_STAGES * 8;                  // mbarriers
 }
 
@@ -77,6 +84,38 @@ __device__ __forceinline__ int ord_of(float x)
 __device__ __forceinline__ float float_of_ord(int i) { return __int_as_float(i >= 0 ? i : i ^ 0x7fffffff); }
 
 __device__ __forceinline__ float2 f2(float a, float b) { return make_float2(a, b); }
+__device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
+
+// The fp16 pair of this lane's part of (w0, w1): hi lanes (mh = ~0x1fff,
+// ml = 0) take w with its mantissa cut to fp16's 10 bits (exact in fp16), lo
+// lanes (mh = ~0, ml = ~0x1fff) the rest, rounded to fp16; the two columns of
+// one head together carry w to about 21 bits.
+__device__ __forceinline__ uint32_t split_pack(float2 u, uint32_t mh, uint32_t ml)
+{
+    const uint32_t ux = __float_as_uint(u.x), uy = __float_as_uint(u.y);
+    const float2 a = f2(__uint_as_float(ux & mh), __uint_as_float(uy & mh));
+    const float2 c = f2(__uint_as_float((ux & ml) ^ 0x80000000u), __uint_as_float((uy & ml) ^ 0x80000000u));
+    return h2_bits(__float22half2_rn(__fadd2_rn(a, c)));
+}
+
+// Four 8 x 8 fp16 matrices from shared memory, transposed (lane i supplies the
+// row address of matrix i / 8).
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+// d += a * b for one 16 x 8 x 16 tile, fp16 operands, fp32 accumulation.
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                          uint32_t b0, uint32_t b1)
+{
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
 
 // acc[g] += q[c][g] * y for the GQ heads: the rotated query row of coordinate
 // c is GQ consecutive floats in shared memory.
@@ -161,11 +200,12 @@ __global__ void __launch_bounds__(AT_WARPS * 32, 1) rvq_attend_kernel(const __gr
     using T = AtTile<BITS>;
     constexpr int W = T::W;
     constexpr int L = 1 << BITS;
-    extern __shared__ __align__(128) unsigned char smem[];
-    float *qs = reinterpret_cast<float *>(smem);
+    constexpr int NT = (2 * GQ + 7) / 8;  // value n-tiles of 8 (head, hi / lo) columns
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    unsigned char *stages = smem_1k(smem_raw);
+    float *qs = reinterpret_cast<float *>(stages + AT_WARPS * AT_STAGES * T::STAGE);
     float *wb = qs + D * GQ;
-    unsigned char *stages = reinterpret_cast<unsigned char *>(wb + AT_WARPS * TK * GQ);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(stages + AT_WARPS * AT_STAGES * T::STAGE);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(wb + AT_WARPS * GQ * WS);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int bh = blockIdx.y, split = blockIdx.x;
@@ -192,8 +232,11 @@ __global__ void __launch_bounds__(AT_WARPS * 32, 1) rvq_attend_kernel(const __gr
             const int k0 = s0 + t * TK;
             const int n = min(TK, s1 - k0);
             unsigned char *dst = my_st + st * T::STAGE;
-            mbar_arrive_expect_tx(&my_bar[st], (uint32_t)(n * (D * 2 + 2 * W * 4)));
-            bulk_g2s(dst, static_cast<const __half *>(p.v) + (kbase + k0) * D, (uint32_t)(n * D * 2), &my_bar[st], pol);
+            // value rows: two boxes of 64 coordinates x 32 rows, 128-byte swizzle
+            // (rows past the tensor are zero-filled, every box counts in full)
+            mbar_arrive_expect_tx(&my_bar[st], (uint32_t)(T::VAL + n * 2 * W * 4));
+            tma_load_2d(dst, &p.tmv, 0, (int)(kbase + k0), &my_bar[st], pol);
+            tma_load_2d(dst + T::VAL / 2, &p.tmv, 64, (int)(kbase + k0), &my_bar[st], pol);
             bulk_g2s(dst + T::VAL, p.p1 + (kbase + k0) * W, (uint32_t)(n * W * 4), &my_bar[st], pol);
             bulk_g2s(dst + T::VAL + T::COD, p.p2 + (kbase + k0) * W, (uint32_t)(n * W * 4), &my_bar[st], pol);
         }
@@ -235,16 +278,29 @@ __global__ void __launch_bounds__(AT_WARPS * 32, 1) rvq_attend_kernel(const __gr
     const float tab = BITS == 4 ? 0.0f : p.c1[lane & (L - 1)] + p.c2[(lane >> BITS) & (L - 1)];
     const float tc1 = p.c1[lane & (L - 1)];
     const float tc2 = p.c2[lane & (L - 1)];
-    float *my_w = wb + warp * TK * GQ;
+    float *my_w = wb + warp * GQ * WS;  // weights [g][key]
 
+    // Values on the tensor cores: O[coord][(head, part)] += sum_k V[k][coord]
+    // w[k][(head, part)], 16 x 8 x 16 tiles.  Lane = 4 g8 + t4: its
+    // accumulator rows are coordinates 16 mt + g8 and + 8, its columns
+    // 2 t4, 2 t4 + 1 head 4 nt + t4, hi and lo; its B column g8 is head
+    // 4 nt + g8 / 2, hi part for even g8, lo part for odd.
+    const int g8 = lane >> 2, t4 = lane & 3;
+    const bool lo = (g8 & 1) != 0;
+    const uint32_t mh = lo ? 0xFFFFFFFFu : 0xFFFFE000u, ml = lo ? 0xFFFFE000u : 0u;
     float m[GQ], l[GQ];
-    float2 o[GQ][2];  // coordinates 4 lane .. 4 lane + 3
+    float acc[NT][8][4];
 #pragma unroll
     for (int g = 0; g < GQ; ++g) {
         m[g] = NEG_INF;
         l[g] = 0.0f;
-        o[g][0] = o[g][1] = f2(0.0f, 0.0f);
     }
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) acc[nt][mt][j] = 0.0f;
 
     for (int it = 0;; ++it) {
         const int t = warp + it * AT_WARPS;
@@ -281,63 +337,77 @@ __global__ void __launch_bounds__(AT_WARPS * 32, 1) rvq_attend_kernel(const __gr
         float s[GQ];
         key_scores<BITS, GQ>(qs, w1, w2, tab, tc1, tc2, s);
 
-        // online softmax over the tile
+        // online softmax over the tile; the running maximum carries an offset
+        // of SIG so the weights reach up to 2^SIG (it cancels in the merge)
+        float fr[GQ];
+        bool resc = false;
 #pragma unroll
         for (int g = 0; g < GQ; ++g) {
             const float sc = valid ? s[g] * nrm : NEG_INF;
-            const float mt = float_of_ord(__reduce_max_sync(FULL_MASK, ord_of(sc)));
-            if (mt > m[g]) {  // warp-uniform
-                const float f = exp2f(m[g] - mt);
-                l[g] *= f;
-                o[g][0] = __fmul2_rn(o[g][0], f2(f, f));
-                o[g][1] = __fmul2_rn(o[g][1], f2(f, f));
-                m[g] = mt;
+            const float cand = float_of_ord(__reduce_max_sync(FULL_MASK, ord_of(sc))) - SIG;
+            fr[g] = 1.0f;
+            if (cand > m[g]) {  // warp-uniform
+                fr[g] = exp2f(m[g] - cand);
+                l[g] *= fr[g];
+                m[g] = cand;
+                resc = true;
             }
             const float w = exp2f(sc - m[g]);
             l[g] += w;
-            s[g] = w;
+            my_w[g * WS + lane] = w;
         }
-        if constexpr (GQ == 1) {
-            my_w[lane] = s[0];
-        } else if constexpr (GQ == 2) {
-            *reinterpret_cast<float2 *>(my_w + lane * 2) = f2(s[0], s[1]);
-        } else {
+        if (resc) {
 #pragma unroll
-            for (int g = 0; g < GQ; g += 4)
-                *reinterpret_cast<float4 *>(my_w + lane * GQ + g) = make_float4(s[g], s[g + 1], s[g + 2], s[g + 3]);
+            for (int nt = 0; nt < NT; ++nt) {
+                float f = fr[4 * nt < GQ ? 4 * nt : 0];
+#pragma unroll
+                for (int j = 1; j < 4; ++j)
+                    if (4 * nt + j < GQ && t4 == j) f = fr[4 * nt + j];
+#pragma unroll
+                for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) acc[nt][mt][j] *= f;
+            }
         }
         __syncwarp();
 
-        // values: lane owns coordinates 4 lane .. 4 lane + 3
-        const uint2 *vr = reinterpret_cast<const uint2 *>(sb) + lane;
-        auto accumulate = [&](int k) {
-            const uint2 u = vr[k * (D / 4)];
-            const float2 v01 = __half22float2(*reinterpret_cast<const __half2 *>(&u.x));
-            const float2 v23 = __half22float2(*reinterpret_cast<const __half2 *>(&u.y));
-            float wk[GQ];
-            if constexpr (GQ == 1) {
-                wk[0] = my_w[k];
-            } else if constexpr (GQ == 2) {
-                const float2 x = *reinterpret_cast<const float2 *>(my_w + k * 2);
-                wk[0] = x.x; wk[1] = x.y;
-            } else {
+        // values: per 16-key half kt, the weight columns, then 8 blocks of 16
+        // coordinates read transposed from the swizzled value boxes
+        const uint32_t vbase = smem_u32(sb);
 #pragma unroll
-                for (int g = 0; g < GQ; g += 4) {
-                    const float4 x = *reinterpret_cast<const float4 *>(my_w + k * GQ + g);
-                    wk[g] = x.x; wk[g + 1] = x.y; wk[g + 2] = x.z; wk[g + 3] = x.w;
+        for (int kt = 0; kt < 2; ++kt) {
+            uint32_t bv[NT][2];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                const int hb = 4 * nt + (g8 >> 1);
+                float2 w01 = f2(0.0f, 0.0f), w89 = f2(0.0f, 0.0f);
+                if (GQ % 4 == 0 || hb < GQ) {
+                    w01 = *reinterpret_cast<const float2 *>(my_w + hb * WS + 16 * kt + 2 * t4);
+                    w89 = *reinterpret_cast<const float2 *>(my_w + hb * WS + 16 * kt + 2 * t4 + 8);
                 }
+                bv[nt][0] = split_pack(w01, mh, ml);
+                bv[nt][1] = split_pack(w89, mh, ml);
             }
+            // keys past n hold stale rows: mask their halves out of the operands
+            uint32_t ka = 0xFFFFFFFFu, kb = 0xFFFFFFFFu;
+            if (n < TK) {
+                const int k = 16 * kt + 2 * t4;
+                ka = (k < n ? 0x0000FFFFu : 0u) | (k + 1 < n ? 0xFFFF0000u : 0u);
+                kb = (k + 8 < n ? 0x0000FFFFu : 0u) | (k + 9 < n ? 0xFFFF0000u : 0u);
+            }
+            // lane i of the ldmatrix supplies row (key) 16 kt + 8 (i / 16) + i % 8 of
+            // 16-byte chunk 2 (mt % 4) + (i / 8) % 2 of box mt / 4
+            const int key = 16 * kt + 8 * (lane >> 4) + (lane & 7);
 #pragma unroll
-            for (int g = 0; g < GQ; ++g) {
-                o[g][0] = __ffma2_rn(f2(wk[g], wk[g]), v01, o[g][0]);
-                o[g][1] = __ffma2_rn(f2(wk[g], wk[g]), v23, o[g][1]);
+            for (int mt = 0; mt < 8; ++mt) {
+                const int c = 2 * (mt & 3) + ((lane >> 3) & 1);
+                const uint32_t addr = vbase + (uint32_t)((mt >> 2) * (T::VAL / 2)) + swz128(key, c);
+                uint32_t a0, a1, a2, a3;
+                ldsm_x4_t(addr, a0, a1, a2, a3);
+                a0 &= ka; a1 &= ka; a2 &= kb; a3 &= kb;
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) mma_16816(acc[nt][mt], a0, a1, a2, a3, bv[nt][0], bv[nt][1]);
             }
-        };
-        if (n == TK) {
-#pragma unroll 8
-            for (int k = 0; k < TK; ++k) accumulate(k);
-        } else {
-            for (int k = 0; k < n; ++k) accumulate(k);
         }
 
         // the stage and the weights are consumed: recycle the stage
@@ -362,8 +432,18 @@ __global__ void __launch_bounds__(AT_WARPS * 32, 1) rvq_attend_kernel(const __gr
             ms[warp * GQ + g] = m[g];
             ls[warp * GQ + g] = l[g];
         }
-        *reinterpret_cast<float4 *>(os + (warp * GQ + g) * D + 4 * lane) =
-            make_float4(o[g][0].x, o[g][0].y, o[g][1].x, o[g][1].y);
+    }
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        const int hh = 4 * nt + t4;
+        if (GQ % 4 == 0 || hh < GQ) {
+            float *o = os + (warp * GQ + hh) * D;
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt) {
+                o[16 * mt + g8] = acc[nt][mt][0] + acc[nt][mt][1];
+                o[16 * mt + g8 + 8] = acc[nt][mt][2] + acc[nt][mt][3];
+            }
+        }
     }
     __syncthreads();
     for (int i = threadIdx.x; i < GQ * D; i += blockDim.x) {
@@ -419,15 +499,24 @@ __global__ void __launch_bounds__(D) rvq_attend_combine_kernel(const __grid_cons
 template <int BITS, int GQ>
 cudaError_t launch_at(const RvqAttendParams &p, cudaStream_t stream)
 {
+    RvqAttendParams q = p;
+    const uint64_t rows = (uint64_t)p.B * p.Hkv * p.S_cap;
+    if (rows > 0x7fffffffULL) return cudaErrorInvalidValue;  // TMA row coordinates are 32-bit
+    if (rows > 0) {
+        const uint64_t dims[2] = {(uint64_t)D, rows};
+        const uint64_t strides[1] = {(uint64_t)D * 2};
+        const uint32_t box[2] = {64u, (uint32_t)TK};
+        if (!encode_tmap_f16(&q.tmv, p.v, 2, dims, strides, box, true, true)) return cudaErrorInvalidValue;
+    }
     auto kern = rvq_attend_kernel<BITS, GQ>;
     constexpr int smem = at_smem<BITS, GQ>();
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    dim3 grid(p.nsplit, p.B * p.Hkv);
-    kern<<<grid, AT_WARPS * 32, smem, stream>>>(p);
+    dim3 grid(q.nsplit, q.B * q.Hkv);
+    kern<<<grid, AT_WARPS * 32, smem, stream>>>(q);
     e = cudaGetLastError();
-    if (e != cudaSuccess || p.nsplit == 1) return e;
-    rvq_attend_combine_kernel<<<p.B * p.Hq, D, 0, stream>>>(p);
+    if (e != cudaSuccess || q.nsplit == 1) return e;
+    rvq_attend_combine_kernel<<<q.B * q.Hq, D, 0, stream>>>(q);
     return cudaGetLastError();
 }
 

@@ -112,6 +112,8 @@ struct KiviDequantParams {
 // Decode-time attention over an RVQ key cache (attend.cu).
 constexpr int AT_PART = 2 + 128;  // floats of one split's partial: max, sum, output
 struct RvqAttendParams {
+    CUtensorMap tmv;               // v as [B*Hkv*S_cap, 128] fp16, 64 x 32 boxes, 128-byte swizzle
+                                   // (set by the launcher)
     const void *q;                 // fp16 [B, Hq, 128]
     const uint32_t *p1, *p2;       // [B, Hkv, S_cap, W]
     const float *norms;            // [B, Hkv, S_cap]
