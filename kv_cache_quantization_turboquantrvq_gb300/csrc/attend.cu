@@ -50,27 +50,29 @@ static __device__ __align__(256) float g_at_scratch[VQ_ATTEND_SCRATCH_BYTES / si
 
 constexpr int D = 128;
 constexpr int AT_WARPS = 8;
-constexpr int TK = 32;  // keys per warp tile: one per lane
+constexpr int TK = 32;    // chunk sizes are multiples of 32 keys
+constexpr int TILE = 16;  // keys per warp tile: two lanes per key, 64 coordinates each
 constexpr int AT_STAGES = 2;
 constexpr float NEG_INF = -__builtin_huge_valf();
 
 template <int BITS>
 struct AtTile {
     static constexpr int W = D * BITS / 32;       // code words per key and stream
-    static constexpr int VAL = TK * D * 2;        // value rows of a tile: two 64-coordinate boxes
-    static constexpr int COD = TK * W * 4;        // one code stream of a tile
-    static constexpr int STAGE = VAL + 2 * COD;
+    static constexpr int VAL = TILE * D * 2;      // value rows of a tile: two 64-coordinate boxes
+    static constexpr int COD = TILE * W * 4;      // one code stream of a tile
+    static constexpr int STAGE = (VAL + 2 * COD + 1023) / 1024 * 1024;  // boxes stay 1024-aligned
 };
 
-constexpr int WS = TK + 8;    // weights row stride (floats) per head: 4 heads on distinct banks
+constexpr int WS = TILE + 8;  // weights row stride (floats) per head: 4 heads on distinct banks
 constexpr float SIG = 14.0f;  // exponent offset of the weights (w <= 2^14, never fp16-subnormal)
+constexpr int QPAD = 4;       // the query's coordinates 64..127 sit 16 bytes further (other banks)
 
 template <int BITS, int GQ>
 constexpr int at_smem()
 {
     return 1024                                         // alignment slack (128-byte swizzle)
            + AT_WARPS * AT_STAGES * AtTile<BITS>::STAGE // stages (multiples of 1024 bytes)
-           + D * GQ * 4                                 // rotated query [c][g]
+           + (D * GQ + QPAD) * 4                        // rotated query [c][g]
            + AT_WARPS * GQ * WS * 4                     // weights [warp][g][key]
            + AT_WARPS * AT_STAGES * 8;                  // mbarriers
 }
@@ -137,12 +139,10 @@ __device__ __forceinline__ void score_coord(const float *qs, int c, float y, flo
 
 // Dot products of the rotated query with the key whose codes are w1, w2.
 // ae/ao take even and odd coordinates (two independent chains).
-template <int BITS, int GQ>
-__device__ __forceinline__ void key_scores(const float *qs, const uint32_t (&w1)[D * BITS / 32],
-                                           const uint32_t (&w2)[D * BITS / 32], float tab, float tc1,
-                                           float tc2, float (&s)[GQ])
+template <int BITS, int GQ, int W>
+__device__ __forceinline__ void key_scores(const float *qs, const uint32_t (&w1)[W], const uint32_t (&w2)[W],
+                                           float tab, float tc1, float tc2, float (&s)[GQ])
 {
-    constexpr int W = D * BITS / 32;
     constexpr int E = 32 / BITS;
     constexpr int NA = GQ > 1 ? GQ / 2 : 1;
     float2 ae[NA], ao[NA];
@@ -195,7 +195,7 @@ __device__ __forceinline__ void key_scores(const float *qs, const uint32_t (&w1)
 }
 
 template <int BITS, int GQ>
-__global__ void __launch_bounds__(AT_WARPS * 32, 1) rvq_attend_kernel(const __grid_constant__ RvqAttendParams p)
+__global__ void __launch_bounds__(AT_WARPS * 32, 2) rvq_attend_kernel(const __grid_constant__ RvqAttendParams p)
 {
     using T = AtTile<BITS>;
     constexpr int W = T::W;
@@ -204,7 +204,7 @@ __global__ void __launch_bounds__(AT_WARPS * 32, 1) rvq_attend_kernel(const __gr
     extern __shared__ __align__(128) unsigned char smem_raw[];
     unsigned char *stages = smem_1k(smem_raw);
     float *qs = reinterpret_cast<float *>(stages + AT_WARPS * AT_STAGES * T::STAGE);
-    float *wb = qs + D * GQ;
+    float *wb = qs + D * GQ + QPAD;
     uint64_t *bars = reinterpret_cast<uint64_t *>(wb + AT_WARPS * GQ * WS);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -215,7 +215,7 @@ __global__ void __launch_bounds__(AT_WARPS * 32, 1) rvq_attend_kernel(const __gr
     const int s0 = split * p.chunk;
     if (s0 >= len && !(split == 0 && p.nsplit == 1)) return;  // no keys: the combine skips this chunk
     const int s1 = min(len, s0 + p.chunk);
-    const int ntiles = s1 > s0 ? (s1 - s0 + TK - 1) / TK : 0;
+    const int ntiles = s1 > s0 ? (s1 - s0 + TILE - 1) / TILE : 0;
 
     unsigned char *my_st = stages + warp * AT_STAGES * T::STAGE;
     uint64_t *my_bar = bars + warp * AT_STAGES;
@@ -229,8 +229,8 @@ __global__ void __launch_bounds__(AT_WARPS * 32, 1) rvq_attend_kernel(const __gr
     const uint64_t pol = l2_policy_evict_first();
     auto issue = [&](int t, int st) {
         if (lane == 0) {
-            const int k0 = s0 + t * TK;
-            const int n = min(TK, s1 - k0);
+            const int k0 = s0 + t * TILE;
+            const int n = min(TILE, s1 - k0);
             unsigned char *dst = my_st + st * T::STAGE;
             // value rows: two boxes of 64 coordinates x 32 rows, 128-byte swizzle
             // (rows past the tensor are zero-filled, every box counts in full)
@@ -271,7 +271,7 @@ __global__ void __launch_bounds__(AT_WARPS * 32, 1) rvq_attend_kernel(const __gr
             }
         }
 #pragma unroll
-        for (int j = 0; j < 4; ++j) qs[(4 * lane + j) * GQ + warp] = a[j] * p.qscale;
+        for (int j = 0; j < 4; ++j) qs[(4 * lane + j) * GQ + (lane >= 16 ? QPAD : 0) + warp] = a[j] * p.qscale;
     }
     __syncthreads();
 
@@ -288,6 +288,7 @@ __global__ void __launch_bounds__(AT_WARPS * 32, 1) rvq_attend_kernel(const __gr
     const int g8 = lane >> 2, t4 = lane & 3;
     const bool lo = (g8 & 1) != 0;
     const uint32_t mh = lo ? 0xFFFFFFFFu : 0xFFFFE000u, ml = lo ? 0xFFFFE000u : 0u;
+    const int key = lane & 15, hf = lane >> 4;  // scoring: key of the tile and its coordinate half
     float m[GQ], l[GQ];
     float acc[NT][8][4];
 #pragma unroll
@@ -306,10 +307,10 @@ __global__ void __launch_bounds__(AT_WARPS * 32, 1) rvq_attend_kernel(const __gr
         const int t = warp + it * AT_WARPS;
         if (t >= ntiles) break;
         const int st = it % AT_STAGES;
-        const int k0 = s0 + t * TK;
-        const int n = min(TK, s1 - k0);
-        const bool valid = lane < n;
-        const float nrm = valid ? __ldg(p.norms + kbase + k0 + lane) : 0.0f;
+        const int k0 = s0 + t * TILE;
+        const int n = min(TILE, s1 - k0);
+        const bool valid = key < n;
+        const float nrm = valid ? __ldg(p.norms + kbase + k0 + key) : 0.0f;
         const bool ok = mbar_wait_bounded(&my_bar[st], (uint32_t)(it / AT_STAGES) & 1u);
         if (!__all_sync(FULL_MASK, ok)) {
             if (lane == 0) atomicOr(&g_at_err, (unsigned)VQ_DEVERR_WAIT_TIMEOUT);
@@ -322,20 +323,29 @@ __global__ void __launch_bounds__(AT_WARPS * 32, 1) rvq_attend_kernel(const __gr
         }
         const unsigned char *sb = my_st + st * T::STAGE;
 
-        // scores: one key per lane
-        uint32_t w1[W], w2[W];
+        // scores: lanes key and key + 16 take coordinates 0..63 and 64..127
+        // of one key (the words W/2 hf .. of both streams), then add up
+        constexpr int HW = W / 2;
+        uint32_t w1[HW], w2[HW];
         {
-            const uint4 *c1p = reinterpret_cast<const uint4 *>(sb + T::VAL) + lane * (W / 4);
-            const uint4 *c2p = reinterpret_cast<const uint4 *>(sb + T::VAL + T::COD) + lane * (W / 4);
+            const uint32_t *c1p = reinterpret_cast<const uint32_t *>(sb + T::VAL) + key * W + hf * HW;
+            const uint32_t *c2p = reinterpret_cast<const uint32_t *>(sb + T::VAL + T::COD) + key * W + hf * HW;
+            if constexpr (HW == 2) {
+                const uint2 x = *reinterpret_cast<const uint2 *>(c1p), y = *reinterpret_cast<const uint2 *>(c2p);
+                w1[0] = x.x; w1[1] = x.y; w2[0] = y.x; w2[1] = y.y;
+            } else {
 #pragma unroll
-            for (int i = 0; i < W / 4; ++i) {
-                const uint4 x = c1p[i], y = c2p[i];
-                w1[4 * i] = x.x; w1[4 * i + 1] = x.y; w1[4 * i + 2] = x.z; w1[4 * i + 3] = x.w;
-                w2[4 * i] = y.x; w2[4 * i + 1] = y.y; w2[4 * i + 2] = y.z; w2[4 * i + 3] = y.w;
+                for (int i = 0; i < HW / 4; ++i) {
+                    const uint4 x = reinterpret_cast<const uint4 *>(c1p)[i], y = reinterpret_cast<const uint4 *>(c2p)[i];
+                    w1[4 * i] = x.x; w1[4 * i + 1] = x.y; w1[4 * i + 2] = x.z; w1[4 * i + 3] = x.w;
+                    w2[4 * i] = y.x; w2[4 * i + 1] = y.y; w2[4 * i + 2] = y.z; w2[4 * i + 3] = y.w;
+                }
             }
         }
         float s[GQ];
-        key_scores<BITS, GQ>(qs, w1, w2, tab, tc1, tc2, s);
+        key_scores<BITS, GQ, HW>(qs + hf * (64 * GQ + QPAD), w1, w2, tab, tc1, tc2, s);
+#pragma unroll
+        for (int g = 0; g < GQ; ++g) s[g] += __shfl_xor_sync(FULL_MASK, s[g], 16);
 
         // online softmax over the tile; the running maximum carries an offset
         // of SIG so the weights reach up to 2^SIG (it cancels in the merge)
@@ -353,8 +363,8 @@ __global__ void __launch_bounds__(AT_WARPS * 32, 1) rvq_attend_kernel(const __gr
                 resc = true;
             }
             const float w = exp2f(sc - m[g]);
-            l[g] += w;
-            my_w[g * WS + lane] = w;
+            l[g] += w;  // both lanes of a key: the warp total is halved at the end
+            if (hf == 0) my_w[g * WS + key] = w;
         }
         if (resc) {
 #pragma unroll
@@ -371,11 +381,11 @@ __global__ void __launch_bounds__(AT_WARPS * 32, 1) rvq_attend_kernel(const __gr
         }
         __syncwarp();
 
-        // values: per 16-key half kt, the weight columns, then 8 blocks of 16
-        // coordinates read transposed from the swizzled value boxes
+        // values: the weight columns, then 8 blocks of 16 coordinates read
+        // transposed from the swizzled value boxes
         const uint32_t vbase = smem_u32(sb);
 #pragma unroll
-        for (int kt = 0; kt < 2; ++kt) {
+        for (int kt = 0; kt < TILE / 16; ++kt) {
             uint32_t bv[NT][2];
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
@@ -390,7 +400,7 @@ __global__ void __launch_bounds__(AT_WARPS * 32, 1) rvq_attend_kernel(const __gr
             }
             // keys past n hold stale rows: mask their halves out of the operands
             uint32_t ka = 0xFFFFFFFFu, kb = 0xFFFFFFFFu;
-            if (n < TK) {
+            if (n < TILE) {
                 const int k = 16 * kt + 2 * t4;
                 ka = (k < n ? 0x0000FFFFu : 0u) | (k + 1 < n ? 0xFFFF0000u : 0u);
                 kb = (k + 8 < n ? 0x0000FFFFu : 0u) | (k + 9 < n ? 0xFFFF0000u : 0u);
@@ -419,9 +429,11 @@ __global__ void __launch_bounds__(AT_WARPS * 32, 1) rvq_attend_kernel(const __gr
     // per-warp sums, then merge the warps through shared memory (the stages
     // are free: every copy this CTA issued has been waited for)
 #pragma unroll
-    for (int g = 0; g < GQ; ++g)
+    for (int g = 0; g < GQ; ++g) {
 #pragma unroll
         for (int off = 16; off >= 1; off >>= 1) l[g] += __shfl_xor_sync(FULL_MASK, l[g], off);
+        l[g] *= 0.5f;
+    }
     __syncthreads();
     float *ms = reinterpret_cast<float *>(stages);
     float *ls = ms + AT_WARPS * GQ;
@@ -505,7 +517,7 @@ cudaError_t launch_at(const RvqAttendParams &p, cudaStream_t stream)
     if (rows > 0) {
         const uint64_t dims[2] = {(uint64_t)D, rows};
         const uint64_t strides[1] = {(uint64_t)D * 2};
-        const uint32_t box[2] = {64u, (uint32_t)TK};
+        const uint32_t box[2] = {64u, (uint32_t)TILE};
         if (!encode_tmap_f16(&q.tmv, p.v, 2, dims, strides, box, true, true)) return cudaErrorInvalidValue;
     }
     auto kern = rvq_attend_kernel<BITS, GQ>;
