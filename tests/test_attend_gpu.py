@@ -184,3 +184,26 @@ def test_attend_decode_shape_sampled(vq, oracle_mod):
         r16, r64 = oracle_mod.rvq_attend(q[sl], p1[sl, :, :L], p2[sl, :, :L], nr[sl, :, :L], v[sl, :, :L],
                                          bits, cb[0], cb[2], scale, want_f64=True)
         _check(o[sl], r16, r64, v[sl, :, :L])
+
+
+@pytest.mark.parametrize("bits,gq", [(1, 8), (2, 4), (4, 1)])
+def test_attend_rows_past_length_may_hold_anything(vq, oracle_mod, bits, gq):
+    """Rows past a sequence's length are never part of the result, whatever
+    they hold: the device copy carries NaN and inf norms and values there
+    (partial tiles read such rows into shared memory), the oracle sees the
+    same cache with finite rows.  Outputs must match the oracle's."""
+    B, Hkv, S = 3, 2, 512
+    cb = oracle_mod.rvq_codebooks(D, bits)
+    p1, p2, nr = _random_cache(B, Hkv, S, bits, 1100 + bits)
+    v = _values(B, Hkv, S, 1101 + bits)
+    q = np.random.default_rng(1102).standard_normal((B, Hkv * gq, D)).astype(np.float16)
+    lens = np.array([500, 17, 1], np.int32)
+    nr_bad, v_bad = nr.copy(), v.copy()
+    for b, n in enumerate(lens):
+        nr_bad[b, :, n:] = np.nan
+        v_bad[b, :, n:, 0::2] = np.float16(np.nan)
+        v_bad[b, :, n:, 1::2] = np.float16(np.inf)
+    o = _attend(vq, q, p1, p2, nr_bad, v_bad, bits, cb, 0.2, lens=lens)
+    r16, r64 = oracle_mod.rvq_attend(q, p1, p2, nr, v, bits, cb[0], cb[2], 0.2, lens=lens, want_f64=True)
+    assert np.all(np.isfinite(o.astype(np.float64)))
+    _check(o, r16, r64, v)

@@ -141,3 +141,35 @@ def test_rejects_bad_arguments(vq, oracle_mod):
         vq.vq_kivi_attend(q, dev, 2, 32, 0.1, k_res=_dev(kr), v_res=_dev(vr),
                           workspace=torch.empty(4, dtype=torch.float32, device="cuda"))
     assert e.value.status == vq.VQ_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("bits,G,gq", [(2, 32, 4), (4, 64, 2), (1, 128, 8)])
+def test_rows_past_length_may_hold_anything(vq, oracle_mod, bits, G, gq):
+    """Tokens past a sequence's length are never part of the result, whatever
+    the cache holds there: the device copy carries NaN and inf value scales
+    and zeros past the length and NaN key scales and zeros in groups wholly
+    past it (partial tiles stage such rows), the oracle sees finite data."""
+    B, Hkv, S_cap, R = 3, 2, 512, 5
+    lens = np.array([500, 40, 0], np.int32)
+    res = np.array([5, 0, 3], np.int32)
+    seed = 1200 + bits + G
+    host, dev, kr, vr, vmax = _cache(oracle_mod, B, Hkv, S_cap, R, bits, G, seed)
+    bad = {n: a.copy() for n, a in host.items()}
+    for b, n in enumerate(lens):
+        bad["v_scale"][b, :, n:] = np.float16(np.nan)
+        bad["v_zero"][b, :, n:] = np.float16(np.inf)
+        g0 = (n + G - 1) // G  # first group with no valid token
+        bad["k_scale"][b, :, g0:] = np.float16(np.nan)
+        bad["k_zero"][b, :, g0:] = np.float16(-np.inf)
+    dev = {n: _dev(a.view(np.int32) if a.dtype == np.uint32 else a) for n, a in bad.items()}
+    q = np.random.default_rng(seed + 2).standard_normal((B, Hkv * gq, D)).astype(np.float16)
+    out = vq.vq_kivi_attend(_dev(q), dev, bits, G, 0.15, k_res=_dev(kr), v_res=_dev(vr), lens=_dev(lens),
+                            res_lens=_dev(res))
+    torch.cuda.synchronize()
+    assert vq.vq_device_error() == 0
+    o = out.cpu().numpy()
+    r16, r64 = oracle_mod.kivi_attend(q, host["k_packed"], host["k_scale"], host["k_zero"], host["v_packed"],
+                                      host["v_scale"], host["v_zero"], bits, G, 0.15, k_res=kr, v_res=vr,
+                                      lens=lens, res_lens=res, want_f64=True)
+    assert np.all(np.isfinite(o.astype(np.float64)))
+    _check(o, r16, r64, vmax)
