@@ -232,7 +232,7 @@ __global__ void __launch_bounds__(AT_WARPS * 32, 2) rvq_attend_kernel(const __gr
             const int k0 = s0 + t * TILE;
             const int n = min(TILE, s1 - k0);
             unsigned char *dst = my_st + st * T::STAGE;
-            // value rows: two boxes of 64 coordinates x 32 rows, 128-byte swizzle
+            // value rows: two boxes of 64 coordinates x 16 rows, 128-byte swizzle
             // (rows past the tensor are zero-filled, every box counts in full)
             mbar_arrive_expect_tx(&my_bar[st], (uint32_t)(T::VAL + n * 2 * W * 4));
             tma_load_2d(dst, &p.tmv, 0, (int)(kbase + k0), &my_bar[st], pol);
