@@ -140,7 +140,10 @@ vq_status vq_rvq_unpack_dequant(const uint32_t *packed1, const uint32_t *packed2
  * over the first lens[b] tokens (all S_cap when lens is NULL; an empty cache
  * gives zeros), where k_s = n_s H (c1[i1] + c2[i2]) / sqrt(D) is the key that
  * vq_rvq_encode_pack encoded.  Keys are scored in the rotated domain straight
- * from their codes and never materialised.  fp32 arithmetic, fp16 output.
+ * from their codes and never materialised (fp32 arithmetic).  The weighted
+ * sum of the values runs on the tensor cores: fp16 values times each weight
+ * carried as two fp16 parts (about 21 bits together), fp32 accumulation.
+ * fp16 output.  Rows past lens[b] are never used, whatever they hold.
  *   q [B, Hq, D] fp16, device.
  *   packed1, packed2 [B, Hkv, S_cap, D*bits/32] uint32, norms [B, Hkv, S_cap]
  *     fp32, v [B, Hkv, S_cap, D] fp16, device (an RVQ cache and its values).
@@ -222,8 +225,13 @@ vq_status vq_rvq_attend_rs(const void *q_f16, const uint32_t *packed1, const uin
  * vq_kivi_attend - decode-time attention over a KIVI cache, reading the packed
  * codes directly (kivi page, first post, closing section: "Dequant-in-SDPA";
  * the reconstruction is the quantizer's g_hat = q * scale + zero, second
- * post, "What KIVI is").  Keys and values are reconstructed in registers in
- * fp32 (q * scale is exact, one rounding for + zero) and never written out.
+ * post, "What KIVI is").  Keys and values are never reconstructed: with the
+ * quantizer's scales and zeros, q . k_t = sum_d (q_d s_d) code + sum_d q_d z_d
+ * and sum_t w_t v_t = sum_t (w_t s_t) code + sum_t w_t z_t, and both code sums
+ * run on the tensor cores (codes exact in fp16, each float factor carried as
+ * two fp16 parts of about 21 bits together, fp32 accumulation); zero terms,
+ * softmax and merging are fp32.  Tokens past lens[b] are never used, whatever
+ * the cache holds there.
  * For every batch b and query head hq, with kv head h = hq / (Hq / Hkv):
  *   out[b][hq] = sum_t softmax_t(scale * q . k_t) v_t
  * over the first lens[b] quantized tokens (all S_cap when lens is NULL)
