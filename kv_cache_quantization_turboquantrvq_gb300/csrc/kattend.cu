@@ -311,6 +311,7 @@ __global__ void __launch_bounds__(KA_WARPS * 32, GQ <= 4 ? 2 : 1)
     float *my_w = wb + warp * KT * GQ;  // weights [head][slot]
 
     float m[NT], l[NT], zb[NT][NV], acc_v[NT][8][4];
+    float fsig = 30.0f;  // running exponent offset of the weights (non-increasing)
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
         m[nt] = NEG_INF;
@@ -408,8 +409,9 @@ __global__ void __launch_bounds__(KA_WARPS * 32, GQ <= 4 ? 2 : 1)
         // exponent offset of the weights: with every value scale of the tile
         // below 2^(E + 1), weights up to 2^(14 - E) keep w s below 2^15 and
         // out of the fp16 subnormals (the offset enters the running max, so
-        // it cancels in the normalisation)
-        float fsig;
+        // it cancels in the normalisation).  The warp keeps the smallest
+        // offset seen so far: a larger one would be as safe for this tile
+        // but would move the running max (and rescale the sums) more often.
         {
             uint32_t mb = 0;
             if (4 * lane < KT * NV) {
@@ -424,7 +426,7 @@ __global__ void __launch_bounds__(KA_WARPS * 32, GQ <= 4 ? 2 : 1)
                 mb = max(mm & 0xffffu, mm >> 16);
             }
             mb = __reduce_max_sync(FULL_MASK, mb);
-            fsig = (float)min(14 - ((int)(mb >> 10) - 15), 30);
+            fsig = fminf(fsig, (float)min(14 - ((int)(mb >> 10) - 15), 30));
         }
 
         // ---- online softmax: this lane holds tokens 16 mt + 2 g8 + rh of head 4 nt + t4
