@@ -323,12 +323,12 @@ def build_workload(name, dev, rank=0, layers=None, batch=None, chunked=False, ch
         def katt(stream=stream):
             api.vq_kivi_attend(q, cache, bits, G, 1.0 / np.sqrt(D), k_res=kr, v_res=vr, lens=lens, res_lens=res,
                                out=out, workspace=ws, stream=stream)
-        ops.append(Op("kivi_attend", "kivi_attend_kernel", katt, nb, ne, gpu_launches=3))
+        ops.append(Op("kivi_attend", "kivi_attend_kernel", katt, nb, ne, gpu_launches=2))
         inputs = [(q_np, q)]
         results.append(out)
         if chunked:
             c = new_chunk(inputs)
-            c["ops"] = [Op("kivi_attend", "kivi_attend_kernel", lambda: katt(chunk_stream), nb, ne, gpu_launches=3)]
+            c["ops"] = [Op("kivi_attend", "kivi_attend_kernel", lambda: katt(chunk_stream), nb, ne, gpu_launches=2)]
             c["results"] = [out]
     else:
         raise ValueError(name)

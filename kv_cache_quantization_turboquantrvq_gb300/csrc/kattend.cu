@@ -28,10 +28,11 @@
 // is scaled by a power of two so that |q| <= 1 and every q s fits in fp16.
 // The zero terms are plain sums (one per head and group).
 // Grid, staging and merging as the RVQ attention: fixed-size chunks of the
-// quantized tokens per CTA, one more CTA per (sequence, kv head) for the
-// residual window, per-warp double-buffered bulk copies (key words, the
-// group's key scale and zero, value words, value scales and zeros), partials
-// (max, sum, unnormalised output) merged by a combine kernel.
+// quantized tokens per CTA, plus one CTA per (sequence, kv head) in the same
+// grid for the residual window (so it overlaps the chunks), per-warp rings of
+// bulk copies (key words, the group's key scale and zero, value words, value
+// scales and zeros), partials (max, sum, unnormalised output) merged by a
+// combine kernel.
 #include <cuda_fp16.h>
 
 #include "device_common.cuh"
@@ -196,6 +197,88 @@ __device__ __forceinline__ void load_groups(const __half *src, float (&f)[NV])
     }
 }
 
+// The fp16 residual window of one (sequence, kv head), taken by one more CTA
+// of the chunk kernel's grid (it overlaps the chunks instead of following
+// them): warp w takes tokens w, w + 8, ..., two at a time with both rows'
+// loads issued first; lanes own 4 channels for the dot product (warp sum) and
+// 4 coordinates for the values.  Writes part nsplit.  qf holds GQ * D floats,
+// scratch the warps' merge.
+template <int GQ>
+__device__ __forceinline__ void ka_window(const KiviAttendParams &p, int bh, float *qf, unsigned char *scratch)
+{
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int b = bh / p.Hkv, h = bh - b * p.Hkv;
+    int rl = p.res_lens ? __ldg(p.res_lens + b) : p.R;
+    rl = rl < 0 ? 0 : (rl > p.R ? p.R : rl);
+    const int nparts = p.nsplit + 1;
+    if (rl == 0) return;  // the combine skips an empty window
+    (void)ka_load_query<GQ, D>(p, b, h, qf, false);
+    __syncthreads();
+    float qv[GQ][4];
+#pragma unroll
+    for (int g = 0; g < GQ; ++g)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) qv[g][c] = qf[g * D + 4 * lane + c];
+    float m[GQ], l[GQ], o[GQ][4];
+#pragma unroll
+    for (int g = 0; g < GQ; ++g) {
+        m[g] = NEG_INF;
+        l[g] = 0.0f;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) o[g][c] = 0.0f;
+    }
+    const __half *kr = static_cast<const __half *>(p.kr) + (size_t)bh * p.R * D;
+    const __half *vr = static_cast<const __half *>(p.vr) + (size_t)bh * p.R * D;
+    auto token = [&](uint2 ku, uint2 vu) {
+        const float2 k01 = __half22float2(*reinterpret_cast<const __half2 *>(&ku.x));
+        const float2 k23 = __half22float2(*reinterpret_cast<const __half2 *>(&ku.y));
+        const float2 v01 = __half22float2(*reinterpret_cast<const __half2 *>(&vu.x));
+        const float2 v23 = __half22float2(*reinterpret_cast<const __half2 *>(&vu.y));
+        const float kk[4] = {k01.x, k01.y, k23.x, k23.y};
+        const float vv[4] = {v01.x, v01.y, v23.x, v23.y};
+#pragma unroll
+        for (int g = 0; g < GQ; ++g) {
+            float s = 0.0f;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) s = fmaf(qv[g][c], kk[c], s);
+#pragma unroll
+            for (int off = 16; off >= 1; off >>= 1) s += __shfl_xor_sync(FULL_MASK, s, off);
+            const float mn = fmaxf(m[g], s);
+            const float f = exp2f(m[g] - mn);
+            const float w = exp2f(s - mn);
+            l[g] = l[g] * f + w;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) o[g][c] = fmaf(w, vv[c], o[g][c] * f);
+            m[g] = mn;
+        }
+    };
+    for (int r = warp; r < rl; r += 2 * KA_WARPS) {
+        const int r2 = r + KA_WARPS;
+        const uint2 ku = __ldg(reinterpret_cast<const uint2 *>(kr + (size_t)r * D) + lane);
+        const uint2 vu = __ldg(reinterpret_cast<const uint2 *>(vr + (size_t)r * D) + lane);
+        uint2 ku2 = make_uint2(0u, 0u), vu2 = make_uint2(0u, 0u);
+        if (r2 < rl) {
+            ku2 = __ldg(reinterpret_cast<const uint2 *>(kr + (size_t)r2 * D) + lane);
+            vu2 = __ldg(reinterpret_cast<const uint2 *>(vr + (size_t)r2 * D) + lane);
+        }
+        token(ku, vu);
+        if (r2 < rl) token(ku2, vu2);
+    }
+    // l is already the warp's total (every lane holds the same sums)
+    float *ms = reinterpret_cast<float *>(scratch);
+    float *ls = ms + KA_WARPS * GQ;
+    float *os = ls + KA_WARPS * GQ;
+#pragma unroll
+    for (int g = 0; g < GQ; ++g) {
+        if (lane == 0) {
+            ms[warp * GQ + g] = m[g];
+            ls[warp * GQ + g] = l[g];
+        }
+        *reinterpret_cast<float4 *>(os + (warp * GQ + g) * D + 4 * lane) = make_float4(o[g][0], o[g][1], o[g][2], o[g][3]);
+    }
+    ka_merge_finish<GQ>(p, scratch, b, h, p.nsplit, nparts);
+}
+
 // The NV fp16 scales (or zeros) of one token, packed: halves 0, 1 in .x and
 // 2, 3 in .y.
 template <int NV>
@@ -237,6 +320,10 @@ __global__ void __launch_bounds__(KA_WARPS * 32, GQ <= 4 ? 2 : 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int bh = blockIdx.y, split = blockIdx.x;
+    if (split == p.nsplit) {  // the residual window's CTA (grid.x = nsplit + 1 when R > 0)
+        ka_window<GQ>(p, bh, qf, stages);
+        return;
+    }
     const int b = bh / p.Hkv, h = bh - b * p.Hkv;
     int len = p.lens ? __ldg(p.lens + b) : p.S_cap;
     len = len < 0 ? 0 : (len > p.S_cap ? p.S_cap : len);
@@ -590,78 +677,6 @@ __global__ void __launch_bounds__(KA_WARPS * 32, GQ <= 4 ? 2 : 1)
     ka_merge_finish<GQ>(p, stages, b, h, split, nparts);
 }
 
-// The fp16 residual window of one (sequence, kv head): warp w takes tokens
-// w, w + 8, ...; lanes own 4 channels for the dot product (warp sum) and 4
-// coordinates for the values.  Writes part nsplit.
-template <int GQ>
-__global__ void __launch_bounds__(KA_WARPS * 32) kivi_attend_residual_kernel(const __grid_constant__ KiviAttendParams p)
-{
-    __shared__ float qf[GQ * D];
-    __shared__ __align__(16) unsigned char scratch[KA_WARPS * GQ * (D + 2) * 4];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int bh = blockIdx.x;
-    const int b = bh / p.Hkv, h = bh - b * p.Hkv;
-    int rl = p.res_lens ? __ldg(p.res_lens + b) : p.R;
-    rl = rl < 0 ? 0 : (rl > p.R ? p.R : rl);
-    const int nparts = p.nsplit + 1;
-    if (rl == 0) return;  // the combine skips an empty window
-    (void)ka_load_query<GQ, D>(p, b, h, qf, false);
-    __syncthreads();
-    float qv[GQ][4];
-#pragma unroll
-    for (int g = 0; g < GQ; ++g)
-#pragma unroll
-        for (int c = 0; c < 4; ++c) qv[g][c] = qf[g * D + 4 * lane + c];
-    float m[GQ], l[GQ], o[GQ][4];
-#pragma unroll
-    for (int g = 0; g < GQ; ++g) {
-        m[g] = NEG_INF;
-        l[g] = 0.0f;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) o[g][c] = 0.0f;
-    }
-    const __half *kr = static_cast<const __half *>(p.kr) + (size_t)bh * p.R * D;
-    const __half *vr = static_cast<const __half *>(p.vr) + (size_t)bh * p.R * D;
-    for (int r = warp; r < rl; r += KA_WARPS) {
-        const uint2 ku = __ldg(reinterpret_cast<const uint2 *>(kr + (size_t)r * D) + lane);
-        const uint2 vu = __ldg(reinterpret_cast<const uint2 *>(vr + (size_t)r * D) + lane);
-        const float2 k01 = __half22float2(*reinterpret_cast<const __half2 *>(&ku.x));
-        const float2 k23 = __half22float2(*reinterpret_cast<const __half2 *>(&ku.y));
-        const float2 v01 = __half22float2(*reinterpret_cast<const __half2 *>(&vu.x));
-        const float2 v23 = __half22float2(*reinterpret_cast<const __half2 *>(&vu.y));
-        const float kk[4] = {k01.x, k01.y, k23.x, k23.y};
-        const float vv[4] = {v01.x, v01.y, v23.x, v23.y};
-#pragma unroll
-        for (int g = 0; g < GQ; ++g) {
-            float s = 0.0f;
-#pragma unroll
-            for (int c = 0; c < 4; ++c) s = fmaf(qv[g][c], kk[c], s);
-#pragma unroll
-            for (int off = 16; off >= 1; off >>= 1) s += __shfl_xor_sync(FULL_MASK, s, off);
-            const float mn = fmaxf(m[g], s);
-            const float f = exp2f(m[g] - mn);
-            const float w = exp2f(s - mn);
-            l[g] = l[g] * f + w;
-#pragma unroll
-            for (int c = 0; c < 4; ++c) o[g][c] = fmaf(w, vv[c], o[g][c] * f);
-            m[g] = mn;
-        }
-    }
-    // l is already the warp's total (every lane holds the same sums)
-    float *ms = reinterpret_cast<float *>(scratch);
-    float *ls = ms + KA_WARPS * GQ;
-    float *os = ls + KA_WARPS * GQ;
-#pragma unroll
-    for (int g = 0; g < GQ; ++g) {
-        if (lane == 0) {
-            ms[warp * GQ + g] = m[g];
-            ls[warp * GQ + g] = l[g];
-        }
-        *reinterpret_cast<float4 *>(os + (warp * GQ + g) * D + 4 * lane) = make_float4(o[g][0], o[g][1], o[g][2], o[g][3]);
-    }
-    ka_merge_finish<GQ>(p, scratch, b, h, p.nsplit, nparts);
-}
-
 // Combine the parts of one (sequence, query head): the quantized chunks that
 // hold tokens and the residual window when it holds any.
 __global__ void __launch_bounds__(D) kivi_attend_combine_kernel(const __grid_constant__ KiviAttendParams p)
@@ -702,15 +717,10 @@ cudaError_t launch_ka(const KiviAttendParams &p, cudaStream_t stream)
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     const int nparts = p.nsplit + (p.R > 0 ? 1 : 0);
-    dim3 grid(p.nsplit, p.B * p.Hkv);
+    dim3 grid(nparts, p.B * p.Hkv);  // the window's part is one more CTA per (sequence, kv head)
     kern<<<grid, KA_WARPS * 32, smem, stream>>>(p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    if (p.R > 0) {
-        kivi_attend_residual_kernel<GQ><<<p.B * p.Hkv, KA_WARPS * 32, 0, stream>>>(p);
-        e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
-    }
     if (nparts == 1) return cudaSuccess;
     kivi_attend_combine_kernel<<<p.B * p.Hq, D, 0, stream>>>(p);
     return cudaGetLastError();
