@@ -13,21 +13,21 @@
 // a fixed number of keys; one CTA of 8 warps takes one chunk, so the grid is
 // balanced whatever the mix of cache lengths.  The GQ = Hq / Hkv query heads
 // of a kv head are served together, so each key and value row is read once.
-// Each warp streams its own tiles of 32 keys: TMA lands the tile's value rows
+// Each warp streams its own 16-key tiles: TMA lands the tile's value rows
 // (two 64-coordinate boxes, 128-byte swizzled) and the bulk-copy engine both
 // code streams in one of two shared-memory stages per warp while the warp
-// works on the other.  Per tile:
-//   scores   one key per lane: the lane decodes its key's 128 coordinates
-//            through a shuffle table (c1 + c2 merged for b <= 2) and forms
-//            the GQ dot products with the rotated query, which every lane
-//            reads from shared memory as a broadcast (paired-FMA arithmetic);
-//   softmax  the tile maximum per head is one warp redux; running maximum,
-//            rescale and the per-lane partial sums follow the online softmax;
-//   values   a dense product on the tensor cores: O[coord][(head, hi/lo)] +=
-//            sum_k V[k][coord] w[k][(head, hi/lo)] in 16 x 8 x 16 tiles, the
-//            fp16 values read transposed from the swizzled boxes (ldmatrix),
-//            each weight carried as two fp16 columns (its leading 11 bits and
-//            the rounded rest) and accumulated in fp32.
+// works on the other.  Both sums of a tile are dense products on the tensor
+// cores (16 x 8 x 16 mma.sync, fp16 operands, fp32 accumulation):
+//   scores   S[key][(head, hi/lo)] = sum_c y[key][c] Q[c][(head, hi/lo)]: y is
+//            the decoded rotated key, one shuffle of a (hi, lo) fp16 pair per
+//            coordinate from the merged c1 + c2 table (two tables at b = 4),
+//            Q the rotated query carried as two fp16 columns per head (built
+//            once per CTA); both scaled by powers of two into fp16 range;
+//   softmax  one head per lane (its two keys), tile maximum by three shuffles;
+//   values   O[coord][(head, hi/lo)] += sum_k V[k][coord] w[k][(head, hi/lo)],
+//            the fp16 values read transposed from the swizzled boxes
+//            (ldmatrix), each weight carried as two fp16 columns.
+// Every float factor keeps about 21 bits through its hi/lo split.
 // Warps, then CTAs (the chunks, through the caller's workspace and a combine
 // kernel), are merged at the end.  Softmax arithmetic is in base 2 (the query
 // carries scale * log2(e)).
@@ -73,17 +73,10 @@ constexpr int at_smem()
     return 1024                                         // alignment slack (128-byte swizzle)
            + AT_WARPS * AT_STAGES * AtTile<BITS>::STAGE // stages (multiples of 1024 bytes)
            + (D * GQ + QPAD) * 4                        // rotated query [c][g]
+           + ((2 * GQ + 7) / 8) * 8 * 32 * 8            // its B fragments [nt][kt][lane] (uint2)
            + AT_WARPS * GQ * WS * 4                     // weights [warp][g][key]
            + AT_WARPS * AT_STAGES * 8;                  // mbarriers
 }
-
-// Order-preserving map of floats (including -inf) to ints, for a warp redux.
-__device__ __forceinline__ int ord_of(float x)
-{
-    const int i = __float_as_int(x);
-    return i >= 0 ? i : i ^ 0x7fffffff;
-}
-__device__ __forceinline__ float float_of_ord(int i) { return __int_as_float(i >= 0 ? i : i ^ 0x7fffffff); }
 
 __device__ __forceinline__ float2 f2(float a, float b) { return make_float2(a, b); }
 __device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
@@ -98,6 +91,13 @@ __device__ __forceinline__ uint32_t split_pack(float2 u, uint32_t mh, uint32_t m
     const float2 a = f2(__uint_as_float(ux & mh), __uint_as_float(uy & mh));
     const float2 c = f2(__uint_as_float((ux & ml) ^ 0x80000000u), __uint_as_float((uy & ml) ^ 0x80000000u));
     return h2_bits(__float22half2_rn(__fadd2_rn(a, c)));
+}
+
+// (fp16(x), fp16(x - fp16(x))) in the low and high halves: x to about 22 bits.
+__device__ __forceinline__ __half2 hilo(float x)
+{
+    const __half hi = __float2half_rn(x);
+    return __halves2half2(hi, __float2half_rn(x - __half2float(hi)));
 }
 
 // Four 8 x 8 fp16 matrices from shared memory, transposed (lane i supplies the
@@ -119,81 +119,6 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// acc[g] += q[c][g] * y for the GQ heads: the rotated query row of coordinate
-// c is GQ consecutive floats in shared memory.
-template <int GQ>
-__device__ __forceinline__ void score_coord(const float *qs, int c, float y, float2 (&acc)[GQ > 1 ? GQ / 2 : 1])
-{
-    if constexpr (GQ == 2) {
-        const float2 q = *reinterpret_cast<const float2 *>(qs + c * 2);
-        acc[0] = __ffma2_rn(q, f2(y, y), acc[0]);
-    } else if constexpr (GQ >= 4) {
-#pragma unroll
-        for (int h = 0; h < GQ / 4; ++h) {
-            const float4 q = *reinterpret_cast<const float4 *>(qs + c * GQ + 4 * h);
-            acc[2 * h] = __ffma2_rn(f2(q.x, q.y), f2(y, y), acc[2 * h]);
-            acc[2 * h + 1] = __ffma2_rn(f2(q.z, q.w), f2(y, y), acc[2 * h + 1]);
-        }
-    }
-}
-
-// Dot products of the rotated query with the key whose codes are w1, w2.
-// ae/ao take even and odd coordinates (two independent chains).
-template <int BITS, int GQ, int W>
-__device__ __forceinline__ void key_scores(const float *qs, const uint32_t (&w1)[W], const uint32_t (&w2)[W],
-                                           float tab, float tc1, float tc2, float (&s)[GQ])
-{
-    constexpr int E = 32 / BITS;
-    constexpr int NA = GQ > 1 ? GQ / 2 : 1;
-    float2 ae[NA], ao[NA];
-#pragma unroll
-    for (int h = 0; h < NA; ++h) ae[h] = ao[h] = f2(0.0f, 0.0f);
-#pragma unroll
-    for (int wi = 0; wi < W; ++wi) {
-        const uint32_t a = w1[wi], b = w2[wi];
-        float y[E];
-        if constexpr (BITS == 4) {
-#pragma unroll
-            for (int c = 0; c < E; ++c)
-                y[c] = __shfl_sync(FULL_MASK, tc1, (int)(a >> (4 * c))) +
-                       __shfl_sync(FULL_MASK, tc2, (int)(b >> (4 * c)));
-        } else {
-            // merged index i1 | i2 << BITS: even coordinates from me, odd from mo
-            constexpr uint32_t CM = BITS == 2 ? 0x33333333u : 0x55555555u;
-            const uint32_t me = (a & CM) | ((b << BITS) & ~CM);
-            const uint32_t mo = ((a >> BITS) & CM) | (b & ~CM);
-#pragma unroll
-            for (int j = 0; j < E / 2; ++j) {
-                y[2 * j] = __shfl_sync(FULL_MASK, tab, (int)(me >> (2 * BITS * j)));
-                y[2 * j + 1] = __shfl_sync(FULL_MASK, tab, (int)(mo >> (2 * BITS * j)));
-            }
-        }
-        if constexpr (GQ == 1) {
-#pragma unroll
-            for (int c = 0; c < E; c += 4) {
-                const float4 q = *reinterpret_cast<const float4 *>(qs + wi * E + c);
-                ae[0] = __ffma2_rn(f2(q.x, q.y), f2(y[c], y[c + 1]), ae[0]);
-                ao[0] = __ffma2_rn(f2(q.z, q.w), f2(y[c + 2], y[c + 3]), ao[0]);
-            }
-        } else {
-#pragma unroll
-            for (int c = 0; c < E; c += 2) {
-                score_coord<GQ>(qs, wi * E + c, y[c], ae);
-                score_coord<GQ>(qs, wi * E + c + 1, y[c + 1], ao);
-            }
-        }
-    }
-    if constexpr (GQ == 1) {
-        s[0] = (ae[0].x + ae[0].y) + (ao[0].x + ao[0].y);
-    } else {
-#pragma unroll
-        for (int h = 0; h < NA; ++h) {
-            s[2 * h] = ae[h].x + ao[h].x;
-            s[2 * h + 1] = ae[h].y + ao[h].y;
-        }
-    }
-}
-
 template <int BITS, int GQ>
 __global__ void __launch_bounds__(AT_WARPS * 32, 2) rvq_attend_kernel(const __grid_constant__ RvqAttendParams p)
 {
@@ -204,7 +129,8 @@ __global__ void __launch_bounds__(AT_WARPS * 32, 2) rvq_attend_kernel(const __gr
     extern __shared__ __align__(128) unsigned char smem_raw[];
     unsigned char *stages = smem_1k(smem_raw);
     float *qs = reinterpret_cast<float *>(stages + AT_WARPS * AT_STAGES * T::STAGE);
-    float *wb = qs + D * GQ + QPAD;
+    uint2 *bqs = reinterpret_cast<uint2 *>(qs + D * GQ + QPAD);  // [nt][kt][lane]
+    float *wb = reinterpret_cast<float *>(bqs + NT * 8 * 32);
     uint64_t *bars = reinterpret_cast<uint64_t *>(wb + AT_WARPS * GQ * WS);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -270,14 +196,66 @@ __global__ void __launch_bounds__(AT_WARPS * 32, 2) rvq_attend_kernel(const __gr
                 a[j] = upper ? (o - a[j]) : (a[j] + o);
             }
         }
+        float amax = 0.0f;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) qs[(4 * lane + j) * GQ + (lane >= 16 ? QPAD : 0) + warp] = a[j] * p.qscale;
+        for (int j = 0; j < 4; ++j) {
+            a[j] *= p.qscale;
+            qs[(4 * lane + j) * GQ + (lane >= 16 ? QPAD : 0) + warp] = a[j];
+            amax = fmaxf(amax, fabsf(a[j]));
+        }
+        amax = __uint_as_float(__reduce_max_sync(FULL_MASK, __float_as_uint(amax)));
+        if (lane == 0) wb[warp] = amax;  // the weights area is free until the tile loop
     }
     __syncthreads();
 
-    const float tab = BITS == 4 ? 0.0f : p.c1[lane & (L - 1)] + p.c2[(lane >> BITS) & (L - 1)];
-    const float tc1 = p.c1[lane & (L - 1)];
-    const float tc2 = p.c2[lane & (L - 1)];
+    // Scores on the tensor cores: S[key][(head, hi/lo)] = sum_c y[key][c]
+    // Q[c][(head, hi/lo)], y the decoded rotated key (table value, fp16 hi +
+    // lo), Q the rotated query scaled by 2^eq (fp16 hi + lo columns).  Both
+    // scales are powers of two that bring the largest |entry| below 2^15.
+    int eq = 0, et = 0;
+    {
+        float qm = 0.0f;
+        for (int g = 0; g < GQ; ++g) qm = fmaxf(qm, wb[g]);
+        if (qm > 0.0f && qm < 1.0e30f) eq = 14 - ((int)((__float_as_uint(qm) >> 23) & 0xffu) - 127);
+        eq = max(-100, min(eq, 100));
+    }
+    // lane holds table entry lane mod 2^(2b) (merged c1 + c2, b <= 2) or the
+    // two stage tables' entries lane mod 16 (b = 4), scaled by 2^et
+    const float ty1 = BITS == 4 ? p.c1[lane & (L - 1)] : p.c1[lane & (L - 1)] + p.c2[(lane >> BITS) & (L - 1)];
+    const float ty2 = BITS == 4 ? p.c2[lane & (L - 1)] : 0.0f;
+    {
+        const float tm = __uint_as_float(__reduce_max_sync(FULL_MASK, __float_as_uint(fmaxf(fabsf(ty1), fabsf(ty2)))));
+        if (tm > 0.0f && tm < 1.0e30f) et = 14 - ((int)((__float_as_uint(tm) >> 23) & 0xffu) - 127);
+        et = max(-100, min(et, 100));
+    }
+    const float tsc = ldexpf(1.0f, et);
+    const uint32_t th1 = h2_bits(hilo(ty1 * tsc)), th2 = h2_bits(hilo(ty2 * tsc));
+    const float sunscale = ldexpf(1.0f, -(et + eq));  // exact: undoes both scales
+
+    // B fragments of the query (built once per CTA, read per k-tile): lane
+    // (g8, t4) of n-tile nt holds column g8 = (head 4 nt + g8 / 2, hi / lo)
+    // at coordinates 16 kt + 4 t4 + {0, 1} and + {2, 3}
+    {
+        const int g8 = lane >> 2, t4 = lane & 3;
+        const bool lo = (g8 & 1) != 0;
+        const uint32_t mh = lo ? 0xFFFFFFFFu : 0xFFFFE000u, ml = lo ? 0xFFFFE000u : 0u;
+        const float qsc = ldexpf(1.0f, eq);
+        for (int i = warp; i < NT * 8; i += AT_WARPS) {
+            const int nt = i >> 3, kt = i & 7;
+            const int hb = 4 * nt + (g8 >> 1);
+            float u[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            if (hb < GQ) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int c = 16 * kt + 4 * t4 + j;
+                    u[j] = qs[c * GQ + (c >= 64 ? QPAD : 0) + hb] * qsc;
+                }
+            }
+            bqs[i * 32 + lane] = make_uint2(split_pack(f2(u[0], u[1]), mh, ml), split_pack(f2(u[2], u[3]), mh, ml));
+        }
+    }
+    __syncthreads();  // the query maxima in wb are read; the weights may overwrite them
+
     float *my_w = wb + warp * GQ * WS;  // weights [g][key]
 
     // Values on the tensor cores: O[coord][(head, part)] += sum_k V[k][coord]
@@ -288,13 +266,12 @@ __global__ void __launch_bounds__(AT_WARPS * 32, 2) rvq_attend_kernel(const __gr
     const int g8 = lane >> 2, t4 = lane & 3;
     const bool lo = (g8 & 1) != 0;
     const uint32_t mh = lo ? 0xFFFFFFFFu : 0xFFFFE000u, ml = lo ? 0xFFFFE000u : 0u;
-    const int key = lane & 15, hf = lane >> 4;  // scoring: key of the tile and its coordinate half
-    float m[GQ], l[GQ];
+    float m[NT], l[NT];  // running max (with the SIG offset) and sum of head 4 nt + t4
     float acc[NT][8][4];
 #pragma unroll
-    for (int g = 0; g < GQ; ++g) {
-        m[g] = NEG_INF;
-        l[g] = 0.0f;
+    for (int nt = 0; nt < NT; ++nt) {
+        m[nt] = NEG_INF;
+        l[nt] = 0.0f;
     }
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
@@ -309,8 +286,9 @@ __global__ void __launch_bounds__(AT_WARPS * 32, 2) rvq_attend_kernel(const __gr
         const int st = it % AT_STAGES;
         const int k0 = s0 + t * TILE;
         const int n = min(TILE, s1 - k0);
-        const bool valid = key < n;
-        const float nrm = valid ? __ldg(p.norms + kbase + k0 + key) : 0.0f;
+        const bool va = g8 < n, vb = g8 + 8 < n;  // this lane's two keys (rows g8, g8 + 8)
+        const float na = va ? __ldg(p.norms + kbase + k0 + g8) : 0.0f;
+        const float nb = vb ? __ldg(p.norms + kbase + k0 + g8 + 8) : 0.0f;
         const bool ok = mbar_wait_bounded(&my_bar[st], (uint32_t)(it / AT_STAGES) & 1u);
         if (!__all_sync(FULL_MASK, ok)) {
             if (lane == 0) atomicOr(&g_at_err, (unsigned)VQ_DEVERR_WAIT_TIMEOUT);
@@ -323,60 +301,95 @@ __global__ void __launch_bounds__(AT_WARPS * 32, 2) rvq_attend_kernel(const __gr
         }
         const unsigned char *sb = my_st + st * T::STAGE;
 
-        // scores: lanes key and key + 16 take coordinates 0..63 and 64..127
-        // of one key (the words W/2 hf .. of both streams), then add up
-        constexpr int HW = W / 2;
-        uint32_t w1[HW], w2[HW];
-        {
-            const uint32_t *c1p = reinterpret_cast<const uint32_t *>(sb + T::VAL) + key * W + hf * HW;
-            const uint32_t *c2p = reinterpret_cast<const uint32_t *>(sb + T::VAL + T::COD) + key * W + hf * HW;
-            if constexpr (HW == 2) {
-                const uint2 x = *reinterpret_cast<const uint2 *>(c1p), y = *reinterpret_cast<const uint2 *>(c2p);
-                w1[0] = x.x; w1[1] = x.y; w2[0] = y.x; w2[1] = y.y;
-            } else {
+        // scores: rows are the tile's keys g8, g8 + 8; the lane's k entries
+        // 2 t4, 2 t4 + 1, 2 t4 + 8, 2 t4 + 9 are coordinates 16 kt + 4 t4 + 0..3
+        float accs[NT][4];
 #pragma unroll
-                for (int i = 0; i < HW / 4; ++i) {
-                    const uint4 x = reinterpret_cast<const uint4 *>(c1p)[i], y = reinterpret_cast<const uint4 *>(c2p)[i];
-                    w1[4 * i] = x.x; w1[4 * i + 1] = x.y; w1[4 * i + 2] = x.z; w1[4 * i + 3] = x.w;
-                    w2[4 * i] = y.x; w2[4 * i + 1] = y.y; w2[4 * i + 2] = y.z; w2[4 * i + 3] = y.w;
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) accs[nt][j] = 0.0f;
+        {
+            const uint32_t *c1a = reinterpret_cast<const uint32_t *>(sb + T::VAL) + g8 * W;
+            const uint32_t *c2a = reinterpret_cast<const uint32_t *>(sb + T::VAL + T::COD) + g8 * W;
+            const uint32_t *c1b = c1a + 8 * W, *c2b = c2a + 8 * W;
+#pragma unroll
+            for (int kt = 0; kt < 8; ++kt) {
+                uint32_t ah[4], al[4];  // A fragments (hi and lo parts of y)
+                uint32_t ah2[4], al2[4];  // b = 4: the stage-2 table's parts
+                auto rows = [&](const uint32_t *p1w, const uint32_t *p2w, int r) {
+                    // r = 0: row g8 (registers 0, 2); r = 1: row g8 + 8 (registers 1, 3)
+                    if constexpr (BITS == 4) {
+                        const uint32_t x1 = p1w[2 * kt + (t4 >> 1)], x2 = p2w[2 * kt + (t4 >> 1)];
+                        const int sh = 16 * (t4 & 1);
+                        uint32_t v1[4], v2[4];
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            v1[j] = __shfl_sync(FULL_MASK, th1, (int)(x1 >> (sh + 4 * j)));
+                            v2[j] = __shfl_sync(FULL_MASK, th2, (int)(x2 >> (sh + 4 * j)));
+                        }
+                        ah[r] = __byte_perm(v1[0], v1[1], 0x5410); al[r] = __byte_perm(v1[0], v1[1], 0x7632);
+                        ah[r + 2] = __byte_perm(v1[2], v1[3], 0x5410); al[r + 2] = __byte_perm(v1[2], v1[3], 0x7632);
+                        ah2[r] = __byte_perm(v2[0], v2[1], 0x5410); al2[r] = __byte_perm(v2[0], v2[1], 0x7632);
+                        ah2[r + 2] = __byte_perm(v2[2], v2[3], 0x5410); al2[r + 2] = __byte_perm(v2[2], v2[3], 0x7632);
+                    } else {
+                        // merged index i1 | i2 << BITS: even coordinates from me, odd from mo
+                        constexpr uint32_t CM = BITS == 2 ? 0x33333333u : 0x55555555u;
+                        constexpr int E = 32 / BITS;
+                        const int wi = (16 * kt) / E;
+                        const int base = (16 * kt) % E + 4 * t4;
+                        const uint32_t x1 = p1w[wi], x2 = p2w[wi];
+                        const uint32_t me = (x1 & CM) | ((x2 << BITS) & ~CM);
+                        const uint32_t mo = ((x1 >> BITS) & CM) | (x2 & ~CM);
+                        const uint32_t v0 = __shfl_sync(FULL_MASK, th1, (int)(me >> (base * BITS)));
+                        const uint32_t v1 = __shfl_sync(FULL_MASK, th1, (int)(mo >> (base * BITS)));
+                        const uint32_t v2 = __shfl_sync(FULL_MASK, th1, (int)(me >> ((base + 2) * BITS)));
+                        const uint32_t v3 = __shfl_sync(FULL_MASK, th1, (int)(mo >> ((base + 2) * BITS)));
+                        ah[r] = __byte_perm(v0, v1, 0x5410); al[r] = __byte_perm(v0, v1, 0x7632);
+                        ah[r + 2] = __byte_perm(v2, v3, 0x5410); al[r + 2] = __byte_perm(v2, v3, 0x7632);
+                    }
+                };
+                rows(c1a, c2a, 0);
+                rows(c1b, c2b, 1);
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    const uint2 bq = bqs[(nt * 8 + kt) * 32 + lane];
+                    mma_16816(accs[nt], ah[0], ah[1], ah[2], ah[3], bq.x, bq.y);
+                    mma_16816(accs[nt], al[0], al[1], al[2], al[3], bq.x, bq.y);
+                    if constexpr (BITS == 4) {
+                        mma_16816(accs[nt], ah2[0], ah2[1], ah2[2], ah2[3], bq.x, bq.y);
+                        mma_16816(accs[nt], al2[0], al2[1], al2[2], al2[3], bq.x, bq.y);
+                    }
                 }
             }
         }
-        float s[GQ];
-        key_scores<BITS, GQ, HW>(qs + hf * (64 * GQ + QPAD), w1, w2, tab, tc1, tc2, s);
-#pragma unroll
-        for (int g = 0; g < GQ; ++g) s[g] += __shfl_xor_sync(FULL_MASK, s[g], 16);
 
-        // online softmax over the tile; the running maximum carries an offset
-        // of SIG so the weights reach up to 2^SIG (it cancels in the merge)
-        float fr[GQ];
-        bool resc = false;
+        // online softmax: this lane holds keys g8, g8 + 8 of head 4 nt + t4;
+        // the running maximum carries an offset of SIG so the weights reach
+        // up to 2^SIG (it cancels in the merge)
 #pragma unroll
-        for (int g = 0; g < GQ; ++g) {
-            const float sc = valid ? s[g] * nrm : NEG_INF;
-            const float cand = float_of_ord(__reduce_max_sync(FULL_MASK, ord_of(sc))) - SIG;
-            fr[g] = 1.0f;
-            if (cand > m[g]) {  // warp-uniform
-                fr[g] = exp2f(m[g] - cand);
-                l[g] *= fr[g];
-                m[g] = cand;
-                resc = true;
-            }
-            const float w = exp2f(sc - m[g]);
-            l[g] += w;  // both lanes of a key: the warp total is halved at the end
-            if (hf == 0) my_w[g * WS + key] = w;
-        }
-        if (resc) {
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-                float f = fr[4 * nt < GQ ? 4 * nt : 0];
-#pragma unroll
-                for (int j = 1; j < 4; ++j)
-                    if (4 * nt + j < GQ && t4 == j) f = fr[4 * nt + j];
+        for (int nt = 0; nt < NT; ++nt) {
+            const float sa = va ? (accs[nt][0] + accs[nt][1]) * sunscale * na : NEG_INF;
+            const float sbb = vb ? (accs[nt][2] + accs[nt][3]) * sunscale * nb : NEG_INF;
+            float mx = fmaxf(sa, sbb);
+            mx = fmaxf(mx, __shfl_xor_sync(FULL_MASK, mx, 4));
+            mx = fmaxf(mx, __shfl_xor_sync(FULL_MASK, mx, 8));
+            mx = fmaxf(mx, __shfl_xor_sync(FULL_MASK, mx, 16));
+            const float cand = mx - SIG;
+            if (cand > m[nt]) {  // uniform over the 8 lanes of the head
+                const float f = exp2f(m[nt] - cand);
+                l[nt] *= f;
 #pragma unroll
                 for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
                     for (int j = 0; j < 4; ++j) acc[nt][mt][j] *= f;
+                m[nt] = cand;
+            }
+            const float wa = exp2f(sa - m[nt]), wbb = exp2f(sbb - m[nt]);
+            l[nt] += wa + wbb;
+            const int hh = 4 * nt + t4;
+            if (GQ % 4 == 0 || hh < GQ) {
+                my_w[hh * WS + g8] = wa;
+                my_w[hh * WS + g8 + 8] = wbb;
             }
         }
         __syncwarp();
@@ -429,26 +442,21 @@ __global__ void __launch_bounds__(AT_WARPS * 32, 2) rvq_attend_kernel(const __gr
     // per-warp sums, then merge the warps through shared memory (the stages
     // are free: every copy this CTA issued has been waited for)
 #pragma unroll
-    for (int g = 0; g < GQ; ++g) {
+    for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-        for (int off = 16; off >= 1; off >>= 1) l[g] += __shfl_xor_sync(FULL_MASK, l[g], off);
-        l[g] *= 0.5f;
-    }
+        for (int off = 4; off <= 16; off <<= 1) l[nt] += __shfl_xor_sync(FULL_MASK, l[nt], off);
     __syncthreads();
     float *ms = reinterpret_cast<float *>(stages);
     float *ls = ms + AT_WARPS * GQ;
     float *os = ls + AT_WARPS * GQ;  // [warp][g][D]
 #pragma unroll
-    for (int g = 0; g < GQ; ++g) {
-        if (lane == 0) {
-            ms[warp * GQ + g] = m[g];
-            ls[warp * GQ + g] = l[g];
-        }
-    }
-#pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
         const int hh = 4 * nt + t4;
         if (GQ % 4 == 0 || hh < GQ) {
+            if (g8 == 0) {
+                ms[warp * GQ + hh] = m[nt];
+                ls[warp * GQ + hh] = l[nt];
+            }
             float *o = os + (warp * GQ + hh) * D;
 #pragma unroll
             for (int mt = 0; mt < 8; ++mt) {
