@@ -91,7 +91,17 @@ __device__ __forceinline__ float ka_load_query(const KiviAttendParams &p, int b,
     if (bounded) {
         const int lane = threadIdx.x & 31;
         float mx = 0.0f;
-        for (int i = lane; i < GQ * D; i += 32) mx = fmaxf(mx, fabsf(__half2float(q[i])));
+        // GQ * D / 8 16-byte pieces (the rows start 256-byte aligned): at most two per lane
+#pragma unroll
+        for (int i = lane; i < GQ * D / 8; i += 32) {
+            const uint4 u = reinterpret_cast<const uint4 *>(q)[i];
+            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&w[j]));
+                mx = fmaxf(mx, fmaxf(fabsf(f.x), fabsf(f.y)));
+            }
+        }
         mx = __uint_as_float(__reduce_max_sync(FULL_MASK, __float_as_uint(mx))) * fabsf(qs);
         if (mx >= 1.0e-30f && mx <= 1.0e30f) {
             const int ex = (int)((__float_as_uint(mx) >> 23) & 0xffu) - 126;  // 2^(ex-1) <= mx < 2^ex
