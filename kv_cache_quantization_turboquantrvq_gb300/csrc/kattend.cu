@@ -87,31 +87,55 @@ __device__ __forceinline__ float ka_load_query(const KiviAttendParams &p, int b,
 {
     const __half *q = static_cast<const __half *>(p.q) + ((size_t)b * p.Hq + (size_t)h * GQ) * D;
     const float qs = p.qscale;
-    float pe = 1.0f, ps = 1.0f;
-    if (bounded) {
-        const int lane = threadIdx.x & 31;
-        float mx = 0.0f;
-        // GQ * D / 8 16-byte pieces (the rows start 256-byte aligned): at most two per lane
+    if (!bounded) {
+        for (int i = threadIdx.x; i < GQ * D; i += blockDim.x) {
+            const int g = i / D, d = i - g * D;
+            qf[g * STRIDE + d] = __half2float(q[i]) * qs;
+        }
+        return 1.0f;
+    }
+    // every warp loads the GQ rows once (GQ * D / 8 16-byte pieces; the rows
+    // start 256-byte aligned), takes the maximum and writes the scaled rows
+    // (the warps write the same values)
+    constexpr int NP = GQ * D / 8;
+    constexpr int PPL = (NP + 31) / 32;
+    const int lane = threadIdx.x & 31;
+    uint4 u[PPL];
+    float mx = 0.0f;
 #pragma unroll
-        for (int i = lane; i < GQ * D / 8; i += 32) {
-            const uint4 u = reinterpret_cast<const uint4 *>(q)[i];
-            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+    for (int k = 0; k < PPL; ++k) {
+        const int i = lane + 32 * k;
+        u[k] = i < NP ? reinterpret_cast<const uint4 *>(q)[i] : make_uint4(0u, 0u, 0u, 0u);
+        const uint32_t w[4] = {u[k].x, u[k].y, u[k].z, u[k].w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&w[j]));
+            mx = fmaxf(mx, fmaxf(fabsf(f.x), fabsf(f.y)));
+        }
+    }
+    mx = __uint_as_float(__reduce_max_sync(FULL_MASK, __float_as_uint(mx))) * fabsf(qs);
+    float pe = 1.0f, ps = 1.0f;
+    if (mx >= 1.0e-30f && mx <= 1.0e30f) {
+        const int ex = (int)((__float_as_uint(mx) >> 23) & 0xffu) - 126;  // 2^(ex-1) <= mx < 2^ex
+        pe = __uint_as_float((uint32_t)(127 + ex) << 23);
+        ps = __uint_as_float((uint32_t)(127 - ex) << 23);
+    }
+#pragma unroll
+    for (int k = 0; k < PPL; ++k) {
+        const int i = lane + 32 * k;
+        if (i < NP) {
+            const int g = (8 * i) / D, d = 8 * i - g * D;
+            const uint32_t w[4] = {u[k].x, u[k].y, u[k].z, u[k].w};
+            float v[8];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&w[j]));
-                mx = fmaxf(mx, fmaxf(fabsf(f.x), fabsf(f.y)));
+                v[2 * j] = f.x * qs * ps;
+                v[2 * j + 1] = f.y * qs * ps;
             }
+            *reinterpret_cast<float4 *>(qf + g * STRIDE + d) = make_float4(v[0], v[1], v[2], v[3]);
+            *reinterpret_cast<float4 *>(qf + g * STRIDE + d + 4) = make_float4(v[4], v[5], v[6], v[7]);
         }
-        mx = __uint_as_float(__reduce_max_sync(FULL_MASK, __float_as_uint(mx))) * fabsf(qs);
-        if (mx >= 1.0e-30f && mx <= 1.0e30f) {
-            const int ex = (int)((__float_as_uint(mx) >> 23) & 0xffu) - 126;  // 2^(ex-1) <= mx < 2^ex
-            pe = __uint_as_float((uint32_t)(127 + ex) << 23);
-            ps = __uint_as_float((uint32_t)(127 - ex) << 23);
-        }
-    }
-    for (int i = threadIdx.x; i < GQ * D; i += blockDim.x) {
-        const int g = i / D, d = i - g * D;
-        qf[g * STRIDE + d] = __half2float(q[i]) * qs * ps;
     }
     return pe;
 }
