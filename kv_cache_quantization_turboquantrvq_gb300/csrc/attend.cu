@@ -51,7 +51,7 @@ static __device__ __align__(256) float g_at_scratch[VQ_ATTEND_SCRATCH_BYTES / si
 constexpr int D = 128;
 constexpr int AT_WARPS = 8;
 constexpr int TK = 32;    // chunk sizes are multiples of 32 keys
-constexpr int TILE = 16;  // keys per warp tile: two lanes per key, 64 coordinates each
+constexpr int TILE = 16;  // keys per warp tile: one 16-row m-tile of the score product
 constexpr int AT_STAGES = 2;
 constexpr float NEG_INF = -__builtin_huge_valf();
 
