@@ -65,6 +65,7 @@ def _load():
     lib.oracle_kivi_quant.argtypes = [P, L, I, I, I, I, I, I, P, P, P, P, P]
     lib.oracle_kivi_dequant.argtypes = [P, P, P, L, I, I, I, I, I, P]
     lib.oracle_kivi_attend.argtypes = [P] * 11 + [I] * 8 + [D, P, P]
+    lib.oracle_qjl_encode.argtypes = [P, L, I, P, I, P, P, P, P]
     _lib = lib
     return lib
 
@@ -316,3 +317,23 @@ def kivi_attend(q, k_packed, k_scale, k_zero, v_packed, v_scale, v_zero, bits: i
                                _p(ln), _p(rl), B, Hq, Hkv, S_cap, R, D, bits, group, float(scale),
                                _p(out.view(np.uint16)), _p(f64))
     return (out, f64) if want_f64 else out
+
+
+def qjl_encode(x_f16: np.ndarray, s_f16: np.ndarray):
+    """QJL encode ([TQ] "Kernel 4: QJL Encode"): x [N, d] and the sketch S
+    [m, d], both fp16.  Returns packed [N, m/32] uint32 (bit j of word w:
+    sign(S x)[32w + j] >= 0), norms [N] fp16, tie [N, m] and norm_tie [N]
+    flags (the exact dot products and norms, see oracle.c)."""
+    x = np.ascontiguousarray(x_f16, dtype=np.float16)
+    s = np.ascontiguousarray(s_f16, dtype=np.float16)
+    N, d = x.shape
+    m, d2 = s.shape
+    assert d2 == d and m % 32 == 0
+    packed = np.zeros((N, m // 32), np.uint32)
+    norms = np.zeros(N, np.uint16)
+    tie = np.zeros((N, m), np.uint8)
+    ntie = np.zeros(N, np.uint8)
+    _load().oracle_qjl_encode(_p(x.view(np.uint16)), N, d, _p(s.view(np.uint16)), m, _p(packed), _p(norms),
+                              _p(tie), _p(ntie))
+    return {"packed": packed, "norms": norms.view(np.float16), "tie": tie.astype(bool),
+            "norm_tie": ntie.astype(bool)}

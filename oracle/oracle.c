@@ -761,3 +761,72 @@ void oracle_kivi_attend(const uint16_t *q_f16, const uint32_t *k_packed, const u
     }
     free(K); free(V); free(sc); free(acc);
 }
+
+/* ------------------------------------------------------------------------ */
+/* QJL encode.                                                               */
+/* [TQ] "Kernel 4: QJL Encode - Simdgroup Sign Packing": for each key x the  */
+/* m bits of sign(S x), a bit being 1 when the dot product with sketch row   */
+/* j is >= 0, packed least-significant bit first (bit j of byte k is sketch  */
+/* row 8k + j; on little-endian words, bit j of word w is row 32w + j), and  */
+/* the key's Euclidean norm stored as fp16.                                  */
+/* Readings: S is the caller's m x d sketch matrix in fp16 (the page reads   */
+/* it as a buffer converted to float); m is a multiple of 32.                */
+/* Every product of two fp16 values is a dyadic rational m1 m2 2^(e1+e2)     */
+/* with |m1 m2| < 2^22 and e1 + e2 >= -48, so the dot product (and the sum  */
+/* of squares) is accumulated exactly as a 128-bit integer in units of       */
+/* 2^-48: the signs are exact.  tie flags a sketch bit whose |dot| is below  */
+/* 1e-5 of sum |S_jd x_d|, norm_tie a norm within 1e-6 (relative) of an fp16 */
+/* rounding boundary: the places where an fp32 evaluation may differ.       */
+/* ------------------------------------------------------------------------ */
+
+/* x (fp16 bits) as an integer multiple of 2^-24: x = mant * 2^-24 exactly. */
+static __int128 f16_to_units24(uint16_t h)
+{
+    int sign = (h >> 15) & 1, e = (h >> 10) & 31;
+    int64_t f = h & 1023;
+    __int128 v;
+    if (e == 0) v = f;                               /* subnormal: f * 2^-24 */
+    else v = (__int128)(f | 1024) << (e - 1);        /* (1024 + f) 2^(e - 25) = ... * 2^-24 */
+    return sign ? -v : v;
+}
+
+static double units48_to_f64(__int128 v)
+{
+    /* exact conversion of the high and low 64-bit halves, then one add */
+    int neg = v < 0;
+    unsigned __int128 u = neg ? (unsigned __int128)(-v) : (unsigned __int128)v;
+    double hi = (double)(uint64_t)(u >> 64) * 18446744073709551616.0;
+    double lo = (double)(uint64_t)u;
+    double r = (hi + lo) * ldexp(1.0, -48);
+    return neg ? -r : r;
+}
+
+void oracle_qjl_encode(const uint16_t *x_f16, long N, int d, const uint16_t *s_f16, int m,
+                       uint32_t *packed, uint16_t *norms_f16, uint8_t *tie, uint8_t *norm_tie)
+{
+    int W = m / 32;
+    for (long n = 0; n < N; ++n) {
+        const uint16_t *x = x_f16 + n * d;
+        for (int w = 0; w < W; ++w) packed[n * W + w] = 0;
+        for (int j = 0; j < m; ++j) {
+            const uint16_t *s = s_f16 + (long)j * d;
+            __int128 dot = 0;
+            double mag = 0.0;
+            for (int k = 0; k < d; ++k) {
+                dot += f16_to_units24(s[k]) * f16_to_units24(x[k]);
+                mag += fabs(oracle_f16_to_f64(s[k]) * oracle_f16_to_f64(x[k]));
+            }
+            if (dot >= 0) packed[n * W + j / 32] |= 1u << (j % 32);
+            if (tie) tie[n * m + j] = fabs(units48_to_f64(dot)) < 1e-5 * mag;
+        }
+        __int128 q = 0;
+        for (int k = 0; k < d; ++k) {
+            __int128 u = f16_to_units24(x[k]);
+            q += u * u;
+        }
+        double nr = sqrt(units48_to_f64(q));
+        norms_f16[n] = oracle_f64_to_f16_rn(nr);
+        if (norm_tie)
+            norm_tie[n] = oracle_f64_to_f16_rn(nr * (1.0 + 1e-6)) != oracle_f64_to_f16_rn(nr * (1.0 - 1e-6));
+    }
+}
