@@ -299,6 +299,27 @@ vq_status vq_kivi_unpack_dequant(const uint32_t *k_packed, const void *k_scale, 
                                  void *k_out_f16, void *v_out_f16, vq_stream_t stream);
 
 /*
+ * vq_qjl_encode - QJL encode (VeloxQuant-MLX blog, tag "turboquant",
+ * "Kernel 4: QJL Encode - Simdgroup Sign Packing"): for every key row x the
+ * m bits of sign(S x) - a bit is 1 when the dot product with sketch row j is
+ * >= 0 - packed least-significant bit first (bit j of word w is sketch row
+ * 32 w + j; on this little-endian device the same bytes as the page's
+ * uint8 packing, byte k bit j = row 8 k + j), and ||x|| rounded to fp16.
+ * The dot products run on the tensor cores (fp16 products are exact, fp32
+ * accumulation): a bit can differ from the exact sign only when |S_j . x| is
+ * within about 1e-5 of sum |S_jd x_d|; a norm only when ||x|| is within about
+ * 1e-6 (relative) of an fp16 rounding boundary.
+ *   x   [N, D] fp16, device (e.g. a key cache [B, H, S, D] as N = B H S rows).
+ *   s   [m, D] fp16, device: the sketch matrix (the caller draws it).
+ *   packed [N, m / 32] uint32, norms [N] fp16, device.
+ * All pointers 16-byte aligned; outputs must not overlap inputs.
+ * D = 128, m a multiple of 32 in [32, 256] (VQ_ERR_UNSUPPORTED otherwise).
+ * Inputs must be finite.
+ */
+vq_status vq_qjl_encode(const void *x_f16, int N, int D, const void *s_f16, int m, uint32_t *packed,
+                        void *norms_f16, vq_stream_t stream);
+
+/*
  * vq_device_error - waits for `stream`, then reads and clears the library's
  * device error word (VQ_DEVERR_* bits) into *code_out (host pointer).
  * Returns VQ_ERR_DEVICE if the word was non-zero, VQ_OK otherwise.

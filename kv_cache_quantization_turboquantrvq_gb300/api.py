@@ -31,7 +31,7 @@ EXPORTED = ("vq_status_str", "vq_version", "vq_rvq_codebook", "vq_rvq_encode_pac
             "vq_rvq_unpack_dequant", "vq_kivi_quant_pack", "vq_kivi_unpack_dequant",
             "vq_device_error", "vq_rvq_attend_workspace", "vq_rvq_attend", "vq_rvq_attend_noalloc",
             "vq_rvq_encode_pack_rs", "vq_rvq_unpack_dequant_rs", "vq_rvq_attend_rs",
-            "vq_kivi_attend_workspace", "vq_kivi_attend")
+            "vq_kivi_attend_workspace", "vq_kivi_attend", "vq_qjl_encode")
 VQ_ATTEND_SCRATCH_BYTES = 16 * 1024 * 1024
 
 
@@ -70,6 +70,7 @@ def lib():
                                    ctypes.c_size_t, P]
     L.vq_kivi_attend_workspace.argtypes = [I, I, I, I, I, ctypes.POINTER(ctypes.c_size_t)]
     L.vq_kivi_attend.argtypes = [P] * 11 + [I] * 8 + [ctypes.c_float, P, P, ctypes.c_size_t, P]
+    L.vq_qjl_encode.argtypes = [P, I, I, P, I, P, P, P]
     for name in EXPORTED[2:]:
         getattr(L, name).restype = I
     _lib = L
@@ -334,3 +335,22 @@ def vq_device_error(stream=None) -> int:
     if st not in (VQ_OK, VQ_ERR_DEVICE):
         raise VQError(st, "vq_device_error")
     return code.value
+
+
+def vq_qjl_encode(x, s, packed=None, norms=None, stream=None):
+    """QJL encode of the key rows x [..., 128] fp16 with the sketch s [m, 128]
+    fp16: returns (packed [..., m/32] int32 sign words, norms [...] fp16)."""
+    import torch
+    D = x.shape[-1]
+    lead = tuple(x.shape[:-1])
+    N = 1
+    for v in lead:
+        N *= v
+    m = s.shape[0]
+    if packed is None:
+        packed = torch.empty(lead + (m // 32,), dtype=torch.int32, device=x.device)
+    if norms is None:
+        norms = torch.empty(lead, dtype=torch.float16, device=x.device)
+    _check(lib().vq_qjl_encode(_ptr(x), N, D, _ptr(s), m, _ptr(packed), _ptr(norms), _stream(stream)),
+           "vq_qjl_encode")
+    return packed, norms

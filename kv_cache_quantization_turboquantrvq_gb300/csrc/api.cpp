@@ -674,6 +674,30 @@ vq_status vq_kivi_unpack_dequant(const uint32_t *k_packed, const void *k_scale, 
     return VQ_OK;
 }
 
+vq_status vq_qjl_encode(const void *x_f16, int N, int D, const void *s_f16, int m, uint32_t *packed,
+                        void *norms_f16, vq_stream_t stream)
+{
+    if (N < 0 || D <= 0 || m <= 0) return VQ_ERR_INVALID_ARG;
+    if (D != 128 || m % 32 != 0 || m > 256) return VQ_ERR_UNSUPPORTED;
+    if (N == 0) return VQ_OK;
+    if (!x_f16 || !s_f16 || !packed || !norms_f16) return VQ_ERR_INVALID_ARG;
+    if (!aligned(x_f16, 16) || !aligned(s_f16, 16) || !aligned(packed, 16) || !aligned(norms_f16, 16))
+        return VQ_ERR_MISALIGNED;
+    const size_t xb = (size_t)N * D * 2, sb = (size_t)m * D * 2, pb = (size_t)N * (m / 32) * 4, nb = (size_t)N * 2;
+    if (overlap(packed, pb, x_f16, xb) || overlap(packed, pb, s_f16, sb) || overlap(norms_f16, nb, x_f16, xb) ||
+        overlap(norms_f16, nb, s_f16, sb) || overlap(packed, pb, norms_f16, nb))
+        return VQ_ERR_ALIASING;
+    QjlEncodeParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.x = x_f16;
+    p.s = s_f16;
+    p.packed = packed;
+    p.norms = norms_f16;
+    p.N = N;
+    p.m = m;
+    return launch_qjl_encode(p, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? VQ_OK : VQ_ERR_CUDA;
+}
+
 vq_status vq_device_error(vq_stream_t stream, int *code_out)
 {
     if (!code_out) return VQ_ERR_INVALID_ARG;
@@ -683,10 +707,11 @@ vq_status vq_device_error(vq_stream_t stream, int *code_out)
     if (kivi_take_device_error(&b, s) != cudaSuccess) return VQ_ERR_CUDA;
     if (attend_take_device_error(&c, s) != cudaSuccess) return VQ_ERR_CUDA;
     if (kivi_attend_take_device_error(&d, s) != cudaSuccess) return VQ_ERR_CUDA;
-    unsigned e = 0;
+    unsigned e = 0, f = 0;
     if (gen_take_device_error(&e, s) != cudaSuccess) return VQ_ERR_CUDA;
-    *code_out = (int)(a | b | c | d | e);
-    return (a | b | c | d | e) ? VQ_ERR_DEVICE : VQ_OK;
+    if (qjl_take_device_error(&f, s) != cudaSuccess) return VQ_ERR_CUDA;
+    *code_out = (int)(a | b | c | d | e | f);
+    return (a | b | c | d | e | f) ? VQ_ERR_DEVICE : VQ_OK;
 }
 
 }  // extern "C"

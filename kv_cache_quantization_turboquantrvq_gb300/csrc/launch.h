@@ -165,6 +165,17 @@ struct RvqGenericParams {
 };
 cudaError_t launch_rvq_generic(const RvqGenericParams &p, int bits, bool encode, cudaStream_t stream);
 cudaError_t gen_take_device_error(unsigned *bits, cudaStream_t stream);
+// QJL encode: sign(S x) bits and ||x|| of every key row.
+struct QjlEncodeParams {
+    CUtensorMap tmx;               // x as [N, 128] fp16, 64 x 16 boxes, 128-byte swizzle (set by the launcher)
+    const void *x;                 // fp16 [N, 128]
+    const void *s;                 // fp16 [m, 128] sketch
+    uint32_t *packed;              // [N, m / 32]
+    void *norms;                   // fp16 [N]
+    int N, m;
+};
+cudaError_t launch_qjl_encode(const QjlEncodeParams &p, cudaStream_t stream);
+cudaError_t qjl_take_device_error(unsigned *bits, cudaStream_t stream);
 
 // Device address and size of the library's static attention scratch on the
 // current device.

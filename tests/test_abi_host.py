@@ -142,3 +142,24 @@ def test_kivi_validation(L):
 def test_device_error_rejects_null(L):
     from kv_cache_quantization_turboquantrvq_gb300 import api
     assert L.vq_device_error(None, None) == api.VQ_ERR_INVALID_ARG
+
+
+def test_qjl_validation(L):
+    """vq_qjl_encode refuses bad shapes, pointers, alignment and overlaps on
+    the host (fake addresses: only refused cases are called)."""
+    from kv_cache_quantization_turboquantrvq_gb300 import api
+
+    def q(x=A, s=A + (1 << 26), p=A + (2 << 26), n=A + (3 << 26), N=64, D=128, m=128):
+        return L.vq_qjl_encode(P(x), N, D, P(s), m, P(p), P(n), None)
+    assert q(D=64) == api.VQ_ERR_UNSUPPORTED
+    assert q(m=48) == api.VQ_ERR_UNSUPPORTED       # not a multiple of 32
+    assert q(m=512) == api.VQ_ERR_UNSUPPORTED      # above 256
+    assert q(m=0) == api.VQ_ERR_INVALID_ARG
+    assert q(N=-1) == api.VQ_ERR_INVALID_ARG
+    assert q(x=0) == api.VQ_ERR_INVALID_ARG
+    assert q(n=0) == api.VQ_ERR_INVALID_ARG
+    assert q(x=A + 8) == api.VQ_ERR_MISALIGNED
+    assert q(n=A + (3 << 26) + 2) == api.VQ_ERR_MISALIGNED
+    assert q(p=A + 1024) == api.VQ_ERR_ALIASING    # packed over the keys
+    assert q(n=A + (2 << 26)) == api.VQ_ERR_ALIASING  # norms over packed
+    assert q(N=0, x=0, p=0, n=0) == api.VQ_OK       # nothing to do
