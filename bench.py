@@ -13,7 +13,7 @@ K and V.  Inputs are 2 GiB, larger than L2 (129 MB), so no L2 flush is needed
 between steps.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload c5|c3|c2|c1|c4|attn|kattn]
+                  [--workload c5|c3|c2|c1|c4|attn|kattn|qjl]
 
 --impl reference times the CPU oracle (single-threaded binary64 C) on a
 bounded sample of the same workload per step.
@@ -80,6 +80,12 @@ def attend_bytes(lens, Hkv, Hq, bits):
     return keys * (2 * (D * bits // 8) + 4 + 2 * D) + len(lens) * Hq * D * 2 * 2
 
 
+def qjl_bytes(rows, m):
+    """Algorithmic bytes of QJL encode: the fp16 key rows in, m sign bits and
+    an fp16 norm per row out."""
+    return rows * (2 * D + m // 8 + 2)
+
+
 def kattend_bytes(lens, res_lens, Hkv, Hq, bits, G):
     """Algorithmic bytes of one KIVI attention call: every valid quantized
     token's key and value codes, its share of the key group's scale/zero and
@@ -97,6 +103,8 @@ def describe(name):
                  "heads x 32 query heads, capacity 16384 (lengths uniform in [1k,16k]) + 128-token fp16 window",
         "attn": "decode attention over RVQ b=2 key caches (fp16 values): 64 seqs x 8 kv heads x "
                 "32 query heads, capacity 16384, lengths uniform in [1k,16k]",
+        "qjl": "QJL encode of long-context keys [4,32,32768,128] fp16 (4x40 outlier channels per head): "
+               "128 sign bits of S x (seeded N(0,1) fp16 sketch) and the fp16 norm per key",
         "c5": "long-context K,V [4,32,32768,128] fp16 (4x40 outlier channels per head): RVQ b=2 "
               "encode+pack on K; KIVI 2-bit G=64 residual 128 on K and V; unpack+dequant of all",
         "c3": "RVQ b=4 encode+pack over 32 layers of keys [1,32,8192,128] fp16 (4x20 outliers), "
@@ -221,6 +229,27 @@ def build_workload(name, dev, rank=0, layers=None, batch=None, chunked=False, ch
                 kivi_ops("", k[b:b + 1], v[b:b + 1], cfg["kivi_bits"], cfg["group"], cfg["residual"],
                          ops=c["ops"], results=c["results"], stream=chunk_stream)
                 c["ops"].sort(key=lambda o: order.index(o.name))
+    elif name == "qjl":
+        cfg = cfgs["qjl_long_32k_m128"]
+        k_np = synth.keys_for(cfg, B=batch)
+        k = t(k_np)
+        m = cfg["m"]
+        s_dev = t(np.random.default_rng(cfg["seed"]).standard_normal((m, D)).astype(np.float16))
+        inputs = [(k_np, k)]
+
+        def qjl_op(kd, ops_, results_, st):
+            Bq, H, S, _ = kd.shape
+            pk = torch.empty((Bq, H, S, m // 32), dtype=torch.int32, device=dev)
+            nr = torch.empty((Bq, H, S), dtype=torch.float16, device=dev)
+            ops_.append(Op("qjl_encode", "qjl_encode_kernel",
+                           lambda: api.vq_qjl_encode(kd, s_dev, packed=pk, norms=nr, stream=st),
+                           qjl_bytes(Bq * H * S, m), Bq * H * S * D))
+            results_.extend([pk, nr])
+        qjl_op(k, ops, results, stream)
+        if chunked:
+            for b in range(k.shape[0]):
+                c = new_chunk([(k_np[b:b + 1], k[b:b + 1])])
+                qjl_op(k[b:b + 1], c["ops"], c["results"], chunk_stream)
     elif name == "c3":
         cfg = cfgs["c3_rvq_b4_32L_8k"]
         for layer in range(cfg["layers"] if layers is None else layers):
@@ -485,6 +514,17 @@ def oracle_sample_rates(name, target_s=2.0):
         r, n, _ = timed(att, attend_bytes([1], 1, 0, bits), 256, smax)
         rates["rvq_attend"] = r
         desc.append("RVQ b=%d attention of %d query heads over one kv head of %d keys" % (bits, gq, n))
+    if name == "qjl":
+        cfg = cfgs["qjl_long_32k_m128"]
+        m = cfg["m"]
+        x = synth.kv_tensor(1, 1, 1 << 15, D, cfg["seed"], 4, 40.0).reshape(-1, D)
+        sk = np.random.default_rng(cfg["seed"]).standard_normal((m, D)).astype(np.float16)
+
+        def qe(n):
+            oracle.qjl_encode(x[:n], sk)
+        r, n, _ = timed(qe, qjl_bytes(1, m), 64, len(x))
+        rates["qjl_encode"] = r
+        desc.append("QJL encode (m=%d) of %d key rows" % (m, n))
     if name == "kattn":
         cfg = cfgs["kattn_decode_64x8x32_16k"]
         bits, G, gq, R = cfg["bits"], cfg["group"], cfg["Hq"] // cfg["Hkv"], cfg["R"]
@@ -552,7 +592,7 @@ def main():
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--workload", choices=("c5", "c3", "c2", "c1", "c4", "attn", "kattn"), default="c5")
+    ap.add_argument("--workload", choices=("c5", "c3", "c2", "c1", "c4", "attn", "kattn", "qjl"), default="c5")
     ap.add_argument("--graph", action="store_true",
                     help="also capture the step in a CUDA graph and time its replays "
                          "(launch-bound workloads: c4, c1); `value` is then the graph's")
@@ -746,7 +786,7 @@ def main():
             "data": "synthetic (seeded N(0,1) fp16 with per-head outlier channels)",
             "config": {"workload": args.workload + ": " + describe(args.workload),
                        "parallelism": "replicas (independent shards per GPU)" if world > 1 else "single GPU",
-                       "l2": "inputs larger than L2 (129 MB); no flush" if args.workload in ("c5", "c3", "c2", "attn", "kattn")
+                       "l2": "inputs larger than L2 (129 MB); no flush" if args.workload in ("c5", "c3", "c2", "attn", "kattn", "qjl")
                              else "inputs smaller than L2; rotating not applied",
                        "bytes_per_step": step_bytes, "elements_per_step": step_elems},
             "pct_of_peak": round(100 * value / world / peak, 2),
@@ -851,6 +891,10 @@ def reference_ops(name):
         lens = synth.cache_lengths(c["B"], c["seed"])
         ops.append(Op("rvq_attend", "rvq_attend", noop, attend_bytes(lens, c["Hkv"], c["Hq"], c["bits"]),
                       int(lens.sum()) * c["Hkv"] * D))
+    elif name == "qjl":
+        c = cfgs["qjl_long_32k_m128"]
+        rows = c["B"] * c["H"] * c["S"]
+        ops.append(Op("qjl_encode", "qjl_encode", noop, qjl_bytes(rows, c["m"]), rows * D))
     return ops
 
 

@@ -15,10 +15,10 @@
 // bytes so that ldmatrix reads are conflict-free); each warp streams its own
 // 16-key blocks (two 64-coordinate TMA boxes with the 128-byte swizzle,
 // double-buffered), loads the block's A fragments once (ldmatrix) and reuses
-// them for every 32-column chunk of the sketch and for one more product
-// X X^T whose diagonal holds the squared norms (the squares are exact, the
-// accumulation fp32).  The signs of a chunk's accumulators are gathered by
-// warp ballots and interleaved into one word per key.
+// them for every 32-column chunk of the sketch; the squared norms come from
+// the same registers by paired fp32 FMAs (the squares are exact).  The signs
+// of a chunk's accumulators are gathered by warp ballots and interleaved into
+// one word per key.
 #include <cuda_fp16.h>
 
 #include "device_common.cuh"
@@ -67,8 +67,12 @@ __device__ __forceinline__ uint32_t spread4(uint32_t n)
     return (n | (n << 1)) & 0x55u;
 }
 
+// W = m / 32 sign words per key; up to 4 words (16 n-tiles, 16 independent
+// accumulator chains) are accumulated together.
+template <int W>
 __global__ void __launch_bounds__(QJ_WARPS * 32) qjl_encode_kernel(const __grid_constant__ QjlEncodeParams p)
 {
+    constexpr int WG = W < 4 ? W : 4;  // words per pass
     extern __shared__ __align__(128) unsigned char smem_raw[];
     unsigned char *stages = smem_1k(smem_raw);
     unsigned char *ss = stages + QJ_WARPS * QJ_STAGES * QJ_STAGE;  // sketch rows [m][SROW]
@@ -116,7 +120,6 @@ __global__ void __launch_bounds__(QJ_WARPS * 32) qjl_encode_kernel(const __grid_
     // row (lane & 7) + 8 (lane >> 4), chunk 2 kt + ((lane >> 3) & 1)
     const int arow = (lane & 7) + 8 * ((lane >> 3) & 1), ach = lane >> 4;
     const int brow = (lane & 7) + 8 * (lane >> 4), bch = (lane >> 3) & 1;
-    const int W = p.m / 32;
 
     for (int it = 0;; ++it) {
         const int blk = gw + it * tw;
@@ -144,39 +147,46 @@ __global__ void __launch_bounds__(QJ_WARPS * 32) qjl_encode_kernel(const __grid_
         if (blk + QJ_STAGES * tw < nblk) issue(blk + QJ_STAGES * tw, st);
 
         const int row0 = blk * QJ_ROWS;
-        // squared norms: the diagonal of X X^T (the key rows of the block are
-        // also the B columns, so the A registers serve as B fragments)
+        // squared norms from the fragments in registers (the tensor pipe is
+        // the busy one): keys g8 (registers 0, 2) and g8 + 8 (1, 3), 32 exact
+        // squares each per lane in paired fp32 FMAs, then the 4 lanes of a key
         {
-            float n0[4] = {0.0f, 0.0f, 0.0f, 0.0f}, n1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            float2 qa = make_float2(0.0f, 0.0f), qb = make_float2(0.0f, 0.0f);
 #pragma unroll
             for (int kt = 0; kt < 8; ++kt) {
-                mma_16816(n0, a[kt][0], a[kt][1], a[kt][2], a[kt][3], a[kt][0], a[kt][2]);
-                mma_16816(n1, a[kt][0], a[kt][1], a[kt][2], a[kt][3], a[kt][1], a[kt][3]);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&a[kt][j]));
+                    if (j & 1) qb = __ffma2_rn(f, f, qb);
+                    else qa = __ffma2_rn(f, f, qa);
+                }
             }
-            // row g8 sits at column g8 of n-tile 0, row g8 + 8 at column g8 of
-            // n-tile 1: the lane with t4 = g8 / 2 holds both
-            if (t4 == (g8 >> 1)) {
-                const float qa = (g8 & 1) ? n0[1] : n0[0];
-                const float qb = (g8 & 1) ? n1[3] : n1[2];
+            float sa = qa.x + qa.y, sb = qb.x + qb.y;
+            sa += __shfl_xor_sync(FULL_MASK, sa, 1);
+            sb += __shfl_xor_sync(FULL_MASK, sb, 1);
+            sa += __shfl_xor_sync(FULL_MASK, sa, 2);
+            sb += __shfl_xor_sync(FULL_MASK, sb, 2);
+            if (t4 == 0) {
                 __half *nr = static_cast<__half *>(p.norms);
-                if (row0 + g8 < p.N) nr[row0 + g8] = __float2half_rn(__fsqrt_rn(qa));
-                if (row0 + g8 + 8 < p.N) nr[row0 + g8 + 8] = __float2half_rn(__fsqrt_rn(qb));
+                if (row0 + g8 < p.N) nr[row0 + g8] = __float2half_rn(__fsqrt_rn(sa));
+                if (row0 + g8 + 8 < p.N) nr[row0 + g8 + 8] = __float2half_rn(__fsqrt_rn(sb));
             }
         }
-        // signs, 32 sketch rows (4 n-tiles, one word per key) at a time
-        for (int w = 0; w < W; ++w) {
-            float acc[4][4];
+        // signs, WG words (32 sketch rows each) per pass
 #pragma unroll
-            for (int nt = 0; nt < 4; ++nt)
+        for (int w0 = 0; w0 < W; w0 += WG) {
+            float acc[4 * WG][4];
+#pragma unroll
+            for (int nt = 0; nt < 4 * WG; ++nt)
 #pragma unroll
                 for (int j = 0; j < 4; ++j) acc[nt][j] = 0.0f;
 #pragma unroll
             for (int kt = 0; kt < 8; ++kt) {
 #pragma unroll
-                for (int np = 0; np < 2; ++np) {  // a pair of n-tiles per ldmatrix
+                for (int np = 0; np < 2 * WG; ++np) {  // a pair of n-tiles per ldmatrix
                     uint32_t b0, b1, b2, b3;
-                    ldsm_x4(sbase + (uint32_t)((32 * w + 16 * np + brow) * SROW + (2 * kt + bch) * 16), b0, b1, b2,
-                            b3);
+                    ldsm_x4(sbase + (uint32_t)((32 * w0 + 16 * np + brow) * SROW + (2 * kt + bch) * 16), b0, b1,
+                            b2, b3);
                     // b0, b1: sketch rows 0..7 of the pair (k 0..7, 8..15); b2, b3: rows 8..15
                     mma_16816(acc[2 * np], a[kt][0], a[kt][1], a[kt][2], a[kt][3], b0, b1);
                     mma_16816(acc[2 * np + 1], a[kt][0], a[kt][1], a[kt][2], a[kt][3], b2, b3);
@@ -185,20 +195,24 @@ __global__ void __launch_bounds__(QJ_WARPS * 32) qjl_encode_kernel(const __grid_
             // lane 4 g8 + t4 holds keys g8 and g8 + 8 at sketch columns 2 t4,
             // 2 t4 + 1 of each n-tile; nibble r of a ballot is key r's four
             // even (or odd) columns of that n-tile
-            uint32_t word = 0;
             const int r = lane & 15;
+            const int sh = 4 * (r & 7);
 #pragma unroll
-            for (int nt = 0; nt < 4; ++nt) {
-                const uint32_t e0 = __ballot_sync(FULL_MASK, acc[nt][0] >= 0.0f);
-                const uint32_t o0 = __ballot_sync(FULL_MASK, acc[nt][1] >= 0.0f);
-                const uint32_t e1 = __ballot_sync(FULL_MASK, acc[nt][2] >= 0.0f);
-                const uint32_t o1 = __ballot_sync(FULL_MASK, acc[nt][3] >= 0.0f);
-                const uint32_t ev = r < 8 ? e0 : e1, od = r < 8 ? o0 : o1;
-                const int sh = 4 * (r & 7);
-                const uint32_t byte = spread4((ev >> sh) & 15u) | (spread4((od >> sh) & 15u) << 1);
-                word |= byte << (8 * nt);
+            for (int w = 0; w < WG; ++w) {
+                uint32_t word = 0;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int nt = 4 * w + q;
+                    const uint32_t e0 = __ballot_sync(FULL_MASK, acc[nt][0] >= 0.0f);
+                    const uint32_t o0 = __ballot_sync(FULL_MASK, acc[nt][1] >= 0.0f);
+                    const uint32_t e1 = __ballot_sync(FULL_MASK, acc[nt][2] >= 0.0f);
+                    const uint32_t o1 = __ballot_sync(FULL_MASK, acc[nt][3] >= 0.0f);
+                    const uint32_t ev = r < 8 ? e0 : e1, od = r < 8 ? o0 : o1;
+                    const uint32_t byte = spread4((ev >> sh) & 15u) | (spread4((od >> sh) & 15u) << 1);
+                    word |= byte << (8 * q);
+                }
+                if (lane < 16 && row0 + r < p.N) p.packed[(size_t)(row0 + r) * W + w0 + w] = word;
             }
-            if (lane < 16 && row0 + r < p.N) p.packed[(size_t)(row0 + r) * W + w] = word;
         }
     }
 }
@@ -216,16 +230,28 @@ cudaError_t launch_qjl_encode(const QjlEncodeParams &p0, cudaStream_t stream)
         if (!encode_tmap_f16(&p.tmx, p.x, 2, dims, strides, box, true, true)) return cudaErrorInvalidValue;
     }
     const int smem = qj_smem(p.m);
-    cudaError_t e = cudaFuncSetAttribute(qjl_encode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    void (*kern)(QjlEncodeParams) = nullptr;
+    switch (p.m / 32) {
+    case 1: kern = qjl_encode_kernel<1>; break;
+    case 2: kern = qjl_encode_kernel<2>; break;
+    case 3: kern = qjl_encode_kernel<3>; break;
+    case 4: kern = qjl_encode_kernel<4>; break;
+    case 5: kern = qjl_encode_kernel<5>; break;
+    case 6: kern = qjl_encode_kernel<6>; break;
+    case 7: kern = qjl_encode_kernel<7>; break;
+    case 8: kern = qjl_encode_kernel<8>; break;
+    default: return cudaErrorInvalidValue;
+    }
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, qjl_encode_kernel, QJ_WARPS * 32, smem);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, QJ_WARPS * 32, smem);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) per_sm = 1;
     const int nblk = (p.N + QJ_ROWS - 1) / QJ_ROWS;
     const int want = (nblk + QJ_WARPS - 1) / QJ_WARPS;
     const int grid = want < sm_count() * per_sm ? want : sm_count() * per_sm;
-    qjl_encode_kernel<<<grid, QJ_WARPS * 32, smem, stream>>>(p);
+    kern<<<grid, QJ_WARPS * 32, smem, stream>>>(p);
     return cudaGetLastError();
 }
 

@@ -96,6 +96,10 @@ CONFIGS = {
     # random fill levels in [0, 128].
     "kattn_decode_64x8x32_16k": dict(kind="kattend", B=64, Hkv=8, Hq=32, S_cap=16384, R=128, bits=2,
                                      group=32, seed=111),
+    # QJL encode of the long-context keys: m = 128 sketch rows (the 16x
+    # compression the pages quote for QJL: 128 fp16 values -> 128 bits), a
+    # seeded N(0, 1) fp16 sketch.
+    "qjl_long_32k_m128": dict(kind="qjl", B=4, H=32, S=32768, m=128, seed=112, k_outliers=(4, 40.0)),
 }
 
 
