@@ -201,9 +201,9 @@ __device__ __forceinline__ uint32_t pair_code(float v, float a, float bc, const 
 // Per-row constants of the symmetric quantizers, in units of S = H x (the
 // unnormalised transform, S = y n sqrt(D)): the positive boundaries B and E
 // of the two stages, B - c2, dc = c3 - c2 and (b = 1) c1, each scaled by
-// den = n sqrt(D).
+// den = n sqrt(D); (b = 2) k1 = 2 / B and k2 = 2 / E in the same units.
 struct SymRow {
-    float bb, be, bc2, dc, c1;
+    float bb, be, bc2, dc, c1, k1, k2;
 };
 
 // t2 = |y| - B is positive exactly when |y| > B; the margin of stage 1 is the
@@ -211,11 +211,16 @@ struct SymRow {
 // the running minimum in one three-input min.  The centroid step uses a
 // saturated multiply (1 when t2 > 0, 0 when t2 <= 0), which keeps the
 // selection on the FMA pipe; ra = |y| - c(i) and t4 = |ra| - E likewise for
-// stage 2.  The code bits are sign bits of y, y t2, y ra and y ra t4: the sign
-// of an IEEE product is the XOR of its operands' signs (zeros and flushed
-// results included), so the XORs run as fp32-pair multiplies on the FMA pipe.
-// A value exactly on a boundary has margin 0 and goes to the exact path.  Two
-// coordinates (a pair) per call.
+// stage 2.  The codes come from two bits of z1 = y k1 and of z2 = ra k2: the
+// sign, and bit 30 (the top exponent bit of an fp32 value, set exactly when
+// |z| >= 2, i.e. |y| >= B or |ra| >= E).  One funnel shift by 2 moves both
+// into the accumulating word (bit 2i + 1: sign, bit 2i: the "outer" bit), and
+// sym2_words turns those into the codes with whole-word logic.  z rounds
+// within 2^-22 relative of the exact ratio, so its bit 30 can differ from the
+// sign of t2 (t4) only within 2^-22 B (E) of the boundary; the symmetric mode
+// is chosen only for boundaries B, E < 1/2, where that is far inside the
+// guard band, whose rows take the exact path (a value exactly on a boundary
+// has margin 0).  Two coordinates (a pair) per call.
 __device__ __forceinline__ void sym2_code2(float2 y, const SymRow &k, uint32_t &a1x, uint32_t &a2x,
                                            uint32_t &a1y, uint32_t &a2y, float &mx, float &my)
 {
@@ -229,17 +234,28 @@ __device__ __forceinline__ void sym2_code2(float2 y, const SymRow &k, uint32_t &
     my = fminf(fminf(my, fabsf(y.y)), fabsf(t2.y));
     mx = fminf(fminf(mx, fabsf(ra.x)), fabsf(t4.x));
     my = fminf(fminf(my, fabsf(ra.y)), fabsf(t4.y));
-    const float2 p1 = __fmul2_rn(y, t2);
-    const float2 p2 = __fmul2_rn(y, ra);
-    const float2 p3 = __fmul2_rn(p2, t4);
-    a1x = __funnelshift_l(__float_as_uint(y.x), a1x, 1);
-    a1x = __funnelshift_l(__float_as_uint(p1.x), a1x, 1);
-    a2x = __funnelshift_l(__float_as_uint(p2.x), a2x, 1);
-    a2x = __funnelshift_l(__float_as_uint(p3.x), a2x, 1);
-    a1y = __funnelshift_l(__float_as_uint(y.y), a1y, 1);
-    a1y = __funnelshift_l(__float_as_uint(p1.y), a1y, 1);
-    a2y = __funnelshift_l(__float_as_uint(p2.y), a2y, 1);
-    a2y = __funnelshift_l(__float_as_uint(p3.y), a2y, 1);
+    const float2 z1 = __fmul2_rn(y, make_float2(k.k1, k.k1));
+    const float2 z2 = __fmul2_rn(ra, make_float2(k.k2, k.k2));
+    a1x = __funnelshift_l(__float_as_uint(z1.x), a1x, 2);
+    a2x = __funnelshift_l(__float_as_uint(z2.x), a2x, 2);
+    a1y = __funnelshift_l(__float_as_uint(z1.y), a1y, 2);
+    a2y = __funnelshift_l(__float_as_uint(z2.y), a2y, 2);
+}
+
+// Code words of 16 coordinates from the accumulated (sign, outer) bit pairs
+// of sym2_code2.  Stage 1: bit 1 = [y >= 0] = NOT sign(y), bit 0 = [y >= 0]
+// XOR [|y| < B] = sign(y) XOR outer.  Stage 2 (residual r = sgn(y) ra): bit 1
+// = NOT (sign(y) XOR sign(ra)), bit 0 = its XOR with NOT outer2; with
+// v = a2 XOR (a1 AND the sign positions) both words have the form
+// f(v) = (NOT v on odd bits) | ((v XOR v >> 1) on even bits).
+__device__ __forceinline__ uint32_t sym2_pairs_to_codes(uint32_t v)
+{
+    return (~v & 0xAAAAAAAAu) | ((v ^ (v >> 1)) & 0x55555555u);
+}
+__device__ __forceinline__ void sym2_words(uint32_t a1, uint32_t a2, uint32_t &w1, uint32_t &w2)
+{
+    w1 = sym2_pairs_to_codes(a1);
+    w2 = sym2_pairs_to_codes(a2 ^ (a1 & 0xAAAAAAAAu));
 }
 
 __device__ __forceinline__ void sym1_code(float y, const SymRow &k, uint32_t &a1, uint32_t &a2, float &m)
@@ -456,6 +472,9 @@ __global__ void __launch_bounds__(enc_warps(BITS, MODE) * 32, 1)
     const float tb2 = p.t2.bnd[lane];
     const int tc2 = p.t2.code[lane];
     const float tcen = p.c1[lane & (L - 1)];
+    // symmetric b = 2: 2 / B and 2 / E of the unit-norm books
+    const float kb1 = MODE == MODE_SYM && BITS == 2 ? __fdiv_rn(2.0f, p.b1[L - 2]) : 0.0f;
+    const float kb2 = MODE == MODE_SYM && BITS == 2 ? __fdiv_rn(2.0f, p.b2[L - 2]) : 0.0f;
     if constexpr (GRID) {
         // cell tables, replicated per lane; an empty cell (boundary -inf)
         // always takes code + 1, so its centroid step is 0
@@ -602,6 +621,14 @@ __global__ void __launch_bounds__(enc_warps(BITS, MODE) * 32, 1)
         sk.bc2 = (p.b1[(1 << BITS) - 2] - p.c1[(1 << BITS) - 2]) * den;
         sk.dc = (p.c1[(1 << BITS) - 1] - p.c1[(1 << BITS) - 2]) * den;
         sk.c1 = p.c1[(1 << BITS) - 1] * den;
+        if constexpr (MODE == MODE_SYM && BITS == 2) {
+            // (a zero row gives inf here; it always takes the exact path)
+            const float rden = __frcp_rn(den);
+            sk.k1 = kb1 * rden;
+            sk.k2 = kb2 * rden;
+        } else {
+            sk.k1 = sk.k2 = 0.0f;
+        }
         const float guard = MODE == MODE_SYM ? p.guard * den : p.guard;
 
         // ---- two-stage boundary count and LSB-first packing: word kx of the
@@ -652,10 +679,15 @@ __global__ void __launch_bounds__(enc_warps(BITS, MODE) * 32, 1)
                         sym1_code(y2.y, sk, a1y, a2y, my);
                     }
                 }
-                wa1[kx] = ~a1x;
-                wa2[kx] = ~a2x;
-                wa1[WL / 2 + kx] = ~a1y;
-                wa2[WL / 2 + kx] = ~a2y;
+                if constexpr (BITS == 2) {
+                    sym2_words(a1x, a2x, wa1[kx], wa2[kx]);
+                    sym2_words(a1y, a2y, wa1[WL / 2 + kx], wa2[WL / 2 + kx]);
+                } else {
+                    wa1[kx] = ~a1x;
+                    wa2[kx] = ~a2x;
+                    wa1[WL / 2 + kx] = ~a1y;
+                    wa2[WL / 2 + kx] = ~a2y;
+                }
             }
         } else {
             // table / plain count: slices of PP pairs through the scratch
