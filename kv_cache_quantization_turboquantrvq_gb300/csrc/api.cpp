@@ -213,9 +213,9 @@ static vq_status rvq_encode_impl(const void *k_f16, int B, int H, int S, int D, 
         p.b2[k] = k < L - 1 ? b2[k] : INFINITY;
     }
     int mode = RVQ_MODE_PLAIN;
-    // (b = 2: the symmetric kernel's boundary tests need B, E < 1/2)
+    // (b = 2: the symmetric kernel's boundary tests need B, E < 1/4)
     if (bits <= 2 && symmetric_codebook(c1, b1, L) && symmetric_codebook(c2, b2, L) &&
-        (bits == 1 || (b1[L - 2] < 0.5f && b2[L - 2] < 0.5f)))
+        (bits == 1 || (b1[L - 2] < 0.25f && b2[L - 2] < 0.25f)))
         mode = RVQ_MODE_SYM;
     else if (build_grid(b1, L - 1, kGuard, p.t1) && build_grid(b2, L - 1, kGuard, p.t2))
         // the shuffle tables also serve the exact recompute of the pair mode

@@ -201,28 +201,34 @@ __device__ __forceinline__ uint32_t pair_code(float v, float a, float bc, const 
 // Per-row constants of the symmetric quantizers, in units of S = H x (the
 // unnormalised transform, S = y n sqrt(D)): the positive boundaries B and E
 // of the two stages, B - c2, dc = c3 - c2 and (b = 1) c1, each scaled by
-// den = n sqrt(D); (b = 2) k1 = 2 / B and k2 = 2 / E in the same units.
+// den = n sqrt(D); for b = 2 also k1 = 2 / B and k2 = 2 / E and the margin
+// thresholds G1 = g (B + 2g) and G2 = g (E + 2g), g the guard band in the
+// same units.
 struct SymRow {
-    float bb, be, bc2, dc, c1, k1, k2;
+    float bb, be, bc2, dc, c1, k1, k2, G1, G2;
 };
 
-// t2 = |y| - B is positive exactly when |y| > B; the margin of stage 1 is the
-// distance to the nearer of its boundaries 0 and B, min(|y|, |t2|), taken with
-// the running minimum in one three-input min.  The centroid step uses a
+// Two coordinates (a pair, both of one row) of the symmetric b = 2 quantizer.
+// t2 = |y| - B is positive exactly when |y| > B.  The centroid step uses a
 // saturated multiply (1 when t2 > 0, 0 when t2 <= 0), which keeps the
 // selection on the FMA pipe; ra = |y| - c(i) and t4 = |ra| - E likewise for
 // stage 2.  The codes come from two bits of z1 = y k1 and of z2 = ra k2: the
 // sign, and bit 30 (the top exponent bit of an fp32 value, set exactly when
 // |z| >= 2, i.e. |y| >= B or |ra| >= E).  One funnel shift by 2 moves both
 // into the accumulating word (bit 2i + 1: sign, bit 2i: the "outer" bit), and
-// sym2_words turns those into the codes with whole-word logic.  z rounds
-// within 2^-22 relative of the exact ratio, so its bit 30 can differ from the
-// sign of t2 (t4) only within 2^-22 B (E) of the boundary; the symmetric mode
-// is chosen only for boundaries B, E < 1/2, where that is far inside the
-// guard band, whose rows take the exact path (a value exactly on a boundary
-// has margin 0).  Two coordinates (a pair) per call.
+// sym2_words turns those into the codes with whole-word logic.
+// Margins: a value within g of a boundary of stage 1 (0 or B) has
+// |y t2| < g (B + g), and one within g of a boundary of stage 2 has
+// |ra t4| < g (E + g); m1 and m2 keep the running minima of those products,
+// and a row whose minimum is below G1 = g (B + 2g) or G2 (the extra g covers
+// the products' rounding) takes the exact path.  Conversely a coordinate of an
+// unflagged row is at least g from every boundary, which is what the bit-30
+// test needs: z rounds within a few ulps of the exact ratio, so that bit can
+// differ from the sign of t2 (t4) only within 2^-21 B (E) of the boundary,
+// and the symmetric mode is chosen only for B, E < 1/4.  A value exactly on
+// a boundary, and y = 0, give a zero product.
 __device__ __forceinline__ void sym2_code2(float2 y, const SymRow &k, uint32_t &a1x, uint32_t &a2x,
-                                           uint32_t &a1y, uint32_t &a2y, float &mx, float &my)
+                                           uint32_t &a1y, uint32_t &a2y, float &m1, float &m2)
 {
     const float2 t2 = make_float2(fabsf(y.x) - k.bb, fabsf(y.y) - k.bb);
     const float2 su = make_float2(__saturatef(t2.x * 1.2676506e30f), __saturatef(t2.y * 1.2676506e30f));  // 2^100
@@ -230,10 +236,10 @@ __device__ __forceinline__ void sym2_code2(float2 y, const SymRow &k, uint32_t &
     const float2 ya = __fadd2_rn(t2, make_float2(k.bc2, k.bc2));
     const float2 ra = __ffma2_rn(make_float2(-k.dc, -k.dc), su, ya);
     const float2 t4 = make_float2(fabsf(ra.x) - k.be, fabsf(ra.y) - k.be);
-    mx = fminf(fminf(mx, fabsf(y.x)), fabsf(t2.x));
-    my = fminf(fminf(my, fabsf(y.y)), fabsf(t2.y));
-    mx = fminf(fminf(mx, fabsf(ra.x)), fabsf(t4.x));
-    my = fminf(fminf(my, fabsf(ra.y)), fabsf(t4.y));
+    const float2 p1 = __fmul2_rn(y, t2);
+    const float2 p2 = __fmul2_rn(ra, t4);
+    m1 = fminf(fminf(m1, fabsf(p1.x)), fabsf(p1.y));
+    m2 = fminf(fminf(m2, fabsf(p2.x)), fabsf(p2.y));
     const float2 z1 = __fmul2_rn(y, make_float2(k.k1, k.k1));
     const float2 z2 = __fmul2_rn(ra, make_float2(k.k2, k.k2));
     a1x = __funnelshift_l(__float_as_uint(z1.x), a1x, 2);
@@ -445,6 +451,7 @@ __global__ void __launch_bounds__(enc_warps(BITS, MODE) * 32, 1)
     constexpr int WARPS = enc_warps(BITS, MODE);
     constexpr bool ROLLED = MODE == MODE_GRID || MODE == MODE_PLAIN;
     constexpr int PP = enc_pairs(BITS);
+    static_assert(!(MODE == MODE_SYM && BITS == 2), "symmetric b = 2 books: rvq_encode_sym2_kernel");
     extern __shared__ __align__(128) unsigned char smem_raw[];
     unsigned char *stab = smem_1k(smem_raw);       // cell tables (GRID), pair table (PAIR)
     uint4 *ssg = reinterpret_cast<uint4 *>(stab + enc_tab_bytes(MODE));  // sign masks
@@ -472,9 +479,6 @@ __global__ void __launch_bounds__(enc_warps(BITS, MODE) * 32, 1)
     const float tb2 = p.t2.bnd[lane];
     const int tc2 = p.t2.code[lane];
     const float tcen = p.c1[lane & (L - 1)];
-    // symmetric b = 2: 2 / B and 2 / E of the unit-norm books
-    const float kb1 = MODE == MODE_SYM && BITS == 2 ? __fdiv_rn(2.0f, p.b1[L - 2]) : 0.0f;
-    const float kb2 = MODE == MODE_SYM && BITS == 2 ? __fdiv_rn(2.0f, p.b2[L - 2]) : 0.0f;
     if constexpr (GRID) {
         // cell tables, replicated per lane; an empty cell (boundary -inf)
         // always takes code + 1, so its centroid step is 0
@@ -621,14 +625,7 @@ __global__ void __launch_bounds__(enc_warps(BITS, MODE) * 32, 1)
         sk.bc2 = (p.b1[(1 << BITS) - 2] - p.c1[(1 << BITS) - 2]) * den;
         sk.dc = (p.c1[(1 << BITS) - 1] - p.c1[(1 << BITS) - 2]) * den;
         sk.c1 = p.c1[(1 << BITS) - 1] * den;
-        if constexpr (MODE == MODE_SYM && BITS == 2) {
-            // (a zero row gives inf here; it always takes the exact path)
-            const float rden = __frcp_rn(den);
-            sk.k1 = kb1 * rden;
-            sk.k2 = kb2 * rden;
-        } else {
-            sk.k1 = sk.k2 = 0.0f;
-        }
+        sk.k1 = sk.k2 = sk.G1 = sk.G2 = 0.0f;
         const float guard = MODE == MODE_SYM ? p.guard * den : p.guard;
 
         // ---- two-stage boundary count and LSB-first packing: word kx of the
@@ -672,22 +669,13 @@ __global__ void __launch_bounds__(enc_warps(BITS, MODE) * 32, 1)
 #pragma unroll
                 for (int i = E - 1; i >= 0; --i) {
                     const float2 y2 = v[kx * E + i];
-                    if constexpr (BITS == 2) {
-                        sym2_code2(y2, sk, a1x, a2x, a1y, a2y, mx, my);
-                    } else {
-                        sym1_code(y2.x, sk, a1x, a2x, mx);
-                        sym1_code(y2.y, sk, a1y, a2y, my);
-                    }
+                    sym1_code(y2.x, sk, a1x, a2x, mx);
+                    sym1_code(y2.y, sk, a1y, a2y, my);
                 }
-                if constexpr (BITS == 2) {
-                    sym2_words(a1x, a2x, wa1[kx], wa2[kx]);
-                    sym2_words(a1y, a2y, wa1[WL / 2 + kx], wa2[WL / 2 + kx]);
-                } else {
-                    wa1[kx] = ~a1x;
-                    wa2[kx] = ~a2x;
-                    wa1[WL / 2 + kx] = ~a1y;
-                    wa2[WL / 2 + kx] = ~a2y;
-                }
+                wa1[kx] = ~a1x;
+                wa2[kx] = ~a2x;
+                wa1[WL / 2 + kx] = ~a1y;
+                wa2[WL / 2 + kx] = ~a2y;
             }
         } else {
             // table / plain count: slices of PP pairs through the scratch
@@ -781,6 +769,301 @@ __global__ void __launch_bounds__(enc_warps(BITS, MODE) * 32, 1)
             if (nb < nblk) issue(nb, s);
         }
 
+    }
+}
+
+// ------------------------------------------- encode, symmetric b = 2, tensor cores
+//
+// The same pass as rvq_encode_kernel for symmetric 4-level books, with the
+// rotation on the tensor cores.  Write a coordinate as c = 8a + b (a < 16,
+// b < 8); the Sylvester matrix factors as H128[8a' + b'][8a + b] =
+// H16[a'][a] H8[b'][b].  Per warp and 16-row block, for each b the product
+// T_b = X_b H16 (X_b: the 16 rows' values x[8a + b], a as the k index) is one
+// pair of 16x8x16 mma.sync (fp16 operands, exact +-1 products, fp32
+// accumulation); then the H8 factor is three fp32x2 butterfly stages across
+// the eight accumulator tiles, in registers.  The columns of the H16 operand
+// are permuted so that the lane with t4 = lane & 3 receives a' = 4 t4 ..
+// 4 t4 + 3, i.e. output coordinates 32 t4 .. 32 t4 + 31: two whole code words
+// of each of its two rows (g8 = lane >> 2 and g8 + 8), so no word is split
+// across lanes.  The A operands come from 16-byte reads of the swizzled
+// staged rows (chunk a of row r holds x[8a .. 8a + 7]) and one byte permute
+// per register.  The norm is taken from the H16 outputs (their squares sum to
+// 16 sum x^2), the quantizer is sym2_code2, rows with a value in the guard
+// band go to rvq_fixup_row.
+constexpr int S2_WARPS = 16;
+constexpr int S2_STAGES = 3;
+
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                              uint32_t b0, uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// fp16 pair (+-1 of H16[a][a'], H16[a + 1][a']) for the B operand
+__device__ __forceinline__ uint32_t h16_pair(int a, int ap)
+{
+    const uint32_t lo = (__popc(a & ap) & 1) ? 0xBC00u : 0x3C00u;
+    const uint32_t hi = (__popc((a + 1) & ap) & 1) ? 0xBC00u : 0x3C00u;
+    return lo | (hi << 16);
+}
+
+// Per-row constants of the symmetric b = 2 quantizer (units of S = H x).
+__device__ __forceinline__ SymRow sym2_row(float den, float g, float b1u, float b2u, float bc2u, float dcu,
+                                           float kb1, float kb2)
+{
+    SymRow k;
+    k.bb = b1u * den;
+    k.be = b2u * den;
+    k.bc2 = bc2u * den;
+    k.dc = dcu * den;
+    k.c1 = 0.0f;
+    // approximate reciprocal (a zero row gives inf here; it always takes the
+    // exact path)
+    float rden;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(rden) : "f"(den));
+    k.k1 = kb1 * rden;
+    k.k2 = kb2 * rden;
+    k.G1 = g * (k.bb + 2.0f * g);
+    k.G2 = g * (k.be + 2.0f * g);
+    return k;
+}
+
+template <bool SGN>
+__global__ void __launch_bounds__(S2_WARPS * 32, 1) rvq_encode_sym2_kernel(const __grid_constant__ RvqEncodeParams p)
+{
+    constexpr int W = D * 2 / 32;  // 8 words per row and stream
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    unsigned char *base = smem_1k(smem_raw);
+    uint4 *ssg = reinterpret_cast<uint4 *>(base);  // sign masks: chunk a = coordinates 8a .. 8a + 7
+    unsigned char *smem = base + ENC_SGN_BYTES;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int g8 = lane >> 2, t4 = lane & 3;
+    unsigned char *ring = smem + warp * (S2_STAGES * ENC_BLOCK);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S2_WARPS * S2_STAGES * ENC_BLOCK) + warp * S2_STAGES;
+
+    if (lane == 0) {
+#pragma unroll
+        for (int s = 0; s < S2_STAGES; ++s) mbar_init(&bars[s], 1);
+        fence_mbar_init();
+    }
+    if (threadIdx.x < 16) {
+        const int c0 = 8 * threadIdx.x;
+        ssg[threadIdx.x] = make_uint4(half2_sign_mask(sign_pair(p.sgn, c0)), half2_sign_mask(sign_pair(p.sgn, c0 + 2)),
+                                      half2_sign_mask(sign_pair(p.sgn, c0 + 4)), half2_sign_mask(sign_pair(p.sgn, c0 + 6)));
+    }
+    __syncthreads();
+
+    const uint64_t pol = l2_policy_evict_first();
+    // shuffle tables of the exact recompute
+    const float tb1 = p.t1.bnd[lane];
+    const int tc1 = p.t1.code[lane];
+    const float tb2 = p.t2.bnd[lane];
+    const int tc2 = p.t2.code[lane];
+    const float tcen = p.c1[lane & 3];
+    // unit-norm book constants: B, E, B - c2, c3 - c2, 2 / B, 2 / E
+    const float b1u = p.b1[2], b2u = p.b2[2];
+    const float bc2u = p.b1[2] - p.c1[2], dcu = p.c1[3] - p.c1[2];
+    const float kb1 = __fdiv_rn(2.0f, b1u), kb2 = __fdiv_rn(2.0f, b2u);
+    // B operand: column n = g8 of n-tile nt is a' = 4 (g8 >> 1) + 2 nt + (g8 & 1);
+    // b0 holds k = 2 t4, 2 t4 + 1 and b1 k = 2 t4 + 8, 2 t4 + 9
+    uint32_t hb[2][2];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+        const int ap = 4 * (g8 >> 1) + 2 * nt + (g8 & 1);
+        hb[nt][0] = h16_pair(2 * t4, ap);
+        hb[nt][1] = h16_pair(2 * t4 + 8, ap);
+    }
+
+    const int nblk = (p.N + ER - 1) / ER;
+    const int gw = blockIdx.x * S2_WARPS + warp;
+    const int tw = gridDim.x * S2_WARPS;
+    auto issue = [&](int blk, int s) {
+        if (lane == 0) {
+            mbar_arrive_expect_tx(&bars[s], (uint32_t)ENC_BLOCK);
+            tma_load_2d(ring + s * ENC_BLOCK, &p.tmap, 0, blk * ER, &bars[s], pol);
+            tma_load_2d(ring + s * ENC_BLOCK + ENC_BLOCK / 2, &p.tmap, 64, blk * ER, &bars[s], pol);
+        }
+    };
+#pragma unroll
+    for (int s = 0; s < S2_STAGES; ++s) {
+        const int blk = gw + s * tw;
+        if (blk < nblk) issue(blk, s);
+    }
+
+    int s = 0;
+    uint32_t ph = 0;
+    for (int it = 0;; ++it) {
+        const int blk = gw + it * tw;
+        if (blk >= nblk) break;
+        const bool ok = mbar_wait_bounded(&bars[s], ph);
+        if (!__all_sync(FULL_MASK, ok)) {
+            if (lane == 0) atomicOr(&g_rvq_err, (unsigned)VQ_DEVERR_WAIT_TIMEOUT);
+            for (int k = 1; k < S2_STAGES; ++k) {
+                const int it2 = it + k;
+                if (gw + it2 * tw < nblk)
+                    (void)mbar_wait_bounded(&bars[it2 % S2_STAGES], (uint32_t)(it2 / S2_STAGES) & 1u);
+            }
+            return;
+        }
+        const unsigned char *sbuf = ring + s * ENC_BLOCK;
+
+        // ---- T_b = X_b H16 for b = 0..7 on the tensor cores
+        float acc[8][2][4];
+        {
+            // u[r][j]: row g8 + 8r, chunk a = 2 t4 + {0, 1, 8, 9}[j]
+            uint4 u[2][4];
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int a = 2 * t4 + (j & 1) + 8 * (j >> 1);
+                    u[r][j] = *reinterpret_cast<const uint4 *>(sbuf + (j >> 1) * (ENC_BLOCK / 2) + swz128(g8 + 8 * r, a & 7));
+                    if constexpr (SGN) {
+                        const uint4 m = ssg[a];
+                        u[r][j] = make_uint4(u[r][j].x ^ m.x, u[r][j].y ^ m.y, u[r][j].z ^ m.z, u[r][j].w ^ m.w);
+                    }
+                }
+            }
+#pragma unroll
+            for (int b = 0; b < 8; ++b) {
+                const uint32_t sel = (b & 1) ? 0x7632u : 0x5410u;
+                auto word = [&](const uint4 &v) -> uint32_t {
+                    return (b >> 1) == 0 ? v.x : (b >> 1) == 1 ? v.y : (b >> 1) == 2 ? v.z : v.w;
+                };
+                const uint32_t a0 = __byte_perm(word(u[0][0]), word(u[0][1]), sel);
+                const uint32_t a1 = __byte_perm(word(u[1][0]), word(u[1][1]), sel);
+                const uint32_t a2 = __byte_perm(word(u[0][2]), word(u[0][3]), sel);
+                const uint32_t a3 = __byte_perm(word(u[1][2]), word(u[1][3]), sel);
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                    acc[b][nt][0] = acc[b][nt][1] = acc[b][nt][2] = acc[b][nt][3] = 0.0f;
+                    mma_f16_16816(acc[b][nt], a0, a1, a2, a3, hb[nt][0], hb[nt][1]);
+                }
+            }
+        }
+
+        // ---- norms: the H16 outputs' squares sum to 16 sum x^2 (per row)
+        float q0, q1;
+        {
+            float2 s0 = make_float2(0.0f, 0.0f), s1 = s0;
+#pragma unroll
+            for (int b = 0; b < 8; ++b) {
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                    const float2 v0 = make_float2(acc[b][nt][0], acc[b][nt][1]);
+                    const float2 v1 = make_float2(acc[b][nt][2], acc[b][nt][3]);
+                    s0 = __ffma2_rn(v0, v0, s0);
+                    s1 = __ffma2_rn(v1, v1, s1);
+                }
+            }
+            q0 = s0.x + s0.y;
+            q1 = s1.x + s1.y;
+            q0 += __shfl_xor_sync(FULL_MASK, q0, 1);
+            q1 += __shfl_xor_sync(FULL_MASK, q1, 1);
+            q0 += __shfl_xor_sync(FULL_MASK, q0, 2);
+            q1 += __shfl_xor_sync(FULL_MASK, q1, 2);
+            q0 *= 0.0625f;
+            q1 *= 0.0625f;
+        }
+        const float n0 = __fsqrt_rn(q0), n1 = __fsqrt_rn(q1);
+        const float den0 = n0 * SQRT_D_HI, den1 = n1 * SQRT_D_HI;
+
+        // ---- H8 across b: acc[b'][nt] = S at coordinates 32 t4 + 16 nt + b' (.x / c2)
+        // and 32 t4 + 16 nt + 8 + b' (.y / c3)
+        const float2 neg1 = make_float2(-1.0f, -1.0f);
+#pragma unroll
+        for (int h = 1; h < 8; h <<= 1) {
+#pragma unroll
+            for (int b = 0; b < 8; ++b) {
+                if ((b & h) == 0) {
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+                        for (int r = 0; r < 2; ++r) {
+                            const float2 x = make_float2(acc[b][nt][2 * r], acc[b][nt][2 * r + 1]);
+                            const float2 y = make_float2(acc[b + h][nt][2 * r], acc[b + h][nt][2 * r + 1]);
+                            const float2 sum = __fadd2_rn(x, y);
+                            const float2 dif = __ffma2_rn(y, neg1, x);
+                            acc[b][nt][2 * r] = sum.x;
+                            acc[b][nt][2 * r + 1] = sum.y;
+                            acc[b + h][nt][2 * r] = dif.x;
+                            acc[b + h][nt][2 * r + 1] = dif.y;
+                        }
+                    }
+                }
+            }
+        }
+
+        // ---- quantize: word 2 t4 + nt of row g8 + 8r gets b' = 0..7 of .x at
+        // positions 0..7 and of .y at positions 8..15
+        const SymRow sk0 = sym2_row(den0, p.guard * den0, b1u, b2u, bc2u, dcu, kb1, kb2);
+        const SymRow sk1 = sym2_row(den1, p.guard * den1, b1u, b2u, bc2u, dcu, kb1, kb2);
+        // running minima of the stage-1 / stage-2 margin products of each row
+        float m0a = __int_as_float(0x7f800000), m0b = m0a, m1a = m0a, m1b = m0a;
+        uint32_t w1[2][2], w2[2][2];
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                uint32_t a1x = 0u, a2x = 0u, a1y = 0u, a2y = 0u;
+#pragma unroll
+                for (int b = 7; b >= 0; --b) {
+                    const float2 y2 = make_float2(acc[b][nt][2 * r], acc[b][nt][2 * r + 1]);
+                    if (r == 0) sym2_code2(y2, sk0, a1x, a2x, a1y, a2y, m0a, m0b);
+                    else sym2_code2(y2, sk1, a1x, a2x, a1y, a2y, m1a, m1b);
+                }
+                sym2_words(__byte_perm(a1x, a1y, 0x5410u), __byte_perm(a2x, a2y, 0x5410u), w1[r][nt], w2[r][nt]);
+            }
+        }
+
+        // ---- guard band: a row is flagged if any of its four lanes saw a value
+        // inside the band (and always when it is zero)
+        const int row0 = blk * ER + g8, row1 = row0 + 8;
+        const bool valid0 = row0 < p.N, valid1 = row1 < p.N;
+        const bool f0 = valid0 && (!(m0a >= sk0.G1) || !(m0b >= sk0.G2) || !(q0 > 0.0f));
+        const bool f1 = valid1 && (!(m1a >= sk1.G1) || !(m1b >= sk1.G2) || !(q1 > 0.0f));
+        int f = (f0 ? 1 : 0) | (f1 ? 2 : 0);
+        f |= __shfl_xor_sync(FULL_MASK, f, 1);
+        f |= __shfl_xor_sync(FULL_MASK, f, 2);
+
+        // ---- fast words: 8 bytes per lane, row and stream (a block's 16 rows are
+        // contiguous in both streams)
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            const int row = r ? row1 : row0;
+            size_t drow = 0;
+            if ((r ? valid1 : valid0) && !(f & (1 << r)) && rvq_dst_row(p, row, drow)) {
+                *reinterpret_cast<uint2 *>(p.p1 + drow * W + 2 * t4) = make_uint2(w1[r][0], w1[r][1]);
+                *reinterpret_cast<uint2 *>(p.p2 + drow * W + 2 * t4) = make_uint2(w2[r][0], w2[r][1]);
+                if (t4 == 0) p.norms[drow] = r ? n1 : n0;
+            }
+        }
+
+        // ---- flagged rows: exact recompute by the warp
+        unsigned fl = (__ballot_sync(FULL_MASK, (f & 1) != 0) & 0x11111111u) |
+                      ((__ballot_sync(FULL_MASK, (f & 2) != 0) & 0x11111111u) << 1);
+        while (fl) {
+            const int bit = __ffs(fl) - 1;
+            fl &= fl - 1;
+            const int r = (bit >> 2) + 8 * (bit & 1);
+            rvq_fixup_row<2, false>(p, sbuf, r, blk * ER + r, lane, tb1, tc1, tb2, tc2, tcen);
+        }
+        __syncwarp();
+
+        fence_proxy_async_smem();
+        {
+            const int nb = blk + S2_STAGES * tw;
+            if (nb < nblk) issue(nb, s);
+        }
+        if (++s == S2_STAGES) {
+            s = 0;
+            ph ^= 1u;
+        }
     }
 }
 
@@ -1056,6 +1339,34 @@ cudaError_t launch_enc(const RvqEncodeParams &p0, cudaStream_t stream)
     return cudaGetLastError();
 }
 
+// Shared memory of the symmetric b = 2 tensor-core encoder: sign masks, the
+// warps' rings, their mbarriers (same layout as the generic encoder's).
+constexpr int S2_SMEM = 1024 + ENC_SGN_BYTES + S2_WARPS * S2_STAGES * (ENC_BLOCK + 8);
+static_assert(S2_SMEM <= SMEM_MAX, "symmetric encoder shared memory");
+
+cudaError_t launch_enc_sym2(const RvqEncodeParams &p0, cudaStream_t stream)
+{
+    RvqEncodeParams p = p0;
+    p.divS = make_fastdiv((uint32_t)p.S);
+    p.divH = make_fastdiv((uint32_t)p.H);
+    {
+        const uint64_t dims[2] = {(uint64_t)D, (uint64_t)p.N};
+        const uint64_t strides[1] = {(uint64_t)D * 2};
+        const uint32_t box[2] = {64u, (uint32_t)ER};
+        if (!encode_tmap_f16(&p.tmap, p.x, 2, dims, strides, box, true, true)) return cudaErrorInvalidValue;
+    }
+    auto kern = p.has_sgn ? rvq_encode_sym2_kernel<true> : rvq_encode_sym2_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S2_SMEM);
+    if (e != cudaSuccess) return e;
+    const int nblk = (p.N + ER - 1) / ER;
+    int grid = (nblk + S2_WARPS - 1) / S2_WARPS;
+    const int sms = sm_count();
+    if (grid > sms) grid = sms;
+    if (grid < 1) grid = 1;
+    kern<<<grid, S2_WARPS * 32, S2_SMEM, stream>>>(p);
+    return cudaGetLastError();
+}
+
 template <int BITS>
 cudaError_t launch_dec(const RvqDecodeParams &p0, cudaStream_t stream)
 {
@@ -1090,7 +1401,7 @@ cudaError_t launch_rvq_encode(const RvqEncodeParams &p, int bits, int mode, cuda
     case 1 * 4 + MODE_SYM: return launch_enc<1, MODE_SYM>(p, stream);
     case 2 * 4 + MODE_PLAIN: return launch_enc<2, MODE_PLAIN>(p, stream);
     case 2 * 4 + MODE_GRID: return launch_enc<2, MODE_GRID>(p, stream);
-    case 2 * 4 + MODE_SYM: return launch_enc<2, MODE_SYM>(p, stream);
+    case 2 * 4 + MODE_SYM: return launch_enc_sym2(p, stream);
     case 4 * 4 + MODE_PLAIN: return launch_enc<4, MODE_PLAIN>(p, stream);
     case 4 * 4 + MODE_GRID: return launch_enc<4, MODE_GRID>(p, stream);
     case 4 * 4 + MODE_PAIR: return launch_enc<4, MODE_PAIR>(p, stream);
