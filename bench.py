@@ -170,7 +170,9 @@ def build_workload(name, dev, rank=0, layers=None, batch=None, chunked=False, ch
                 api.vq_rvq_unpack_dequant(p1, p2, nr, bits, cb[0], cb[2], out=out, stream=stream)
         else:
             dec = None
-        ops.append(Op(tag + "rvq_encode", "rvq_encode_kernel", enc, rvq_bytes(rows, bits), rows * D))
+        # the library's b = 2 books are symmetric: their encoder is the tensor-core kernel
+        ekern = "rvq_encode_sym2_kernel" if bits == 2 else "rvq_encode_kernel"
+        ops.append(Op(tag + "rvq_encode", ekern, enc, rvq_bytes(rows, bits), rows * D))
         if dec is not None:
             ops.append(Op(tag + "rvq_decode", "rvq_decode_kernel", dec, rvq_bytes(rows, bits), rows * D))
         results.extend([p1, p2, nr])
@@ -260,7 +262,7 @@ def build_workload(name, dev, rank=0, layers=None, batch=None, chunked=False, ch
             if chunked:
                 c = new_chunk([(k_np, k)])
                 rvq_ops("L%02d_" % layer, k, cfg["bits"], ops=c["ops"], results=c["results"], stream=chunk_stream)
-        ops.sort(key=lambda o: (o.kernel != "rvq_encode_kernel", o.name))
+        ops.sort(key=lambda o: (not o.kernel.startswith("rvq_encode"), o.name))
     elif name == "c2":
         cfg = cfgs["c2_kivi_b2_32x4096"]
         k_np, v_np = synth.keys_for(cfg), synth.values_for(cfg)

@@ -32,6 +32,9 @@
 //    band of a boundary; such rows are redone by the whole warp in exact /
 //    double-float arithmetic (rvq_fixup_row), so the packed words equal those
 //    of exact arithmetic.
+// Symmetric 4-level books (b = 2, the library's) have their own encoder,
+// rvq_encode_sym2_kernel: the same rings and exact recompute, the rotation on
+// the tensor cores and four lanes per row.
 #include <cuda_fp16.h>
 
 #include "device_common.cuh"
@@ -882,6 +885,8 @@ __global__ void __launch_bounds__(S2_WARPS * 32, 1) rvq_encode_sym2_kernel(const
     const int nblk = (p.N + ER - 1) / ER;
     const int gw = blockIdx.x * S2_WARPS + warp;
     const int tw = gridDim.x * S2_WARPS;
+    // destination row = source row (no batch offsets, same capacity)
+    const bool dense = p.dst_off == nullptr && p.S_dst == p.S;
     auto issue = [&](int blk, int s) {
         if (lane == 0) {
             mbar_arrive_expect_tx(&bars[s], (uint32_t)ENC_BLOCK);
@@ -1036,8 +1041,8 @@ __global__ void __launch_bounds__(S2_WARPS * 32, 1) rvq_encode_sym2_kernel(const
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
             const int row = r ? row1 : row0;
-            size_t drow = 0;
-            if ((r ? valid1 : valid0) && !(f & (1 << r)) && rvq_dst_row(p, row, drow)) {
+            size_t drow = (size_t)row;
+            if ((r ? valid1 : valid0) && !(f & (1 << r)) && (dense || rvq_dst_row(p, row, drow))) {
                 *reinterpret_cast<uint2 *>(p.p1 + drow * W + 2 * t4) = make_uint2(w1[r][0], w1[r][1]);
                 *reinterpret_cast<uint2 *>(p.p2 + drow * W + 2 * t4) = make_uint2(w2[r][0], w2[r][1]);
                 if (t4 == 0) p.norms[drow] = r ? n1 : n0;
