@@ -160,42 +160,6 @@ __device__ __forceinline__ void code_pair(__half a, __half b, const GroupQ &g, u
     code_pair2<BITS>(a, b, make_float2(g.mn, g.mn), make_float2(g.f, g.f), make_float2(g.rr, g.rr), qa, qb);
 }
 
-// fp16(q*s + z) rounded once from the exact value: q*s is exact in fp32, the
-// sum is carried as a rounded value plus its exact error, and a non-zero error
-// is folded in as a sticky bit (round-to-odd) before the final fp16 rounding.
-__device__ __forceinline__ __half recon_exact(uint32_t q, float s, float z)
-{
-    const float p = (float)q * s;
-    float sum, err;
-    two_sum(p, z, sum, err);
-    if (err != 0.0f) {
-        uint32_t b = __float_as_uint(sum);
-        if ((err < 0.0f) != (sum < 0.0f)) b -= 1u;  // truncate toward zero
-        b |= 1u;                                     // sticky
-        sum = __uint_as_float(b);
-    }
-    return __float2half_rn(sum);
-}
-
-// True when q*s + z is exact in fp32 for every q in [0, C]: the sum then
-// needs no more than 24 significant bits.  s and z are fp16 values; their
-// quanta are ulp16 (2^-24 for subnormals).
-__device__ __forceinline__ float ulp16_of(float x)
-{
-    int e = ((__float_as_int(x) >> 23) & 0xff) - 127;
-    e = e < -14 ? -14 : e;
-    return __int_as_float((e - 10 + 127) << 23);
-}
-
-template <int BITS>
-__device__ __forceinline__ bool group_sum_exact(float s, float z)
-{
-    constexpr float C = (float)((1 << BITS) - 1);
-    if (s == 0.0f || z == 0.0f) return true;
-    const float q = fminf(ulp16_of(s), ulp16_of(z));
-    return fabsf(z) + C * s < 8388608.0f * q;  // 2^23 quanta: one bit of headroom
-}
-
 // ------------------------------------------------------------ fast codes
 //
 // The common path takes q = rint(A f) with A = fl(x - min) and
@@ -718,12 +682,15 @@ constexpr int DQ_THREADS = 256;
 // Values: two threads per row: lane l works on row l & 15 of a 16-row block
 // and on channels [64h, 64h + 64), h = l >> 4.  The words of a block
 // (contiguous in memory) arrive by one bulk copy into a per-warp 3-stage
-// ring; scale/zero of the lane's groups are read one block ahead; per group
-// the exactness test picks one FMA per element or the rare round-to-odd path
-// (a small rolled loop over the staged words); the fp16 half rows are staged
-// in shared memory and written out coalesced (the 16 rows of a block are
-// contiguous).
-constexpr int VDQ_WARPS = 16;
+// ring; scale/zero of the lane's groups are read one block ahead.  Each
+// element is one fp16x2 fused multiply-add, q s + z rounded once from its
+// exact value (the definition of the dequant), two elements per instruction:
+// codes k and k + E/2 of a word sit at bits b k and b k + 16, so one shift and
+// one mask-or put both into the mantissas of 1024 + q, a subtract of 1024
+// leaves q exactly, and byte permutes pair the results as consecutive
+// elements.  The fp16 half rows are staged in shared memory and written out
+// coalesced (the 16 rows of a block are contiguous).
+constexpr int VDQ_WARPS = 24;
 constexpr int VDQ_STAGES = 3;
 constexpr int VDR = 16;  // rows per block
 __host__ __device__ constexpr int vdq_stage(int bits) { return VDR * (D * bits / 32) * 4; }
@@ -740,6 +707,7 @@ __global__ void __launch_bounds__(VDQ_WARPS * 32, 1) kivi_values_dequant_kernel(
     constexpr int GL = G < 64 ? G : 64;    // group members held by one thread
     constexpr int NGL = 64 / GL;           // groups (or group halves) per thread
     constexpr uint32_t MASK = (1u << BITS) - 1u;
+    static_assert(GL % E == 0, "a packed word lies inside one group");
     constexpr int STG = vdq_stage(BITS);
     constexpr int WB = vdq_warp_bytes(BITS);
     extern __shared__ __align__(128) unsigned char smem[];
@@ -792,11 +760,11 @@ __global__ void __launch_bounds__(VDQ_WARPS * 32, 1) kivi_values_dequant_kernel(
         const int blk = gw + it * tw;
         if (blk >= nblk) break;
         const int s = it % VDQ_STAGES;
-        float sf[NGL], zf[NGL];
+        __half2 s2[NGL], z2[NGL];
 #pragma unroll
         for (int j = 0; j < NGL; ++j) {
-            sf[j] = __half2float(sh[j]);
-            zf[j] = __half2float(zh[j]);
+            s2[j] = __half2half2(sh[j]);
+            z2[j] = __half2half2(zh[j]);
         }
         load_sz(blk + tw);
         const bool ok = mbar_wait_bounded(&bars[s], (uint32_t)(it / VDQ_STAGES) & 1u);
@@ -822,35 +790,28 @@ __global__ void __launch_bounds__(VDQ_WARPS * 32, 1) kivi_values_dequant_kernel(
             }
         }
         uint4 *orow = reinterpret_cast<uint4 *>(obuf + rr * ROW_STRIDE + hh * 128);
+        const __half2 k1024 = __float2half2_rn(1024.0f);
 #pragma unroll
-        for (int jl = 0; jl < NGL; ++jl) {
-            if (group_sum_exact<BITS>(sf[jl], zf[jl])) {
-                const float2 s2 = make_float2(sf[jl], sf[jl]), z2 = make_float2(zf[jl], zf[jl]);
+        for (int i = 0; i < WL; ++i) {
+            const int jl = (i * E) / GL;  // a word lies inside one group (GL >= E)
+            uint32_t r[E / 2];
 #pragma unroll
-                for (int c = 0; c < GL / 8; ++c) {
-                    uint32_t o[4];
-#pragma unroll
-                    for (int jj = 0; jj < 4; ++jj) {
-                        const int e = jl * GL + 8 * c + 2 * jj;  // element within the half row
-                        const uint32_t q0 = (wd[e / E] >> ((e % E) * BITS)) & MASK;
-                        const uint32_t q1 = (wd[(e + 1) / E] >> (((e + 1) % E) * BITS)) & MASK;
-                        const float2 r2 = __ffma2_rn(make_float2((float)q0, (float)q1), s2, z2);
-                        const __half2 hv = __floats2half2_rn(r2.x, r2.y);
-                        o[jj] = *reinterpret_cast<const uint32_t *>(&hv);
-                    }
-                    orow[jl * (GL / 8) + c] = make_uint4(o[0], o[1], o[2], o[3]);
-                }
-            } else {
-                // q*s + z not exact in fp32 for this group (rare): round once
-                // from the exact value, element by element
-#pragma unroll 1
-                for (int e = jl * GL; e < jl * GL + GL; e += 2) {
-                    const uint32_t q0 = (wrow[e / E] >> ((e % E) * BITS)) & MASK;
-                    const uint32_t q1 = (wrow[(e + 1) / E] >> (((e + 1) % E) * BITS)) & MASK;
-                    const __half2 hv = __halves2half2(recon_exact(q0, sf[jl], zf[jl]), recon_exact(q1, sf[jl], zf[jl]));
-                    reinterpret_cast<uint32_t *>(orow)[e / 2] = *reinterpret_cast<const uint32_t *>(&hv);
-                }
+            for (int k = 0; k < E / 2; ++k) {
+                const uint32_t x = ((wd[i] >> (BITS * k)) & (MASK | (MASK << 16))) | 0x64006400u;
+                const __half2 q2 = __hsub2(*reinterpret_cast<const __half2 *>(&x), k1024);
+                const __half2 v2 = __hfma2(q2, s2[jl], z2[jl]);
+                r[k] = *reinterpret_cast<const uint32_t *>(&v2);
             }
+            // r[k] = (element k, element k + E/2) of the word -> consecutive pairs
+            uint32_t o[E / 2];
+#pragma unroll
+            for (int j = 0; j < E / 4; ++j) {
+                o[j] = __byte_perm(r[2 * j], r[2 * j + 1], 0x5410);
+                o[E / 4 + j] = __byte_perm(r[2 * j], r[2 * j + 1], 0x7632);
+            }
+#pragma unroll
+            for (int c = 0; c < E / 8; ++c)
+                orow[(i * E) / 8 + c] = make_uint4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
         }
         __syncwarp();
         fence_proxy_async_smem();
@@ -884,33 +845,27 @@ __global__ void __launch_bounds__(DQ_THREADS) kivi_keys_dequant_kernel(const __g
         const int ntok = min(G, p.S_q - g * G);
         const uint2 sraw = __ldg(reinterpret_cast<const uint2 *>(static_cast<const __half *>(p.scale) + (size_t)tile * D + 4 * lane));
         const uint2 zraw = __ldg(reinterpret_cast<const uint2 *>(static_cast<const __half *>(p.zero) + (size_t)tile * D + 4 * lane));
-        const __half *sh = reinterpret_cast<const __half *>(&sraw);
-        const __half *zh = reinterpret_cast<const __half *>(&zraw);
-        float s[4], z[4];
-        bool all_exact = true;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            s[j] = __half2float(sh[j]);
-            z[j] = __half2float(zh[j]);
-            all_exact &= group_sum_exact<BITS>(s[j], z[j]);
-        }
+        // scale / zero of channels (4l, 4l + 1) and (4l + 2, 4l + 3) as fp16 pairs
+        const __half2 sa = *reinterpret_cast<const __half2 *>(&sraw.x), sb = *reinterpret_cast<const __half2 *>(&sraw.y);
+        const __half2 za = *reinterpret_cast<const __half2 *>(&zraw.x), zb = *reinterpret_cast<const __half2 *>(&zraw.y);
+        const __half2 k1024 = __float2half2_rn(1024.0f);
         for (int k = 0; k < WG; ++k) {
             const uint4 wv = __ldg(reinterpret_cast<const uint4 *>(p.packed + ((size_t)tile * WG + k) * D + 4 * lane));
-            const uint32_t wk[4] = {wv.x, wv.y, wv.z, wv.w};
+            // the two channels of a pair side by side: tokens j < E/2 from the low
+            // halves of their words, the others from the high halves
+            const uint32_t alo = __byte_perm(wv.x, wv.y, 0x5410), ahi = __byte_perm(wv.x, wv.y, 0x7632);
+            const uint32_t blo = __byte_perm(wv.z, wv.w, 0x5410), bhi = __byte_perm(wv.z, wv.w, 0x7632);
 #pragma unroll 4
             for (int j = 0; j < E; ++j) {
                 const int i = k * E + j;
                 if (i >= ntok) break;
-                __half o[4];
-                if (all_exact) {
-#pragma unroll
-                    for (int c = 0; c < 4; ++c)
-                        o[c] = __float2half_rn(fmaf((float)((wk[c] >> (j * BITS)) & MASK), s[c], z[c]));
-                } else {
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) o[c] = recon_exact((wk[c] >> (j * BITS)) & MASK, s[c], z[c]);
-                }
-                const __half2 a = __halves2half2(o[0], o[1]), b = __halves2half2(o[2], o[3]);
+                // q s + z rounded once from its exact value: one fp16x2 FMA per
+                // channel pair (codes as the mantissas of 1024 + q)
+                const int sh = BITS * (j % (E / 2));
+                const uint32_t xa = (((j < E / 2 ? alo : ahi) >> sh) & (MASK | (MASK << 16))) | 0x64006400u;
+                const uint32_t xb = (((j < E / 2 ? blo : bhi) >> sh) & (MASK | (MASK << 16))) | 0x64006400u;
+                const __half2 a = __hfma2(__hsub2(*reinterpret_cast<const __half2 *>(&xa), k1024), sa, za);
+                const __half2 b = __hfma2(__hsub2(*reinterpret_cast<const __half2 *>(&xb), k1024), sb, zb);
                 *reinterpret_cast<uint2 *>(static_cast<__half *>(p.out) + ((size_t)bh * p.S_q + g * G + i) * D + 4 * lane) =
                     make_uint2(*reinterpret_cast<const uint32_t *>(&a), *reinterpret_cast<const uint32_t *>(&b));
             }

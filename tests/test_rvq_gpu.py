@@ -116,6 +116,23 @@ def test_encode_asymmetric_codebook(vq, oracle_mod, bits):
     check_rvq(p1, p2, n, ora, bits)
 
 
+@pytest.mark.parametrize("outer", [0.24, 0.3])
+def test_encode_symmetric_books_wide_boundaries(vq, oracle_mod, outer):
+    """Symmetric 4-level books scaled so that the stage-1 outer boundary is
+    `outer`: below 1/4 they take the tensor-core encoder (whose scaled boundary
+    test is argued for B, E < 1/4), at 0.3 the shuffle-table encoder; both
+    must equal exact arithmetic."""
+    bits = 2
+    c1, b1, c2, b2 = [a.astype(np.float64) for a in oracle_mod.rvq_codebooks(D, bits)[:4]]
+    f = outer / b1[2]
+    c1, b1, c2, b2 = [np.float32(f) * a.astype(np.float32) for a in (c1, b1, c2, b2)]
+    assert b1[1] == 0 and np.all(c1 == -c1[::-1]) and np.all(b1 == -b1[::-1])
+    x = _rows((1, 3, 800), 123, outliers=(4, 40.0))
+    p1, p2, n = _encode(vq, x, bits, (c1, b1, c2, b2))
+    ora = oracle_mod.rvq_encode(x.reshape(-1, D), bits, c1, b1, c2, b2)
+    check_rvq(p1, p2, n, ora, bits)
+
+
 @pytest.mark.parametrize("bits", [2, 4])
 def test_encode_plain_count_fallback(vq, oracle_mod, bits):
     """A codebook with two boundaries inside one guard band has no lookup
