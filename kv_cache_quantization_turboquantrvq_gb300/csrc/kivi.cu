@@ -23,11 +23,15 @@
 // The stored scale is fp16(fp32(range/(2^b - 1))) with both roundings to
 // nearest even.
 //
-// Values (per token): one row per thread, rows staged by per-row bulk copies
-// into a per-warp 3-stage ring (as the RVQ encoder).  Keys (per channel): one
-// [G x 128] tile (contiguous in memory) per warp per step, staged by a single
-// bulk copy; lane l owns channels 4l..4l+3 and walks the G tokens, so no
-// cross-thread reduction is needed (the pages' "one thread, one whole group").
+// Values (per token): two threads per row (64 channels each), 16-row blocks
+// staged as two swizzled TMA boxes into a per-warp ring (as the RVQ encoder).
+// Keys (per channel): one [G x 64] half-tile per warp step as one TMA box; lane
+// l owns two channels and walks the G tokens, so no cross-thread reduction is
+// needed (the pages' "one thread, one whole group").
+//
+// Dequant: one fp16x2 fused multiply-add per element pair, q * scale + zero
+// rounded once from its exact value (fma.rn.f16x2), the code entering exactly
+// as (1024 + q) - 1024 in fp16.
 #include <cuda_fp16.h>
 
 #include "device_common.cuh"
