@@ -778,7 +778,7 @@ def main():
     if rank == 0 and not args.no_cpu_baseline:
         rates, desc = oracle_sample_rates(args.workload)
         cpu = {"value": round(step_rate_from_ops(ops, rates) / 1e9, 6), "unit": UNIT, "cores": 1,
-               "kind": "oracle", "sample": desc}
+               "host_cores": os.cpu_count(), "kind": "oracle", "sample": desc}
 
     if rank == 0:
         line = {
@@ -841,8 +841,8 @@ def run_reference(args, world):
         "config": {"workload": args.workload + ": " + describe(args.workload),
                    "bytes_per_step": step_bytes},
         "impl": "reference",
-        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": desc + "; wall %.1f s over %d steps" % (t_total, K)},
+        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": 1, "host_cores": os.cpu_count(),
+                         "kind": "oracle", "sample": desc + "; wall %.1f s over %d steps" % (t_total, K)},
         "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
