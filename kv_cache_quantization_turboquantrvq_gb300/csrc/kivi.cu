@@ -853,25 +853,36 @@ __global__ void __launch_bounds__(DQ_THREADS) kivi_keys_dequant_kernel(const __g
         const __half2 sa = *reinterpret_cast<const __half2 *>(&sraw.x), sb = *reinterpret_cast<const __half2 *>(&sraw.y);
         const __half2 za = *reinterpret_cast<const __half2 *>(&zraw.x), zb = *reinterpret_cast<const __half2 *>(&zraw.y);
         const __half2 k1024 = __float2half2_rn(1024.0f);
-        for (int k = 0; k < WG; ++k) {
-            const uint4 wv = __ldg(reinterpret_cast<const uint4 *>(p.packed + ((size_t)tile * WG + k) * D + 4 * lane));
-            // the two channels of a pair side by side: tokens j < E/2 from the low
-            // halves of their words, the others from the high halves
-            const uint32_t alo = __byte_perm(wv.x, wv.y, 0x5410), ahi = __byte_perm(wv.x, wv.y, 0x7632);
-            const uint32_t blo = __byte_perm(wv.z, wv.w, 0x5410), bhi = __byte_perm(wv.z, wv.w, 0x7632);
+        // up to four word rows of the tile in flight before any is used (a
+        // ragged last group's pad words exist and hold code 0)
+        constexpr int KB = WG < 4 ? WG : 4;
+        for (int k0 = 0; k0 < WG; k0 += KB) {
+            uint4 wvs[KB];
+#pragma unroll
+            for (int kk = 0; kk < KB; ++kk)
+                wvs[kk] = __ldg(reinterpret_cast<const uint4 *>(p.packed + ((size_t)tile * WG + k0 + kk) * D + 4 * lane));
+#pragma unroll
+            for (int kk = 0; kk < KB; ++kk) {
+                const int k = k0 + kk;
+                const uint4 wv = wvs[kk];
+                // the two channels of a pair side by side: tokens j < E/2 from the
+                // low halves of their words, the others from the high halves
+                const uint32_t alo = __byte_perm(wv.x, wv.y, 0x5410), ahi = __byte_perm(wv.x, wv.y, 0x7632);
+                const uint32_t blo = __byte_perm(wv.z, wv.w, 0x5410), bhi = __byte_perm(wv.z, wv.w, 0x7632);
 #pragma unroll 4
-            for (int j = 0; j < E; ++j) {
-                const int i = k * E + j;
-                if (i >= ntok) break;
-                // q s + z rounded once from its exact value: one fp16x2 FMA per
-                // channel pair (codes as the mantissas of 1024 + q)
-                const int sh = BITS * (j % (E / 2));
-                const uint32_t xa = (((j < E / 2 ? alo : ahi) >> sh) & (MASK | (MASK << 16))) | 0x64006400u;
-                const uint32_t xb = (((j < E / 2 ? blo : bhi) >> sh) & (MASK | (MASK << 16))) | 0x64006400u;
-                const __half2 a = __hfma2(__hsub2(*reinterpret_cast<const __half2 *>(&xa), k1024), sa, za);
-                const __half2 b = __hfma2(__hsub2(*reinterpret_cast<const __half2 *>(&xb), k1024), sb, zb);
-                *reinterpret_cast<uint2 *>(static_cast<__half *>(p.out) + ((size_t)bh * p.S_q + g * G + i) * D + 4 * lane) =
-                    make_uint2(*reinterpret_cast<const uint32_t *>(&a), *reinterpret_cast<const uint32_t *>(&b));
+                for (int j = 0; j < E; ++j) {
+                    const int i = k * E + j;
+                    if (i >= ntok) break;
+                    // q s + z rounded once from its exact value: one fp16x2 FMA
+                    // per channel pair (codes as the mantissas of 1024 + q)
+                    const int sh = BITS * (j % (E / 2));
+                    const uint32_t xa = (((j < E / 2 ? alo : ahi) >> sh) & (MASK | (MASK << 16))) | 0x64006400u;
+                    const uint32_t xb = (((j < E / 2 ? blo : bhi) >> sh) & (MASK | (MASK << 16))) | 0x64006400u;
+                    const __half2 ha = __hfma2(__hsub2(*reinterpret_cast<const __half2 *>(&xa), k1024), sa, za);
+                    const __half2 hb = __hfma2(__hsub2(*reinterpret_cast<const __half2 *>(&xb), k1024), sb, zb);
+                    *reinterpret_cast<uint2 *>(static_cast<__half *>(p.out) + ((size_t)bh * p.S_q + g * G + i) * D + 4 * lane) =
+                        make_uint2(*reinterpret_cast<const uint32_t *>(&ha), *reinterpret_cast<const uint32_t *>(&hb));
+                }
             }
         }
     }

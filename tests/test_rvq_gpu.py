@@ -80,6 +80,25 @@ def test_encode_special_rows(vq, oracle_mod, bits):
     assert n.reshape(-1)[0] == 0.0
 
 
+@pytest.mark.parametrize("bits", [2, 4])
+def test_encode_wide_dynamic_range_rows(vq, oracle_mod, bits):
+    """Rows that stress the fast rotation's accumulation: one large value among
+    values near the bottom of the fp16 range, and rows whose values spread
+    over the whole fp16 exponent range.  Codes must still equal exact
+    arithmetic (a row the fast path cannot decide is recomputed)."""
+    rng = np.random.default_rng(2024 + bits)
+    n = 1536
+    x = rng.standard_normal((n, D)) * 2.0 ** rng.integers(-24, 0, (n, D))
+    big = rng.integers(0, D, n)
+    x[np.arange(n), big] = rng.choice([-1.0, 1.0], n) * 2.0 ** rng.integers(0, 16, n) * rng.uniform(1, 1.99, n)
+    x[n // 2:] = rng.standard_normal((n - n // 2, D)) * 2.0 ** rng.integers(-14, 15, (n - n // 2, D))
+    x = np.clip(x, -65504, 65504).astype(np.float16).reshape(1, 2, n // 2, D)
+    cb = oracle_mod.rvq_codebooks(D, bits)[:4]
+    p1, p2, nr = _encode(vq, x, bits, cb)
+    ora = oracle_mod.rvq_encode(x.reshape(-1, D), bits, *cb)
+    check_rvq(p1, p2, nr, ora, bits)
+
+
 def test_encode_custom_codebook_boundary_at_rotated_value(vq, oracle_mod):
     """A boundary placed at fp32(1/sqrt(D)) (where x = e_0 rotates to) forces the
     exact path; its decision must follow exact arithmetic."""
