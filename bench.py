@@ -170,8 +170,9 @@ def build_workload(name, dev, rank=0, layers=None, batch=None, chunked=False, ch
                 api.vq_rvq_unpack_dequant(p1, p2, nr, bits, cb[0], cb[2], out=out, stream=stream)
         else:
             dec = None
-        # the library's b = 2 books are symmetric: their encoder is the tensor-core kernel
-        ekern = "rvq_encode_sym2_kernel" if bits == 2 else "rvq_encode_kernel"
+        # the library's books take the tensor-core encoders (b = 2: symmetric
+        # books, b = 4: the pair table)
+        ekern = {2: "rvq_encode_sym2_kernel", 4: "rvq_encode_pair4_kernel"}.get(bits, "rvq_encode_kernel")
         ops.append(Op(tag + "rvq_encode", ekern, enc, rvq_bytes(rows, bits), rows * D))
         if dec is not None:
             ops.append(Op(tag + "rvq_decode", "rvq_decode_kernel", dec, rvq_bytes(rows, bits), rows * D))

@@ -32,9 +32,10 @@
 //    band of a boundary; such rows are redone by the whole warp in exact /
 //    double-float arithmetic (rvq_fixup_row), so the packed words equal those
 //    of exact arithmetic.
-// Symmetric 4-level books (b = 2, the library's) have their own encoder,
-// rvq_encode_sym2_kernel: the same rings and exact recompute, the rotation on
-// the tensor cores and four lanes per row.
+// The library's books have encoders of their own, with the same rings and
+// exact recompute, the rotation on the tensor cores and four lanes per row:
+// rvq_encode_sym2_kernel for symmetric 4-level books (b = 2) and
+// rvq_encode_pair4_kernel for 16-level books with a pair table (b = 4).
 #include <cuda_fp16.h>
 
 #include "device_common.cuh"
@@ -66,7 +67,7 @@ __host__ __device__ constexpr int enc_pairs(int bits) { return 32 / bits > 8 ? 3
 __host__ __device__ constexpr int enc_warp_bytes(int bits, int mode)
 {
     return ENC_STAGES * (ENC_BLOCK + 8) +
-           (mode == MODE_SYM || mode == MODE_PAIR ? 0 : enc_pairs(bits) * 32 * 8 + 2 * 32 * (D * bits / 64 + 1) * 4);
+           (mode == MODE_SYM ? 0 : enc_pairs(bits) * 32 * 8 + 2 * 32 * (D * bits / 64 + 1) * 4);
 }
 // The table-driven quantizer reads its cell tables from shared memory,
 // replicated per lane (entry g of lane l at g * 32 + l: conflict-free): stage 1
@@ -75,7 +76,7 @@ __host__ __device__ constexpr int enc_warp_bytes(int bits, int mode)
 constexpr int ENC_TAB_BYTES = 32 * 32 * 16 + 32 * 32 * 8;
 __host__ __device__ constexpr int enc_tab_bytes(int mode)
 {
-    return mode == MODE_GRID ? ENC_TAB_BYTES : (mode == MODE_PAIR ? PT_CELLS * 8 : 0);
+    return mode == MODE_GRID ? ENC_TAB_BYTES : 0;
 }
 // sign masks of the randomised rotation (2 halves x 8 chunks x 16 B), padded so
 // that the TMA rings after them stay 1024-byte aligned (128-byte swizzle)
@@ -455,8 +456,9 @@ __global__ void __launch_bounds__(enc_warps(BITS, MODE) * 32, 1)
     constexpr bool ROLLED = MODE == MODE_GRID || MODE == MODE_PLAIN;
     constexpr int PP = enc_pairs(BITS);
     static_assert(!(MODE == MODE_SYM && BITS == 2), "symmetric b = 2 books: rvq_encode_sym2_kernel");
+    static_assert(MODE != MODE_PAIR, "the b = 4 pair table: rvq_encode_pair4_kernel");
     extern __shared__ __align__(128) unsigned char smem_raw[];
-    unsigned char *stab = smem_1k(smem_raw);       // cell tables (GRID), pair table (PAIR)
+    unsigned char *stab = smem_1k(smem_raw);       // cell tables (GRID)
     uint4 *ssg = reinterpret_cast<uint4 *>(stab + enc_tab_bytes(MODE));  // sign masks
     unsigned char *smem = stab + enc_tab_bytes(MODE) + ENC_SGN_BYTES;
     const int warp = threadIdx.x >> 5;
@@ -497,10 +499,6 @@ __global__ void __launch_bounds__(enc_warps(BITS, MODE) * 32, 1)
             t2s[i] = make_float2(p.t2.bnd[g], __int_as_float(p.t2.code[g]));
         }
         __syncthreads();
-    }
-    if constexpr (MODE == MODE_PAIR) {
-        uint2 *pt = reinterpret_cast<uint2 *>(stab);
-        for (int i = threadIdx.x; i < PT_CELLS; i += blockDim.x) pt[i] = p.pt.ent[i];
     }
     if (threadIdx.x < 16) {
         // chunk t & 7 (8 coordinates) of half t >> 3: coordinates 64 (t >> 3) + 8 (t & 7) ..
@@ -636,35 +634,7 @@ __global__ void __launch_bounds__(enc_warps(BITS, MODE) * 32, 1)
         // kx + WL/2 from the second ones.
         float mx = __int_as_float(0x7f800000), my = mx;
         uint32_t wa1[WL], wa2[WL];
-        if constexpr (MODE == MODE_PAIR) {
-            // 4-bit pair table, unrolled: the pairs of a word's 8 coordinates
-            // collect as bytes (even coordinates in b0, odd in b1, first at
-            // byte 0), then the low nibbles make the stage-1 word and the
-            // high nibbles the stage-2 word
-            const uint2 *ptab = reinterpret_cast<const uint2 *>(stab);
-            const float pa = p.pt.a, pbc = p.pt.bc;
-#pragma unroll
-            for (int kx = 0; kx < WL / 2; ++kx) {
-                uint32_t b0x = 0u, b1x = 0u, b0y = 0u, b1y = 0u;
-#pragma unroll
-                for (int i = 0; i < E; ++i) {
-                    const float2 y2 = v[kx * E + i];
-                    const uint32_t px = pair_code(y2.x, pa, pbc, ptab, mx);
-                    const uint32_t py = pair_code(y2.y, pa, pbc, ptab, my);
-                    if (i & 1) {
-                        b1x = __funnelshift_r(b1x, px, 8);
-                        b1y = __funnelshift_r(b1y, py, 8);
-                    } else {
-                        b0x = __funnelshift_r(b0x, px, 8);
-                        b0y = __funnelshift_r(b0y, py, 8);
-                    }
-                }
-                wa1[kx] = (b0x & 0x0F0F0F0Fu) | ((b1x & 0x0F0F0F0Fu) << 4);
-                wa2[kx] = ((b0x >> 4) & 0x0F0F0F0Fu) | (b1x & 0xF0F0F0F0u);
-                wa1[WL / 2 + kx] = (b0y & 0x0F0F0F0Fu) | ((b1y & 0x0F0F0F0Fu) << 4);
-                wa2[WL / 2 + kx] = ((b0y >> 4) & 0x0F0F0F0Fu) | (b1y & 0xF0F0F0F0u);
-            }
-        } else if constexpr (!ROLLED) {
+        if constexpr (!ROLLED) {
             // symmetric 1/2-bit books: unrolled, in registers
 #pragma unroll
             for (int kx = 0; kx < WL / 2; ++kx) {
@@ -761,7 +731,7 @@ __global__ void __launch_bounds__(enc_warps(BITS, MODE) * 32, 1)
         while (fl) {
             const int r = __ffs(fl) - 1;
             fl &= fl - 1;
-            rvq_fixup_row<BITS, GRID || MODE == MODE_PAIR>(p, sbuf, r, blk * ER + r, lane, tb1, tc1, tb2, tc2, tcen);
+            rvq_fixup_row<BITS, GRID>(p, sbuf, r, blk * ER + r, lane, tb1, tc1, tb2, tc2, tcen);
         }
         __syncwarp();
 
@@ -833,6 +803,100 @@ __device__ __forceinline__ SymRow sym2_row(float den, float g, float b1u, float 
     k.G1 = g * (k.bb + 2.0f * g);
     k.G2 = g * (k.be + 2.0f * g);
     return k;
+}
+
+// S = X H128 for rows g8 and g8 + 8 of a staged 16-row block: the A operands
+// from 16-byte reads of the swizzled rows (chunk a of a row holds
+// x[8a .. 8a + 7]) and one byte permute per register, X_b H16 for b = 0..7 as
+// 16x8x16 mma.sync with the permuted H16 columns in hb, the rows' sums of
+// squares (q0, q1) from the H16 outputs, then H8 as three butterfly stages
+// across b.  Afterwards acc[b'][nt][2r + e] = S at coordinate
+// 32 t4 + 16 nt + 8 e + b' of row g8 + 8r.
+template <bool SGN>
+__device__ __forceinline__ void tc_rotate_block(const unsigned char *sbuf, const uint4 *ssg, const uint32_t (&hb)[2][2],
+                                                int g8, int t4, float (&acc)[8][2][4], float &q0, float &q1)
+{
+    // ---- T_b = X_b H16 for b = 0..7 on the tensor cores
+    {
+        // u[r][j]: row g8 + 8r, chunk a = 2 t4 + {0, 1, 8, 9}[j]
+        uint4 u[2][4];
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int a = 2 * t4 + (j & 1) + 8 * (j >> 1);
+                u[r][j] = *reinterpret_cast<const uint4 *>(sbuf + (j >> 1) * (ENC_BLOCK / 2) + swz128(g8 + 8 * r, a & 7));
+                if constexpr (SGN) {
+                    const uint4 m = ssg[a];
+                    u[r][j] = make_uint4(u[r][j].x ^ m.x, u[r][j].y ^ m.y, u[r][j].z ^ m.z, u[r][j].w ^ m.w);
+                }
+            }
+        }
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+            const uint32_t sel = (b & 1) ? 0x7632u : 0x5410u;
+            auto word = [&](const uint4 &v) -> uint32_t {
+                return (b >> 1) == 0 ? v.x : (b >> 1) == 1 ? v.y : (b >> 1) == 2 ? v.z : v.w;
+            };
+            const uint32_t a0 = __byte_perm(word(u[0][0]), word(u[0][1]), sel);
+            const uint32_t a1 = __byte_perm(word(u[1][0]), word(u[1][1]), sel);
+            const uint32_t a2 = __byte_perm(word(u[0][2]), word(u[0][3]), sel);
+            const uint32_t a3 = __byte_perm(word(u[1][2]), word(u[1][3]), sel);
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                acc[b][nt][0] = acc[b][nt][1] = acc[b][nt][2] = acc[b][nt][3] = 0.0f;
+                mma_f16_16816(acc[b][nt], a0, a1, a2, a3, hb[nt][0], hb[nt][1]);
+            }
+        }
+    }
+
+    // ---- norms: the H16 outputs' squares sum to 16 sum x^2 (per row)
+    {
+        float2 s0 = make_float2(0.0f, 0.0f), s1 = s0;
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                const float2 v0 = make_float2(acc[b][nt][0], acc[b][nt][1]);
+                const float2 v1 = make_float2(acc[b][nt][2], acc[b][nt][3]);
+                s0 = __ffma2_rn(v0, v0, s0);
+                s1 = __ffma2_rn(v1, v1, s1);
+            }
+        }
+        q0 = s0.x + s0.y;
+        q1 = s1.x + s1.y;
+        q0 += __shfl_xor_sync(FULL_MASK, q0, 1);
+        q1 += __shfl_xor_sync(FULL_MASK, q1, 1);
+        q0 += __shfl_xor_sync(FULL_MASK, q0, 2);
+        q1 += __shfl_xor_sync(FULL_MASK, q1, 2);
+        q0 *= 0.0625f;
+        q1 *= 0.0625f;
+    }
+    // ---- H8 across b: acc[b'][nt] = S at coordinates 32 t4 + 16 nt + b' (.x / c2)
+    // and 32 t4 + 16 nt + 8 + b' (.y / c3)
+    const float2 neg1 = make_float2(-1.0f, -1.0f);
+#pragma unroll
+    for (int h = 1; h < 8; h <<= 1) {
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+            if ((b & h) == 0) {
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+                    for (int r = 0; r < 2; ++r) {
+                        const float2 x = make_float2(acc[b][nt][2 * r], acc[b][nt][2 * r + 1]);
+                        const float2 y = make_float2(acc[b + h][nt][2 * r], acc[b + h][nt][2 * r + 1]);
+                        const float2 sum = __fadd2_rn(x, y);
+                        const float2 dif = __ffma2_rn(y, neg1, x);
+                        acc[b][nt][2 * r] = sum.x;
+                        acc[b][nt][2 * r + 1] = sum.y;
+                        acc[b + h][nt][2 * r] = dif.x;
+                        acc[b + h][nt][2 * r + 1] = dif.y;
+                    }
+                }
+            }
+        }
+    }
 }
 
 template <bool SGN>
@@ -917,92 +981,11 @@ __global__ void __launch_bounds__(S2_WARPS * 32, 1) rvq_encode_sym2_kernel(const
         }
         const unsigned char *sbuf = ring + s * ENC_BLOCK;
 
-        // ---- T_b = X_b H16 for b = 0..7 on the tensor cores
         float acc[8][2][4];
-        {
-            // u[r][j]: row g8 + 8r, chunk a = 2 t4 + {0, 1, 8, 9}[j]
-            uint4 u[2][4];
-#pragma unroll
-            for (int r = 0; r < 2; ++r) {
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int a = 2 * t4 + (j & 1) + 8 * (j >> 1);
-                    u[r][j] = *reinterpret_cast<const uint4 *>(sbuf + (j >> 1) * (ENC_BLOCK / 2) + swz128(g8 + 8 * r, a & 7));
-                    if constexpr (SGN) {
-                        const uint4 m = ssg[a];
-                        u[r][j] = make_uint4(u[r][j].x ^ m.x, u[r][j].y ^ m.y, u[r][j].z ^ m.z, u[r][j].w ^ m.w);
-                    }
-                }
-            }
-#pragma unroll
-            for (int b = 0; b < 8; ++b) {
-                const uint32_t sel = (b & 1) ? 0x7632u : 0x5410u;
-                auto word = [&](const uint4 &v) -> uint32_t {
-                    return (b >> 1) == 0 ? v.x : (b >> 1) == 1 ? v.y : (b >> 1) == 2 ? v.z : v.w;
-                };
-                const uint32_t a0 = __byte_perm(word(u[0][0]), word(u[0][1]), sel);
-                const uint32_t a1 = __byte_perm(word(u[1][0]), word(u[1][1]), sel);
-                const uint32_t a2 = __byte_perm(word(u[0][2]), word(u[0][3]), sel);
-                const uint32_t a3 = __byte_perm(word(u[1][2]), word(u[1][3]), sel);
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {
-                    acc[b][nt][0] = acc[b][nt][1] = acc[b][nt][2] = acc[b][nt][3] = 0.0f;
-                    mma_f16_16816(acc[b][nt], a0, a1, a2, a3, hb[nt][0], hb[nt][1]);
-                }
-            }
-        }
-
-        // ---- norms: the H16 outputs' squares sum to 16 sum x^2 (per row)
         float q0, q1;
-        {
-            float2 s0 = make_float2(0.0f, 0.0f), s1 = s0;
-#pragma unroll
-            for (int b = 0; b < 8; ++b) {
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {
-                    const float2 v0 = make_float2(acc[b][nt][0], acc[b][nt][1]);
-                    const float2 v1 = make_float2(acc[b][nt][2], acc[b][nt][3]);
-                    s0 = __ffma2_rn(v0, v0, s0);
-                    s1 = __ffma2_rn(v1, v1, s1);
-                }
-            }
-            q0 = s0.x + s0.y;
-            q1 = s1.x + s1.y;
-            q0 += __shfl_xor_sync(FULL_MASK, q0, 1);
-            q1 += __shfl_xor_sync(FULL_MASK, q1, 1);
-            q0 += __shfl_xor_sync(FULL_MASK, q0, 2);
-            q1 += __shfl_xor_sync(FULL_MASK, q1, 2);
-            q0 *= 0.0625f;
-            q1 *= 0.0625f;
-        }
+        tc_rotate_block<SGN>(sbuf, ssg, hb, g8, t4, acc, q0, q1);
         const float n0 = __fsqrt_rn(q0), n1 = __fsqrt_rn(q1);
         const float den0 = n0 * SQRT_D_HI, den1 = n1 * SQRT_D_HI;
-
-        // ---- H8 across b: acc[b'][nt] = S at coordinates 32 t4 + 16 nt + b' (.x / c2)
-        // and 32 t4 + 16 nt + 8 + b' (.y / c3)
-        const float2 neg1 = make_float2(-1.0f, -1.0f);
-#pragma unroll
-        for (int h = 1; h < 8; h <<= 1) {
-#pragma unroll
-            for (int b = 0; b < 8; ++b) {
-                if ((b & h) == 0) {
-#pragma unroll
-                    for (int nt = 0; nt < 2; ++nt) {
-#pragma unroll
-                        for (int r = 0; r < 2; ++r) {
-                            const float2 x = make_float2(acc[b][nt][2 * r], acc[b][nt][2 * r + 1]);
-                            const float2 y = make_float2(acc[b + h][nt][2 * r], acc[b + h][nt][2 * r + 1]);
-                            const float2 sum = __fadd2_rn(x, y);
-                            const float2 dif = __ffma2_rn(y, neg1, x);
-                            acc[b][nt][2 * r] = sum.x;
-                            acc[b][nt][2 * r + 1] = sum.y;
-                            acc[b + h][nt][2 * r] = dif.x;
-                            acc[b + h][nt][2 * r + 1] = dif.y;
-                        }
-                    }
-                }
-            }
-        }
 
         // ---- quantize: word 2 t4 + nt of row g8 + 8r gets b' = 0..7 of .x at
         // positions 0..7 and of .y at positions 8..15
@@ -1057,6 +1040,183 @@ __global__ void __launch_bounds__(S2_WARPS * 32, 1) rvq_encode_sym2_kernel(const
             fl &= fl - 1;
             const int r = (bit >> 2) + 8 * (bit & 1);
             rvq_fixup_row<2, false>(p, sbuf, r, blk * ER + r, lane, tb1, tc1, tb2, tc2, tcen);
+        }
+        __syncwarp();
+
+        fence_proxy_async_smem();
+        {
+            const int nb = blk + S2_STAGES * tw;
+            if (nb < nblk) issue(nb, s);
+        }
+        if (++s == S2_STAGES) {
+            s = 0;
+            ph ^= 1u;
+        }
+    }
+}
+
+// ------------------------------------------- encode, b = 4 pair table, tensor cores
+//
+// The rotation of rvq_encode_sym2_kernel (tc_rotate_block) with the
+// 16-level quantizer of the pair table (pair_code, PairTable in launch.h): y =
+// S / (n sqrt(D)), one cell lookup per coordinate gives both codes.  After
+// the rotation acc[b'][nt][2r + e], b' = 0..7, are the eight coordinates of
+// word 4 t4 + 2 nt + e of row g8 + 8r, so each lane packs and stores four
+// whole words per row and stream.  Rows with a value inside the guard band go
+// to rvq_fixup_row.
+constexpr int P4_TAB_BYTES = PT_CELLS * 8;
+
+template <bool SGN>
+__global__ void __launch_bounds__(S2_WARPS * 32, 1) rvq_encode_pair4_kernel(const __grid_constant__ RvqEncodeParams p)
+{
+    constexpr int W = D * 4 / 32;  // 16 words per row and stream
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    unsigned char *base = smem_1k(smem_raw);
+    uint4 *ssg = reinterpret_cast<uint4 *>(base);  // sign masks: chunk a = coordinates 8a .. 8a + 7
+    uint2 *ptab = reinterpret_cast<uint2 *>(base + ENC_SGN_BYTES);
+    unsigned char *smem = base + ENC_SGN_BYTES + P4_TAB_BYTES;  // 1024-byte aligned
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int g8 = lane >> 2, t4 = lane & 3;
+    unsigned char *ring = smem + warp * (S2_STAGES * ENC_BLOCK);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S2_WARPS * S2_STAGES * ENC_BLOCK) + warp * S2_STAGES;
+
+    if (lane == 0) {
+#pragma unroll
+        for (int s = 0; s < S2_STAGES; ++s) mbar_init(&bars[s], 1);
+        fence_mbar_init();
+    }
+    if (threadIdx.x < 16) {
+        const int c0 = 8 * threadIdx.x;
+        ssg[threadIdx.x] = make_uint4(half2_sign_mask(sign_pair(p.sgn, c0)), half2_sign_mask(sign_pair(p.sgn, c0 + 2)),
+                                      half2_sign_mask(sign_pair(p.sgn, c0 + 4)), half2_sign_mask(sign_pair(p.sgn, c0 + 6)));
+    }
+    for (int i = threadIdx.x; i < PT_CELLS; i += blockDim.x) ptab[i] = p.pt.ent[i];
+    __syncthreads();
+
+    const uint64_t pol = l2_policy_evict_first();
+    // shuffle tables of the exact recompute
+    const float tb1 = p.t1.bnd[lane];
+    const int tc1 = p.t1.code[lane];
+    const float tb2 = p.t2.bnd[lane];
+    const int tc2 = p.t2.code[lane];
+    const float tcen = p.c1[lane & 15];
+    const float pa = p.pt.a, pbc = p.pt.bc;
+    uint32_t hb[2][2];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+        const int ap = 4 * (g8 >> 1) + 2 * nt + (g8 & 1);
+        hb[nt][0] = h16_pair(2 * t4, ap);
+        hb[nt][1] = h16_pair(2 * t4 + 8, ap);
+    }
+
+    const int nblk = (p.N + ER - 1) / ER;
+    const int gw = blockIdx.x * S2_WARPS + warp;
+    const int tw = gridDim.x * S2_WARPS;
+    // destination row = source row (no batch offsets, same capacity)
+    const bool dense = p.dst_off == nullptr && p.S_dst == p.S;
+    auto issue = [&](int blk, int s) {
+        if (lane == 0) {
+            mbar_arrive_expect_tx(&bars[s], (uint32_t)ENC_BLOCK);
+            tma_load_2d(ring + s * ENC_BLOCK, &p.tmap, 0, blk * ER, &bars[s], pol);
+            tma_load_2d(ring + s * ENC_BLOCK + ENC_BLOCK / 2, &p.tmap, 64, blk * ER, &bars[s], pol);
+        }
+    };
+#pragma unroll
+    for (int s = 0; s < S2_STAGES; ++s) {
+        const int blk = gw + s * tw;
+        if (blk < nblk) issue(blk, s);
+    }
+
+    int s = 0;
+    uint32_t ph = 0;
+    for (int it = 0;; ++it) {
+        const int blk = gw + it * tw;
+        if (blk >= nblk) break;
+        const bool ok = mbar_wait_bounded(&bars[s], ph);
+        if (!__all_sync(FULL_MASK, ok)) {
+            if (lane == 0) atomicOr(&g_rvq_err, (unsigned)VQ_DEVERR_WAIT_TIMEOUT);
+            for (int k = 1; k < S2_STAGES; ++k) {
+                const int it2 = it + k;
+                if (gw + it2 * tw < nblk)
+                    (void)mbar_wait_bounded(&bars[it2 % S2_STAGES], (uint32_t)(it2 / S2_STAGES) & 1u);
+            }
+            return;
+        }
+        const unsigned char *sbuf = ring + s * ENC_BLOCK;
+
+        float acc[8][2][4];
+        float q0, q1;
+        tc_rotate_block<SGN>(sbuf, ssg, hb, g8, t4, acc, q0, q1);
+        const float n0 = __fsqrt_rn(q0), n1 = __fsqrt_rn(q1);
+        const float inv0 = q0 > 0.0f ? __frcp_rn(n0 * SQRT_D_HI) : 0.0f;
+        const float inv1 = q1 > 0.0f ? __frcp_rn(n1 * SQRT_D_HI) : 0.0f;
+
+        // ---- quantize: word 2 nt + e of the lane (word 4 t4 + 2 nt + e of the
+        // row) from b' = 0..7 of acc[.][nt][2r + e]; the pairs i1 | i2 << 4 of
+        // even coordinates collect in b0, of odd ones in b1 (first at byte 0),
+        // then the low nibbles make the stage-1 word and the high nibbles the
+        // stage-2 word
+        float m0 = __int_as_float(0x7f800000), m1 = m0;
+        uint32_t w1[2][4], w2[2][4];
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            const float2 inv2 = r ? make_float2(inv1, inv1) : make_float2(inv0, inv0);
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                uint32_t b0[2] = {0u, 0u}, b1[2] = {0u, 0u};
+#pragma unroll
+                for (int b = 0; b < 8; ++b) {
+                    const float2 y2 = __fmul2_rn(make_float2(acc[b][nt][2 * r], acc[b][nt][2 * r + 1]), inv2);
+                    const uint32_t px = pair_code(y2.x, pa, pbc, ptab, r ? m1 : m0);
+                    const uint32_t py = pair_code(y2.y, pa, pbc, ptab, r ? m1 : m0);
+                    if (b & 1) {
+                        b1[0] = __funnelshift_r(b1[0], px, 8);
+                        b1[1] = __funnelshift_r(b1[1], py, 8);
+                    } else {
+                        b0[0] = __funnelshift_r(b0[0], px, 8);
+                        b0[1] = __funnelshift_r(b0[1], py, 8);
+                    }
+                }
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    w1[r][2 * nt + e] = (b0[e] & 0x0F0F0F0Fu) | ((b1[e] & 0x0F0F0F0Fu) << 4);
+                    w2[r][2 * nt + e] = ((b0[e] >> 4) & 0x0F0F0F0Fu) | (b1[e] & 0xF0F0F0F0u);
+                }
+            }
+        }
+
+        // ---- guard band: a row is flagged if any of its four lanes saw a value
+        // inside the band (and always when it is zero)
+        const int row0 = blk * ER + g8, row1 = row0 + 8;
+        const bool valid0 = row0 < p.N, valid1 = row1 < p.N;
+        const bool f0 = valid0 && (!(m0 >= p.guard) || !(q0 > 0.0f));
+        const bool f1 = valid1 && (!(m1 >= p.guard) || !(q1 > 0.0f));
+        int f = (f0 ? 1 : 0) | (f1 ? 2 : 0);
+        f |= __shfl_xor_sync(FULL_MASK, f, 1);
+        f |= __shfl_xor_sync(FULL_MASK, f, 2);
+
+        // ---- fast words: 16 bytes per lane, row and stream (a block's 16 rows
+        // are contiguous in both streams)
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            const int row = r ? row1 : row0;
+            size_t drow = (size_t)row;
+            if ((r ? valid1 : valid0) && !(f & (1 << r)) && (dense || rvq_dst_row(p, row, drow))) {
+                *reinterpret_cast<uint4 *>(p.p1 + drow * W + 4 * t4) = make_uint4(w1[r][0], w1[r][1], w1[r][2], w1[r][3]);
+                *reinterpret_cast<uint4 *>(p.p2 + drow * W + 4 * t4) = make_uint4(w2[r][0], w2[r][1], w2[r][2], w2[r][3]);
+                if (t4 == 0) p.norms[drow] = r ? n1 : n0;
+            }
+        }
+
+        // ---- flagged rows: exact recompute by the warp
+        unsigned fl = (__ballot_sync(FULL_MASK, (f & 1) != 0) & 0x11111111u) |
+                      ((__ballot_sync(FULL_MASK, (f & 2) != 0) & 0x11111111u) << 1);
+        while (fl) {
+            const int bit = __ffs(fl) - 1;
+            fl &= fl - 1;
+            const int r = (bit >> 2) + 8 * (bit & 1);
+            rvq_fixup_row<4, true>(p, sbuf, r, blk * ER + r, lane, tb1, tc1, tb2, tc2, tcen);
         }
         __syncwarp();
 
@@ -1349,7 +1509,8 @@ cudaError_t launch_enc(const RvqEncodeParams &p0, cudaStream_t stream)
 constexpr int S2_SMEM = 1024 + ENC_SGN_BYTES + S2_WARPS * S2_STAGES * (ENC_BLOCK + 8);
 static_assert(S2_SMEM <= SMEM_MAX, "symmetric encoder shared memory");
 
-cudaError_t launch_enc_sym2(const RvqEncodeParams &p0, cudaStream_t stream)
+// Launch of the tensor-core encoders: one persistent 16-warp CTA per SM.
+cudaError_t launch_enc_tc(const RvqEncodeParams &p0, void (*kern)(RvqEncodeParams), int smem, cudaStream_t stream)
 {
     RvqEncodeParams p = p0;
     p.divS = make_fastdiv((uint32_t)p.S);
@@ -1360,16 +1521,29 @@ cudaError_t launch_enc_sym2(const RvqEncodeParams &p0, cudaStream_t stream)
         const uint32_t box[2] = {64u, (uint32_t)ER};
         if (!encode_tmap_f16(&p.tmap, p.x, 2, dims, strides, box, true, true)) return cudaErrorInvalidValue;
     }
-    auto kern = p.has_sgn ? rvq_encode_sym2_kernel<true> : rvq_encode_sym2_kernel<false>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S2_SMEM);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     const int nblk = (p.N + ER - 1) / ER;
     int grid = (nblk + S2_WARPS - 1) / S2_WARPS;
     const int sms = sm_count();
     if (grid > sms) grid = sms;
     if (grid < 1) grid = 1;
-    kern<<<grid, S2_WARPS * 32, S2_SMEM, stream>>>(p);
+    kern<<<grid, S2_WARPS * 32, smem, stream>>>(p);
     return cudaGetLastError();
+}
+
+cudaError_t launch_enc_sym2(const RvqEncodeParams &p, cudaStream_t stream)
+{
+    return launch_enc_tc(p, p.has_sgn ? rvq_encode_sym2_kernel<true> : rvq_encode_sym2_kernel<false>, S2_SMEM, stream);
+}
+
+// Shared memory of the b = 4 tensor-core encoder: the same plus the pair table.
+constexpr int P4_SMEM = S2_SMEM + P4_TAB_BYTES;
+static_assert(P4_SMEM <= SMEM_MAX, "b = 4 encoder shared memory");
+
+cudaError_t launch_enc_pair4(const RvqEncodeParams &p, cudaStream_t stream)
+{
+    return launch_enc_tc(p, p.has_sgn ? rvq_encode_pair4_kernel<true> : rvq_encode_pair4_kernel<false>, P4_SMEM, stream);
 }
 
 template <int BITS>
@@ -1409,7 +1583,7 @@ cudaError_t launch_rvq_encode(const RvqEncodeParams &p, int bits, int mode, cuda
     case 2 * 4 + MODE_SYM: return launch_enc_sym2(p, stream);
     case 4 * 4 + MODE_PLAIN: return launch_enc<4, MODE_PLAIN>(p, stream);
     case 4 * 4 + MODE_GRID: return launch_enc<4, MODE_GRID>(p, stream);
-    case 4 * 4 + MODE_PAIR: return launch_enc<4, MODE_PAIR>(p, stream);
+    case 4 * 4 + MODE_PAIR: return launch_enc_pair4(p, stream);
     default: return cudaErrorInvalidValue;
     }
 }
