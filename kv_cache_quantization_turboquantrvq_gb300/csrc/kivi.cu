@@ -218,8 +218,8 @@ __device__ __noinline__ uint32_t code_exact(__half h, const GroupQ g, float mx)
 
 constexpr int ROW_BYTES = D * 2;
 constexpr int ROW_STRIDE = ROW_BYTES + 16;
-constexpr int VAL_WARPS = 16;
-constexpr int VAL_STAGES = 3;
+constexpr int VAL_WARPS = 20;
+constexpr int VAL_STAGES = 2;
 constexpr int VROWS = 16;
 constexpr int VSTAGE_BYTES = VROWS * ROW_BYTES;  // two 2 KB swizzled boxes
 __host__ __device__ constexpr int val_smem() { return 1024 + VAL_WARPS * VAL_STAGES * (VSTAGE_BYTES + 8); }
