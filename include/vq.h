@@ -169,8 +169,9 @@ vq_status vq_rvq_attend(const void *q_f16, const uint32_t *packed1, const uint32
  * library for callers that cannot hand over device memory (for example, a
  * captured graph whose allocations are fixed).  The per-chunk partial
  * results go to a scratch array that the library itself holds in device
- * memory, one per device, VQ_ATTEND_SCRATCH_BYTES long; its address is looked
- * up once per device on first use.  Same arguments, computation and results
+ * memory, one per device, VQ_ATTEND_SCRATCH_BYTES long; each call looks up
+ * its address on the current device (the first call on a device also loads
+ * the library's device code there, so make it before any stream capture).  Same arguments, computation and results
  * as vq_rvq_attend with a workspace of the size vq_rvq_attend_workspace
  * reports (the same chunking, so the output is bit-identical).
  *   Size limit: when that chunking needs more than VQ_ATTEND_SCRATCH_BYTES of

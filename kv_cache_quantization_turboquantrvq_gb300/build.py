@@ -64,7 +64,7 @@ def build(force: bool = False, verbose_ptxas: bool = False) -> str:
     with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(lambda s: _compile(s, verbose_ptxas), SOURCES))
     tmp = LIB + ".tmp.%d" % os.getpid()
-    cmd = [nvcc(), "-shared", "-o", tmp] + objs + ARCH + ["-lcudart_static" if False else "-cudart=static"]
+    cmd = [nvcc(), "-shared", "-o", tmp] + objs + ARCH + ["-cudart=static"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError("link failed:\n%s\n%s" % (r.stdout, r.stderr))

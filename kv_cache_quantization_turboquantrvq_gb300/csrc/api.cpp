@@ -90,13 +90,11 @@ void set_signs(P &p, const uint32_t *signs)
 
 int sm_count()
 {
-    static int cache[64] = {0};
-    int dev = 0;
+    // queried on every call (an attribute read, no synchronisation), so the
+    // value always belongs to the device that is current now
+    int dev = 0, n = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 148;
-    if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
-    int n = 0;
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
-    if (dev >= 0 && dev < 64) cache[dev] = n;
     return n;
 }
 

@@ -33,7 +33,6 @@
 // carries scale * log2(e)).
 #include <cuda_fp16.h>
 
-#include <mutex>
 
 #include "device_common.cuh"
 #include "launch.h"
@@ -605,19 +604,13 @@ cudaError_t launch_rvq_attend(const RvqAttendParams &p, int bits, cudaStream_t s
 
 cudaError_t attend_static_scratch(void **ptr, size_t *bytes)
 {
-    // the symbol's device address, looked up once per device
-    static std::mutex mu;
-    static void *addr[64] = {nullptr};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    // The symbol's device address on the current device, looked up on every
+    // call (a table lookup once the module is loaded): a cached address would
+    // outlive a cudaDeviceReset, after which the array lives elsewhere.
+    void *addr = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&addr, g_at_scratch);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    std::lock_guard<std::mutex> lock(mu);
-    if (addr[dev] == nullptr) {
-        e = cudaGetSymbolAddress(&addr[dev], g_at_scratch);
-        if (e != cudaSuccess) return e;
-    }
-    *ptr = addr[dev];
+    *ptr = addr;
     *bytes = sizeof(g_at_scratch);
     return cudaSuccess;
 }

@@ -204,7 +204,7 @@ int pair_cell_host(float v, float a, float bc);
 bool build_pair_table(const float *c1, const float *b1, const float *c2, const float *b2, int bits,
                       float guard, PairTable &t);
 
-// Number of SMs of the current device (cached per device).
+// Number of SMs of the current device.
 int sm_count();
 
 // Tiled tensor map of an fp16 tensor: dims innermost first, strides in bytes

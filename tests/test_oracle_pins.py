@@ -497,3 +497,110 @@ def test_three_bit_words_leave_the_top_bits_clear(oracle_mod):
     # a row of D = 128 codes takes 13 words, the last holding 8 codes
     w = oracle_mod.pack_lsb_first(np.full(128, 7, np.uint8), 3)
     assert len(w) == 13 and w[-1] == (1 << 24) - 1
+
+
+# ---------------------------------------------------------------- tie-band edges
+#
+# The tie flags decide which GPU mismatches the parity rule forgives, so the
+# band's width, its strictness and its units are pinned from both sides: a
+# value 0.9 band from a boundary (or a rounding tie) is flagged, one 1.1 band
+# away is not.  Distances are checked with exact arithmetic first, so the
+# fixtures themselves cannot drift.
+
+RVQ_BAND = 1e-5
+KIVI_BAND = 1e-4
+
+
+def _e0_row():
+    x = np.zeros((1, 128), np.float16)
+    x[0, 0] = 1.0  # rotates to the constant 1/sqrt(128)
+    return x
+
+
+@pytest.mark.parametrize("frac", [0.9, -0.9, 1.1, -1.1])
+def test_rvq_tie_band_edge_stage1(oracle_mod, frac):
+    """A stage-1 boundary at y0 + frac * band (y0 = the rotated value of e_0):
+    flagged at |frac| = 0.9, not at 1.1, and a stage-1 flag also flags the
+    stage-2 code (its input depends on the stage-1 decision)."""
+    bits = 2
+    _, _, c2, b2, _ = oracle_mod.rvq_codebooks(128, bits)
+    y0 = 1 / np.sqrt(128.0)
+    b1 = np.array([-0.3, y0 + frac * RVQ_BAND, 0.3], np.float32)
+    c1 = np.array([-0.5, 0.0, 0.2, 0.5], np.float32)
+    out = oracle_mod.rvq_encode(_e0_row(), bits, c1, b1, c2, b2, want_values=True)
+    y = out["y"][0]
+    dist = np.abs(y - np.float64(b1[1]))
+    assert np.all(np.abs(dist / RVQ_BAND - abs(frac)) < 0.01)  # fixture check
+    # the residual is far from every stage-2 boundary: only propagation can flag it
+    assert np.min(np.abs(out["r"][0][:, None] - b2.astype(np.float64)[None, :])) > 100 * RVQ_BAND
+    flagged = abs(frac) < 1
+    assert np.all(out["tie1"] == flagged)
+    assert np.all(out["tie2"] == flagged)
+    assert np.all(out["idx1"] == (1 if frac > 0 else 2))
+
+
+@pytest.mark.parametrize("frac", [0.9, -0.9, 1.1, -1.1])
+def test_rvq_tie_band_edge_stage2(oracle_mod, frac):
+    """The residual r = y0 - c1[i1] placed frac * band from a stage-2 boundary,
+    with y0 far from every stage-1 boundary: only tie2 follows the band."""
+    bits = 2
+    _, _, c2, b2, _ = oracle_mod.rvq_codebooks(128, bits)
+    y0 = 1 / np.sqrt(128.0)
+    target = np.float64(b2[2]) + frac * RVQ_BAND  # r = y0 - c  ->  c = y0 - target
+    c1 = np.array([-0.5, -0.1, y0 - target, 0.5], np.float32)
+    b1 = np.array([-0.3, 0.0, 0.3], np.float32)
+    out = oracle_mod.rvq_encode(_e0_row(), bits, c1, b1, c2, b2, want_values=True)
+    assert np.all(out["idx1"] == 2)
+    r = out["r"][0]
+    assert np.allclose(r, out["y"][0] - np.float64(c1[2]), rtol=0, atol=1e-17)
+    assert np.all(np.abs(np.abs(r - np.float64(b2[2])) / RVQ_BAND - abs(frac)) < 0.01)
+    flagged = abs(frac) < 1
+    assert np.all(out["tie1"] == 0)
+    assert np.all(out["tie2"] == flagged)
+    assert np.all(out["idx2"] == (3 if frac > 0 else 2))
+
+
+# (min, probe, max) fp16 groups whose exact t = (probe - min) (2^b - 1) / (max - min)
+# lies the stated distance from a rounding tie k + 1/2; "big" groups have a
+# scale near 667 (b = 2) or 133 (b = 4), "small" ones near 7e-4, so a flag
+# measured in x units instead of t units would flip one of each pair.
+KIVI_EDGES = [
+    # bits, regime, frac of band, (min, probe, max)
+    (2, "big", 0.9, (-0.11883544921875, 1000.0, 2000.0)),
+    (2, "big", 1.1, (-0.145263671875, 1000.0, 2000.0)),
+    (2, "small", 0.9, (-1.1920928955078125e-07, 0.0010004043579101562, 0.0020008087158203125)),
+    (2, "small", 1.1, (-1.7881393432617188e-07, 0.0012073516845703125, 0.002414703369140625)),
+    (4, "big", 0.9, (-0.023773193359375, 1000.0, 2000.0)),
+    (4, "big", 1.1, (-0.029052734375, 1000.0, 2000.0)),
+]
+
+
+@pytest.mark.parametrize("per_channel", [True, False])
+@pytest.mark.parametrize("bits,regime,frac,grp", KIVI_EDGES)
+def test_kivi_tie_band_edge(oracle_mod, bits, regime, frac, grp, per_channel):
+    mn, probe, mx = grp
+    levels = (1 << bits) - 1
+    t = Fraction(levels) * (Fraction(probe) - Fraction(mn)) / (Fraction(mx) - Fraction(mn))
+    d = abs(t - (t.numerator // t.denominator) - Fraction(1, 2))
+    assert abs(float(d) / KIVI_BAND - frac) < 0.02  # fixture check (exact arithmetic)
+    G = 32
+    # one group: min, max, the probe, the rest at the min (t = 0, far from a tie)
+    g = np.full(G, mn, np.float64)
+    g[1], g[2] = mx, probe
+    g = g.astype(np.float16)
+    assert [float(v) for v in g[:3]] == [mn, mx, probe]  # all exact in fp16
+    if per_channel:
+        x = np.zeros((1, 1, G, 128), np.float16)
+        x[0, 0, :, 7] = g
+        o = oracle_mod.kivi_quant(x, bits, G, 0, per_channel=True)
+        tie = o["tie"][0, :, 7]
+        code = o["codes"][0, 2, 7]
+    else:
+        x = np.zeros((1, 1, 1, 128), np.float16)
+        x[0, 0, 0, 32:64] = g
+        o = oracle_mod.kivi_quant(x, bits, G, 0, per_channel=False)
+        tie = o["tie"][0, 0, 32:64]
+        code = o["codes"][0, 0, 34]
+    assert tie[2] == (1 if frac < 1 else 0)
+    assert not tie[[0, 1]].any() and not tie[3:].any()
+    assert code == round(t)  # Python round of a Fraction: nearest (not a tie here)
