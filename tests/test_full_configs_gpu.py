@@ -99,12 +99,13 @@ def test_c4_every_sequence(vq, oracle_mod, pool):
         P1, P2, N = _host(p1), _host(p2), _host(nr)
         tasks = [dict(x=k[b].reshape(-1, D), p1=P1[b, :, off[b]:off[b] + S], p2=P2[b, :, off[b]:off[b] + S],
                       norms=N[b, :, off[b]:off[b] + S], dec=None, bits=bits, cb=cb) for b in range(B)]
+        st = fp.merge(pool.map(fp.rvq_slice, tasks))
+        # (the tasks hold views of the outputs: blank the windows only now)
         for b in range(B):
             P1[b, :, off[b]:off[b] + S] = sentinel
             P2[b, :, off[b]:off[b] + S] = sentinel
             N[b, :, off[b]:off[b] + S] = -1.0
         assert np.all(P1 == sentinel) and np.all(P2 == sentinel) and np.all(N == -1.0)
-        st = fp.merge(pool.map(fp.rvq_slice, tasks))
         reports.append(fp.assert_rule(st, ["s1_", "s2_"], "C4 RVQ b=%d" % bits))
         del p1, p2, nr
     for bits in cfg["kivi_bits"]:
