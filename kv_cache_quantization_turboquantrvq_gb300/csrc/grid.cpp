@@ -178,21 +178,21 @@ bool build_pair_table(const float *c1, const float *b1, const float *c2, const f
     }
     const double span = (double)bnd[nb - 1] - (double)bnd[0];
     std::vector<int> cell(nb);
-    for (int trial = 0; trial < 48; ++trial) {
-        for (int ph = 0; ph < 8; ++ph) {
+    for (int trial = 0; trial < 64; ++trial) {
+        for (int ph = 0; ph < 16; ++ph) {
             const double pad = span * (2.0 / (PT_CELLS - 1) + 0.0013 * trial);
             const double width = span + 2.0 * pad;
-            const double phase = (0.5 + 0.37 * ph) / (PT_CELLS - 1);
+            const double phase = (0.5 + 0.0613 * ph) / (PT_CELLS - 1);
             t.a = (float)(1.0 / width);
             t.bc = (float)(-((double)bnd[0] - pad) / width + phase - 0.5 / (PT_CELLS - 1));
             bool ok = true;
             for (int i = 0; i < nb && ok; ++i) {
                 cell[i] = pair_cell_host(bnd[i], t.a, t.bc);
-                // own cell, and every fp32 value within the guard band of the
-                // boundary in that same cell (the map is monotone)
+                // own cell, and every fp32 value within three guard bands of
+                // the boundary in that same cell (the map is monotone)
                 if (i > 0 && cell[i] <= cell[i - 1]) ok = false;
-                if (pair_cell_host(f32_down((double)bnd[i] - guard), t.a, t.bc) != cell[i] ||
-                    pair_cell_host(f32_up((double)bnd[i] + guard), t.a, t.bc) != cell[i])
+                if (pair_cell_host(f32_down((double)bnd[i] - 3.0 * guard), t.a, t.bc) != cell[i] ||
+                    pair_cell_host(f32_up((double)bnd[i] + 3.0 * guard), t.a, t.bc) != cell[i])
                     ok = false;
             }
             if (!ok) continue;

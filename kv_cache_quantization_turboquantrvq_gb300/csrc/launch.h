@@ -27,10 +27,12 @@ struct GridTable {
 // stage-1 cell k, the stage-2 boundaries shifted by c1[k] (i2 counts
 // y - c1[k] > b2_j, i.e. y > c1[k] + b2_j).  The device maps y to one of
 // PT_CELLS cells, g(v) = RN((PT_CELLS - 1) sat(fma(v, a, bc))); a table is
-// accepted when every boundary has a cell of its own and lies at least the
-// guard band away from that cell's edges.  Entry g: the boundary in the cell
-// (-inf if none) and the pairs below / above it, i1 | i2 << 4, in bytes 0 / 1.
-constexpr int PT_CELLS = 1024;
+// accepted when every boundary has a cell of its own and every value within
+// three guard bands of it maps to that same cell (the encoder evaluates the
+// map on the unnormalised transform with a per-row slope, whose rounding the
+// extra bands absorb).  Entry g: the boundary in the cell (-inf if none) and
+// the pairs below / above it, i1 | i2 << 4, in bytes 0 / 1.
+constexpr int PT_CELLS = 512;
 struct PairTable {
     float a, bc;
     uint2 ent[PT_CELLS];  // x: boundary (fp32 bits), y: pairs

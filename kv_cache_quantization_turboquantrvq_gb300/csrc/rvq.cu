@@ -1058,13 +1058,43 @@ __global__ void __launch_bounds__(S2_WARPS * 32, 1) rvq_encode_sym2_kernel(const
 // ------------------------------------------- encode, b = 4 pair table, tensor cores
 //
 // The rotation of rvq_encode_sym2_kernel (tc_rotate_block) with the
-// 16-level quantizer of the pair table (pair_code, PairTable in launch.h): y =
-// S / (n sqrt(D)), one cell lookup per coordinate gives both codes.  After
-// the rotation acc[b'][nt][2r + e], b' = 0..7, are the eight coordinates of
-// word 4 t4 + 2 nt + e of row g8 + 8r, so each lane packs and stores four
-// whole words per row and stream.  Rows with a value inside the guard band go
-// to rvq_fixup_row.
-constexpr int P4_TAB_BYTES = PT_CELLS * 8;
+// 16-level quantizer of the pair table (PairTable in launch.h): one cell
+// lookup per coordinate gives both codes.  The table lives in shared memory
+// replicated P4_REP = 16 times (cell g, replica j at byte (16 g + j) 8) and
+// lane l reads replica l & 15: an 8-byte read is served per half-warp, so the
+// 16 lanes of each half always hit 16 distinct bank pairs and the lookup is
+// free of bank conflicts.  The quantizer works on S = H x directly: with
+// den = n sqrt(D), y > bnd exactly when bnd den - S is negative (one FMA
+// rounding of an exact product-difference), the cell coordinate is
+// fma(S, a / den, bc), and the margin |bnd den - S| is compared with
+// guard den; the host builds the table with every step at least three guard
+// bands inside its cell, which absorbs the rounding of a / den (the cell a
+// value lands in can differ from the y-domain map only near cell edges,
+// where the neighbouring cell's entry gives the same pair).  After the
+// rotation acc[b'][nt][2r + e], b' = 0..7, are the eight coordinates of word
+// 4 t4 + 2 nt + e of row g8 + 8r, so each lane packs and stores four whole
+// words per row and stream.  Rows with a value inside the guard band go to
+// rvq_fixup_row.
+constexpr int P4_STAGES = 2;
+constexpr int P4_REP = 16;
+constexpr int P4_TAB_BYTES = PT_CELLS * P4_REP * 8;
+
+// Both 4-bit codes of the coordinate S (pair i1 | i2 << 4 in the low byte).
+// tab: this lane's replica as a 32-bit shared address, less the magic
+// constant's bits shifted by 7, so that the cell's entry is at tab + (gb << 7)
+// with gb the bits of the cell FMA (0x4B400000 + cell).
+__device__ __forceinline__ uint32_t pair_code_s(float s, float a, float bc, float den, uint32_t tab, float &m)
+{
+    const float u = __saturatef(fmaf(s, a, bc));
+    // cell in [0, PT_CELLS - 1]: u is saturated (NaN saturates to 0)
+    const uint32_t gb = __float_as_uint(fmaf(u, (float)(PT_CELLS - 1), GRID_MAGIC));
+    uint32_t ex, ey;
+    asm("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(ex), "=r"(ey) : "r"(tab + (gb << 7)));
+    // S > bnd den exactly when d is negative (an exact tie gives +0)
+    const float d = fmaf(__uint_as_float(ex), den, -s);
+    m = fminf(m, fabsf(d));
+    return __byte_perm(ey, 0u, __float_as_uint(d) >> 31);
+}
 
 template <bool SGN>
 __global__ void __launch_bounds__(S2_WARPS * 32, 1) rvq_encode_pair4_kernel(const __grid_constant__ RvqEncodeParams p)
@@ -1078,12 +1108,12 @@ __global__ void __launch_bounds__(S2_WARPS * 32, 1) rvq_encode_pair4_kernel(cons
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int g8 = lane >> 2, t4 = lane & 3;
-    unsigned char *ring = smem + warp * (S2_STAGES * ENC_BLOCK);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S2_WARPS * S2_STAGES * ENC_BLOCK) + warp * S2_STAGES;
+    unsigned char *ring = smem + warp * (P4_STAGES * ENC_BLOCK);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S2_WARPS * P4_STAGES * ENC_BLOCK) + warp * P4_STAGES;
 
     if (lane == 0) {
 #pragma unroll
-        for (int s = 0; s < S2_STAGES; ++s) mbar_init(&bars[s], 1);
+        for (int s = 0; s < P4_STAGES; ++s) mbar_init(&bars[s], 1);
         fence_mbar_init();
     }
     if (threadIdx.x < 16) {
@@ -1091,7 +1121,7 @@ __global__ void __launch_bounds__(S2_WARPS * 32, 1) rvq_encode_pair4_kernel(cons
         ssg[threadIdx.x] = make_uint4(half2_sign_mask(sign_pair(p.sgn, c0)), half2_sign_mask(sign_pair(p.sgn, c0 + 2)),
                                       half2_sign_mask(sign_pair(p.sgn, c0 + 4)), half2_sign_mask(sign_pair(p.sgn, c0 + 6)));
     }
-    for (int i = threadIdx.x; i < PT_CELLS; i += blockDim.x) ptab[i] = p.pt.ent[i];
+    for (int i = threadIdx.x; i < PT_CELLS * P4_REP; i += blockDim.x) ptab[i] = p.pt.ent[i / P4_REP];
     __syncthreads();
 
     const uint64_t pol = l2_policy_evict_first();
@@ -1102,6 +1132,7 @@ __global__ void __launch_bounds__(S2_WARPS * 32, 1) rvq_encode_pair4_kernel(cons
     const int tc2 = p.t2.code[lane];
     const float tcen = p.c1[lane & 15];
     const float pa = p.pt.a, pbc = p.pt.bc;
+    const uint32_t tab = smem_u32(ptab) + 8u * (uint32_t)(lane & (P4_REP - 1)) - (0x4B400000u << 7);
     uint32_t hb[2][2];
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
@@ -1123,7 +1154,7 @@ __global__ void __launch_bounds__(S2_WARPS * 32, 1) rvq_encode_pair4_kernel(cons
         }
     };
 #pragma unroll
-    for (int s = 0; s < S2_STAGES; ++s) {
+    for (int s = 0; s < P4_STAGES; ++s) {
         const int blk = gw + s * tw;
         if (blk < nblk) issue(blk, s);
     }
@@ -1136,10 +1167,10 @@ __global__ void __launch_bounds__(S2_WARPS * 32, 1) rvq_encode_pair4_kernel(cons
         const bool ok = mbar_wait_bounded(&bars[s], ph);
         if (!__all_sync(FULL_MASK, ok)) {
             if (lane == 0) atomicOr(&g_rvq_err, (unsigned)VQ_DEVERR_WAIT_TIMEOUT);
-            for (int k = 1; k < S2_STAGES; ++k) {
+            for (int k = 1; k < P4_STAGES; ++k) {
                 const int it2 = it + k;
                 if (gw + it2 * tw < nblk)
-                    (void)mbar_wait_bounded(&bars[it2 % S2_STAGES], (uint32_t)(it2 / S2_STAGES) & 1u);
+                    (void)mbar_wait_bounded(&bars[it2 % P4_STAGES], (uint32_t)(it2 / P4_STAGES) & 1u);
             }
             return;
         }
@@ -1149,8 +1180,10 @@ __global__ void __launch_bounds__(S2_WARPS * 32, 1) rvq_encode_pair4_kernel(cons
         float q0, q1;
         tc_rotate_block<SGN>(sbuf, ssg, hb, g8, t4, acc, q0, q1);
         const float n0 = __fsqrt_rn(q0), n1 = __fsqrt_rn(q1);
-        const float inv0 = q0 > 0.0f ? __frcp_rn(n0 * SQRT_D_HI) : 0.0f;
-        const float inv1 = q1 > 0.0f ? __frcp_rn(n1 * SQRT_D_HI) : 0.0f;
+        // per row: den = n sqrt(D), the cell slope a / den and the margin
+        // threshold guard den (a zero row gives den = 0 and is always flagged)
+        const float den0 = n0 * SQRT_D_HI, den1 = n1 * SQRT_D_HI;
+        const float sa0 = pa * __frcp_rn(den0), sa1 = pa * __frcp_rn(den1);
 
         // ---- quantize: word 2 nt + e of the lane (word 4 t4 + 2 nt + e of the
         // row) from b' = 0..7 of acc[.][nt][2r + e]; the pairs i1 | i2 << 4 of
@@ -1161,15 +1194,14 @@ __global__ void __launch_bounds__(S2_WARPS * 32, 1) rvq_encode_pair4_kernel(cons
         uint32_t w1[2][4], w2[2][4];
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
-            const float2 inv2 = r ? make_float2(inv1, inv1) : make_float2(inv0, inv0);
+            const float sa = r ? sa1 : sa0, den = r ? den1 : den0;
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt) {
                 uint32_t b0[2] = {0u, 0u}, b1[2] = {0u, 0u};
 #pragma unroll
                 for (int b = 0; b < 8; ++b) {
-                    const float2 y2 = __fmul2_rn(make_float2(acc[b][nt][2 * r], acc[b][nt][2 * r + 1]), inv2);
-                    const uint32_t px = pair_code(y2.x, pa, pbc, ptab, r ? m1 : m0);
-                    const uint32_t py = pair_code(y2.y, pa, pbc, ptab, r ? m1 : m0);
+                    const uint32_t px = pair_code_s(acc[b][nt][2 * r], sa, pbc, den, tab, r ? m1 : m0);
+                    const uint32_t py = pair_code_s(acc[b][nt][2 * r + 1], sa, pbc, den, tab, r ? m1 : m0);
                     if (b & 1) {
                         b1[0] = __funnelshift_r(b1[0], px, 8);
                         b1[1] = __funnelshift_r(b1[1], py, 8);
@@ -1190,8 +1222,8 @@ __global__ void __launch_bounds__(S2_WARPS * 32, 1) rvq_encode_pair4_kernel(cons
         // inside the band (and always when it is zero)
         const int row0 = blk * ER + g8, row1 = row0 + 8;
         const bool valid0 = row0 < p.N, valid1 = row1 < p.N;
-        const bool f0 = valid0 && (!(m0 >= p.guard) || !(q0 > 0.0f));
-        const bool f1 = valid1 && (!(m1 >= p.guard) || !(q1 > 0.0f));
+        const bool f0 = valid0 && (!(m0 >= p.guard * den0) || !(q0 > 0.0f));
+        const bool f1 = valid1 && (!(m1 >= p.guard * den1) || !(q1 > 0.0f));
         int f = (f0 ? 1 : 0) | (f1 ? 2 : 0);
         f |= __shfl_xor_sync(FULL_MASK, f, 1);
         f |= __shfl_xor_sync(FULL_MASK, f, 2);
@@ -1222,10 +1254,10 @@ __global__ void __launch_bounds__(S2_WARPS * 32, 1) rvq_encode_pair4_kernel(cons
 
         fence_proxy_async_smem();
         {
-            const int nb = blk + S2_STAGES * tw;
+            const int nb = blk + P4_STAGES * tw;
             if (nb < nblk) issue(nb, s);
         }
-        if (++s == S2_STAGES) {
+        if (++s == P4_STAGES) {
             s = 0;
             ph ^= 1u;
         }
@@ -1537,8 +1569,9 @@ cudaError_t launch_enc_sym2(const RvqEncodeParams &p, cudaStream_t stream)
     return launch_enc_tc(p, p.has_sgn ? rvq_encode_sym2_kernel<true> : rvq_encode_sym2_kernel<false>, S2_SMEM, stream);
 }
 
-// Shared memory of the b = 4 tensor-core encoder: the same plus the pair table.
-constexpr int P4_SMEM = S2_SMEM + P4_TAB_BYTES;
+// Shared memory of the b = 4 tensor-core encoder: sign masks, the replicated
+// pair table, the warps' two-stage rings and their mbarriers.
+constexpr int P4_SMEM = 1024 + ENC_SGN_BYTES + P4_TAB_BYTES + S2_WARPS * P4_STAGES * (ENC_BLOCK + 8);
 static_assert(P4_SMEM <= SMEM_MAX, "b = 4 encoder shared memory");
 
 cudaError_t launch_enc_pair4(const RvqEncodeParams &p, cudaStream_t stream)

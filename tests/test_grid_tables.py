@@ -80,7 +80,10 @@ def test_pair_table_for_library_4bit_codebook(harness):
 
 def test_pair_table_for_scaled_and_perturbed_codebooks(harness):
     """Other 16-level books (the library's at other dimensions, and randomly
-    perturbed ones): a table is either built and exact, or refused."""
+    perturbed ones): a table is either built and exact, or refused.  The
+    library's books at D = 64 and 256 must get one; perturbed books whose
+    steps crowd closer than a 512-cell grid can separate are refused (the
+    encoder then uses the two-table quantizer)."""
     from kv_cache_quantization_turboquantrvq_gb300 import api, build
     build.build()
     rng = np.random.default_rng(5)
@@ -92,10 +95,11 @@ def test_pair_table_for_scaled_and_perturbed_codebooks(harness):
         j2 = np.sort(c2 * rng.uniform(0.95, 1.05, 16)).astype(np.float32)
         books.append((j1, (0.5 * (j1[1:] + j1[:-1])).astype(np.float32), j2,
                       (0.5 * (j2[1:] + j2[:-1])).astype(np.float32)))
-    for book in books:
+    for i, book in enumerate(books):
         r = subprocess.run([harness] + _pair_args(*book), capture_output=True, text=True)
         if r.stdout.strip() == "NOTABLE":
+            assert i >= 2, "no table for the library's book"
             continue  # the encoder then uses the two-table quantizer
         assert r.returncode == 0, r.stdout
         built += 1
-    assert built >= 6
+    assert built >= 4
