@@ -4,6 +4,7 @@
 #include <cstdint>
 #include <cstring>
 #include <cuda_runtime_api.h>
+#include <mutex>
 
 #include "launch.h"
 #include "vq.h"
@@ -87,6 +88,73 @@ void set_signs(P &p, const uint32_t *signs)
 }
 
 }  // namespace
+
+// Quantizer tables derived from an RVQ codebook.  Searching for the grid and
+// pair tables costs the host 50-200 us per codebook, more than a whole
+// decode-time flush on the GPU, so the tables of the last few codebooks are
+// kept (keyed by the exact bits of the four arrays) and a call with the same
+// books only copies them.  Shared by all threads under a mutex.
+namespace {
+struct RvqTableEntry {
+    int bits = 0;
+    float c1[16], b1[16], c2[16], b2[16];
+    int mode = 0;
+    GridTable t1, t2;
+    PairTable pt;
+};
+constexpr int kTableSlots = 4;
+std::mutex g_table_mu;
+RvqTableEntry g_tables[kTableSlots];
+int g_table_used = 0, g_table_next = 0;
+
+bool same_books(const RvqTableEntry &e, int bits, const float *c1, const float *b1, const float *c2,
+                const float *b2)
+{
+    const int L = 1 << bits;
+    return e.bits == bits && std::memcmp(e.c1, c1, 4 * L) == 0 && std::memcmp(e.c2, c2, 4 * L) == 0 &&
+           std::memcmp(e.b1, b1, 4 * (L - 1)) == 0 && std::memcmp(e.b2, b2, 4 * (L - 1)) == 0;
+}
+}  // namespace
+
+int rvq_quantizer_tables(int bits, const float *c1, const float *b1, const float *c2, const float *b2,
+                         float guard, GridTable &t1, GridTable &t2, PairTable &pt)
+{
+    const int L = 1 << bits;
+    {
+        std::lock_guard<std::mutex> lock(g_table_mu);
+        for (int i = 0; i < g_table_used; ++i) {
+            const RvqTableEntry &e = g_tables[i];
+            if (same_books(e, bits, c1, b1, c2, b2)) {
+                t1 = e.t1;
+                t2 = e.t2;
+                if (e.mode == RVQ_MODE_PAIR) pt = e.pt;
+                return e.mode;
+            }
+        }
+    }
+    int mode = RVQ_MODE_PLAIN;
+    // (b = 2: the symmetric kernel's boundary tests need B, E < 1/4)
+    if (bits <= 2 && symmetric_codebook(c1, b1, L) && symmetric_codebook(c2, b2, L) &&
+        (bits == 1 || (b1[L - 2] < 0.25f && b2[L - 2] < 0.25f)))
+        mode = RVQ_MODE_SYM;
+    else if (build_grid(b1, L - 1, guard, t1) && build_grid(b2, L - 1, guard, t2))
+        // the shuffle tables also serve the exact recompute of the pair mode
+        mode = bits == 4 && build_pair_table(c1, b1, c2, b2, bits, guard, pt) ? RVQ_MODE_PAIR : RVQ_MODE_GRID;
+    std::lock_guard<std::mutex> lock(g_table_mu);
+    RvqTableEntry &e = g_tables[g_table_next];
+    g_table_next = (g_table_next + 1) % kTableSlots;
+    if (g_table_used < kTableSlots) ++g_table_used;
+    e.bits = bits;
+    std::memcpy(e.c1, c1, 4 * L);
+    std::memcpy(e.c2, c2, 4 * L);
+    std::memcpy(e.b1, b1, 4 * (L - 1));
+    std::memcpy(e.b2, b2, 4 * (L - 1));
+    e.mode = mode;
+    e.t1 = t1;
+    e.t2 = t2;
+    if (mode == RVQ_MODE_PAIR) e.pt = pt;
+    return mode;
+}
 
 int sm_count()
 {
@@ -210,15 +278,7 @@ static vq_status rvq_encode_impl(const void *k_f16, int B, int H, int S, int D, 
         p.b1[k] = k < L - 1 ? b1[k] : INFINITY;
         p.b2[k] = k < L - 1 ? b2[k] : INFINITY;
     }
-    int mode = RVQ_MODE_PLAIN;
-    // (b = 2: the symmetric kernel's boundary tests need B, E < 1/4)
-    if (bits <= 2 && symmetric_codebook(c1, b1, L) && symmetric_codebook(c2, b2, L) &&
-        (bits == 1 || (b1[L - 2] < 0.25f && b2[L - 2] < 0.25f)))
-        mode = RVQ_MODE_SYM;
-    else if (build_grid(b1, L - 1, kGuard, p.t1) && build_grid(b2, L - 1, kGuard, p.t2))
-        // the shuffle tables also serve the exact recompute of the pair mode
-        mode = bits == 4 && build_pair_table(c1, b1, c2, b2, bits, kGuard, p.pt) ? RVQ_MODE_PAIR
-                                                                                 : RVQ_MODE_GRID;
+    const int mode = rvq_quantizer_tables(bits, c1, b1, c2, b2, kGuard, p.t1, p.t2, p.pt);
     set_signs(p, signs);
     return cuda_status(launch_rvq_encode(p, bits, mode, reinterpret_cast<cudaStream_t>(stream)));
 }
