@@ -61,8 +61,10 @@ class Op:
         self.gpu_launches = launches if gpu_launches is None else gpu_launches
 
 
-def rvq_bytes(rows, bits):
-    return rows * (2 * D + 2 * (D * bits // 8) + 4)
+def rvq_bytes(rows, bits, d=D):
+    """Algorithmic bytes of RVQ encode (or decode) of `rows` rows of width d:
+    the fp16 row, two streams of floor(32/b)-code words and the fp32 norm."""
+    return rows * (2 * d + 2 * 4 * -(-d // (32 // bits)) + 4)
 
 
 def kivi_bytes(bh, s_q, bits, G, per_channel):
@@ -112,7 +114,10 @@ def describe(name):
         "c2": "KIVI 2-bit flush on K,V [1,32,4096,128] G=32 residual 128, then unpack+dequant",
         "c1": "RVQ b=2 encode+pack of keys [1,8,512,128], then unpack+dequant",
         "c4": "decode flush: 64 seqs x 8 heads x 128 new tokens into caches of random lengths; "
-              "RVQ b=2 and KIVI 2-bit G=32 (K,V), then unpack+dequant",
+              "RVQ b=2 on K and KIVI 2-bit G=32 on K and V, written at the sequences' offsets",
+        "gen": "RVQ encode+pack then unpack+dequant at the general widths: keys [4,32,32768,64] b=2, "
+               "[1,32,32768,256] b=4 and [2,32,32768,128] b=3 (ten 3-bit codes per word), fp16 N(0,1) "
+               "with 4x20 outlier channels per head",
     }[name]
 
 
@@ -177,6 +182,8 @@ def build_workload(name, dev, rank=0, layers=None, batch=None, chunked=False, ch
         if dec is not None:
             ops.append(Op(tag + "rvq_decode", "rvq_decode_kernel", dec, rvq_bytes(rows, bits), rows * D))
         results.extend([p1, p2, nr])
+        if dec is not None:
+            results.append(out)  # the round trip's reconstruction leaves the device too
 
     def kivi_ops(tag, k_dev, v_dev, bits, G, R, dst_off=None, S_dst=None, ops=ops, results=results,
                  stream=stream):
@@ -206,6 +213,8 @@ def build_workload(name, dev, rank=0, layers=None, batch=None, chunked=False, ch
             ops.append(Op(tag + "kivi_dequant_v", "kivi_values_dequant_kernel", lambda: api.vq_kivi_unpack_dequant(
                 outs, B, H, S_q, bits, G, v_out=vo, want_k=False, stream=stream), vb, B * H * S_q * D))
         results.extend(outs.values())
+        if dst_off is None:
+            results.extend([ko, vo])
 
     chunks = []
 
@@ -264,6 +273,28 @@ def build_workload(name, dev, rank=0, layers=None, batch=None, chunked=False, ch
                 c = new_chunk([(k_np, k)])
                 rvq_ops("L%02d_" % layer, k, cfg["bits"], ops=c["ops"], results=c["results"], stream=chunk_stream)
         ops.sort(key=lambda o: (not o.kernel.startswith("rvq_encode"), o.name))
+    elif name == "gen":
+        # the general-width path (rvq_generic.cu): other widths and b = 3
+        for tag, (Bg, Dg, bits) in (("D64b2_", (4, 64, 2)), ("D256b4_", (1, 256, 4)), ("D128b3_", (2, 128, 3))):
+            xg_np = synth.kv_tensor(Bg, 32, 32768, Dg, 120 + Dg + bits, 4, 20.0)
+            xg = t(xg_np)
+            inputs.append((xg_np, xg))
+            cbg = [np.ascontiguousarray(a) for a in api.vq_rvq_codebook(Dg, bits)]
+            Wg = api.rvq_words(Dg, bits)
+            rows = Bg * 32 * 32768
+            g1 = torch.empty((Bg, 32, 32768, Wg), dtype=torch.int32, device=dev)
+            g2 = torch.empty_like(g1)
+            gn = torch.empty((Bg, 32, 32768), dtype=torch.float32, device=dev)
+            go = torch.empty_like(xg)
+
+            def genc(xg=xg, bits=bits, cbg=cbg, g1=g1, g2=g2, gn=gn):
+                api.vq_rvq_encode_pack(xg, bits, *cbg, packed1=g1, packed2=g2, norms=gn, stream=stream)
+
+            def gdec(bits=bits, cbg=cbg, g1=g1, g2=g2, gn=gn, go=go, Dg=Dg):
+                api.vq_rvq_unpack_dequant(g1, g2, gn, bits, cbg[0], cbg[2], out=go, stream=stream, D=Dg)
+            ops.append(Op(tag + "rvq_encode", "rvq_generic_encode_kernel", genc, rvq_bytes(rows, bits, Dg), rows * Dg))
+            ops.append(Op(tag + "rvq_decode", "rvq_generic_decode_kernel", gdec, rvq_bytes(rows, bits, Dg), rows * Dg))
+            results.extend([g1, g2, gn, go])
     elif name == "c2":
         cfg = cfgs["c2_kivi_b2_32x4096"]
         k_np, v_np = synth.keys_for(cfg), synth.values_for(cfg)
@@ -426,27 +457,34 @@ class ClockSampler:
 # --------------------------------------------------------------------------- oracle timing
 
 
-def oracle_sample_rates(name, target_s=2.0):
-    """Time the CPU oracle on bounded samples of each op of the workload.
-    Returns ({op: bytes/s}, description)."""
+def oracle_sample_plan(name, target_s=2.0):
+    """Bounded samples of each op of the workload for the CPU oracle: per op a
+    function of a unit count, the algorithmic bytes per unit and the unit count
+    that takes about target_s (found by untimed doubling).  Returns
+    ([(op, fn, bytes_per_unit, units)], description)."""
     import oracle
     from kv_cache_quantization_turboquantrvq_gb300 import synth
 
-    rates, desc = {}, []
+    plan, desc = [], []
     cfgs = synth.CONFIGS
 
-    def timed(fn, nbytes_per_unit, units0, max_units=1 << 22):
+    def sized(fn, nbytes_per_unit, units0, max_units=1 << 22):
         units = min(units0, max_units)
         while True:
             t0 = time.perf_counter()
             fn(units)
             dt = time.perf_counter() - t0
             if dt >= target_s or units >= max_units:
-                return units * nbytes_per_unit / dt, units, dt
-            units = min(max_units, int(units * max(2.0, 1.2 * target_s / max(dt, 1e-4))))
+                return units
+            units = min(max_units, int(units * max(2.0, 1.1 * target_s / max(dt, 1e-4))))
 
-    def rvq_rates(bits, x_rows):
-        c1, b1, c2, b2, _ = oracle.rvq_codebooks(D, bits)
+    def timed(fn, nbytes_per_unit, units0, max_units=1 << 22, op=None):
+        n = sized(fn, nbytes_per_unit, units0, max_units)
+        plan.append((op, fn, nbytes_per_unit, n))
+        return None, n, None
+
+    def rvq_rates(bits, x_rows, d=D, tag=""):
+        c1, b1, c2, b2, _ = oracle.rvq_codebooks(d, bits)
         o = oracle.rvq_encode(x_rows[:1], bits, c1, b1, c2, b2)
 
         def enc(n):
@@ -454,10 +492,10 @@ def oracle_sample_rates(name, target_s=2.0):
 
         def dec(n):
             reps = np.repeat(o["packed1"], n, 0), np.repeat(o["packed2"], n, 0), np.repeat(o["norms"], n)
-            oracle.rvq_decode(*reps, D, bits, c1, c2)
-        r1, n1, _ = timed(enc, rvq_bytes(1, bits), 64, len(x_rows))
-        r2, n2, _ = timed(dec, rvq_bytes(1, bits), 64)
-        return r1, r2, n1, n2
+            oracle.rvq_decode(*reps, d, bits, c1, c2)
+        _, n1, _ = timed(enc, rvq_bytes(1, bits, d), 64, len(x_rows), op=tag + "rvq_encode")
+        _, n2, _ = timed(dec, rvq_bytes(1, bits, d), 64, op=tag + "rvq_decode")
+        return n1, n2
 
     def kivi_rates(bits, G, x):
         def kq(n):
@@ -465,8 +503,8 @@ def oracle_sample_rates(name, target_s=2.0):
 
         def vq_(n):
             oracle.kivi_quant(x[:, :, :n], bits, G, 0, False)
-        rk, nk, _ = timed(kq, kivi_bytes(1, G, bits, G, True), 1, x.shape[2] // G)
-        rv, nv, _ = timed(vq_, kivi_bytes(1, 1, bits, G, False), 64, x.shape[2])
+        _, nk, _ = timed(kq, kivi_bytes(1, G, bits, G, True), 1, x.shape[2] // G, op="kivi_quant_k")
+        _, nv, _ = timed(vq_, kivi_bytes(1, 1, bits, G, False), 64, x.shape[2], op="kivi_quant_v")
         ok = oracle.kivi_quant(x[:, :, :G], bits, G, 0, True)
         ov = oracle.kivi_quant(x[:, :, :G], bits, G, 0, False)
 
@@ -478,25 +516,28 @@ def oracle_sample_rates(name, target_s=2.0):
             m = max(1, n // G)
             oracle.kivi_dequant(np.repeat(ov["packed"], m, 1), np.repeat(ov["scale"], m, 1),
                                 np.repeat(ov["zero"], m, 1), 1, G * m, D, bits, G, False)
-        rkd, _, _ = timed(kd, kivi_bytes(1, G, bits, G, True), 1)
-        rvd, _, _ = timed(vd, kivi_bytes(1, 1, bits, G, False), 64)
-        return rk, rv, rkd, rvd, nk, nv
+        timed(kd, kivi_bytes(1, G, bits, G, True), 1, op="kivi_dequant_k")
+        timed(vd, kivi_bytes(1, 1, bits, G, False), 64, op="kivi_dequant_v")
+        return nk, nv
 
     if name in ("c5", "c1", "c3", "c4"):
         bits = {"c5": 2, "c1": 2, "c3": 4, "c4": 2}[name]
         cfg = {"c5": cfgs["c5_long_32k"], "c1": cfgs["c1_rvq_b2_8x512"],
                "c3": cfgs["c3_rvq_b4_32L_8k"], "c4": cfgs["c4_decode_flush_64x8x128"]}[name]
         x = synth.kv_tensor(1, 1, 1 << 16, D, cfg["seed"], *cfg.get("k_outliers", (0, 1.0))).reshape(-1, D)
-        r1, r2, n1, n2 = rvq_rates(bits, x)
-        rates["rvq_encode"], rates["rvq_decode"] = r1, r2
+        n1, n2 = rvq_rates(bits, x)
         desc.append("RVQ b=%d encode %d rows, decode %d rows" % (bits, n1, n2))
+    if name == "gen":
+        for tag, (dg, bits) in (("D64b2_", (64, 2)), ("D256b4_", (256, 4)), ("D128b3_", (128, 3))):
+            x = synth.kv_tensor(1, 1, 1 << 14, dg, 120 + dg + bits, 4, 20.0).reshape(-1, dg)
+            n1, n2 = rvq_rates(bits, x, dg, tag)
+            desc.append("RVQ D=%d b=%d encode %d rows, decode %d rows" % (dg, bits, n1, n2))
     if name in ("c5", "c2", "c4"):
         cfg = {"c5": cfgs["c5_long_32k"], "c2": cfgs["c2_kivi_b2_32x4096"],
                "c4": cfgs["c4_decode_flush_64x8x128"]}[name]
         G = cfg["group"]
         x = synth.kv_tensor(1, 1, 1 << 16, D, cfg["seed"], 4, 20.0)
-        rk, rv, rkd, rvd, nk, nv = kivi_rates(2, G, x)
-        rates.update(kivi_quant_k=rk, kivi_quant_v=rv, kivi_dequant_k=rkd, kivi_dequant_v=rvd)
+        nk, nv = kivi_rates(2, G, x)
         desc.append("KIVI 2-bit G=%d: %d key groups, %d value rows (and their dequant)" % (G, nk * D, nv))
     if name == "attn":
         cfg = cfgs["attn_decode_64x8x32_16k"]
@@ -514,8 +555,7 @@ def oracle_sample_rates(name, target_s=2.0):
         def att(n):
             oracle.rvq_attend(q, p1[:, :, :n], p2[:, :, :n], nr[:, :, :n], v[:, :, :n], bits, c1, c2,
                               1.0 / np.sqrt(D))
-        r, n, _ = timed(att, attend_bytes([1], 1, 0, bits), 256, smax)
-        rates["rvq_attend"] = r
+        _, n, _ = timed(att, attend_bytes([1], 1, 0, bits), 256, smax, op="rvq_attend")
         desc.append("RVQ b=%d attention of %d query heads over one kv head of %d keys" % (bits, gq, n))
     if name == "qjl":
         cfg = cfgs["qjl_long_32k_m128"]
@@ -525,8 +565,7 @@ def oracle_sample_rates(name, target_s=2.0):
 
         def qe(n):
             oracle.qjl_encode(x[:n], sk)
-        r, n, _ = timed(qe, qjl_bytes(1, m), 64, len(x))
-        rates["qjl_encode"] = r
+        _, n, _ = timed(qe, qjl_bytes(1, m), 64, len(x), op="qjl_encode")
         desc.append("QJL encode (m=%d) of %d key rows" % (m, n))
     if name == "kattn":
         cfg = cfgs["kattn_decode_64x8x32_16k"]
@@ -548,10 +587,28 @@ def oracle_sample_rates(name, target_s=2.0):
                                vq_["scale"].reshape(1, 1, smax, -1)[:, :, :ng * G],
                                vq_["zero"].reshape(1, 1, smax, -1)[:, :, :ng * G], bits, G, 1.0 / np.sqrt(D))
         per_tok = kattend_bytes([1], [0], 1, 0, bits, G)
-        r, n, _ = timed(katt, per_tok, 256, smax)
-        rates["kivi_attend"] = r
+        _, n, _ = timed(katt, per_tok, 256, smax, op="kivi_attend")
         desc.append("KIVI %d-bit G=%d attention of %d query heads over one kv head of %d tokens" % (bits, G, gq, n))
-    return rates, "; ".join(desc) + " (about %.0f s of CPU per op)" % target_s
+    return plan, "; ".join(desc)
+
+
+def time_plan(plan):
+    """Run each op of a sample plan once; returns ({op: bytes/s}, seconds)."""
+    rates, total = {}, 0.0
+    for op, fn, nbytes_per_unit, n in plan:
+        t0 = time.perf_counter()
+        fn(n)
+        dt = time.perf_counter() - t0
+        rates[op] = n * nbytes_per_unit / dt
+        total += dt
+    return rates, total
+
+
+def oracle_sample_rates(name, target_s=2.0):
+    """The oracle's rate per op on samples of about target_s each."""
+    plan, desc = oracle_sample_plan(name, target_s)
+    rates, total = time_plan(plan)
+    return rates, desc + " (%.1f s of CPU for %d ops)" % (total, len(plan))
 
 
 def step_rate_from_ops(ops, rates):
@@ -559,7 +616,7 @@ def step_rate_from_ops(ops, rates):
     t = 0.0
     for o in ops:
         base = o.name.split("_", 1)[1] if o.name.startswith("L") else o.name
-        t += o.nbytes / rates[base]
+        t += o.nbytes / rates[base if base in rates else o.name]
     return sum(o.nbytes for o in ops) / t
 
 
@@ -595,7 +652,8 @@ def main():
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--workload", choices=("c5", "c3", "c2", "c1", "c4", "attn", "kattn", "qjl"), default="c5")
+    ap.add_argument("--workload", choices=("c5", "c3", "c2", "c1", "c4", "attn", "kattn", "qjl", "gen"),
+                    default="c5")
     ap.add_argument("--graph", action="store_true",
                     help="also capture the step in a CUDA graph and time its replays "
                          "(launch-bound workloads: c4, c1); `value` is then the graph's")
@@ -823,12 +881,12 @@ def run_reference(args, world):
     ops = reference_ops(args.workload)
     W, K = max(args.warmup, 0), args.steps
     vals, t_total = [], 0.0
-    # about two minutes in all, at most 1 s of CPU per step
-    per_step_target = min(1.0, 120.0 / max(W + K, 1))
+    # the same fixed samples every step, sized once (untimed) so that the
+    # W + K steps take about two minutes in all
+    per_step_target = min(2.0, 120.0 / max(W + K, 1))
+    plan, desc = oracle_sample_plan(args.workload, target_s=max(per_step_target / 6, 0.05))
     for i in range(W + K):
-        t0 = time.perf_counter()
-        rates, desc = oracle_sample_rates(args.workload, target_s=per_step_target / 6)
-        dt = time.perf_counter() - t0
+        rates, dt = time_plan(plan)
         if i >= W:
             vals.append(step_rate_from_ops(ops, rates) / 1e9)
             t_total += dt
@@ -898,6 +956,11 @@ def reference_ops(name):
         c = cfgs["qjl_long_32k_m128"]
         rows = c["B"] * c["H"] * c["S"]
         ops.append(Op("qjl_encode", "qjl_encode", noop, qjl_bytes(rows, c["m"]), rows * D))
+    elif name == "gen":
+        for tag, (Bg, dg, bits) in (("D64b2_", (4, 64, 2)), ("D256b4_", (1, 256, 4)), ("D128b3_", (2, 128, 3))):
+            rows = Bg * 32 * 32768
+            for n in ("rvq_encode", "rvq_decode"):
+                ops.append(Op(tag + n, tag + n, noop, rvq_bytes(rows, bits, dg), rows * dg))
     return ops
 
 

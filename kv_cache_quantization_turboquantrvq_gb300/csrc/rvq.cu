@@ -1111,10 +1111,28 @@ __global__ void __launch_bounds__(S2_WARPS * 32, 1) rvq_encode_pair4_kernel(cons
     unsigned char *ring = smem + warp * (P4_STAGES * ENC_BLOCK);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S2_WARPS * P4_STAGES * ENC_BLOCK) + warp * P4_STAGES;
 
+    const uint64_t pol = l2_policy_evict_first();
+    const int nblk = (p.N + ER - 1) / ER;
+    const int gw = blockIdx.x * S2_WARPS + warp;
+    const int tw = gridDim.x * S2_WARPS;
+    auto issue = [&](int blk, int s) {
+        if (lane == 0) {
+            mbar_arrive_expect_tx(&bars[s], (uint32_t)ENC_BLOCK);
+            tma_load_2d(ring + s * ENC_BLOCK, &p.tmap, 0, blk * ER, &bars[s], pol);
+            tma_load_2d(ring + s * ENC_BLOCK + ENC_BLOCK / 2, &p.tmap, 64, blk * ER, &bars[s], pol);
+        }
+    };
+    // the warp's barriers, then its first blocks in flight while the CTA
+    // fills the sign masks and the replicated table
     if (lane == 0) {
 #pragma unroll
         for (int s = 0; s < P4_STAGES; ++s) mbar_init(&bars[s], 1);
         fence_mbar_init();
+#pragma unroll
+        for (int s = 0; s < P4_STAGES; ++s) {
+            const int blk = gw + s * tw;
+            if (blk < nblk) issue(blk, s);
+        }
     }
     if (threadIdx.x < 16) {
         const int c0 = 8 * threadIdx.x;
@@ -1124,7 +1142,6 @@ __global__ void __launch_bounds__(S2_WARPS * 32, 1) rvq_encode_pair4_kernel(cons
     for (int i = threadIdx.x; i < PT_CELLS * P4_REP; i += blockDim.x) ptab[i] = p.pt.ent[i / P4_REP];
     __syncthreads();
 
-    const uint64_t pol = l2_policy_evict_first();
     // shuffle tables of the exact recompute
     const float tb1 = p.t1.bnd[lane];
     const int tc1 = p.t1.code[lane];
@@ -1141,23 +1158,8 @@ __global__ void __launch_bounds__(S2_WARPS * 32, 1) rvq_encode_pair4_kernel(cons
         hb[nt][1] = h16_pair(2 * t4 + 8, ap);
     }
 
-    const int nblk = (p.N + ER - 1) / ER;
-    const int gw = blockIdx.x * S2_WARPS + warp;
-    const int tw = gridDim.x * S2_WARPS;
     // destination row = source row (no batch offsets, same capacity)
     const bool dense = p.dst_off == nullptr && p.S_dst == p.S;
-    auto issue = [&](int blk, int s) {
-        if (lane == 0) {
-            mbar_arrive_expect_tx(&bars[s], (uint32_t)ENC_BLOCK);
-            tma_load_2d(ring + s * ENC_BLOCK, &p.tmap, 0, blk * ER, &bars[s], pol);
-            tma_load_2d(ring + s * ENC_BLOCK + ENC_BLOCK / 2, &p.tmap, 64, blk * ER, &bars[s], pol);
-        }
-    };
-#pragma unroll
-    for (int s = 0; s < P4_STAGES; ++s) {
-        const int blk = gw + s * tw;
-        if (blk < nblk) issue(blk, s);
-    }
 
     int s = 0;
     uint32_t ph = 0;
