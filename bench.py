@@ -114,7 +114,11 @@ def describe(name):
         "c2": "KIVI 2-bit flush on K,V [1,32,4096,128] G=32 residual 128, then unpack+dequant",
         "c1": "RVQ b=2 encode+pack of keys [1,8,512,128], then unpack+dequant",
         "c4": "decode flush: 64 seqs x 8 heads x 128 new tokens into caches of random lengths; "
-              "RVQ b=2 on K and KIVI 2-bit G=32 on K and V, written at the sequences' offsets",
+              "RVQ b=2 on K and KIVI 2-bit G=32 on K and V, written at the sequences' offsets, "
+              "in one launch (vq_flush_decode)",
+        "c4s": "decode flush: 64 seqs x 8 heads x 128 new tokens into caches of random lengths; "
+               "RVQ b=2 on K and KIVI 2-bit G=32 on K and V, written at the sequences' offsets, "
+               "as three separate calls",
         "gen": "RVQ encode+pack then unpack+dequant at the general widths: keys [4,32,32768,64] b=2, "
                "[1,32,32768,256] b=4 and [2,32,32768,128] b=3 (ten 3-bit codes per word), fp16 N(0,1) "
                "with 4x20 outlier channels per head",
@@ -307,14 +311,39 @@ def build_workload(name, dev, rank=0, layers=None, batch=None, chunked=False, ch
         k = t(k_np)
         inputs = [(k_np, k)]
         rvq_ops("", k, cfg["bits"])
-    elif name == "c4":
+    elif name in ("c4", "c4s"):
         cfg = cfgs["c4_decode_flush_64x8x128"]
         k_np, v_np = synth.keys_for(cfg), synth.values_for(cfg)
         k, v = t(k_np), t(v_np)
         off = t(synth.cache_lengths(cfg["B"], cfg["seed"]))
         inputs = [(k_np, k), (v_np, v)]
-        rvq_ops("", k, 2, dst_off=off, S_dst=cfg["s_dst"])
-        kivi_ops("", k, v, 2, cfg["group"], 0, dst_off=off, S_dst=cfg["s_dst"])
+        if name == "c4s":  # the same flush as three separate calls
+            rvq_ops("", k, 2, dst_off=off, S_dst=cfg["s_dst"])
+            kivi_ops("", k, v, 2, cfg["group"], 0, dst_off=off, S_dst=cfg["s_dst"])
+        else:  # one launch (vq_flush_decode): RVQ b=2 keys, KIVI 2-bit keys and values
+            Bc, Hc, Sc, G, S_dst = cfg["B"], cfg["H"], cfg["S"], cfg["group"], cfg["s_dst"]
+            cbf = [np.ascontiguousarray(a) for a in api.vq_rvq_codebook(D, 2)]
+            shp = api.kivi_shapes(Bc, Hc, S_dst, D, 2, G)
+            fo = {"packed1": torch.empty((Bc, Hc, S_dst, 8), dtype=torch.int32, device=dev),
+                  "packed2": torch.empty((Bc, Hc, S_dst, 8), dtype=torch.int32, device=dev),
+                  "norms": torch.empty((Bc, Hc, S_dst), dtype=torch.float32, device=dev),
+                  "k_packed": torch.empty(shp["k_packed"], dtype=torch.int32, device=dev),
+                  "k_scale": torch.empty(shp["k_scale"], dtype=torch.float16, device=dev),
+                  "k_zero": torch.empty(shp["k_scale"], dtype=torch.float16, device=dev),
+                  "v_packed": torch.empty(shp["v_packed"], dtype=torch.int32, device=dev),
+                  "v_scale": torch.empty(shp["v_scale"], dtype=torch.float16, device=dev),
+                  "v_zero": torch.empty(shp["v_scale"], dtype=torch.float16, device=dev)}
+            rows = Bc * Hc * Sc
+
+            def flush(stream=stream):
+                api.vq_flush_decode(k, v, 0, dst_off=off, S_dst=S_dst,
+                                    rvq=dict(bits=2, books=cbf, packed1=fo["packed1"], packed2=fo["packed2"],
+                                             norms=fo["norms"]),
+                                    kivi=dict(bits=2, group=G, **{n: fo[n] for n in fo if n[0] in "kv"}),
+                                    stream=stream)
+            nb = rvq_bytes(rows, 2) + kivi_bytes(Bc * Hc, Sc, 2, G, True) + kivi_bytes(Bc * Hc, Sc, 2, G, False)
+            ops.append(Op("flush_decode", "vq_flush_kernel", flush, nb, 2 * rows * D))
+            results.extend(fo.values())
     elif name == "attn":
         # the cache (codes, norms, values) is resident state; a step's input is
         # the batch of queries and its result the attention output
@@ -520,10 +549,11 @@ def oracle_sample_plan(name, target_s=2.0):
         timed(vd, kivi_bytes(1, 1, bits, G, False), 64, op="kivi_dequant_v")
         return nk, nv
 
-    if name in ("c5", "c1", "c3", "c4"):
-        bits = {"c5": 2, "c1": 2, "c3": 4, "c4": 2}[name]
+    if name in ("c5", "c1", "c3", "c4", "c4s"):
+        bits = {"c5": 2, "c1": 2, "c3": 4, "c4": 2, "c4s": 2}[name]
         cfg = {"c5": cfgs["c5_long_32k"], "c1": cfgs["c1_rvq_b2_8x512"],
-               "c3": cfgs["c3_rvq_b4_32L_8k"], "c4": cfgs["c4_decode_flush_64x8x128"]}[name]
+               "c3": cfgs["c3_rvq_b4_32L_8k"], "c4": cfgs["c4_decode_flush_64x8x128"],
+               "c4s": cfgs["c4_decode_flush_64x8x128"]}[name]
         x = synth.kv_tensor(1, 1, 1 << 16, D, cfg["seed"], *cfg.get("k_outliers", (0, 1.0))).reshape(-1, D)
         n1, n2 = rvq_rates(bits, x)
         desc.append("RVQ b=%d encode %d rows, decode %d rows" % (bits, n1, n2))
@@ -532,9 +562,9 @@ def oracle_sample_plan(name, target_s=2.0):
             x = synth.kv_tensor(1, 1, 1 << 14, dg, 120 + dg + bits, 4, 20.0).reshape(-1, dg)
             n1, n2 = rvq_rates(bits, x, dg, tag)
             desc.append("RVQ D=%d b=%d encode %d rows, decode %d rows" % (dg, bits, n1, n2))
-    if name in ("c5", "c2", "c4"):
+    if name in ("c5", "c2", "c4", "c4s"):
         cfg = {"c5": cfgs["c5_long_32k"], "c2": cfgs["c2_kivi_b2_32x4096"],
-               "c4": cfgs["c4_decode_flush_64x8x128"]}[name]
+               "c4": cfgs["c4_decode_flush_64x8x128"], "c4s": cfgs["c4_decode_flush_64x8x128"]}[name]
         G = cfg["group"]
         x = synth.kv_tensor(1, 1, 1 << 16, D, cfg["seed"], 4, 20.0)
         nk, nv = kivi_rates(2, G, x)
@@ -652,7 +682,7 @@ def main():
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--workload", choices=("c5", "c3", "c2", "c1", "c4", "attn", "kattn", "qjl", "gen"),
+    ap.add_argument("--workload", choices=("c5", "c3", "c2", "c1", "c4", "c4s", "attn", "kattn", "qjl", "gen"),
                     default="c5")
     ap.add_argument("--graph", action="store_true",
                     help="also capture the step in a CUDA graph and time its replays "
@@ -836,7 +866,8 @@ def main():
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         rates, desc = oracle_sample_rates(args.workload)
-        cpu = {"value": round(step_rate_from_ops(ops, rates) / 1e9, 6), "unit": UNIT, "cores": 1,
+        # (the oracle runs the step's parts one by one: the same bytes)
+        cpu = {"value": round(step_rate_from_ops(reference_ops(args.workload), rates) / 1e9, 6), "unit": UNIT, "cores": 1,
                "host_cores": os.cpu_count(), "kind": "oracle", "sample": desc}
 
     if rank == 0:
@@ -934,7 +965,7 @@ def reference_ops(name):
         for n, pc in (("kivi_quant_k", True), ("kivi_quant_v", False), ("kivi_dequant_k", True),
                       ("kivi_dequant_v", False)):
             ops.append(Op(n, n, noop, kivi_bytes(bh, s_q, 2, c["group"], pc), bh * s_q * D))
-    elif name == "c4":
+    elif name in ("c4", "c4s"):
         c = cfgs["c4_decode_flush_64x8x128"]
         rows = c["B"] * c["H"] * c["S"]
         ops.append(Op("rvq_encode", "rvq_encode", noop, rvq_bytes(rows, 2), rows * D))

@@ -289,6 +289,42 @@ vq_status vq_kivi_quant_pack(const void *k_f16, const void *v_f16, int B, int H,
                              const int32_t *dst_off, int S_dst, vq_stream_t stream);
 
 /*
+ * vq_flush_decode - the decode-time flush of one layer in one launch (kivi
+ * page, "Why it's invisible, and why that was predictable": decode flushes are
+ * small, so separate launches are mostly latency).  A block of T new tokens
+ * per sequence: tokens [0, T - R), R = residual_length, are quantized into
+ * the resident caches at the sequences' offsets, tokens [T - R, T) are copied
+ * in fp16 into the window buffers.  Every part is optional and equals the
+ * stand-alone call bit for bit:
+ *   RVQ of the keys (packed1 != NULL; packed2, norms and the four codebook
+ *     arrays required): vq_rvq_encode_pack of tokens [0, T - R) with
+ *     rvq_bits in {1, 2, 4}; the books must be the library's kind
+ *     (symmetric for b = 1, 2, or 16-level books with a pair table, such as
+ *     vq_rvq_codebook's), else VQ_ERR_UNSUPPORTED (use vq_rvq_encode_pack);
+ *   KIVI of the keys (k_packed != NULL) and of the values (v_packed != NULL):
+ *     vq_kivi_quant_pack of tokens [0, T - R) with kivi_bits in {2, 4} and
+ *     group in {32, 64} (others: VQ_ERR_UNSUPPORTED);
+ *   the window (residual_length > 0, k_win and/or v_win non-NULL): token
+ *     T - R + j of (b, h) is copied to row win_off[b] + j of k_win / v_win
+ *     [B, H, R_cap, D] fp16 (win_off NULL: row j); win_off[b] + R must not
+ *     exceed R_cap, else that batch's window is skipped and
+ *     VQ_DEVERR_BAD_OFFSET is set.
+ *   k_f16, v_f16 [B, H, T, D] fp16, device (each needed by its parts).
+ *   dst_off, S_dst, output layouts and device errors: as vq_rvq_encode_pack
+ *     and vq_kivi_quant_pack (S_q = T - R).  D = 128.
+ * All pointers are device pointers except the codebooks (host).  Outputs may
+ * not overlap each other or the inputs.  Asynchronous on `stream`; one
+ * kernel launch; nothing is allocated.
+ */
+vq_status vq_flush_decode(const void *k_f16, const void *v_f16, int B, int H, int T, int D,
+                          int residual_length, const int32_t *dst_off, int S_dst, int rvq_bits,
+                          const float *c1, const float *b1, const float *c2, const float *b2,
+                          uint32_t *packed1, uint32_t *packed2, float *norms, int kivi_bits, int group,
+                          uint32_t *k_packed, void *k_scale, void *k_zero, uint32_t *v_packed,
+                          void *v_scale, void *v_zero, void *k_win, void *v_win, const int32_t *win_off,
+                          int R_cap, vq_stream_t stream);
+
+/*
  * vq_kivi_unpack_dequant - KIVI unpack + dequant of S_q stored tokens:
  *   x_hat = fp16(q * scale + zero), evaluated exactly and rounded once.
  * Layouts as written by vq_kivi_quant_pack with S_dst = S_q (NG = ceil(S_q/G)).

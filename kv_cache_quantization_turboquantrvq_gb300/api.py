@@ -31,7 +31,7 @@ EXPORTED = ("vq_status_str", "vq_version", "vq_rvq_codebook", "vq_rvq_encode_pac
             "vq_rvq_unpack_dequant", "vq_kivi_quant_pack", "vq_kivi_unpack_dequant",
             "vq_device_error", "vq_rvq_attend_workspace", "vq_rvq_attend", "vq_rvq_attend_noalloc",
             "vq_rvq_encode_pack_rs", "vq_rvq_unpack_dequant_rs", "vq_rvq_attend_rs",
-            "vq_kivi_attend_workspace", "vq_kivi_attend", "vq_qjl_encode")
+            "vq_kivi_attend_workspace", "vq_kivi_attend", "vq_qjl_encode", "vq_flush_decode")
 VQ_ATTEND_SCRATCH_BYTES = 16 * 1024 * 1024
 
 
@@ -71,6 +71,8 @@ def lib():
     L.vq_kivi_attend_workspace.argtypes = [I, I, I, I, I, ctypes.POINTER(ctypes.c_size_t)]
     L.vq_kivi_attend.argtypes = [P] * 11 + [I] * 8 + [ctypes.c_float, P, P, ctypes.c_size_t, P]
     L.vq_qjl_encode.argtypes = [P, I, I, P, I, P, P, P]
+    L.vq_flush_decode.argtypes = [P, P, I, I, I, I, I, P, I, I, P, P, P, P, P, P, P, I, I,
+                                  P, P, P, P, P, P, P, P, P, I, P]
     for name in EXPORTED[2:]:
         getattr(L, name).restype = I
     _lib = L
@@ -354,3 +356,61 @@ def vq_qjl_encode(x, s, packed=None, norms=None, stream=None):
     _check(lib().vq_qjl_encode(_ptr(x), N, D, _ptr(s), m, _ptr(packed), _ptr(norms), _stream(stream)),
            "vq_qjl_encode")
     return packed, norms
+
+
+def vq_flush_decode(k, v, residual_length: int, dst_off=None, S_dst=None, rvq=None, kivi=None,
+                    window=None, stream=None):
+    """The decode-time flush of one layer in one launch: k, v [B, H, T, 128]
+    fp16 (either may be None when no part needs it); tokens [0, T - R) are
+    quantized at the sequences' offsets, tokens [T - R, T) copied to the fp16
+    window.  Parts (each optional, outputs allocated when absent):
+      rvq = dict(bits, books=(c1, b1, c2, b2)[, packed1, packed2, norms])
+      kivi = dict(bits, group[, keys=True, values=True, k_packed, ..., v_zero])
+      window = dict([k_win, v_win, win_off, R_cap])
+    Returns a dict with every output tensor."""
+    import torch
+    ref = k if k is not None else v
+    B, H, T, D = ref.shape
+    R = int(residual_length)
+    S_q = T - R
+    S_dst = S_q if S_dst is None else S_dst
+    dev = ref.device
+    out = {}
+    keep = []
+    rb, rp = 0, [None] * 4
+    if rvq is not None:
+        rb = int(rvq["bits"])
+        keep = [_host(a) for a in rvq["books"]]
+        rp = [p_ for _, p_ in keep]
+        W = rvq_words(D, rb)
+        out["packed1"] = rvq.get("packed1", torch.empty((B, H, S_dst, W), dtype=torch.int32, device=dev))
+        out["packed2"] = rvq.get("packed2", torch.empty((B, H, S_dst, W), dtype=torch.int32, device=dev))
+        out["norms"] = rvq.get("norms", torch.empty((B, H, S_dst), dtype=torch.float32, device=dev))
+    kb, G = 0, 0
+    if kivi is not None:
+        kb, G = int(kivi["bits"]), int(kivi["group"])
+        shp = kivi_shapes(B, H, S_dst, D, kb, G)
+        if kivi.get("keys", True):
+            out["k_packed"] = kivi.get("k_packed", torch.empty(shp["k_packed"], dtype=torch.int32, device=dev))
+            out["k_scale"] = kivi.get("k_scale", torch.empty(shp["k_scale"], dtype=torch.float16, device=dev))
+            out["k_zero"] = kivi.get("k_zero", torch.empty(shp["k_scale"], dtype=torch.float16, device=dev))
+        if kivi.get("values", True):
+            out["v_packed"] = kivi.get("v_packed", torch.empty(shp["v_packed"], dtype=torch.int32, device=dev))
+            out["v_scale"] = kivi.get("v_scale", torch.empty(shp["v_scale"], dtype=torch.float16, device=dev))
+            out["v_zero"] = kivi.get("v_zero", torch.empty(shp["v_scale"], dtype=torch.float16, device=dev))
+    win_off, R_cap = None, 0
+    if window is not None and R > 0:
+        R_cap = int(window.get("R_cap", R))
+        win_off = window.get("win_off")
+        if k is not None:
+            out["k_win"] = window.get("k_win", torch.empty((B, H, R_cap, D), dtype=torch.float16, device=dev))
+        if v is not None:
+            out["v_win"] = window.get("v_win", torch.empty((B, H, R_cap, D), dtype=torch.float16, device=dev))
+    g = out.get
+    _check(lib().vq_flush_decode(_ptr(k), _ptr(v), B, H, T, D, R, _ptr(dst_off), S_dst, rb, *rp,
+                                 _ptr(g("packed1")), _ptr(g("packed2")), _ptr(g("norms")), kb, G,
+                                 _ptr(g("k_packed")), _ptr(g("k_scale")), _ptr(g("k_zero")),
+                                 _ptr(g("v_packed")), _ptr(g("v_scale")), _ptr(g("v_zero")),
+                                 _ptr(g("k_win")), _ptr(g("v_win")), _ptr(win_off), R_cap, _stream(stream)),
+           "vq_flush_decode")
+    return out

@@ -17,7 +17,7 @@ INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(HERE, "libvqflush.so")
 BUILD = os.path.join(HERE, "_build")
 
-SOURCES = ["rvq.cu", "rvq_generic.cu", "kivi.cu", "attend.cu", "kattend.cu", "qjl.cu", "api.cpp", "codebook.cpp", "grid.cpp", "tmap.cpp"]
+SOURCES = ["rvq.cu", "rvq_generic.cu", "kivi.cu", "flush.cu", "attend.cu", "kattend.cu", "qjl.cu", "api.cpp", "codebook.cpp", "grid.cpp", "tmap.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-std=c++17", "-O3", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
 

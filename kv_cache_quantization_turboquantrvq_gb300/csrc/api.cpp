@@ -5,6 +5,8 @@
 #include <cstring>
 #include <cuda_runtime_api.h>
 #include <mutex>
+#include <utility>
+#include <vector>
 
 #include "launch.h"
 #include "vq.h"
@@ -269,6 +271,7 @@ static vq_status rvq_encode_impl(const void *k_f16, int B, int H, int S, int D, 
     p.dst_off = dst_off;
     p.N = (int)N;
     p.S = S;
+    p.S_q = S;
     p.H = H;
     p.S_dst = S_dst;
     p.guard = kGuard;
@@ -680,6 +683,143 @@ vq_status vq_kivi_quant_pack(const void *k_f16, const void *v_f16, int B, int H,
     return VQ_OK;
 }
 
+vq_status vq_flush_decode(const void *k_f16, const void *v_f16, int B, int H, int T, int D,
+                          int residual_length, const int32_t *dst_off, int S_dst, int rvq_bits,
+                          const float *c1, const float *b1, const float *c2, const float *b2,
+                          uint32_t *packed1, uint32_t *packed2, float *norms, int kivi_bits, int group,
+                          uint32_t *k_packed, void *k_scale, void *k_zero, uint32_t *v_packed,
+                          void *v_scale, void *v_zero, void *k_win, void *v_win, const int32_t *win_off,
+                          int R_cap, vq_stream_t stream)
+{
+    if (B < 0 || H < 0 || T < 0 || residual_length < 0 || residual_length > T) return VQ_ERR_INVALID_ARG;
+    if (D != kD) return D > 0 ? VQ_ERR_UNSUPPORTED : VQ_ERR_INVALID_ARG;
+    const int R = residual_length, S_q = T - R;
+    const bool do_rvq = packed1 != nullptr, do_kk = k_packed != nullptr, do_kv = v_packed != nullptr;
+    const bool do_win = R > 0 && (k_win != nullptr || v_win != nullptr);
+    if (!do_rvq && !do_kk && !do_kv && !do_win) return VQ_ERR_INVALID_ARG;
+    if ((do_rvq || do_kk || (do_win && k_win)) && !k_f16) return VQ_ERR_INVALID_ARG;
+    if ((do_kv || (do_win && v_win)) && !v_f16) return VQ_ERR_INVALID_ARG;
+    if (dst_off == nullptr ? S_dst != S_q : S_dst < S_q) return VQ_ERR_INVALID_ARG;
+    if (do_win && R_cap < R) return VQ_ERR_INVALID_ARG;
+    const long long rows = (long long)B * H * T;
+    if (rows >= (1LL << 31) || (long long)B * H * S_dst >= (1LL << 31) ||
+        (do_win && (long long)B * H * R_cap >= (1LL << 31)))
+        return VQ_ERR_UNSUPPORTED;
+
+    FlushParams fp;
+    std::memset(&fp, 0, sizeof(fp));
+    std::vector<std::pair<const void *, size_t>> ins, outs;
+    const size_t in_b = (size_t)rows * kD * 2;
+    if (k_f16) ins.push_back({k_f16, in_b});
+    if (v_f16) ins.push_back({v_f16, in_b});
+    if (dst_off) ins.push_back({dst_off, (size_t)B * 4});
+    if (win_off) ins.push_back({win_off, (size_t)B * 4});
+    if (!aligned(k_f16, 16) || !aligned(v_f16, 16) || !aligned(dst_off, 4) || !aligned(win_off, 4))
+        return VQ_ERR_MISALIGNED;
+    if (do_rvq) {
+        if (rvq_bits != 1 && rvq_bits != 2 && rvq_bits != 4) return VQ_ERR_INVALID_ARG;
+        if (!packed2 || !norms || !c1 || !b1 || !c2 || !b2) return VQ_ERR_INVALID_ARG;
+        const int L = 1 << rvq_bits;
+        if (!valid_codebook(c1, b1, L) || !valid_codebook(c2, b2, L)) return VQ_ERR_INVALID_ARG;
+        if (!aligned(packed1, 16) || !aligned(packed2, 16) || !aligned(norms, 4)) return VQ_ERR_MISALIGNED;
+        RvqEncodeParams &p = fp.rvq;
+        const int mode = rvq_quantizer_tables(rvq_bits, c1, b1, c2, b2, kGuard, p.t1, p.t2, p.pt);
+        // the fused flush carries the encoders of the symmetric 1/2-bit books
+        // and of 4-bit books with a pair table (the library's books)
+        if (!((rvq_bits <= 2 && mode == RVQ_MODE_SYM) || (rvq_bits == 4 && mode == RVQ_MODE_PAIR)))
+            return VQ_ERR_UNSUPPORTED;
+        fp.rvq_kind = rvq_bits;
+        p.x = k_f16;
+        p.p1 = packed1;
+        p.p2 = packed2;
+        p.norms = norms;
+        p.dst_off = dst_off;
+        p.N = (int)rows;
+        p.S = T;
+        p.S_q = S_q;
+        p.H = H;
+        p.S_dst = S_dst;
+        p.guard = kGuard;
+        for (int k = 0; k < 16; ++k) {
+            p.c1[k] = k < L ? c1[k] : 0.0f;
+            p.c2[k] = k < L ? c2[k] : 0.0f;
+            p.b1[k] = k < L - 1 ? b1[k] : INFINITY;
+            p.b2[k] = k < L - 1 ? b2[k] : INFINITY;
+        }
+        const size_t pk_b = (size_t)B * H * S_dst * rvq_words(kD, rvq_bits) * 4;
+        outs.push_back({packed1, pk_b});
+        outs.push_back({packed2, pk_b});
+        outs.push_back({norms, (size_t)B * H * S_dst * 4});
+    }
+    if (do_kk || do_kv) {
+        if (kivi_bits != 2 && kivi_bits != 4) return VQ_ERR_UNSUPPORTED;
+        if (group != 32 && group != 64) return VQ_ERR_UNSUPPORTED;
+        fp.kbits = kivi_bits;
+        KiviQuantParams q;
+        std::memset(&q, 0, sizeof(q));
+        q.dst_off = dst_off;
+        q.B = B;
+        q.H = H;
+        q.S = T;
+        q.S_q = S_q;
+        q.S_dst = S_dst;
+        q.group = group;
+        q.NG_dst = (S_dst + group - 1) / group;
+        const size_t kpk_b = (size_t)B * H * q.NG_dst * group * kivi_bits / 32 * kD * 4;
+        const size_t ksz_b = (size_t)B * H * q.NG_dst * kD * 2;
+        const size_t vpk_b = (size_t)B * H * S_dst * kD * kivi_bits / 32 * 4;
+        const size_t vsz_b = (size_t)B * H * S_dst * (kD / group) * 2;
+        if (do_kk) {
+            if (!k_scale || !k_zero) return VQ_ERR_INVALID_ARG;
+            if (!aligned(k_packed, 16) || !aligned(k_scale, 8) || !aligned(k_zero, 8)) return VQ_ERR_MISALIGNED;
+            fp.kk = q;
+            fp.kk.x = k_f16;
+            fp.kk.packed = k_packed;
+            fp.kk.scale = k_scale;
+            fp.kk.zero = k_zero;
+            outs.push_back({k_packed, kpk_b});
+            outs.push_back({k_scale, ksz_b});
+            outs.push_back({k_zero, ksz_b});
+        }
+        if (do_kv) {
+            if (!v_scale || !v_zero) return VQ_ERR_INVALID_ARG;
+            if (!aligned(v_packed, 16) || !aligned(v_scale, 2) || !aligned(v_zero, 2)) return VQ_ERR_MISALIGNED;
+            fp.kv = q;
+            fp.kv.x = v_f16;
+            fp.kv.packed = v_packed;
+            fp.kv.scale = v_scale;
+            fp.kv.zero = v_zero;
+            outs.push_back({v_packed, vpk_b});
+            outs.push_back({v_scale, vsz_b});
+            outs.push_back({v_zero, vsz_b});
+        }
+    }
+    if (do_win) {
+        if (!aligned(k_win, 16) || !aligned(v_win, 16)) return VQ_ERR_MISALIGNED;
+        fp.win.k = k_win ? k_f16 : nullptr;
+        fp.win.v = v_win ? v_f16 : nullptr;
+        fp.win.k_win = k_win;
+        fp.win.v_win = v_win;
+        fp.win.win_off = win_off;
+        fp.win.B = B;
+        fp.win.H = H;
+        fp.win.T = T;
+        fp.win.R = R;
+        fp.win.R_cap = R_cap;
+        const size_t w_b = (size_t)B * H * R_cap * kD * 2;
+        if (k_win) outs.push_back({k_win, w_b});
+        if (v_win) outs.push_back({v_win, w_b});
+    }
+    for (size_t i = 0; i < outs.size(); ++i) {
+        for (const auto &in : ins)
+            if (overlap(outs[i].first, outs[i].second, in.first, in.second)) return VQ_ERR_ALIASING;
+        for (size_t j = i + 1; j < outs.size(); ++j)
+            if (overlap(outs[i].first, outs[i].second, outs[j].first, outs[j].second)) return VQ_ERR_ALIASING;
+    }
+    if (rows == 0) return VQ_OK;
+    return cuda_status(launch_flush(fp, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 vq_status vq_kivi_unpack_dequant(const uint32_t *k_packed, const void *k_scale, const void *k_zero,
                                  const uint32_t *v_packed, const void *v_scale, const void *v_zero,
                                  int B, int H, int S_q, int D, int bits, int group,
@@ -767,11 +907,12 @@ vq_status vq_device_error(vq_stream_t stream, int *code_out)
     if (kivi_take_device_error(&b, s) != cudaSuccess) return VQ_ERR_CUDA;
     if (attend_take_device_error(&c, s) != cudaSuccess) return VQ_ERR_CUDA;
     if (kivi_attend_take_device_error(&d, s) != cudaSuccess) return VQ_ERR_CUDA;
-    unsigned e = 0, f = 0;
+    unsigned e = 0, f = 0, g = 0;
     if (gen_take_device_error(&e, s) != cudaSuccess) return VQ_ERR_CUDA;
     if (qjl_take_device_error(&f, s) != cudaSuccess) return VQ_ERR_CUDA;
-    *code_out = (int)(a | b | c | d | e | f);
-    return (a | b | c | d | e | f) ? VQ_ERR_DEVICE : VQ_OK;
+    if (flush_take_device_error(&g, s) != cudaSuccess) return VQ_ERR_CUDA;
+    *code_out = (int)(a | b | c | d | e | f | g);
+    return (a | b | c | d | e | f | g) ? VQ_ERR_DEVICE : VQ_OK;
 }
 
 }  // extern "C"

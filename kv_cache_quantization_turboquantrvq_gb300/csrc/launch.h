@@ -73,6 +73,8 @@ struct RvqEncodeParams {
     float *norms;        // [B, H, S_dst]
     const int32_t *dst_off;
     int N, S, H, S_dst;
+    int S_q;             // tokens [S_q, S) of each (b, h) slice are not encoded (the fused
+                         // flush's fp16 window); S_q = S for vq_rvq_encode_pack
     FastDiv divS, divH;  // by S and by H (set by the launcher)
     float guard;         // |y - boundary| below this sends the row to the exact path
     GridTable t1, t2;
@@ -187,6 +189,31 @@ cudaError_t attend_static_scratch(void **ptr, size_t *bytes);
 // tables (GridTable), and the table-free symmetric 1/2-bit quantizer.
 enum RvqMode { RVQ_MODE_PLAIN = 0, RVQ_MODE_GRID = 1, RVQ_MODE_SYM = 2, RVQ_MODE_PAIR = 3 };
 cudaError_t launch_rvq_encode(const RvqEncodeParams &p, int bits, int mode, cudaStream_t stream);
+// Fill the launcher-set fields (fast divisors, tensor map) of encoder and
+// KIVI-quantizer parameters; false if the tensor map cannot be encoded.
+bool prepare_rvq_encode(RvqEncodeParams &p);
+bool prepare_kivi_quant(KiviQuantParams &p, bool per_channel);
+
+// Decode-time flush of one layer in one launch (flush.cu): the RVQ encode of
+// the new keys, the KIVI quantization of keys and values, and the copy of
+// the tokens that stay fp16 into the caller's window buffers, each part on
+// its own range of CTAs of one grid.
+struct FlushWindowParams {
+    const void *k, *v;       // fp16 [B, H, T, 128]: tokens [T - R, T) are copied
+    void *k_win, *v_win;     // fp16 [B, H, R_cap, 128] (either may be null)
+    const int32_t *win_off;  // [B] first window row written (null: 0)
+    int B, H, T, R, R_cap;
+};
+struct FlushParams {
+    RvqEncodeParams rvq;     // the keys' RVQ part (rvq_kind != 0)
+    KiviQuantParams kk, kv;  // KIVI keys / values (x == nullptr: absent)
+    FlushWindowParams win;
+    int rvq_kind;            // 0: none; 1, 2: symmetric b = 1, 2 books; 4: b = 4 pair table
+    int kbits;               // KIVI bits (2 or 4; group 32 or 64) when kk or kv is present
+    int n_rvq, n_kk, n_kv, n_win;  // CTAs of each part (set by the launcher)
+};
+cudaError_t launch_flush(FlushParams &p, cudaStream_t stream);
+cudaError_t flush_take_device_error(unsigned *bits, cudaStream_t stream);
 cudaError_t launch_rvq_decode(const RvqDecodeParams &p, int bits, cudaStream_t stream);
 cudaError_t launch_kivi_quant(const KiviQuantParams &p, int bits, bool per_channel,
                               cudaStream_t stream);

@@ -163,3 +163,43 @@ def test_qjl_validation(L):
     assert q(p=A + 1024) == api.VQ_ERR_ALIASING    # packed over the keys
     assert q(n=A + (2 << 26)) == api.VQ_ERR_ALIASING  # norms over packed
     assert q(N=0, x=0, p=0, n=0) == api.VQ_OK       # nothing to do
+
+
+def test_flush_decode_validation(L):
+    """vq_flush_decode refuses bad parts, shapes, alignment and overlaps on the
+    host (fake addresses: only refused cases and an empty call reach it)."""
+    from kv_cache_quantization_turboquantrvq_gb300 import api
+    cb2 = _cb(2)
+    M = 1 << 26
+
+    def f(k=A, v=A + M, B=2, H=2, T=40, D=128, R=8, off=None, S_dst=None, rb=2, cb=cb2,
+          p1=A + 2 * M, p2=A + 3 * M, nr=A + 4 * M, kb=2, G=32, kp=A + 5 * M, ks=A + 6 * M, kz=A + 7 * M,
+          vp=A + 8 * M, vs=A + 9 * M, vz=A + 10 * M, kw=A + 11 * M, vw=A + 12 * M, woff=None, R_cap=8):
+        S_q = T - R
+        cbp = [None] * 4 if cb is None else [P(c.ctypes.data) for c in cb]
+        return L.vq_flush_decode(P(k), P(v), B, H, T, D, R, P(off), S_q if S_dst is None else S_dst, rb, *cbp,
+                                 P(p1), P(p2), P(nr), kb, G, P(kp), P(ks), P(kz), P(vp), P(vs), P(vz),
+                                 P(kw), P(vw), P(woff), R_cap, None)
+    none = dict(p1=0, kp=0, vp=0, kw=0, vw=0)
+    assert f(**none) == api.VQ_ERR_INVALID_ARG                     # no part at all
+    assert f(D=64) == api.VQ_ERR_UNSUPPORTED
+    assert f(R=41) == api.VQ_ERR_INVALID_ARG                       # window longer than the block
+    assert f(k=0) == api.VQ_ERR_INVALID_ARG                        # keys' parts need k
+    assert f(v=0) == api.VQ_ERR_INVALID_ARG                        # values' parts need v
+    assert f(rb=3) == api.VQ_ERR_INVALID_ARG
+    assert f(cb=None) == api.VQ_ERR_INVALID_ARG
+    c1, b1, c2, b2 = cb2
+    asym = c1.copy()
+    asym[3] *= np.float32(1.5)
+    assert f(cb=[asym, b1, c2, b2]) == api.VQ_ERR_UNSUPPORTED       # not the library's kind of book
+    assert f(kb=1, G=32) == api.VQ_ERR_UNSUPPORTED
+    assert f(G=128) == api.VQ_ERR_UNSUPPORTED
+    assert f(R_cap=4) == api.VQ_ERR_INVALID_ARG                    # window capacity below R
+    assert f(S_dst=50) == api.VQ_ERR_INVALID_ARG                   # no dst_off: S_dst must be T - R
+    assert f(k=A + 8) == api.VQ_ERR_MISALIGNED
+    assert f(nr=A + 4 * M + 2) == api.VQ_ERR_MISALIGNED
+    assert f(kw=A + 11 * M + 8) == api.VQ_ERR_MISALIGNED
+    assert f(p1=A + 512) == api.VQ_ERR_ALIASING                    # packed1 inside the keys
+    assert f(vw=A + 11 * M + 64) == api.VQ_ERR_ALIASING            # the two windows overlap
+    assert f(vs=A + 5 * M) == api.VQ_ERR_ALIASING                  # v_scale over k_packed
+    assert f(B=0) == api.VQ_OK                                     # nothing to do
