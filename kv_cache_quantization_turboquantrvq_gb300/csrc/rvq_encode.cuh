@@ -285,7 +285,7 @@ __device__ __forceinline__ bool rvq_dst_row(const RvqEncodeParams &p, int row, s
     int off = 0;
     if (p.dst_off != nullptr) {
         off = __ldg(p.dst_off + fdiv(p.divH, bh));
-        if (off < 0 || off > p.S_dst - p.S) {
+        if (off < 0 || off > p.S_dst - p.S_q) {
             atomicOr(&VQ_RVQ_ERR, (unsigned)VQ_DEVERR_BAD_OFFSET);
             return false;
         }
