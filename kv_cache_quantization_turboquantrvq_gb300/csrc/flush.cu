@@ -189,23 +189,28 @@ cudaError_t launch_flush(FlushParams &p, cudaStream_t stream)
         items[3] = 2 * nb;
         bytes[3] = (double)((p.win.k_win ? 1 : 0) + (p.win.v_win ? 1 : 0)) * p.win.B * p.win.H * p.win.R * D * 4;
     }
-    // CTAs: at most one per SM in all, shared by bytes, at least one per
-    // present part and no more than the part has warp items for
+    // CTAs: at most one per SM in all, shared by each part's expected time
+    // (its bytes over the rate one SM sustains on it: the parts' measured
+    // whole-GPU rates, in GB/s, the encoders being the slow ones), at least
+    // one per present part and no more than the part has warp items for
+    const double rate[4] = {p.rvq_kind == 4 ? 2300.0 : 3800.0, 5900.0, 6000.0, 6000.0};
     const int sms = sm_count();
-    double total = 0;
+    double cost[4], total = 0;
     int parts = 0;
-    for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < 4; ++i) {
+        cost[i] = (bytes[i] > 0 ? bytes[i] : 1.0) / rate[i];
         if (items[i] > 0) {
-            total += bytes[i] > 0 ? bytes[i] : 1.0;
+            total += cost[i];
             ++parts;
         }
+    }
     if (parts == 0) return cudaSuccess;
     int n[4] = {0, 0, 0, 0};
     const int budget = sms > parts ? sms : parts;
     for (int i = 0; i < 4; ++i) {
         if (items[i] == 0) continue;
         const long long useful = (items[i] + FL_WARPS - 1) / FL_WARPS;
-        long long want = (long long)(budget * ((bytes[i] > 0 ? bytes[i] : 1.0) / total) + 0.5);
+        long long want = (long long)(budget * (cost[i] / total) + 0.5);
         if (want < 1) want = 1;
         if (want > useful) want = useful;
         n[i] = (int)want;

@@ -8,17 +8,11 @@
 // which is the page's byte order on a little-endian machine), and ||x|| as
 // fp16.
 //
-// Design.  The sketch is a dense product X S^T: [keys x 128] by [128 x m], on
-// the tensor cores as 16 x 8 x 16 tiles (mma.sync, fp16 operands - every
-// product of two fp16 values is exact - fp32 accumulation).  Persistent CTAs
-// of 8 warps; the CTA copies S into shared memory once (rows padded to 272
-// bytes so that ldmatrix reads are conflict-free); each warp streams its own
-// 16-key blocks (two 64-coordinate TMA boxes with the 128-byte swizzle,
-// double-buffered), loads the block's A fragments once (ldmatrix) and reuses
-// them for every 32-column chunk of the sketch; the squared norms come from
-// the same registers by paired fp32 FMAs (the squares are exact).  The signs
-// of a chunk's accumulators are gathered by warp ballots and interleaved into
-// one word per key.
+// Design.  The sketch is the dense product X S^T: [keys x 128] by [128 x m],
+// the one real contraction of the path, on the 5th-generation tensor cores
+// (tcgen05.mma from shared memory into tensor memory; fp16 operands - every
+// product of two fp16 values is exact - fp32 accumulation).  See the
+// tcgen05 section below for the tiling and the roles of the warps.
 #include <cuda_fp16.h>
 
 #include "device_common.cuh"
@@ -31,190 +25,291 @@ namespace {
 VQ_DEFINE_ERROR_WORD(g_qjl_err);
 
 constexpr int D = 128;
-constexpr int QJ_WARPS = 8;
-constexpr int QJ_ROWS = 16;                 // keys per warp block
-constexpr int QJ_BOX = QJ_ROWS * 128;       // one 64-coordinate box (bytes)
-constexpr int QJ_STAGE = 2 * QJ_BOX;        // a block: two boxes (4 KB, 1024-aligned)
-constexpr int QJ_STAGES = 2;
-constexpr int SROW = D * 2 + 16;            // padded sketch row (bytes)
+// ------------------------------------------------------------ tcgen05 path
+//
+// The sketch of a tile of 128 keys is one D = X S^T of M = 128, N = m,
+// K = 128 on the 5th-generation tensor cores: eight tcgen05.mma (K = 16
+// each) from shared-memory operands, the fp32 accumulator in tensor memory.
+// Both operands are K-major with the 128-byte swizzle: a tile of X arrives by
+// two TMA boxes (coordinates 0-63 and 64-127, 128 rows of 128 bytes each), S
+// is copied once per CTA into the same layout.  Roles (one persistent CTA
+// per SM, 6 warps): warp 0 streams X tiles into a 4-stage ring, warp 1 owns
+// the tensor memory and issues the MMAs (one thread), warps 2-5 are the
+// epilogue: thread t of the four owns key row t of the tile (the tensor
+// memory lane it may read), reads its m accumulators (tcgen05.ld), packs
+// bit j = [dot_j >= 0] and takes the norm from the key's row in the staged
+// tile.  The accumulator is double-buffered in tensor memory,
+// so the MMAs of tile i + 1 run during the epilogue of tile i.  Every wait
+// is bounded; on a timeout the CTA records VQ_DEVERR_WAIT_TIMEOUT, waits
+// (bounded) for its copies in flight, frees its tensor memory and returns.
+constexpr int QT_M = 128;                // keys per tile (MMA M)
+constexpr int QT_STAGES = 4;             // X tiles in flight
+constexpr int QT_HALF = QT_M * 128;      // one 64-coordinate half of a tile (bytes)
+constexpr int QT_TILE = 2 * QT_HALF;     // 32 KB
+constexpr int QT_EPI = 4;                // epilogue warps
+constexpr int QT_THREADS = 32 * (2 + QT_EPI);
 
-constexpr int qj_smem(int m)
+__host__ __device__ constexpr int qt_smem(int m)
 {
-    return 1024 + QJ_WARPS * QJ_STAGES * QJ_STAGE + m * SROW + QJ_WARPS * QJ_STAGES * 8;
+    // 1024-byte alignment, the sketch (two halves of m rows x 128 bytes),
+    // the ring, then the barriers and the tensor-memory address slot
+    return 1024 + m * 256 + QT_STAGES * QT_TILE + 256;
 }
 
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3)
+// Shared-memory matrix descriptor (tcgen05): K-major, 128-byte swizzle, rows
+// of 128 bytes in groups of 8 (stride 1024 bytes between groups); start
+// address in 16-byte units, descriptor version 1, layout type 2 (128B swizzle).
+__device__ __forceinline__ uint64_t qt_desc(uint32_t saddr)
 {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(addr));
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+           ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
 
-// d += a * b for one 16 x 8 x 16 tile, fp16 operands, fp32 accumulation.
-__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                          uint32_t b0, uint32_t b1)
+// Instruction descriptor of kind::f16: fp32 accumulator, fp16 A and B, both
+// K-major, N = n, M = 128.
+__host__ __device__ constexpr uint32_t qt_idesc(int n)
 {
-    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
-        "{%0, %1, %2, %3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+    return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(QT_M >> 4) << 24);
 }
 
-// The 4 bits of n at the even positions of a byte.
-__device__ __forceinline__ uint32_t spread4(uint32_t n)
+__device__ __forceinline__ void qt_mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc)
 {
-    n = (n | (n << 2)) & 0x33u;
-    return (n | (n << 1)) & 0x55u;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(acc));
 }
 
-// W = m / 32 sign words per key; up to 4 words (16 n-tiles, 16 independent
-// accumulator chains) are accumulated together.
-template <int W>
-__global__ void __launch_bounds__(QJ_WARPS * 32) qjl_encode_kernel(const __grid_constant__ QjlEncodeParams p)
+__device__ __forceinline__ void qt_commit(uint64_t *bar)
 {
-    constexpr int WG = W < 4 ? W : 4;  // words per pass
-    extern __shared__ __align__(128) unsigned char smem_raw[];
-    unsigned char *stages = smem_1k(smem_raw);
-    unsigned char *ss = stages + QJ_WARPS * QJ_STAGES * QJ_STAGE;  // sketch rows [m][SROW]
-    uint64_t *bars = reinterpret_cast<uint64_t *>(ss + p.m * SROW);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nblk = (p.N + QJ_ROWS - 1) / QJ_ROWS;
-    const int tw = gridDim.x * QJ_WARPS;      // warps of the grid
-    const int gw = blockIdx.x * QJ_WARPS + warp;
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
 
-    unsigned char *my_st = stages + warp * QJ_STAGES * QJ_STAGE;
-    uint64_t *my_bar = bars + warp * QJ_STAGES;
-    if (lane == 0) {
+__device__ __forceinline__ void qt_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void qt_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// 32 consecutive fp32 columns of this thread's tensor-memory lane.
+__device__ __forceinline__ void qt_ld32(uint32_t taddr, uint32_t (&r)[32])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+        "%14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+}
+
+__device__ __forceinline__ void qt_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// The registers of a tcgen05.ld hold its data only after tcgen05.wait::ld:
+// an empty volatile asm that "modifies" each one, placed after the wait,
+// keeps the compiler from moving their uses above it.
+__device__ __forceinline__ void qt_hold(uint32_t (&r)[32])
+{
 #pragma unroll
-        for (int s = 0; s < QJ_STAGES; ++s) mbar_init(&my_bar[s], 1);
+    for (int j = 0; j < 32; ++j) asm volatile("" : "+r"(r[j])::"memory");
+}
+
+// Bit j of the result: [v_j >= 0].  Adding +0 turns a negative zero into +0
+// (round to nearest), so the complemented sign bit is exactly [v >= 0]; the
+// funnel shift appends each sign below the ones already taken (j from 31
+// down to 0 leaves bit j at position j).
+__device__ __forceinline__ uint32_t qt_signs(const uint32_t (&r)[32])
+{
+    uint32_t w = 0u;
+#pragma unroll
+    for (int j = 31; j >= 0; --j) w = __funnelshift_l(__float_as_uint(__uint_as_float(r[j]) + 0.0f), w, 1);
+    return ~w;
+}
+
+template <int W>
+__global__ void __launch_bounds__(QT_THREADS, 1) qjl_encode_tc_kernel(const __grid_constant__ QjlEncodeParams p)
+{
+    constexpr int M = 32 * W;  // sketch rows (MMA N, accumulator columns per buffer)
+    // tensor-memory columns: two accumulator buffers of M fp32 columns at a
+    // power-of-two stride
+    constexpr uint32_t ASTRIDE = M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256;
+    constexpr uint32_t TCOLS = 2 * ASTRIDE;
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    unsigned char *base = smem_1k(smem_raw);
+    unsigned char *ss = base;                        // sketch: half h at h * M * 128
+    unsigned char *ring = base + M * 256;            // 1024-aligned (M is a multiple of 32)
+    uint64_t *bars = reinterpret_cast<uint64_t *>(ring + QT_STAGES * QT_TILE);
+    uint64_t *x_full = bars, *x_empty = bars + QT_STAGES;
+    uint64_t *acc_full = bars + 2 * QT_STAGES, *acc_empty = acc_full + 2;
+    volatile uint32_t *tslot = reinterpret_cast<volatile uint32_t *>(acc_empty + 2);
+    volatile uint32_t *abort_flag = tslot + 1;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int ntiles = (p.N + QT_M - 1) / QT_M;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < QT_STAGES; ++s) {
+            mbar_init(&x_full[s], 1);
+            mbar_init(&x_empty[s], QT_EPI);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&acc_full[a], 1);
+            mbar_init(&acc_empty[a], QT_EPI);
+        }
+        *abort_flag = 0u;
         fence_mbar_init();
     }
-    __syncwarp();
-    const uint64_t pol = l2_policy_evict_first();
-    auto issue = [&](int blk, int st) {
-        if (lane == 0) {
-            unsigned char *dst = my_st + st * QJ_STAGE;
-            mbar_arrive_expect_tx(&my_bar[st], (uint32_t)QJ_STAGE);
-            tma_load_2d(dst, &p.tmx, 0, blk * QJ_ROWS, &my_bar[st], pol);
-            tma_load_2d(dst + QJ_BOX, &p.tmx, 64, blk * QJ_ROWS, &my_bar[st], pol);
-        }
-    };
-#pragma unroll
-    for (int s = 0; s < QJ_STAGES; ++s)
-        if (gw + s * tw < nblk) issue(gw + s * tw, s);
-
-    // the sketch, once per CTA: 16-byte pieces into padded rows
+    // the sketch into the swizzled K-major layout: 16-byte chunk c of row r
     {
         const uint4 *src = static_cast<const uint4 *>(p.s);
-        for (int i = threadIdx.x; i < p.m * (D / 8); i += blockDim.x) {
+        for (int i = threadIdx.x; i < M * 16; i += blockDim.x) {
             const int r = i >> 4, c = i & 15;
-            *reinterpret_cast<uint4 *>(ss + r * SROW + c * 16) = __ldg(src + i);
+            *reinterpret_cast<uint4 *>(ss + (c >> 3) * (M * 128) + swz128(r, c & 7)) = __ldg(src + i);
         }
+        fence_proxy_async_smem();  // generic-proxy writes, read by the MMA (async proxy)
     }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32((const void *)tslot)),
+                     "r"(TCOLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    qt_fence_before();
     __syncthreads();
+    qt_fence_after();
+    const uint32_t tmem = *tslot;
 
-    const int g8 = lane >> 2, t4 = lane & 3;
-    const uint32_t sbase = smem_u32(ss);
-    // ldmatrix rows: A (keys) row (lane & 7) + 8 ((lane >> 3) & 1), 16-byte
-    // chunk 2 kt' + (lane >> 4) of its box; B (sketch rows) for two n-tiles:
-    // row (lane & 7) + 8 (lane >> 4), chunk 2 kt + ((lane >> 3) & 1)
-    const int arow = (lane & 7) + 8 * ((lane >> 3) & 1), ach = lane >> 4;
-    const int brow = (lane & 7) + 8 * (lane >> 4), bch = (lane >> 3) & 1;
-
-    for (int it = 0;; ++it) {
-        const int blk = gw + it * tw;
-        if (blk >= nblk) break;
-        const int st = it % QJ_STAGES;
-        const bool ok = mbar_wait_bounded(&my_bar[st], (uint32_t)(it / QJ_STAGES) & 1u);
-        if (!__all_sync(FULL_MASK, ok)) {
-            if (lane == 0) atomicOr(&g_qjl_err, (unsigned)VQ_DEVERR_WAIT_TIMEOUT);
-            for (int k = 1; k < QJ_STAGES; ++k) {
-                const int it2 = it + k;
-                if (gw + it2 * tw < nblk)
-                    (void)mbar_wait_bounded(&my_bar[it2 % QJ_STAGES], (uint32_t)(it2 / QJ_STAGES) & 1u);
+    if (warp == 0) {
+        // ---- producer: X tiles into the ring
+        if (lane == 0) {
+            const uint64_t pol = l2_policy_evict_first();
+            int i = 0;
+            for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++i) {
+                const int s = i % QT_STAGES;
+                if (i >= QT_STAGES && !mbar_wait_bounded(&x_empty[s], (uint32_t)((i / QT_STAGES) - 1) & 1u)) {
+                    atomicOr(&g_qjl_err, (unsigned)VQ_DEVERR_WAIT_TIMEOUT);
+                    *abort_flag = 1u;
+                    break;
+                }
+                if (*abort_flag) break;
+                unsigned char *dst = ring + s * QT_TILE;
+                mbar_arrive_expect_tx(&x_full[s], (uint32_t)QT_TILE);
+                tma_load_2d(dst, &p.tmx, 0, t * QT_M, &x_full[s], pol);
+                tma_load_2d(dst + QT_HALF, &p.tmx, 64, t * QT_M, &x_full[s], pol);
             }
-            break;
+            // the copies this CTA issued have all landed before it may exit
+            for (int k = 0; k < QT_STAGES && k < i; ++k) {
+                const int j = i - 1 - k;
+                (void)mbar_wait_bounded(&x_full[j % QT_STAGES], (uint32_t)(j / QT_STAGES) & 1u);
+            }
         }
-        const uint32_t xb = smem_u32(my_st + st * QJ_STAGE);
-        uint32_t a[8][4];
+    } else if (warp == 1) {
+        // ---- MMA issue (one thread)
+        if (lane == 0) {
+            constexpr uint32_t IDESC = qt_idesc(M);
+            const uint32_t sb = smem_u32(ss), rb = smem_u32(ring);
+            int i = 0;
+            for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++i) {
+                const int s = i % QT_STAGES, a = i & 1;
+                bool ok = mbar_wait_bounded(&x_full[s], (uint32_t)(i / QT_STAGES) & 1u);
+                if (ok && i >= 2) ok = mbar_wait_bounded(&acc_empty[a], (uint32_t)((i >> 1) - 1) & 1u);
+                if (!ok || *abort_flag) {
+                    if (!ok) atomicOr(&g_qjl_err, (unsigned)VQ_DEVERR_WAIT_TIMEOUT);
+                    *abort_flag = 1u;
+                    break;
+                }
+                qt_fence_after();
+                const uint32_t xa = rb + s * QT_TILE;
 #pragma unroll
-        for (int kt = 0; kt < 8; ++kt)
-            ldsm_x4(xb + (kt >> 2) * QJ_BOX + swz128(arow, 2 * (kt & 3) + ach), a[kt][0], a[kt][1], a[kt][2],
-                    a[kt][3]);
-        // the stage is consumed (the fragments are in registers): refill it
+                for (int kb = 0; kb < 2; ++kb) {
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint64_t ad = qt_desc(xa + kb * QT_HALF + kk * 32);
+                        const uint64_t bd = qt_desc(sb + kb * (M * 128) + kk * 32);
+                        qt_mma(tmem + (uint32_t)a * ASTRIDE, ad, bd, IDESC, (kb | kk) ? 1u : 0u);
+                    }
+                }
+                qt_commit(&acc_full[a]);  // arrives when the MMAs are done (operands read, D written)
+            }
+        }
         __syncwarp();
-        fence_proxy_async_smem();
-        if (blk + QJ_STAGES * tw < nblk) issue(blk + QJ_STAGES * tw, st);
-
-        const int row0 = blk * QJ_ROWS;
-        // squared norms from the fragments in registers (the tensor pipe is
-        // the busy one): keys g8 (registers 0, 2) and g8 + 8 (1, 3), 32 exact
-        // squares each per lane in paired fp32 FMAs, then the 4 lanes of a key
-        {
-            float2 qa = make_float2(0.0f, 0.0f), qb = make_float2(0.0f, 0.0f);
+    } else {
+        // ---- epilogue: warp q = warp % 4 reads tensor-memory lanes 32 q .. 32 q + 31
+        const int q = warp & 3;
+        const int row = 32 * q + lane;
+        int i = 0;
+        for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++i) {
+            const int s = i % QT_STAGES, a = i & 1;
+            const bool ok = mbar_wait_bounded(&acc_full[a], (uint32_t)(i >> 1) & 1u);
+            if (!__all_sync(FULL_MASK, ok) || *abort_flag) {
+                if (!ok && lane == 0) atomicOr(&g_qjl_err, (unsigned)VQ_DEVERR_WAIT_TIMEOUT);
+                *abort_flag = 1u;
+                break;
+            }
+            qt_fence_after();
+            uint32_t words[W];
 #pragma unroll
-            for (int kt = 0; kt < 8; ++kt) {
+            for (int w = 0; w < W; ++w) {
+                uint32_t r[32];
+                qt_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)a * ASTRIDE + (uint32_t)(32 * w), r);
+                qt_wait_ld();
+                qt_hold(r);
+                words[w] = qt_signs(r);
+            }
+            // the accumulator buffer is free for tile i + 2
+            qt_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[a]);
+            // the key's norm from its row of the staged tile (exact squares,
+            // fp32 sums), then the stage is free
+            const unsigned char *xt = ring + s * QT_TILE;
+            float2 acc2 = make_float2(0.0f, 0.0f), acc3 = acc2;
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&a[kt][j]));
-                    if (j & 1) qb = __ffma2_rn(f, f, qb);
-                    else qa = __ffma2_rn(f, f, qa);
+            for (int h = 0; h < 2; ++h) {
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const uint4 v = *reinterpret_cast<const uint4 *>(xt + h * QT_HALF + swz128(row, c));
+                    const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&u[j]));
+                        if (j & 1) acc3 = __ffma2_rn(f, f, acc3);
+                        else acc2 = __ffma2_rn(f, f, acc2);
+                    }
                 }
             }
-            float sa = qa.x + qa.y, sb = qb.x + qb.y;
-            sa += __shfl_xor_sync(FULL_MASK, sa, 1);
-            sb += __shfl_xor_sync(FULL_MASK, sb, 1);
-            sa += __shfl_xor_sync(FULL_MASK, sa, 2);
-            sb += __shfl_xor_sync(FULL_MASK, sb, 2);
-            if (t4 == 0) {
-                __half *nr = static_cast<__half *>(p.norms);
-                if (row0 + g8 < p.N) nr[row0 + g8] = __float2half_rn(__fsqrt_rn(sa));
-                if (row0 + g8 + 8 < p.N) nr[row0 + g8 + 8] = __float2half_rn(__fsqrt_rn(sb));
-            }
-        }
-        // signs, WG words (32 sketch rows each) per pass
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&x_empty[s]);
+            const int key = t * QT_M + row;
+            if (key < p.N) {
+                const float ss2 = (acc2.x + acc2.y) + (acc3.x + acc3.y);
+                static_cast<__half *>(p.norms)[key] = __float2half_rn(__fsqrt_rn(ss2));
+                uint32_t *dst = p.packed + (size_t)key * W;
+                if constexpr (W % 4 == 0) {
 #pragma unroll
-        for (int w0 = 0; w0 < W; w0 += WG) {
-            float acc[4 * WG][4];
+                    for (int w = 0; w < W; w += 4)
+                        *reinterpret_cast<uint4 *>(dst + w) = make_uint4(words[w], words[w + 1], words[w + 2], words[w + 3]);
+                } else if constexpr (W % 2 == 0) {
 #pragma unroll
-            for (int nt = 0; nt < 4 * WG; ++nt)
+                    for (int w = 0; w < W; w += 2) *reinterpret_cast<uint2 *>(dst + w) = make_uint2(words[w], words[w + 1]);
+                } else {
 #pragma unroll
-                for (int j = 0; j < 4; ++j) acc[nt][j] = 0.0f;
-#pragma unroll
-            for (int kt = 0; kt < 8; ++kt) {
-#pragma unroll
-                for (int np = 0; np < 2 * WG; ++np) {  // a pair of n-tiles per ldmatrix
-                    uint32_t b0, b1, b2, b3;
-                    ldsm_x4(sbase + (uint32_t)((32 * w0 + 16 * np + brow) * SROW + (2 * kt + bch) * 16), b0, b1,
-                            b2, b3);
-                    // b0, b1: sketch rows 0..7 of the pair (k 0..7, 8..15); b2, b3: rows 8..15
-                    mma_16816(acc[2 * np], a[kt][0], a[kt][1], a[kt][2], a[kt][3], b0, b1);
-                    mma_16816(acc[2 * np + 1], a[kt][0], a[kt][1], a[kt][2], a[kt][3], b2, b3);
+                    for (int w = 0; w < W; ++w) dst[w] = words[w];
                 }
-            }
-            // lane 4 g8 + t4 holds keys g8 and g8 + 8 at sketch columns 2 t4,
-            // 2 t4 + 1 of each n-tile; nibble r of a ballot is key r's four
-            // even (or odd) columns of that n-tile
-            const int r = lane & 15;
-            const int sh = 4 * (r & 7);
-#pragma unroll
-            for (int w = 0; w < WG; ++w) {
-                uint32_t word = 0;
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int nt = 4 * w + q;
-                    const uint32_t e0 = __ballot_sync(FULL_MASK, acc[nt][0] >= 0.0f);
-                    const uint32_t o0 = __ballot_sync(FULL_MASK, acc[nt][1] >= 0.0f);
-                    const uint32_t e1 = __ballot_sync(FULL_MASK, acc[nt][2] >= 0.0f);
-                    const uint32_t o1 = __ballot_sync(FULL_MASK, acc[nt][3] >= 0.0f);
-                    const uint32_t ev = r < 8 ? e0 : e1, od = r < 8 ? o0 : o1;
-                    const uint32_t byte = spread4((ev >> sh) & 15u) | (spread4((od >> sh) & 15u) << 1);
-                    word |= byte << (8 * q);
-                }
-                if (lane < 16 && row0 + r < p.N) p.packed[(size_t)(row0 + r) * W + w0 + w] = word;
             }
         }
     }
+
+    // every tcgen05.ld has completed (wait::ld) and every MMA has been
+    // consumed or abandoned: free the tensor memory
+    qt_fence_before();
+    __syncthreads();
+    qt_fence_after();
+    if (warp == 1)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TCOLS) : "memory");
 }
 
 }  // namespace
@@ -226,32 +321,28 @@ cudaError_t launch_qjl_encode(const QjlEncodeParams &p0, cudaStream_t stream)
     {
         const uint64_t dims[2] = {(uint64_t)D, (uint64_t)p.N};
         const uint64_t strides[1] = {(uint64_t)D * 2};
-        const uint32_t box[2] = {64u, (uint32_t)QJ_ROWS};
+        const uint32_t box[2] = {64u, (uint32_t)QT_M};
         if (!encode_tmap_f16(&p.tmx, p.x, 2, dims, strides, box, true, true)) return cudaErrorInvalidValue;
     }
-    const int smem = qj_smem(p.m);
+    const int smem = qt_smem(p.m);
     void (*kern)(QjlEncodeParams) = nullptr;
     switch (p.m / 32) {
-    case 1: kern = qjl_encode_kernel<1>; break;
-    case 2: kern = qjl_encode_kernel<2>; break;
-    case 3: kern = qjl_encode_kernel<3>; break;
-    case 4: kern = qjl_encode_kernel<4>; break;
-    case 5: kern = qjl_encode_kernel<5>; break;
-    case 6: kern = qjl_encode_kernel<6>; break;
-    case 7: kern = qjl_encode_kernel<7>; break;
-    case 8: kern = qjl_encode_kernel<8>; break;
+    case 1: kern = qjl_encode_tc_kernel<1>; break;
+    case 2: kern = qjl_encode_tc_kernel<2>; break;
+    case 3: kern = qjl_encode_tc_kernel<3>; break;
+    case 4: kern = qjl_encode_tc_kernel<4>; break;
+    case 5: kern = qjl_encode_tc_kernel<5>; break;
+    case 6: kern = qjl_encode_tc_kernel<6>; break;
+    case 7: kern = qjl_encode_tc_kernel<7>; break;
+    case 8: kern = qjl_encode_tc_kernel<8>; break;
     default: return cudaErrorInvalidValue;
     }
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, QJ_WARPS * 32, smem);
-    if (e != cudaSuccess) return e;
-    if (per_sm < 1) per_sm = 1;
-    const int nblk = (p.N + QJ_ROWS - 1) / QJ_ROWS;
-    const int want = (nblk + QJ_WARPS - 1) / QJ_WARPS;
-    const int grid = want < sm_count() * per_sm ? want : sm_count() * per_sm;
-    kern<<<grid, QJ_WARPS * 32, smem, stream>>>(p);
+    // one CTA per SM (it holds up to 512 tensor-memory columns)
+    const int ntiles = (p.N + QT_M - 1) / QT_M;
+    const int grid = ntiles < sm_count() ? ntiles : sm_count();
+    kern<<<grid, QT_THREADS, smem, stream>>>(p);
     return cudaGetLastError();
 }
 

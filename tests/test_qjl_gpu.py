@@ -47,7 +47,7 @@ def _check(vq, oracle_mod, x, S):
     return got, gn
 
 
-@pytest.mark.parametrize("m", [32, 64, 128, 256])
+@pytest.mark.parametrize("m", [32, 64, 96, 128, 224, 256])
 @pytest.mark.parametrize("N", [1, 5, 33, 700])
 def test_parity_small_and_ragged(vq, oracle_mod, m, N):
     from kv_cache_quantization_turboquantrvq_gb300 import synth
