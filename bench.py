@@ -257,7 +257,7 @@ def build_workload(name, dev, rank=0, layers=None, batch=None, chunked=False, ch
             Bq, H, S, _ = kd.shape
             pk = torch.empty((Bq, H, S, m // 32), dtype=torch.int32, device=dev)
             nr = torch.empty((Bq, H, S), dtype=torch.float16, device=dev)
-            ops_.append(Op("qjl_encode", "qjl_encode_kernel",
+            ops_.append(Op("qjl_encode", "qjl_encode_tc_kernel",
                            lambda: api.vq_qjl_encode(kd, s_dev, packed=pk, norms=nr, stream=st),
                            qjl_bytes(Bq * H * S, m), Bq * H * S * D))
             results_.extend([pk, nr])

@@ -206,6 +206,7 @@ __global__ void __launch_bounds__(QT_THREADS, 1) qjl_encode_tc_kernel(const __gr
                 (void)mbar_wait_bounded(&x_full[j % QT_STAGES], (uint32_t)(j / QT_STAGES) & 1u);
             }
         }
+        __syncwarp();
     } else if (warp == 1) {
         // ---- MMA issue (one thread)
         if (lane == 0) {
