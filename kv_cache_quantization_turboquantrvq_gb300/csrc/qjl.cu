@@ -17,6 +17,7 @@
 
 #include "device_common.cuh"
 #include "launch.h"
+#include "tcgen05.cuh"
 
 namespace vq {
 
@@ -54,68 +55,6 @@ __host__ __device__ constexpr int qt_smem(int m)
     // 1024-byte alignment, the sketch (two halves of m rows x 128 bytes),
     // the ring, then the barriers and the tensor-memory address slot
     return 1024 + m * 256 + QT_STAGES * QT_TILE + 256;
-}
-
-// Shared-memory matrix descriptor (tcgen05): K-major, 128-byte swizzle, rows
-// of 128 bytes in groups of 8 (stride 1024 bytes between groups); start
-// address in 16-byte units, descriptor version 1, layout type 2 (128B swizzle).
-__device__ __forceinline__ uint64_t qt_desc(uint32_t saddr)
-{
-    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
-           ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
-}
-
-// Instruction descriptor of kind::f16: fp32 accumulator, fp16 A and B, both
-// K-major, N = n, M = 128.
-__host__ __device__ constexpr uint32_t qt_idesc(int n)
-{
-    return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(QT_M >> 4) << 24);
-}
-
-__device__ __forceinline__ void qt_mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc)
-{
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-        ::"r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(acc));
-}
-
-__device__ __forceinline__ void qt_commit(uint64_t *bar)
-{
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
-                 : "memory");
-}
-
-__device__ __forceinline__ void qt_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void qt_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
-{
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
-// 32 consecutive fp32 columns of this thread's tensor-memory lane.
-__device__ __forceinline__ void qt_ld32(uint32_t taddr, uint32_t (&r)[32])
-{
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
-        "%14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-        : "r"(taddr));
-}
-
-__device__ __forceinline__ void qt_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-
-// The registers of a tcgen05.ld hold its data only after tcgen05.wait::ld:
-// an empty volatile asm that "modifies" each one, placed after the wait,
-// keeps the compiler from moving their uses above it.
-__device__ __forceinline__ void qt_hold(uint32_t (&r)[32])
-{
-#pragma unroll
-    for (int j = 0; j < 32; ++j) asm volatile("" : "+r"(r[j])::"memory");
 }
 
 // Bit j of the result: [v_j >= 0].  Adding +0 turns a negative zero into +0
@@ -171,12 +110,7 @@ __global__ void __launch_bounds__(QT_THREADS, 1) qjl_encode_tc_kernel(const __gr
         }
         fence_proxy_async_smem();  // generic-proxy writes, read by the MMA (async proxy)
     }
-    if (warp == 1) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32((const void *)tslot)),
-                     "r"(TCOLS)
-                     : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-    }
+    if (warp == 1) tmem_alloc(const_cast<uint32_t *>(tslot), TCOLS);
     qt_fence_before();
     __syncthreads();
     qt_fence_after();
@@ -309,8 +243,7 @@ __global__ void __launch_bounds__(QT_THREADS, 1) qjl_encode_tc_kernel(const __gr
     qt_fence_before();
     __syncthreads();
     qt_fence_after();
-    if (warp == 1)
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TCOLS) : "memory");
+    if (warp == 1) tmem_free(tmem, TCOLS);
 }
 
 }  // namespace

@@ -15,6 +15,7 @@ VQ_DEFINE_ERROR_WORD(g_rvq_err);
 
 #define VQ_RVQ_ERR g_rvq_err
 #include "rvq_encode.cuh"
+#include "tcgen05.cuh"
 
 namespace vq {
 
@@ -39,6 +40,289 @@ template <bool SGN>
 __global__ void __launch_bounds__(S2_WARPS * 32, 1) rvq_encode_pair4_kernel(const __grid_constant__ RvqEncodeParams p)
 {
     rvq_encode_pair4_body<SGN>(p, blockIdx.x, gridDim.x);
+}
+
+// ------------------------------------------- encode on the 5th-generation tensor cores
+//
+// The library's books (symmetric b = 2, and b = 4 with a pair table), 128 rows
+// per tile: the whole rotation S = X H128 is one D = X B^T of M = N = K = 128
+// (eight tcgen05.mma of K = 16, fp16 operands - the products x_d (+-1) are
+// exact - fp32 accumulation) into tensor memory; B = H128 diag(s) (the
+// randomised signs, when given, ride in B for free) is built once per CTA in
+// the K-major 128-byte-swizzled layout the X tiles arrive in by TMA.  Then a
+// thread owns a row: it reads its 128 accumulators (tcgen05.ld, tensor-memory
+// lane = row), takes the norm from them (sum S^2 = 128 sum x^2), quantizes
+// its coordinates in natural order and stores whole words; no butterflies,
+// no operand permutes, no cross-lane packing.  Roles (one persistent CTA per
+// SM): warp 0 streams X tiles (TMA, TE_STAGES-deep ring), warp 1 owns the
+// tensor memory and issues the MMAs (one thread), TE_G groups of four warps
+// run the epilogue on alternate tiles, each group with its own accumulator
+// buffer (128 columns).  Rows with a value inside the guard band go to the
+// warp's exact recompute (rvq_fixup_row) while the stage is still held.
+// Every wait is bounded; on a timeout the CTA records VQ_DEVERR_WAIT_TIMEOUT,
+// waits (bounded) for its copies in flight, frees its tensor memory and
+// returns.
+constexpr int TE_M = 128;
+constexpr int TE_G = 4;                       // epilogue groups (4 warps each)
+constexpr int TE_THREADS = 32 * (2 + 4 * TE_G);
+constexpr int TE_HALF = TE_M * 128;           // a 64-coordinate half of a tile (16 KB)
+constexpr int TE_TILE = 2 * TE_HALF;          // 32 KB
+constexpr int TE_BOP = 2 * 128 * 128;         // B = H128 diag(s), fp16, 32 KB
+__host__ __device__ constexpr int te_stages(int mode) { return mode == MODE_PAIR ? 3 : 4; }
+__host__ __device__ constexpr int te_smem(int mode)
+{
+    return 1024 + TE_BOP + (mode == MODE_PAIR ? P4_TAB_BYTES : 0) + te_stages(mode) * TE_TILE + 256;
+}
+static_assert(te_smem(MODE_PAIR) <= SMEM_MAX && te_smem(MODE_SYM) <= SMEM_MAX, "tensor-memory encoder shared memory");
+
+template <int MODE>
+__global__ void __launch_bounds__(TE_THREADS, 1) rvq_encode_tc_kernel(const __grid_constant__ RvqEncodeParams p)
+{
+    constexpr int BITS = MODE == MODE_PAIR ? 4 : 2;
+    constexpr int W = D * BITS / 32;  // words per row and stream
+    constexpr int NST = te_stages(MODE);
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    unsigned char *base = smem_1k(smem_raw);
+    unsigned char *bop = base;                                    // B: half h at h * 16 KB
+    uint2 *ptab = reinterpret_cast<uint2 *>(base + TE_BOP);       // MODE_PAIR only
+    unsigned char *ring = base + TE_BOP + (MODE == MODE_PAIR ? P4_TAB_BYTES : 0);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(ring + NST * TE_TILE);
+    uint64_t *x_full = bars, *x_empty = bars + NST;
+    uint64_t *acc_full = bars + 2 * NST, *acc_empty = acc_full + TE_G;
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(acc_empty + TE_G);
+    volatile uint32_t *abort_flag = tslot + 1;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int ntiles = (p.N + TE_M - 1) / TE_M;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NST; ++s) {
+            mbar_init(&x_full[s], 1);
+            mbar_init(&x_empty[s], 4);
+        }
+        for (int g = 0; g < TE_G; ++g) {
+            mbar_init(&acc_full[g], 1);
+            mbar_init(&acc_empty[g], 4);
+        }
+        *abort_flag = 0u;
+        fence_mbar_init();
+    }
+    // B[j][k] = H128[j][k] s_k, fp16, K-major with the 128-byte swizzle:
+    // 16-byte chunk c (k = 8c .. 8c + 7) of row j
+    for (int i = threadIdx.x; i < 128 * 16; i += blockDim.x) {
+        const int j = i >> 4, c = i & 15;
+        uint32_t h[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int k0 = 8 * c + 2 * e;
+            const uint32_t lo = ((__popc(j & k0) & 1) ? 0xBC00u : 0x3C00u) ^ (p.has_sgn ? (((p.sgn[k0 >> 5] >> (k0 & 31)) & 1u) << 15) : 0u);
+            const uint32_t hi = ((__popc(j & (k0 + 1)) & 1) ? 0xBC00u : 0x3C00u) ^
+                                (p.has_sgn ? (((p.sgn[(k0 + 1) >> 5] >> ((k0 + 1) & 31)) & 1u) << 15) : 0u);
+            h[e] = lo | (hi << 16);
+        }
+        *reinterpret_cast<uint4 *>(bop + (c >> 3) * TE_HALF + swz128(j, c & 7)) = make_uint4(h[0], h[1], h[2], h[3]);
+    }
+    if constexpr (MODE == MODE_PAIR)
+        for (int i = threadIdx.x; i < PT_CELLS * P4_REP; i += blockDim.x) ptab[i] = p.pt.ent[i / P4_REP];
+    fence_proxy_async_smem();  // B is read by the MMAs (async proxy)
+    if (warp == 1) tmem_alloc(tslot, 512);
+    qt_fence_before();
+    __syncthreads();
+    qt_fence_after();
+    const uint32_t tmem = *tslot;
+
+    if (warp == 0) {
+        // ---- producer
+        if (lane == 0) {
+            const uint64_t pol = l2_policy_evict_first();
+            int i = 0;
+            for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++i) {
+                const int s = i % NST;
+                if (i >= NST && !mbar_wait_bounded(&x_empty[s], (uint32_t)((i / NST) - 1) & 1u)) {
+                    atomicOr(&g_rvq_err, (unsigned)VQ_DEVERR_WAIT_TIMEOUT);
+                    *abort_flag = 1u;
+                    break;
+                }
+                if (*abort_flag) break;
+                unsigned char *dst = ring + s * TE_TILE;
+                mbar_arrive_expect_tx(&x_full[s], (uint32_t)TE_TILE);
+                tma_load_2d(dst, &p.tmap, 0, t * TE_M, &x_full[s], pol);
+                tma_load_2d(dst + TE_HALF, &p.tmap, 64, t * TE_M, &x_full[s], pol);
+            }
+            for (int k = 0; k < NST && k < i; ++k) {
+                const int j = i - 1 - k;
+                (void)mbar_wait_bounded(&x_full[j % NST], (uint32_t)(j / NST) & 1u);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ---- MMA issue: tile i into accumulator buffer i % TE_G
+        if (lane == 0) {
+            constexpr uint32_t IDESC = qt_idesc(128);
+            const uint32_t bb = smem_u32(bop), rb = smem_u32(ring);
+            int i = 0;
+            for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++i) {
+                const int s = i % NST, a = i % TE_G;
+                bool ok = mbar_wait_bounded(&x_full[s], (uint32_t)(i / NST) & 1u);
+                if (ok && i >= TE_G) ok = mbar_wait_bounded(&acc_empty[a], (uint32_t)((i / TE_G) - 1) & 1u);
+                if (!ok || *abort_flag) {
+                    if (!ok) atomicOr(&g_rvq_err, (unsigned)VQ_DEVERR_WAIT_TIMEOUT);
+                    *abort_flag = 1u;
+                    break;
+                }
+                qt_fence_after();
+                const uint32_t xa = rb + s * TE_TILE;
+#pragma unroll
+                for (int kb = 0; kb < 2; ++kb) {
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        qt_mma(tmem + (uint32_t)(a * 128), qt_desc(xa + kb * TE_HALF + kk * 32),
+                               qt_desc(bb + kb * TE_HALF + kk * 32), IDESC, (kb | kk) ? 1u : 0u);
+                }
+                qt_commit(&acc_full[a]);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ---- epilogue group g: tiles i with i % TE_G == g; thread = row
+        const int g = (warp - 2) >> 2;
+        const int q = warp & 3;  // tensor-memory lane quadrant of this warp
+        const int r = 32 * q + lane;
+        const uint32_t tl = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(g * 128);
+        // exact-recompute tables (shuffle) and book constants
+        const float tb1 = p.t1.bnd[lane];
+        const int tc1 = p.t1.code[lane];
+        const float tb2 = p.t2.bnd[lane];
+        const int tc2 = p.t2.code[lane];
+        const float tcen = p.c1[lane & ((1 << BITS) - 1)];
+        [[maybe_unused]] const float b1u = p.b1[2], b2u = p.b2[2];
+        [[maybe_unused]] const float bc2u = p.b1[2] - p.c1[2], dcu = p.c1[3] - p.c1[2];
+        [[maybe_unused]] const float kb1 = __fdiv_rn(2.0f, b1u), kb2 = __fdiv_rn(2.0f, b2u);
+        [[maybe_unused]] const float pa = p.pt.a, pbc = p.pt.bc;
+        [[maybe_unused]] const uint32_t tab =
+            smem_u32(ptab) + 8u * (uint32_t)(lane & (P4_REP - 1)) - (0x4B400000u << 7);
+        const bool dense = p.dst_off == nullptr && p.S_dst == p.S && p.S_q == p.S;
+        int i = 0;
+        for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++i) {
+            if (i % TE_G != g) continue;
+            const int s = i % NST;
+            const bool ok = mbar_wait_bounded(&acc_full[g], (uint32_t)(i / TE_G) & 1u);
+            if (!__all_sync(FULL_MASK, ok) || *abort_flag) {
+                if (!ok && lane == 0) atomicOr(&g_rvq_err, (unsigned)VQ_DEVERR_WAIT_TIMEOUT);
+                *abort_flag = 1u;
+                break;
+            }
+            qt_fence_after();
+            const int row = t * TE_M + r;
+            const bool valid = row < p.N;
+
+            // pass 1: the norm, sum S^2 / 128 in 16 partial sums
+            float2 ps[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) ps[k] = make_float2(0.0f, 0.0f);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t v[32];
+                qt_ld32(tl + 32 * c, v);
+                qt_wait_ld();
+                qt_hold(v);
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                    const float2 f = make_float2(__uint_as_float(v[2 * k]), __uint_as_float(v[2 * k + 1]));
+                    ps[k & 7] = __ffma2_rn(f, f, ps[k & 7]);
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < 4; ++k) ps[k] = __fadd2_rn(ps[k], ps[k + 4]);
+            ps[0] = __fadd2_rn(ps[0], ps[2]);
+            ps[1] = __fadd2_rn(ps[1], ps[3]);
+            ps[0] = __fadd2_rn(ps[0], ps[1]);
+            const float qn = (ps[0].x + ps[0].y) * 0.0078125f;
+            const float n = __fsqrt_rn(qn);
+            const float den = n * SQRT_D_HI;
+
+            // pass 2: quantize the row in natural coordinate order
+            uint32_t w1[W], w2[W];
+            bool flag;
+            if constexpr (MODE == MODE_SYM) {
+                const SymRow sk = sym2_row(den, p.guard * den, b1u, b2u, bc2u, dcu, kb1, kb2);
+                float m1 = __int_as_float(0x7f800000), m2 = m1;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t v[32];
+                    qt_ld32(tl + 32 * c, v);
+                    qt_wait_ld();
+                    qt_hold(v);
+                    // words 2c (coordinates 32c .. 32c + 15) and 2c + 1, code j at bits 2j
+                    uint32_t a1x = 0u, a2x = 0u, a1y = 0u, a2y = 0u;
+#pragma unroll
+                    for (int b = 15; b >= 0; --b)
+                        sym2_code2(make_float2(__uint_as_float(v[b]), __uint_as_float(v[16 + b])), sk, a1x, a2x, a1y,
+                                   a2y, m1, m2);
+                    sym2_words(a1x, a2x, w1[2 * c], w2[2 * c]);
+                    sym2_words(a1y, a2y, w1[2 * c + 1], w2[2 * c + 1]);
+                }
+                flag = !(m1 >= sk.G1) || !(m2 >= sk.G2) || !(qn > 0.0f);
+            } else {
+                const float sa = pa * __frcp_rn(den);
+                float m = __int_as_float(0x7f800000);
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t v[32];
+                    qt_ld32(tl + 32 * c, v);
+                    qt_wait_ld();
+                    qt_hold(v);
+                    // words 4c .. 4c + 3, eight coordinates each: pairs of even
+                    // coordinates collect in b0, of odd ones in b1
+#pragma unroll
+                    for (int w = 0; w < 4; ++w) {
+                        uint32_t b0 = 0u, b1 = 0u;
+#pragma unroll
+                        for (int e = 0; e < 8; e += 2) {
+                            b0 = __funnelshift_r(b0, pair_code_s(__uint_as_float(v[8 * w + e]), sa, pbc, den, tab, m), 8);
+                            b1 = __funnelshift_r(b1, pair_code_s(__uint_as_float(v[8 * w + e + 1]), sa, pbc, den, tab, m), 8);
+                        }
+                        w1[4 * c + w] = (b0 & 0x0F0F0F0Fu) | ((b1 & 0x0F0F0F0Fu) << 4);
+                        w2[4 * c + w] = ((b0 >> 4) & 0x0F0F0F0Fu) | (b1 & 0xF0F0F0F0u);
+                    }
+                }
+                flag = !(m >= p.guard * den) || !(qn > 0.0f);
+            }
+            // the accumulator buffer is free for tile i + TE_G
+            qt_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[g]);
+
+            flag = flag && valid;
+            size_t drow = (size_t)row;
+            if (valid && !flag && (dense || rvq_dst_row(p, row, drow))) {
+                uint4 *d1 = reinterpret_cast<uint4 *>(p.p1 + drow * W);
+                uint4 *d2 = reinterpret_cast<uint4 *>(p.p2 + drow * W);
+#pragma unroll
+                for (int k = 0; k < W / 4; ++k) {
+                    d1[k] = make_uint4(w1[4 * k], w1[4 * k + 1], w1[4 * k + 2], w1[4 * k + 3]);
+                    d2[k] = make_uint4(w2[4 * k], w2[4 * k + 1], w2[4 * k + 2], w2[4 * k + 3]);
+                }
+                p.norms[drow] = n;
+            }
+            // rows inside the guard band: exact recompute by the warp, from the
+            // staged tile; then the stage is free
+            unsigned fl = __ballot_sync(FULL_MASK, flag);
+            const unsigned char *xt = ring + s * TE_TILE;
+            while (fl) {
+                const int bit = __ffs(fl) - 1;
+                fl &= fl - 1;
+                rvq_fixup_row<BITS, MODE == MODE_PAIR, TE_HALF>(p, xt, 32 * q + bit, t * TE_M + 32 * q + bit, lane, tb1, tc1,
+                                                                tb2, tc2, tcen);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&x_empty[s]);
+        }
+    }
+
+    qt_fence_before();
+    __syncthreads();
+    qt_fence_after();
+    if (warp == 1) tmem_free(tmem, 512);
 }
 
 // ---------------------------------------------------------------- decode
@@ -327,9 +611,32 @@ cudaError_t launch_enc_tc(const RvqEncodeParams &p0, void (*kern)(RvqEncodeParam
     return cudaGetLastError();
 }
 
+// Launch of the tensor-memory encoder (128-row tiles): one persistent CTA per SM.
+template <int MODE>
+cudaError_t launch_enc_tm(const RvqEncodeParams &p0, cudaStream_t stream)
+{
+    RvqEncodeParams p = p0;
+    p.divS = make_fastdiv((uint32_t)p.S);
+    p.divH = make_fastdiv((uint32_t)p.H);
+    {
+        const uint64_t dims[2] = {(uint64_t)D, (uint64_t)p.N};
+        const uint64_t strides[1] = {(uint64_t)D * 2};
+        const uint32_t box[2] = {64u, (uint32_t)TE_M};
+        if (!encode_tmap_f16(&p.tmap, p.x, 2, dims, strides, box, true, true)) return cudaErrorInvalidValue;
+    }
+    auto kern = rvq_encode_tc_kernel<MODE>;
+    constexpr int smem = te_smem(MODE);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    const int ntiles = (p.N + TE_M - 1) / TE_M;
+    const int grid = ntiles < sm_count() ? ntiles : sm_count();
+    kern<<<grid, TE_THREADS, smem, stream>>>(p);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_enc_sym2(const RvqEncodeParams &p, cudaStream_t stream)
 {
-    return launch_enc_tc(p, p.has_sgn ? rvq_encode_sym2_kernel<true> : rvq_encode_sym2_kernel<false>, S2_SMEM, stream);
+    return launch_enc_tm<MODE_SYM>(p, stream);
 }
 
 // Shared memory of the b = 4 tensor-core encoder: sign masks, the replicated
@@ -339,7 +646,7 @@ static_assert(P4_SMEM <= SMEM_MAX, "b = 4 encoder shared memory");
 
 cudaError_t launch_enc_pair4(const RvqEncodeParams &p, cudaStream_t stream)
 {
-    return launch_enc_tc(p, p.has_sgn ? rvq_encode_pair4_kernel<true> : rvq_encode_pair4_kernel<false>, P4_SMEM, stream);
+    return launch_enc_tm<MODE_PAIR>(p, stream);
 }
 
 template <int BITS>

@@ -323,7 +323,9 @@ __device__ __forceinline__ void wht_lane_exact(float (&a)[4], int lane)
 //    boundary count is taken on the double-float value.
 // The row's raw values are read from the staged block (row r of it, global
 // row `row`); its words and norm go straight to global memory.
-template <int BITS, bool GRID>
+// HALF: bytes between the staged block's two 64-coordinate halves (16-row
+// blocks: ENC_BLOCK / 2; the 128-row tiles of the tensor-memory encoder: 16 KB).
+template <int BITS, bool GRID, int HALF = ENC_BLOCK / 2>
 __device__ __noinline__ void rvq_fixup_row(const RvqEncodeParams &p, const unsigned char *sblk,
                                            int r, int row, int lane, float tb1, int tc1, float tb2,
                                            int tc2, float tcen)
@@ -332,7 +334,7 @@ __device__ __noinline__ void rvq_fixup_row(const RvqEncodeParams &p, const unsig
     constexpr int W = D * BITS / 32;
     constexpr int LPW = E / 4;  // lanes per packed word
     // x[4l .. 4l+3]: box l >> 4, 16-byte chunk (l & 15) >> 1, half (l & 1)
-    uint2 raw = *reinterpret_cast<const uint2 *>(sblk + (lane >> 4) * (ENC_BLOCK / 2) +
+    uint2 raw = *reinterpret_cast<const uint2 *>(sblk + (lane >> 4) * HALF +
                                                  swz128(r, (lane & 15) >> 1) + 8 * (lane & 1));
     if (p.has_sgn) {
         raw.x ^= half2_sign_mask(sign_pair(p.sgn, 4 * lane));
