@@ -50,9 +50,10 @@ __global__ void __launch_bounds__(S2_WARPS * 32, 1) rvq_encode_pair4_kernel(cons
 // exact - fp32 accumulation) into tensor memory; B = H128 diag(s) (the
 // randomised signs, when given, ride in B for free) is built once per CTA in
 // the K-major 128-byte-swizzled layout the X tiles arrive in by TMA.  Then a
-// thread owns a row: it reads its 128 accumulators (tcgen05.ld, tensor-memory
-// lane = row), takes the norm from them (sum S^2 = 128 sum x^2), quantizes
-// its coordinates in natural order and stores whole words; no butterflies,
+// thread owns a row: it takes the norm from its fp16 row in the staged tile
+// (exact squares by mixed-precision FMAs), reads its 128 accumulators
+// (tcgen05.ld, tensor-memory lane = row), quantizes its coordinates in
+// natural order and stores whole words; no butterflies,
 // no operand permutes, no cross-lane packing.  Roles (one persistent CTA per
 // SM): warp 0 streams X tiles (TMA, TE_STAGES-deep ring), warp 1 owns the
 // tensor memory and issues the MMAs (one thread), TE_G groups of four warps
@@ -62,6 +63,21 @@ __global__ void __launch_bounds__(S2_WARPS * 32, 1) rvq_encode_pair4_kernel(cons
 // Every wait is bounded; on a timeout the CTA records VQ_DEVERR_WAIT_TIMEOUT,
 // waits (bounded) for its copies in flight, frees its tensor memory and
 // returns.
+// Sum of the squares of the 8 fp16 values of a 16-byte chunk: each square
+// exact (fp16 operands, fp32 result of a mixed-precision FMA), 8 fp32 sums.
+__device__ __forceinline__ float sq8_f16(uint4 v)
+{
+    float a = 0.0f;
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const unsigned short lo = (unsigned short)(w[j] & 0xffffu), hi = (unsigned short)(w[j] >> 16);
+        asm("fma.rn.f32.f16 %0, %1, %1, %0;" : "+f"(a) : "h"(lo));
+        asm("fma.rn.f32.f16 %0, %1, %1, %0;" : "+f"(a) : "h"(hi));
+    }
+    return a;
+}
+
 constexpr int TE_M = 128;
 constexpr int TE_G = 4;                       // epilogue groups (4 warps each)
 constexpr int TE_THREADS = 32 * (2 + 4 * TE_G);
@@ -215,28 +231,26 @@ __global__ void __launch_bounds__(TE_THREADS, 1) rvq_encode_tc_kernel(const __gr
             const int row = t * TE_M + r;
             const bool valid = row < p.N;
 
-            // pass 1: the norm, sum S^2 / 128 in 16 partial sums
-            float2 ps[8];
+            // the norm from the row's fp16 values in the staged tile: exact
+            // squares (fp16 operands, fp32 result), fp32 sums in 16 partial
+            // sums of 8 (12 roundings deep at most)
+            const unsigned char *xt = ring + s * TE_TILE;
+            float ps[16];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) ps[k] = make_float2(0.0f, 0.0f);
+            for (int h = 0; h < 2; ++h) {
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t v[32];
-                qt_ld32(tl + 32 * c, v);
-                qt_wait_ld();
-                qt_hold(v);
-#pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                    const float2 f = make_float2(__uint_as_float(v[2 * k]), __uint_as_float(v[2 * k + 1]));
-                    ps[k & 7] = __ffma2_rn(f, f, ps[k & 7]);
+                for (int c = 0; c < 8; ++c) {
+                    const uint4 v = *reinterpret_cast<const uint4 *>(xt + h * TE_HALF + swz128(r, c));
+                    ps[8 * h + c] = sq8_f16(v);
                 }
             }
 #pragma unroll
-            for (int k = 0; k < 4; ++k) ps[k] = __fadd2_rn(ps[k], ps[k + 4]);
-            ps[0] = __fadd2_rn(ps[0], ps[2]);
-            ps[1] = __fadd2_rn(ps[1], ps[3]);
-            ps[0] = __fadd2_rn(ps[0], ps[1]);
-            const float qn = (ps[0].x + ps[0].y) * 0.0078125f;
+            for (int k = 0; k < 8; ++k) ps[k] += ps[k + 8];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) ps[k] += ps[k + 4];
+            ps[0] += ps[2];
+            ps[1] += ps[3];
+            const float qn = ps[0] + ps[1];
             const float n = __fsqrt_rn(qn);
             const float den = n * SQRT_D_HI;
 
@@ -307,7 +321,6 @@ __global__ void __launch_bounds__(TE_THREADS, 1) rvq_encode_tc_kernel(const __gr
             // rows inside the guard band: exact recompute by the warp, from the
             // staged tile; then the stage is free
             unsigned fl = __ballot_sync(FULL_MASK, flag);
-            const unsigned char *xt = ring + s * TE_TILE;
             while (fl) {
                 const int bit = __ffs(fl) - 1;
                 fl &= fl - 1;
