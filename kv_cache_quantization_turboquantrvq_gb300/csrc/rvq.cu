@@ -253,6 +253,12 @@ __global__ void __launch_bounds__(TE_THREADS, 1) rvq_encode_tc_kernel(const __gr
             const float qn = ps[0] + ps[1];
             const float n = __fsqrt_rn(qn);
             const float den = n * SQRT_D_HI;
+            // the staged tile has been read (the MMAs are done with it too):
+            // free the stage now, so that the producer keeps the ring full
+            // through the quantization (a flagged row is re-read from global
+            // memory by the exact recompute)
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&x_empty[s]);
 
             // pass 2: quantize the row in natural coordinate order
             uint32_t w1[W], w2[W];
@@ -318,17 +324,16 @@ __global__ void __launch_bounds__(TE_THREADS, 1) rvq_encode_tc_kernel(const __gr
                 }
                 p.norms[drow] = n;
             }
-            // rows inside the guard band: exact recompute by the warp, from the
-            // staged tile; then the stage is free
+            // rows inside the guard band: exact recompute by the warp, the row
+            // read again from global memory
             unsigned fl = __ballot_sync(FULL_MASK, flag);
             while (fl) {
                 const int bit = __ffs(fl) - 1;
                 fl &= fl - 1;
-                rvq_fixup_row<BITS, MODE == MODE_PAIR, TE_HALF>(p, xt, 32 * q + bit, t * TE_M + 32 * q + bit, lane, tb1, tc1,
-                                                                tb2, tc2, tcen);
+                rvq_fixup_row<BITS, MODE == MODE_PAIR, 0>(p, nullptr, 32 * q + bit, t * TE_M + 32 * q + bit, lane, tb1, tc1,
+                                                          tb2, tc2, tcen);
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(&x_empty[s]);
         }
     }
 

@@ -324,7 +324,8 @@ __device__ __forceinline__ void wht_lane_exact(float (&a)[4], int lane)
 // The row's raw values are read from the staged block (row r of it, global
 // row `row`); its words and norm go straight to global memory.
 // HALF: bytes between the staged block's two 64-coordinate halves (16-row
-// blocks: ENC_BLOCK / 2; the 128-row tiles of the tensor-memory encoder: 16 KB).
+// blocks: ENC_BLOCK / 2); HALF = 0: the row is read from global memory (the
+// input, p.x), where it is contiguous.
 template <int BITS, bool GRID, int HALF = ENC_BLOCK / 2>
 __device__ __noinline__ void rvq_fixup_row(const RvqEncodeParams &p, const unsigned char *sblk,
                                            int r, int row, int lane, float tb1, int tc1, float tb2,
@@ -334,8 +335,11 @@ __device__ __noinline__ void rvq_fixup_row(const RvqEncodeParams &p, const unsig
     constexpr int W = D * BITS / 32;
     constexpr int LPW = E / 4;  // lanes per packed word
     // x[4l .. 4l+3]: box l >> 4, 16-byte chunk (l & 15) >> 1, half (l & 1)
-    uint2 raw = *reinterpret_cast<const uint2 *>(sblk + (lane >> 4) * HALF +
-                                                 swz128(r, (lane & 15) >> 1) + 8 * (lane & 1));
+    uint2 raw;
+    if constexpr (HALF == 0)
+        raw = __ldg(reinterpret_cast<const uint2 *>(static_cast<const unsigned char *>(p.x) + (size_t)row * ROW_BYTES) + lane);
+    else
+        raw = *reinterpret_cast<const uint2 *>(sblk + (lane >> 4) * HALF + swz128(r, (lane & 15) >> 1) + 8 * (lane & 1));
     if (p.has_sgn) {
         raw.x ^= half2_sign_mask(sign_pair(p.sgn, 4 * lane));
         raw.y ^= half2_sign_mask(sign_pair(p.sgn, 4 * lane + 2));
