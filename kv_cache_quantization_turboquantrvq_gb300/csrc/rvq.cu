@@ -30,18 +30,6 @@ __global__ void __launch_bounds__(enc_warps(BITS, MODE) * 32, 1)
     rvq_encode_body<BITS, MODE, SGN>(p, blockIdx.x, gridDim.x);
 }
 
-template <bool SGN>
-__global__ void __launch_bounds__(S2_WARPS * 32, 1) rvq_encode_sym2_kernel(const __grid_constant__ RvqEncodeParams p)
-{
-    rvq_encode_sym2_body<SGN>(p, blockIdx.x, gridDim.x);
-}
-
-template <bool SGN>
-__global__ void __launch_bounds__(S2_WARPS * 32, 1) rvq_encode_pair4_kernel(const __grid_constant__ RvqEncodeParams p)
-{
-    rvq_encode_pair4_body<SGN>(p, blockIdx.x, gridDim.x);
-}
-
 // ------------------------------------------- encode on the 5th-generation tensor cores
 //
 // The library's books (symmetric b = 2, and b = 4 with a pair table), 128 rows
@@ -92,7 +80,7 @@ __host__ __device__ constexpr int te_smem(int mode)
 static_assert(te_smem(MODE_PAIR) <= SMEM_MAX && te_smem(MODE_SYM) <= SMEM_MAX, "tensor-memory encoder shared memory");
 
 template <int MODE>
-__global__ void __launch_bounds__(TE_THREADS, 1) rvq_encode_tc_kernel(const __grid_constant__ RvqEncodeParams p)
+__global__ void __maxnreg__(112) rvq_encode_tc_kernel(const __grid_constant__ RvqEncodeParams p)
 {
     constexpr int BITS = MODE == MODE_PAIR ? 4 : 2;
     constexpr int W = D * BITS / 32;  // words per row and stream
@@ -260,39 +248,53 @@ __global__ void __launch_bounds__(TE_THREADS, 1) rvq_encode_tc_kernel(const __gr
             __syncwarp();
             if (lane == 0) mbar_arrive(&x_empty[s]);
 
-            // pass 2: quantize the row in natural coordinate order
-            uint32_t w1[W], w2[W];
+            // pass 2: quantize the row in natural coordinate order, 32
+            // coordinates (one tensor-memory load) at a time, the next load in
+            // flight during each chunk; the words go straight to the row's
+            // destination (a flagged row is rewritten by the exact recompute)
+            size_t drow = (size_t)row;
+            const bool okrow = valid && (dense || rvq_dst_row(p, row, drow));
+            uint32_t *d1 = p.p1 + drow * W, *d2 = p.p2 + drow * W;
+            uint32_t va[32], vb[32];
             bool flag;
             if constexpr (MODE == MODE_SYM) {
                 const SymRow sk = sym2_row(den, p.guard * den, b1u, b2u, bc2u, dcu, kb1, kb2);
                 float m1 = __int_as_float(0x7f800000), m2 = m1;
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t v[32];
-                    qt_ld32(tl + 32 * c, v);
-                    qt_wait_ld();
-                    qt_hold(v);
-                    // words 2c (coordinates 32c .. 32c + 15) and 2c + 1, code j at bits 2j
+                // words 2c (coordinates 32c .. 32c + 15) and 2c + 1, code j at bits 2j
+                auto chunk = [&](const uint32_t (&v)[32], int c) {
                     uint32_t a1x = 0u, a2x = 0u, a1y = 0u, a2y = 0u;
 #pragma unroll
                     for (int b = 15; b >= 0; --b)
                         sym2_code2(make_float2(__uint_as_float(v[b]), __uint_as_float(v[16 + b])), sk, a1x, a2x, a1y,
                                    a2y, m1, m2);
-                    sym2_words(a1x, a2x, w1[2 * c], w2[2 * c]);
-                    sym2_words(a1y, a2y, w1[2 * c + 1], w2[2 * c + 1]);
+                    uint32_t x1, x2, y1, y2;
+                    sym2_words(a1x, a2x, x1, x2);
+                    sym2_words(a1y, a2y, y1, y2);
+                    if (okrow) {
+                        *reinterpret_cast<uint2 *>(d1 + 2 * c) = make_uint2(x1, y1);
+                        *reinterpret_cast<uint2 *>(d2 + 2 * c) = make_uint2(x2, y2);
+                    }
+                };
+                qt_ld32(tl, va);
+#pragma unroll 1
+                for (int c = 0; c < 4; c += 2) {
+                    qt_wait_ld();
+                    qt_hold(va);
+                    qt_ld32(tl + 32 * (c + 1), vb);
+                    chunk(va, c);
+                    qt_wait_ld();
+                    qt_hold(vb);
+                    if (c + 2 < 4) qt_ld32(tl + 32 * (c + 2), va);
+                    chunk(vb, c + 1);
                 }
                 flag = !(m1 >= sk.G1) || !(m2 >= sk.G2) || !(qn > 0.0f);
             } else {
                 const float sa = pa * __frcp_rn(den);
                 float m = __int_as_float(0x7f800000);
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t v[32];
-                    qt_ld32(tl + 32 * c, v);
-                    qt_wait_ld();
-                    qt_hold(v);
-                    // words 4c .. 4c + 3, eight coordinates each: pairs of even
-                    // coordinates collect in b0, of odd ones in b1
+                // words 4c .. 4c + 3, eight coordinates each: pairs of even
+                // coordinates collect in b0, of odd ones in b1
+                auto chunk = [&](const uint32_t (&v)[32], int c) {
+                    uint32_t o1[4], o2[4];
 #pragma unroll
                     for (int w = 0; w < 4; ++w) {
                         uint32_t b0 = 0u, b1 = 0u;
@@ -301,9 +303,25 @@ __global__ void __launch_bounds__(TE_THREADS, 1) rvq_encode_tc_kernel(const __gr
                             b0 = __funnelshift_r(b0, pair_code_s(__uint_as_float(v[8 * w + e]), sa, pbc, den, tab, m), 8);
                             b1 = __funnelshift_r(b1, pair_code_s(__uint_as_float(v[8 * w + e + 1]), sa, pbc, den, tab, m), 8);
                         }
-                        w1[4 * c + w] = (b0 & 0x0F0F0F0Fu) | ((b1 & 0x0F0F0F0Fu) << 4);
-                        w2[4 * c + w] = ((b0 >> 4) & 0x0F0F0F0Fu) | (b1 & 0xF0F0F0F0u);
+                        o1[w] = (b0 & 0x0F0F0F0Fu) | ((b1 & 0x0F0F0F0Fu) << 4);
+                        o2[w] = ((b0 >> 4) & 0x0F0F0F0Fu) | (b1 & 0xF0F0F0F0u);
                     }
+                    if (okrow) {
+                        *reinterpret_cast<uint4 *>(d1 + 4 * c) = make_uint4(o1[0], o1[1], o1[2], o1[3]);
+                        *reinterpret_cast<uint4 *>(d2 + 4 * c) = make_uint4(o2[0], o2[1], o2[2], o2[3]);
+                    }
+                };
+                qt_ld32(tl, va);
+#pragma unroll 1
+                for (int c = 0; c < 4; c += 2) {
+                    qt_wait_ld();
+                    qt_hold(va);
+                    qt_ld32(tl + 32 * (c + 1), vb);
+                    chunk(va, c);
+                    qt_wait_ld();
+                    qt_hold(vb);
+                    if (c + 2 < 4) qt_ld32(tl + 32 * (c + 2), va);
+                    chunk(vb, c + 1);
                 }
                 flag = !(m >= p.guard * den) || !(qn > 0.0f);
             }
@@ -313,17 +331,8 @@ __global__ void __launch_bounds__(TE_THREADS, 1) rvq_encode_tc_kernel(const __gr
             if (lane == 0) mbar_arrive(&acc_empty[g]);
 
             flag = flag && valid;
-            size_t drow = (size_t)row;
-            if (valid && !flag && (dense || rvq_dst_row(p, row, drow))) {
-                uint4 *d1 = reinterpret_cast<uint4 *>(p.p1 + drow * W);
-                uint4 *d2 = reinterpret_cast<uint4 *>(p.p2 + drow * W);
-#pragma unroll
-                for (int k = 0; k < W / 4; ++k) {
-                    d1[k] = make_uint4(w1[4 * k], w1[4 * k + 1], w1[4 * k + 2], w1[4 * k + 3]);
-                    d2[k] = make_uint4(w2[4 * k], w2[4 * k + 1], w2[4 * k + 2], w2[4 * k + 3]);
-                }
-                p.norms[drow] = n;
-            }
+            if (okrow && !flag) p.norms[drow] = n;
+            __syncwarp();  // the fast words of a flagged row are written before its exact ones
             // rows inside the guard band: exact recompute by the warp, the row
             // read again from global memory
             unsigned fl = __ballot_sync(FULL_MASK, flag);
@@ -608,27 +617,6 @@ cudaError_t launch_enc(const RvqEncodeParams &p0, cudaStream_t stream)
     return cudaGetLastError();
 }
 
-// Shared memory of the symmetric b = 2 tensor-core encoder: sign masks, the
-// warps' rings, their mbarriers (same layout as the generic encoder's).
-constexpr int S2_SMEM = 1024 + ENC_SGN_BYTES + S2_WARPS * S2_STAGES * (ENC_BLOCK + 8);
-static_assert(S2_SMEM <= SMEM_MAX, "symmetric encoder shared memory");
-
-// Launch of the tensor-core encoders: one persistent 16-warp CTA per SM.
-cudaError_t launch_enc_tc(const RvqEncodeParams &p0, void (*kern)(RvqEncodeParams), int smem, cudaStream_t stream)
-{
-    RvqEncodeParams p = p0;
-    if (!prepare_rvq_encode(p)) return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    const int nblk = (p.N + ER - 1) / ER;
-    int grid = (nblk + S2_WARPS - 1) / S2_WARPS;
-    const int sms = sm_count();
-    if (grid > sms) grid = sms;
-    if (grid < 1) grid = 1;
-    kern<<<grid, S2_WARPS * 32, smem, stream>>>(p);
-    return cudaGetLastError();
-}
-
 // Launch of the tensor-memory encoder (128-row tiles): one persistent CTA per SM.
 template <int MODE>
 cudaError_t launch_enc_tm(const RvqEncodeParams &p0, cudaStream_t stream)
@@ -657,10 +645,6 @@ cudaError_t launch_enc_sym2(const RvqEncodeParams &p, cudaStream_t stream)
     return launch_enc_tm<MODE_SYM>(p, stream);
 }
 
-// Shared memory of the b = 4 tensor-core encoder: sign masks, the replicated
-// pair table, the warps' two-stage rings and their mbarriers.
-constexpr int P4_SMEM = 1024 + ENC_SGN_BYTES + P4_TAB_BYTES + S2_WARPS * P4_STAGES * (ENC_BLOCK + 8);
-static_assert(P4_SMEM <= SMEM_MAX, "b = 4 encoder shared memory");
 
 cudaError_t launch_enc_pair4(const RvqEncodeParams &p, cudaStream_t stream)
 {
