@@ -67,7 +67,7 @@ __device__ __forceinline__ float sq8_f16(uint4 v)
 }
 
 constexpr int TE_M = 128;
-constexpr int TE_G = 4;                       // epilogue groups (4 warps each)
+constexpr int TE_G = 3;                       // epilogue groups (4 warps each)
 constexpr int TE_THREADS = 32 * (2 + 4 * TE_G);
 constexpr int TE_HALF = TE_M * 128;           // a 64-coordinate half of a tile (16 KB)
 constexpr int TE_TILE = 2 * TE_HALF;          // 32 KB
@@ -80,7 +80,7 @@ __host__ __device__ constexpr int te_smem(int mode)
 static_assert(te_smem(MODE_PAIR) <= SMEM_MAX && te_smem(MODE_SYM) <= SMEM_MAX, "tensor-memory encoder shared memory");
 
 template <int MODE>
-__global__ void __maxnreg__(112) rvq_encode_tc_kernel(const __grid_constant__ RvqEncodeParams p)
+__global__ void __launch_bounds__(TE_THREADS, 1) rvq_encode_tc_kernel(const __grid_constant__ RvqEncodeParams p)
 {
     constexpr int BITS = MODE == MODE_PAIR ? 4 : 2;
     constexpr int W = D * BITS / 32;  // words per row and stream
