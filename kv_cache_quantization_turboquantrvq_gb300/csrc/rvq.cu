@@ -110,10 +110,16 @@ __global__ void __launch_bounds__(TE_THREADS, 1) rvq_encode_tc_kernel(const __gr
         *abort_flag = 0u;
         fence_mbar_init();
     }
-    // B[j][k] = H128[j][k] s_k, fp16, K-major with the 128-byte swizzle:
-    // 16-byte chunk c (k = 8c .. 8c + 7) of row j
+    // B[n][k] = H128[j(n)][k] s_k, fp16, K-major with the 128-byte swizzle:
+    // 16-byte chunk c (k = 8c .. 8c + 7) of row n.  Row n of B is column n of
+    // the accumulator; for the symmetric books the output coordinates are
+    // interleaved so that a thread's registers 2b and 2b + 1 of a 32-column
+    // load are coordinates 32q + b and 32q + 16 + b (the two words the
+    // quantizer fills side by side, as one fp32 pair): j(32q + 2b + e) =
+    // 32q + 16e + b.  The b = 4 quantizer works per coordinate: j(n) = n.
     for (int i = threadIdx.x; i < 128 * 16; i += blockDim.x) {
-        const int j = i >> 4, c = i & 15;
+        const int n = i >> 4, c = i & 15;
+        const int j = MODE == MODE_SYM ? (n & ~31) + 16 * (n & 1) + ((n & 31) >> 1) : n;
         uint32_t h[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -123,7 +129,7 @@ __global__ void __launch_bounds__(TE_THREADS, 1) rvq_encode_tc_kernel(const __gr
                                 (p.has_sgn ? (((p.sgn[(k0 + 1) >> 5] >> ((k0 + 1) & 31)) & 1u) << 15) : 0u);
             h[e] = lo | (hi << 16);
         }
-        *reinterpret_cast<uint4 *>(bop + (c >> 3) * TE_HALF + swz128(j, c & 7)) = make_uint4(h[0], h[1], h[2], h[3]);
+        *reinterpret_cast<uint4 *>(bop + (c >> 3) * TE_HALF + swz128(n, c & 7)) = make_uint4(h[0], h[1], h[2], h[3]);
     }
     if constexpr (MODE == MODE_PAIR)
         for (int i = threadIdx.x; i < PT_CELLS * P4_REP; i += blockDim.x) ptab[i] = p.pt.ent[i / P4_REP];
@@ -265,8 +271,8 @@ __global__ void __launch_bounds__(TE_THREADS, 1) rvq_encode_tc_kernel(const __gr
                     uint32_t a1x = 0u, a2x = 0u, a1y = 0u, a2y = 0u;
 #pragma unroll
                     for (int b = 15; b >= 0; --b)
-                        sym2_code2(make_float2(__uint_as_float(v[b]), __uint_as_float(v[16 + b])), sk, a1x, a2x, a1y,
-                                   a2y, m1, m2);
+                        sym2_code2(make_float2(__uint_as_float(v[2 * b]), __uint_as_float(v[2 * b + 1])), sk, a1x, a2x,
+                                   a1y, a2y, m1, m2);
                     uint32_t x1, x2, y1, y2;
                     sym2_words(a1x, a2x, x1, x2);
                     sym2_words(a1y, a2y, y1, y2);
