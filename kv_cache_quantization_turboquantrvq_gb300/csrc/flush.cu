@@ -32,7 +32,7 @@ namespace vq {
 namespace {
 
 constexpr int FL_WARPS = 16;
-static_assert(S2_WARPS == FL_WARPS && enc_warps(1, MODE_SYM) == FL_WARPS, "encoder bodies run 16 warps");
+static_assert(enc_warps(1, MODE_SYM) == FL_WARPS && TE_THREADS <= FL_WARPS * 32, "encoder bodies fit 16 warps");
 static_assert(key_warps<2, 32>() == FL_WARPS && key_warps<4, 64>() == FL_WARPS, "key bodies run 16 warps");
 
 constexpr int WIN_ROWS = 16;  // window rows per warp item
@@ -74,12 +74,24 @@ __device__ __forceinline__ void window_body(const FlushWindowParams &w, int cta,
 
 // Each part is its own function (not inlined), so that the register
 // allocation of one part does not weigh on the others.
-__device__ __noinline__ void part_rvq(const FlushParams &p, int c)
+__device__ __noinline__ void part_rvq1(const RvqEncodeParams &q, int c, int n)
+{
+    rvq_encode_body<1, MODE_SYM, false>(q, c, n);
+}
+
+// the tensor-memory encoder runs 14 of the CTA's 16 warps
+template <int MODE>
+__device__ __noinline__ void part_rvq_tm(const RvqEncodeParams &q, int c, int n)
+{
+    rvq_encode_tm_body<MODE>(q, c, n);
+}
+
+__device__ __forceinline__ void part_rvq(const FlushParams &p, int c)
 {
     switch (p.rvq_kind) {
-    case 1: rvq_encode_body<1, MODE_SYM, false>(p.rvq, c, p.n_rvq); break;
-    case 2: rvq_encode_sym2_body<false>(p.rvq, c, p.n_rvq); break;
-    default: rvq_encode_pair4_body<false>(p.rvq, c, p.n_rvq); break;
+    case 1: part_rvq1(p.rvq, c, p.n_rvq); break;
+    case 2: part_rvq_tm<MODE_SYM>(p.rvq, c, p.n_rvq); break;
+    default: part_rvq_tm<MODE_PAIR>(p.rvq, c, p.n_rvq); break;
     }
 }
 
@@ -142,8 +154,8 @@ int rvq_part_smem(int kind)
 {
     switch (kind) {
     case 1: return enc_smem(1, MODE_SYM);
-    case 2: return 1024 + ENC_SGN_BYTES + S2_WARPS * S2_STAGES * (ENC_BLOCK + 8);
-    default: return 1024 + ENC_SGN_BYTES + P4_TAB_BYTES + S2_WARPS * P4_STAGES * (ENC_BLOCK + 8);
+    case 2: return te_smem(MODE_SYM);
+    default: return te_smem(MODE_PAIR);
     }
 }
 int keys_part_smem(int G) { return 1024 + FL_WARPS * ((G <= 64 ? 1 : 2) * G * KEY_ROW + 16); }
@@ -160,9 +172,14 @@ cudaError_t launch_flush(FlushParams &p, cudaStream_t stream)
     double bytes[4] = {0, 0, 0, 0};
     int smem = 0;
     if (p.rvq_kind && p.rvq.S_q == 0) p.rvq_kind = 0;  // every token stays fp16
+    long long rvq_ctas = 0;  // CTAs the RVQ part can use
     if (p.rvq_kind) {
-        if (!prepare_rvq_encode(p.rvq)) return cudaErrorInvalidValue;
-        items[0] = (rq + 15) / 16;
+        // the tensor-memory encoder takes 128-row tiles (one CTA each at a
+        // time), the b = 1 encoder 16-row blocks (one per warp)
+        const int rows_per_item = p.rvq_kind == 1 ? 16 : TE_M;
+        if (!prepare_rvq_encode(p.rvq, rows_per_item)) return cudaErrorInvalidValue;
+        items[0] = (rq + rows_per_item - 1) / rows_per_item;
+        rvq_ctas = p.rvq_kind == 1 ? (items[0] + FL_WARPS - 1) / FL_WARPS : items[0];
         const long long rows_q = (long long)p.rvq.N / p.rvq.S * p.rvq.S_q;
         bytes[0] = (double)rows_q * (256 + 2 * 16 * p.rvq_kind + 4);
         smem = rvq_part_smem(p.rvq_kind);
@@ -209,7 +226,7 @@ cudaError_t launch_flush(FlushParams &p, cudaStream_t stream)
     const int budget = sms > parts ? sms : parts;
     for (int i = 0; i < 4; ++i) {
         if (items[i] == 0) continue;
-        const long long useful = (items[i] + FL_WARPS - 1) / FL_WARPS;
+        const long long useful = i == 0 ? rvq_ctas : (items[i] + FL_WARPS - 1) / FL_WARPS;
         long long want = (long long)(budget * (cost[i] / total) + 0.5);
         if (want < 1) want = 1;
         if (want > useful) want = useful;

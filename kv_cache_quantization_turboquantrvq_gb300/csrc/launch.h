@@ -191,7 +191,9 @@ enum RvqMode { RVQ_MODE_PLAIN = 0, RVQ_MODE_GRID = 1, RVQ_MODE_SYM = 2, RVQ_MODE
 cudaError_t launch_rvq_encode(const RvqEncodeParams &p, int bits, int mode, cudaStream_t stream);
 // Fill the launcher-set fields (fast divisors, tensor map) of encoder and
 // KIVI-quantizer parameters; false if the tensor map cannot be encoded.
-bool prepare_rvq_encode(RvqEncodeParams &p);
+// box_rows: rows per TMA box of the input (16: the two-threads-per-row
+// encoder; 128: the tensor-memory encoder's tiles).
+bool prepare_rvq_encode(RvqEncodeParams &p, int box_rows);
 bool prepare_kivi_quant(KiviQuantParams &p, bool per_channel);
 
 // Decode-time flush of one layer in one launch (flush.cu): the RVQ encode of
@@ -208,7 +210,8 @@ struct FlushParams {
     RvqEncodeParams rvq;     // the keys' RVQ part (rvq_kind != 0)
     KiviQuantParams kk, kv;  // KIVI keys / values (x == nullptr: absent)
     FlushWindowParams win;
-    int rvq_kind;            // 0: none; 1, 2: symmetric b = 1, 2 books; 4: b = 4 pair table
+    int rvq_kind;            // 0: none; 1: symmetric b = 1 books (16-row blocks); 2, 4: the
+                             // tensor-memory encoder (symmetric b = 2, b = 4 pair table)
     int kbits;               // KIVI bits (2 or 4; group 32 or 64) when kk or kv is present
     int n_rvq, n_kk, n_kv, n_win;  // CTAs of each part (set by the launcher)
 };

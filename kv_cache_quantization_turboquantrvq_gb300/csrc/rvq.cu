@@ -15,7 +15,6 @@ VQ_DEFINE_ERROR_WORD(g_rvq_err);
 
 #define VQ_RVQ_ERR g_rvq_err
 #include "rvq_encode.cuh"
-#include "tcgen05.cuh"
 
 namespace vq {
 
@@ -30,332 +29,12 @@ __global__ void __launch_bounds__(enc_warps(BITS, MODE) * 32, 1)
     rvq_encode_body<BITS, MODE, SGN>(p, blockIdx.x, gridDim.x);
 }
 
-// ------------------------------------------- encode on the 5th-generation tensor cores
-//
-// The library's books (symmetric b = 2, and b = 4 with a pair table), 128 rows
-// per tile: the whole rotation S = X H128 is one D = X B^T of M = N = K = 128
-// (eight tcgen05.mma of K = 16, fp16 operands - the products x_d (+-1) are
-// exact - fp32 accumulation) into tensor memory; B = H128 diag(s) (the
-// randomised signs, when given, ride in B for free) is built once per CTA in
-// the K-major 128-byte-swizzled layout the X tiles arrive in by TMA.  Then a
-// thread owns a row: it takes the norm from its fp16 row in the staged tile
-// (exact squares by mixed-precision FMAs), reads its 128 accumulators
-// (tcgen05.ld, tensor-memory lane = row), quantizes its coordinates in
-// natural order and stores whole words; no butterflies,
-// no operand permutes, no cross-lane packing.  Roles (one persistent CTA per
-// SM): warp 0 streams X tiles (TMA, TE_STAGES-deep ring), warp 1 owns the
-// tensor memory and issues the MMAs (one thread), TE_G groups of four warps
-// run the epilogue on alternate tiles, each group with its own accumulator
-// buffer (128 columns).  Rows with a value inside the guard band go to the
-// warp's exact recompute (rvq_fixup_row) while the stage is still held.
-// Every wait is bounded; on a timeout the CTA records VQ_DEVERR_WAIT_TIMEOUT,
-// waits (bounded) for its copies in flight, frees its tensor memory and
-// returns.
-// Sum of the squares of the 8 fp16 values of a 16-byte chunk: each square
-// exact (fp16 operands, fp32 result of a mixed-precision FMA), 8 fp32 sums.
-__device__ __forceinline__ float sq8_f16(uint4 v)
-{
-    float a = 0.0f;
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const unsigned short lo = (unsigned short)(w[j] & 0xffffu), hi = (unsigned short)(w[j] >> 16);
-        asm("fma.rn.f32.f16 %0, %1, %1, %0;" : "+f"(a) : "h"(lo));
-        asm("fma.rn.f32.f16 %0, %1, %1, %0;" : "+f"(a) : "h"(hi));
-    }
-    return a;
-}
-
-constexpr int TE_M = 128;
-constexpr int TE_G = 3;                       // epilogue groups (4 warps each)
-constexpr int TE_THREADS = 32 * (2 + 4 * TE_G);
-constexpr int TE_HALF = TE_M * 128;           // a 64-coordinate half of a tile (16 KB)
-constexpr int TE_TILE = 2 * TE_HALF;          // 32 KB
-constexpr int TE_BOP = 2 * 128 * 128;         // B = H128 diag(s), fp16, 32 KB
-__host__ __device__ constexpr int te_stages(int mode) { return mode == MODE_PAIR ? 3 : 4; }
-__host__ __device__ constexpr int te_smem(int mode)
-{
-    return 1024 + TE_BOP + (mode == MODE_PAIR ? P4_TAB_BYTES : 0) + te_stages(mode) * TE_TILE + 256;
-}
-static_assert(te_smem(MODE_PAIR) <= SMEM_MAX && te_smem(MODE_SYM) <= SMEM_MAX, "tensor-memory encoder shared memory");
-
+// The tensor-memory encoder of the library's books (rvq_encode.cuh), one
+// persistent CTA per SM.
 template <int MODE>
 __global__ void __launch_bounds__(TE_THREADS, 1) rvq_encode_tc_kernel(const __grid_constant__ RvqEncodeParams p)
 {
-    constexpr int BITS = MODE == MODE_PAIR ? 4 : 2;
-    constexpr int W = D * BITS / 32;  // words per row and stream
-    constexpr int NST = te_stages(MODE);
-    extern __shared__ __align__(128) unsigned char smem_raw[];
-    unsigned char *base = smem_1k(smem_raw);
-    unsigned char *bop = base;                                    // B: half h at h * 16 KB
-    uint2 *ptab = reinterpret_cast<uint2 *>(base + TE_BOP);       // MODE_PAIR only
-    unsigned char *ring = base + TE_BOP + (MODE == MODE_PAIR ? P4_TAB_BYTES : 0);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(ring + NST * TE_TILE);
-    uint64_t *x_full = bars, *x_empty = bars + NST;
-    uint64_t *acc_full = bars + 2 * NST, *acc_empty = acc_full + TE_G;
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(acc_empty + TE_G);
-    volatile uint32_t *abort_flag = tslot + 1;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int ntiles = (p.N + TE_M - 1) / TE_M;
-
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < NST; ++s) {
-            mbar_init(&x_full[s], 1);
-            mbar_init(&x_empty[s], 4);
-        }
-        for (int g = 0; g < TE_G; ++g) {
-            mbar_init(&acc_full[g], 1);
-            mbar_init(&acc_empty[g], 4);
-        }
-        *abort_flag = 0u;
-        fence_mbar_init();
-    }
-    // B[n][k] = H128[j(n)][k] s_k, fp16, K-major with the 128-byte swizzle:
-    // 16-byte chunk c (k = 8c .. 8c + 7) of row n.  Row n of B is column n of
-    // the accumulator; for the symmetric books the output coordinates are
-    // interleaved so that a thread's registers 2b and 2b + 1 of a 32-column
-    // load are coordinates 32q + b and 32q + 16 + b (the two words the
-    // quantizer fills side by side, as one fp32 pair): j(32q + 2b + e) =
-    // 32q + 16e + b.  The b = 4 quantizer works per coordinate: j(n) = n.
-    for (int i = threadIdx.x; i < 128 * 16; i += blockDim.x) {
-        const int n = i >> 4, c = i & 15;
-        const int j = MODE == MODE_SYM ? (n & ~31) + 16 * (n & 1) + ((n & 31) >> 1) : n;
-        uint32_t h[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const int k0 = 8 * c + 2 * e;
-            const uint32_t lo = ((__popc(j & k0) & 1) ? 0xBC00u : 0x3C00u) ^ (p.has_sgn ? (((p.sgn[k0 >> 5] >> (k0 & 31)) & 1u) << 15) : 0u);
-            const uint32_t hi = ((__popc(j & (k0 + 1)) & 1) ? 0xBC00u : 0x3C00u) ^
-                                (p.has_sgn ? (((p.sgn[(k0 + 1) >> 5] >> ((k0 + 1) & 31)) & 1u) << 15) : 0u);
-            h[e] = lo | (hi << 16);
-        }
-        *reinterpret_cast<uint4 *>(bop + (c >> 3) * TE_HALF + swz128(n, c & 7)) = make_uint4(h[0], h[1], h[2], h[3]);
-    }
-    if constexpr (MODE == MODE_PAIR)
-        for (int i = threadIdx.x; i < PT_CELLS * P4_REP; i += blockDim.x) ptab[i] = p.pt.ent[i / P4_REP];
-    fence_proxy_async_smem();  // B is read by the MMAs (async proxy)
-    if (warp == 1) tmem_alloc(tslot, 512);
-    qt_fence_before();
-    __syncthreads();
-    qt_fence_after();
-    const uint32_t tmem = *tslot;
-
-    if (warp == 0) {
-        // ---- producer
-        if (lane == 0) {
-            const uint64_t pol = l2_policy_evict_first();
-            int i = 0;
-            for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++i) {
-                const int s = i % NST;
-                if (i >= NST && !mbar_wait_bounded(&x_empty[s], (uint32_t)((i / NST) - 1) & 1u)) {
-                    atomicOr(&g_rvq_err, (unsigned)VQ_DEVERR_WAIT_TIMEOUT);
-                    *abort_flag = 1u;
-                    break;
-                }
-                if (*abort_flag) break;
-                unsigned char *dst = ring + s * TE_TILE;
-                mbar_arrive_expect_tx(&x_full[s], (uint32_t)TE_TILE);
-                tma_load_2d(dst, &p.tmap, 0, t * TE_M, &x_full[s], pol);
-                tma_load_2d(dst + TE_HALF, &p.tmap, 64, t * TE_M, &x_full[s], pol);
-            }
-            for (int k = 0; k < NST && k < i; ++k) {
-                const int j = i - 1 - k;
-                (void)mbar_wait_bounded(&x_full[j % NST], (uint32_t)(j / NST) & 1u);
-            }
-        }
-        __syncwarp();
-    } else if (warp == 1) {
-        // ---- MMA issue: tile i into accumulator buffer i % TE_G
-        if (lane == 0) {
-            constexpr uint32_t IDESC = qt_idesc(128);
-            const uint32_t bb = smem_u32(bop), rb = smem_u32(ring);
-            int i = 0;
-            for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++i) {
-                const int s = i % NST, a = i % TE_G;
-                bool ok = mbar_wait_bounded(&x_full[s], (uint32_t)(i / NST) & 1u);
-                if (ok && i >= TE_G) ok = mbar_wait_bounded(&acc_empty[a], (uint32_t)((i / TE_G) - 1) & 1u);
-                if (!ok || *abort_flag) {
-                    if (!ok) atomicOr(&g_rvq_err, (unsigned)VQ_DEVERR_WAIT_TIMEOUT);
-                    *abort_flag = 1u;
-                    break;
-                }
-                qt_fence_after();
-                const uint32_t xa = rb + s * TE_TILE;
-#pragma unroll
-                for (int kb = 0; kb < 2; ++kb) {
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        qt_mma(tmem + (uint32_t)(a * 128), qt_desc(xa + kb * TE_HALF + kk * 32),
-                               qt_desc(bb + kb * TE_HALF + kk * 32), IDESC, (kb | kk) ? 1u : 0u);
-                }
-                qt_commit(&acc_full[a]);
-            }
-        }
-        __syncwarp();
-    } else {
-        // ---- epilogue group g: tiles i with i % TE_G == g; thread = row
-        const int g = (warp - 2) >> 2;
-        const int q = warp & 3;  // tensor-memory lane quadrant of this warp
-        const int r = 32 * q + lane;
-        const uint32_t tl = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(g * 128);
-        // exact-recompute tables (shuffle) and book constants
-        const float tb1 = p.t1.bnd[lane];
-        const int tc1 = p.t1.code[lane];
-        const float tb2 = p.t2.bnd[lane];
-        const int tc2 = p.t2.code[lane];
-        const float tcen = p.c1[lane & ((1 << BITS) - 1)];
-        [[maybe_unused]] const float b1u = p.b1[2], b2u = p.b2[2];
-        [[maybe_unused]] const float bc2u = p.b1[2] - p.c1[2], dcu = p.c1[3] - p.c1[2];
-        [[maybe_unused]] const float kb1 = __fdiv_rn(2.0f, b1u), kb2 = __fdiv_rn(2.0f, b2u);
-        [[maybe_unused]] const float pa = p.pt.a, pbc = p.pt.bc;
-        [[maybe_unused]] const uint32_t tab =
-            smem_u32(ptab) + 8u * (uint32_t)(lane & (P4_REP - 1)) - (0x4B400000u << 7);
-        const bool dense = p.dst_off == nullptr && p.S_dst == p.S && p.S_q == p.S;
-        int i = 0;
-        for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++i) {
-            if (i % TE_G != g) continue;
-            const int s = i % NST;
-            const bool ok = mbar_wait_bounded(&acc_full[g], (uint32_t)(i / TE_G) & 1u);
-            if (!__all_sync(FULL_MASK, ok) || *abort_flag) {
-                if (!ok && lane == 0) atomicOr(&g_rvq_err, (unsigned)VQ_DEVERR_WAIT_TIMEOUT);
-                *abort_flag = 1u;
-                break;
-            }
-            qt_fence_after();
-            const int row = t * TE_M + r;
-            const bool valid = row < p.N;
-
-            // the norm from the row's fp16 values in the staged tile: exact
-            // squares (fp16 operands, fp32 result), fp32 sums in 16 partial
-            // sums of 8 (12 roundings deep at most)
-            const unsigned char *xt = ring + s * TE_TILE;
-            float ps[16];
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-#pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    const uint4 v = *reinterpret_cast<const uint4 *>(xt + h * TE_HALF + swz128(r, c));
-                    ps[8 * h + c] = sq8_f16(v);
-                }
-            }
-#pragma unroll
-            for (int k = 0; k < 8; ++k) ps[k] += ps[k + 8];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) ps[k] += ps[k + 4];
-            ps[0] += ps[2];
-            ps[1] += ps[3];
-            const float qn = ps[0] + ps[1];
-            const float n = __fsqrt_rn(qn);
-            const float den = n * SQRT_D_HI;
-            // the staged tile has been read (the MMAs are done with it too):
-            // free the stage now, so that the producer keeps the ring full
-            // through the quantization (a flagged row is re-read from global
-            // memory by the exact recompute)
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&x_empty[s]);
-
-            // pass 2: quantize the row in natural coordinate order, 32
-            // coordinates (one tensor-memory load) at a time, the next load in
-            // flight during each chunk; the words go straight to the row's
-            // destination (a flagged row is rewritten by the exact recompute)
-            size_t drow = (size_t)row;
-            const bool okrow = valid && (dense || rvq_dst_row(p, row, drow));
-            uint32_t *d1 = p.p1 + drow * W, *d2 = p.p2 + drow * W;
-            uint32_t va[32], vb[32];
-            bool flag;
-            if constexpr (MODE == MODE_SYM) {
-                const SymRow sk = sym2_row(den, p.guard * den, b1u, b2u, bc2u, dcu, kb1, kb2);
-                float m1 = __int_as_float(0x7f800000), m2 = m1;
-                // words 2c (coordinates 32c .. 32c + 15) and 2c + 1, code j at bits 2j
-                auto chunk = [&](const uint32_t (&v)[32], int c) {
-                    uint32_t a1x = 0u, a2x = 0u, a1y = 0u, a2y = 0u;
-#pragma unroll
-                    for (int b = 15; b >= 0; --b)
-                        sym2_code2(make_float2(__uint_as_float(v[2 * b]), __uint_as_float(v[2 * b + 1])), sk, a1x, a2x,
-                                   a1y, a2y, m1, m2);
-                    uint32_t x1, x2, y1, y2;
-                    sym2_words(a1x, a2x, x1, x2);
-                    sym2_words(a1y, a2y, y1, y2);
-                    if (okrow) {
-                        *reinterpret_cast<uint2 *>(d1 + 2 * c) = make_uint2(x1, y1);
-                        *reinterpret_cast<uint2 *>(d2 + 2 * c) = make_uint2(x2, y2);
-                    }
-                };
-                qt_ld32(tl, va);
-#pragma unroll 1
-                for (int c = 0; c < 4; c += 2) {
-                    qt_wait_ld();
-                    qt_hold(va);
-                    qt_ld32(tl + 32 * (c + 1), vb);
-                    chunk(va, c);
-                    qt_wait_ld();
-                    qt_hold(vb);
-                    if (c + 2 < 4) qt_ld32(tl + 32 * (c + 2), va);
-                    chunk(vb, c + 1);
-                }
-                flag = !(m1 >= sk.G1) || !(m2 >= sk.G2) || !(qn > 0.0f);
-            } else {
-                const float sa = pa * __frcp_rn(den);
-                float m = __int_as_float(0x7f800000);
-                // words 4c .. 4c + 3, eight coordinates each: pairs of even
-                // coordinates collect in b0, of odd ones in b1
-                auto chunk = [&](const uint32_t (&v)[32], int c) {
-                    uint32_t o1[4], o2[4];
-#pragma unroll
-                    for (int w = 0; w < 4; ++w) {
-                        uint32_t b0 = 0u, b1 = 0u;
-#pragma unroll
-                        for (int e = 0; e < 8; e += 2) {
-                            b0 = __funnelshift_r(b0, pair_code_s(__uint_as_float(v[8 * w + e]), sa, pbc, den, tab, m), 8);
-                            b1 = __funnelshift_r(b1, pair_code_s(__uint_as_float(v[8 * w + e + 1]), sa, pbc, den, tab, m), 8);
-                        }
-                        o1[w] = (b0 & 0x0F0F0F0Fu) | ((b1 & 0x0F0F0F0Fu) << 4);
-                        o2[w] = ((b0 >> 4) & 0x0F0F0F0Fu) | (b1 & 0xF0F0F0F0u);
-                    }
-                    if (okrow) {
-                        *reinterpret_cast<uint4 *>(d1 + 4 * c) = make_uint4(o1[0], o1[1], o1[2], o1[3]);
-                        *reinterpret_cast<uint4 *>(d2 + 4 * c) = make_uint4(o2[0], o2[1], o2[2], o2[3]);
-                    }
-                };
-                qt_ld32(tl, va);
-#pragma unroll 1
-                for (int c = 0; c < 4; c += 2) {
-                    qt_wait_ld();
-                    qt_hold(va);
-                    qt_ld32(tl + 32 * (c + 1), vb);
-                    chunk(va, c);
-                    qt_wait_ld();
-                    qt_hold(vb);
-                    if (c + 2 < 4) qt_ld32(tl + 32 * (c + 2), va);
-                    chunk(vb, c + 1);
-                }
-                flag = !(m >= p.guard * den) || !(qn > 0.0f);
-            }
-            // the accumulator buffer is free for tile i + TE_G
-            qt_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&acc_empty[g]);
-
-            flag = flag && valid;
-            if (okrow && !flag) p.norms[drow] = n;
-            __syncwarp();  // the fast words of a flagged row are written before its exact ones
-            // rows inside the guard band: exact recompute by the warp, the row
-            // read again from global memory
-            unsigned fl = __ballot_sync(FULL_MASK, flag);
-            while (fl) {
-                const int bit = __ffs(fl) - 1;
-                fl &= fl - 1;
-                rvq_fixup_row<BITS, MODE == MODE_PAIR, 0>(p, nullptr, 32 * q + bit, t * TE_M + 32 * q + bit, lane, tb1, tc1,
-                                                          tb2, tc2, tcen);
-            }
-            __syncwarp();
-        }
-    }
-
-    qt_fence_before();
-    __syncthreads();
-    qt_fence_after();
-    if (warp == 1) tmem_free(tmem, 512);
+    rvq_encode_tm_body<MODE>(p, blockIdx.x, gridDim.x);
 }
 
 // ---------------------------------------------------------------- decode
@@ -608,7 +287,7 @@ template <int BITS, int MODE>
 cudaError_t launch_enc(const RvqEncodeParams &p0, cudaStream_t stream)
 {
     RvqEncodeParams p = p0;
-    if (!prepare_rvq_encode(p)) return cudaErrorInvalidValue;
+    if (!prepare_rvq_encode(p, ER)) return cudaErrorInvalidValue;
     auto kern = p.has_sgn ? rvq_encode_kernel<BITS, MODE, true> : rvq_encode_kernel<BITS, MODE, false>;
     constexpr int smem = enc_smem(BITS, MODE);
     constexpr int warps = enc_warps(BITS, MODE);
@@ -628,14 +307,7 @@ template <int MODE>
 cudaError_t launch_enc_tm(const RvqEncodeParams &p0, cudaStream_t stream)
 {
     RvqEncodeParams p = p0;
-    p.divS = make_fastdiv((uint32_t)p.S);
-    p.divH = make_fastdiv((uint32_t)p.H);
-    {
-        const uint64_t dims[2] = {(uint64_t)D, (uint64_t)p.N};
-        const uint64_t strides[1] = {(uint64_t)D * 2};
-        const uint32_t box[2] = {64u, (uint32_t)TE_M};
-        if (!encode_tmap_f16(&p.tmap, p.x, 2, dims, strides, box, true, true)) return cudaErrorInvalidValue;
-    }
+    if (!prepare_rvq_encode(p, TE_M)) return cudaErrorInvalidValue;
     auto kern = rvq_encode_tc_kernel<MODE>;
     constexpr int smem = te_smem(MODE);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -682,13 +354,13 @@ cudaError_t launch_dec(const RvqDecodeParams &p0, cudaStream_t stream)
 
 }  // namespace
 
-bool prepare_rvq_encode(RvqEncodeParams &p)
+bool prepare_rvq_encode(RvqEncodeParams &p, int box_rows)
 {
     p.divS = make_fastdiv((uint32_t)p.S);
     p.divH = make_fastdiv((uint32_t)p.H);
     const uint64_t dims[2] = {(uint64_t)D, (uint64_t)p.N};
     const uint64_t strides[1] = {(uint64_t)D * 2};
-    const uint32_t box[2] = {64u, (uint32_t)ER};
+    const uint32_t box[2] = {64u, (uint32_t)box_rows};
     return encode_tmap_f16(&p.tmap, p.x, 2, dims, strides, box, true, true);
 }
 

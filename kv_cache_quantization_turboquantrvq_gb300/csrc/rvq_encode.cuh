@@ -47,6 +47,7 @@
 
 #include "device_common.cuh"
 #include "launch.h"
+#include "tcgen05.cuh"
 
 #ifndef VQ_RVQ_ERR
 #error "define VQ_RVQ_ERR (the device error word) before including rvq_encode.cuh"
@@ -750,44 +751,22 @@ __device__ __forceinline__ void rvq_encode_body(const RvqEncodeParams &p, int ct
     }
 }
 
-// ------------------------------------------- encode, symmetric b = 2, tensor cores
+// ------------------------------------------- the library's books: shared pieces
 //
-// The same pass as rvq_encode_kernel for symmetric 4-level books, with the
-// rotation on the tensor cores.  Write a coordinate as c = 8a + b (a < 16,
-// b < 8); the Sylvester matrix factors as H128[8a' + b'][8a + b] =
-// H16[a'][a] H8[b'][b].  Per warp and 16-row block, for each b the product
-// T_b = X_b H16 (X_b: the 16 rows' values x[8a + b], a as the k index) is one
-// pair of 16x8x16 mma.sync (fp16 operands, exact +-1 products, fp32
-// accumulation); then the H8 factor is three fp32x2 butterfly stages across
-// the eight accumulator tiles, in registers.  The columns of the H16 operand
-// are permuted so that the lane with t4 = lane & 3 receives a' = 4 t4 ..
-// 4 t4 + 3, i.e. output coordinates 32 t4 .. 32 t4 + 31: two whole code words
-// of each of its two rows (g8 = lane >> 2 and g8 + 8), so no word is split
-// across lanes.  The A operands come from 16-byte reads of the swizzled
-// staged rows (chunk a of row r holds x[8a .. 8a + 7]) and one byte permute
-// per register.  The norm is taken from the H16 outputs (their squares sum to
-// 16 sum x^2), the quantizer is sym2_code2, rows with a value in the guard
-// band go to rvq_fixup_row.
-constexpr int S2_WARPS = 16;
-constexpr int S2_STAGES = 3;
-
-__device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                              uint32_t b0, uint32_t b1)
-{
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-// fp16 pair (+-1 of H16[a][a'], H16[a + 1][a']) for the B operand
-__device__ __forceinline__ uint32_t h16_pair(int a, int ap)
-{
-    const uint32_t lo = (__popc(a & ap) & 1) ? 0xBC00u : 0x3C00u;
-    const uint32_t hi = (__popc((a + 1) & ap) & 1) ? 0xBC00u : 0x3C00u;
-    return lo | (hi << 16);
-}
+// The pair table of the b = 4 books lives in shared memory replicated
+// P4_REP = 16 times (cell g, replica j at byte (16 g + j) 8) and lane l reads
+// replica l & 15: an 8-byte read is served per half-warp, so the 16 lanes of
+// each half always hit 16 distinct bank pairs and the lookup is free of bank
+// conflicts.  The quantizers work on S = H x directly: with den = n sqrt(D),
+// y > bnd exactly when bnd den - S is negative (one FMA rounding of an exact
+// product-difference), the cell coordinate is fma(S, a / den, bc) and the
+// margin |bnd den - S| is compared with guard den; the host builds the table
+// with every step at least three guard bands inside its cell, which absorbs
+// the rounding of a / den (the cell a value lands in can differ from the
+// y-domain map only near cell edges, where the neighbouring cell's entry
+// gives the same pair).
+constexpr int P4_REP = 16;
+constexpr int P4_TAB_BYTES = PT_CELLS * P4_REP * 8;
 
 // Per-row constants of the symmetric b = 2 quantizer (units of S = H x).
 __device__ __forceinline__ SymRow sym2_row(float den, float g, float b1u, float b2u, float bc2u, float dcu,
@@ -810,280 +789,6 @@ __device__ __forceinline__ SymRow sym2_row(float den, float g, float b1u, float 
     return k;
 }
 
-// S = X H128 for rows g8 and g8 + 8 of a staged 16-row block: the A operands
-// from 16-byte reads of the swizzled rows (chunk a of a row holds
-// x[8a .. 8a + 7]) and one byte permute per register, X_b H16 for b = 0..7 as
-// 16x8x16 mma.sync with the permuted H16 columns in hb, the rows' sums of
-// squares (q0, q1) from the H16 outputs, then H8 as three butterfly stages
-// across b.  Afterwards acc[b'][nt][2r + e] = S at coordinate
-// 32 t4 + 16 nt + 8 e + b' of row g8 + 8r.
-template <bool SGN>
-__device__ __forceinline__ void tc_rotate_block(const unsigned char *sbuf, const uint4 *ssg, const uint32_t (&hb)[2][2],
-                                                int g8, int t4, float (&acc)[8][2][4], float &q0, float &q1)
-{
-    // ---- T_b = X_b H16 for b = 0..7 on the tensor cores
-    {
-        // u[r][j]: row g8 + 8r, chunk a = 2 t4 + {0, 1, 8, 9}[j]
-        uint4 u[2][4];
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int a = 2 * t4 + (j & 1) + 8 * (j >> 1);
-                u[r][j] = *reinterpret_cast<const uint4 *>(sbuf + (j >> 1) * (ENC_BLOCK / 2) + swz128(g8 + 8 * r, a & 7));
-                if constexpr (SGN) {
-                    const uint4 m = ssg[a];
-                    u[r][j] = make_uint4(u[r][j].x ^ m.x, u[r][j].y ^ m.y, u[r][j].z ^ m.z, u[r][j].w ^ m.w);
-                }
-            }
-        }
-#pragma unroll
-        for (int b = 0; b < 8; ++b) {
-            const uint32_t sel = (b & 1) ? 0x7632u : 0x5410u;
-            auto word = [&](const uint4 &v) -> uint32_t {
-                return (b >> 1) == 0 ? v.x : (b >> 1) == 1 ? v.y : (b >> 1) == 2 ? v.z : v.w;
-            };
-            const uint32_t a0 = __byte_perm(word(u[0][0]), word(u[0][1]), sel);
-            const uint32_t a1 = __byte_perm(word(u[1][0]), word(u[1][1]), sel);
-            const uint32_t a2 = __byte_perm(word(u[0][2]), word(u[0][3]), sel);
-            const uint32_t a3 = __byte_perm(word(u[1][2]), word(u[1][3]), sel);
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                acc[b][nt][0] = acc[b][nt][1] = acc[b][nt][2] = acc[b][nt][3] = 0.0f;
-                mma_f16_16816(acc[b][nt], a0, a1, a2, a3, hb[nt][0], hb[nt][1]);
-            }
-        }
-    }
-
-    // ---- norms: the H16 outputs' squares sum to 16 sum x^2 (per row)
-    {
-        float2 s0 = make_float2(0.0f, 0.0f), s1 = s0;
-#pragma unroll
-        for (int b = 0; b < 8; ++b) {
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                const float2 v0 = make_float2(acc[b][nt][0], acc[b][nt][1]);
-                const float2 v1 = make_float2(acc[b][nt][2], acc[b][nt][3]);
-                s0 = __ffma2_rn(v0, v0, s0);
-                s1 = __ffma2_rn(v1, v1, s1);
-            }
-        }
-        q0 = s0.x + s0.y;
-        q1 = s1.x + s1.y;
-        q0 += __shfl_xor_sync(FULL_MASK, q0, 1);
-        q1 += __shfl_xor_sync(FULL_MASK, q1, 1);
-        q0 += __shfl_xor_sync(FULL_MASK, q0, 2);
-        q1 += __shfl_xor_sync(FULL_MASK, q1, 2);
-        q0 *= 0.0625f;
-        q1 *= 0.0625f;
-    }
-    // ---- H8 across b: acc[b'][nt] = S at coordinates 32 t4 + 16 nt + b' (.x / c2)
-    // and 32 t4 + 16 nt + 8 + b' (.y / c3)
-    const float2 neg1 = make_float2(-1.0f, -1.0f);
-#pragma unroll
-    for (int h = 1; h < 8; h <<= 1) {
-#pragma unroll
-        for (int b = 0; b < 8; ++b) {
-            if ((b & h) == 0) {
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {
-#pragma unroll
-                    for (int r = 0; r < 2; ++r) {
-                        const float2 x = make_float2(acc[b][nt][2 * r], acc[b][nt][2 * r + 1]);
-                        const float2 y = make_float2(acc[b + h][nt][2 * r], acc[b + h][nt][2 * r + 1]);
-                        const float2 sum = __fadd2_rn(x, y);
-                        const float2 dif = __ffma2_rn(y, neg1, x);
-                        acc[b][nt][2 * r] = sum.x;
-                        acc[b][nt][2 * r + 1] = sum.y;
-                        acc[b + h][nt][2 * r] = dif.x;
-                        acc[b + h][nt][2 * r + 1] = dif.y;
-                    }
-                }
-            }
-        }
-    }
-}
-
-template <bool SGN>
-__device__ __forceinline__ void rvq_encode_sym2_body(const RvqEncodeParams &p, int cta, int ncta)
-{
-    constexpr int W = D * 2 / 32;  // 8 words per row and stream
-    extern __shared__ __align__(128) unsigned char smem_raw[];
-    unsigned char *base = smem_1k(smem_raw);
-    uint4 *ssg = reinterpret_cast<uint4 *>(base);  // sign masks: chunk a = coordinates 8a .. 8a + 7
-    unsigned char *smem = base + ENC_SGN_BYTES;
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
-    const int g8 = lane >> 2, t4 = lane & 3;
-    unsigned char *ring = smem + warp * (S2_STAGES * ENC_BLOCK);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S2_WARPS * S2_STAGES * ENC_BLOCK) + warp * S2_STAGES;
-
-    if (lane == 0) {
-#pragma unroll
-        for (int s = 0; s < S2_STAGES; ++s) mbar_init(&bars[s], 1);
-        fence_mbar_init();
-    }
-    if (threadIdx.x < 16) {
-        const int c0 = 8 * threadIdx.x;
-        ssg[threadIdx.x] = make_uint4(half2_sign_mask(sign_pair(p.sgn, c0)), half2_sign_mask(sign_pair(p.sgn, c0 + 2)),
-                                      half2_sign_mask(sign_pair(p.sgn, c0 + 4)), half2_sign_mask(sign_pair(p.sgn, c0 + 6)));
-    }
-    __syncthreads();
-
-    const uint64_t pol = l2_policy_evict_first();
-    // shuffle tables of the exact recompute
-    const float tb1 = p.t1.bnd[lane];
-    const int tc1 = p.t1.code[lane];
-    const float tb2 = p.t2.bnd[lane];
-    const int tc2 = p.t2.code[lane];
-    const float tcen = p.c1[lane & 3];
-    // unit-norm book constants: B, E, B - c2, c3 - c2, 2 / B, 2 / E
-    const float b1u = p.b1[2], b2u = p.b2[2];
-    const float bc2u = p.b1[2] - p.c1[2], dcu = p.c1[3] - p.c1[2];
-    const float kb1 = __fdiv_rn(2.0f, b1u), kb2 = __fdiv_rn(2.0f, b2u);
-    // B operand: column n = g8 of n-tile nt is a' = 4 (g8 >> 1) + 2 nt + (g8 & 1);
-    // b0 holds k = 2 t4, 2 t4 + 1 and b1 k = 2 t4 + 8, 2 t4 + 9
-    uint32_t hb[2][2];
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-        const int ap = 4 * (g8 >> 1) + 2 * nt + (g8 & 1);
-        hb[nt][0] = h16_pair(2 * t4, ap);
-        hb[nt][1] = h16_pair(2 * t4 + 8, ap);
-    }
-
-    const int nblk = (p.N + ER - 1) / ER;
-    const int gw = cta * S2_WARPS + warp;
-    const int tw = ncta * S2_WARPS;
-    // destination row = source row (no batch offsets, same capacity)
-    const bool dense = p.dst_off == nullptr && p.S_dst == p.S && p.S_q == p.S;
-    auto issue = [&](int blk, int s) {
-        if (lane == 0) {
-            mbar_arrive_expect_tx(&bars[s], (uint32_t)ENC_BLOCK);
-            tma_load_2d(ring + s * ENC_BLOCK, &p.tmap, 0, blk * ER, &bars[s], pol);
-            tma_load_2d(ring + s * ENC_BLOCK + ENC_BLOCK / 2, &p.tmap, 64, blk * ER, &bars[s], pol);
-        }
-    };
-#pragma unroll
-    for (int s = 0; s < S2_STAGES; ++s) {
-        const int blk = gw + s * tw;
-        if (blk < nblk) issue(blk, s);
-    }
-
-    int s = 0;
-    uint32_t ph = 0;
-    for (int it = 0;; ++it) {
-        const int blk = gw + it * tw;
-        if (blk >= nblk) break;
-        const bool ok = mbar_wait_bounded(&bars[s], ph);
-        if (!__all_sync(FULL_MASK, ok)) {
-            if (lane == 0) atomicOr(&VQ_RVQ_ERR, (unsigned)VQ_DEVERR_WAIT_TIMEOUT);
-            for (int k = 1; k < S2_STAGES; ++k) {
-                const int it2 = it + k;
-                if (gw + it2 * tw < nblk)
-                    (void)mbar_wait_bounded(&bars[it2 % S2_STAGES], (uint32_t)(it2 / S2_STAGES) & 1u);
-            }
-            return;
-        }
-        const unsigned char *sbuf = ring + s * ENC_BLOCK;
-
-        float acc[8][2][4];
-        float q0, q1;
-        tc_rotate_block<SGN>(sbuf, ssg, hb, g8, t4, acc, q0, q1);
-        const float n0 = __fsqrt_rn(q0), n1 = __fsqrt_rn(q1);
-        const float den0 = n0 * SQRT_D_HI, den1 = n1 * SQRT_D_HI;
-
-        // ---- quantize: word 2 t4 + nt of row g8 + 8r gets b' = 0..7 of .x at
-        // positions 0..7 and of .y at positions 8..15
-        const SymRow sk0 = sym2_row(den0, p.guard * den0, b1u, b2u, bc2u, dcu, kb1, kb2);
-        const SymRow sk1 = sym2_row(den1, p.guard * den1, b1u, b2u, bc2u, dcu, kb1, kb2);
-        // running minima of the stage-1 / stage-2 margin products of each row
-        float m0a = __int_as_float(0x7f800000), m0b = m0a, m1a = m0a, m1b = m0a;
-        uint32_t w1[2][2], w2[2][2];
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                uint32_t a1x = 0u, a2x = 0u, a1y = 0u, a2y = 0u;
-#pragma unroll
-                for (int b = 7; b >= 0; --b) {
-                    const float2 y2 = make_float2(acc[b][nt][2 * r], acc[b][nt][2 * r + 1]);
-                    if (r == 0) sym2_code2(y2, sk0, a1x, a2x, a1y, a2y, m0a, m0b);
-                    else sym2_code2(y2, sk1, a1x, a2x, a1y, a2y, m1a, m1b);
-                }
-                sym2_words(__byte_perm(a1x, a1y, 0x5410u), __byte_perm(a2x, a2y, 0x5410u), w1[r][nt], w2[r][nt]);
-            }
-        }
-
-        // ---- guard band: a row is flagged if any of its four lanes saw a value
-        // inside the band (and always when it is zero)
-        const int row0 = blk * ER + g8, row1 = row0 + 8;
-        const bool valid0 = row0 < p.N, valid1 = row1 < p.N;
-        const bool f0 = valid0 && (!(m0a >= sk0.G1) || !(m0b >= sk0.G2) || !(q0 > 0.0f));
-        const bool f1 = valid1 && (!(m1a >= sk1.G1) || !(m1b >= sk1.G2) || !(q1 > 0.0f));
-        int f = (f0 ? 1 : 0) | (f1 ? 2 : 0);
-        f |= __shfl_xor_sync(FULL_MASK, f, 1);
-        f |= __shfl_xor_sync(FULL_MASK, f, 2);
-
-        // ---- fast words: 8 bytes per lane, row and stream (a block's 16 rows are
-        // contiguous in both streams)
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-            const int row = r ? row1 : row0;
-            size_t drow = (size_t)row;
-            if ((r ? valid1 : valid0) && !(f & (1 << r)) && (dense || rvq_dst_row(p, row, drow))) {
-                *reinterpret_cast<uint2 *>(p.p1 + drow * W + 2 * t4) = make_uint2(w1[r][0], w1[r][1]);
-                *reinterpret_cast<uint2 *>(p.p2 + drow * W + 2 * t4) = make_uint2(w2[r][0], w2[r][1]);
-                if (t4 == 0) p.norms[drow] = r ? n1 : n0;
-            }
-        }
-
-        // ---- flagged rows: exact recompute by the warp
-        unsigned fl = (__ballot_sync(FULL_MASK, (f & 1) != 0) & 0x11111111u) |
-                      ((__ballot_sync(FULL_MASK, (f & 2) != 0) & 0x11111111u) << 1);
-        while (fl) {
-            const int bit = __ffs(fl) - 1;
-            fl &= fl - 1;
-            const int r = (bit >> 2) + 8 * (bit & 1);
-            rvq_fixup_row<2, false>(p, sbuf, r, blk * ER + r, lane, tb1, tc1, tb2, tc2, tcen);
-        }
-        __syncwarp();
-
-        fence_proxy_async_smem();
-        {
-            const int nb = blk + S2_STAGES * tw;
-            if (nb < nblk) issue(nb, s);
-        }
-        if (++s == S2_STAGES) {
-            s = 0;
-            ph ^= 1u;
-        }
-    }
-}
-
-// ------------------------------------------- encode, b = 4 pair table, tensor cores
-//
-// The rotation of rvq_encode_sym2_kernel (tc_rotate_block) with the
-// 16-level quantizer of the pair table (PairTable in launch.h): one cell
-// lookup per coordinate gives both codes.  The table lives in shared memory
-// replicated P4_REP = 16 times (cell g, replica j at byte (16 g + j) 8) and
-// lane l reads replica l & 15: an 8-byte read is served per half-warp, so the
-// 16 lanes of each half always hit 16 distinct bank pairs and the lookup is
-// free of bank conflicts.  The quantizer works on S = H x directly: with
-// den = n sqrt(D), y > bnd exactly when bnd den - S is negative (one FMA
-// rounding of an exact product-difference), the cell coordinate is
-// fma(S, a / den, bc), and the margin |bnd den - S| is compared with
-// guard den; the host builds the table with every step at least three guard
-// bands inside its cell, which absorbs the rounding of a / den (the cell a
-// value lands in can differ from the y-domain map only near cell edges,
-// where the neighbouring cell's entry gives the same pair).  After the
-// rotation acc[b'][nt][2r + e], b' = 0..7, are the eight coordinates of word
-// 4 t4 + 2 nt + e of row g8 + 8r, so each lane packs and stores four whole
-// words per row and stream.  Rows with a value inside the guard band go to
-// rvq_fixup_row.
-constexpr int P4_STAGES = 2;
-constexpr int P4_REP = 16;
-constexpr int P4_TAB_BYTES = PT_CELLS * P4_REP * 8;
-
 // Both 4-bit codes of the coordinate S (pair i1 | i2 << 4 in the low byte).
 // tab: this lane's replica as a 32-bit shared address, less the magic
 // constant's bits shifted by 7, so that the cell's entry is at tab + (gb << 7)
@@ -1101,174 +806,332 @@ __device__ __forceinline__ uint32_t pair_code_s(float s, float a, float bc, floa
     return __byte_perm(ey, 0u, __float_as_uint(d) >> 31);
 }
 
-template <bool SGN>
-__device__ __forceinline__ void rvq_encode_pair4_body(const RvqEncodeParams &p, int cta, int ncta)
+// ------------------------------------------- encode on the 5th-generation tensor cores
+//
+// The library's books (symmetric b = 2, and b = 4 with a pair table), 128 rows
+// per tile: the whole rotation S = X H128 is one D = X B^T of M = N = K = 128
+// (eight tcgen05.mma of K = 16, fp16 operands - the products x_d (+-1) are
+// exact - fp32 accumulation) into tensor memory; B = H128 diag(s) (the
+// randomised signs, when given, ride in B for free) is built once per CTA in
+// the K-major 128-byte-swizzled layout the X tiles arrive in by TMA.  Then a
+// thread owns a row: it takes the norm from its fp16 row in the staged tile
+// (exact squares by mixed-precision FMAs), reads its 128 accumulators
+// (tcgen05.ld, tensor-memory lane = row), quantizes its coordinates in
+// natural order and stores whole words; no butterflies,
+// no operand permutes, no cross-lane packing.  Roles (one persistent CTA per
+// SM): warp 0 streams X tiles (TMA, TE_STAGES-deep ring), warp 1 owns the
+// tensor memory and issues the MMAs (one thread), TE_G groups of four warps
+// run the epilogue on alternate tiles, each group with its own accumulator
+// buffer (128 columns).  Rows with a value inside the guard band go to the
+// warp's exact recompute (rvq_fixup_row) while the stage is still held.
+// Every wait is bounded; on a timeout the CTA records VQ_DEVERR_WAIT_TIMEOUT,
+// waits (bounded) for its copies in flight, frees its tensor memory and
+// returns.
+// Sum of the squares of the 8 fp16 values of a 16-byte chunk: each square
+// exact (fp16 operands, fp32 result of a mixed-precision FMA), 8 fp32 sums.
+__device__ __forceinline__ float sq8_f16(uint4 v)
 {
-    constexpr int W = D * 4 / 32;  // 16 words per row and stream
+    float a = 0.0f;
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const unsigned short lo = (unsigned short)(w[j] & 0xffffu), hi = (unsigned short)(w[j] >> 16);
+        asm("fma.rn.f32.f16 %0, %1, %1, %0;" : "+f"(a) : "h"(lo));
+        asm("fma.rn.f32.f16 %0, %1, %1, %0;" : "+f"(a) : "h"(hi));
+    }
+    return a;
+}
+
+constexpr int TE_M = 128;
+constexpr int TE_G = 3;                       // epilogue groups (4 warps each)
+constexpr int TE_THREADS = 32 * (2 + 4 * TE_G);
+constexpr int TE_HALF = TE_M * 128;           // a 64-coordinate half of a tile (16 KB)
+constexpr int TE_TILE = 2 * TE_HALF;          // 32 KB
+constexpr int TE_BOP = 2 * 128 * 128;         // B = H128 diag(s), fp16, 32 KB
+__host__ __device__ constexpr int te_stages(int mode) { return mode == MODE_PAIR ? 3 : 4; }
+__host__ __device__ constexpr int te_smem(int mode)
+{
+    return 1024 + TE_BOP + (mode == MODE_PAIR ? P4_TAB_BYTES : 0) + te_stages(mode) * TE_TILE + 256;
+}
+static_assert(te_smem(MODE_PAIR) <= SMEM_MAX && te_smem(MODE_SYM) <= SMEM_MAX, "tensor-memory encoder shared memory");
+
+template <int MODE>
+__device__ __forceinline__ void rvq_encode_tm_body(const RvqEncodeParams &p, int cta, int ncta)
+{
+    constexpr int BITS = MODE == MODE_PAIR ? 4 : 2;
+    constexpr int W = D * BITS / 32;  // words per row and stream
+    constexpr int NST = te_stages(MODE);
     extern __shared__ __align__(128) unsigned char smem_raw[];
     unsigned char *base = smem_1k(smem_raw);
-    uint4 *ssg = reinterpret_cast<uint4 *>(base);  // sign masks: chunk a = coordinates 8a .. 8a + 7
-    uint2 *ptab = reinterpret_cast<uint2 *>(base + ENC_SGN_BYTES);
-    unsigned char *smem = base + ENC_SGN_BYTES + P4_TAB_BYTES;  // 1024-byte aligned
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
-    const int g8 = lane >> 2, t4 = lane & 3;
-    unsigned char *ring = smem + warp * (P4_STAGES * ENC_BLOCK);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S2_WARPS * P4_STAGES * ENC_BLOCK) + warp * P4_STAGES;
+    unsigned char *bop = base;                                    // B: half h at h * 16 KB
+    uint2 *ptab = reinterpret_cast<uint2 *>(base + TE_BOP);       // MODE_PAIR only
+    unsigned char *ring = base + TE_BOP + (MODE == MODE_PAIR ? P4_TAB_BYTES : 0);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(ring + NST * TE_TILE);
+    uint64_t *x_full = bars, *x_empty = bars + NST;
+    uint64_t *acc_full = bars + 2 * NST, *acc_empty = acc_full + TE_G;
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(acc_empty + TE_G);
+    volatile uint32_t *abort_flag = tslot + 1;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int ntiles = (p.N + TE_M - 1) / TE_M;
 
-    const uint64_t pol = l2_policy_evict_first();
-    const int nblk = (p.N + ER - 1) / ER;
-    const int gw = cta * S2_WARPS + warp;
-    const int tw = ncta * S2_WARPS;
-    auto issue = [&](int blk, int s) {
-        if (lane == 0) {
-            mbar_arrive_expect_tx(&bars[s], (uint32_t)ENC_BLOCK);
-            tma_load_2d(ring + s * ENC_BLOCK, &p.tmap, 0, blk * ER, &bars[s], pol);
-            tma_load_2d(ring + s * ENC_BLOCK + ENC_BLOCK / 2, &p.tmap, 64, blk * ER, &bars[s], pol);
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NST; ++s) {
+            mbar_init(&x_full[s], 1);
+            mbar_init(&x_empty[s], 4);
         }
-    };
-    // the warp's barriers, then its first blocks in flight while the CTA
-    // fills the sign masks and the replicated table
-    if (lane == 0) {
-#pragma unroll
-        for (int s = 0; s < P4_STAGES; ++s) mbar_init(&bars[s], 1);
+        for (int g = 0; g < TE_G; ++g) {
+            mbar_init(&acc_full[g], 1);
+            mbar_init(&acc_empty[g], 4);
+        }
+        *abort_flag = 0u;
         fence_mbar_init();
+    }
+    // B[n][k] = H128[j(n)][k] s_k, fp16, K-major with the 128-byte swizzle:
+    // 16-byte chunk c (k = 8c .. 8c + 7) of row n.  Row n of B is column n of
+    // the accumulator; for the symmetric books the output coordinates are
+    // interleaved so that a thread's registers 2b and 2b + 1 of a 32-column
+    // load are coordinates 32q + b and 32q + 16 + b (the two words the
+    // quantizer fills side by side, as one fp32 pair): j(32q + 2b + e) =
+    // 32q + 16e + b.  The b = 4 quantizer works per coordinate: j(n) = n.
+    for (int i = threadIdx.x; i < 128 * 16; i += blockDim.x) {
+        const int n = i >> 4, c = i & 15;
+        const int j = MODE == MODE_SYM ? (n & ~31) + 16 * (n & 1) + ((n & 31) >> 1) : n;
+        uint32_t h[4];
 #pragma unroll
-        for (int s = 0; s < P4_STAGES; ++s) {
-            const int blk = gw + s * tw;
-            if (blk < nblk) issue(blk, s);
+        for (int e = 0; e < 4; ++e) {
+            const int k0 = 8 * c + 2 * e;
+            const uint32_t lo = ((__popc(j & k0) & 1) ? 0xBC00u : 0x3C00u) ^ (p.has_sgn ? (((p.sgn[k0 >> 5] >> (k0 & 31)) & 1u) << 15) : 0u);
+            const uint32_t hi = ((__popc(j & (k0 + 1)) & 1) ? 0xBC00u : 0x3C00u) ^
+                                (p.has_sgn ? (((p.sgn[(k0 + 1) >> 5] >> ((k0 + 1) & 31)) & 1u) << 15) : 0u);
+            h[e] = lo | (hi << 16);
         }
+        *reinterpret_cast<uint4 *>(bop + (c >> 3) * TE_HALF + swz128(n, c & 7)) = make_uint4(h[0], h[1], h[2], h[3]);
     }
-    if (threadIdx.x < 16) {
-        const int c0 = 8 * threadIdx.x;
-        ssg[threadIdx.x] = make_uint4(half2_sign_mask(sign_pair(p.sgn, c0)), half2_sign_mask(sign_pair(p.sgn, c0 + 2)),
-                                      half2_sign_mask(sign_pair(p.sgn, c0 + 4)), half2_sign_mask(sign_pair(p.sgn, c0 + 6)));
-    }
-    for (int i = threadIdx.x; i < PT_CELLS * P4_REP; i += blockDim.x) ptab[i] = p.pt.ent[i / P4_REP];
+    if constexpr (MODE == MODE_PAIR)
+        for (int i = threadIdx.x; i < PT_CELLS * P4_REP; i += blockDim.x) ptab[i] = p.pt.ent[i / P4_REP];
+    fence_proxy_async_smem();  // B is read by the MMAs (async proxy)
+    if (warp == 1) tmem_alloc(tslot, 512);
+    qt_fence_before();
     __syncthreads();
+    qt_fence_after();
+    const uint32_t tmem = *tslot;
 
-    // shuffle tables of the exact recompute
-    const float tb1 = p.t1.bnd[lane];
-    const int tc1 = p.t1.code[lane];
-    const float tb2 = p.t2.bnd[lane];
-    const int tc2 = p.t2.code[lane];
-    const float tcen = p.c1[lane & 15];
-    const float pa = p.pt.a, pbc = p.pt.bc;
-    const uint32_t tab = smem_u32(ptab) + 8u * (uint32_t)(lane & (P4_REP - 1)) - (0x4B400000u << 7);
-    uint32_t hb[2][2];
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-        const int ap = 4 * (g8 >> 1) + 2 * nt + (g8 & 1);
-        hb[nt][0] = h16_pair(2 * t4, ap);
-        hb[nt][1] = h16_pair(2 * t4 + 8, ap);
-    }
-
-    // destination row = source row (no batch offsets, same capacity)
-    const bool dense = p.dst_off == nullptr && p.S_dst == p.S && p.S_q == p.S;
-
-    int s = 0;
-    uint32_t ph = 0;
-    for (int it = 0;; ++it) {
-        const int blk = gw + it * tw;
-        if (blk >= nblk) break;
-        const bool ok = mbar_wait_bounded(&bars[s], ph);
-        if (!__all_sync(FULL_MASK, ok)) {
-            if (lane == 0) atomicOr(&VQ_RVQ_ERR, (unsigned)VQ_DEVERR_WAIT_TIMEOUT);
-            for (int k = 1; k < P4_STAGES; ++k) {
-                const int it2 = it + k;
-                if (gw + it2 * tw < nblk)
-                    (void)mbar_wait_bounded(&bars[it2 % P4_STAGES], (uint32_t)(it2 / P4_STAGES) & 1u);
-            }
-            return;
-        }
-        const unsigned char *sbuf = ring + s * ENC_BLOCK;
-
-        float acc[8][2][4];
-        float q0, q1;
-        tc_rotate_block<SGN>(sbuf, ssg, hb, g8, t4, acc, q0, q1);
-        const float n0 = __fsqrt_rn(q0), n1 = __fsqrt_rn(q1);
-        // per row: den = n sqrt(D), the cell slope a / den and the margin
-        // threshold guard den (a zero row gives den = 0 and is always flagged)
-        const float den0 = n0 * SQRT_D_HI, den1 = n1 * SQRT_D_HI;
-        const float sa0 = pa * __frcp_rn(den0), sa1 = pa * __frcp_rn(den1);
-
-        // ---- quantize: word 2 nt + e of the lane (word 4 t4 + 2 nt + e of the
-        // row) from b' = 0..7 of acc[.][nt][2r + e]; the pairs i1 | i2 << 4 of
-        // even coordinates collect in b0, of odd ones in b1 (first at byte 0),
-        // then the low nibbles make the stage-1 word and the high nibbles the
-        // stage-2 word
-        float m0 = __int_as_float(0x7f800000), m1 = m0;
-        uint32_t w1[2][4], w2[2][4];
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-            const float sa = r ? sa1 : sa0, den = r ? den1 : den0;
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                uint32_t b0[2] = {0u, 0u}, b1[2] = {0u, 0u};
-#pragma unroll
-                for (int b = 0; b < 8; ++b) {
-                    const uint32_t px = pair_code_s(acc[b][nt][2 * r], sa, pbc, den, tab, r ? m1 : m0);
-                    const uint32_t py = pair_code_s(acc[b][nt][2 * r + 1], sa, pbc, den, tab, r ? m1 : m0);
-                    if (b & 1) {
-                        b1[0] = __funnelshift_r(b1[0], px, 8);
-                        b1[1] = __funnelshift_r(b1[1], py, 8);
-                    } else {
-                        b0[0] = __funnelshift_r(b0[0], px, 8);
-                        b0[1] = __funnelshift_r(b0[1], py, 8);
-                    }
+    if (warp == 0) {
+        // ---- producer
+        if (lane == 0) {
+            const uint64_t pol = l2_policy_evict_first();
+            int i = 0;
+            for (int t = cta; t < ntiles; t += ncta, ++i) {
+                const int s = i % NST;
+                if (i >= NST && !mbar_wait_bounded(&x_empty[s], (uint32_t)((i / NST) - 1) & 1u)) {
+                    atomicOr(&VQ_RVQ_ERR, (unsigned)VQ_DEVERR_WAIT_TIMEOUT);
+                    *abort_flag = 1u;
+                    break;
                 }
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    w1[r][2 * nt + e] = (b0[e] & 0x0F0F0F0Fu) | ((b1[e] & 0x0F0F0F0Fu) << 4);
-                    w2[r][2 * nt + e] = ((b0[e] >> 4) & 0x0F0F0F0Fu) | (b1[e] & 0xF0F0F0F0u);
-                }
+                if (*abort_flag) break;
+                unsigned char *dst = ring + s * TE_TILE;
+                mbar_arrive_expect_tx(&x_full[s], (uint32_t)TE_TILE);
+                tma_load_2d(dst, &p.tmap, 0, t * TE_M, &x_full[s], pol);
+                tma_load_2d(dst + TE_HALF, &p.tmap, 64, t * TE_M, &x_full[s], pol);
             }
-        }
-
-        // ---- guard band: a row is flagged if any of its four lanes saw a value
-        // inside the band (and always when it is zero)
-        const int row0 = blk * ER + g8, row1 = row0 + 8;
-        const bool valid0 = row0 < p.N, valid1 = row1 < p.N;
-        const bool f0 = valid0 && (!(m0 >= p.guard * den0) || !(q0 > 0.0f));
-        const bool f1 = valid1 && (!(m1 >= p.guard * den1) || !(q1 > 0.0f));
-        int f = (f0 ? 1 : 0) | (f1 ? 2 : 0);
-        f |= __shfl_xor_sync(FULL_MASK, f, 1);
-        f |= __shfl_xor_sync(FULL_MASK, f, 2);
-
-        // ---- fast words: 16 bytes per lane, row and stream (a block's 16 rows
-        // are contiguous in both streams)
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-            const int row = r ? row1 : row0;
-            size_t drow = (size_t)row;
-            if ((r ? valid1 : valid0) && !(f & (1 << r)) && (dense || rvq_dst_row(p, row, drow))) {
-                *reinterpret_cast<uint4 *>(p.p1 + drow * W + 4 * t4) = make_uint4(w1[r][0], w1[r][1], w1[r][2], w1[r][3]);
-                *reinterpret_cast<uint4 *>(p.p2 + drow * W + 4 * t4) = make_uint4(w2[r][0], w2[r][1], w2[r][2], w2[r][3]);
-                if (t4 == 0) p.norms[drow] = r ? n1 : n0;
+            for (int k = 0; k < NST && k < i; ++k) {
+                const int j = i - 1 - k;
+                (void)mbar_wait_bounded(&x_full[j % NST], (uint32_t)(j / NST) & 1u);
             }
-        }
-
-        // ---- flagged rows: exact recompute by the warp
-        unsigned fl = (__ballot_sync(FULL_MASK, (f & 1) != 0) & 0x11111111u) |
-                      ((__ballot_sync(FULL_MASK, (f & 2) != 0) & 0x11111111u) << 1);
-        while (fl) {
-            const int bit = __ffs(fl) - 1;
-            fl &= fl - 1;
-            const int r = (bit >> 2) + 8 * (bit & 1);
-            rvq_fixup_row<4, true>(p, sbuf, r, blk * ER + r, lane, tb1, tc1, tb2, tc2, tcen);
         }
         __syncwarp();
-
-        fence_proxy_async_smem();
-        {
-            const int nb = blk + P4_STAGES * tw;
-            if (nb < nblk) issue(nb, s);
+    } else if (warp == 1) {
+        // ---- MMA issue: tile i into accumulator buffer i % TE_G
+        if (lane == 0) {
+            constexpr uint32_t IDESC = qt_idesc(128);
+            const uint32_t bb = smem_u32(bop), rb = smem_u32(ring);
+            int i = 0;
+            for (int t = cta; t < ntiles; t += ncta, ++i) {
+                const int s = i % NST, a = i % TE_G;
+                bool ok = mbar_wait_bounded(&x_full[s], (uint32_t)(i / NST) & 1u);
+                if (ok && i >= TE_G) ok = mbar_wait_bounded(&acc_empty[a], (uint32_t)((i / TE_G) - 1) & 1u);
+                if (!ok || *abort_flag) {
+                    if (!ok) atomicOr(&VQ_RVQ_ERR, (unsigned)VQ_DEVERR_WAIT_TIMEOUT);
+                    *abort_flag = 1u;
+                    break;
+                }
+                qt_fence_after();
+                const uint32_t xa = rb + s * TE_TILE;
+#pragma unroll
+                for (int kb = 0; kb < 2; ++kb) {
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        qt_mma(tmem + (uint32_t)(a * 128), qt_desc(xa + kb * TE_HALF + kk * 32),
+                               qt_desc(bb + kb * TE_HALF + kk * 32), IDESC, (kb | kk) ? 1u : 0u);
+                }
+                qt_commit(&acc_full[a]);
+            }
         }
-        if (++s == P4_STAGES) {
-            s = 0;
-            ph ^= 1u;
+        __syncwarp();
+    } else {
+        // ---- epilogue group g: tiles i with i % TE_G == g; thread = row
+        const int g = (warp - 2) >> 2;
+        const int q = warp & 3;  // tensor-memory lane quadrant of this warp
+        const int r = 32 * q + lane;
+        const uint32_t tl = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(g * 128);
+        // exact-recompute tables (shuffle) and book constants
+        const float tb1 = p.t1.bnd[lane];
+        const int tc1 = p.t1.code[lane];
+        const float tb2 = p.t2.bnd[lane];
+        const int tc2 = p.t2.code[lane];
+        const float tcen = p.c1[lane & ((1 << BITS) - 1)];
+        [[maybe_unused]] const float b1u = p.b1[2], b2u = p.b2[2];
+        [[maybe_unused]] const float bc2u = p.b1[2] - p.c1[2], dcu = p.c1[3] - p.c1[2];
+        [[maybe_unused]] const float kb1 = __fdiv_rn(2.0f, b1u), kb2 = __fdiv_rn(2.0f, b2u);
+        [[maybe_unused]] const float pa = p.pt.a, pbc = p.pt.bc;
+        [[maybe_unused]] const uint32_t tab =
+            smem_u32(ptab) + 8u * (uint32_t)(lane & (P4_REP - 1)) - (0x4B400000u << 7);
+        const bool dense = p.dst_off == nullptr && p.S_dst == p.S && p.S_q == p.S;
+        int i = 0;
+        for (int t = cta; t < ntiles; t += ncta, ++i) {
+            if (i % TE_G != g) continue;
+            const int s = i % NST;
+            const bool ok = mbar_wait_bounded(&acc_full[g], (uint32_t)(i / TE_G) & 1u);
+            if (!__all_sync(FULL_MASK, ok) || *abort_flag) {
+                if (!ok && lane == 0) atomicOr(&VQ_RVQ_ERR, (unsigned)VQ_DEVERR_WAIT_TIMEOUT);
+                *abort_flag = 1u;
+                break;
+            }
+            qt_fence_after();
+            const int row = t * TE_M + r;
+            const bool valid = row < p.N;
+
+            // the norm from the row's fp16 values in the staged tile: exact
+            // squares (fp16 operands, fp32 result), fp32 sums in 16 partial
+            // sums of 8 (12 roundings deep at most)
+            const unsigned char *xt = ring + s * TE_TILE;
+            float ps[16];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const uint4 v = *reinterpret_cast<const uint4 *>(xt + h * TE_HALF + swz128(r, c));
+                    ps[8 * h + c] = sq8_f16(v);
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < 8; ++k) ps[k] += ps[k + 8];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) ps[k] += ps[k + 4];
+            ps[0] += ps[2];
+            ps[1] += ps[3];
+            const float qn = ps[0] + ps[1];
+            const float n = __fsqrt_rn(qn);
+            const float den = n * SQRT_D_HI;
+            // the staged tile has been read (the MMAs are done with it too):
+            // free the stage now, so that the producer keeps the ring full
+            // through the quantization (a flagged row is re-read from global
+            // memory by the exact recompute)
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&x_empty[s]);
+
+            // pass 2: quantize the row in natural coordinate order, 32
+            // coordinates (one tensor-memory load) at a time, the next load in
+            // flight during each chunk; the words go straight to the row's
+            // destination (a flagged row is rewritten by the exact recompute)
+            size_t drow = (size_t)row;
+            const bool okrow = valid && (dense || rvq_dst_row(p, row, drow));
+            uint32_t *d1 = p.p1 + drow * W, *d2 = p.p2 + drow * W;
+            uint32_t va[32], vb[32];
+            bool flag;
+            if constexpr (MODE == MODE_SYM) {
+                const SymRow sk = sym2_row(den, p.guard * den, b1u, b2u, bc2u, dcu, kb1, kb2);
+                float m1 = __int_as_float(0x7f800000), m2 = m1;
+                // words 2c (coordinates 32c .. 32c + 15) and 2c + 1, code j at bits 2j
+                auto chunk = [&](const uint32_t (&v)[32], int c) {
+                    uint32_t a1x = 0u, a2x = 0u, a1y = 0u, a2y = 0u;
+#pragma unroll
+                    for (int b = 15; b >= 0; --b)
+                        sym2_code2(make_float2(__uint_as_float(v[2 * b]), __uint_as_float(v[2 * b + 1])), sk, a1x, a2x,
+                                   a1y, a2y, m1, m2);
+                    uint32_t x1, x2, y1, y2;
+                    sym2_words(a1x, a2x, x1, x2);
+                    sym2_words(a1y, a2y, y1, y2);
+                    if (okrow) {
+                        *reinterpret_cast<uint2 *>(d1 + 2 * c) = make_uint2(x1, y1);
+                        *reinterpret_cast<uint2 *>(d2 + 2 * c) = make_uint2(x2, y2);
+                    }
+                };
+                qt_ld32(tl, va);
+#pragma unroll 1
+                for (int c = 0; c < 4; c += 2) {
+                    qt_wait_ld();
+                    qt_hold(va);
+                    qt_ld32(tl + 32 * (c + 1), vb);
+                    chunk(va, c);
+                    qt_wait_ld();
+                    qt_hold(vb);
+                    if (c + 2 < 4) qt_ld32(tl + 32 * (c + 2), va);
+                    chunk(vb, c + 1);
+                }
+                flag = !(m1 >= sk.G1) || !(m2 >= sk.G2) || !(qn > 0.0f);
+            } else {
+                const float sa = pa * __frcp_rn(den);
+                float m = __int_as_float(0x7f800000);
+                // words 4c .. 4c + 3, eight coordinates each: pairs of even
+                // coordinates collect in b0, of odd ones in b1
+                auto chunk = [&](const uint32_t (&v)[32], int c) {
+                    uint32_t o1[4], o2[4];
+#pragma unroll
+                    for (int w = 0; w < 4; ++w) {
+                        uint32_t b0 = 0u, b1 = 0u;
+#pragma unroll
+                        for (int e = 0; e < 8; e += 2) {
+                            b0 = __funnelshift_r(b0, pair_code_s(__uint_as_float(v[8 * w + e]), sa, pbc, den, tab, m), 8);
+                            b1 = __funnelshift_r(b1, pair_code_s(__uint_as_float(v[8 * w + e + 1]), sa, pbc, den, tab, m), 8);
+                        }
+                        o1[w] = (b0 & 0x0F0F0F0Fu) | ((b1 & 0x0F0F0F0Fu) << 4);
+                        o2[w] = ((b0 >> 4) & 0x0F0F0F0Fu) | (b1 & 0xF0F0F0F0u);
+                    }
+                    if (okrow) {
+                        *reinterpret_cast<uint4 *>(d1 + 4 * c) = make_uint4(o1[0], o1[1], o1[2], o1[3]);
+                        *reinterpret_cast<uint4 *>(d2 + 4 * c) = make_uint4(o2[0], o2[1], o2[2], o2[3]);
+                    }
+                };
+                qt_ld32(tl, va);
+#pragma unroll 1
+                for (int c = 0; c < 4; c += 2) {
+                    qt_wait_ld();
+                    qt_hold(va);
+                    qt_ld32(tl + 32 * (c + 1), vb);
+                    chunk(va, c);
+                    qt_wait_ld();
+                    qt_hold(vb);
+                    if (c + 2 < 4) qt_ld32(tl + 32 * (c + 2), va);
+                    chunk(vb, c + 1);
+                }
+                flag = !(m >= p.guard * den) || !(qn > 0.0f);
+            }
+            // the accumulator buffer is free for tile i + TE_G
+            qt_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[g]);
+
+            flag = flag && valid;
+            if (okrow && !flag) p.norms[drow] = n;
+            __syncwarp();  // the fast words of a flagged row are written before its exact ones
+            // rows inside the guard band: exact recompute by the warp, the row
+            // read again from global memory
+            unsigned fl = __ballot_sync(FULL_MASK, flag);
+            while (fl) {
+                const int bit = __ffs(fl) - 1;
+                fl &= fl - 1;
+                rvq_fixup_row<BITS, MODE == MODE_PAIR, 0>(p, nullptr, 32 * q + bit, t * TE_M + 32 * q + bit, lane, tb1, tc1,
+                                                          tb2, tc2, tcen);
+            }
+            __syncwarp();
         }
     }
+
+    qt_fence_before();
+    __syncthreads();
+    qt_fence_after();
+    if (warp == 1) tmem_free(tmem, 512);
 }
 
 }  // namespace
