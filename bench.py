@@ -181,7 +181,7 @@ def build_workload(name, dev, rank=0, layers=None, batch=None, chunked=False, ch
             dec = None
         # the library's books take the tensor-core encoders (b = 2: symmetric
         # books, b = 4: the pair table)
-        ekern = {2: "rvq_encode_sym2_kernel", 4: "rvq_encode_pair4_kernel"}.get(bits, "rvq_encode_kernel")
+        ekern = "rvq_encode_tc_kernel" if bits in (2, 4) else "rvq_encode_kernel"
         ops.append(Op(tag + "rvq_encode", ekern, enc, rvq_bytes(rows, bits), rows * D))
         if dec is not None:
             ops.append(Op(tag + "rvq_decode", "rvq_decode_kernel", dec, rvq_bytes(rows, bits), rows * D))

@@ -12,11 +12,12 @@
 // The Walsh-Hadamard butterflies run over j in registers and over the lane
 // bits by shuffles.  Codes go through a per-warp byte buffer in shared memory
 // so that lanes can assemble words whose codes straddle lanes (b = 3).
-// Exactness: the row is computed in fp32; a step with any value within the
-// guard band of a boundary (or a zero row) is recomputed by the same code in
-// binary64 (the fp16 inputs are exact there; the rounding then differs from the
-// oracle's only far inside its tie band).  The row norm is always summed in
-// binary64.
+// Exactness: the row is computed in fp32 (the norm from a double-float sum of
+// the exact squares, no binary64 on the common path: that pipe is slow on
+// this GPU); a step with any value within the guard band of a boundary (or a
+// zero row) is recomputed by the same code in binary64 (the fp16 inputs are
+// exact there; the rounding then differs from the oracle's only far inside
+// its tie band).
 #include <cuda_fp16.h>
 
 #include "device_common.cuh"
@@ -134,6 +135,14 @@ __device__ __forceinline__ void load_halves(const __half *src, float (&x)[C])
     }
 }
 
+// sqrt(D) as the nearest fp32 (D a power of two from 8 to 256)
+template <int D>
+__host__ __device__ constexpr float sqrt_d_f()
+{
+    return D == 8 ? 2.8284271247461903f : D == 16 ? 4.0f : D == 32 ? 5.656854249492381f : D == 64 ? 8.0f
+         : D == 128 ? 11.313708498984761f : 16.0f;
+}
+
 template <int D, int BITS>
 __global__ void __launch_bounds__(GEN_WARPS * 32) rvq_generic_encode_kernel(const __grid_constant__ RvqGenericParams p)
 {
@@ -158,13 +167,33 @@ __global__ void __launch_bounds__(GEN_WARPS * 32) rvq_generic_encode_kernel(cons
 #pragma unroll
             for (int j = 0; j < C; ++j) x[j] = 0.0f;
         }
-        // row norm: squares of fp16 values are exact in fp32, summed in binary64
-        double s2 = 0.0;
+        // row norm: squares of fp16 values are exact in fp32, summed as a
+        // double-float (two_sum), the square root corrected once: the norm is
+        // the correctly rounded fp32 of the exact one but for rare ties, with
+        // no binary64 arithmetic (a slow pipe on this GPU) on the common path
+        float qh = 0.0f, ql = 0.0f;
 #pragma unroll
-        for (int j = 0; j < C; ++j) s2 += (double)(x[j] * x[j]);
+        for (int j = 0; j < C; ++j) {
+            float t, e;
+            two_sum(qh, x[j] * x[j], t, e);
+            qh = t;
+            ql += e;
+        }
 #pragma unroll
-        for (int m = 1; m < LPR; m <<= 1) s2 += __shfl_xor_sync(FULL_MASK, s2, m);
-        const double n64 = sqrt(s2);
+        for (int m = 1; m < LPR; m <<= 1) {
+            const float oh = __shfl_xor_sync(FULL_MASK, qh, m);
+            const float ol = __shfl_xor_sync(FULL_MASK, ql, m);
+            float t, e;
+            two_sum(qh, oh, t, e);
+            e += ql + ol;
+            fast_two_sum(t, e, qh, ql);
+        }
+        float nh = 0.0f, nl = 0.0f;
+        if (qh > 0.0f) {
+            nh = __fsqrt_rn(qh);
+            nl = __fdiv_rn(fmaf(-nh, nh, qh) + ql, 2.0f * nh);
+        }
+        const float nrm = __fadd_rn(nh, nl);
 
         // fp32 fast path
         uint32_t q1[C], q2[C];
@@ -173,14 +202,15 @@ __global__ void __launch_bounds__(GEN_WARPS * 32) rvq_generic_encode_kernel(cons
 #pragma unroll
             for (int j = 0; j < C; ++j) y[j] = x[j];
             gen_wht<float, C, LPR>(y, ll);
-            const float inv = n64 > 0.0 ? (float)(inv_sqrt_d / n64) : 0.0f;
+            const float inv = qh > 0.0f ? __frcp_rn(nrm * (float)sqrt_d_f<D>()) : 0.0f;
 #pragma unroll
             for (int j = 0; j < C; ++j) y[j] *= inv;
             float m = __int_as_float(0x7f800000);
             gen_quant<float, BITS, C>(p, y, tcen, q1, q2, m);
-            const bool flag = valid && (!(m >= p.guard) || !(n64 > 0.0));
+            const bool flag = valid && (!(m >= p.guard) || !(qh > 0.0f));
             if (__any_sync(FULL_MASK, flag)) {
                 // binary64 recompute of the whole step (uniform across the warp)
+                const double n64 = (double)nh + (double)nl;
                 double u[C];
 #pragma unroll
                 for (int j = 0; j < C; ++j) u[j] = n64 > 0.0 ? (double)x[j] / n64 : 0.0;
@@ -220,7 +250,7 @@ __global__ void __launch_bounds__(GEN_WARPS * 32) rvq_generic_encode_kernel(cons
         }
         if (valid && ll == 0) {
             size_t drow = 0;
-            if (gen_dst_row(p, row, drow)) p.norms[drow] = (float)n64;
+            if (gen_dst_row(p, row, drow)) p.norms[drow] = nrm;
         }
         __syncwarp();
     }
