@@ -296,8 +296,10 @@ def build_workload(name, dev, rank=0, layers=None, batch=None, chunked=False, ch
 
             def gdec(bits=bits, cbg=cbg, g1=g1, g2=g2, gn=gn, go=go, Dg=Dg):
                 api.vq_rvq_unpack_dequant(g1, g2, gn, bits, cbg[0], cbg[2], out=go, stream=stream, D=Dg)
-            ops.append(Op(tag + "rvq_encode", "rvq_generic_encode_kernel", genc, rvq_bytes(rows, bits, Dg), rows * Dg))
-            ops.append(Op(tag + "rvq_decode", "rvq_generic_decode_kernel", gdec, rvq_bytes(rows, bits, Dg), rows * Dg))
+            ops.append(Op(tag + "rvq_encode", "rvq_generic_encode_kernel<%d, %d>" % (Dg, bits), genc,
+                          rvq_bytes(rows, bits, Dg), rows * Dg))
+            ops.append(Op(tag + "rvq_decode", "rvq_generic_decode_kernel<%d, %d>" % (Dg, bits), gdec,
+                          rvq_bytes(rows, bits, Dg), rows * Dg))
             results.extend([g1, g2, gn, go])
     elif name == "c2":
         cfg = cfgs["c2_kivi_b2_32x4096"]

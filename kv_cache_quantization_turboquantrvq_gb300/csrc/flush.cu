@@ -32,7 +32,7 @@ namespace vq {
 namespace {
 
 constexpr int FL_WARPS = 16;
-static_assert(enc_warps(1, MODE_SYM) == FL_WARPS && TE_THREADS <= FL_WARPS * 32, "encoder bodies fit 16 warps");
+static_assert(enc_warps(1, MODE_SYM) == FL_WARPS && TE_THREADS == FL_WARPS * 32, "encoder bodies take 16 warps");
 static_assert(key_warps<2, 32>() == FL_WARPS && key_warps<4, 64>() == FL_WARPS, "key bodies run 16 warps");
 
 constexpr int WIN_ROWS = 16;  // window rows per warp item
@@ -79,7 +79,7 @@ __device__ __noinline__ void part_rvq1(const RvqEncodeParams &q, int c, int n)
     rvq_encode_body<1, MODE_SYM, false>(q, c, n);
 }
 
-// the tensor-memory encoder runs 14 of the CTA's 16 warps
+// the tensor-memory encoder runs all 16 warps of the CTA (two of them fixup warps)
 template <int MODE>
 __device__ __noinline__ void part_rvq_tm(const RvqEncodeParams &q, int c, int n)
 {

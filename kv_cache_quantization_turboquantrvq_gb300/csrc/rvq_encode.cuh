@@ -822,8 +822,13 @@ __device__ __forceinline__ uint32_t pair_code_s(float s, float a, float bc, floa
 // SM): warp 0 streams X tiles (TMA, TE_STAGES-deep ring), warp 1 owns the
 // tensor memory and issues the MMAs (one thread), TE_G groups of four warps
 // run the epilogue on alternate tiles, each group with its own accumulator
-// buffer (128 columns).  Rows with a value inside the guard band go to the
-// warp's exact recompute (rvq_fixup_row) while the stage is still held.
+// buffer (128 columns), and TE_FIX warps recompute flagged rows.  A row with
+// a value inside the guard band is queued (its global index, in a shared-memory
+// list) for the fixup warps, which redo it exactly (rvq_fixup_row, the row
+// read again from global memory) off the epilogue's critical path: an epilogue
+// warp that stopped for a recompute would hold its accumulator buffer and,
+// through the in-order MMA issue, the whole pipeline.  When the list is full
+// the epilogue warp recomputes the row itself.
 // Every wait is bounded; on a timeout the CTA records VQ_DEVERR_WAIT_TIMEOUT,
 // waits (bounded) for its copies in flight, frees its tensor memory and
 // returns.
@@ -844,14 +849,18 @@ __device__ __forceinline__ float sq8_f16(uint4 v)
 
 constexpr int TE_M = 128;
 constexpr int TE_G = 3;                       // epilogue groups (4 warps each)
-constexpr int TE_THREADS = 32 * (2 + 4 * TE_G);
+constexpr int TE_FIX = 2;                     // fixup warps
+constexpr int TE_FIX0 = 2 + 4 * TE_G;         // first fixup warp
+constexpr int TE_THREADS = 32 * (TE_FIX0 + TE_FIX);
+constexpr int TE_FQ = 1024;                   // flagged-row list entries per CTA
+constexpr int TE_FQ_BACKLOG = 2;              // list entries allowed to wait for a fixup warp
 constexpr int TE_HALF = TE_M * 128;           // a 64-coordinate half of a tile (16 KB)
 constexpr int TE_TILE = 2 * TE_HALF;          // 32 KB
 constexpr int TE_BOP = 2 * 128 * 128;         // B = H128 diag(s), fp16, 32 KB
 __host__ __device__ constexpr int te_stages(int mode) { return mode == MODE_PAIR ? 3 : 4; }
 __host__ __device__ constexpr int te_smem(int mode)
 {
-    return 1024 + TE_BOP + (mode == MODE_PAIR ? P4_TAB_BYTES : 0) + te_stages(mode) * TE_TILE + 256;
+    return 1024 + TE_BOP + (mode == MODE_PAIR ? P4_TAB_BYTES : 0) + te_stages(mode) * TE_TILE + 256 + 4 * TE_FQ + 32;
 }
 static_assert(te_smem(MODE_PAIR) <= SMEM_MAX && te_smem(MODE_SYM) <= SMEM_MAX, "tensor-memory encoder shared memory");
 
@@ -871,6 +880,10 @@ __device__ __forceinline__ void rvq_encode_tm_body(const RvqEncodeParams &p, int
     uint64_t *acc_full = bars + 2 * NST, *acc_empty = acc_full + TE_G;
     uint32_t *tslot = reinterpret_cast<uint32_t *>(acc_empty + TE_G);
     volatile uint32_t *abort_flag = tslot + 1;
+    // flagged-row list: entries written, entries claimed by the fixup warps,
+    // epilogue warps done, the entries (global row + 1; 0 = not yet written)
+    uint32_t *fq_n = tslot + 2, *fq_take = tslot + 3, *fq_done = tslot + 4;
+    volatile uint32_t *fq = tslot + 8;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int ntiles = (p.N + TE_M - 1) / TE_M;
 
@@ -884,8 +897,12 @@ __device__ __forceinline__ void rvq_encode_tm_body(const RvqEncodeParams &p, int
             mbar_init(&acc_empty[g], 4);
         }
         *abort_flag = 0u;
+        *fq_n = 0u;
+        *fq_take = 0u;
+        *fq_done = 0u;
         fence_mbar_init();
     }
+    for (int i = threadIdx.x; i < TE_FQ; i += blockDim.x) fq[i] = 0u;
     // B[n][k] = H128[j(n)][k] s_k, fp16, K-major with the 128-byte swizzle:
     // 16-byte chunk c (k = 8c .. 8c + 7) of row n.  Row n of B is column n of
     // the accumulator; for the symmetric books the output coordinates are
@@ -968,7 +985,7 @@ __device__ __forceinline__ void rvq_encode_tm_body(const RvqEncodeParams &p, int
             }
         }
         __syncwarp();
-    } else {
+    } else if (warp < TE_FIX0) {
         // ---- epilogue group g: tiles i with i % TE_G == g; thread = row
         const int g = (warp - 2) >> 2;
         const int q = warp & 3;  // tensor-memory lane quadrant of this warp
@@ -1112,12 +1129,28 @@ __device__ __forceinline__ void rvq_encode_tm_body(const RvqEncodeParams &p, int
             __syncwarp();
             if (lane == 0) mbar_arrive(&acc_empty[g]);
 
-            flag = flag && valid;
+            flag = flag && okrow;
             if (okrow && !flag) p.norms[drow] = n;
+            // rows inside the guard band go to the fixup warps (this thread's
+            // fast words ordered before their exact ones by the fence and the
+            // list entry) while they keep up (at most TE_FQ_BACKLOG entries
+            // waiting) and the list has room; else the warp recomputes them here
+            bool here = false;
+            if (flag) {
+                const int pend = (int)(*reinterpret_cast<volatile uint32_t *>(fq_n) -
+                                       *reinterpret_cast<volatile uint32_t *>(fq_take));
+                here = pend >= TE_FQ_BACKLOG;
+                if (!here) {
+                    __threadfence_block();
+                    const uint32_t k = atomicAdd(fq_n, 1u);
+                    if (k < (uint32_t)TE_FQ)
+                        fq[k] = (uint32_t)row + 1u;
+                    else
+                        here = true;
+                }
+            }
             __syncwarp();  // the fast words of a flagged row are written before its exact ones
-            // rows inside the guard band: exact recompute by the warp, the row
-            // read again from global memory
-            unsigned fl = __ballot_sync(FULL_MASK, flag);
+            unsigned fl = __ballot_sync(FULL_MASK, here);
             while (fl) {
                 const int bit = __ffs(fl) - 1;
                 fl &= fl - 1;
@@ -1125,6 +1158,50 @@ __device__ __forceinline__ void rvq_encode_tm_body(const RvqEncodeParams &p, int
                                                           tb2, tc2, tcen);
             }
             __syncwarp();
+        }
+        __syncwarp();
+        if (lane == 0) {
+            __threadfence_block();
+            atomicAdd(fq_done, 1u);
+        }
+    } else {
+        // ---- fixup warps: each claims the next entry of the flagged-row list
+        const float tb1 = p.t1.bnd[lane];
+        const int tc1 = p.t1.code[lane];
+        const float tb2 = p.t2.bnd[lane];
+        const int tc2 = p.t2.code[lane];
+        const float tcen = p.c1[lane & ((1 << BITS) - 1)];
+        for (;;) {
+            uint32_t k = 0u;
+            if (lane == 0) k = atomicAdd(fq_take, 1u);
+            k = __shfl_sync(FULL_MASK, k, 0);
+            if (k >= (uint32_t)TE_FQ) break;
+            // wait for entry k, or for every epilogue warp to finish with fewer entries
+            uint32_t e = 0u;
+            bool ok = true;
+            const uint64_t t0 = globaltimer_ns();
+            for (;;) {
+                e = fq[k];
+                if (e != 0u) break;
+                if (*reinterpret_cast<volatile uint32_t *>(fq_done) == 4u * TE_G) {
+                    __threadfence_block();
+                    e = fq[k];
+                    if (e != 0u || *reinterpret_cast<volatile uint32_t *>(fq_n) <= k) break;
+                }
+                if (globaltimer_ns() - t0 > MBAR_TIMEOUT_NS) {
+                    ok = false;
+                    break;
+                }
+                __nanosleep(256);
+            }
+            e = __shfl_sync(FULL_MASK, e, 0);
+            if (!__all_sync(FULL_MASK, ok)) {
+                if (lane == 0) atomicOr(&VQ_RVQ_ERR, (unsigned)VQ_DEVERR_WAIT_TIMEOUT);
+                break;
+            }
+            if (e == 0u) break;  // the list ended before entry k
+            __threadfence_block();
+            rvq_fixup_row<BITS, MODE == MODE_PAIR, 0>(p, nullptr, 0, (int)(e - 1u), lane, tb1, tc1, tb2, tc2, tcen);
         }
     }
 
