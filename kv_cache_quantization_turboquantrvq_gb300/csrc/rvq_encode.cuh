@@ -448,6 +448,231 @@ __device__ __noinline__ void rvq_fixup_row(const RvqEncodeParams &p, const unsig
     if (lane == 0) p.norms[drow] = __fadd_rn(nh, nl);
 }
 
+// Book constants of the tensor-memory encoder's exact recompute, held in
+// registers: the 32-cell stage tables (lane entries, read by shuffle; b = 4)
+// and their grid maps, or the three boundaries of each stage (b = 2), and the
+// stage-1 centroid of lane l & (2^b - 1).
+struct FixBooks {
+    float tb1, tb2, tcen;
+    int tc1, tc2;
+    float a1, bc1, a2, bc2;
+    float b1[3], b2[3];
+};
+
+template <int MODE>
+__device__ __forceinline__ FixBooks fix_books(const RvqEncodeParams &p, int lane)
+{
+    FixBooks f;
+    f.tcen = p.c1[lane & (MODE == MODE_PAIR ? 15 : 3)];
+    if constexpr (MODE == MODE_PAIR) {
+        f.tb1 = p.t1.bnd[lane];
+        f.tc1 = p.t1.code[lane];
+        f.tb2 = p.t2.bnd[lane];
+        f.tc2 = p.t2.code[lane];
+        f.a1 = p.t1.a;
+        f.bc1 = p.t1.bc;
+        f.a2 = p.t2.a;
+        f.bc2 = p.t2.bc;
+    } else {
+#pragma unroll
+        for (int k = 0; k < 3; ++k) {
+            f.b1[k] = p.b1[k];
+            f.b2[k] = p.b2[k];
+        }
+    }
+    return f;
+}
+
+// [v > b] for the double-float v = vh + vl and an fp32 b
+__device__ __forceinline__ int df_gt(float vh, float vl, float b) { return (vh > b || (vh == b && vl > 0.0f)) ? 1 : 0; }
+
+// Boundary count of a double-float value in one stage (the tensor-memory
+// encoder's books): table lookup (b = 4) or the three boundaries (b = 2).
+template <int MODE>
+__device__ __forceinline__ int fix_count(float vh, float vl, float tb, int tc, float a, float bc, const float (&b)[3])
+{
+    if constexpr (MODE == MODE_PAIR) {
+        const int g = grid_cell(vh, a, bc);
+        const float bnd = __shfl_sync(FULL_MASK, tb, g);
+        const int cl = __shfl_sync(FULL_MASK, tc, g);
+        return cl + df_gt(vh, vl, bnd);
+    } else {
+        return df_gt(vh, vl, b[0]) + df_gt(vh, vl, b[1]) + df_gt(vh, vl, b[2]);
+    }
+}
+
+// Exact recompute of one row by one warp, for the tensor-memory encoder's
+// books (symmetric b = 2, or b = 4 with grid tables): lane l holds coordinates
+// 4l .. 4l + 3 (one 8-byte load).  Same arithmetic as rvq_fixup_row: S = H
+// diag(s) x exactly from three pieces whose transforms are exact in fp32, Q,
+// n and 1 / (n sqrt(D)) as double-floats, y = S / (n sqrt(D)) as a
+// double-float, each boundary count on it; the book constants come in
+// registers (no kernel-parameter reads by a runtime index).  (A variant that
+// took two rows per warp, sixteen lanes each, ran slower.)  Words and norm go
+// to the row's destination.
+template <int MODE>
+__device__ __noinline__ void rvq_fixup_tm(const RvqEncodeParams &p, int row, int lane, const FixBooks &fbm)
+{
+    constexpr int NR = 1;
+    constexpr int BITS = MODE == MODE_PAIR ? 4 : 2;
+    constexpr int W = D * BITS / 32;
+    constexpr int LPR = 32 / NR, C = 4 * NR;
+    constexpr int LPW = 32 / (C * BITS);  // lanes per word
+    const FixBooks fb = fbm;  // to registers once (the caller's copy is in local memory)
+    const int ll = lane;
+    float x[C];
+    {
+        uint32_t w[C / 2];
+#pragma unroll
+        for (int k = 0; k < C / 2; ++k) w[k] = 0u;
+        if (row >= 0) {
+            const unsigned char *src = static_cast<const unsigned char *>(p.x) + (size_t)row * ROW_BYTES + ll * (2 * C);
+            if constexpr (C == 8) {
+                const uint4 u = __ldg(reinterpret_cast<const uint4 *>(src));
+                w[0] = u.x; w[1] = u.y; w[2] = u.z; w[3] = u.w;
+            } else {
+                const uint2 u = __ldg(reinterpret_cast<const uint2 *>(src));
+                w[0] = u.x; w[1] = u.y;
+            }
+        }
+        if (p.has_sgn) {
+#pragma unroll
+            for (int k = 0; k < C / 2; ++k) w[k] ^= half2_sign_mask(sign_pair(p.sgn, C * ll + 2 * k));
+        }
+#pragma unroll
+        for (int k = 0; k < C / 2; ++k) {
+            const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&w[k]));
+            x[2 * k] = f.x;
+            x[2 * k + 1] = f.y;
+        }
+    }
+    // row max |x| and sum of squares (double-float) over the row's lanes
+    float amax = 0.0f, qh = 0.0f, ql = 0.0f;
+#pragma unroll
+    for (int j = 0; j < C; ++j) {
+        amax = fmaxf(amax, fabsf(x[j]));
+        float t, e;
+        two_sum(qh, x[j] * x[j], t, e);
+        qh = t;
+        ql += e;
+    }
+#pragma unroll
+    for (int m = LPR / 2; m >= 1; m >>= 1) {
+        amax = fmaxf(amax, __shfl_xor_sync(FULL_MASK, amax, m));
+        const float oh = __shfl_xor_sync(FULL_MASK, qh, m);
+        const float ol = __shfl_xor_sync(FULL_MASK, ql, m);
+        float t, e;
+        two_sum(qh, oh, t, e);
+        e += ql + ol;
+        fast_two_sum(t, e, qh, ql);
+    }
+    // n = sqrt(Q), den = n sqrt(D), inv = 1 / den, as double-floats
+    float nh = 0.0f, nl = 0.0f, ih = 0.0f, il = 0.0f;
+    if (qh > 0.0f) {
+        nh = __fsqrt_rn(qh);
+        nl = __fdiv_rn(fmaf(-nh, nh, qh) + ql, 2.0f * nh);
+        const float ph = nh * SQRT_D_HI;
+        const float pl = fmaf(nh, SQRT_D_HI, -ph) + (nh * SQRT_D_LO + nl * SQRT_D_HI);
+        float dh, dl;
+        fast_two_sum(ph, pl, dh, dl);
+        ih = __fdiv_rn(1.0f, dh);
+        const float t = fmaf(-dh, ih, 1.0f) - dl * ih;
+        il = ih * t;
+    }
+    // exact S = H x from three pieces on the grids 2^(e-15), 2^(e-32) (e the
+    // exponent of max |x|): every partial sum of up to 128 pieces is an
+    // integer below 2^24 in its grid's unit
+    float s1[C], s2[C], s3[C];
+    {
+        const int eM = amax > 0.0f ? ((__float_as_int(amax) >> 23) & 0xff) - 127 : 0;
+        const float q1 = __int_as_float((eM - 15 + 127) << 23);
+        const float iq1 = __int_as_float((15 - eM + 127) << 23);
+        const float q2 = __int_as_float((eM - 32 + 127) << 23);
+        const float iq2 = __int_as_float((32 - eM + 127) << 23);
+#pragma unroll
+        for (int j = 0; j < C; ++j) {
+            const float a = rintf(x[j] * iq1) * q1;
+            const float rem = x[j] - a;
+            const float b = rintf(rem * iq2) * q2;
+            s1[j] = a;
+            s2[j] = b;
+            s3[j] = rem - b;
+        }
+    }
+    auto wht = [&](float (&a)[C]) {
+#pragma unroll
+        for (int h = 1; h < C; h <<= 1)
+#pragma unroll
+            for (int j = 0; j < C; ++j)
+                if ((j & h) == 0) {
+                    const float u = a[j], v = a[j + h];
+                    a[j] = u + v;
+                    a[j + h] = u - v;
+                }
+#pragma unroll
+        for (int m = 1; m < LPR; m <<= 1) {
+            const bool upper = (ll & m) != 0;
+#pragma unroll
+            for (int j = 0; j < C; ++j) {
+                const float o = __shfl_xor_sync(FULL_MASK, a[j], m);
+                a[j] = upper ? (o - a[j]) : (a[j] + o);
+            }
+        }
+    };
+    wht(s1);
+    wht(s2);
+    wht(s3);
+
+    uint32_t part1 = 0u, part2 = 0u;
+#pragma unroll
+    for (int j = 0; j < C; ++j) {
+        float a, e1, b, e2, sh, sl;
+        two_sum(s1[j], s2[j], a, e1);
+        two_sum(a, s3[j], b, e2);
+        fast_two_sum(b, e1 + e2, sh, sl);
+        const float yh0 = sh * ih;
+        const float yl0 = fmaf(sh, ih, -yh0) + (sh * il + sl * ih);
+        float yh, yl;
+        fast_two_sum(yh0, yl0, yh, yl);
+        const int code1 = fix_count<MODE>(yh, yl, fb.tb1, fb.tc1, fb.a1, fb.bc1, fb.b1);
+        const float c = __shfl_sync(FULL_MASK, fb.tcen, code1);
+        float rh, rl0, rh2, rl;
+        two_sum(yh, -c, rh, rl0);
+        fast_two_sum(rh, rl0 + yl, rh2, rl);
+        const int code2 = fix_count<MODE>(rh2, rl, fb.tb2, fb.tc2, fb.a2, fb.bc2, fb.b2);
+        part1 |= (uint32_t)code1 << (j * BITS);
+        part2 |= (uint32_t)code2 << (j * BITS);
+    }
+    // words: lanes [w LPW, (w + 1) LPW) of a row hold word w
+    const int sub = ll % LPW;
+    part1 <<= sub * C * BITS;
+    part2 <<= sub * C * BITS;
+#pragma unroll
+    for (int o = 1; o < LPW; o <<= 1) {
+        part1 |= __shfl_xor_sync(FULL_MASK, part1, o);
+        part2 |= __shfl_xor_sync(FULL_MASK, part2, o);
+    }
+    size_t drow = 0;
+    if (row < 0 || !rvq_dst_row(p, row, drow)) return;
+    if (sub == 0) {
+        p.p1[drow * W + ll / LPW] = part1;
+        p.p2[drow * W + ll / LPW] = part2;
+    }
+    if (ll == 0) p.norms[drow] = __fadd_rn(nh, nl);
+}
+
+// The tensor-memory encoder's exact recompute of one row: b = 2 books by
+// rvq_fixup_tm; b = 4 by rvq_fixup_row (the grid tables read in place), which
+// measured a few per cent faster there.
+template <int MODE>
+__device__ __forceinline__ void fixup_one(const RvqEncodeParams &p, int row, int lane, const FixBooks &fb)
+{
+    if constexpr (MODE == MODE_PAIR)
+        rvq_fixup_row<4, true, 0>(p, nullptr, 0, row, lane, fb.tb1, fb.tc1, fb.tb2, fb.tc2, fb.tcen);
+    else
+        rvq_fixup_tm<MODE>(p, row, lane, fb);
+}
+
 // SGN: the randomised-sign rotation (a separate instantiation, so that the
 // plain rotation carries no per-row test).
 template <int BITS, int MODE, bool SGN>
@@ -853,7 +1078,10 @@ constexpr int TE_FIX = 2;                     // fixup warps
 constexpr int TE_FIX0 = 2 + 4 * TE_G;         // first fixup warp
 constexpr int TE_THREADS = 32 * (TE_FIX0 + TE_FIX);
 constexpr int TE_FQ = 1024;                   // flagged-row list entries per CTA
-constexpr int TE_FQ_BACKLOG = 2;              // list entries allowed to wait for a fixup warp
+// List entries allowed to wait for a fixup warp: the symmetric b = 2 books flag
+// ~0.3 % of rows, which two fixup warps absorb; the b = 4 books flag ~2 %, more
+// than they keep up with, so the epilogue takes the excess at once.
+__host__ __device__ constexpr int te_fq_backlog(int mode) { return mode == MODE_PAIR ? 2 : TE_FQ; }
 constexpr int TE_HALF = TE_M * 128;           // a 64-coordinate half of a tile (16 KB)
 constexpr int TE_TILE = 2 * TE_HALF;          // 32 KB
 constexpr int TE_BOP = 2 * 128 * 128;         // B = H128 diag(s), fp16, 32 KB
@@ -991,12 +1219,7 @@ __device__ __forceinline__ void rvq_encode_tm_body(const RvqEncodeParams &p, int
         const int q = warp & 3;  // tensor-memory lane quadrant of this warp
         const int r = 32 * q + lane;
         const uint32_t tl = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(g * 128);
-        // exact-recompute tables (shuffle) and book constants
-        const float tb1 = p.t1.bnd[lane];
-        const int tc1 = p.t1.code[lane];
-        const float tb2 = p.t2.bnd[lane];
-        const int tc2 = p.t2.code[lane];
-        const float tcen = p.c1[lane & ((1 << BITS) - 1)];
+        const FixBooks fb = fix_books<MODE>(p, lane);  // exact recompute
         [[maybe_unused]] const float b1u = p.b1[2], b2u = p.b2[2];
         [[maybe_unused]] const float bc2u = p.b1[2] - p.c1[2], dcu = p.c1[3] - p.c1[2];
         [[maybe_unused]] const float kb1 = __fdiv_rn(2.0f, b1u), kb2 = __fdiv_rn(2.0f, b2u);
@@ -1133,13 +1356,13 @@ __device__ __forceinline__ void rvq_encode_tm_body(const RvqEncodeParams &p, int
             if (okrow && !flag) p.norms[drow] = n;
             // rows inside the guard band go to the fixup warps (this thread's
             // fast words ordered before their exact ones by the fence and the
-            // list entry) while they keep up (at most TE_FQ_BACKLOG entries
+            // list entry) while they keep up (at most te_fq_backlog entries
             // waiting) and the list has room; else the warp recomputes them here
             bool here = false;
             if (flag) {
                 const int pend = (int)(*reinterpret_cast<volatile uint32_t *>(fq_n) -
                                        *reinterpret_cast<volatile uint32_t *>(fq_take));
-                here = pend >= TE_FQ_BACKLOG;
+                here = pend >= te_fq_backlog(MODE);
                 if (!here) {
                     __threadfence_block();
                     const uint32_t k = atomicAdd(fq_n, 1u);
@@ -1154,8 +1377,7 @@ __device__ __forceinline__ void rvq_encode_tm_body(const RvqEncodeParams &p, int
             while (fl) {
                 const int bit = __ffs(fl) - 1;
                 fl &= fl - 1;
-                rvq_fixup_row<BITS, MODE == MODE_PAIR, 0>(p, nullptr, 32 * q + bit, t * TE_M + 32 * q + bit, lane, tb1, tc1,
-                                                          tb2, tc2, tcen);
+                fixup_one<MODE>(p, t * TE_M + 32 * q + bit, lane, fb);
             }
             __syncwarp();
         }
@@ -1166,11 +1388,7 @@ __device__ __forceinline__ void rvq_encode_tm_body(const RvqEncodeParams &p, int
         }
     } else {
         // ---- fixup warps: each claims the next entry of the flagged-row list
-        const float tb1 = p.t1.bnd[lane];
-        const int tc1 = p.t1.code[lane];
-        const float tb2 = p.t2.bnd[lane];
-        const int tc2 = p.t2.code[lane];
-        const float tcen = p.c1[lane & ((1 << BITS) - 1)];
+        const FixBooks fb = fix_books<MODE>(p, lane);
         for (;;) {
             uint32_t k = 0u;
             if (lane == 0) k = atomicAdd(fq_take, 1u);
@@ -1201,7 +1419,7 @@ __device__ __forceinline__ void rvq_encode_tm_body(const RvqEncodeParams &p, int
             }
             if (e == 0u) break;  // the list ended before entry k
             __threadfence_block();
-            rvq_fixup_row<BITS, MODE == MODE_PAIR, 0>(p, nullptr, 0, (int)(e - 1u), lane, tb1, tc1, tb2, tc2, tcen);
+            fixup_one<MODE>(p, (int)(e - 1u), lane, fb);
         }
     }
 
