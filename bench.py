@@ -665,11 +665,15 @@ def recorded_traffic(kernel):
         return None
     if not rec:
         return None
-    src = os.path.join(ROOT, "kv_cache_quantization_turboquantrvq_gb300", "csrc", rec["source"])
+    # the kernel's source files (one name or a list), hashed in order
+    names = rec["source"] if isinstance(rec["source"], list) else [rec["source"]]
+    hsh = hashlib.sha256()
     try:
-        h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        for n in names:
+            hsh.update(open(os.path.join(ROOT, "kv_cache_quantization_turboquantrvq_gb300", "csrc", n), "rb").read())
     except Exception:
         return None
+    h = hsh.hexdigest()[:16]
     if h != rec.get("source_sha256_16"):
         return None
     return rec
