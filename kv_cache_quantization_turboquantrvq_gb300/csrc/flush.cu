@@ -158,8 +158,8 @@ int rvq_part_smem(int kind)
     default: return te_smem(MODE_PAIR);
     }
 }
-int keys_part_smem(int G) { return 1024 + FL_WARPS * ((G <= 64 ? 1 : 2) * G * KEY_ROW + 16); }
-int values_part_smem() { return 1024 + FL_WARPS * VAL_STAGES * (VSTAGE_BYTES + 8); }
+int keys_part_smem(int G) { return 1024 + FL_WARPS * ((G <= 64 ? 1 : 2) * G * KEY_ROW + 16) + 16; }
+int values_part_smem() { return val_smem_w(FL_WARPS); }
 
 }  // namespace
 
@@ -206,40 +206,80 @@ cudaError_t launch_flush(FlushParams &p, cudaStream_t stream)
         items[3] = 2 * nb;
         bytes[3] = (double)((p.win.k_win ? 1 : 0) + (p.win.v_win ? 1 : 0)) * p.win.B * p.win.H * p.win.R * D * 4;
     }
-    // CTAs: at most one per SM in all, shared by each part's expected time
-    // (its bytes over the rate one SM sustains on it: the parts' measured
-    // whole-GPU rates, in GB/s, the encoders being the slow ones), at least
-    // one per present part and no more than the part has warp items for
-    const double rate[4] = {p.rvq_kind == 4 ? 2300.0 : 3800.0, 5900.0, 6000.0, 6000.0};
+    // CTAs: at most one per SM in all, shared by each part's expected time:
+    // its bytes over the rate one CTA sustains on it (whole-GPU rates in
+    // GB/s, measured on a decode flush of 64 sequences x 8 heads x 128 tokens,
+    // where each part runs below its full-size rate), at least one per
+    // present part and no more than the part has work items for.  The KIVI
+    // and window parts balance their items inside each CTA; the RVQ part's
+    // CTAs each take whole tiles, so its count is chosen with the others':
+    // the split whose slowest part is expected to finish first.
+    const double rate[4] = {p.rvq_kind == 4 ? 1300.0 : p.rvq_kind == 2 ? 2800.0 : 2000.0, 4860.0, 3840.0, 6000.0};
     const int sms = sm_count();
-    double cost[4], total = 0;
     int parts = 0;
-    for (int i = 0; i < 4; ++i) {
-        cost[i] = (bytes[i] > 0 ? bytes[i] : 1.0) / rate[i];
-        if (items[i] > 0) {
-            total += cost[i];
-            ++parts;
-        }
-    }
+    for (int i = 0; i < 4; ++i) parts += items[i] > 0 ? 1 : 0;
     if (parts == 0) return cudaSuccess;
-    int n[4] = {0, 0, 0, 0};
     const int budget = sms > parts ? sms : parts;
-    for (int i = 0; i < 4; ++i) {
-        if (items[i] == 0) continue;
-        const long long useful = i == 0 ? rvq_ctas : (items[i] + FL_WARPS - 1) / FL_WARPS;
-        long long want = (long long)(budget * (cost[i] / total) + 0.5);
-        if (want < 1) want = 1;
-        if (want > useful) want = useful;
-        n[i] = (int)want;
+    long long useful[4];
+    for (int i = 0; i < 4; ++i)
+        useful[i] = items[i] == 0 ? 0 : i == 0 ? rvq_ctas : (items[i] + FL_WARPS - 1) / FL_WARPS;
+    // the KIVI / window parts share `left` CTAs by their costs; the expected
+    // finish (in units of bytes / (GB/s / SM)) of that share
+    auto share = [&](int left, int (&n)[4]) {
+        double tot = 0.0;
+        for (int i = 1; i < 4; ++i)
+            if (items[i] > 0) tot += bytes[i] / rate[i];
+        double worst = 0.0;
+        int used = 0;
+        for (int i = 1; i < 4; ++i) {
+            n[i] = 0;
+            if (items[i] == 0) continue;
+            long long w = (long long)(left * (bytes[i] / rate[i]) / tot + 0.5);
+            if (w < 1) w = 1;
+            if (w > useful[i]) w = useful[i];
+            n[i] = (int)w;
+            used += n[i];
+        }
+        while (used > left) {  // rounding overshoot: trim the largest part
+            int j = 1;
+            for (int i = 2; i < 4; ++i)
+                if (n[i] > n[j]) j = i;
+            if (n[j] <= 1) break;
+            --n[j];
+            --used;
+        }
+        for (int i = 1; i < 4; ++i)
+            if (n[i] > 0) {
+                const double t = bytes[i] / rate[i] / n[i];
+                worst = worst > t ? worst : t;
+            }
+        return worst;
+    };
+    int n[4] = {0, 0, 0, 0};
+    if (items[0] == 0) {
+        (void)share(budget, n);
+    } else {
+        const int others = parts - 1;
+        const double tile_cost = bytes[0] / rate[0] / (double)items[0];  // per item (tile or block)
+        const int per_cta = p.rvq_kind == 1 ? FL_WARPS : 1;             // items a CTA takes at once
+        double best = 1e300;
+        int best_n0 = 1;
+        const long long top = useful[0] < budget - others ? useful[0] : budget - others;
+        for (int n0 = 1; n0 <= top; ++n0) {
+            int m[4];
+            const double t_others = others ? share(budget - n0, m) : 0.0;
+            const long long waves = (items[0] + (long long)n0 * per_cta - 1) / ((long long)n0 * per_cta);
+            const double t0 = waves * per_cta * tile_cost;
+            const double t = t0 > t_others ? t0 : t_others;
+            if (t < best * (1.0 - 1e-9)) {
+                best = t;
+                best_n0 = n0;
+            }
+        }
+        n[0] = best_n0;
+        if (others) (void)share(budget - best_n0, n);
     }
     int sum = n[0] + n[1] + n[2] + n[3];
-    while (sum > budget) {  // rounding overshoot: trim the largest part
-        int j = 0;
-        for (int i = 1; i < 4; ++i)
-            if (n[i] > n[j]) j = i;
-        --n[j];
-        --sum;
-    }
     p.n_rvq = n[0];
     p.n_kk = n[1];
     p.n_kv = n[2];

@@ -236,7 +236,9 @@ constexpr int VAL_WARPS = 20;
 constexpr int VAL_STAGES = 2;
 constexpr int VROWS = 16;
 constexpr int VSTAGE_BYTES = VROWS * ROW_BYTES;  // two 2 KB swizzled boxes
-__host__ __device__ constexpr int val_smem() { return 1024 + VAL_WARPS * VAL_STAGES * (VSTAGE_BYTES + 8); }
+// stages, mbarriers and the CTA's block counter
+__host__ __device__ constexpr int val_smem_w(int warps) { return 1024 + warps * VAL_STAGES * (VSTAGE_BYTES + 8) + 16; }
+__host__ __device__ constexpr int val_smem() { return val_smem_w(VAL_WARPS); }
 
 
 __device__ __forceinline__ bool kivi_off(const KiviQuantParams &p, int b, int &off)
@@ -286,19 +288,28 @@ __device__ __forceinline__ void kivi_values_body(const KiviQuantParams &p, int c
     const int lane = threadIdx.x & 31;
     const int rr = lane & 15, hh = lane >> 4;
     unsigned char *wbuf = smem + warp * (VAL_STAGES * VSTAGE_BYTES);
-    uint64_t *bars =
-        reinterpret_cast<uint64_t *>(smem + WARPS * VAL_STAGES * VSTAGE_BYTES) + warp * VAL_STAGES;
+    uint64_t *bars_all = reinterpret_cast<uint64_t *>(smem + WARPS * VAL_STAGES * VSTAGE_BYTES);
+    uint64_t *bars = bars_all + warp * VAL_STAGES;
+    // the CTA takes the blocks [lo, hi) and its warps claim them one at a
+    // time (a shared counter): warps whose blocks run slower take fewer, so
+    // they finish together
+    uint32_t *claimed = reinterpret_cast<uint32_t *>(bars_all + WARPS * VAL_STAGES);
     if (lane == 0) {
 #pragma unroll
         for (int s = 0; s < VAL_STAGES; ++s) mbar_init(&bars[s], 1);
         fence_mbar_init();
     }
-    __syncwarp();
+    if (threadIdx.x == 0) *claimed = 0u;
+    __syncthreads();
     const uint64_t pol = l2_policy_evict_first();
     const int nsb = (p.S_q + VROWS - 1) / VROWS;  // blocks per (b, h) slice
     const int nblk = p.B * p.H * nsb;
-    const int gw = cta * WARPS + warp;
-    const int tw = ncta * WARPS;
+    const int lo = (int)((long long)cta * nblk / ncta), hi = (int)((long long)(cta + 1) * nblk / ncta);
+    auto claim = [&]() {
+        int b = 0;
+        if (lane == 0) b = lo + (int)atomicAdd(claimed, 1u);
+        return __shfl_sync(FULL_MASK, b, 0);
+    };
 
     auto issue = [&](int blk, int s) {
         if (lane == 0) {
@@ -309,23 +320,23 @@ __device__ __forceinline__ void kivi_values_body(const KiviQuantParams &p, int c
             tma_load_3d(dst + VSTAGE_BYTES / 2, &p.tmap, 64, sb * VROWS, bh, &bars[s], pol);
         }
     };
-#pragma unroll
-    for (int s = 0; s < VAL_STAGES; ++s) {
-        const int blk = gw + s * tw;
-        if (blk < nblk) issue(blk, s);
-    }
+    // sb0, sb1: the blocks staged in stages 0 and 1 (claims are increasing,
+    // and the stages are consumed in claim order)
+    static_assert(VAL_STAGES == 2, "two stages per warp");
+    int sb0 = claim();
+    if (sb0 < hi) issue(sb0, 0);
+    int sb1 = claim();
+    if (sb1 < hi) issue(sb1, 1);
     for (int it = 0;; ++it) {
-        const int blk = gw + it * tw;
-        if (blk >= nblk) break;
-        const int s = it % VAL_STAGES;
+        const int s = it & 1;
+        const int blk = s ? sb1 : sb0;
+        if (blk >= hi) break;
         const bool ok = mbar_wait_bounded(&bars[s], (uint32_t)(it / VAL_STAGES) & 1u);
         if (!__all_sync(FULL_MASK, ok)) {
             if (lane == 0) atomicOr(&VQ_KIVI_ERR, (unsigned)VQ_DEVERR_WAIT_TIMEOUT);
-            for (int k = 1; k < VAL_STAGES; ++k) {
-                const int it2 = it + k;
-                if (gw + it2 * tw < nblk)
-                    (void)mbar_wait_bounded(&bars[it2 % VAL_STAGES], (uint32_t)(it2 / VAL_STAGES) & 1u);
-            }
+            // the other stage's copy, if any, is still in flight
+            const int it2 = it + 1;
+            if ((s ? sb0 : sb1) < hi) (void)mbar_wait_bounded(&bars[it2 & 1], (uint32_t)(it2 >> 1) & 1u);
             return;
         }
         // this thread's 64 values to registers, then refill the stage
@@ -397,8 +408,12 @@ __device__ __forceinline__ void kivi_values_body(const KiviQuantParams &p, int c
         __syncwarp();
         fence_proxy_async_smem();
         {
-            const int nb = blk + VAL_STAGES * tw;
-            if (nb < nblk) issue(nb, s);
+            const int nb = claim();
+            if (s)
+                sb1 = nb;
+            else
+                sb0 = nb;
+            if (nb < hi) issue(nb, s);
         }
         if (!okrow) continue;
         uint32_t *dst = p.packed + dr * W + hh * WL;
@@ -470,7 +485,7 @@ __host__ __device__ constexpr int key_warps()
 template <int BITS, int G>
 __host__ __device__ constexpr int key_smem()
 {
-    return 1024 + key_warps<BITS, G>() * (key_warp_bytes<BITS, G>() + 16);
+    return 1024 + key_warps<BITS, G>() * (key_warp_bytes<BITS, G>() + 16) + 16;  // + the CTA's tile counter
 }
 
 // Words of a tile column whose group range is not held exactly by fp32 and
@@ -509,18 +524,27 @@ __device__ __forceinline__ void kivi_keys_body(const KiviQuantParams &p, int cta
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     unsigned char *wbuf = smem + warp * WBYTES;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + KEY_WARPS * WBYTES) + warp * KEY_STAGES;
+    uint64_t *bars_all = reinterpret_cast<uint64_t *>(smem + KEY_WARPS * WBYTES);
+    uint64_t *bars = bars_all + warp * KEY_STAGES;
+    // the CTA takes the half-tiles [lo, hi) and its warps claim them one at a
+    // time (a shared counter), so that they finish together
+    uint32_t *claimed = reinterpret_cast<uint32_t *>(bars_all + KEY_WARPS * KEY_STAGES);
     if (lane == 0) {
 #pragma unroll
         for (int s = 0; s < KEY_STAGES; ++s) mbar_init(&bars[s], 1);
         fence_mbar_init();
     }
-    __syncwarp();
+    if (threadIdx.x == 0) *claimed = 0u;
+    __syncthreads();
     const uint64_t pol = l2_policy_evict_first();
     const int NG = (p.S_q + G - 1) / G;
     const int ntiles = p.B * p.H * NG * 2;
-    const int gw = cta * KEY_WARPS + warp;
-    const int tw = ncta * KEY_WARPS;
+    const int lo = (int)((long long)cta * ntiles / ncta), hi = (int)((long long)(cta + 1) * ntiles / ncta);
+    auto claim = [&]() {
+        int t = 0;
+        if (lane == 0) t = lo + (int)atomicAdd(claimed, 1u);
+        return __shfl_sync(FULL_MASK, t, 0);
+    };
 
     auto ntok_of = [&](int tile) {
         const int gi = tile >> 1;
@@ -535,22 +559,33 @@ __device__ __forceinline__ void kivi_keys_body(const KiviQuantParams &p, int cta
             tma_load_3d(wbuf + s * TILE, &p.tmap, 64 * chh, g * G, bh, &bars[s], pol);
         }
     };
-#pragma unroll
-    for (int s = 0; s < KEY_STAGES; ++s) {
-        const int t = gw + s * tw;
-        if (t < ntiles) issue(t, s);
+    // st0, st1: the half-tiles staged in stages 0 and 1 (claims are
+    // increasing and consumed in claim order; one stage for G <= 64)
+    static_assert(KEY_STAGES == 1 || KEY_STAGES == 2, "one or two stages per warp");
+    int st0 = claim(), st1 = hi;
+    if (st0 < hi) issue(st0, 0);
+    if constexpr (KEY_STAGES == 2) {
+        st1 = claim();
+        if (st1 < hi) issue(st1, 1);
     }
+    auto refill = [&](int s) {
+        const int nt = claim();
+        if (s)
+            st1 = nt;
+        else
+            st0 = nt;
+        if (nt < hi) issue(nt, s);
+    };
     for (int it = 0;; ++it) {
-        const int tile = gw + it * tw;
-        if (tile >= ntiles) break;
-        const int s = it % KEY_STAGES;
+        const int s = KEY_STAGES == 2 ? (it & 1) : 0;
+        const int tile = s ? st1 : st0;
+        if (tile >= hi) break;
         const bool ok = mbar_wait_bounded(&bars[s], (uint32_t)(it / KEY_STAGES) & 1u);
         if (!__all_sync(FULL_MASK, ok)) {
             if (lane == 0) atomicOr(&VQ_KIVI_ERR, (unsigned)VQ_DEVERR_WAIT_TIMEOUT);
-            for (int k = 1; k < KEY_STAGES; ++k) {
-                const int it2 = it + k;
-                if (gw + it2 * tw < ntiles)
-                    (void)mbar_wait_bounded(&bars[it2 % KEY_STAGES], (uint32_t)(it2 / KEY_STAGES) & 1u);
+            if (KEY_STAGES == 2 && (s ? st0 : st1) < hi) {
+                const int it2 = it + 1;  // the other stage's copy is still in flight
+                (void)mbar_wait_bounded(&bars[it2 & 1], (uint32_t)(it2 >> 1) & 1u);
             }
             return;
         }
@@ -575,10 +610,7 @@ __device__ __forceinline__ void kivi_keys_body(const KiviQuantParams &p, int cta
             // the column is in registers: refill the stage now
             __syncwarp();
             fence_proxy_async_smem();
-            {
-                const int nt = tile + KEY_STAGES * tw;
-                if (nt < ntiles) issue(nt, s);
-            }
+            refill(s);
             __half2 l2 = u2h2(v[0]), h2 = l2, l3 = u2h2(v[1]), h3 = l3;
 #pragma unroll
             for (int i = 2; i < G; i += 2) {
@@ -680,8 +712,7 @@ __device__ __forceinline__ void kivi_keys_body(const KiviQuantParams &p, int cta
             // the tile is consumed: recycle the stage
             __syncwarp();
             fence_proxy_async_smem();
-            const int nt = tile + KEY_STAGES * tw;
-            if (nt < ntiles) issue(nt, s);
+            refill(s);
         }
         if (!okoff) continue;
         *reinterpret_cast<__half2 *>(static_cast<__half *>(p.scale) + gd * D + 64 * chh + 2 * lane) =
