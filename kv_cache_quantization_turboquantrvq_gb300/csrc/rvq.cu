@@ -61,9 +61,10 @@ __host__ __device__ constexpr int dec_table_bytes(int bits) { return bits == 4 ?
 __host__ __device__ constexpr int dec_smem(int bits)
 {
     // 1024-byte alignment of the (swizzled) stages, the b = 4 table, every
-    // warp's stages, every warp's output staging, the mbarriers and the sign
-    // masks of the randomised rotation (64 pair words)
-    return 1024 + dec_table_bytes(bits) + DEC_WARPS * dec_warp_bytes(bits) + DEC_WARPS * DEC_STAGES * 8 + 256;
+    // warp's stages, every warp's output staging, the mbarriers, the sign
+    // masks of the randomised rotation (64 pair words) and the CTA's block
+    // counter
+    return 1024 + dec_table_bytes(bits) + DEC_WARPS * dec_warp_bytes(bits) + DEC_WARPS * DEC_STAGES * 8 + 256 + 16;
 }
 
 // Decoded values c1[i1] + c2[i2] of the 64 coordinates of one half row, as 32
@@ -129,6 +130,9 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) rvq_decode_kernel(const __g
     uint64_t *bars = bars_all + warp * DEC_STAGES;
     // sign masks: word hh * 32 + k flips output coordinates 64 hh + 2k, 64 hh + 2k + 1
     uint32_t *sgm = reinterpret_cast<uint32_t *>(bars_all + DEC_WARPS * DEC_STAGES);
+    // the CTA takes the blocks [lo, hi) and its warps claim them one at a
+    // time (a shared counter), so that they finish together
+    uint32_t *claimed = sgm + 64;
     if (lane == 0) {
 #pragma unroll
         for (int s = 0; s < DEC_STAGES; ++s) mbar_init(&bars[s], 1);
@@ -141,6 +145,7 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) rvq_decode_kernel(const __g
         }
     }
     if (threadIdx.x < 64) sgm[threadIdx.x] = half2_sign_mask(sign_pair(p.sgn, 2 * threadIdx.x));
+    if (threadIdx.x == 0) *claimed = 0u;
     __syncthreads();
     __syncwarp();
     const uint64_t pol = l2_policy_evict_first();
@@ -148,8 +153,13 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) rvq_decode_kernel(const __g
     // i1 | i2 << BITS, replicated every 2^(2 BITS) lanes; b <= 2 only)
     const float tab = BITS == 4 ? 0.0f : p.c1[lane & (L - 1)] + p.c2[(lane >> BITS) & (L - 1)];
     const int nblk = (p.N + DROWS - 1) / DROWS;
-    const int gw = blockIdx.x * DEC_WARPS + warp;
-    const int tw = gridDim.x * DEC_WARPS;
+    const int lo = (int)((long long)blockIdx.x * nblk / gridDim.x);
+    const int hi = (int)((long long)(blockIdx.x + 1) * nblk / gridDim.x);
+    auto claim = [&]() {
+        int b = 0;
+        if (lane == 0) b = lo + (int)atomicAdd(claimed, 1u);
+        return __shfl_sync(FULL_MASK, b, 0);
+    };
     const float2 neg1 = make_float2(-1.0f, -1.0f);
     const float2 sgn = hh ? neg1 : make_float2(1.0f, 1.0f);
 
@@ -170,25 +180,30 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) rvq_decode_kernel(const __g
             }
         }
     };
-#pragma unroll
-    for (int s = 0; s < DEC_STAGES; ++s) {
-        const int blk = gw + s * tw;
-        if (blk < nblk) issue(blk, s);
-    }
+    // sb[s]: the block staged in stage s (claims are increasing and consumed
+    // in claim order), held as three scalars
+    static_assert(DEC_STAGES == 3, "three stages per warp");
+    int sb0 = claim();
+    if (sb0 < hi) issue(sb0, 0);
+    int sb1 = claim();
+    if (sb1 < hi) issue(sb1, 1);
+    int sb2 = claim();
+    if (sb2 < hi) issue(sb2, 2);
     for (int it = 0;; ++it) {
-        const int blk = gw + it * tw;
-        if (blk >= nblk) break;
         const int s = it % DEC_STAGES;
+        const int blk = s == 0 ? sb0 : (s == 1 ? sb1 : sb2);
+        if (blk >= hi) break;
         const int row = blk * DROWS + rr;
         const bool valid = row < p.N;
         const float n = valid ? __ldg(p.norms + row) : 0.0f;
         const bool ok = mbar_wait_bounded(&bars[s], (uint32_t)(it / DEC_STAGES) & 1u);
         if (!__all_sync(FULL_MASK, ok)) {
             if (lane == 0) atomicOr(&g_rvq_err, (unsigned)VQ_DEVERR_WAIT_TIMEOUT);
+            // the other stages' copies, if any, are still in flight
             for (int k = 1; k < DEC_STAGES; ++k) {
-                const int it2 = it + k;
-                if (gw + it2 * tw < nblk)
-                    (void)mbar_wait_bounded(&bars[it2 % DEC_STAGES], (uint32_t)(it2 / DEC_STAGES) & 1u);
+                const int it2 = it + k, s2 = it2 % DEC_STAGES;
+                if ((s2 == 0 ? sb0 : (s2 == 1 ? sb1 : sb2)) < hi)
+                    (void)mbar_wait_bounded(&bars[s2], (uint32_t)(it2 / DEC_STAGES) & 1u);
             }
             return;
         }
@@ -223,8 +238,14 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) rvq_decode_kernel(const __g
         __syncwarp();
         fence_proxy_async_smem();
         {
-            const int nb = blk + DEC_STAGES * tw;
-            if (nb < nblk) issue(nb, s);
+            const int nb = claim();
+            if (s == 0)
+                sb0 = nb;
+            else if (s == 1)
+                sb1 = nb;
+            else
+                sb2 = nb;
+            if (nb < hi) issue(nb, s);
         }
         float2 v[32];
         dec_lookup<BITS>(w1, w2, tab, stab + lane, v);
