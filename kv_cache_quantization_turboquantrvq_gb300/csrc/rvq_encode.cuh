@@ -1078,10 +1078,7 @@ constexpr int TE_FIX = 2;                     // fixup warps
 constexpr int TE_FIX0 = 2 + 4 * TE_G;         // first fixup warp
 constexpr int TE_THREADS = 32 * (TE_FIX0 + TE_FIX);
 constexpr int TE_FQ = 1024;                   // flagged-row list entries per CTA
-// List entries allowed to wait for a fixup warp: the symmetric b = 2 books flag
-// ~0.3 % of rows, which two fixup warps absorb; the b = 4 books flag ~2 %, more
-// than they keep up with, so the epilogue takes the excess at once.
-__host__ __device__ constexpr int te_fq_backlog(int mode) { return mode == MODE_PAIR ? 2 : TE_FQ; }
+
 constexpr int TE_HALF = TE_M * 128;           // a 64-coordinate half of a tile (16 KB)
 constexpr int TE_TILE = 2 * TE_HALF;          // 32 KB
 constexpr int TE_BOP = 2 * 128 * 128;         // B = H128 diag(s), fp16, 32 KB
@@ -1130,6 +1127,17 @@ __device__ __forceinline__ void rvq_encode_tm_body(const RvqEncodeParams &p, int
         *fq_done = 0u;
         fence_mbar_init();
     }
+    __syncthreads();
+    // the producer's first tiles go out now, under the rest of the set-up
+    const uint64_t pol = l2_policy_evict_first();
+    auto load_tile = [&](int t, int s) {
+        unsigned char *dst = ring + s * TE_TILE;
+        mbar_arrive_expect_tx(&x_full[s], (uint32_t)TE_TILE);
+        tma_load_2d(dst, &p.tmap, 0, t * TE_M, &x_full[s], pol);
+        tma_load_2d(dst + TE_HALF, &p.tmap, 64, t * TE_M, &x_full[s], pol);
+    };
+    if (threadIdx.x == 0)
+        for (int s = 0; s < NST && cta + s * ncta < ntiles; ++s) load_tile(cta + s * ncta, s);
     for (int i = threadIdx.x; i < TE_FQ; i += blockDim.x) fq[i] = 0u;
     // B[n][k] = H128[j(n)][k] s_k, fp16, K-major with the 128-byte swizzle:
     // 16-byte chunk c (k = 8c .. 8c + 7) of row n.  Row n of B is column n of
@@ -1161,23 +1169,60 @@ __device__ __forceinline__ void rvq_encode_tm_body(const RvqEncodeParams &p, int
     qt_fence_after();
     const uint32_t tmem = *tslot;
 
+    // Exact recomputes from the flagged-row list: the calling warp claims the
+    // next entry until the list ends (every epilogue warp done and no entry
+    // left).  The fixup warps run this from the start, the epilogue warps
+    // once their tiles are done (so that a list still full at the end drains
+    // on all of them).
+    auto drain = [&](const FixBooks &fb) {
+        for (;;) {
+            uint32_t k = 0u;
+            if (lane == 0) k = atomicAdd(fq_take, 1u);
+            k = __shfl_sync(FULL_MASK, k, 0);
+            if (k >= (uint32_t)TE_FQ) break;
+            // wait for entry k, or for every epilogue warp to finish with fewer entries
+            uint32_t e = 0u;
+            bool ok = true;
+            const uint64_t t0 = globaltimer_ns();
+            for (;;) {
+                e = fq[k];
+                if (e != 0u) break;
+                if (*reinterpret_cast<volatile uint32_t *>(fq_done) == 4u * TE_G) {
+                    __threadfence_block();
+                    e = fq[k];
+                    if (e != 0u || *reinterpret_cast<volatile uint32_t *>(fq_n) <= k) break;
+                }
+                if (globaltimer_ns() - t0 > MBAR_TIMEOUT_NS) {
+                    ok = false;
+                    break;
+                }
+                __nanosleep(256);
+            }
+            e = __shfl_sync(FULL_MASK, e, 0);
+            if (!__all_sync(FULL_MASK, ok)) {
+                if (lane == 0) atomicOr(&VQ_RVQ_ERR, (unsigned)VQ_DEVERR_WAIT_TIMEOUT);
+                break;
+            }
+            if (e == 0u) break;  // the list ended before entry k
+            __threadfence_block();
+            fixup_one<MODE>(p, (int)(e - 1u), lane, fb);
+        }
+    };
+
     if (warp == 0) {
-        // ---- producer
+        // ---- producer (tiles 0 .. NST - 1 went out during the set-up)
         if (lane == 0) {
-            const uint64_t pol = l2_policy_evict_first();
             int i = 0;
             for (int t = cta; t < ntiles; t += ncta, ++i) {
+                if (i < NST) continue;
                 const int s = i % NST;
-                if (i >= NST && !mbar_wait_bounded(&x_empty[s], (uint32_t)((i / NST) - 1) & 1u)) {
+                if (!mbar_wait_bounded(&x_empty[s], (uint32_t)((i / NST) - 1) & 1u)) {
                     atomicOr(&VQ_RVQ_ERR, (unsigned)VQ_DEVERR_WAIT_TIMEOUT);
                     *abort_flag = 1u;
                     break;
                 }
                 if (*abort_flag) break;
-                unsigned char *dst = ring + s * TE_TILE;
-                mbar_arrive_expect_tx(&x_full[s], (uint32_t)TE_TILE);
-                tma_load_2d(dst, &p.tmap, 0, t * TE_M, &x_full[s], pol);
-                tma_load_2d(dst + TE_HALF, &p.tmap, 64, t * TE_M, &x_full[s], pol);
+                load_tile(t, s);
             }
             for (int k = 0; k < NST && k < i; ++k) {
                 const int j = i - 1 - k;
@@ -1354,23 +1399,22 @@ __device__ __forceinline__ void rvq_encode_tm_body(const RvqEncodeParams &p, int
 
             flag = flag && okrow;
             if (okrow && !flag) p.norms[drow] = n;
-            // rows inside the guard band go to the fixup warps (this thread's
-            // fast words ordered before their exact ones by the fence and the
-            // list entry) while they keep up (at most te_fq_backlog entries
-            // waiting) and the list has room; else the warp recomputes them here
+            // rows inside the guard band go to the list (this thread's fast
+            // words ordered before their exact ones by the fence and the list
+            // entry) while it has room; else the warp recomputes them here.
+            // The b = 4 books flag ~2 % of rows, more than the two fixup
+            // warps keep up with: the rest wait for the epilogue warps, which
+            // drain the list with them once their tiles are done (measured:
+            // better than recomputing the excess in the epilogue at once,
+            // which held the MMA pipeline)
             bool here = false;
             if (flag) {
-                const int pend = (int)(*reinterpret_cast<volatile uint32_t *>(fq_n) -
-                                       *reinterpret_cast<volatile uint32_t *>(fq_take));
-                here = pend >= te_fq_backlog(MODE);
-                if (!here) {
-                    __threadfence_block();
-                    const uint32_t k = atomicAdd(fq_n, 1u);
-                    if (k < (uint32_t)TE_FQ)
-                        fq[k] = (uint32_t)row + 1u;
-                    else
-                        here = true;
-                }
+                __threadfence_block();
+                const uint32_t k = atomicAdd(fq_n, 1u);
+                if (k < (uint32_t)TE_FQ)
+                    fq[k] = (uint32_t)row + 1u;
+                else
+                    here = true;
             }
             __syncwarp();  // the fast words of a flagged row are written before its exact ones
             unsigned fl = __ballot_sync(FULL_MASK, here);
@@ -1386,41 +1430,10 @@ __device__ __forceinline__ void rvq_encode_tm_body(const RvqEncodeParams &p, int
             __threadfence_block();
             atomicAdd(fq_done, 1u);
         }
+        drain(fb);
     } else {
-        // ---- fixup warps: each claims the next entry of the flagged-row list
-        const FixBooks fb = fix_books<MODE>(p, lane);
-        for (;;) {
-            uint32_t k = 0u;
-            if (lane == 0) k = atomicAdd(fq_take, 1u);
-            k = __shfl_sync(FULL_MASK, k, 0);
-            if (k >= (uint32_t)TE_FQ) break;
-            // wait for entry k, or for every epilogue warp to finish with fewer entries
-            uint32_t e = 0u;
-            bool ok = true;
-            const uint64_t t0 = globaltimer_ns();
-            for (;;) {
-                e = fq[k];
-                if (e != 0u) break;
-                if (*reinterpret_cast<volatile uint32_t *>(fq_done) == 4u * TE_G) {
-                    __threadfence_block();
-                    e = fq[k];
-                    if (e != 0u || *reinterpret_cast<volatile uint32_t *>(fq_n) <= k) break;
-                }
-                if (globaltimer_ns() - t0 > MBAR_TIMEOUT_NS) {
-                    ok = false;
-                    break;
-                }
-                __nanosleep(256);
-            }
-            e = __shfl_sync(FULL_MASK, e, 0);
-            if (!__all_sync(FULL_MASK, ok)) {
-                if (lane == 0) atomicOr(&VQ_RVQ_ERR, (unsigned)VQ_DEVERR_WAIT_TIMEOUT);
-                break;
-            }
-            if (e == 0u) break;  // the list ended before entry k
-            __threadfence_block();
-            fixup_one<MODE>(p, (int)(e - 1u), lane, fb);
-        }
+        // ---- fixup warps
+        drain(fix_books<MODE>(p, lane));
     }
 
     qt_fence_before();
