@@ -407,7 +407,10 @@ __device__ __noinline__ void rvq_fixup_row(const RvqEncodeParams &p, const unsig
     }
     wht_lane_exact(s1, lane);
     wht_lane_exact(s2, lane);
-    wht_lane_exact(s3, lane);
+    // the third piece holds only values 2^22 and more below the row's largest
+    // (almost never): skip its transform when it is zero everywhere
+    if (__any_sync(FULL_MASK, s3[0] != 0.0f || s3[1] != 0.0f || s3[2] != 0.0f || s3[3] != 0.0f))
+        wht_lane_exact(s3, lane);
 
     uint32_t part1 = 0, part2 = 0;
 #pragma unroll
@@ -621,7 +624,12 @@ __device__ __noinline__ void rvq_fixup_tm(const RvqEncodeParams &p, int row, int
     };
     wht(s1);
     wht(s2);
-    wht(s3);
+    {
+        bool nz = false;  // the third piece is almost always zero: skip its transform then
+#pragma unroll
+        for (int j = 0; j < C; ++j) nz = nz || s3[j] != 0.0f;
+        if (__any_sync(FULL_MASK, nz)) wht(s3);
+    }
 
     uint32_t part1 = 0u, part2 = 0u;
 #pragma unroll
@@ -1160,8 +1168,6 @@ __device__ __forceinline__ void rvq_encode_tm_body(const RvqEncodeParams &p, int
         }
         *reinterpret_cast<uint4 *>(bop + (c >> 3) * TE_HALF + swz128(n, c & 7)) = make_uint4(h[0], h[1], h[2], h[3]);
     }
-    if constexpr (MODE == MODE_PAIR)
-        for (int i = threadIdx.x; i < PT_CELLS * P4_REP; i += blockDim.x) ptab[i] = p.pt.ent[i / P4_REP];
     fence_proxy_async_smem();  // B is read by the MMAs (async proxy)
     if (warp == 1) tmem_alloc(tslot, 512);
     qt_fence_before();
@@ -1265,6 +1271,15 @@ __device__ __forceinline__ void rvq_encode_tm_body(const RvqEncodeParams &p, int
         const int r = 32 * q + lane;
         const uint32_t tl = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(g * 128);
         const FixBooks fb = fix_books<MODE>(p, lane);  // exact recompute
+        if constexpr (MODE == MODE_PAIR) {
+            // the replicated pair table, built here by the epilogue warps (the
+            // only ones that read it) while the first tiles load and multiply:
+            // PT_CELLS * P4_REP entries, entry i a copy of cell i / P4_REP.
+            // (Reading the cells with warp-uniform addresses, 32 to a warp, or
+            // one per thread with shuffles to copy them, measured slower.)
+            for (int i = threadIdx.x - 64; i < PT_CELLS * P4_REP; i += 4 * TE_G * 32) ptab[i] = p.pt.ent[i / P4_REP];
+            asm volatile("bar.sync 1, %0;" ::"n"(4 * TE_G * 32) : "memory");
+        }
         [[maybe_unused]] const float b1u = p.b1[2], b2u = p.b2[2];
         [[maybe_unused]] const float bc2u = p.b1[2] - p.c1[2], dcu = p.c1[3] - p.c1[2];
         [[maybe_unused]] const float kb1 = __fdiv_rn(2.0f, b1u), kb2 = __fdiv_rn(2.0f, b2u);
@@ -1409,6 +1424,10 @@ __device__ __forceinline__ void rvq_encode_tm_body(const RvqEncodeParams &p, int
             // which held the MMA pipeline)
             bool here = false;
             if (flag) {
+                // the recompute reads the row again: start bringing it to L1
+                const char *xr = static_cast<const char *>(p.x) + (size_t)row * ROW_BYTES;
+                asm volatile("prefetch.global.L1 [%0];" ::"l"(xr));
+                asm volatile("prefetch.global.L1 [%0];" ::"l"(xr + 128));
                 __threadfence_block();
                 const uint32_t k = atomicAdd(fq_n, 1u);
                 if (k < (uint32_t)TE_FQ)
