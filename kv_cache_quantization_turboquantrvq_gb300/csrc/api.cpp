@@ -282,6 +282,7 @@ static vq_status rvq_encode_impl(const void *k_f16, int B, int H, int S, int D, 
         p.b2[k] = k < L - 1 ? b2[k] : INFINITY;
     }
     const int mode = rvq_quantizer_tables(bits, c1, b1, c2, b2, kGuard, p.t1, p.t2, p.pt);
+    p.pt_dev = mode == RVQ_MODE_PAIR ? pair_table_device(p.pt, reinterpret_cast<cudaStream_t>(stream)) : nullptr;
     set_signs(p, signs);
     return cuda_status(launch_rvq_encode(p, bits, mode, reinterpret_cast<cudaStream_t>(stream)));
 }
@@ -724,6 +725,7 @@ vq_status vq_flush_decode(const void *k_f16, const void *v_f16, int B, int H, in
         if (!aligned(packed1, 16) || !aligned(packed2, 16) || !aligned(norms, 4)) return VQ_ERR_MISALIGNED;
         RvqEncodeParams &p = fp.rvq;
         const int mode = rvq_quantizer_tables(rvq_bits, c1, b1, c2, b2, kGuard, p.t1, p.t2, p.pt);
+        p.pt_dev = mode == RVQ_MODE_PAIR ? pair_table_device(p.pt, reinterpret_cast<cudaStream_t>(stream)) : nullptr;
         // the fused flush carries the encoders of the symmetric 1/2-bit books
         // and of 4-bit books with a pair table (the library's books)
         if (!((rvq_bits <= 2 && mode == RVQ_MODE_SYM) || (rvq_bits == 4 && mode == RVQ_MODE_PAIR)))

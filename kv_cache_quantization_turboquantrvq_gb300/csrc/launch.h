@@ -82,7 +82,15 @@ struct RvqEncodeParams {
     uint32_t sgn[4];  // randomised-sign rotation H diag(s): bit j negates coordinate j
     int has_sgn;
     PairTable pt;  // RVQ_MODE_PAIR only
+    const uint2 *pt_dev;  // RVQ_MODE_PAIR: the same cells in device memory, or null (read pt)
 };
+
+// The pair table's cells in device memory (static slots, one per distinct
+// table, never reused; uploaded on `stream` at first use): the kernels read
+// them there instead of from the kernel parameters (which are slow to read
+// at per-thread addresses).  Null when every slot is taken, or when the table
+// is new and `stream` is being captured (the kernel then reads pt itself).
+const uint2 *pair_table_device(const PairTable &pt, cudaStream_t stream);
 
 struct RvqDecodeParams {
     CUtensorMap tm1, tm2;  // b >= 2: the packed words as [N rows, W] uint32, 16-row boxes,

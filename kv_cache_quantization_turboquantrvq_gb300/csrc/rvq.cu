@@ -9,6 +9,9 @@
 #include "device_common.cuh"
 #include "launch.h"
 
+#include <cstring>
+#include <mutex>
+
 namespace vq {
 VQ_DEFINE_ERROR_WORD(g_rvq_err);
 }  // namespace vq
@@ -425,6 +428,71 @@ cudaError_t rvq_take_device_error(unsigned *bits, cudaStream_t stream)
                                            cudaMemcpyHostToDevice, stream);
     if (e != cudaSuccess) return e;
     return cudaStreamSynchronize(stream);
+}
+
+// ------------------------------------------------ pair tables in device memory
+
+namespace {
+constexpr int kPtSlots = 16;
+constexpr int kPtDevices = 8;
+__device__ uint2 g_pt_slots[kPtSlots][PT_CELLS];
+struct PtSlot {
+    bool used = false;
+    bool done = false;  // the upload is known to be complete
+    uint2 ent[PT_CELLS];
+    cudaEvent_t uploaded = nullptr;
+};
+std::mutex g_pt_mu;
+PtSlot g_pt[kPtDevices][kPtSlots];
+}  // namespace
+
+const uint2 *pair_table_device(const PairTable &pt, cudaStream_t stream)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kPtDevices) return nullptr;
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) return nullptr;
+    const bool capturing = cap != cudaStreamCaptureStatusNone;
+    void *base = nullptr;
+    if (cudaGetSymbolAddress(&base, g_pt_slots) != cudaSuccess) return nullptr;
+    std::lock_guard<std::mutex> lock(g_pt_mu);
+    for (int i = 0; i < kPtSlots; ++i) {
+        PtSlot &sl = g_pt[dev][i];
+        if (!sl.used || std::memcmp(sl.ent, pt.ent, sizeof(sl.ent)) != 0) continue;
+        if (!sl.done) {
+            // during a capture no event may be queried or waited on: use the
+            // slot only once its upload is known to be complete
+            if (capturing) return nullptr;
+            const cudaError_t q = cudaEventQuery(sl.uploaded);
+            if (q == cudaSuccess) {
+                sl.done = true;
+            } else if (q == cudaErrorNotReady) {
+                // uploaded on another stream and not yet done: order this one after it
+                if (cudaStreamWaitEvent(stream, sl.uploaded, 0) != cudaSuccess) return nullptr;
+            } else {
+                return nullptr;
+            }
+        }
+        return static_cast<const uint2 *>(base) + (size_t)i * PT_CELLS;
+    }
+    if (capturing) return nullptr;  // no upload inside a capture
+    for (int i = 0; i < kPtSlots; ++i) {
+        PtSlot &sl = g_pt[dev][i];
+        if (sl.used) continue;
+        std::memcpy(sl.ent, pt.ent, sizeof(sl.ent));
+        if (sl.uploaded == nullptr && cudaEventCreateWithFlags(&sl.uploaded, cudaEventDisableTiming) != cudaSuccess) {
+            sl.uploaded = nullptr;
+            return nullptr;
+        }
+        if (cudaMemcpyToSymbolAsync(g_pt_slots, sl.ent, sizeof(sl.ent), (size_t)i * sizeof(sl.ent),
+                                    cudaMemcpyHostToDevice, stream) != cudaSuccess ||
+            cudaEventRecord(sl.uploaded, stream) != cudaSuccess)
+            return nullptr;
+        sl.used = true;
+        sl.done = false;
+        return static_cast<const uint2 *>(base) + (size_t)i * PT_CELLS;
+    }
+    return nullptr;  // every slot taken
 }
 
 }  // namespace vq

@@ -1120,6 +1120,25 @@ __device__ __forceinline__ void rvq_encode_tm_body(const RvqEncodeParams &p, int
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int ntiles = (p.N + TE_M - 1) / TE_M;
 
+    // The b = 4 pair table, replicated P4_REP times (entry i a copy of cell
+    // i / P4_REP): its cells are read first thing, before the tile loads
+    // crowd the memory system, from device memory when the host placed them
+    // there (else from the kernel parameters, slower at per-thread
+    // addresses), all of a thread's reads before its stores; the stores
+    // follow the first barrier and the set-up's last barrier covers them.
+    constexpr int NPT = MODE == MODE_PAIR ? (PT_CELLS * P4_REP + TE_THREADS - 1) / TE_THREADS : 1;
+    [[maybe_unused]] uint2 cell[NPT];
+    if constexpr (MODE == MODE_PAIR) {
+        static_assert((PT_CELLS * P4_REP) % TE_THREADS == 0, "whole rounds of the table copy");
+        if (p.pt_dev != nullptr) {
+#pragma unroll
+            for (int k = 0; k < NPT; ++k) cell[k] = __ldg(p.pt_dev + (threadIdx.x + k * TE_THREADS) / P4_REP);
+        } else {
+#pragma unroll
+            for (int k = 0; k < NPT; ++k) cell[k] = p.pt.ent[(threadIdx.x + k * TE_THREADS) / P4_REP];
+        }
+    }
+
     if (threadIdx.x == 0) {
         for (int s = 0; s < NST; ++s) {
             mbar_init(&x_full[s], 1);
@@ -1146,6 +1165,10 @@ __device__ __forceinline__ void rvq_encode_tm_body(const RvqEncodeParams &p, int
     };
     if (threadIdx.x == 0)
         for (int s = 0; s < NST && cta + s * ncta < ntiles; ++s) load_tile(cta + s * ncta, s);
+    if constexpr (MODE == MODE_PAIR) {
+#pragma unroll
+        for (int k = 0; k < NPT; ++k) ptab[threadIdx.x + k * TE_THREADS] = cell[k];
+    }
     for (int i = threadIdx.x; i < TE_FQ; i += blockDim.x) fq[i] = 0u;
     // B[n][k] = H128[j(n)][k] s_k, fp16, K-major with the 128-byte swizzle:
     // 16-byte chunk c (k = 8c .. 8c + 7) of row n.  Row n of B is column n of
@@ -1271,15 +1294,6 @@ __device__ __forceinline__ void rvq_encode_tm_body(const RvqEncodeParams &p, int
         const int r = 32 * q + lane;
         const uint32_t tl = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(g * 128);
         const FixBooks fb = fix_books<MODE>(p, lane);  // exact recompute
-        if constexpr (MODE == MODE_PAIR) {
-            // the replicated pair table, built here by the epilogue warps (the
-            // only ones that read it) while the first tiles load and multiply:
-            // PT_CELLS * P4_REP entries, entry i a copy of cell i / P4_REP.
-            // (Reading the cells with warp-uniform addresses, 32 to a warp, or
-            // one per thread with shuffles to copy them, measured slower.)
-            for (int i = threadIdx.x - 64; i < PT_CELLS * P4_REP; i += 4 * TE_G * 32) ptab[i] = p.pt.ent[i / P4_REP];
-            asm volatile("bar.sync 1, %0;" ::"n"(4 * TE_G * 32) : "memory");
-        }
         [[maybe_unused]] const float b1u = p.b1[2], b2u = p.b2[2];
         [[maybe_unused]] const float bc2u = p.b1[2] - p.c1[2], dcu = p.c1[3] - p.c1[2];
         [[maybe_unused]] const float kb1 = __fdiv_rn(2.0f, b1u), kb2 = __fdiv_rn(2.0f, b2u);
