@@ -25,7 +25,14 @@
  *    tensors are IEEE binary16 ("void*" in the signatures), row-major and
  *    contiguous.  Codebook arrays are HOST pointers read during the call.
  *  - The caller owns and allocates every buffer.  The library allocates no
- *    memory, keeps no per-call state and never synchronizes the stream.
+ *    memory at call time and never synchronizes with the host.  It keeps
+ *    library-wide caches: the quantizer tables of the last four codebooks
+ *    (host memory) and, for 16-level books quantized by a pair table (the
+ *    library's b = 4 books), that 4 KB table in one of 16 static device slots
+ *    per device, uploaded on `stream` by the first call that uses it (a later
+ *    call on another stream waits for that upload on the device, if it has
+ *    not finished); a call made while `stream` is being captured never
+ *    uploads (its kernel then reads the table from its own parameters).
  *  - Work is enqueued on `stream` (NULL = the legacy default stream).
  *  - Arguments are validated on the host before anything is enqueued; a
  *    non-VQ_OK status means nothing was enqueued, except VQ_ERR_CUDA, which
