@@ -34,10 +34,9 @@
 //    band of a boundary; such rows are redone by the whole warp in exact /
 //    double-float arithmetic (rvq_fixup_row), so the packed words equal those
 //    of exact arithmetic.
-// The library's books have encoders of their own, with the same rings and
-// exact recompute, the rotation on the tensor cores and four lanes per row:
-// rvq_encode_sym2_kernel for symmetric 4-level books (b = 2) and
-// rvq_encode_pair4_kernel for 16-level books with a pair table (b = 4).
+// The library's books (symmetric 4-level books, b = 2, and 16-level books
+// with a pair table, b = 4) have an encoder of their own with the rotation on
+// the 5th-generation tensor cores: rvq_encode_tm_body, further below.
 //
 // The including translation unit defines VQ_RVQ_ERR, the device error word
 // the bodies report into (VQ_DEVERR_* bits).
@@ -694,8 +693,8 @@ __device__ __forceinline__ void rvq_encode_body(const RvqEncodeParams &p, int ct
     constexpr int WARPS = enc_warps(BITS, MODE);
     constexpr bool ROLLED = MODE == MODE_GRID || MODE == MODE_PLAIN;
     constexpr int PP = enc_pairs(BITS);
-    static_assert(!(MODE == MODE_SYM && BITS == 2), "symmetric b = 2 books: rvq_encode_sym2_kernel");
-    static_assert(MODE != MODE_PAIR, "the b = 4 pair table: rvq_encode_pair4_kernel");
+    static_assert(!(MODE == MODE_SYM && BITS == 2), "symmetric b = 2 books: rvq_encode_tm_body");
+    static_assert(MODE != MODE_PAIR, "the b = 4 pair table: rvq_encode_tm_body");
     extern __shared__ __align__(128) unsigned char smem_raw[];
     unsigned char *stab = smem_1k(smem_raw);       // cell tables (GRID)
     uint4 *ssg = reinterpret_cast<uint4 *>(stab + enc_tab_bytes(MODE));  // sign masks
