@@ -353,6 +353,173 @@ cudaError_t launch_enc_pair4(const RvqEncodeParams &p, cudaStream_t stream)
     return launch_enc_tm<MODE_PAIR>(p, stream);
 }
 
+// Decode, b = 2, a thread per row: the same table decode and fp32 butterflies
+// as rvq_decode_kernel, but a lane holds all 128 coordinates of its row, so
+// the last Hadamard stage is two register adds instead of a partner
+// exchange (about 7 instructions per element against 10.4).  32-row blocks
+// (one row per lane) arrive as 2D TMA boxes of both streams (32-byte swizzle)
+// into a 2-stage ring per warp; the fp16 rows are staged in shared memory
+// (16-byte chunks swizzled by row) and written out as whole contiguous
+// blocks.  12 warps per SM (about 150 registers a thread).
+constexpr int DR_WARPS = 12;
+constexpr int DR_ROWS = 32;
+constexpr int DR_NST = 2;
+constexpr int DR_W = 8;                                 // words per row and stream (b = 2)
+constexpr int DR_STAGE = 2 * DR_ROWS * DR_W * 4;        // both streams: 2 KB
+constexpr int DR_OUT = DR_ROWS * 256;                   // fp16 rows of a block: 8 KB
+__host__ __device__ constexpr int dr_smem()
+{
+    return 1024 + DR_WARPS * (DR_NST * DR_STAGE + DR_OUT) + DR_WARPS * DR_NST * 8 + 256 + 16;
+}
+
+template <bool SGN>
+__global__ void __launch_bounds__(DR_WARPS * 32, 1) rvq_decode_row_kernel(const __grid_constant__ RvqDecodeParams p)
+{
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    unsigned char *smem = smem_1k(smem_raw);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    unsigned char *wbuf = smem + warp * (DR_NST * DR_STAGE);
+    unsigned char *obuf = smem + DR_WARPS * DR_NST * DR_STAGE + warp * DR_OUT;
+    uint64_t *bars_all = reinterpret_cast<uint64_t *>(smem + DR_WARPS * (DR_NST * DR_STAGE + DR_OUT));
+    uint64_t *bars = bars_all + warp * DR_NST;
+    // sign masks: word k flips output coordinates 2k, 2k + 1
+    uint32_t *sgm = reinterpret_cast<uint32_t *>(bars_all + DR_WARPS * DR_NST);
+    uint32_t *claimed = sgm + 64;
+    if (lane == 0) {
+#pragma unroll
+        for (int s = 0; s < DR_NST; ++s) mbar_init(&bars[s], 1);
+        fence_mbar_init();
+    }
+    if (threadIdx.x < 64) sgm[threadIdx.x] = half2_sign_mask(sign_pair(p.sgn, 2 * threadIdx.x));
+    if (threadIdx.x == 0) *claimed = 0u;
+    __syncthreads();
+    const uint64_t pol = l2_policy_evict_first();
+    const float tab = p.c1[lane & 3] + p.c2[(lane >> 2) & 3];  // merged table, index i1 | i2 << 2
+    const int nblk = (p.N + DR_ROWS - 1) / DR_ROWS;
+    const int lo = (int)((long long)blockIdx.x * nblk / gridDim.x);
+    const int hi = (int)((long long)(blockIdx.x + 1) * nblk / gridDim.x);
+    auto claim = [&]() {
+        int b = 0;
+        if (lane == 0) b = lo + (int)atomicAdd(claimed, 1u);
+        return __shfl_sync(FULL_MASK, b, 0);
+    };
+    auto issue = [&](int blk, int s) {
+        if (lane == 0) {
+            mbar_arrive_expect_tx(&bars[s], (uint32_t)DR_STAGE);
+            tma_load_2d(wbuf + s * DR_STAGE, &p.tm1, 0, blk * DR_ROWS, &bars[s], pol);
+            tma_load_2d(wbuf + s * DR_STAGE + DR_STAGE / 2, &p.tm2, 0, blk * DR_ROWS, &bars[s], pol);
+        }
+    };
+    static_assert(DR_NST == 2, "two stages per warp");
+    int sb0 = claim();
+    if (sb0 < hi) issue(sb0, 0);
+    int sb1 = claim();
+    if (sb1 < hi) issue(sb1, 1);
+    const float2 neg1 = make_float2(-1.0f, -1.0f);
+    for (int it = 0;; ++it) {
+        const int s = it & 1;
+        const int blk = s ? sb1 : sb0;
+        if (blk >= hi) break;
+        const int row = blk * DR_ROWS + lane;
+        const bool valid = row < p.N;
+        const float n = valid ? __ldg(p.norms + row) : 0.0f;
+        const bool ok = mbar_wait_bounded(&bars[s], (uint32_t)(it >> 1) & 1u);
+        if (!__all_sync(FULL_MASK, ok)) {
+            if (lane == 0) atomicOr(&g_rvq_err, (unsigned)VQ_DEVERR_WAIT_TIMEOUT);
+            const int it2 = it + 1;  // the other stage's copy, if any, is still in flight
+            if ((s ? sb0 : sb1) < hi) (void)mbar_wait_bounded(&bars[it2 & 1], (uint32_t)(it2 >> 1) & 1u);
+            return;
+        }
+        // the row's words (32-byte rows, 32-byte swizzle: chunk k at k ^ ((lane >> 2) & 1))
+        uint32_t w1[DR_W], w2[DR_W];
+        {
+            const unsigned char *ra = wbuf + s * DR_STAGE + lane * (DR_W * 4);
+            const unsigned char *rb = ra + DR_STAGE / 2;
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                const int pk = k ^ ((lane >> 2) & 1);
+                const uint4 a = *reinterpret_cast<const uint4 *>(ra + (pk << 4));
+                const uint4 b = *reinterpret_cast<const uint4 *>(rb + (pk << 4));
+                w1[4 * k] = a.x; w1[4 * k + 1] = a.y; w1[4 * k + 2] = a.z; w1[4 * k + 3] = a.w;
+                w2[4 * k] = b.x; w2[4 * k + 1] = b.y; w2[4 * k + 2] = b.z; w2[4 * k + 3] = b.w;
+            }
+        }
+        __syncwarp();
+        fence_proxy_async_smem();
+        {
+            const int nb = claim();
+            if (s)
+                sb1 = nb;
+            else
+                sb0 = nb;
+            if (nb < hi) issue(nb, s);
+        }
+        // y_hat of the two halves, H64 on each (coordinate bits 1-5 across the
+        // array, bit 0 in the pair), then bit 6 across the halves
+        float2 v0[32], v1[32];
+        {
+            uint32_t a[4], b[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) { a[k] = w1[k]; b[k] = w2[k]; }
+            dec_lookup<2>(a, b, tab, nullptr, v0);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) { a[k] = w1[4 + k]; b[k] = w2[4 + k]; }
+            dec_lookup<2>(a, b, tab, nullptr, v1);
+        }
+#pragma unroll
+        for (int h = 1; h < 32; h <<= 1) {
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+                if ((k & h) == 0) {
+                    const float2 a0 = v0[k], b0 = v0[k + h];
+                    v0[k] = __fadd2_rn(a0, b0);
+                    v0[k + h] = __ffma2_rn(b0, neg1, a0);
+                    const float2 a1 = v1[k], b1 = v1[k + h];
+                    v1[k] = __fadd2_rn(a1, b1);
+                    v1[k + h] = __ffma2_rn(b1, neg1, a1);
+                }
+            }
+        }
+        // bit 6, bit 0, the scale n / sqrt(D), fp16, signs; staged by row
+        const float sc = __fdiv_rn(n, SQRT_D_HI);
+        const float2 sc2 = make_float2(sc, sc);
+        unsigned char *orow = obuf + lane * 256;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            uint32_t o0[4], o1[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int k = 4 * c + e;
+                const float2 a = v0[k], b = v1[k];
+                const float2 u = __fadd2_rn(a, b), w = __ffma2_rn(b, neg1, a);  // coordinates 2k, 2k+1 | 64 + 2k, 64 + 2k + 1 before bit 0
+                const float2 xu = __fmul2_rn(make_float2(u.x + u.y, u.x - u.y), sc2);
+                const float2 xw = __fmul2_rn(make_float2(w.x + w.y, w.x - w.y), sc2);
+                const __half2 hu = __floats2half2_rn(xu.x, xu.y), hw = __floats2half2_rn(xw.x, xw.y);
+                o0[e] = *reinterpret_cast<const uint32_t *>(&hu);
+                o1[e] = *reinterpret_cast<const uint32_t *>(&hw);
+                if constexpr (SGN) {
+                    o0[e] ^= sgm[k];
+                    o1[e] ^= sgm[32 + k];
+                }
+            }
+            // 16-byte chunk c (coordinates 8c .. 8c + 7) and chunk 8 + c, swizzled by row
+            *reinterpret_cast<uint4 *>(orow + ((c ^ (lane & 15)) << 4)) = make_uint4(o0[0], o0[1], o0[2], o0[3]);
+            *reinterpret_cast<uint4 *>(orow + (((8 + c) ^ (lane & 15)) << 4)) = make_uint4(o1[0], o1[1], o1[2], o1[3]);
+        }
+        __syncwarp();
+        // coalesced write-out: 16-byte chunk idx = i * 32 + lane is chunk idx % 16 of row idx / 16
+        const int nrows = min(DR_ROWS, p.N - blk * DR_ROWS);
+        uint4 *gout = reinterpret_cast<uint4 *>(static_cast<__half *>(p.out) + (size_t)blk * DR_ROWS * D);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int idx = i * 32 + lane;
+            const int r = idx >> 4, c = idx & 15;
+            if (r < nrows) gout[idx] = *reinterpret_cast<const uint4 *>(obuf + r * 256 + ((c ^ (r & 15)) << 4));
+        }
+        __syncwarp();
+    }
+}
+
 template <int BITS>
 cudaError_t launch_dec(const RvqDecodeParams &p0, cudaStream_t stream)
 {
@@ -405,12 +572,33 @@ cudaError_t launch_rvq_encode(const RvqEncodeParams &p, int bits, int mode, cuda
     }
 }
 
+namespace {
+cudaError_t launch_dec_row(const RvqDecodeParams &p0, cudaStream_t stream)
+{
+    RvqDecodeParams p = p0;
+    if (!encode_tmap_words(&p.tm1, p.p1, (uint64_t)p.N, DR_W, DR_ROWS, DR_W * 4) ||
+        !encode_tmap_words(&p.tm2, p.p2, (uint64_t)p.N, DR_W, DR_ROWS, DR_W * 4))
+        return cudaErrorInvalidValue;
+    auto kern = p.has_sgn ? rvq_decode_row_kernel<true> : rvq_decode_row_kernel<false>;
+    constexpr int smem = dr_smem();
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    const int nblk = (p.N + DR_ROWS - 1) / DR_ROWS;
+    int grid = (nblk + DR_WARPS - 1) / DR_WARPS;
+    const int sms = sm_count();
+    if (grid > sms) grid = sms;
+    if (grid < 1) grid = 1;
+    kern<<<grid, DR_WARPS * 32, smem, stream>>>(p);
+    return cudaGetLastError();
+}
+}  // namespace
+
 cudaError_t launch_rvq_decode(const RvqDecodeParams &p, int bits, cudaStream_t stream)
 {
     if (p.N <= 0) return cudaSuccess;
     switch (bits) {
     case 1: return launch_dec<1>(p, stream);
-    case 2: return launch_dec<2>(p, stream);
+    case 2: return launch_dec_row(p, stream);
     case 4: return launch_dec<4>(p, stream);
     default: return cudaErrorInvalidValue;
     }
