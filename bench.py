@@ -184,7 +184,7 @@ def build_workload(name, dev, rank=0, layers=None, batch=None, chunked=False, ch
         ekern = "rvq_encode_tc_kernel" if bits in (2, 4) else "rvq_encode_kernel"
         ops.append(Op(tag + "rvq_encode", ekern, enc, rvq_bytes(rows, bits), rows * D))
         if dec is not None:
-            dkern = "rvq_decode_row_kernel" if bits == 2 else "rvq_decode_kernel"
+            dkern = "rvq_decode_row_kernel" if bits in (2, 4) else "rvq_decode_kernel"
             ops.append(Op(tag + "rvq_decode", dkern, dec, rvq_bytes(rows, bits), rows * D))
         results.extend([p1, p2, nr])
         if dec is not None:

@@ -42,32 +42,31 @@ __global__ void __launch_bounds__(TE_THREADS, 1) rvq_encode_tc_kernel(const __gr
 
 // ---------------------------------------------------------------- decode
 //
-// x_hat = n * H (c1[i1] + c2[i2]) / sqrt(D), two threads per row: lane l
-// works on row l & 15 of a 16-row block and on the coordinates
-// [64h, 64h + 64), h = l >> 4.  With H = [[H64, H64], [H64, -H64]], thread h
-// transforms its own half, A_h = H64 u_h, scales it, swaps it with its
-// partner (lane l ^ 16) and keeps A_0 + A_1 (h = 0) or A_0 - A_1 (h = 1): the
-// coordinates it outputs.  The packed words of a 16-row block (contiguous in
-// both streams) arrive by two bulk copies into a 3-stage ring.  For b <= 2
-// the two codes of a coordinate index one merged table c1[i1] + c2[i2] (16 or
-// 4 fp32 entries held one per lane and replicated across the warp, read by
-// shuffle): the words of both streams are first interleaved so that a plain
-// shift leaves the merged index in the low bits.  For b = 4 each stage has its
-// own 16-entry table.  The fp16 half rows are staged in shared memory and
-// written out coalesced.
+// x_hat = n * H (c1[i1] + c2[i2]) / sqrt(D).  Two kernels share the table
+// decode below: rvq_decode_row_kernel (b = 2, 4: a thread per row) and
+// rvq_decode_kernel (b = 1: two threads per row, whose 16-byte rows are too
+// narrow for the row kernel's 16-byte chunks per half row).
+//
+// rvq_decode_kernel: lane l works on row l & 15 of a 16-row block and on the
+// coordinates [64h, 64h + 64), h = l >> 4.  With H = [[H64, H64], [H64,
+// -H64]], thread h transforms its own half, A_h = H64 u_h, scales it, swaps
+// it with its partner (lane l ^ 16) and keeps A_0 + A_1 (h = 0) or A_0 - A_1
+// (h = 1): the coordinates it outputs.  The packed words of a 16-row block
+// (contiguous in both streams) arrive by two bulk copies into a 3-stage ring.
+// The fp16 half rows are staged in shared memory and written out coalesced.
 constexpr int DEC_STAGES = 3;
 constexpr int DEC_WARPS = 16;
 constexpr int DROWS = 16;
 __host__ __device__ constexpr int dec_stage(int bits) { return 2 * DROWS * (D * bits / 32) * 4; }
 __host__ __device__ constexpr int dec_warp_bytes(int bits) { return DEC_STAGES * dec_stage(bits) + DROWS * ROW_STRIDE; }
+// b = 4: the merged 256-entry table, replicated per lane (row kernel)
 __host__ __device__ constexpr int dec_table_bytes(int bits) { return bits == 4 ? 256 * 32 * 4 : 0; }
 __host__ __device__ constexpr int dec_smem(int bits)
 {
-    // 1024-byte alignment of the (swizzled) stages, the b = 4 table, every
-    // warp's stages, every warp's output staging, the mbarriers, the sign
-    // masks of the randomised rotation (64 pair words) and the CTA's block
-    // counter
-    return 1024 + dec_table_bytes(bits) + DEC_WARPS * dec_warp_bytes(bits) + DEC_WARPS * DEC_STAGES * 8 + 256 + 16;
+    // 1024-byte alignment, every warp's stages, every warp's output staging,
+    // the mbarriers, the sign masks of the randomised rotation (64 pair
+    // words) and the CTA's block counter
+    return 1024 + DEC_WARPS * dec_warp_bytes(bits) + DEC_WARPS * DEC_STAGES * 8 + 256 + 16;
 }
 
 // Decoded values c1[i1] + c2[i2] of the 64 coordinates of one half row, as 32
@@ -115,6 +114,7 @@ __device__ __forceinline__ void dec_lookup(const uint32_t (&w1)[BITS * 2], const
 template <int BITS, bool SGN>
 __global__ void __launch_bounds__(DEC_WARPS * 32, 1) rvq_decode_kernel(const __grid_constant__ RvqDecodeParams p)
 {
+    static_assert(BITS == 1, "b = 2 and b = 4 decode in rvq_decode_row_kernel");
     constexpr int L = 1 << BITS;
     constexpr int W = D * BITS / 32;
     constexpr int WH = W / 2;  // words per half row
@@ -123,9 +123,7 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) rvq_decode_kernel(const __g
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int rr = lane & 15, hh = lane >> 4;
-    unsigned char *smem = smem_1k(smem_raw);
-    float *stab = reinterpret_cast<float *>(smem);  // b = 4: merged table, replicated per lane
-    unsigned char *stages = smem + dec_table_bytes(BITS);  // every warp's stages, 1024-byte aligned
+    unsigned char *stages = smem_1k(smem_raw);  // every warp's stages
     unsigned char *wbuf = stages + warp * DEC_STAGES * STG;
     unsigned char *obufs = stages + DEC_WARPS * DEC_STAGES * STG;
     unsigned char *obuf = obufs + warp * DROWS * ROW_STRIDE;
@@ -141,20 +139,12 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) rvq_decode_kernel(const __g
         for (int s = 0; s < DEC_STAGES; ++s) mbar_init(&bars[s], 1);
         fence_mbar_init();
     }
-    if constexpr (BITS == 4) {
-        for (int i = threadIdx.x; i < 256 * 32; i += blockDim.x) {
-            const int e = i >> 5;
-            stab[i] = p.c1[e & 15] + p.c2[e >> 4];
-        }
-    }
     if (threadIdx.x < 64) sgm[threadIdx.x] = half2_sign_mask(sign_pair(p.sgn, 2 * threadIdx.x));
     if (threadIdx.x == 0) *claimed = 0u;
     __syncthreads();
-    __syncwarp();
     const uint64_t pol = l2_policy_evict_first();
-    // tables: per-stage (replicated every 2^BITS lanes) and merged (index
-    // i1 | i2 << BITS, replicated every 2^(2 BITS) lanes; b <= 2 only)
-    const float tab = BITS == 4 ? 0.0f : p.c1[lane & (L - 1)] + p.c2[(lane >> BITS) & (L - 1)];
+    // the merged table, index i1 | i2 << BITS, replicated every 2^(2 BITS) lanes
+    const float tab = p.c1[lane & (L - 1)] + p.c2[(lane >> BITS) & (L - 1)];
     const int nblk = (p.N + DROWS - 1) / DROWS;
     const int lo = (int)((long long)blockIdx.x * nblk / gridDim.x);
     const int hi = (int)((long long)(blockIdx.x + 1) * nblk / gridDim.x);
@@ -169,18 +159,10 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) rvq_decode_kernel(const __g
     auto issue = [&](int blk, int s) {
         if (lane == 0) {
             const int r0 = blk * DROWS;
-            if constexpr (BITS >= 2) {
-                // 16-row boxes of both streams with the 32- (b = 2) or 64-byte
-                // (b = 4) swizzle; rows past N arrive as zeros
-                mbar_arrive_expect_tx(&bars[s], (uint32_t)(2 * DROWS * W * 4));
-                tma_load_2d(wbuf + s * STG, &p.tm1, 0, r0, &bars[s], pol);
-                tma_load_2d(wbuf + s * STG + STG / 2, &p.tm2, 0, r0, &bars[s], pol);
-            } else {
-                const uint32_t bytes = (uint32_t)(min(DROWS, p.N - r0) * W * 4);
-                mbar_arrive_expect_tx(&bars[s], 2 * bytes);
-                bulk_g2s(wbuf + s * STG, p.p1 + (size_t)r0 * W, bytes, &bars[s], pol);
-                bulk_g2s(wbuf + s * STG + STG / 2, p.p2 + (size_t)r0 * W, bytes, &bars[s], pol);
-            }
+            const uint32_t bytes = (uint32_t)(min(DROWS, p.N - r0) * W * 4);
+            mbar_arrive_expect_tx(&bars[s], 2 * bytes);
+            bulk_g2s(wbuf + s * STG, p.p1 + (size_t)r0 * W, bytes, &bars[s], pol);
+            bulk_g2s(wbuf + s * STG + STG / 2, p.p2 + (size_t)r0 * W, bytes, &bars[s], pol);
         }
     };
     // sb[s]: the block staged in stage s (claims are increasing and consumed
@@ -211,22 +193,7 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) rvq_decode_kernel(const __g
             return;
         }
         uint32_t w1[WH], w2[WH];
-        if constexpr (BITS >= 2) {
-            // 16-byte chunk k of row rr sits at chunk k ^ ((rr >> 1) & 3) (64-byte
-            // rows, 64-byte swizzle) or k ^ ((rr >> 2) & 1) (32-byte rows, 32-byte
-            // swizzle): the lanes of a quarter warp read distinct banks
-            const unsigned char *ra = wbuf + s * STG + rr * (W * 4);
-            const unsigned char *rb = ra + STG / 2;
-#pragma unroll
-            for (int k2 = 0; k2 < WH / 4; ++k2) {
-                const int k = hh * (WH / 4) + k2;
-                const int pk = BITS == 4 ? (k ^ ((rr >> 1) & 3)) : (k ^ ((rr >> 2) & 1));
-                const uint4 a = *reinterpret_cast<const uint4 *>(ra + (pk << 4));
-                const uint4 b = *reinterpret_cast<const uint4 *>(rb + (pk << 4));
-                w1[4 * k2] = a.x; w1[4 * k2 + 1] = a.y; w1[4 * k2 + 2] = a.z; w1[4 * k2 + 3] = a.w;
-                w2[4 * k2] = b.x; w2[4 * k2 + 1] = b.y; w2[4 * k2 + 2] = b.z; w2[4 * k2 + 3] = b.w;
-            }
-        } else {
+        {
             const uint32_t *sa = reinterpret_cast<const uint32_t *>(wbuf + s * STG) + rr * W + hh * WH;
             const uint32_t *sb = reinterpret_cast<const uint32_t *>(wbuf + s * STG + STG / 2) + rr * W + hh * WH;
 #pragma unroll
@@ -251,7 +218,7 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) rvq_decode_kernel(const __g
             if (nb < hi) issue(nb, s);
         }
         float2 v[32];
-        dec_lookup<BITS>(w1, w2, tab, stab + lane, v);
+        dec_lookup<BITS>(w1, w2, tab, nullptr, v);
         // H64 on the half: coordinate bits 1-5 across the array, bit 0 in the pair
 #pragma unroll
         for (int h = 1; h < 32; h <<= 1) {
@@ -353,30 +320,37 @@ cudaError_t launch_enc_pair4(const RvqEncodeParams &p, cudaStream_t stream)
     return launch_enc_tm<MODE_PAIR>(p, stream);
 }
 
-// Decode, b = 2, a thread per row: the same table decode and fp32 butterflies
-// as rvq_decode_kernel, but a lane holds all 128 coordinates of its row, so
-// the last Hadamard stage is two register adds instead of a partner
-// exchange (about 7 instructions per element against 10.4).  32-row blocks
-// (one row per lane) arrive as 2D TMA boxes of both streams (32-byte swizzle)
-// into a 2-stage ring per warp; the fp16 rows are staged in shared memory
-// (16-byte chunks swizzled by row) and written out as whole contiguous
-// blocks.  12 warps per SM (about 150 registers a thread).
+// Decode, b in {2, 4}, a thread per row: the same table decode and fp32
+// butterflies as rvq_decode_kernel, but a lane holds all 128 coordinates of
+// its row, so the last Hadamard stage is two register adds instead of a
+// partner exchange (about 7 instructions per element against 10.4).  32-row
+// blocks (one row per lane) arrive as 2D TMA boxes of both streams (32- or
+// 64-byte swizzle) into a 2-stage ring per warp; the fp16 rows are staged in
+// shared memory (16-byte chunks swizzled by row) and written out as whole
+// contiguous blocks.  12 warps per SM (168 registers a thread); b = 4
+// reads the merged table from shared memory, replicated per lane.
 constexpr int DR_WARPS = 12;
 constexpr int DR_ROWS = 32;
 constexpr int DR_NST = 2;
-constexpr int DR_W = 8;                                 // words per row and stream (b = 2)
-constexpr int DR_STAGE = 2 * DR_ROWS * DR_W * 4;        // both streams: 2 KB
+__host__ __device__ constexpr int dr_w(int bits) { return D * bits / 32; }       // words per row and stream
+__host__ __device__ constexpr int dr_stage(int bits) { return 2 * DR_ROWS * dr_w(bits) * 4; }  // both streams
 constexpr int DR_OUT = DR_ROWS * 256;                   // fp16 rows of a block: 8 KB
-__host__ __device__ constexpr int dr_smem()
+__host__ __device__ constexpr int dr_smem(int bits)
 {
-    return 1024 + DR_WARPS * (DR_NST * DR_STAGE + DR_OUT) + DR_WARPS * DR_NST * 8 + 256 + 16;
+    return 1024 + dec_table_bytes(bits) + DR_WARPS * (DR_NST * dr_stage(bits) + DR_OUT) + DR_WARPS * DR_NST * 8 + 256 + 16;
 }
+static_assert(dr_smem(4) <= SMEM_MAX, "row decoder shared memory");
 
-template <bool SGN>
+template <int BITS, bool SGN>
 __global__ void __launch_bounds__(DR_WARPS * 32, 1) rvq_decode_row_kernel(const __grid_constant__ RvqDecodeParams p)
 {
+    constexpr int DR_W = dr_w(BITS);
+    constexpr int DR_STAGE = dr_stage(BITS);
+    constexpr int WH = DR_W / 2;  // words per half row
     extern __shared__ __align__(128) unsigned char smem_raw[];
-    unsigned char *smem = smem_1k(smem_raw);
+    unsigned char *smem0 = smem_1k(smem_raw);
+    float *stab = reinterpret_cast<float *>(smem0);  // b = 4: merged table, replicated per lane
+    unsigned char *smem = smem0 + dec_table_bytes(BITS);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     unsigned char *wbuf = smem + warp * (DR_NST * DR_STAGE);
     unsigned char *obuf = smem + DR_WARPS * DR_NST * DR_STAGE + warp * DR_OUT;
@@ -392,9 +366,16 @@ __global__ void __launch_bounds__(DR_WARPS * 32, 1) rvq_decode_row_kernel(const 
     }
     if (threadIdx.x < 64) sgm[threadIdx.x] = half2_sign_mask(sign_pair(p.sgn, 2 * threadIdx.x));
     if (threadIdx.x == 0) *claimed = 0u;
+    if constexpr (BITS == 4) {
+        for (int i = threadIdx.x; i < 256 * 32; i += blockDim.x) {
+            const int e = i >> 5;
+            stab[i] = p.c1[e & 15] + p.c2[e >> 4];
+        }
+    }
     __syncthreads();
     const uint64_t pol = l2_policy_evict_first();
-    const float tab = p.c1[lane & 3] + p.c2[(lane >> 2) & 3];  // merged table, index i1 | i2 << 2
+    // b = 2: merged table, index i1 | i2 << 2, one entry per lane
+    const float tab = BITS == 4 ? 0.0f : p.c1[lane & 3] + p.c2[(lane >> 2) & 3];
     const int nblk = (p.N + DR_ROWS - 1) / DR_ROWS;
     const int lo = (int)((long long)blockIdx.x * nblk / gridDim.x);
     const int hi = (int)((long long)(blockIdx.x + 1) * nblk / gridDim.x);
@@ -430,20 +411,28 @@ __global__ void __launch_bounds__(DR_WARPS * 32, 1) rvq_decode_row_kernel(const 
             if ((s ? sb0 : sb1) < hi) (void)mbar_wait_bounded(&bars[it2 & 1], (uint32_t)(it2 >> 1) & 1u);
             return;
         }
-        // the row's words (32-byte rows, 32-byte swizzle: chunk k at k ^ ((lane >> 2) & 1))
-        uint32_t w1[DR_W], w2[DR_W];
-        {
-            const unsigned char *ra = wbuf + s * DR_STAGE + lane * (DR_W * 4);
-            const unsigned char *rb = ra + DR_STAGE / 2;
+        // the row's words (rows of 4 W bytes with the matching swizzle: 16-byte
+        // chunk k at k ^ ((lane >> 2) & 1) for 32-byte rows, k ^ ((lane >> 1) & 3)
+        // for 64-byte rows), half row h from chunks [h C, h C + C)
+        constexpr int CH = DR_W / 8;  // 16-byte chunks per half row
+        const unsigned char *ra = wbuf + s * DR_STAGE + lane * (DR_W * 4);
+        const unsigned char *rb = ra + DR_STAGE / 2;
+        auto words = [&](int h, uint32_t (&a)[WH], uint32_t (&b)[WH]) {
 #pragma unroll
-            for (int k = 0; k < 2; ++k) {
-                const int pk = k ^ ((lane >> 2) & 1);
-                const uint4 a = *reinterpret_cast<const uint4 *>(ra + (pk << 4));
-                const uint4 b = *reinterpret_cast<const uint4 *>(rb + (pk << 4));
-                w1[4 * k] = a.x; w1[4 * k + 1] = a.y; w1[4 * k + 2] = a.z; w1[4 * k + 3] = a.w;
-                w2[4 * k] = b.x; w2[4 * k + 1] = b.y; w2[4 * k + 2] = b.z; w2[4 * k + 3] = b.w;
+            for (int k2 = 0; k2 < CH; ++k2) {
+                const int k = h * CH + k2;
+                const int pk = BITS == 4 ? (k ^ ((lane >> 1) & 3)) : (k ^ ((lane >> 2) & 1));
+                const uint4 x = *reinterpret_cast<const uint4 *>(ra + (pk << 4));
+                const uint4 y = *reinterpret_cast<const uint4 *>(rb + (pk << 4));
+                a[4 * k2] = x.x; a[4 * k2 + 1] = x.y; a[4 * k2 + 2] = x.z; a[4 * k2 + 3] = x.w;
+                b[4 * k2] = y.x; b[4 * k2 + 1] = y.y; b[4 * k2 + 2] = y.z; b[4 * k2 + 3] = y.w;
             }
-        }
+        };
+        // all of the row's words into registers first, so that the stage is
+        // refilled before the table decode
+        uint32_t a0[WH], b0[WH], a1[WH], b1[WH];
+        words(0, a0, b0);
+        words(1, a1, b1);
         __syncwarp();
         fence_proxy_async_smem();
         {
@@ -457,15 +446,8 @@ __global__ void __launch_bounds__(DR_WARPS * 32, 1) rvq_decode_row_kernel(const 
         // y_hat of the two halves, H64 on each (coordinate bits 1-5 across the
         // array, bit 0 in the pair), then bit 6 across the halves
         float2 v0[32], v1[32];
-        {
-            uint32_t a[4], b[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) { a[k] = w1[k]; b[k] = w2[k]; }
-            dec_lookup<2>(a, b, tab, nullptr, v0);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) { a[k] = w1[4 + k]; b[k] = w2[4 + k]; }
-            dec_lookup<2>(a, b, tab, nullptr, v1);
-        }
+        dec_lookup<BITS>(a0, b0, tab, stab + lane, v0);
+        dec_lookup<BITS>(a1, b1, tab, stab + lane, v1);
 #pragma unroll
         for (int h = 1; h < 32; h <<= 1) {
 #pragma unroll
@@ -521,15 +503,8 @@ __global__ void __launch_bounds__(DR_WARPS * 32, 1) rvq_decode_row_kernel(const 
 }
 
 template <int BITS>
-cudaError_t launch_dec(const RvqDecodeParams &p0, cudaStream_t stream)
+cudaError_t launch_dec(const RvqDecodeParams &p, cudaStream_t stream)
 {
-    RvqDecodeParams p = p0;
-    if constexpr (BITS >= 2) {
-        constexpr uint32_t W = D * BITS / 32;
-        if (!encode_tmap_words(&p.tm1, p.p1, (uint64_t)p.N, W, DROWS, (int)(W * 4)) ||
-            !encode_tmap_words(&p.tm2, p.p2, (uint64_t)p.N, W, DROWS, (int)(W * 4)))
-            return cudaErrorInvalidValue;
-    }
     auto kern = p.has_sgn ? rvq_decode_kernel<BITS, true> : rvq_decode_kernel<BITS, false>;
     constexpr int smem = dec_smem(BITS);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -573,14 +548,16 @@ cudaError_t launch_rvq_encode(const RvqEncodeParams &p, int bits, int mode, cuda
 }
 
 namespace {
+template <int BITS>
 cudaError_t launch_dec_row(const RvqDecodeParams &p0, cudaStream_t stream)
 {
     RvqDecodeParams p = p0;
-    if (!encode_tmap_words(&p.tm1, p.p1, (uint64_t)p.N, DR_W, DR_ROWS, DR_W * 4) ||
-        !encode_tmap_words(&p.tm2, p.p2, (uint64_t)p.N, DR_W, DR_ROWS, DR_W * 4))
+    constexpr int W = dr_w(BITS);
+    if (!encode_tmap_words(&p.tm1, p.p1, (uint64_t)p.N, W, DR_ROWS, W * 4) ||
+        !encode_tmap_words(&p.tm2, p.p2, (uint64_t)p.N, W, DR_ROWS, W * 4))
         return cudaErrorInvalidValue;
-    auto kern = p.has_sgn ? rvq_decode_row_kernel<true> : rvq_decode_row_kernel<false>;
-    constexpr int smem = dr_smem();
+    auto kern = p.has_sgn ? rvq_decode_row_kernel<BITS, true> : rvq_decode_row_kernel<BITS, false>;
+    constexpr int smem = dr_smem(BITS);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     const int nblk = (p.N + DR_ROWS - 1) / DR_ROWS;
@@ -598,8 +575,8 @@ cudaError_t launch_rvq_decode(const RvqDecodeParams &p, int bits, cudaStream_t s
     if (p.N <= 0) return cudaSuccess;
     switch (bits) {
     case 1: return launch_dec<1>(p, stream);
-    case 2: return launch_dec_row(p, stream);
-    case 4: return launch_dec<4>(p, stream);
+    case 2: return launch_dec_row<2>(p, stream);
+    case 4: return launch_dec_row<4>(p, stream);
     default: return cudaErrorInvalidValue;
     }
 }
