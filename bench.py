@@ -55,10 +55,11 @@ class Op:
     """One timed call.  `launches` counts the launches of `kernel` (per-launch
     figures divide by it); `gpu_launches` counts every kernel the call starts."""
 
-    def __init__(self, name, kernel, run, nbytes, nelem, launches=1, gpu_launches=None):
+    def __init__(self, name, kernel, run, nbytes, nelem, launches=1, gpu_launches=None, stream=None):
         self.name, self.kernel, self.run = name, kernel, run
         self.nbytes, self.nelem, self.launches = nbytes, nelem, launches
         self.gpu_launches = launches if gpu_launches is None else gpu_launches
+        self.stream = stream  # the stream the call launches on (None: the step's stream)
 
 
 def rvq_bytes(rows, bits, d=D):
@@ -144,12 +145,13 @@ def shard_configs(rank: int) -> dict:
     return {k: dict(v, seed=v["seed"] + 100003 * rank) for k, v in synth.CONFIGS.items()}
 
 
-def build_workload(name, dev, rank=0, layers=None, batch=None, chunked=False, chunk_stream=None):
+def build_workload(name, dev, rank=0, layers=None, batch=None, chunked=False, chunk_stream=None, lanes=None):
     """Device buffers and the op list for one step; also host inputs for e2e.
 
     With chunked=True, also returns the same step split into chunks that own
     their inputs (views of the full device inputs), ops and results, for the
-    pipelined end-to-end measurement (C5: per batch, C3: per layer)."""
+    pipelined end-to-end measurement (C5: per batch, C3: per layer).  C3 with
+    `lanes` (a list of streams): layer l launches on lanes[l % len(lanes)]."""
     import torch
     from kv_cache_quantization_turboquantrvq_gb300 import api, synth
 
@@ -182,10 +184,10 @@ def build_workload(name, dev, rank=0, layers=None, batch=None, chunked=False, ch
         # the library's books take the tensor-core encoders (b = 2: symmetric
         # books, b = 4: the pair table)
         ekern = "rvq_encode_tc_kernel" if bits in (2, 4) else "rvq_encode_kernel"
-        ops.append(Op(tag + "rvq_encode", ekern, enc, rvq_bytes(rows, bits), rows * D))
+        ops.append(Op(tag + "rvq_encode", ekern, enc, rvq_bytes(rows, bits), rows * D, stream=stream))
         if dec is not None:
             dkern = "rvq_decode_row_kernel" if bits in (2, 4) else "rvq_decode_kernel"
-            ops.append(Op(tag + "rvq_decode", dkern, dec, rvq_bytes(rows, bits), rows * D))
+            ops.append(Op(tag + "rvq_decode", dkern, dec, rvq_bytes(rows, bits), rows * D, stream=stream))
         results.extend([p1, p2, nr])
         if dec is not None:
             results.append(out)  # the round trip's reconstruction leaves the device too
@@ -273,7 +275,7 @@ def build_workload(name, dev, rank=0, layers=None, batch=None, chunked=False, ch
             k_np = synth.keys_for(cfg, layer=layer)
             k = t(k_np)
             inputs.append((k_np, k))
-            rvq_ops("L%02d_" % layer, k, cfg["bits"])
+            rvq_ops("L%02d_" % layer, k, cfg["bits"], stream=stream if lanes is None else lanes[layer % len(lanes)])
             if chunked:
                 c = new_chunk([(k_np, k)])
                 rvq_ops("L%02d_" % layer, k, cfg["bits"], ops=c["ops"], results=c["results"], stream=chunk_stream)
@@ -703,7 +705,13 @@ def main():
                     help="c5 and attn only: batch size B (default 4 and 64; fewer for small profiling runs)")
     ap.add_argument("--layers", type=int, default=None,
                     help="c3 only: number of layers (default 32; fewer for small profiling runs)")
+    ap.add_argument("--streams", type=int, default=1,
+                    help="c3 only: the layers round-robin over this many streams (a layer's decode "
+                         "waits for its own encode only), so that one launch's tail overlaps the "
+                         "next one's start; per-kernel times then overlap")
     args = ap.parse_args()
+    if args.streams < 1 or (args.streams > 1 and args.workload != "c3"):
+        raise SystemExit("--streams N > 1 applies to --workload c3 only")
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -731,20 +739,40 @@ def main():
         # a graph is captured on a side stream: run the whole bench there
         torch.cuda.set_stream(torch.cuda.Stream())
     s_run = torch.cuda.Stream()  # e2e kernel stream
+    stream = torch.cuda.current_stream()
+    lanes = [stream] + [torch.cuda.Stream() for _ in range(args.streams - 1)] if args.streams > 1 else None
     built = build_workload(args.workload, dev, rank, layers=args.layers, batch=args.batch,
-                           chunked=not args.no_e2e, chunk_stream=s_run)
+                           chunked=not args.no_e2e, chunk_stream=s_run, lanes=lanes)
     ops, inputs, results = built[:3]
     chunks = built[3] if len(built) > 3 else []
-    stream = torch.cuda.current_stream()
     K, W = args.steps, max(args.warmup, 3)
+    # per-op events: one stream, op i runs from event i to event i + 1; several
+    # streams, op i from event 2i to event 2i + 1 on its own stream
+    n_ev = len(ops) + 1 if lanes is None else 2 * len(ops)
 
     def step(evs=None):
+        if lanes is None:
+            for i, o in enumerate(ops):
+                if evs is not None:
+                    evs[i].record(stream)
+                o.run()
+            if evs is not None:
+                evs[len(ops)].record(stream)
+            return
+        fork = torch.cuda.Event()
+        fork.record(stream)
+        for s in lanes[1:]:
+            s.wait_event(fork)
         for i, o in enumerate(ops):
             if evs is not None:
-                evs[i].record(stream)
+                evs[2 * i].record(o.stream)
             o.run()
-        if evs is not None:
-            evs[len(ops)].record(stream)
+            if evs is not None:
+                evs[2 * i + 1].record(o.stream)
+        for s in lanes[1:]:
+            join = torch.cuda.Event()
+            join.record(s)
+            stream.wait_event(join)
 
     for _ in range(W):
         step()
@@ -752,7 +780,7 @@ def main():
     assert api.vq_device_error() == 0
     if world > 1:
         dist.barrier()
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(ops) + 1)] for _ in range(K)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(K)]
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local_rank)
     time.sleep(0.1)
@@ -804,7 +832,8 @@ def main():
     # per-op average durations (events on the launching stream)
     per_ms, per_step = {}, {}
     for i, o in enumerate(ops):
-        per_step[o.name] = [evs[k][i].elapsed_time(evs[k][i + 1]) for k in range(K)]
+        a, b = (i, i + 1) if lanes is None else (2 * i, 2 * i + 1)
+        per_step[o.name] = [evs[k][a].elapsed_time(evs[k][b]) for k in range(K)]
         per_ms[o.name] = statistics.mean(per_step[o.name])
     by_kernel = {}
     for o in ops:
@@ -898,7 +927,9 @@ def main():
                        "bytes_per_step": step_bytes, "elements_per_step": step_elems,
                        "timing": ("CUDA graph replays of the step" if args.graph else
                                   "CUDA events on the stream; the host queues ahead of the GPU "
-                                  "(a 20 ms GPU spin before the timed region)")},
+                                  "(a 20 ms GPU spin before the timed region)"),
+                       **({"streams": "the layers round-robin over %d streams; per-kernel times overlap "
+                                      "(each measured on its own stream)" % args.streams} if lanes else {})},
             "pct_of_peak": round(100 * value / world / peak, 2),
             "pct_of_nominal_8tbs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
             "gelem_per_s": round(gelem, 3),
