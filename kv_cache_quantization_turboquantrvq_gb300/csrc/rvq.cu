@@ -323,7 +323,7 @@ cudaError_t launch_enc_pair4(const RvqEncodeParams &p, cudaStream_t stream)
 // Decode, b in {2, 4}, a thread per row: the same table decode and fp32
 // butterflies as rvq_decode_kernel, but a lane holds all 128 coordinates of
 // its row, so the last Hadamard stage is two register adds instead of a
-// partner exchange (about 7 instructions per element against 10.4).  32-row
+// partner exchange (9.7 instructions per element against 10.4).  32-row
 // blocks (one row per lane) arrive as 2D TMA boxes of both streams (32- or
 // 64-byte swizzle) into a 2-stage ring per warp; the fp16 rows are staged in
 // shared memory (16-byte chunks swizzled by row) and written out as whole
