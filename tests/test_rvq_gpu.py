@@ -229,6 +229,36 @@ def test_decode_parity(vq, oracle_mod, bits):
     assert np.mean(got == ref.astype(np.float64)) > 0.95
 
 
+@pytest.mark.parametrize("bits", [1, 2, 4])
+@pytest.mark.parametrize("shape,signed", [((1, 1, 1), False), ((1, 1, 31), True), ((1, 1, 32), False),
+                                          ((1, 1, 33), True), ((1, 2, 4000), False), ((3, 1, 6113), True)])
+def test_decode_parity_shapes(vq, oracle_mod, bits, shape, signed):
+    """Decode of a single row, one short block, exactly one 32-row block, one
+    block and a row, and launches whose blocks do not fill the grid or end in
+    a partial block (6113 = 191 blocks of 32 and one row at b = 2, 4; 382
+    blocks of 16 and one row at b = 1), with and without the randomised signs;
+    every output against the oracle's binary64 dequant."""
+    x = _rows(shape, 90 + bits + shape[2])
+    cb = oracle_mod.rvq_codebooks(D, bits)[:4]
+    signs = np.random.default_rng(91 + bits).integers(0, 2 ** 32, 4, dtype=np.uint32) if signed else None
+    ora = oracle_mod.rvq_encode(x.reshape(-1, D), bits, *cb, signs=signs)
+    ref, ref64 = oracle_mod.rvq_decode(ora["packed1"], ora["packed2"], ora["norms"], D, bits,
+                                       cb[0], cb[2], want_f64=True, signs=signs)
+    W = 4 * bits
+    B, H, S = shape
+    out = vq.vq_rvq_unpack_dequant(_dev(ora["packed1"].view(np.int32).reshape(B, H, S, W)),
+                                   _dev(ora["packed2"].view(np.int32).reshape(B, H, S, W)),
+                                   _dev(ora["norms"].reshape(B, H, S)), bits, cb[0], cb[2], signs=signs)
+    torch.cuda.synchronize()
+    assert vq.vq_device_error() == 0
+    assert out.shape == (B, H, S, D)
+    got = out.cpu().numpy().reshape(-1, D).astype(np.float64)
+    n = ora["norms"].astype(np.float64)[:, None]
+    assert np.all(np.abs(got - ref64) <= 1e-3 * n + 1e-30)
+    if got.shape[0] >= 32:
+        assert np.mean(got == ref.astype(np.float64)) > 0.95
+
+
 def test_c1_full_parity_and_roundtrip(vq, oracle_mod):
     """TurboQuantRVQ b=2 on keys [1, 8, 512, 128] with per-channel scales."""
     from kv_cache_quantization_turboquantrvq_gb300 import synth
