@@ -862,7 +862,7 @@ def main():
         for c in chunks:
             c["pin_in"] = [torch.from_numpy(np.ascontiguousarray(h)).pin_memory() for h, _ in c["inputs"]]
             c["pin_out"] = [torch.empty(r.shape, dtype=r.dtype, pin_memory=True) for r in c["results"]]
-            c["ev_in"], c["ev_run"] = torch.cuda.Event(), torch.cuda.Event()
+            c["ev_in"], c["ev_run"], c["ev_out"] = torch.cuda.Event(), torch.cuda.Event(), torch.cuda.Event()
         h2d = sum(p.numel() * p.element_size() for c in chunks for p in c["pin_in"])
         d2h = sum(p.numel() * p.element_size() for c in chunks for p in c["pin_out"])
         assert sum(o.nbytes for c in chunks for o in c["ops"]) == step_bytes
@@ -875,11 +875,14 @@ def main():
                         dv.copy_(p, non_blocking=True)
                 c["ev_in"].record(s_in)
                 s_run.wait_event(c["ev_in"])
+                # the outputs' previous copy to the host is done (a no-op the first time)
+                s_run.wait_event(c["ev_out"])
                 if c.get("own_stream", True):
                     for o in c["ops"]:
                         o.run()
                 else:  # the step's own ops run on the current stream: order it after the copies
                     stream.wait_event(c["ev_in"])
+                    stream.wait_event(c["ev_out"])
                     for o in c["ops"]:
                         o.run()
                     s_run.wait_stream(stream)
@@ -888,6 +891,7 @@ def main():
                 with torch.cuda.stream(s_out):
                     for p, r in zip(c["pin_out"], c["results"]):
                         p.copy_(r, non_blocking=True)
+                c["ev_out"].record(s_out)
 
         Ke = max(3, min(K, 20))
         for _ in range(2):
