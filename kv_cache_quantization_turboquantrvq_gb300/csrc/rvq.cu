@@ -327,19 +327,48 @@ cudaError_t launch_enc_pair4(const RvqEncodeParams &p, cudaStream_t stream)
 // blocks (one row per lane) arrive as 2D TMA boxes of both streams (32- or
 // 64-byte swizzle) into a 2-stage ring per warp; the fp16 rows are staged in
 // shared memory (16-byte chunks swizzled by row) and written out as whole
-// contiguous blocks.  12 warps per SM (168 registers a thread); b = 4
-// reads the merged table from shared memory, replicated per lane.
+// contiguous blocks.  12 warps per SM (168 registers a thread).  The
+// tables sit in shared memory, replicated per lane (entry e of lane l at
+// 32 e + l: every read is conflict-free): b = 4, the merged per-coordinate
+// table c1[i1] + c2[i2] (256 entries); b = 2, a table per coordinate pair
+// (2k, 2k + 1) indexed by both coordinates' merged 4-bit indices, holding
+// (T[a] + T[b], T[a] - T[b]) with T[i] = c1[i & 3] + c2[i >> 2] - the first
+// Hadamard stage (bit 0) taken in the lookup, one 8-byte read per pair.
 constexpr int DR_WARPS = 12;
 constexpr int DR_ROWS = 32;
 constexpr int DR_NST = 2;
 __host__ __device__ constexpr int dr_w(int bits) { return D * bits / 32; }       // words per row and stream
 __host__ __device__ constexpr int dr_stage(int bits) { return 2 * DR_ROWS * dr_w(bits) * 4; }  // both streams
 constexpr int DR_OUT = DR_ROWS * 256;                   // fp16 rows of a block: 8 KB
+__host__ __device__ constexpr int dr_table_bytes(int bits) { return bits == 2 ? 256 * 32 * 8 : dec_table_bytes(bits); }
 __host__ __device__ constexpr int dr_smem(int bits)
 {
-    return 1024 + dec_table_bytes(bits) + DR_WARPS * (DR_NST * dr_stage(bits) + DR_OUT) + DR_WARPS * DR_NST * 8 + 256 + 16;
+    return 1024 + dr_table_bytes(bits) + DR_WARPS * (DR_NST * dr_stage(bits) + DR_OUT) + DR_WARPS * DR_NST * 8 + 256 + 16;
 }
-static_assert(dr_smem(4) <= SMEM_MAX, "row decoder shared memory");
+static_assert(dr_smem(4) <= SMEM_MAX && dr_smem(2) <= SMEM_MAX, "row decoder shared memory");
+
+// b = 2: the decoded pairs (u[2k] + u[2k + 1], u[2k] - u[2k + 1]) of the 64
+// coordinates of one half row (k = 0 .. 31), from the half row's words and
+// the per-lane pair table (this lane's replica).  me / mo hold the merged
+// 4-bit indices of the even / odd coordinates (nibble m of word j: coordinate
+// 16 j + 2 m, resp. + 1); their nibbles are paired into bytes, byte q of A
+// for pair 2q and of B for pair 2q + 1.
+__device__ __forceinline__ void dec_lookup_pairs2(const uint32_t (&w1)[4], const uint32_t (&w2)[4],
+                                                  const float2 *ptab, float2 (&v)[32])
+{
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const uint32_t me = (w1[j] & 0x33333333u) | ((w2[j] << 2) & 0xCCCCCCCCu);
+        const uint32_t mo = ((w1[j] >> 2) & 0x33333333u) | (w2[j] & 0xCCCCCCCCu);
+        const uint32_t a = (me & 0x0F0F0F0Fu) | ((mo << 4) & 0xF0F0F0F0u);
+        const uint32_t b = ((me >> 4) & 0x0F0F0F0Fu) | (mo & 0xF0F0F0F0u);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            v[8 * j + 2 * q] = ptab[__byte_perm(a, 0u, 0x4440u + q) * 32];
+            v[8 * j + 2 * q + 1] = ptab[__byte_perm(b, 0u, 0x4440u + q) * 32];
+        }
+    }
+}
 
 template <int BITS, bool SGN>
 __global__ void __launch_bounds__(DR_WARPS * 32, 1) rvq_decode_row_kernel(const __grid_constant__ RvqDecodeParams p)
@@ -349,8 +378,9 @@ __global__ void __launch_bounds__(DR_WARPS * 32, 1) rvq_decode_row_kernel(const 
     constexpr int WH = DR_W / 2;  // words per half row
     extern __shared__ __align__(128) unsigned char smem_raw[];
     unsigned char *smem0 = smem_1k(smem_raw);
-    float *stab = reinterpret_cast<float *>(smem0);  // b = 4: merged table, replicated per lane
-    unsigned char *smem = smem0 + dec_table_bytes(BITS);
+    float *stab = reinterpret_cast<float *>(smem0);    // b = 4: merged table, replicated per lane
+    float2 *ptab = reinterpret_cast<float2 *>(smem0);  // b = 2: pair table, replicated per lane
+    unsigned char *smem = smem0 + dr_table_bytes(BITS);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     unsigned char *wbuf = smem + warp * (DR_NST * DR_STAGE);
     unsigned char *obuf = smem + DR_WARPS * DR_NST * DR_STAGE + warp * DR_OUT;
@@ -371,11 +401,18 @@ __global__ void __launch_bounds__(DR_WARPS * 32, 1) rvq_decode_row_kernel(const 
             const int e = i >> 5;
             stab[i] = p.c1[e & 15] + p.c2[e >> 4];
         }
+    } else {
+        // T[lane & 15], index i1 | i2 << 2; entry e (warp-uniform: 32 | blockDim)
+        // pairs a = e & 15 (even coordinate) with b = e >> 4 (odd)
+        const float t = p.c1[lane & 3] + p.c2[(lane >> 2) & 3];
+        for (int i = threadIdx.x; i < 256 * 32; i += blockDim.x) {
+            const int e = i >> 5;
+            const float ta = __shfl_sync(FULL_MASK, t, e & 15), tb = __shfl_sync(FULL_MASK, t, e >> 4);
+            ptab[i] = make_float2(ta + tb, ta - tb);
+        }
     }
     __syncthreads();
     const uint64_t pol = l2_policy_evict_first();
-    // b = 2: merged table, index i1 | i2 << 2, one entry per lane
-    const float tab = BITS == 4 ? 0.0f : p.c1[lane & 3] + p.c2[(lane >> 2) & 3];
     const int nblk = (p.N + DR_ROWS - 1) / DR_ROWS;
     const int lo = (int)((long long)blockIdx.x * nblk / gridDim.x);
     const int hi = (int)((long long)(blockIdx.x + 1) * nblk / gridDim.x);
@@ -444,10 +481,16 @@ __global__ void __launch_bounds__(DR_WARPS * 32, 1) rvq_decode_row_kernel(const 
             if (nb < hi) issue(nb, s);
         }
         // y_hat of the two halves, H64 on each (coordinate bits 1-5 across the
-        // array, bit 0 in the pair), then bit 6 across the halves
+        // array, bit 0 in the pair: already taken by the b = 2 pair table),
+        // then bit 6 across the halves
         float2 v0[32], v1[32];
-        dec_lookup<BITS>(a0, b0, tab, stab + lane, v0);
-        dec_lookup<BITS>(a1, b1, tab, stab + lane, v1);
+        if constexpr (BITS == 2) {
+            dec_lookup_pairs2(a0, b0, ptab + lane, v0);
+            dec_lookup_pairs2(a1, b1, ptab + lane, v1);
+        } else {
+            dec_lookup<BITS>(a0, b0, 0.0f, stab + lane, v0);
+            dec_lookup<BITS>(a1, b1, 0.0f, stab + lane, v1);
+        }
 #pragma unroll
         for (int h = 1; h < 32; h <<= 1) {
 #pragma unroll
@@ -473,9 +516,9 @@ __global__ void __launch_bounds__(DR_WARPS * 32, 1) rvq_decode_row_kernel(const 
             for (int e = 0; e < 4; ++e) {
                 const int k = 4 * c + e;
                 const float2 a = v0[k], b = v1[k];
-                const float2 u = __fadd2_rn(a, b), w = __ffma2_rn(b, neg1, a);  // coordinates 2k, 2k+1 | 64 + 2k, 64 + 2k + 1 before bit 0
-                const float2 xu = __fmul2_rn(make_float2(u.x + u.y, u.x - u.y), sc2);
-                const float2 xw = __fmul2_rn(make_float2(w.x + w.y, w.x - w.y), sc2);
+                const float2 u = __fadd2_rn(a, b), w = __ffma2_rn(b, neg1, a);  // coordinates 2k, 2k+1 | 64 + 2k, 64 + 2k + 1 (b = 4: before bit 0)
+                const float2 xu = BITS == 2 ? __fmul2_rn(u, sc2) : __fmul2_rn(make_float2(u.x + u.y, u.x - u.y), sc2);
+                const float2 xw = BITS == 2 ? __fmul2_rn(w, sc2) : __fmul2_rn(make_float2(w.x + w.y, w.x - w.y), sc2);
                 const __half2 hu = __floats2half2_rn(xu.x, xu.y), hw = __floats2half2_rn(xw.x, xw.y);
                 o0[e] = *reinterpret_cast<const uint32_t *>(&hu);
                 o1[e] = *reinterpret_cast<const uint32_t *>(&hw);
