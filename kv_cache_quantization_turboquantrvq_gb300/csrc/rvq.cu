@@ -320,20 +320,20 @@ cudaError_t launch_enc_pair4(const RvqEncodeParams &p, cudaStream_t stream)
     return launch_enc_tm<MODE_PAIR>(p, stream);
 }
 
-// Decode, b in {2, 4}, a thread per row: the same table decode and fp32
-// butterflies as rvq_decode_kernel, but a lane holds all 128 coordinates of
-// its row, so the last Hadamard stage is two register adds instead of a
-// partner exchange (9.7 instructions per element against 10.4).  32-row
-// blocks (one row per lane) arrive as 2D TMA boxes of both streams (32- or
-// 64-byte swizzle) into a 2-stage ring per warp; the fp16 rows are staged in
-// shared memory (16-byte chunks swizzled by row) and written out as whole
-// contiguous blocks.  12 warps per SM (168 registers a thread).  The
-// tables sit in shared memory, replicated per lane (entry e of lane l at
-// 32 e + l: every read is conflict-free): b = 4, the merged per-coordinate
-// table c1[i1] + c2[i2] (256 entries); b = 2, a table per coordinate pair
-// (2k, 2k + 1) indexed by both coordinates' merged 4-bit indices, holding
-// (T[a] + T[b], T[a] - T[b]) with T[i] = c1[i & 3] + c2[i >> 2] - the first
-// Hadamard stage (bit 0) taken in the lookup, one 8-byte read per pair.
+// Decode, b in {2, 4}, a thread per row: a lane holds all 128 coordinates
+// of its row, so every Hadamard stage is register arithmetic (fp32x2
+// butterflies; the last stage two adds instead of a partner exchange).
+// The values c1[i1] + c2[i2] come from tables in shared memory, replicated
+// per lane (entry e of lane l at 32 e + l): b = 4, the merged per-coordinate
+// table (256 entries, read as 4 bytes); b = 2, a table per coordinate pair
+// (2k, 2k + 1), indexed by both coordinates' merged 4-bit indices and holding
+// (T[a] + T[b], T[a] - T[b]) with T[i] = c1[i & 3] + c2[i >> 2], so that the
+// first stage (bit 0) is taken in the lookup, one 8-byte read per pair (8.8
+// instructions per element at b = 2, against 10.4 for two threads per row).
+// 32-row blocks (one row per lane) arrive as 2D TMA boxes of both streams
+// (32- or 64-byte swizzle) into a 2-stage ring per warp; the fp16 rows are
+// staged in shared memory (16-byte chunks swizzled by row) and written out as
+// whole contiguous blocks.  12 warps per SM (168 registers a thread).
 constexpr int DR_WARPS = 12;
 constexpr int DR_ROWS = 32;
 constexpr int DR_NST = 2;
