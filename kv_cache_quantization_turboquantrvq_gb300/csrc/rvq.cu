@@ -397,9 +397,12 @@ __global__ void __launch_bounds__(DR_WARPS * 32, 1) rvq_decode_row_kernel(const 
     if (threadIdx.x < 64) sgm[threadIdx.x] = half2_sign_mask(sign_pair(p.sgn, 2 * threadIdx.x));
     if (threadIdx.x == 0) *claimed = 0u;
     if constexpr (BITS == 4) {
+        // entry e (warp-uniform: 32 | blockDim) from the two books held one
+        // entry per lane: no memory latency per entry
+        const float t1 = p.c1[lane & 15], t2 = p.c2[lane & 15];
         for (int i = threadIdx.x; i < 256 * 32; i += blockDim.x) {
             const int e = i >> 5;
-            stab[i] = p.c1[e & 15] + p.c2[e >> 4];
+            stab[i] = __shfl_sync(FULL_MASK, t1, e & 15) + __shfl_sync(FULL_MASK, t2, e >> 4);
         }
     } else {
         // T[lane & 15], index i1 | i2 << 2; entry e (warp-uniform: 32 | blockDim)
