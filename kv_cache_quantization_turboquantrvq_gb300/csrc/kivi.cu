@@ -279,8 +279,19 @@ cudaError_t launch_q(const KiviQuantParams &p0, bool per_channel, cudaStream_t s
 template <int BITS, int G>
 cudaError_t launch_dq(const KiviDequantParams &p, bool per_channel, cudaStream_t stream)
 {
-    const int cap = sm_count() * 8;
     if (per_channel) {
+        // one resident wave: as many CTAs as fit on the SMs at once (the warps
+        // stride over the tiles), so that no partial second wave forms the tail
+        static int per_sm = 0;
+        if (per_sm == 0) {
+            int b = 0;
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kivi_keys_dequant_kernel<BITS, G>, DQ_THREADS, 0) !=
+                    cudaSuccess ||
+                b < 1)
+                b = 1;
+            per_sm = b;
+        }
+        const int cap = sm_count() * per_sm;
         const int ntiles = p.BH * p.NG;
         int grid = (ntiles + DQ_THREADS / 32 - 1) / (DQ_THREADS / 32);
         if (grid > cap) grid = cap;
