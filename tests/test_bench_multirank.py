@@ -69,3 +69,13 @@ def test_reference_arm_under_torchrun():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle"
+
+
+@pytest.mark.parametrize("args", [["--workload", "c5", "--streams", "2"], ["--workload", "c3", "--streams", "0"]])
+def test_streams_option_is_checked_before_any_work(args):
+    """--streams N > 1 spreads the 32-layer workload's layers over N streams;
+    any other workload, or N < 1, is refused before the GPU is touched."""
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py")] + args, capture_output=True, text=True,
+                       timeout=120)
+    assert r.returncode != 0
+    assert "--streams N > 1 applies to --workload c3 only" in (r.stderr + r.stdout)
